@@ -1,0 +1,288 @@
+"""Pins for the CPU oracle: checks against facts other than the oracle itself.
+
+Each ``pin_*`` takes an oracle ctypes library (``oracle.load_library``) and
+raises AssertionError when the oracle disagrees with:
+  * a worked example (tests/golden/hand_2x2.txt),
+  * an independent float64 ``np.einsum`` on tiny shapes with dyadic inputs,
+    where every partial sum is exact, so the result is unique,
+  * an int64 matmul on the pages' integer fill (exact in float32 and double),
+  * closed forms and invariants (K=1 correctly rounded product, alpha=0,
+    beta=0 with NaN in C, identity, (AB)^T = B^T A^T, op='T' of a transposed
+    copy, exact power-of-two scaling of alpha, padding never read),
+  * a float64 BLAS matmul at a medium size within the final rounding,
+  * the bound magnitude S = |alpha| |A|@|B| + |beta C|.
+The same pins run against deliberately broken copies of the oracle in
+test_oracle_mutations.py, which shows that each plausible mistake fails one.
+"""
+from __future__ import annotations
+
+import itertools
+import os
+
+import numpy as np
+
+import oracle
+import sgemm_inputs as si
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+OPS = [("N", "N"), ("N", "T"), ("T", "N"), ("T", "T")]
+
+
+def _op(X: np.ndarray, t: str) -> np.ndarray:
+    return X.T if t == "T" else X
+
+
+def _stored(rng, op, rows, cols, dyadic_bits=None):
+    shp = si.stored_shape(op, rows, cols)
+    if dyadic_bits is None:
+        return (2.0 * rng.random(shp) - 1.0).astype(np.float32)
+    scale = 2 ** dyadic_bits
+    return (rng.integers(-scale, scale, size=shp) / scale).astype(np.float32)
+
+
+def read_golden_matrix_file(name):
+    rows = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            rows[key] = np.array([float(v) for v in vals], dtype=np.float32)
+    return rows
+
+
+def pin_hand_2x2(lib):
+    g = read_golden_matrix_file("hand_2x2.txt")
+    A, B, C = (g[k].reshape(2, 2) for k in "ABC")
+    out = oracle.sgemm("N", "N", A, B, lib=lib)
+    assert np.array_equal(out, C), out
+
+
+def pin_bruteforce_tiny(lib):
+    """All 4 ops, M,N,K in {1,2,3,5,7}, alpha/beta in {0,1,-0.5,2}: equal to float64 einsum.
+
+    Inputs are multiples of 2^-6 in [-1, 1), so products have <= 14 significant
+    bits and every partial sum is exact in double: any summation order gives
+    the same double, and one rounding to float32 gives a unique answer.
+    """
+    rng = np.random.default_rng(1234)
+    sizes = [1, 2, 3, 5, 7]
+    scalars = [0.0, 1.0, -0.5, 2.0]
+    for (ta, tb), M, N, K in itertools.product(OPS, sizes, sizes, sizes):
+        A = _stored(rng, ta, M, K, dyadic_bits=6)
+        B = _stored(rng, tb, K, N, dyadic_bits=6)
+        C = _stored(rng, "N", M, N, dyadic_bits=6)
+        alpha, beta = scalars[rng.integers(4)], scalars[rng.integers(4)]
+        ref = (alpha * np.einsum("ik,kj->ij", _op(A, ta).astype(np.float64), _op(B, tb).astype(np.float64))
+               + beta * C.astype(np.float64)).astype(np.float32)
+        out = oracle.sgemm(ta, tb, A, B, C, alpha, beta, lib=lib)
+        assert np.array_equal(out, ref), (ta, tb, M, N, K, alpha, beta)
+
+
+def pin_integer_pattern(lib, M=1000, N=1300, K=700, ops=OPS):
+    """The pages' (j-i)%3 fill on both stored operands: equal to an int64 matmul."""
+    for ta, tb in ops:
+        A = si.int_pattern(*si.stored_shape(ta, M, K))
+        B = si.int_pattern(*si.stored_shape(tb, K, N))
+        ref = _op(A, ta).astype(np.int64) @ _op(B, tb).astype(np.int64)
+        assert np.abs(ref).max() < 2 ** 24
+        out = oracle.sgemm(ta, tb, A, B, lib=lib)
+        assert np.array_equal(out, ref.astype(np.float32)), (ta, tb)
+
+
+def pin_integer_alpha_beta(lib, M=37, N=41, K=53):
+    """Integer fill with alpha=1.5, beta=-0.5 and integer C: exact in float32."""
+    rng = np.random.default_rng(7)
+    for ta, tb in OPS:
+        A = si.int_pattern(*si.stored_shape(ta, M, K))
+        B = si.int_pattern(*si.stored_shape(tb, K, N))
+        C = rng.integers(-4, 5, size=(M, N)).astype(np.float32)
+        ref = 1.5 * (_op(A, ta).astype(np.int64) @ _op(B, tb).astype(np.int64)) - 0.5 * C.astype(np.float64)
+        out = oracle.sgemm(ta, tb, A, B, C, 1.5, -0.5, lib=lib)
+        assert np.array_equal(out, ref.astype(np.float32)), (ta, tb)
+
+
+def pin_k1_exact(lib):
+    """K=1, alpha=1, beta=0: each element is one correctly rounded float32 product."""
+    rng = np.random.default_rng(5)
+    for ta, tb in OPS:
+        A = _stored(rng, ta, 23, 1)
+        B = _stored(rng, tb, 1, 29)
+        ref = _op(A, ta).astype(np.float32) * _op(B, tb).astype(np.float32)  # float32 IEEE multiply
+        out = oracle.sgemm(ta, tb, A, B, lib=lib)
+        assert np.array_equal(out, ref), (ta, tb)
+
+
+def pin_alpha_zero(lib):
+    """alpha = 0: C = fl32(beta*C) and A, B are not read (NaN operands do not leak)."""
+    rng = np.random.default_rng(6)
+    A = np.full((9, 11), np.nan, np.float32)
+    B = np.full((11, 13), np.nan, np.float32)
+    C = _stored(rng, "N", 9, 13)
+    for beta in (0.0, 1.0, -0.5, 3.0):
+        out = oracle.sgemm("N", "N", A, B, C, 0.0, beta, lib=lib)
+        assert np.array_equal(out, (np.float64(beta) * C.astype(np.float64)).astype(np.float32)), beta
+
+
+def pin_k_zero(lib):
+    """K = 0: C = fl32(beta*C)."""
+    rng = np.random.default_rng(16)
+    C = _stored(rng, "N", 5, 6)
+    A = np.zeros((5, 0), np.float32)
+    B = np.zeros((0, 6), np.float32)
+    out = oracle.sgemm("N", "N", A, B, C, 2.0, -0.5, M=5, N=6, K=0, lib=lib)
+    assert np.array_equal(out, (-0.5 * C.astype(np.float64)).astype(np.float32))
+
+
+def pin_beta_zero_nan_c(lib):
+    """beta = 0: C is not read, so a NaN-filled C gives the same result as a zero C."""
+    rng = np.random.default_rng(8)
+    for ta, tb in OPS:
+        A = _stored(rng, ta, 17, 19)
+        B = _stored(rng, tb, 19, 15)
+        Cnan = np.full((17, 15), np.nan, np.float32)
+        out = oracle.sgemm(ta, tb, A, B, Cnan, 1.25, 0.0, lib=lib)
+        ref = oracle.sgemm(ta, tb, A, B, None, 1.25, 0.0, lib=lib)
+        assert np.all(np.isfinite(out)) and np.array_equal(out, ref), (ta, tb)
+
+
+def pin_identity(lib):
+    """op(A) = I: C = fl32(alpha*B + beta*C)."""
+    rng = np.random.default_rng(9)
+    n = 31
+    eye = np.eye(n, dtype=np.float32)
+    for ta in "NT":
+        B = _stored(rng, "N", n, 24)
+        C = _stored(rng, "N", n, 24)
+        out = oracle.sgemm(ta, "N", eye, B, C, 0.75, -1.5, lib=lib)
+        ref = (0.75 * B.astype(np.float64) - 1.5 * C.astype(np.float64)).astype(np.float32)
+        assert np.array_equal(out, ref), ta
+
+
+def pin_transpose_identity(lib):
+    """(AB)^T = B^T A^T: sgemm('T','T', N, M, K, B, A) equals the transpose of sgemm('N','N')."""
+    rng = np.random.default_rng(10)
+    A = _stored(rng, "N", 33, 47)
+    B = _stored(rng, "N", 47, 29)
+    C = oracle.sgemm("N", "N", A, B, lib=lib)
+    Ct = oracle.sgemm("T", "T", B, A, lib=lib)          # stored B is K x N -> op(B^T) is N x K
+    assert Ct.shape == (29, 33)
+    assert np.array_equal(Ct, C.T)                       # same products, same k order
+
+
+def pin_transposed_copy(lib):
+    """op='T' on an explicitly transposed copy equals op='N' on the original."""
+    rng = np.random.default_rng(11)
+    A = _stored(rng, "N", 21, 34)
+    B = _stored(rng, "N", 34, 18)
+    C = _stored(rng, "N", 21, 18)
+    ref = oracle.sgemm("N", "N", A, B, C, 1.5, -0.5, lib=lib)
+    At = np.ascontiguousarray(A.T)
+    Bt = np.ascontiguousarray(B.T)
+    for ta, tb, AA, BB in (("T", "N", At, B), ("N", "T", A, Bt), ("T", "T", At, Bt)):
+        out = oracle.sgemm(ta, tb, AA, BB, C, 1.5, -0.5, lib=lib)
+        assert np.array_equal(out, ref), (ta, tb)
+
+
+def pin_alpha_pow2(lib):
+    """alpha * 2^e scales C exactly when beta = 0 (no overflow/underflow)."""
+    rng = np.random.default_rng(12)
+    A = _stored(rng, "N", 19, 26)
+    B = _stored(rng, "N", 26, 23)
+    base = oracle.sgemm("N", "N", A, B, None, 0.75, 0.0, lib=lib)
+    for e in (-3, 1, 5):
+        out = oracle.sgemm("N", "N", A, B, None, 0.75 * 2.0 ** e, 0.0, lib=lib)
+        assert np.array_equal(out, (base.astype(np.float64) * 2.0 ** e).astype(np.float32)), e
+
+
+def pin_padding_not_read(lib):
+    """Row strides larger than the logical width: NaN padding never reaches C."""
+    rng = np.random.default_rng(13)
+    for ta, tb in OPS:
+        A = _stored(rng, ta, 14, 22)
+        B = _stored(rng, tb, 22, 17)
+        C = _stored(rng, "N", 14, 17)
+        ref = oracle.sgemm(ta, tb, A, B, C, 1.0, 1.0, lib=lib)
+        Ap = si.embed_padded(A, A.shape[1] + 7)
+        Bp = si.embed_padded(B, B.shape[1] + 5)
+        out = oracle.sgemm(ta, tb, Ap[:, :A.shape[1]], Bp[:, :B.shape[1]], C, 1.0, 1.0, lib=lib)
+        assert np.array_equal(out, ref), (ta, tb)
+        # and the raw interface with a padded C: padding of C is left untouched
+        Cp = si.embed_padded(C, 17 + 3)
+        flatC = Cp.reshape(-1).copy()
+        st = oracle.sgemm_raw(ta, tb, 14, 17, 22, 1.0, Ap.reshape(-1), Ap.shape[1], Bp.reshape(-1), Bp.shape[1],
+                              1.0, flatC, 20, lib=lib)
+        assert st == 0
+        got = flatC.reshape(14, 20)
+        assert np.array_equal(got[:, :17], ref) and np.all(np.isnan(got[:, 17:])), (ta, tb)
+
+
+def pin_random_vs_float64_matmul(lib, M=150, N=170, K=700):
+    """Random uniform inputs: within the final float32 rounding of a float64 BLAS matmul."""
+    rng = np.random.default_rng(14)
+    for ta, tb in OPS:
+        A = _stored(rng, ta, M, K)
+        B = _stored(rng, tb, K, N)
+        C = _stored(rng, "N", M, N)
+        ref = 1.5 * (_op(A, ta).astype(np.float64) @ _op(B, tb).astype(np.float64)) - 0.5 * C.astype(np.float64)
+        out = oracle.sgemm(ta, tb, A, B, C, 1.5, -0.5, lib=lib).astype(np.float64)
+        absref = 1.5 * (np.abs(_op(A, ta)).astype(np.float64) @ np.abs(_op(B, tb)).astype(np.float64)) \
+            + 0.5 * np.abs(C.astype(np.float64))
+        # one float32 rounding (2^-24 |ref|) plus double-precision summation noise
+        err = np.abs(out - ref)
+        assert np.all(err <= 2.0 ** -24 * np.abs(ref) + 1e-12 * absref), (ta, tb, err.max())
+
+
+def pin_bound_magnitude(lib):
+    """S_ij = |alpha| sum_k |a_ik b_kj| + |beta c_ij|, against |A| @ |B| in float64."""
+    rng = np.random.default_rng(15)
+    for ta, tb in OPS:
+        A = _stored(rng, ta, 12, 40)
+        B = _stored(rng, tb, 40, 10)
+        C = _stored(rng, "N", 12, 10)
+        _, S = oracle.sgemm(ta, tb, A, B, C, -2.0, -0.5, want_bound=True, lib=lib)
+        ref = 2.0 * (np.abs(_op(A, ta)).astype(np.float64) @ np.abs(_op(B, tb)).astype(np.float64)) \
+            + 0.5 * np.abs(C.astype(np.float64))
+        assert np.allclose(S, ref, rtol=1e-13, atol=0), (ta, tb)
+
+
+def pin_argument_errors(lib):
+    """Invalid arguments are rejected with -(argument index), BLAS style."""
+    A = np.zeros(16, np.float32)
+    cases = [
+        (("X", "N", 2, 2, 2, 2, 2, 2), -1),
+        (("N", "Q", 2, 2, 2, 2, 2, 2), -2),
+        (("N", "N", -1, 2, 2, 2, 2, 2), -3),
+        (("N", "N", 2, -1, 2, 2, 2, 2), -4),
+        (("N", "N", 2, 2, -1, 2, 2, 2), -5),
+        (("N", "N", 2, 2, 3, 2, 2, 2), -8),     # lda < K
+        (("T", "N", 3, 2, 2, 2, 2, 2), -8),     # lda < M for 'T'
+        (("N", "N", 2, 3, 2, 2, 2, 3), -10),    # ldb < N
+        (("N", "T", 2, 2, 3, 3, 2, 2), -10),    # ldb < K for 'T'
+        (("N", "N", 2, 3, 2, 2, 3, 2), -13),    # ldc < N
+    ]
+    for (ta, tb, M, N, K, lda, ldb, ldc), want in cases:
+        st = oracle.sgemm_raw(ta, tb, M, N, K, 1.0, A, lda, A, ldb, 0.0, A.copy(), ldc, lib=lib)
+        assert st == want, ((ta, tb, M, N, K, lda, ldb, ldc), st, want)
+
+
+def pin_conjugate_is_transpose(lib):
+    """'C' (conjugate transpose) on real data is 'T'; lower-case letters are accepted."""
+    rng = np.random.default_rng(17)
+    A = _stored(rng, "T", 9, 12)
+    B = _stored(rng, "T", 12, 8)
+    ref = oracle.sgemm("T", "T", A, B, lib=lib)
+    for ta, tb in (("C", "C"), ("c", "t"), ("t", "C")):
+        assert np.array_equal(oracle.sgemm(ta, tb, A, B, lib=lib), ref), (ta, tb)
+    An = _stored(rng, "N", 9, 12)
+    assert np.array_equal(oracle.sgemm("n", "t", An, B, lib=lib), oracle.sgemm("N", "T", An, B, lib=lib))
+
+
+ALL_PINS = [
+    pin_hand_2x2, pin_bruteforce_tiny, pin_integer_pattern, pin_integer_alpha_beta, pin_k1_exact,
+    pin_alpha_zero, pin_k_zero, pin_beta_zero_nan_c, pin_identity, pin_transpose_identity,
+    pin_transposed_copy, pin_alpha_pow2, pin_padding_not_read, pin_random_vs_float64_matmul,
+    pin_bound_magnitude, pin_argument_errors, pin_conjugate_is_transpose,
+]
