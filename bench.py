@@ -1,0 +1,386 @@
+"""SGEMM benchmark: TFLOPS (2MNK/t) of libsgemm on the 4096^3 NN workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+
+One step is one sgemm() call over the whole problem (C = 1.5*A*B - 0.5*C at
+4096^3 by default).  Prints ONE JSON line (rank 0).  Timing: W untimed
+warm-up steps, then exactly K steps between a barrier + device synchronise
+on both sides; per-step CUDA events on the launching stream give the kernel
+time for the roofline.  Two input sets of 192 MiB are used in turn, so every
+step reads inputs larger than the 129 MB L2 (no flush kernel).
+
+``e2e``: the same metric through the C ABI with host buffers: every step
+copies A, B, C from pinned host memory, runs sgemm(), and reads C back.
+
+``--impl reference``: the CPU oracle (plain triple loop, double accumulation)
+timed on this machine's host cores on a bounded sample of rows of the same
+workload, scaled to TFLOPS.  Under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import sgemm_inputs as si  # noqa: E402
+
+METRIC = "SGEMM TFLOPS (2MNK/t) at 4096^3 NN on 1 GB300; % of FP32 FFMA peak"
+UNIT = "TFLOPS"
+FMA_PER_SM_PER_CLK = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "tma_gemm_square4096.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=si.HEADLINE, help="workload name from sgemm_inputs.CASES")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons in the background."""
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.gpu_id = gpu_id
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines: list[tuple[float, str]] = []
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+               "--format=csv,noheader,nounits", "-lms", str(self.period_ms)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [l.split(", ") for (t, l) in self.lines if t0 <= t <= t1]
+        rows = [r for r in rows if len(r) == len(self.FIELDS)]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in timed region"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip().lower() == "active"})
+        power = [float(r[3]) for r in rows if re.match(r"^[0-9.]+$", r[3])]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def gpu_selector(device_index: int) -> str:
+    import torch
+    try:
+        uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        if uuid and uuid != "None":
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [p for p in vis.split(",") if p.strip()]
+    if device_index < len(parts) and parts[device_index].strip().isdigit():
+        return parts[device_index].strip()
+    return str(device_index)
+
+
+# ---------------------------------------------------------------- helpers
+
+def traffic_from_profile(digest: str):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, if it is current."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    d = re.search(r"kernel_digest:\s*([0-9a-f]+)", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not d or not t or d.group(1) != digest:
+        return None
+    return int(t.group(1))
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return {}
+
+
+def oracle_sample_run(case, d, rows):
+    """Oracle on `rows` of C; returns seconds."""
+    import oracle
+    from_rows = np.asarray(rows, dtype=np.int64)
+    A = d["A"][:, :(case.M if case.transA == "T" else case.K)]
+    A = np.ascontiguousarray(A[:, from_rows] if case.transA == "T" else A[from_rows, :])
+    B = d["B"][:, :(case.K if case.transB == "T" else case.N)]
+    C = np.ascontiguousarray(d["C"][from_rows, :case.N])
+    t0 = time.perf_counter()
+    oracle.sgemm(case.transA, case.transB, A, B, C, case.alpha, case.beta, M=len(from_rows), N=case.N, K=case.K)
+    return time.perf_counter() - t0
+
+
+def cpu_rows_for(case, d, seconds: float):
+    """Rows of C whose oracle run takes about `seconds` (calibrated on a few rows)."""
+    probe = list(range(min(4, case.M)))
+    t = max(oracle_sample_run(case, d, probe), 1e-4)
+    n = int(max(1, min(case.M, round(len(probe) * seconds / t))))
+    return list(range(n))
+
+
+def cpu_baseline(case, d, seconds):
+    import oracle
+    rows = cpu_rows_for(case, d, seconds)
+    t = oracle_sample_run(case, d, rows)
+    flops = si.flops(len(rows), case.N, case.K)
+    return {"value": flops / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} of {case.M} rows of C ({len(rows)}x{case.N}x{case.K}, "
+                      f"{flops / 1e9:.2f} GFLOP) in {t:.1f} s; TFLOPS = 2*rows*N*K/t"}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    case = si.case(args.config)
+    d = si.make_case(case)
+    import oracle
+    oracle.build()
+    per_step = max(0.5, min(5.0, 100.0 / max(1, args.steps + args.warmup)))
+    rows = cpu_rows_for(case, d, per_step)
+    for _ in range(args.warmup):
+        oracle_sample_run(case, d, rows)
+    times = [oracle_sample_run(case, d, rows) for _ in range(args.steps)]
+    total = sum(times)
+    flops = si.flops(len(rows), case.N, case.K) * args.steps
+    value = flops / total / 1e12
+    sample = (f"each step: {len(rows)} of {case.M} rows of C ({len(rows)}x{case.N}x{case.K}); "
+              f"TFLOPS = 2*rows*N*K/t")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate",
+        "data": "synthetic", "config": config_block(case, args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(case, n_gpus):
+    return {"workload": f"sgemm_{case.transA}{case.transB}_{case.M}x{case.N}x{case.K}",
+            "name": case.name, "M": case.M, "N": case.N, "K": case.K, "ops": case.ops,
+            "alpha": case.alpha, "beta": case.beta, "inputs": case.dist, "layout": "row-major fp32",
+            "l2": "two input sets used in turn, each larger than the 129 MB L2; no flush kernel",
+            "parallelism": f"replicas x{n_gpus}"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from sgemm_row_major_gb300 import build as lib_build
+    lib_build.build()
+    import sgemm_row_major_gb300 as sg
+
+    case = si.case(args.config)
+    d = si.make_case(case)
+    M, N, K = case.M, case.N, case.K
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    # two device-resident input sets, used in turn
+    sets = []
+    for _ in range(2):
+        sets.append(tuple(torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C")))
+    torch.cuda.synchronize(dev)
+
+    plan = sg.sgemm_plan(case.transA, case.transB, M, N, K, case.alpha, sets[0][0], d["lda"], sets[0][1],
+                         d["ldb"], case.beta, sets[0][2], d["ldc"])
+
+    def step(i):
+        A, B, C = sets[i & 1]
+        sg.sgemm(case.transA, case.transB, M, N, K, case.alpha, A, d["lda"], B, d["ldb"], case.beta, C,
+                 d["ldc"], sh)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # pre-warm ~0.5 s so clocks settle, then exactly W warm-up steps
+    t_end = time.time() + 0.5
+    i = 0
+    while time.time() < t_end:
+        step(i)
+        i += 1
+        if i % 20 == 0:
+            torch.cuda.synchronize(dev)
+    for w in range(args.warmup):
+        step(w)
+    barrier()
+
+    sampler = ClockSampler(gpu_selector(local))
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    t0_wall = time.time()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        step(s)
+        ev[s][1].record(stream)
+    g1.record(stream)
+    barrier()
+    t1_wall = time.time()
+    time.sleep(0.1)
+    sampler.stop()
+    if sg.sgemm_sync_status(sh) != 0:
+        raise RuntimeError("libsgemm reported a kernel fault during the benchmark")
+
+    total_ms = g0.elapsed_time(g1)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops_step = si.flops(M, N, K)
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    kernel_ms = statistics.mean(step_ms)
+    achieved = flops_step / (kernel_ms * 1e-3) / 1e12
+
+    # ---- e2e: host buffers through the C ABI, copies inside the timed region
+    hA, hB, hC = (torch.from_numpy(d[k]).pin_memory() for k in ("A", "B", "C"))
+    hOut = torch.empty_like(hC).pin_memory()
+    A0, B0, C0 = sets[0]
+
+    def e2e_step():
+        A0.copy_(hA, non_blocking=True)
+        B0.copy_(hB, non_blocking=True)
+        C0.copy_(hC, non_blocking=True)
+        sg.sgemm(case.transA, case.transB, M, N, K, case.alpha, A0, d["lda"], B0, d["ldb"], case.beta, C0,
+                 d["ldc"], sh)
+        hOut.copy_(C0, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flops_step * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
+    h2d = (hA.numel() + hB.numel() + hC.numel()) * 4
+    d2h = hOut.numel() * 4
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    clocks = sampler.summary(t0_wall, t1_wall)
+    peaks = measured_peaks()
+    max_mhz = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
+    peak = sms * FMA_PER_SM_PER_CLK * 2 * max_mhz * 1e6 / 1e12
+    roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": traffic_from_profile(lib_build.source_digest()),
+            "peak_basis": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz max SM clock",
+            "kernel": "tma_gemm_kernel (SIMT FFMA2)" if plan["variant_name"].startswith("TMA") else plan["variant_name"],
+            "kernel_ms": kernel_ms}
+    if clocks.get("sm_mhz"):
+        roof["frac_at_sampled_clock"] = achieved / (sms * FMA_PER_SM_PER_CLK * 2 * clocks["sm_mhz"] * 1e6 / 1e12)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {**config_block(case, world), "prewarm_s": 0.5,
+                   "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "tile_k", "stages",
+                                                 "split_k", "grid_x", "grid_y")}},
+        "pct_ffma_peak": 100.0 * achieved / peak,
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": plan["kernel_launches"] * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, d, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

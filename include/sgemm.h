@@ -1,0 +1,145 @@
+/*
+ * sgemm.h -- C ABI of libsgemm, a single-precision GEMM for NVIDIA GB300 (sm_103a).
+ *
+ * Operation (BLAS SGEMM; itan.pw "CUDA NVIDIA 4090 高性能計算", 概要, with the
+ * row-major element definition of klklkl10086.github.io "Sgemm单精度矩阵乘法",
+ * 问题定义):
+ *
+ *     C = alpha * op(A) * op(B) + beta * C,     op(X) = X or X^T,
+ *
+ * on ROW-MAJOR float32 matrices: op(A) is M x K, op(B) is K x N, C is M x N.
+ *
+ * Layout (CBLAS row-major conventions; ld = row stride of the STORED matrix,
+ * in elements):
+ *   transA 'N': A stored M x K,  op(A)_ik = A[i*lda + k],  lda >= max(1, K)
+ *   transA 'T': A stored K x M,  op(A)_ik = A[k*lda + i],  lda >= max(1, M)
+ *   transB 'N': B stored K x N,  op(B)_kj = B[k*ldb + j],  ldb >= max(1, N)
+ *   transB 'T': B stored N x K,  op(B)_kj = B[j*ldb + k],  ldb >= max(1, K)
+ *   C_ij at C[i*ldc + j], ldc >= max(1, N)
+ * 'n'/'t' are accepted, and 'C'/'c' mean 'T' (the data are real).
+ *
+ * Ownership: A, B, C are caller-owned DEVICE pointers on the current CUDA
+ * device; the library never frees or retains them.  The library owns only
+ * internal state: a per-device stream-ordered memory pool for split-K
+ * partial sums (allocated and freed in stream order on the caller's stream),
+ * per-device kernel attributes, and a per-device fault word.
+ *
+ * Semantics of special values (BLAS conventions; the pages do not say):
+ *   - M == 0 or N == 0: nothing is done, SGEMM_OK.
+ *   - beta == 0: C is not read (NaN/Inf in C do not propagate).
+ *   - alpha == 0 or K == 0: A and B are not read; C = beta * C.
+ *   - Unaligned pointers or leading dimensions are NOT errors; they take a
+ *     slower path.  C overlapping A or B is undefined.
+ *
+ * Errors: invalid arguments return -(argument index) (1 = transA ... 14 =
+ * stream) before anything is launched, and C is untouched.  CUDA launch or
+ * allocation failures return SGEMM_ERR_CUDA / SGEMM_ERR_NOMEM (the CUDA
+ * error code is kept per thread, see sgemm_last_cuda_error).  Execution is
+ * asynchronous: sgemm() returns once the work is enqueued on `stream`;
+ * kernel faults appear at the caller's next synchronisation.  Every wait
+ * inside a kernel is bounded; a wait that gives up sets the device fault
+ * word, which sgemm_sync_status() reports as SGEMM_ERR_TIMEOUT.
+ */
+#ifndef SGEMM_H
+#define SGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *`; NULL = legacy default stream */
+
+enum sgemm_status {
+    SGEMM_OK = 0,
+    SGEMM_ERR_CUDA = 1,        /* a CUDA runtime call failed (see sgemm_last_cuda_error) */
+    SGEMM_ERR_TIMEOUT = 2,     /* a bounded in-kernel wait gave up (reported by sgemm_sync_status) */
+    SGEMM_ERR_NOMEM = 3,       /* split-K workspace could not be allocated */
+    SGEMM_ERR_UNSUPPORTED = 4  /* a dimension or leading dimension >= 2^31, or no usable device */
+    /* negative values: -(index of the invalid argument), BLAS xerbla style */
+};
+
+/* Kernel variants, as reported by sgemm_plan() and accepted by sgemm_set_variant_override(). */
+enum sgemm_variant {
+    SGEMM_VARIANT_AUTO = 0,       /* override only: let the planner choose */
+    SGEMM_VARIANT_NONE = 1,       /* M == 0 or N == 0: no launch */
+    SGEMM_VARIANT_SCALE = 2,      /* alpha == 0 or K == 0: C = beta * C */
+    SGEMM_VARIANT_GENERIC = 3,    /* any alignment: 64x64 tiles, predicated loads */
+    SGEMM_VARIANT_TMA_128x128 = 4,/* TMA-fed SIMT FFMA, 128x128x32 tiles, 4-stage mbarrier ring */
+    SGEMM_VARIANT_TMA_64x256 = 5  /* same kernel, 64x256 tiles for short M */
+};
+
+/*
+ * C = alpha * op(A) * op(B) + beta * C on row-major float32 matrices (see above).
+ * Returns SGEMM_OK once the work is enqueued on `stream`, or an error status.
+ */
+int sgemm(char transA, char transB, int64_t M, int64_t N, int64_t K,
+          float alpha, const float *A, int64_t lda,
+          const float *B, int64_t ldb,
+          float beta, float *C, int64_t ldc,
+          struct CUstream_st *stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *sgemm_status_string(int status);
+
+/* cudaError_t of the last CUDA failure seen by a libsgemm call on this thread (0 = none). */
+int sgemm_last_cuda_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's fault
+ * word.  Returns SGEMM_ERR_TIMEOUT if a kernel's bounded wait gave up since
+ * the last call, SGEMM_ERR_CUDA if the synchronisation failed, else SGEMM_OK.
+ */
+int sgemm_sync_status(struct CUstream_st *stream);
+
+/* What sgemm() would launch for these arguments. */
+typedef struct sgemm_plan_t {
+    int variant;             /* enum sgemm_variant */
+    int tile_m, tile_n, tile_k;
+    int stages;              /* shared-memory pipeline depth (0 when no GEMM kernel) */
+    int threads;             /* threads per CTA of the GEMM kernel */
+    int split_k;             /* number of K slices (1 = no split) */
+    int kernel_launches;     /* kernels one sgemm() call launches */
+    int64_t grid_x, grid_y;  /* CTAs of the GEMM kernel: tiles x K slices */
+    int64_t workspace_bytes; /* split-K partial-sum bytes taken from the pool */
+    int64_t smem_bytes;      /* dynamic shared memory per CTA */
+} sgemm_plan_t;
+
+/*
+ * Fills *plan with the launch sgemm() would make for these arguments on a
+ * device with `sm_count` SMs (sm_count <= 0: query the current device).
+ * Pure host logic when sm_count > 0; validates arguments like sgemm().
+ * Pointers are only inspected for alignment and NULL.
+ */
+int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
+               float alpha, const float *A, int64_t lda,
+               const float *B, int64_t ldb,
+               float beta, const float *C, int64_t ldc,
+               int sm_count, sgemm_plan_t *plan);
+
+/*
+ * Process-wide override of the planner, for tests and benchmarks:
+ * variant = SGEMM_VARIANT_AUTO restores automatic choice; split_k = 0 keeps
+ * the planner's split, >= 1 forces it (clamped to the number of K tiles).
+ * A forced TMA variant whose alignment rules the operands break falls back
+ * to GENERIC.  Returns SGEMM_OK or -1 for an unknown variant.
+ */
+int sgemm_set_variant_override(int variant, int split_k);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one CTA that waits on a
+ * shared-memory mbarrier nothing will ever complete, with a limit of
+ * `timeout_us` microseconds (1..10,000,000), synchronises `stream` and reports
+ * what the kernel recorded.  Returns SGEMM_ERR_TIMEOUT when the wait gave up
+ * and the fault word was set as designed (the expected outcome), SGEMM_OK if
+ * it did not, or SGEMM_ERR_CUDA.  Clears the fault word afterwards.
+ */
+int sgemm_selftest_wait_timeout(unsigned timeout_us, struct CUstream_st *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_H */

@@ -1,0 +1,398 @@
+// api.cu -- the C ABI of libsgemm: argument checks, the variant planner,
+// TMA descriptor encoding, workspace management and kernel launches.
+//
+// Argument conventions are those of BLAS/CBLAS row-major SGEMM (the pages
+// give only the formula: itan.pw "CUDA NVIDIA 4090 高性能計算", 概要); error
+// checking after each CUDA call follows youngju.dev "CUDA architecture
+// visualized" (よくある落とし穴 6, cudaGetLastError).
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "kernel_tma.cuh"
+#include "sgemm.h"
+#include "sgemm_internal.h"
+
+using namespace sgemm_impl;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+thread_local int t_last_cuda_error = 0;
+std::atomic<int> g_override_variant{SGEMM_VARIANT_AUTO};
+std::atomic<int> g_override_split{0};
+
+struct DeviceState {
+  std::once_flag once;
+  cudaError_t init_error = cudaSuccess;
+  int sm_count = 0;
+  unsigned* fault = nullptr;
+  cudaMemPool_t pool = nullptr;
+};
+DeviceState g_devices[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return SGEMM_ERR_CUDA;
+}
+
+int op_code(char t) {
+  if (t == 'N' || t == 'n') return 0;
+  if (t == 'T' || t == 't' || t == 'C' || t == 'c') return 1;
+  return -1;
+}
+
+uint64_t wait_timeout_ns() {
+  static const uint64_t ns = [] {
+    const char* env = std::getenv("SGEMM_WAIT_TIMEOUT_MS");
+    long long ms = env ? std::atoll(env) : 2000;
+    if (ms < 1) ms = 1;
+    return (uint64_t)ms * 1000000ull;
+  }();
+  return ns;
+}
+
+// One-time per-device state: SM count, fault word address, kernel attributes,
+// and the stream-ordered pool split-K partial sums come from.
+int device_state(int* device_out, DeviceState** st_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
+  DeviceState& st = g_devices[dev];
+  std::call_once(st.once, [&] {
+    cudaError_t err = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess) err = fault_word(&st.fault);
+    if (err == cudaSuccess) err = prepare_tma_op_nn();
+    if (err == cudaSuccess) err = prepare_tma_op_nt();
+    if (err == cudaSuccess) err = prepare_tma_op_tn();
+    if (err == cudaSuccess) err = prepare_tma_op_tt();
+    if (err == cudaSuccess) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      err = cudaMemPoolCreate(&st.pool, &props);
+      if (err == cudaSuccess) {
+        uint64_t keep = UINT64_MAX;  // keep freed workspace for the next call
+        err = cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      }
+    }
+    st.init_error = err;
+  });
+  if (st.init_error != cudaSuccess) return cuda_fail(st.init_error);
+  *device_out = dev;
+  *st_out = &st;
+  return SGEMM_OK;
+}
+
+int encode_fn(EncodeTiledFn* fn) {
+  static cudaError_t err = cudaSuccess;
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q != cudaDriverEntryPointSuccess) err = cudaErrorNotSupported;
+    g_encode = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (err != cudaSuccess || !g_encode) return cuda_fail(err != cudaSuccess ? err : cudaErrorNotSupported);
+  *fn = g_encode;
+  return SGEMM_OK;
+}
+
+// 2-D float32 tensor map over a row-major matrix: `inner` contiguous elements
+// per row, `outer` rows, row stride `ld` elements; box {box_inner, box_outer}.
+int encode_2d(const float* base, int64_t inner, int64_t outer, int64_t ld, int box_inner, int box_outer,
+              bool swizzle128, CUtensorMap* map) {
+  EncodeTiledFn fn;
+  int st = encode_fn(&fn);
+  if (st != SGEMM_OK) return st;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 4u};
+  const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return SGEMM_OK;
+}
+
+struct Problem {
+  int ta, tb;
+  int64_t M, N, K;
+  float alpha, beta;
+  const float* A;
+  const float* B;
+  const float* C;
+  int64_t lda, ldb, ldc;
+};
+
+int validate(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+             int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc, Problem* pr) {
+  const int ta = op_code(transA), tb = op_code(transB);
+  if (ta < 0) return -1;
+  if (tb < 0) return -2;
+  if (M < 0) return -3;
+  if (N < 0) return -4;
+  if (K < 0) return -5;
+  const bool work = M > 0 && N > 0;
+  const bool reads_ab = work && K > 0 && alpha != 0.0f;
+  if (reads_ab && !A) return -7;
+  if (lda < std::max<int64_t>(1, ta ? M : K)) return -8;
+  if (reads_ab && !B) return -9;
+  if (ldb < std::max<int64_t>(1, tb ? K : N)) return -10;
+  if (work && !C) return -12;
+  if (ldc < std::max<int64_t>(1, N)) return -13;
+  *pr = Problem{ta, tb, M, N, K, alpha, beta, A, B, C, lda, ldb, ldc};
+  return SGEMM_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The planner: a pure function of the problem, the SM count and the override.
+int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
+  *plan = sgemm_plan_t{};
+  plan->split_k = 1;
+  if (pr.M == 0 || pr.N == 0) {
+    plan->variant = SGEMM_VARIANT_NONE;
+    return SGEMM_OK;
+  }
+  if (pr.M > INT_MAX || pr.N > INT_MAX || pr.K > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
+  if (pr.K == 0 || pr.alpha == 0.0f) {
+    plan->variant = SGEMM_VARIANT_SCALE;
+    plan->kernel_launches = 1;
+    plan->threads = 256;
+    return SGEMM_OK;
+  }
+  // TMA needs 16-byte aligned bases and row strides that are multiples of 16 bytes.
+  const bool tma_ok = aligned16(pr.A) && aligned16(pr.B) && pr.lda % 4 == 0 && pr.ldb % 4 == 0;
+  int variant = tma_ok ? (pr.M <= 64 ? SGEMM_VARIANT_TMA_64x256 : SGEMM_VARIANT_TMA_128x128)
+                       : SGEMM_VARIANT_GENERIC;
+  const int ov = g_override_variant.load();
+  if (ov == SGEMM_VARIANT_GENERIC || ov == SGEMM_VARIANT_TMA_128x128 || ov == SGEMM_VARIANT_TMA_64x256)
+    variant = (ov == SGEMM_VARIANT_GENERIC || tma_ok) ? ov : SGEMM_VARIANT_GENERIC;
+
+  int bm, bn, bk, threads, stages;
+  int64_t smem = 0;
+  if (variant == SGEMM_VARIANT_GENERIC) {
+    const GenericTileShape g = generic_tile_shape();
+    bm = g.bm; bn = g.bn; bk = g.bk; threads = g.threads; stages = 2;
+  } else if (variant == SGEMM_VARIANT_TMA_128x128) {
+    using T = tma::Tile<4, 2>;
+    bm = T::BM; bn = T::BN; bk = tma::kBK; threads = tma::kThreads; stages = tma::kStages; smem = T::SMEM_BYTES;
+  } else {
+    using T = tma::Tile<2, 4>;
+    bm = T::BM; bn = T::BN; bk = tma::kBK; threads = tma::kThreads; stages = tma::kStages; smem = T::SMEM_BYTES;
+  }
+  const int64_t tiles = ceil_div(pr.M, bm) * ceil_div(pr.N, bn);
+  const int64_t kt = ceil_div(pr.K, bk);
+  if (tiles > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
+
+  // Split K only when the output tiles cannot fill the SMs, keeping at least
+  // 4 K tiles per slice.
+  int64_t split = 1;
+  if (tiles < sm_count) split = std::min<int64_t>(sm_count / tiles, kt / 4);
+  const int ov_split = g_override_split.load();
+  if (ov_split > 0) split = ov_split;
+  split = std::max<int64_t>(1, std::min<int64_t>({split, kt, 256}));
+  const int64_t per = ceil_div(kt, split);
+  split = ceil_div(kt, per);  // no empty slice
+
+  plan->variant = variant;
+  plan->tile_m = bm;
+  plan->tile_n = bn;
+  plan->tile_k = bk;
+  plan->stages = stages;
+  plan->threads = threads;
+  plan->split_k = (int)split;
+  plan->kernel_launches = split > 1 ? 2 : 1;
+  plan->grid_x = tiles;
+  plan->grid_y = split;
+  plan->smem_bytes = smem;
+  plan->workspace_bytes = split > 1 ? split * pr.M * (ceil_div(pr.N, 4) * 4) * 4 : 0;
+  return SGEMM_OK;
+}
+
+int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& st, float* C,
+                cudaStream_t stream) {
+  GemmParams p{};
+  p.M = (int)pr.M;
+  p.N = (int)pr.N;
+  p.K = (int)pr.K;
+  p.alpha = pr.alpha;
+  p.beta = pr.beta;
+  p.A = pr.A;
+  p.B = pr.B;
+  p.C = C;
+  p.lda = pr.lda;
+  p.ldb = pr.ldb;
+  p.ldc = pr.ldc;
+  p.c_vec = aligned16(C) && pr.ldc % 4 == 0;
+  p.timeout_ns = wait_timeout_ns();
+  p.fault = st.fault;
+
+  if (plan.variant == SGEMM_VARIANT_SCALE) {
+    cudaError_t e = launch_scale(p, stream);
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
+  }
+
+  const int split = plan.split_k;
+  p.tiles_m = (int)ceil_div(pr.M, plan.tile_m);
+  p.tiles_n = (int)ceil_div(pr.N, plan.tile_n);
+  p.k_tiles_per_split = (int)ceil_div(ceil_div(pr.K, plan.tile_k), split);
+  p.ws_ld = ceil_div(pr.N, 4) * 4;
+
+  CUtensorMap mapA, mapB;
+  if (plan.variant != SGEMM_VARIANT_GENERIC) {
+    const int bm = plan.tile_m, bn = plan.tile_n, bk = plan.tile_k;
+    // op(A): 'N' -> stored M x K, K contiguous (swizzled K-major tile);
+    //        'T' -> stored K x M, M contiguous.
+    int s = pr.ta ? encode_2d(pr.A, pr.M, pr.K, pr.lda, bm, bk, false, &mapA)
+                  : encode_2d(pr.A, pr.K, pr.M, pr.lda, bk, bm, true, &mapA);
+    if (s != SGEMM_OK) return s;
+    // op(B): 'N' -> stored K x N, N contiguous; 'T' -> stored N x K, K contiguous (swizzled).
+    s = pr.tb ? encode_2d(pr.B, pr.K, pr.N, pr.ldb, bk, bn, true, &mapB)
+              : encode_2d(pr.B, pr.N, pr.K, pr.ldb, bn, bk, false, &mapB);
+    if (s != SGEMM_OK) return s;
+  }
+
+  void* ws = nullptr;
+  if (split > 1) {
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)plan.workspace_bytes, st.pool, stream);
+    if (e != cudaSuccess) {
+      t_last_cuda_error = (int)e;
+      return e == cudaErrorMemoryAllocation ? SGEMM_ERR_NOMEM : SGEMM_ERR_CUDA;
+    }
+    p.ws = static_cast<float*>(ws);
+  }
+
+  cudaError_t e;
+  if (plan.variant == SGEMM_VARIANT_GENERIC) {
+    e = launch_generic_gemm(pr.ta, pr.tb, p, split, stream);
+  } else {
+    const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
+    if (!pr.ta && !pr.tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, stream);
+    else if (!pr.ta && pr.tb) e = launch_tma_op_nt(tile, mapA, mapB, p, split, stream);
+    else if (pr.ta && !pr.tb) e = launch_tma_op_tn(tile, mapA, mapB, p, split, stream);
+    else e = launch_tma_op_tt(tile, mapA, mapB, p, split, stream);
+  }
+  if (e == cudaSuccess && split > 1) e = launch_splitk_reduce(p, split, stream);
+  if (ws) {
+    cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = ef;
+  }
+  return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int sgemm(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+          const float* B, int64_t ldb, float beta, float* C, int64_t ldc, struct CUstream_st* stream) {
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  int dev;
+  DeviceState* st;
+  s = device_state(&dev, &st);
+  if (s != SGEMM_OK) return s;
+  sgemm_plan_t plan;
+  s = make_plan(pr, st->sm_count, &plan);
+  if (s != SGEMM_OK) return s;
+  return launch_gemm(pr, plan, *st, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+               int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc, int sm_count,
+               sgemm_plan_t* plan) {
+  if (!plan) return -15;
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  if (sm_count <= 0) {
+    int dev;
+    DeviceState* st;
+    s = device_state(&dev, &st);
+    if (s != SGEMM_OK) return s;
+    sm_count = st->sm_count;
+  }
+  return make_plan(pr, sm_count, plan);
+}
+
+int sgemm_set_variant_override(int variant, int split_k) {
+  if (variant != SGEMM_VARIANT_AUTO && variant != SGEMM_VARIANT_GENERIC && variant != SGEMM_VARIANT_TMA_128x128 &&
+      variant != SGEMM_VARIANT_TMA_64x256)
+    return -1;
+  g_override_variant.store(variant);
+  g_override_split.store(split_k < 0 ? 0 : split_k);
+  return SGEMM_OK;
+}
+
+const char* sgemm_status_string(int status) {
+  switch (status) {
+    case SGEMM_OK: return "SGEMM_OK";
+    case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: a CUDA runtime call failed";
+    case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a bounded in-kernel wait gave up";
+    case SGEMM_ERR_NOMEM: return "SGEMM_ERR_NOMEM: split-K workspace allocation failed";
+    case SGEMM_ERR_UNSUPPORTED: return "SGEMM_ERR_UNSUPPORTED: dimension too large or no usable device";
+    case -1: return "invalid argument 1 (transA)";
+    case -2: return "invalid argument 2 (transB)";
+    case -3: return "invalid argument 3 (M < 0)";
+    case -4: return "invalid argument 4 (N < 0)";
+    case -5: return "invalid argument 5 (K < 0)";
+    case -7: return "invalid argument 7 (A is NULL)";
+    case -8: return "invalid argument 8 (lda too small)";
+    case -9: return "invalid argument 9 (B is NULL)";
+    case -10: return "invalid argument 10 (ldb too small)";
+    case -12: return "invalid argument 12 (C is NULL)";
+    case -13: return "invalid argument 13 (ldc too small)";
+    case -15: return "invalid argument 15 (plan is NULL)";
+    default: return status < 0 ? "invalid argument" : "unknown status";
+  }
+}
+
+int sgemm_last_cuda_error(void) { return t_last_cuda_error; }
+
+int sgemm_sync_status(struct CUstream_st* stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned bits = 0;
+  e = take_faults(&bits);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return bits ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
+}
+
+int sgemm_selftest_wait_timeout(unsigned timeout_us, struct CUstream_st* stream) {
+  if (timeout_us < 1 || timeout_us > 10000000u) return -1;
+  int dev;
+  DeviceState* st;
+  int s = device_state(&dev, &st);
+  if (s != SGEMM_OK) return s;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  unsigned bits = 0;
+  cudaError_t e = cudaStreamSynchronize(cs);
+  if (e == cudaSuccess) e = take_faults(&bits);  // start from a clear fault word
+  if (e == cudaSuccess) e = launch_wait_selftest((uint64_t)timeout_us * 1000ull, st->fault, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e == cudaSuccess) e = take_faults(&bits);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return (bits & kFaultSelftest) ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
+}
+
+}  // extern "C"

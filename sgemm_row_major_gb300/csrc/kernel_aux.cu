@@ -1,0 +1,119 @@
+// kernel_aux.cu -- the small kernels around the GEMM kernels: the split-K
+// reduction with the fused alpha/beta epilogue, C = beta*C for alpha == 0 or
+// K == 0, the bounded-wait self-test, and the device fault word.
+#include "device_utils.cuh"
+#include "sgemm_internal.h"
+
+namespace sgemm_impl {
+
+// One fault word per device (each device that loads the library has its own
+// copy of a __device__ variable).  Kernels receive its address in GemmParams.
+__device__ unsigned g_fault_word;
+
+namespace {
+
+__device__ __forceinline__ float epilogue(float alpha, float beta, float v, const float* c) {
+  return beta == 0.0f ? alpha * v : fmaf(alpha, v, beta * *c);
+}
+
+// Sums the split partial tiles in slice order 0, 1, ..., split-1 (a fixed
+// order, so the result does not depend on scheduling), then applies
+// C = alpha * sum + beta * C.  One thread per 4 consecutive columns.
+template <bool CVEC>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p, int split) {
+  const int64_t groups = (p.N + 3) / 4;
+  const int64_t total = (int64_t)p.M * groups;
+  const int64_t slice = (int64_t)p.M * p.ws_ld;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int row = (int)(g / groups);
+    const int col = (int)(g % groups) * 4;
+    const float* w = p.ws + (int64_t)row * p.ws_ld + col;
+    float4 v = *reinterpret_cast<const float4*>(w);
+    for (int z = 1; z < split; ++z) {
+      const float4 u = *reinterpret_cast<const float4*>(w + z * slice);
+      v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+    }
+    float* c = p.C + (int64_t)row * p.ldc + col;
+    if (CVEC && col + 3 < p.N) {
+      float4 o;
+      if (p.beta == 0.0f) {
+        o = make_float4(p.alpha * v.x, p.alpha * v.y, p.alpha * v.z, p.alpha * v.w);
+      } else {
+        const float4 old = *reinterpret_cast<const float4*>(c);
+        o = make_float4(fmaf(p.alpha, v.x, p.beta * old.x), fmaf(p.alpha, v.y, p.beta * old.y),
+                        fmaf(p.alpha, v.z, p.beta * old.z), fmaf(p.alpha, v.w, p.beta * old.w));
+      }
+      *reinterpret_cast<float4*>(c) = o;
+    } else {
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (col + q < p.N) c[q] = epilogue(p.alpha, p.beta, vv[q], c + q);
+    }
+  }
+}
+
+// C = beta * C; with beta == 0, C = 0 without reading C.
+__global__ void __launch_bounds__(256) scale_kernel(const GemmParams p) {
+  const int64_t total = (int64_t)p.M * p.N;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    float* c = p.C + (e / p.N) * p.ldc + (e % p.N);
+    *c = p.beta == 0.0f ? 0.0f : p.beta * *c;
+  }
+}
+
+// Waits on a shared-memory mbarrier that nothing arrives on.  The wait must
+// give up after `timeout_ns` and record kFaultSelftest; no copy is in flight.
+__global__ void wait_selftest_kernel(uint64_t timeout_ns, unsigned* fault) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(b, 0, timeout_ns)) atomicOr(fault, (unsigned)kFaultSelftest);
+}
+
+unsigned grid_for(int64_t work, int per_block) {
+  int64_t blocks = (work + per_block - 1) / per_block;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 152 * 32) blocks = 152 * 32;  // grid-stride beyond ~32 blocks per SM
+  return (unsigned)blocks;
+}
+
+}  // namespace
+
+cudaError_t launch_splitk_reduce(const GemmParams& p, int split, cudaStream_t stream) {
+  const int64_t work = (int64_t)p.M * ((p.N + 3) / 4);
+  if (p.c_vec)
+    splitk_reduce_kernel<true><<<grid_for(work, 256), 256, 0, stream>>>(p, split);
+  else
+    splitk_reduce_kernel<false><<<grid_for(work, 256), 256, 0, stream>>>(p, split);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale(const GemmParams& p, cudaStream_t stream) {
+  scale_kernel<<<grid_for((int64_t)p.M * p.N, 256), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, unsigned* fault, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns, fault);
+  return cudaGetLastError();
+}
+
+cudaError_t fault_word(unsigned** ptr) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_fault_word);
+}
+
+cudaError_t take_faults(unsigned* bits) {
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_fault_word, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(unsigned));
+}
+
+}  // namespace sgemm_impl

@@ -1,0 +1,139 @@
+"""CPU tests of the C-ABI boundary: the library loads, exports every declared
+symbol, and its host-side logic (argument checks, planner, status strings)
+behaves as include/sgemm.h states.  No call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sgemm_row_major_gb300 as sg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sgemm.h")
+
+FAKE = 1 << 20        # 16-byte aligned fake device address (never dereferenced here)
+FAKE_ODD = FAKE + 4   # 4-byte aligned only
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(sgemm\w*)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sgemm_row_major_gb300 import build
+    build.build()
+    return sg.load()
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("sgemm", "sgemm_status_string", "sgemm_last_cuda_error", "sgemm_sync_status", "sgemm_plan",
+              "sgemm_set_variant_override", "sgemm_selftest_wait_timeout"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libsgemm.so does not export {name}"
+
+
+def test_invalid_arguments_rejected_without_launch(lib):
+    # (transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> status
+    cases = [
+        (("X", "N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -1),
+        (("N", "?", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -2),
+        (("N", "N", -1, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -3),
+        (("N", "N", 4, -2, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -4),
+        (("N", "N", 4, 4, -3, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -5),
+        (("N", "N", 4, 4, 4, 1.0, None, 4, FAKE, 4, 0.0, FAKE, 4), -7),
+        (("N", "N", 4, 4, 8, 1.0, FAKE, 7, FAKE, 4, 0.0, FAKE, 4), -8),   # lda < K
+        (("T", "N", 9, 4, 4, 1.0, FAKE, 8, FAKE, 4, 0.0, FAKE, 4), -8),   # lda < M for 'T'
+        (("N", "N", 4, 4, 4, 1.0, FAKE, 4, None, 4, 0.0, FAKE, 4), -9),
+        (("N", "N", 4, 6, 4, 1.0, FAKE, 4, FAKE, 5, 0.0, FAKE, 6), -10),  # ldb < N
+        (("N", "T", 4, 4, 6, 1.0, FAKE, 6, FAKE, 5, 0.0, FAKE, 4), -10),  # ldb < K for 'T'
+        (("N", "N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, None, 4), -12),
+        (("N", "N", 4, 6, 4, 1.0, FAKE, 4, FAKE, 6, 0.0, FAKE, 5), -13),  # ldc < N
+    ]
+    for args, want in cases:
+        assert sg.sgemm(*args, stream=0, raise_on_error=False) == want, (args, want)
+        assert "invalid argument" in sg.sgemm_status_string(want)
+
+
+def test_null_operands_allowed_when_not_read(lib):
+    # M == 0 or N == 0: nothing to do, no device needed, pointers never inspected
+    assert sg.sgemm("N", "N", 0, 5, 5, 1.0, None, 5, None, 5, 0.0, None, 5, stream=0) == 0
+    assert sg.sgemm("N", "N", 5, 0, 5, 1.0, None, 5, None, 1, 0.0, None, 1, stream=0) == 0
+    # alpha == 0: A and B are not read, so NULL is valid (planning only)
+    p = sg.sgemm_plan("N", "N", 8, 8, 8, 0.0, None, 8, None, 8, 2.0, FAKE, 8, sm_count=152)
+    assert p["variant_name"] == "SCALE" and p["kernel_launches"] == 1
+
+
+def test_status_strings(lib):
+    assert sg.sgemm_status_string(0) == "SGEMM_OK"
+    for code in (1, 2, 3, 4):
+        assert sg.sgemm_status_string(code).startswith("SGEMM_ERR")
+    assert sg.sgemm_last_cuda_error() == 0
+
+
+def plan(ta, tb, M, N, K, A=FAKE, B=FAKE, lda=None, ldb=None, sm=152, alpha=1.0):
+    lda = lda if lda is not None else ((M if ta == "T" else K) or 1)
+    ldb = ldb if ldb is not None else ((K if tb == "T" else N) or 1)
+    return sg.sgemm_plan(ta, tb, M, N, K, alpha, A, lda, B, ldb, 0.0, FAKE, max(N, 1), sm_count=sm)
+
+
+def test_planner_variants(lib):
+    assert plan("N", "N", 0, 10, 10)["variant_name"] == "NONE"
+    assert plan("N", "N", 10, 10, 0)["variant_name"] == "SCALE"
+    big = plan("N", "N", 4096, 4096, 4096)
+    assert big["variant_name"] == "TMA_128x128" and big["split_k"] == 1 and big["kernel_launches"] == 1
+    assert big["grid_x"] == 32 * 32 and big["tile_k"] == 32 and big["threads"] == 256
+    assert big["smem_bytes"] <= 227 * 1024
+    # unaligned base or ld not a multiple of 4 -> the generic (edge) kernel
+    assert plan("N", "N", 512, 512, 512, A=FAKE_ODD)["variant_name"] == "GENERIC"
+    assert plan("N", "N", 512, 512, 513, lda=515)["variant_name"] == "GENERIC"
+    assert plan("T", "T", 512, 512, 512, ldb=514)["variant_name"] == "GENERIC"
+    # ragged padded shapes of the transpose sweep keep the TMA path (ld % 4 == 0)
+    for ta, tb, lda, ldb in (("N", "N", 2060, 3008), ("N", "T", 2060, 2060), ("T", "N", 4104, 3008),
+                             ("T", "T", 4104, 2060)):
+        assert plan(ta, tb, 4097, 3001, 2053, lda=lda, ldb=ldb)["variant_name"] == "TMA_128x128"
+
+
+def test_planner_split_k(lib):
+    # 1024^3: 64 tiles of 128x128 on 152 SMs -> split K in 2
+    p = plan("N", "N", 1024, 1024, 1024)
+    assert p["split_k"] == 2 and p["kernel_launches"] == 2 and p["grid_y"] == 2
+    assert p["workspace_bytes"] == 2 * 1024 * 1024 * 4
+    # skinny FC shape: 64x256 tiles, 16 of them -> 9 slices
+    s = plan("N", "N", 64, 4096, 16384)
+    assert s["variant_name"] == "TMA_64x256" and s["grid_x"] == 16 and s["split_k"] == 9
+    # never more slices than K tiles, and every slice non-empty
+    t = plan("N", "N", 8, 8, 64)
+    assert t["split_k"] <= 2
+    # more SMs never reduce the split
+    assert plan("N", "N", 256, 256, 8192, sm=304)["split_k"] >= plan("N", "N", 256, 256, 8192)["split_k"]
+
+
+def test_variant_override(lib):
+    try:
+        sg.sgemm_set_variant_override("GENERIC", 3)
+        p = plan("N", "N", 4096, 4096, 4096)
+        assert p["variant_name"] == "GENERIC" and p["split_k"] == 3
+        sg.sgemm_set_variant_override("TMA_64x256", 0)
+        assert plan("N", "N", 4096, 4096, 4096)["variant_name"] == "TMA_64x256"
+        # a forced TMA variant falls back when alignment forbids it
+        assert plan("N", "N", 4096, 4096, 4096, A=FAKE_ODD)["variant_name"] == "GENERIC"
+        with pytest.raises(sg.SgemmError):
+            sg.sgemm_set_variant_override(99, 0)
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
+    assert plan("N", "N", 4096, 4096, 4096)["variant_name"] == "TMA_128x128"
+
+
+def test_plan_rejects_huge_dimensions(lib):
+    with pytest.raises(sg.SgemmError) as e:
+        plan("N", "N", 1 << 31, 8, 8, lda=8, ldb=8)
+    assert e.value.status == 4
