@@ -57,7 +57,8 @@ enum sgemm_status {
     SGEMM_ERR_CUDA = 1,        /* a CUDA runtime call failed (see sgemm_last_cuda_error) */
     SGEMM_ERR_TIMEOUT = 2,     /* a bounded in-kernel wait gave up (reported by sgemm_sync_status) */
     SGEMM_ERR_NOMEM = 3,       /* split-K workspace could not be allocated */
-    SGEMM_ERR_UNSUPPORTED = 4  /* a dimension or leading dimension >= 2^31, or no usable device */
+    SGEMM_ERR_UNSUPPORTED = 4, /* a dimension or leading dimension >= 2^31, or no usable device */
+    SGEMM_ERR_SCRATCH_LIMIT = 5 /* sgemm_noalloc: the problem needs more scratch than its static array */
     /* negative values: -(index of the invalid argument), BLAS xerbla style */
 };
 
@@ -137,6 +138,36 @@ int sgemm_set_variant_override(int variant, int split_k);
  * it did not, or SGEMM_ERR_CUDA.  Clears the fault word afterwards.
  */
 int sgemm_selftest_wait_timeout(unsigned timeout_us, struct CUstream_st *stream);
+
+/*
+ * sgemm_noalloc -- the same operation, arguments and results as sgemm(), for
+ * callers that cannot allocate device memory during the call.  (The pages
+ * have no counterpart; this is a library convenience.)
+ *
+ * sgemm() may grow its memory pool to hold split-K partial sums.  A caller
+ * that has already given nearly all device memory to its own allocator, or
+ * latency-critical code that cannot absorb a pool growing mid-run, cannot
+ * allow that.  sgemm_noalloc() calls no cudaMalloc, cudaFree or other
+ * allocating routine: the partial sums go to a fixed scratch array of
+ * SGEMM_NOALLOC_SCRATCH_BYTES compiled into the library, one per device,
+ * held by every GPU that loads the library until the process exits.
+ *
+ * Limit: a problem whose split-K partial sums need more than
+ * SGEMM_NOALLOC_SCRATCH_BYTES (see sgemm_plan_t.workspace_bytes) is rejected
+ * with SGEMM_ERR_SCRATCH_LIMIT before anything is launched; C is untouched.
+ * The first call on a device does a one-time set-up there (it looks up the
+ * array's device address and sets kernel attributes); make that first call
+ * before any stream capture.  All calls on a device share the one array:
+ * calls whose kernels can overlap on the GPU (e.g. on unordered streams) race
+ * on it, so order them.  CUDA failures return SGEMM_ERR_CUDA.
+ */
+#define SGEMM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20) /* 16 MiB per device */
+
+int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                  float alpha, const float *A, int64_t lda,
+                  const float *B, int64_t ldb,
+                  float beta, float *C, int64_t ldc,
+                  struct CUstream_st *stream);
 
 #ifdef __cplusplus
 }

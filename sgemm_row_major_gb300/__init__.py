@@ -16,7 +16,7 @@ import os
 import threading
 
 __all__ = [
-    "SgemmError", "load", "library_path", "sgemm", "sgemm_plan", "sgemm_status_string",
+    "SgemmError", "load", "library_path", "sgemm", "sgemm_noalloc", "sgemm_plan", "sgemm_status_string",
     "sgemm_last_cuda_error", "sgemm_sync_status", "sgemm_set_variant_override",
     "sgemm_selftest_wait_timeout", "matmul", "VARIANTS", "STATUS",
 ]
@@ -24,7 +24,8 @@ __all__ = [
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_lib", "libsgemm.so")
 
-STATUS = {"OK": 0, "ERR_CUDA": 1, "ERR_TIMEOUT": 2, "ERR_NOMEM": 3, "ERR_UNSUPPORTED": 4}
+STATUS = {"OK": 0, "ERR_CUDA": 1, "ERR_TIMEOUT": 2, "ERR_NOMEM": 3, "ERR_UNSUPPORTED": 4, "ERR_SCRATCH_LIMIT": 5}
+NOALLOC_SCRATCH_BYTES = 16 << 20  # SGEMM_NOALLOC_SCRATCH_BYTES in include/sgemm.h
 VARIANTS = {"AUTO": 0, "NONE": 1, "SCALE": 2, "GENERIC": 3, "TMA_128x128": 4, "TMA_64x256": 5}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 
@@ -64,6 +65,8 @@ def load() -> ctypes.CDLL:
         i64, f32, vp, ch = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_char
         lib.sgemm.restype = ctypes.c_int
         lib.sgemm.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        lib.sgemm_noalloc.restype = ctypes.c_int
+        lib.sgemm_noalloc.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_plan.restype = ctypes.c_int
         lib.sgemm_plan.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ctypes.c_int,
                                    ctypes.POINTER(PlanStruct)]
@@ -121,6 +124,22 @@ def sgemm(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=N
                       _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), _stream(stream))
     if st != 0 and raise_on_error:
         raise SgemmError(st)
+    return st
+
+
+def sgemm_noalloc(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None, *,
+                  raise_on_error: bool = True) -> int:
+    """sgemm() for callers that cannot allocate device memory during the call.
+
+    Same arguments and results as sgemm(); split-K partial sums go to a fixed
+    16 MiB array inside the library instead of a memory pool.  Problems that
+    need more scratch return ERR_SCRATCH_LIMIT.  All calls on a device share
+    that array, so calls that can overlap on the GPU must be ordered.
+    """
+    st = load().sgemm_noalloc(_ch(transA), _ch(transB), int(M), int(N), int(K), float(alpha), _ptr(A),
+                              int(lda), _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), _stream(stream))
+    if st != 0 and raise_on_error:
+        raise SgemmError(st, "sgemm_noalloc")
     return st
 
 

@@ -351,6 +351,8 @@ const char* sgemm_status_string(int status) {
     case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a bounded in-kernel wait gave up";
     case SGEMM_ERR_NOMEM: return "SGEMM_ERR_NOMEM: split-K workspace allocation failed";
     case SGEMM_ERR_UNSUPPORTED: return "SGEMM_ERR_UNSUPPORTED: dimension too large or no usable device";
+    case SGEMM_ERR_SCRATCH_LIMIT:
+      return "SGEMM_ERR_SCRATCH_LIMIT: split-K partial sums exceed sgemm_noalloc's static scratch array";
     case -1: return "invalid argument 1 (transA)";
     case -2: return "invalid argument 2 (transB)";
     case -3: return "invalid argument 3 (M < 0)";

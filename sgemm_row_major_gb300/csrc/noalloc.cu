@@ -1,0 +1,164 @@
+// noalloc.cu -- sgemm_noalloc(): the same SGEMM as sgemm(), for callers that
+// cannot allocate device memory while the call runs.
+//
+// Who needs it: sgemm() takes its split-K partial sums from a stream-ordered
+// memory pool, which may grow (allocate) on a call.  Some callers cannot allow
+// that: an application that has already handed nearly all device memory to
+// its own allocator (so a new allocation can fail at an arbitrary call), or
+// latency-critical code that cannot absorb the cost of a pool growing in the
+// middle of its work.  sgemm_noalloc() gives them the same kernels with the
+// partial sums in a fixed array that is part of the library image itself.
+//
+// The scratch array: a file-scope __device__ array of
+// SGEMM_NOALLOC_SCRATCH_BYTES.  Every GPU that loads the library holds one
+// copy of it until the process exits.  Host code cannot use the array's name
+// as a device address (on the host it names a stand-in object), so the
+// device address is looked up with cudaGetSymbolAddress once per device, with
+// that device current, on the first sgemm_noalloc() call there; that first
+// call should therefore come before any stream capture.  Nothing in the array
+// needs to start at zero: the GEMM kernel writes every partial sum the
+// reduction reads in the same call.  All calls on a device share the array,
+// so two calls whose kernels overlap on the GPU (different streams, no
+// ordering between them) race on it.
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "kernel_tma.cuh"
+#include "sgemm.h"
+#include "sgemm_internal.h"
+
+using namespace sgemm_impl;
+
+namespace {
+
+static __device__ __align__(256) float g_noalloc_scratch[SGEMM_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+
+struct NoallocDevice {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  int sm_count = 0;
+  unsigned* fault = nullptr;
+  float* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoallocDevice g_nd[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Per-device set-up, once, with the device current: SM count, fault word,
+// scratch address and kernel attributes.  No allocation happens here.
+cudaError_t setup(int dev, NoallocDevice** out) {
+  NoallocDevice& d = g_nd[dev];
+  std::call_once(d.once, [&] {
+    cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = fault_word(&d.fault);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.scratch), g_noalloc_scratch);
+    if (e == cudaSuccess) e = prepare_tma_op_nn();
+    if (e == cudaSuccess) e = prepare_tma_op_nt();
+    if (e == cudaSuccess) e = prepare_tma_op_tn();
+    if (e == cudaSuccess) e = prepare_tma_op_tt();
+    d.err = e;
+  });
+  *out = &d;
+  return d.err;
+}
+
+cudaError_t encode_2d(const float* base, int64_t inner, int64_t outer, int64_t ld, int box_inner, int box_outer,
+                      bool swizzle128, CUtensorMap* map) {
+  static EncodeTiledFn fn = nullptr;
+  static cudaError_t fn_err = cudaSuccess;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    fn_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (fn_err == cudaSuccess && (q != cudaDriverEntryPointSuccess || !p)) fn_err = cudaErrorNotSupported;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (fn_err != cudaSuccess) return fn_err;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 4u};
+  const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
+                             const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                             int64_t ldc, struct CUstream_st* stream) {
+  // Same argument checks and the same planner as sgemm() (pure host logic);
+  // a first pass with a nominal SM count rejects bad arguments before any
+  // CUDA call, the second uses the device's SM count.
+  sgemm_plan_t plan;
+  int st = sgemm_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 152, &plan);
+  if (st != SGEMM_OK) return st;
+  if (plan.variant == SGEMM_VARIANT_NONE) return SGEMM_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return SGEMM_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
+  NoallocDevice* nd = nullptr;
+  if (setup(dev, &nd) != cudaSuccess) return SGEMM_ERR_CUDA;
+  st = sgemm_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nd->sm_count, &plan);
+  if (st != SGEMM_OK) return st;
+  if ((uint64_t)plan.workspace_bytes > (uint64_t)SGEMM_NOALLOC_SCRATCH_BYTES) return SGEMM_ERR_SCRATCH_LIMIT;
+
+  const bool ta = transA == 'T' || transA == 't' || transA == 'C' || transA == 'c';
+  const bool tb = transB == 'T' || transB == 't' || transB == 'C' || transB == 'c';
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  GemmParams p{};
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.A = A;
+  p.B = B;
+  p.C = C;
+  p.lda = lda;
+  p.ldb = ldb;
+  p.ldc = ldc;
+  p.c_vec = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0;
+  p.timeout_ns = 2000ull * 1000000ull;
+  p.fault = nd->fault;
+
+  if (plan.variant == SGEMM_VARIANT_SCALE) {
+    e = launch_scale(p, cs);
+    return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+  }
+  const int split = plan.split_k;
+  p.tiles_m = (int)ceil_div(M, plan.tile_m);
+  p.tiles_n = (int)ceil_div(N, plan.tile_n);
+  p.k_tiles_per_split = (int)ceil_div(ceil_div(K, plan.tile_k), split);
+  p.ws_ld = ceil_div(N, 4) * 4;
+  p.ws = split > 1 ? nd->scratch : nullptr;
+
+  if (plan.variant == SGEMM_VARIANT_GENERIC) {
+    e = launch_generic_gemm(ta, tb, p, split, cs);
+  } else {
+    CUtensorMap mapA, mapB;
+    const int bm = plan.tile_m, bn = plan.tile_n, bk = plan.tile_k;
+    e = ta ? encode_2d(A, M, K, lda, bm, bk, false, &mapA) : encode_2d(A, K, M, lda, bk, bm, true, &mapA);
+    if (e == cudaSuccess)
+      e = tb ? encode_2d(B, K, N, ldb, bk, bn, true, &mapB) : encode_2d(B, N, K, ldb, bn, bk, false, &mapB);
+    if (e != cudaSuccess) return SGEMM_ERR_CUDA;
+    const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
+    if (!ta && !tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, cs);
+    else if (!ta && tb) e = launch_tma_op_nt(tile, mapA, mapB, p, split, cs);
+    else if (ta && !tb) e = launch_tma_op_tn(tile, mapA, mapB, p, split, cs);
+    else e = launch_tma_op_tt(tile, mapA, mapB, p, split, cs);
+  }
+  if (e == cudaSuccess && split > 1) e = launch_splitk_reduce(p, split, cs);
+  return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
