@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prewarm-s", type=float, default=0.5, help="untimed seconds of steps before the warm-up")
+    ap.add_argument("--no-cublas-context", action="store_true",
+                    help="skip the cuBLAS FP32 context number (torch.matmul, TF32 off)")
     return ap.parse_args()
 
 
@@ -218,6 +221,42 @@ def config_block(case, n_gpus):
 
 # ---------------------------------------------------------------- our arm
 
+def cublas_context(case, sets, steps, stream):
+    """cuBLAS FP32 SGEMM through torch.matmul with TF32 disabled, same shapes, as a context number.
+
+    Computes alpha*op(A)@op(B) + beta*C with torch.addmm into a preallocated
+    output; not part of the measured path.
+    """
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        outs = [torch.empty_like(s[2][:, :case.N]) for s in sets]
+
+        def one(i):
+            A, B, C = sets[i & 1]
+            a = A[:, :(case.M if case.transA == "T" else case.K)]
+            b = B[:, :(case.K if case.transB == "T" else case.N)]
+            a = a.t() if case.transA == "T" else a
+            b = b.t() if case.transB == "T" else b
+            torch.addmm(C[:, :case.N], a, b, beta=case.beta, alpha=case.alpha, out=outs[i & 1])
+
+        for i in range(5):
+            one(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            one(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        return {"value": si.flops(case.M, case.N, case.K) / (ms * 1e-3) / 1e12, "unit": UNIT,
+                "what": "cuBLAS FP32 via torch.addmm, allow_tf32=False, same shapes and input sets; context only"}
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -259,8 +298,8 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    # pre-warm ~0.5 s so clocks settle, then exactly W warm-up steps
-    t_end = time.time() + 0.5
+    # pre-warm so clocks settle, then exactly W warm-up steps
+    t_end = time.time() + args.prewarm_s
     i = 0
     while time.time() < t_end:
         step(i)
@@ -316,7 +355,7 @@ def run_ours(args):
                  d["ldc"], sh)
         hOut.copy_(C0, non_blocking=True)
 
-    for _ in range(2):
+    for _ in range(2 if args.e2e_steps > 0 else 0):
         e2e_step()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -331,7 +370,7 @@ def run_ours(args):
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    e2e_value = world * flops_step * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_value = world * flops_step * args.e2e_steps / (e2e_ms * 1e-3) / 1e12 if args.e2e_steps > 0 else None
     h2d = (hA.numel() + hB.numel() + hC.numel()) * 4
     d2h = hOut.numel() * 4
 
@@ -347,7 +386,7 @@ def run_ours(args):
     max_mhz = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
     peak = sms * FMA_PER_SM_PER_CLK * 2 * max_mhz * 1e6 / 1e12
     roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": traffic_from_profile(lib_build.source_digest()),
+            "traffic": traffic_from_profile(lib_build.tma_kernel_digest()),
             "peak_basis": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz max SM clock",
             "kernel": "tma_gemm_kernel (SIMT FFMA2)" if plan["variant_name"].startswith("TMA") else plan["variant_name"],
             "kernel_ms": kernel_ms}
@@ -358,7 +397,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {**config_block(case, world), "prewarm_s": 0.5,
+        "config": {**config_block(case, world), "prewarm_s": args.prewarm_s,
                    "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "tile_k", "stages",
                                                  "split_k", "grid_x", "grid_y")}},
         "pct_ffma_peak": 100.0 * achieved / peak,
@@ -367,6 +406,8 @@ def run_ours(args):
         "gpu_launches": plan["kernel_launches"] * args.steps,
         "clocks": clocks,
     }
+    if not args.no_cublas_context:
+        line["context_cublas_fp32"] = cublas_context(case, sets, min(args.steps, 50), stream)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, d, args.cpu_seconds)
     print(json.dumps(line), flush=True)

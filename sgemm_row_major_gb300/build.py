@@ -54,6 +54,20 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
+TMA_KERNEL_FILES = ["kernel_tma.cuh", "device_utils.cuh", "sgemm_internal.h", "kernel_tma_nn.cu",
+                    "kernel_tma_nt.cu", "kernel_tma_tn.cu", "kernel_tma_tt.cu"]
+
+
+def tma_kernel_digest() -> str:
+    """Hash of the sources of the TMA-fed GEMM kernel only (identifies the profiled kernel build)."""
+    h = hashlib.sha256()
+    for name in TMA_KERNEL_FILES:
+        h.update(name.encode())
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]

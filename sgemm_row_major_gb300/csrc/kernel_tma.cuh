@@ -10,13 +10,21 @@
 //     N and K for free.  (A separate producer warp would put 3 warps on one
 //     SM sub-partition and cap every thread at 168 registers.)
 //   * all threads wait for a stage ("full" mbarrier), run the register outer
-//     products out of shared memory and release the stage.
-//   * each consumer thread owns an 8x8 block of C (warp tile 32x64) and
-//     accumulates with packed fma.rn.f32x2 (two IEEE fp32 FMAs per issue).
-//   * every kFlushTiles K tiles the running sums are folded into a second
-//     accumulator, so no float accumulator adds more than 128 products; this
-//     keeps the relative Frobenius error near 3e-7 at K = 4096 instead of the
-//     ~1.2e-6 a single accumulator over all of K gives.
+//     products out of shared memory and release the stage.  Shared-memory
+//     fragments are double-buffered in registers: the loads of k-group g+1
+//     (across a stage boundary, the next tile's first group) issue while
+//     group g's FMAs run, so the two warps of an SM sub-partition do not
+//     stall together on shared-memory latency.
+//   * each thread owns an 8x8 block of C (warp tile 32x64) and accumulates
+//     with packed fma.rn.f32x2 (two IEEE fp32 FMAs per issue, a broadcast
+//     A value times a pair of adjacent B values).
+//   * every kFlushTiles K tiles the register sums are folded into running
+//     sums kept in tensor memory (TMEM, otherwise unused by this SIMT kernel),
+//     so no float accumulator adds more than 128 products; this keeps the
+//     relative Frobenius error near 3e-7 at K = 4096 instead of the ~1.2e-6 a
+//     single accumulator over all of K gives, and costs no registers.
+//   * every bounded wait is voted across the warp, so a warp leaves the loop
+//     as a whole and the warp-collective TMEM instructions stay converged.
 //   * epilogue C = alpha*acc + beta*C fused, 128-bit where C allows it; C is
 //     not read when beta == 0.  With a K split, the raw partial sums go to a
 //     workspace instead and a reduction kernel applies the epilogue.
@@ -47,6 +55,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers;
 constexpr int kFlushTiles = 4;
+constexpr uint32_t kTmemCols = 128;  // 2 warp columns x 64 running sums per thread
 constexpr int kGroupM = 8;  // tile rows per raster group (L2 reuse of B)
 
 template <int WM, int WN>
@@ -95,55 +104,144 @@ __device__ __forceinline__ int col_of(int j, int wn, int tx) {
             : wn * 64 + 32 * (j >> 2) + 4 * tx + (j & 3);  // 2 groups of 4 adjacent columns
 }
 
-// One K tile (32 k) of outer products out of one pipeline stage.
+// Per-thread byte offsets into a stage's tiles (see load_group).
+struct Offsets {
+  uint32_t xa_even, xa_odd;  // K-major A: rows of even / odd i, with their swizzle phase
+  uint32_t xa_mn;            // M-major A
+  uint32_t xb_k;             // K-major B
+  uint32_t xb_mn;            // N-major B
+};
+
+// Fragments of one group of 4 k: a[kk][i] = op(A)(row_i, k), b[kk][j] = op(B)(k, col_j).
+// Each operand takes 8 128-bit shared-memory loads per group, whatever its layout.
 template <int WM, int WN, bool TA, bool TB>
-__device__ __forceinline__ void mma_stage(const uint8_t* a_tile, const uint8_t* b_tile, uint32_t xa_even,
-                                          uint32_t xa_odd, uint32_t xa_mn, uint32_t xb_k, uint32_t xb_mn,
-                                          float2 (&acc)[8][4]) {
+__device__ __forceinline__ void load_group(const uint8_t* a_tile, const uint8_t* b_tile, int g, const Offsets& o,
+                                           float (&a)[4][8], float (&b)[4][8]) {
   using T = Tile<WM, WN>;
+  if (!TA) {
+    // K-contiguous rows, 128-byte swizzle: one load = 4 k of one row.
 #pragma unroll
-  for (int g = 0; g < kBK / 4; ++g) {  // groups of 4 k
-    float a[4][8], b[4][8];
-    if (!TA) {
-      // K-contiguous rows, swizzled: one 128-bit load = 4 k of one row.
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t off = (((i & 1) ? xa_odd : xa_even) ^ (uint32_t)(g << 4)) + (uint32_t)(i >> 1) * 1024u;
-        const float4 v = lds128(a_tile, off);
-        a[0][i] = v.x; a[1][i] = v.y; a[2][i] = v.z; a[3][i] = v.w;
-      }
-    } else {
-      // M-contiguous: one 128-bit load = 4 adjacent rows at one k.
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float4 v = lds128(a_tile, xa_mn + (uint32_t)((4 * g + kk) * T::BM * 4 + h * 64));
-          a[kk][4 * h + 0] = v.x; a[kk][4 * h + 1] = v.y; a[kk][4 * h + 2] = v.z; a[kk][4 * h + 3] = v.w;
-        }
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t off = (((i & 1) ? o.xa_odd : o.xa_even) ^ (uint32_t)(g << 4)) + (uint32_t)(i >> 1) * 1024u;
+      const float4 v = lds128(a_tile, off);
+      a[0][i] = v.x; a[1][i] = v.y; a[2][i] = v.z; a[3][i] = v.w;
     }
-    if (!TB) {
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float4 v = lds128(b_tile, xb_mn + (uint32_t)((4 * g + kk) * T::BN * 4 + h * 128));
-          b[kk][4 * h + 0] = v.x; b[kk][4 * h + 1] = v.y; b[kk][4 * h + 2] = v.z; b[kk][4 * h + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 v = lds128(b_tile, (xb_k ^ (uint32_t)(g << 4)) + (uint32_t)j * 1024u);
-        b[0][j] = v.x; b[1][j] = v.y; b[2][j] = v.z; b[3][j] = v.w;
-      }
-    }
+  } else {
+    // M-contiguous: one load = 4 adjacent rows at one k.
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int h = 0; h < 2; ++h) {
+        const float4 v = lds128(a_tile, o.xa_mn + (uint32_t)((4 * g + kk) * T::BM * 4 + h * 64));
+        a[kk][4 * h + 0] = v.x; a[kk][4 * h + 1] = v.y; a[kk][4 * h + 2] = v.z; a[kk][4 * h + 3] = v.w;
+      }
+  }
+  if (!TB) {
 #pragma unroll
-        for (int p = 0; p < 4; ++p)
-          acc[i][p] = ffma2(a[kk][i], make_float2(b[kk][2 * p], b[kk][2 * p + 1]), acc[i][p]);
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float4 v = lds128(b_tile, o.xb_mn + (uint32_t)((4 * g + kk) * T::BN * 4 + h * 128));
+        b[kk][4 * h + 0] = v.x; b[kk][4 * h + 1] = v.y; b[kk][4 * h + 2] = v.z; b[kk][4 * h + 3] = v.w;
+      }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 v = lds128(b_tile, (o.xb_k ^ (uint32_t)(g << 4)) + (uint32_t)j * 1024u);
+      b[0][j] = v.x; b[1][j] = v.y; b[2][j] = v.z; b[3][j] = v.w;
+    }
+  }
+}
+
+// 4 rank-1 updates of the 8x8 accumulator block: 128 packed FMAs, k ascending.
+__device__ __forceinline__ void fma_group(const float (&a)[4][8], const float (&b)[4][8], float2 (&acc)[8][4]) {
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        acc[i][p] = ffma2(a[kk][i], make_float2(b[kk][2 * p], b[kk][2 * p + 1]), acc[i][p]);
+}
+
+// The thread's 64 running sums live in 64 consecutive TMEM columns of its own
+// lane (warps 0-3: columns 0-63 of lanes 0-127; warps 4-7: columns 64-127).
+// Element (i, 2p + h) of the 8x8 block is column 8i + 2p + h.
+__device__ __forceinline__ void fold_into_tmem(uint32_t taddr, float2 (&acc)[8][4]) {
+  float m[4][16];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld16(taddr + 16u * c, m[c]);
+  tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld_ready(m[c]);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int i = 2 * c + (e >> 2), p = e & 3;
+      m[c][2 * e] += acc[i][p].x;
+      m[c][2 * e + 1] += acc[i][p].y;
+      acc[i][p] = make_float2(0.0f, 0.0f);
+    }
+    tmem_st16(taddr + 16u * c, m[c]);
+  }
+  tmem_wait_st();
+}
+
+// C = alpha * v + beta * C for the thread's 8x8 block (v[8i + j] is row i,
+// column j of the block), or the raw sums into slice blockIdx.y of the
+// split-K workspace.  C is not read when beta == 0; 128-bit accesses where
+// the 4 columns are in range and C allows it.
+template <int WM, int WN, bool TA, bool TB, bool SPLIT>
+__device__ __forceinline__ void epilogue(const GemmParams& p, int m0, int n0, int wm, int wn, int ty, int tx,
+                                         const float (&v)[64]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = m0 + row_of<TA>(i, wm, ty);
+    if (row >= p.M) continue;
+    if (!TB) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int col = n0 + col_of<false>(4 * h, wn, tx);
+        const float* x = &v[8 * i + 4 * h];
+        if (SPLIT) {
+          if (col < p.N) {
+            float* w = p.ws + ((int64_t)blockIdx.y * p.M + row) * p.ws_ld + col;
+            *reinterpret_cast<float4*>(w) = make_float4(x[0], x[1], x[2], x[3]);
+          }
+          continue;
+        }
+        float* c = p.C + (int64_t)row * p.ldc + col;
+        if (p.c_vec && col + 3 < p.N) {
+          float4 o;
+          if (p.beta == 0.0f) {
+            o = make_float4(p.alpha * x[0], p.alpha * x[1], p.alpha * x[2], p.alpha * x[3]);
+          } else {
+            const float4 old = *reinterpret_cast<const float4*>(c);
+            o = make_float4(fmaf(p.alpha, x[0], p.beta * old.x), fmaf(p.alpha, x[1], p.beta * old.y),
+                            fmaf(p.alpha, x[2], p.beta * old.z), fmaf(p.alpha, x[3], p.beta * old.w));
+          }
+          *reinterpret_cast<float4*>(c) = o;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (col + q < p.N) c[q] = p.beta == 0.0f ? p.alpha * x[q] : fmaf(p.alpha, x[q], p.beta * c[q]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int col = n0 + col_of<true>(j, wn, tx);
+        if (col >= p.N) continue;
+        const float x = v[8 * i + j];
+        if (SPLIT) {
+          p.ws[((int64_t)blockIdx.y * p.M + row) * p.ws_ld + col] = x;
+        } else {
+          float* c = p.C + (int64_t)row * p.ldc + col;
+          *c = p.beta == 0.0f ? p.alpha * x : fmaf(p.alpha, x, p.beta * *c);
+        }
+      }
+    }
   }
 }
 
@@ -155,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ uint32_t tmem_slot;
 
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -172,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kt0 = blockIdx.y * p.k_tiles_per_split;
   const int nkt = min(kt_total, kt0 + p.k_tiles_per_split) - kt0;  // >= 1 by construction
 
+  if (warp == 0) tmem_alloc(smem_addr(&tmem_slot), kTmemCols);
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
@@ -180,7 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
+  tmem_fence_before_sync();
   __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t taddr = tmem_slot + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(64 * (warp >> 2));
 
   // Producer side (thread 0): load K tile t into stage t % kStages.
   auto issue = [&](int t) {
@@ -205,124 +308,119 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int wm = warp / WN, wn = warp % WN;
   const int ty = lane >> 3, tx = lane & 7;
+  Offsets o;
+  {
+    const uint32_t ra_even = (uint32_t)(wm * 32 + ty);  // rows of even i: & 7 == ty
+    const uint32_t ra_odd = ra_even + 4;                 // rows of odd i:  & 7 == ty + 4
+    o.xa_even = ra_even * 128u + ((ra_even & 7u) << 4);
+    o.xa_odd = ra_odd * 128u + ((ra_odd & 7u) << 4);
+    o.xa_mn = (uint32_t)(wm * 32 + 4 * ty) * 4u;
+    const uint32_t cb = (uint32_t)(wn * 64 + tx);        // & 7 == tx
+    o.xb_k = cb * 128u + ((cb & 7u) << 4);
+    o.xb_mn = (uint32_t)(wn * 64 + 4 * tx) * 4u;
+  }
 
-  // Per-thread byte offsets into a stage's tiles (see mma_stage).
-  const uint32_t ra_even = (uint32_t)(wm * 32 + ty);      // rows of even i: & 7 == ty
-  const uint32_t ra_odd = ra_even + 4;                     // rows of odd i:  & 7 == ty + 4
-  const uint32_t xa_even = ra_even * 128u + ((ra_even & 7u) << 4);
-  const uint32_t xa_odd = ra_odd * 128u + ((ra_odd & 7u) << 4);
-  const uint32_t xa_mn = (uint32_t)(wm * 32 + 4 * ty) * 4u;
-  const uint32_t cb = (uint32_t)(wn * 64 + tx);            // & 7 == tx
-  const uint32_t xb_k = cb * 128u + ((cb & 7u) << 4);
-  const uint32_t xb_mn = (uint32_t)(wn * 64 + 4 * tx) * 4u;
-
-  float2 acc[8][4], mst[8][4];
+  float2 acc[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[i][q] = mst[i][q] = make_float2(0.0f, 0.0f);
+    for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.0f, 0.0f);
+  {
+    // the TMEM running sums start at zero
+    float z[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) z[e] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_st16(taddr + 16u * c, z);
+    tmem_wait_st();
+  }
 
-  bool ok = true;
-  for (int t = 0; t < nkt; ++t) {
+  // Fragments are double-buffered: group g+1 (or the next tile's group 0)
+  // is loaded while group g's FMAs issue.
+  float a0[4][8], b0[4][8], a1[4][8], b1[4][8];
+  bool ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&full_bar[0]), 0u, p.timeout_ns));
+  if (!ok) {
+    if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
+  } else {
+    load_group<WM, WN, TA, TB>(smem, smem + T::A_BYTES, 0, o, a0, b0);
+  }
+
+  for (int t = 0; ok && t < nkt; ++t) {
     const int s = t % kStages;
     // Refill the stage consumed in the previous iteration with tile t-1+kStages.
     if (producer && t >= 1 && issued < nkt) {
       const int tp = t - 1;
-      if (!mbar_wait(smem_addr(&empty_bar[tp % kStages]), (uint32_t)(tp / kStages) & 1u, p.timeout_ns)) {
+      if (mbar_wait(smem_addr(&empty_bar[tp % kStages]), (uint32_t)(tp / kStages) & 1u, p.timeout_ns)) {
+        issue(issued++);
+      } else {
         atomicOr(p.fault, (unsigned)kFaultEmptyWait);
         ok = false;
-        break;
       }
-      issue(issued++);
     }
-    if (!mbar_wait(smem_addr(&full_bar[s]), (uint32_t)(t / kStages) & 1u, p.timeout_ns)) {
-      atomicOr(p.fault, (unsigned)kFaultFullWait);
-      ok = false;
-      break;
-    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+
     const uint8_t* a_tile = smem + s * T::STAGE_BYTES;
-    mma_stage<WM, WN, TA, TB>(a_tile, a_tile + T::A_BYTES, xa_even, xa_odd, xa_mn, xb_k, xb_mn, acc);
-    mbar_arrive(smem_addr(&empty_bar[s]));
-    if (t % kFlushTiles == kFlushTiles - 1) {
+    const uint8_t* b_tile = a_tile + T::A_BYTES;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          mst[i][q].x += acc[i][q].x;
-          mst[i][q].y += acc[i][q].y;
-          acc[i][q] = make_float2(0.0f, 0.0f);
+    for (int gp = 0; gp < 4; ++gp) {
+      load_group<WM, WN, TA, TB>(a_tile, b_tile, 2 * gp + 1, o, a1, b1);
+      fma_group(a0, b0, acc);
+      if (gp < 3) {
+        load_group<WM, WN, TA, TB>(a_tile, b_tile, 2 * gp + 2, o, a0, b0);
+      } else if (t + 1 < nkt) {
+        const int sn = (t + 1) % kStages;
+        const bool w = __all_sync(0xffffffffu,
+                                  mbar_wait(smem_addr(&full_bar[sn]), (uint32_t)((t + 1) / kStages) & 1u, p.timeout_ns));
+        if (w) {
+          const uint8_t* na = smem + sn * T::STAGE_BYTES;
+          load_group<WM, WN, TA, TB>(na, na + T::A_BYTES, 0, o, a0, b0);
+        } else {
+          if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
+          ok = false;
         }
+      }
+      fma_group(a1, b1, acc);
     }
+    mbar_arrive(smem_addr(&empty_bar[s]));
+    if (t % kFlushTiles == kFlushTiles - 1) fold_into_tmem(taddr, acc);
   }
-  if (!ok) {
+
+  if (ok) {
+    // fold the last partial sums: the block's results end up in fin[64]
+    float m[4][16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld16(taddr + 16u * c, m[c]);
+    tmem_wait_ld();
+    float fin[64];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      tmem_ld_ready(m[c]);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) fin[16 * c + e] = m[c][e];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        fin[8 * i + 2 * q] += acc[i][q].x;
+        fin[8 * i + 2 * q + 1] += acc[i][q].y;
+      }
+    epilogue<WM, WN, TA, TB, SPLIT>(p, m0, n0, wm, wn, ty, tx, fin);
+  } else if (producer) {
     // A wait gave up.  Thread 0 must not leave while copies it issued into this
     // CTA's shared memory may still land: wait (bounded) for the last phase of
-    // every stage that received a load, then everyone returns without writing C.
-    if (producer) {
-      for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
-        if (!mbar_wait(smem_addr(&full_bar[t % kStages]), (uint32_t)(t / kStages) & 1u, p.timeout_ns))
-          atomicOr(p.fault, (unsigned)kFaultDrainWait);
-    }
-    return;
+    // every stage that received a load.  C is not written.
+    for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
+      if (!mbar_wait(smem_addr(&full_bar[t % kStages]), (uint32_t)(t / kStages) & 1u, p.timeout_ns))
+        atomicOr(p.fault, (unsigned)kFaultDrainWait);
   }
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      mst[i][q].x += acc[i][q].x;
-      mst[i][q].y += acc[i][q].y;
-    }
 
-  // ---------------- epilogue ----------------
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int row = m0 + row_of<TA>(i, wm, ty);
-    if (row >= p.M) continue;
-    if (!TB) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int col = n0 + col_of<false>(4 * h, wn, tx);
-        const float v[4] = {mst[i][2 * h].x, mst[i][2 * h].y, mst[i][2 * h + 1].x, mst[i][2 * h + 1].y};
-        if (SPLIT) {
-          if (col < p.N) {
-            float* w = p.ws + ((int64_t)blockIdx.y * p.M + row) * p.ws_ld + col;
-            *reinterpret_cast<float4*>(w) = make_float4(v[0], v[1], v[2], v[3]);
-          }
-          continue;
-        }
-        float* c = p.C + (int64_t)row * p.ldc + col;
-        if (p.c_vec && col + 3 < p.N) {
-          float4 o;
-          if (p.beta == 0.0f) {
-            o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
-          } else {
-            const float4 old = *reinterpret_cast<const float4*>(c);
-            o = make_float4(fmaf(p.alpha, v[0], p.beta * old.x), fmaf(p.alpha, v[1], p.beta * old.y),
-                            fmaf(p.alpha, v[2], p.beta * old.z), fmaf(p.alpha, v[3], p.beta * old.w));
-          }
-          *reinterpret_cast<float4*>(c) = o;
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (col + q < p.N)
-              c[q] = p.beta == 0.0f ? p.alpha * v[q] : fmaf(p.alpha, v[q], p.beta * c[q]);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int col = n0 + col_of<true>(j, wn, tx);
-        if (col >= p.N) continue;
-        const float v = (j & 1) ? mst[i][j >> 1].y : mst[i][j >> 1].x;
-        if (SPLIT) {
-          p.ws[((int64_t)blockIdx.y * p.M + row) * p.ws_ld + col] = v;
-        } else {
-          float* c = p.C + (int64_t)row * p.ldc + col;
-          *c = p.beta == 0.0f ? p.alpha * v : fmaf(p.alpha, v, p.beta * *c);
-        }
-      }
-    }
-  }
+  // release the tensor memory once every warp is done with it
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem_slot, kTmemCols);
 }
 
 template <int WM, int WN, bool TA, bool TB>
