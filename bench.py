@@ -52,6 +52,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prewarm-s", type=float, default=0.5, help="untimed seconds of steps before the warm-up")
+    ap.add_argument("--variant", default="AUTO", help="planner override (tests and experiments)")
     ap.add_argument("--no-cublas-context", action="store_true",
                     help="skip the cuBLAS FP32 context number (torch.matmul, TF32 off)")
     return ap.parse_args()
@@ -277,6 +278,8 @@ def run_ours(args):
     d = si.make_case(case)
     M, N, K = case.M, case.N, case.K
     stream = torch.cuda.current_stream(dev)
+    if args.variant != "AUTO":
+        sg.sgemm_set_variant_override(args.variant, 0)
     sh = stream.cuda_stream
 
     # two device-resident input sets, used in turn
@@ -388,7 +391,9 @@ def run_ours(args):
     roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": traffic_from_profile(lib_build.tma_kernel_digest()),
             "peak_basis": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz max SM clock",
-            "kernel": "tma_gemm_kernel (SIMT FFMA2)" if plan["variant_name"].startswith("TMA") else plan["variant_name"],
+            "kernel": {"TMA_128x128": "tma_gemm_kernel (SIMT FFMA2)", "TMA_64x256": "tma_gemm_kernel (SIMT FFMA2)",
+                       "TC_TF32X3": "tf32x3_gemm_kernel (tcgen05, 3xTF32)"}.get(plan["variant_name"],
+                                                                                plan["variant_name"]),
             "kernel_ms": kernel_ms}
     if clocks.get("sm_mhz"):
         roof["frac_at_sampled_clock"] = achieved / (sms * FMA_PER_SM_PER_CLK * 2 * clocks["sm_mhz"] * 1e6 / 1e12)

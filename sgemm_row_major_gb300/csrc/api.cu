@@ -77,6 +77,7 @@ int device_state(int* device_out, DeviceState** st_out) {
     if (err == cudaSuccess) err = prepare_tma_op_nt();
     if (err == cudaSuccess) err = prepare_tma_op_tn();
     if (err == cudaSuccess) err = prepare_tma_op_tt();
+    if (err == cudaSuccess) err = prepare_tf32x3();
     if (err == cudaSuccess) {
       cudaMemPoolProps props = {};
       props.allocType = cudaMemAllocationTypePinned;
@@ -185,12 +186,17 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   const int ov = g_override_variant.load();
   if (ov == SGEMM_VARIANT_GENERIC || ov == SGEMM_VARIANT_TMA_128x128 || ov == SGEMM_VARIANT_TMA_64x256)
     variant = (ov == SGEMM_VARIANT_GENERIC || tma_ok) ? ov : SGEMM_VARIANT_GENERIC;
+  // The tensor-core kernel handles op = NN on TMA-compatible operands, without a K split.
+  const bool tc_ok = tma_ok && !pr.ta && !pr.tb;
+  if (ov == SGEMM_VARIANT_TC_TF32X3) variant = tc_ok ? ov : variant;
 
   int bm, bn, bk, threads, stages;
   int64_t smem = 0;
   if (variant == SGEMM_VARIANT_GENERIC) {
     const GenericTileShape g = generic_tile_shape();
     bm = g.bm; bn = g.bn; bk = g.bk; threads = g.threads; stages = 2;
+  } else if (variant == SGEMM_VARIANT_TC_TF32X3) {
+    bm = 128; bn = 128; bk = 32; threads = 320; stages = 3; smem = 3 * 32768 + 2 * 65536 + 1024;
   } else if (variant == SGEMM_VARIANT_TMA_128x128) {
     using T = tma::Tile<4, 2>;
     bm = T::BM; bn = T::BN; bk = tma::kBK; threads = tma::kThreads; stages = tma::kStages; smem = T::SMEM_BYTES;
@@ -209,6 +215,7 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   const int ov_split = g_override_split.load();
   if (ov_split > 0) split = ov_split;
   split = std::max<int64_t>(1, std::min<int64_t>({split, kt, 256}));
+  if (variant == SGEMM_VARIANT_TC_TF32X3) split = 1;
   const int64_t per = ceil_div(kt, split);
   split = ceil_div(kt, per);  // no empty slice
 
@@ -283,6 +290,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   cudaError_t e;
   if (plan.variant == SGEMM_VARIANT_GENERIC) {
     e = launch_generic_gemm(pr.ta, pr.tb, p, split, stream);
+  } else if (plan.variant == SGEMM_VARIANT_TC_TF32X3) {
+    e = launch_tf32x3_nn(mapA, mapB, p, stream);
   } else {
     const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
     if (!pr.ta && !pr.tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, stream);
@@ -337,7 +346,7 @@ int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float 
 
 int sgemm_set_variant_override(int variant, int split_k) {
   if (variant != SGEMM_VARIANT_AUTO && variant != SGEMM_VARIANT_GENERIC && variant != SGEMM_VARIANT_TMA_128x128 &&
-      variant != SGEMM_VARIANT_TMA_64x256)
+      variant != SGEMM_VARIANT_TMA_64x256 && variant != SGEMM_VARIANT_TC_TF32X3)
     return -1;
   g_override_variant.store(variant);
   g_override_split.store(split_k < 0 ? 0 : split_k);

@@ -1,0 +1,351 @@
+// kernel_tf32x3.cu -- SGEMM on the 5th-generation tensor cores (tcgen05) with
+// the 3xTF32 split, for sm_103a.
+//
+// Each float x is split into hi = x rounded to TF32 (round to nearest, ties
+// away, done with integer ops on the bits) and lo = x - hi (exact in float).
+// The tensor core reads TF32 operands as the top 19 bits of each 32-bit word,
+// so it sees lo truncated: x = hi + lo' + e with |e| < 2^-21 |x|, and e has
+// the sign of lo, which is random, so the split adds no bias.  A product is
+// formed from three TF32 tensor-core products,
+//     a*b ~= a_lo*b_hi + a_hi*b_lo + a_hi*b_hi      (a_lo*b_lo, < 2^-22 |ab|, dropped)
+// accumulated in FP32 in tensor memory.  The pages name tensor cores as the
+// missing piece of their SGEMM and TF32 as the tensor-core format for FP32
+// inputs (itan.pw "CUDA NVIDIA 4090 高性能計算", §4; youngju.dev "CUDA
+// architecture visualized", テンソルコア); the split keeps FP32 accuracy, and
+// the result must pass the same error bounds as the SIMT kernel.
+//
+// The tensor core's FP32 accumulation is not round-to-nearest: measured on
+// GB300, one accumulator over K = 4096 drifts to a relative Frobenius error of
+// ~3e-5, growing linearly with the number of accumulated MMAs.  So every 32-k
+// tile gets a fresh accumulator (12 MMAs), and the splitter warps fold it into
+// FP32 registers with round-to-nearest adds; the error then no longer grows
+// with K (~2e-7 relative).
+//
+// CTA (one 128x128 output tile, 10 warps):
+//   warp 0     TMA producer: FP32 tiles of op(A) and op(B) (as stored) into a
+//              3-stage "raw" ring (32 KB per stage).
+//   warp 1     MMA issuer (one thread): per 32-k tile, 4 k-steps x 3
+//              tcgen05.mma (M=128, N=128, K=8) into one of two 128x128 FP32
+//              accumulators in TMEM; tcgen05.commit releases the split stage
+//              and hands the accumulator to the folders.
+//   warps 2-9  split raw stage t -> hi/lo tiles in the K-major, 128-byte
+//              swizzled layout the tensor core reads (A keeps its layout; B,
+//              N-contiguous in memory, is transposed on the way) in a 2-stage
+//              "split" ring (64 KB per stage); fold accumulator t-1 into
+//              registers (each thread: 64 columns of one row); finally the
+//              alpha/beta epilogue.
+// Every wait is bounded (mbarrier phases).
+#include "device_utils.cuh"
+#include "sgemm_internal.h"
+
+namespace sgemm_impl {
+namespace tc {
+
+constexpr int BM = 128, BN = 128, BK = 32;
+constexpr int kRawStages = 3, kSplitStages = 2;
+constexpr int kTileBytes = 128 * BK * 4;            // one 128 x 32 operand tile, 16 KB
+constexpr int kRawBytes = 2 * kTileBytes;           // A + B as loaded
+constexpr int kSplitBytes = 4 * kTileBytes;         // A_hi, A_lo, B_hi, B_lo
+constexpr int kSmemBytes = kRawStages * kRawBytes + kSplitStages * kSplitBytes + 1024;
+constexpr int kThreads = 320;
+constexpr int kSplitters = 256;                     // warps 2-9
+constexpr uint32_t kAccCols = 128;                  // one 128 x 128 FP32 accumulator
+constexpr uint32_t kTmemCols = 2 * kAccCols;        // double-buffered
+
+// tcgen05 instruction descriptor, kind::tf32: FP32 accumulator, TF32 A and B,
+// both K-major, N = 128, M = 128.
+constexpr uint32_t kIdesc = (1u << 4)                 // D format: F32
+                          | (2u << 7)                 // A format: TF32
+                          | (2u << 10)                // B format: TF32
+                          | ((uint32_t)(BN >> 3) << 17)
+                          | ((uint32_t)(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major tile with the 128-byte swizzle:
+// rows of 128 bytes (32 TF32 values of K), 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t smem_byte_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_byte_addr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)(16u >> 4) << 16;                    // leading byte offset (unused: K fits one atom)
+  d |= (uint64_t)(1024u >> 4) << 32;                  // stride byte offset: next 8 rows
+  d |= (uint64_t)1 << 46;                             // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                             // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on `bar` once every tcgen05.mma this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// x rounded to TF32 (10 explicit mantissa bits), to nearest with ties away
+// from zero: add half of the dropped range to the magnitude bits, then clear
+// them (a carry into the exponent is the correct rounding).
+__device__ __forceinline__ float tf32_round(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
+
+__device__ __forceinline__ void split4(const float4 x, float4& hi, float4& lo) {
+  hi = make_float4(tf32_round(x.x), tf32_round(x.y), tf32_round(x.z), tf32_round(x.w));
+  lo = make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
+}
+
+__device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, int& tm, int& tn) {
+  constexpr int kGroupM = 8;
+  const int span = kGroupM * tiles_n;
+  const int group = bid / span;
+  const int first = group * kGroupM;
+  const int rows = min(tiles_m - first, kGroupM);
+  const int local = bid - group * span;
+  tm = first + local % rows;
+  tn = local / rows;
+}
+
+// NN only: op(A) = A (K contiguous, loaded swizzled), op(B) = B (N contiguous).
+__global__ void __launch_bounds__(kThreads, 1)
+    tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                       const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t raw_full[kRawStages], raw_empty[kRawStages];
+  __shared__ __align__(8) uint64_t split_full[kSplitStages], split_empty[kSplitStages];
+  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
+  __shared__ uint32_t tmem_slot;
+
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_addr + pad;
+  // [raw stages][split stages], every tile 1024-byte aligned
+  auto raw_a = [&](int r) { return sbase + (uint32_t)(r * kRawBytes); };
+  auto raw_b = [&](int r) { return sbase + (uint32_t)(r * kRawBytes + kTileBytes); };
+  auto split_tile = [&](int s, int which) {  // 0 A_hi, 1 A_lo, 2 B_hi, 3 B_lo
+    return sbase + (uint32_t)(kRawStages * kRawBytes + s * kSplitBytes + which * kTileBytes);
+  };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int tm, tn;
+  tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
+  const int m0 = tm * BM, n0 = tn * BN;
+  const int nkt = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int r = 0; r < kRawStages; ++r) {
+      mbar_init(smem_addr(&raw_full[r]), 1);
+      mbar_init(smem_addr(&raw_empty[r]), kSplitters);
+    }
+    for (int s = 0; s < kSplitStages; ++s) {
+      mbar_init(smem_addr(&split_full[s]), kSplitters);
+      mbar_init(smem_addr(&split_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&acc_full[b]), 1);
+      mbar_init(smem_addr(&acc_empty[b]), kSplitters);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_addr(&tmem_slot), kTmemCols);
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&mapA);
+      prefetch_tensormap(&mapB);
+      int issued = 0;
+      for (int t = 0; t < nkt; ++t) {
+        const int r = t % kRawStages;
+        if (t >= kRawStages &&
+            !mbar_wait(smem_addr(&raw_empty[r]), (uint32_t)((t / kRawStages) - 1) & 1u, p.timeout_ns)) {
+          atomicOr(p.fault, (unsigned)kFaultEmptyWait);
+          break;
+        }
+        const uint32_t fb = smem_addr(&raw_full[r]);
+        mbar_arrive_expect_tx(fb, (uint32_t)kRawBytes);
+        tma_load_2d(raw_a(r), &mapA, fb, t * BK, m0);   // A: [128 rows of M][32 k], swizzled
+        tma_load_2d(raw_b(r), &mapB, fb, n0, t * BK);   // B: [32 k][128 n]
+        issued = t + 1;
+      }
+      // leave only when every copy into shared memory has landed
+      for (int t = issued > kRawStages ? issued - kRawStages : 0; t < issued; ++t)
+        if (!mbar_wait(smem_addr(&raw_full[t % kRawStages]), (uint32_t)(t / kRawStages) & 1u, p.timeout_ns))
+          atomicOr(p.fault, (unsigned)kFaultDrainWait);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int done = 0;  // K tiles whose MMAs were issued
+      for (int t = 0; t < nkt; ++t) {
+        const int s = t % kSplitStages, b = t & 1;
+        bool w = mbar_wait(smem_addr(&split_full[s]), (uint32_t)(t / kSplitStages) & 1u, p.timeout_ns);
+        if (w && t >= 2) w = mbar_wait(smem_addr(&acc_empty[b]), (uint32_t)((t >> 1) - 1) & 1u, p.timeout_ns);
+        if (!w) {
+          atomicOr(p.fault, (unsigned)kFaultFullWait);
+          break;
+        }
+        tmem_fence_after_sync();
+        const uint32_t acc = tmem + (uint32_t)b * kAccCols;
+        const uint64_t ahi = kmajor_sw128_desc(split_tile(s, 0)), alo = kmajor_sw128_desc(split_tile(s, 1));
+        const uint64_t bhi = kmajor_sw128_desc(split_tile(s, 2)), blo = kmajor_sw128_desc(split_tile(s, 3));
+#pragma unroll
+        for (int ks = 0; ks < BK / 8; ++ks) {
+          const uint64_t step = (uint64_t)(ks * 32) >> 4;  // 8 TF32 = 32 bytes along K
+          mma_tf32(acc, alo + step, bhi + step, ks > 0 ? 1u : 0u);  // fresh accumulator per K tile
+          mma_tf32(acc, ahi + step, blo + step, 1u);
+          mma_tf32(acc, ahi + step, bhi + step, 1u);
+        }
+        mma_commit(smem_addr(&split_empty[s]));  // split stage reusable once these MMAs have read it
+        mma_commit(smem_addr(&acc_full[b]));     // accumulator b holds K tile t
+        done = t + 1;
+      }
+      // leave only when no MMA is in flight: the last commit of each buffer has landed
+      for (int t = done > 2 ? done - 2 : 0; t < done; ++t)
+        if (!mbar_wait(smem_addr(&acc_full[t & 1]), (uint32_t)(t >> 1) & 1u, p.timeout_ns))
+          atomicOr(p.fault, (unsigned)kFaultDrainWait);
+    }
+  } else {
+    // ------------------------------------------------ splitters / folders, then epilogue
+    const int st = threadIdx.x - 64;                 // 0..255
+    const int q = warp & 3;                          // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;                // which 64 accumulator columns
+    const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * half);
+    float master[64];
+#pragma unroll
+    for (int e = 0; e < 64; ++e) master[e] = 0.0f;
+
+    // fold accumulator of K tile u into master (round-to-nearest FP32 adds)
+    auto fold = [&](int u) -> bool {
+      const int b = u & 1;
+      bool w = __all_sync(0xffffffffu, mbar_wait(smem_addr(&acc_full[b]), (uint32_t)(u >> 1) & 1u, p.timeout_ns));
+      if (!w) return false;
+      tmem_fence_after_sync();
+      float v[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld16(tq + (uint32_t)b * kAccCols + 16u * c, v[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld_ready(v[c]);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) master[16 * c + e] += v[c][e];
+      }
+      tmem_fence_before_sync();
+      mbar_arrive(smem_addr(&acc_empty[b]));
+      return true;
+    };
+
+    bool ok = true;
+    for (int t = 0; t < nkt; ++t) {
+      const int r = t % kRawStages, s = t % kSplitStages;
+      bool w = mbar_wait(smem_addr(&raw_full[r]), (uint32_t)(t / kRawStages) & 1u, p.timeout_ns);
+      if (w && t >= kSplitStages)
+        w = mbar_wait(smem_addr(&split_empty[s]), (uint32_t)((t / kSplitStages) - 1) & 1u, p.timeout_ns);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) {
+        if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
+        break;
+      }
+      // A: same swizzled K-major layout in and out -> elementwise on 16-byte chunks.
+      const uint8_t* ra = smem + (raw_a(r) - sbase);
+      uint8_t* ahi = smem + (split_tile(s, 0) - sbase);
+      uint8_t* alo = smem + (split_tile(s, 1) - sbase);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t off = (uint32_t)(st + kSplitters * j) * 16u;
+        float4 hi, lo;
+        split4(*reinterpret_cast<const float4*>(ra + off), hi, lo);
+        *reinterpret_cast<float4*>(ahi + off) = hi;
+        *reinterpret_cast<float4*>(alo + off) = lo;
+      }
+      // B: raw [32 k][128 n] -> K-major [128 n][32 k], 128-byte swizzle;
+      // thread st owns column n = st % 128 and k chunks 4*(st/128) .. +3.
+      const float* rb = reinterpret_cast<const float*>(smem + (raw_b(r) - sbase));
+      uint8_t* bhi = smem + (split_tile(s, 2) - sbase);
+      uint8_t* blo = smem + (split_tile(s, 3) - sbase);
+      const int n = st & 127, kh = st >> 7;
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        const int kc = 4 * kh + kq;
+        const float4 x = make_float4(rb[(4 * kc + 0) * BN + n], rb[(4 * kc + 1) * BN + n],
+                                     rb[(4 * kc + 2) * BN + n], rb[(4 * kc + 3) * BN + n]);
+        float4 hi, lo;
+        split4(x, hi, lo);
+        const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(kc ^ (n & 7)) << 4);
+        *reinterpret_cast<float4*>(bhi + off) = hi;
+        *reinterpret_cast<float4*>(blo + off) = lo;
+      }
+      fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+      mbar_arrive(smem_addr(&split_full[s]));
+      mbar_arrive(smem_addr(&raw_empty[r]));
+      if (t >= 1 && !fold(t - 1)) {
+        ok = false;
+        if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
+        break;
+      }
+    }
+    if (ok && nkt >= 1 && !fold(nkt - 1)) {
+      ok = false;
+      if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
+    }
+    if (ok) {
+      // epilogue: this thread holds row 32q + lane, columns 64*half .. +63 of the tile
+      const int row = m0 + 32 * q + lane;
+      if (row < p.M) {
+        float* crow = p.C + (int64_t)row * p.ldc;
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {
+          const int col = n0 + 64 * half + 4 * g;
+          const float* x = &master[4 * g];
+          if (p.c_vec && col + 3 < p.N) {
+            float4 o;
+            if (p.beta == 0.0f) {
+              o = make_float4(p.alpha * x[0], p.alpha * x[1], p.alpha * x[2], p.alpha * x[3]);
+            } else {
+              const float4 old = *reinterpret_cast<const float4*>(crow + col);
+              o = make_float4(fmaf(p.alpha, x[0], p.beta * old.x), fmaf(p.alpha, x[1], p.beta * old.y),
+                              fmaf(p.alpha, x[2], p.beta * old.z), fmaf(p.alpha, x[3], p.beta * old.w));
+            }
+            *reinterpret_cast<float4*>(crow + col) = o;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (col + e < p.N)
+                crow[col + e] = p.beta == 0.0f ? p.alpha * x[e] : fmaf(p.alpha, x[e], p.beta * crow[col + e]);
+          }
+        }
+      }
+    }
+  }
+
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace tc
+
+cudaError_t prepare_tf32x3() {
+  return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
+}
+
+cudaError_t launch_tf32x3_nn(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
+                             cudaStream_t stream) {
+  tc::tf32x3_gemm_kernel<<<(unsigned)(p.tiles_m * p.tiles_n), tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB,
+                                                                                                       p);
+  return cudaGetLastError();
+}
+
+}  // namespace sgemm_impl
