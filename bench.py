@@ -38,7 +38,11 @@ import sgemm_inputs as si  # noqa: E402
 METRIC = "SGEMM TFLOPS (2MNK/t) at 4096^3 NN on 1 GB300; % of FP32 FFMA peak"
 UNIT = "TFLOPS"
 FMA_PER_SM_PER_CLK = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "tma_gemm_square4096.md")
+PROFILES = {"TC_TF32X3": os.path.join(ROOT, "profiles", "tf32x3_gemm_square4096.md"),
+            "TMA_128x128": os.path.join(ROOT, "profiles", "tma_gemm_square4096.md")}
+# dense tensor-core peaks (PFLOP/s, nominal) used to scale the measured bf16 peak to tf32
+NOMINAL_BF16_PF, NOMINAL_TF32_PF = 2.25, 1.1
+TF32_PRODUCTS = 3  # tensor-core products per useful FMA in the 3xTF32 split
 
 
 def parse_args():
@@ -129,11 +133,11 @@ def gpu_selector(device_index: int) -> str:
 
 # ---------------------------------------------------------------- helpers
 
-def traffic_from_profile(digest: str):
+def traffic_from_profile(variant: str, digest: str):
     """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, if it is current."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
+        text = open(PROFILES[variant]).read()
+    except (OSError, KeyError):
         return None
     d = re.search(r"kernel_digest:\s*([0-9a-f]+)", text)
     t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
@@ -387,16 +391,29 @@ def run_ours(args):
     clocks = sampler.summary(t0_wall, t1_wall)
     peaks = measured_peaks()
     max_mhz = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
-    peak = sms * FMA_PER_SM_PER_CLK * 2 * max_mhz * 1e6 / 1e12
-    roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": traffic_from_profile(lib_build.tma_kernel_digest()),
-            "peak_basis": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz max SM clock",
-            "kernel": {"TMA_128x128": "tma_gemm_kernel (SIMT FFMA2)", "TMA_64x256": "tma_gemm_kernel (SIMT FFMA2)",
-                       "TC_TF32X3": "tf32x3_gemm_kernel (tcgen05, 3xTF32)"}.get(plan["variant_name"],
-                                                                                plan["variant_name"]),
-            "kernel_ms": kernel_ms}
-    if clocks.get("sm_mhz"):
-        roof["frac_at_sampled_clock"] = achieved / (sms * FMA_PER_SM_PER_CLK * 2 * clocks["sm_mhz"] * 1e6 / 1e12)
+    ffma_peak = sms * FMA_PER_SM_PER_CLK * 2 * max_mhz * 1e6 / 1e12
+    variant = plan["variant_name"]
+    if variant == "TC_TF32X3":
+        bf16 = peaks.get("bf16_tflops")
+        basis = "measured" if bf16 else "fallback"
+        bf16 = bf16 or 1900.0
+        tf32 = bf16 * NOMINAL_TF32_PF / NOMINAL_BF16_PF
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf32 / TF32_PRODUCTS, "unit": "TFLOP/s",
+                "frac": achieved / (tf32 / TF32_PRODUCTS),
+                "traffic": traffic_from_profile(variant, lib_build.tc_kernel_digest()),
+                "peak_basis": f"{basis} bf16 burst {bf16:.0f} TFLOP/s x nominal tf32/bf16 "
+                              f"{NOMINAL_TF32_PF}/{NOMINAL_BF16_PF} = {tf32:.0f} TFLOP/s of tf32, / {TF32_PRODUCTS} "
+                              f"tensor products per SGEMM FMA (3xTF32 split); achieved counts 2MNK only",
+                "kernel": "tf32x3_gemm_kernel (tcgen05.mma kind::tf32, 3xTF32 split)", "kernel_ms": kernel_ms}
+    else:
+        roof = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
+                "frac": achieved / ffma_peak,
+                "traffic": traffic_from_profile(variant, lib_build.tma_kernel_digest()),
+                "peak_basis": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz max SM clock",
+                "kernel": "tma_gemm_kernel (SIMT FFMA2)" if variant.startswith("TMA") else variant,
+                "kernel_ms": kernel_ms}
+        if clocks.get("sm_mhz"):
+            roof["frac_at_sampled_clock"] = achieved / (sms * FMA_PER_SM_PER_CLK * 2 * clocks["sm_mhz"] * 1e6 / 1e12)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -405,7 +422,9 @@ def run_ours(args):
         "config": {**config_block(case, world), "prewarm_s": args.prewarm_s,
                    "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "tile_k", "stages",
                                                  "split_k", "grid_x", "grid_y")}},
-        "pct_ffma_peak": 100.0 * achieved / peak,
+        "pct_ffma_peak": 100.0 * achieved / ffma_peak,
+        "ffma_peak": {"value": ffma_peak, "unit": "TFLOP/s",
+                      "basis": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz"},
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": plan["kernel_launches"] * args.steps,

@@ -31,6 +31,16 @@
  *   - Unaligned pointers or leading dimensions are NOT errors; they take a
  *     slower path.  C overlapping A or B is undefined.
  *
+ * Arithmetic: the default kernel (16-byte aligned A and B, lda % 4 == 0,
+ * ldb % 4 == 0) runs on the tensor cores with each float split into two
+ * TF32 parts (3 products per term, partial sums folded in FP32 every 32 k);
+ * results meet |C - C_exact| <= (K+2) 2^-24 (|alpha| sum|a b| + |beta c|) and
+ * are deterministic, but are not the IEEE FP32 FMA sums of a SIMT loop, and
+ * an Inf in A or B may give NaN where IEEE arithmetic gives Inf (a NaN input
+ * gives NaN on every path).  The FP32 FFMA kernels (IEEE operations, exact Inf
+ * handling) are selected with sgemm_set_variant_override(SGEMM_VARIANT_TMA_128x128
+ * or SGEMM_VARIANT_TMA_64x256, 0); unaligned operands always use the FFMA path.
+ *
  * Errors: invalid arguments return -(argument index) (1 = transA ... 14 =
  * stream) before anything is launched, and C is untouched.  CUDA launch or
  * allocation failures return SGEMM_ERR_CUDA / SGEMM_ERR_NOMEM (the CUDA
@@ -70,7 +80,7 @@ enum sgemm_variant {
     SGEMM_VARIANT_GENERIC = 3,    /* any alignment: 64x64 tiles, predicated loads */
     SGEMM_VARIANT_TMA_128x128 = 4,/* TMA-fed SIMT FFMA, 128x128x32 tiles, 4-stage mbarrier ring */
     SGEMM_VARIANT_TMA_64x256 = 5, /* same kernel, 64x256 tiles for short M */
-    SGEMM_VARIANT_TC_TF32X3 = 6   /* tcgen05 tensor cores, 3xTF32 split, 128x128x32 tiles (NN) */
+    SGEMM_VARIANT_TC_TF32X3 = 6   /* tcgen05 tensor cores, 3xTF32 split, 128x128x32 tiles */
 };
 
 /*

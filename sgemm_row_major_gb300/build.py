@@ -58,10 +58,22 @@ TMA_KERNEL_FILES = ["kernel_tma.cuh", "device_utils.cuh", "sgemm_internal.h", "k
                     "kernel_tma_nt.cu", "kernel_tma_tn.cu", "kernel_tma_tt.cu"]
 
 
+TC_KERNEL_FILES = ["kernel_tf32x3.cu", "device_utils.cuh", "sgemm_internal.h"]
+
+
 def tma_kernel_digest() -> str:
-    """Hash of the sources of the TMA-fed GEMM kernel only (identifies the profiled kernel build)."""
+    """Hash of the sources of the TMA-fed FFMA kernel only (identifies the profiled kernel build)."""
+    return _digest(TMA_KERNEL_FILES)
+
+
+def tc_kernel_digest() -> str:
+    """Hash of the sources of the 3xTF32 tensor-core kernel only."""
+    return _digest(TC_KERNEL_FILES)
+
+
+def _digest(files) -> str:
     h = hashlib.sha256()
-    for name in TMA_KERNEL_FILES:
+    for name in files:
         h.update(name.encode())
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(f.read())

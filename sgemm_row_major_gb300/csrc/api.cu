@@ -181,14 +181,14 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   }
   // TMA needs 16-byte aligned bases and row strides that are multiples of 16 bytes.
   const bool tma_ok = aligned16(pr.A) && aligned16(pr.B) && pr.lda % 4 == 0 && pr.ldb % 4 == 0;
-  int variant = tma_ok ? (pr.M <= 64 ? SGEMM_VARIANT_TMA_64x256 : SGEMM_VARIANT_TMA_128x128)
-                       : SGEMM_VARIANT_GENERIC;
+  // Default: the 3xTF32 tensor-core kernel whenever TMA can load the operands
+  // (it beats the FP32 FFMA kernels on every measured shape); the generic
+  // SIMT kernel otherwise.  The FFMA kernels stay selectable by override.
+  int variant = tma_ok ? SGEMM_VARIANT_TC_TF32X3 : SGEMM_VARIANT_GENERIC;
   const int ov = g_override_variant.load();
-  if (ov == SGEMM_VARIANT_GENERIC || ov == SGEMM_VARIANT_TMA_128x128 || ov == SGEMM_VARIANT_TMA_64x256)
+  if (ov == SGEMM_VARIANT_GENERIC || ov == SGEMM_VARIANT_TMA_128x128 || ov == SGEMM_VARIANT_TMA_64x256 ||
+      ov == SGEMM_VARIANT_TC_TF32X3)
     variant = (ov == SGEMM_VARIANT_GENERIC || tma_ok) ? ov : SGEMM_VARIANT_GENERIC;
-  // The tensor-core kernel handles op = NN on TMA-compatible operands, without a K split.
-  const bool tc_ok = tma_ok && !pr.ta && !pr.tb;
-  if (ov == SGEMM_VARIANT_TC_TF32X3) variant = tc_ok ? ov : variant;
 
   int bm, bn, bk, threads, stages;
   int64_t smem = 0;
@@ -196,7 +196,7 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
     const GenericTileShape g = generic_tile_shape();
     bm = g.bm; bn = g.bn; bk = g.bk; threads = g.threads; stages = 2;
   } else if (variant == SGEMM_VARIANT_TC_TF32X3) {
-    bm = 128; bn = 128; bk = 32; threads = 320; stages = 3; smem = 3 * 32768 + 2 * 65536 + 1024;
+    bm = 128; bn = 128; bk = 32; threads = 608; stages = 4; smem = 4 * 32768 + 2 * 32768 + 1024;
   } else if (variant == SGEMM_VARIANT_TMA_128x128) {
     using T = tma::Tile<4, 2>;
     bm = T::BM; bn = T::BN; bk = tma::kBK; threads = tma::kThreads; stages = tma::kStages; smem = T::SMEM_BYTES;
@@ -215,7 +215,6 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   const int ov_split = g_override_split.load();
   if (ov_split > 0) split = ov_split;
   split = std::max<int64_t>(1, std::min<int64_t>({split, kt, 256}));
-  if (variant == SGEMM_VARIANT_TC_TF32X3) split = 1;
   const int64_t per = ceil_div(kt, split);
   split = ceil_div(kt, per);  // no empty slice
 
@@ -291,7 +290,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   if (plan.variant == SGEMM_VARIANT_GENERIC) {
     e = launch_generic_gemm(pr.ta, pr.tb, p, split, stream);
   } else if (plan.variant == SGEMM_VARIANT_TC_TF32X3) {
-    e = launch_tf32x3_nn(mapA, mapB, p, stream);
+    e = launch_tf32x3(pr.ta, pr.tb, mapA, mapB, p, split, stream);
   } else {
     const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
     if (!pr.ta && !pr.tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, stream);

@@ -21,20 +21,34 @@
 // FP32 registers with round-to-nearest adds; the error then no longer grows
 // with K (~2e-7 relative).
 //
-// CTA (one 128x128 output tile, 10 warps):
+// Shared-memory bandwidth is the limit of this design (TMA writes, split
+// reads and writes and the tensor core's operand reads all use the same
+// shared-memory data path), so the A operand's hi/lo parts go to tensor
+// memory instead (tcgen05.mma reads A from TMEM, B from shared memory).
+//
+// CTA (one 128x128 output tile or, with a K split, one K slice of it; 19 warps):
 //   warp 0     TMA producer: FP32 tiles of op(A) and op(B) (as stored) into a
-//              3-stage "raw" ring (32 KB per stage).
-//   warp 1     MMA issuer (one thread): per 32-k tile, 4 k-steps x 3
-//              tcgen05.mma (M=128, N=128, K=8) into one of two 128x128 FP32
-//              accumulators in TMEM; tcgen05.commit releases the split stage
-//              and hands the accumulator to the folders.
-//   warps 2-9  split raw stage t -> hi/lo tiles in the K-major, 128-byte
-//              swizzled layout the tensor core reads (A keeps its layout; B,
-//              N-contiguous in memory, is transposed on the way) in a 2-stage
-//              "split" ring (64 KB per stage); fold accumulator t-1 into
-//              registers (each thread: 64 columns of one row); finally the
+//              4-stage "raw" ring (32 KB per stage).
+//   warps 1,18 MMA issuers (one thread each; warp 1 takes even K tiles into
+//              accumulator 0, warp 18 odd K tiles into accumulator 1): per
+//              32-k tile, 4 k-steps x 3 tcgen05.mma (M=128, N=128, K=8);
+//              tcgen05.commit releases the split stage and hands the
+//              accumulator to the folders.  Issuing one tcgen05.mma takes a
+//              thread ~100 cycles on GB300, more than the 64 cycles the tensor
+//              core needs for it, so one issuer alone starves the tensor core.
+//   warps 2-9  splitters: raw stage t -> A hi/lo in TMEM (row m in lane m, k
+//              in columns) and B hi/lo tiles in the K-major, 128-byte swizzled
+//              shared-memory layout the tensor core reads (transposed on the
+//              way when B is N-contiguous in memory), 2 split stages.
+//   warps 10-17 folders: add accumulator t into FP32 registers (each thread:
+//              64 columns of one row) as soon as its MMAs complete, then the
 //              alpha/beta epilogue.
-// Every wait is bounded (mbarrier phases).
+// Only lane 0 of a warp polls a barrier (the others then confirm the
+// completed phase once) and arrives on it, which keeps barrier traffic off
+// the shared-memory path.  Every wait is bounded (mbarrier phases).
+//
+// TMEM columns: [0,128) and [128,256) accumulators; [256 + 64 s, +32) A hi
+// and [288 + 64 s, +32) A lo of split stage s (s < 2).
 #include "device_utils.cuh"
 #include "sgemm_internal.h"
 
@@ -42,15 +56,21 @@ namespace sgemm_impl {
 namespace tc {
 
 constexpr int BM = 128, BN = 128, BK = 32;
-constexpr int kRawStages = 3, kSplitStages = 2;
+constexpr int kRawStages = 4, kSplitStages = 2;
 constexpr int kTileBytes = 128 * BK * 4;            // one 128 x 32 operand tile, 16 KB
 constexpr int kRawBytes = 2 * kTileBytes;           // A + B as loaded
-constexpr int kSplitBytes = 4 * kTileBytes;         // A_hi, A_lo, B_hi, B_lo
+constexpr int kSplitBytes = 2 * kTileBytes;         // B_hi, B_lo (A's parts live in TMEM)
 constexpr int kSmemBytes = kRawStages * kRawBytes + kSplitStages * kSplitBytes + 1024;
-constexpr int kThreads = 320;
-constexpr int kSplitters = 256;                     // warps 2-9
+constexpr int kSplitWarps = 8;                      // warps 2-9
+constexpr int kSplitters = 32 * kSplitWarps;
+constexpr int kFoldWarps = 8;                       // warps 10-17
+constexpr int kFirstFoldWarp = 2 + kSplitWarps;
+constexpr int kSecondMmaWarp = kFirstFoldWarp + kFoldWarps;  // warp 18
+constexpr int kThreads = 32 * (3 + kSplitWarps + kFoldWarps);
 constexpr uint32_t kAccCols = 128;                  // one 128 x 128 FP32 accumulator
-constexpr uint32_t kTmemCols = 2 * kAccCols;        // double-buffered
+constexpr uint32_t kACols = 64;                     // A hi (32 k) + A lo (32 k) of one split stage
+constexpr uint32_t kAColBase = 2 * kAccCols;
+constexpr uint32_t kTmemCols = 512;                 // 2 accumulators + 2 A stages (384 used)
 
 // tcgen05 instruction descriptor, kind::tf32: FP32 accumulator, TF32 A and B,
 // both K-major, N = 128, M = 128.
@@ -72,13 +92,25 @@ __device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t smem_byte_addr) {
   return d;
 }
 
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+// D (TMEM) = or += A (TMEM, 128 lanes x 8 columns) * B (shared memory, descriptor)
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
       : "memory");
+}
+
+// Warp-level bounded wait: lane 0 polls, then every lane confirms the phase
+// (an immediate success) so each thread has its own acquire.  Warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  const int lane = threadIdx.x & 31;
+  bool ok = true;
+  if (lane == 0) ok = mbar_wait(bar, parity, timeout_ns);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  if (ok) ok = mbar_wait(bar, parity, timeout_ns);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // Arrives on `bar` once every tcgen05.mma this thread issued so far has completed.
@@ -110,7 +142,11 @@ __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, i
   tn = local / rows;
 }
 
-// NN only: op(A) = A (K contiguous, loaded swizzled), op(B) = B (N contiguous).
+// Raw tile layouts (as the TMA engine copies them):
+//   op(A) 'N': [128 rows of M][32 k], K contiguous, 128-byte swizzle;  'T': [32 k][128 m], M contiguous.
+//   op(B) 'N': [32 k][128 n], N contiguous;  'T': [128 n][32 k], K contiguous, 128-byte swizzle.
+// SPLIT: write the raw sums of this CTA's K slice (blockIdx.y) to the workspace instead of C.
+template <bool TA, bool TB, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                        const GemmParams p) {
@@ -127,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // [raw stages][split stages], every tile 1024-byte aligned
   auto raw_a = [&](int r) { return sbase + (uint32_t)(r * kRawBytes); };
   auto raw_b = [&](int r) { return sbase + (uint32_t)(r * kRawBytes + kTileBytes); };
-  auto split_tile = [&](int s, int which) {  // 0 A_hi, 1 A_lo, 2 B_hi, 3 B_lo
+  auto split_tile = [&](int s, int which) {  // 0 B_hi, 1 B_lo
     return sbase + (uint32_t)(kRawStages * kRawBytes + s * kSplitBytes + which * kTileBytes);
   };
 
@@ -136,20 +172,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   int tm, tn;
   tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
   const int m0 = tm * BM, n0 = tn * BN;
-  const int nkt = (p.K + BK - 1) / BK;
+  const int kt_total = (p.K + BK - 1) / BK;
+  const int kt0 = blockIdx.y * p.k_tiles_per_split;
+  const int nkt = min(kt_total, kt0 + p.k_tiles_per_split) - kt0;  // >= 1 by construction
 
   if (threadIdx.x == 0) {
     for (int r = 0; r < kRawStages; ++r) {
       mbar_init(smem_addr(&raw_full[r]), 1);
-      mbar_init(smem_addr(&raw_empty[r]), kSplitters);
+      mbar_init(smem_addr(&raw_empty[r]), kSplitWarps);
     }
     for (int s = 0; s < kSplitStages; ++s) {
-      mbar_init(smem_addr(&split_full[s]), kSplitters);
+      mbar_init(smem_addr(&split_full[s]), kSplitWarps);
       mbar_init(smem_addr(&split_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&acc_full[b]), 1);
-      mbar_init(smem_addr(&acc_empty[b]), kSplitters);
+      mbar_init(smem_addr(&acc_empty[b]), kFoldWarps);
     }
     fence_mbar_init();
   }
@@ -174,8 +212,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t fb = smem_addr(&raw_full[r]);
         mbar_arrive_expect_tx(fb, (uint32_t)kRawBytes);
-        tma_load_2d(raw_a(r), &mapA, fb, t * BK, m0);   // A: [128 rows of M][32 k], swizzled
-        tma_load_2d(raw_b(r), &mapB, fb, n0, t * BK);   // B: [32 k][128 n]
+        const int k0 = (kt0 + t) * BK;
+        if (!TA) tma_load_2d(raw_a(r), &mapA, fb, k0, m0);
+        else     tma_load_2d(raw_a(r), &mapA, fb, m0, k0);
+        if (!TB) tma_load_2d(raw_b(r), &mapB, fb, n0, k0);
+        else     tma_load_2d(raw_b(r), &mapB, fb, k0, n0);
         issued = t + 1;
       }
       // leave only when every copy into shared memory has landed
@@ -183,12 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(smem_addr(&raw_full[t % kRawStages]), (uint32_t)(t / kRawStages) & 1u, p.timeout_ns))
           atomicOr(p.fault, (unsigned)kFaultDrainWait);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kSecondMmaWarp) {
+    // ------------------------------------------------ MMA issuers (K tiles t with t & 1 == b)
     if (lane == 0) {
-      int done = 0;  // K tiles whose MMAs were issued
-      for (int t = 0; t < nkt; ++t) {
-        const int s = t % kSplitStages, b = t & 1;
+      const int b = warp == 1 ? 0 : 1;
+      int done = -1;  // last K tile whose MMAs this thread issued
+      for (int t = b; t < nkt; t += 2) {
+        const int s = t % kSplitStages;
         bool w = mbar_wait(smem_addr(&split_full[s]), (uint32_t)(t / kSplitStages) & 1u, p.timeout_ns);
         if (w && t >= 2) w = mbar_wait(smem_addr(&acc_empty[b]), (uint32_t)((t >> 1) - 1) & 1u, p.timeout_ns);
         if (!w) {
@@ -197,39 +239,126 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_fence_after_sync();
         const uint32_t acc = tmem + (uint32_t)b * kAccCols;
-        const uint64_t ahi = kmajor_sw128_desc(split_tile(s, 0)), alo = kmajor_sw128_desc(split_tile(s, 1));
-        const uint64_t bhi = kmajor_sw128_desc(split_tile(s, 2)), blo = kmajor_sw128_desc(split_tile(s, 3));
+        const uint32_t ahi = tmem + kAColBase + (uint32_t)s * kACols, alo = ahi + 32u;
+        const uint64_t bhi = kmajor_sw128_desc(split_tile(s, 0)), blo = kmajor_sw128_desc(split_tile(s, 1));
 #pragma unroll
         for (int ks = 0; ks < BK / 8; ++ks) {
           const uint64_t step = (uint64_t)(ks * 32) >> 4;  // 8 TF32 = 32 bytes along K
-          mma_tf32(acc, alo + step, bhi + step, ks > 0 ? 1u : 0u);  // fresh accumulator per K tile
-          mma_tf32(acc, ahi + step, blo + step, 1u);
-          mma_tf32(acc, ahi + step, bhi + step, 1u);
+          const uint32_t acol = (uint32_t)(8 * ks);        // 8 TF32 = 8 TMEM columns
+          mma_tf32_ts(acc, alo + acol, bhi + step, ks > 0 ? 1u : 0u);  // fresh accumulator per K tile
+          mma_tf32_ts(acc, ahi + acol, blo + step, 1u);
+          mma_tf32_ts(acc, ahi + acol, bhi + step, 1u);
         }
         mma_commit(smem_addr(&split_empty[s]));  // split stage reusable once these MMAs have read it
         mma_commit(smem_addr(&acc_full[b]));     // accumulator b holds K tile t
-        done = t + 1;
+        done = t;
       }
-      // leave only when no MMA is in flight: the last commit of each buffer has landed
-      for (int t = done > 2 ? done - 2 : 0; t < done; ++t)
-        if (!mbar_wait(smem_addr(&acc_full[t & 1]), (uint32_t)(t >> 1) & 1u, p.timeout_ns))
-          atomicOr(p.fault, (unsigned)kFaultDrainWait);
+      // leave only when none of this thread's MMAs is in flight
+      if (done >= 0 && !mbar_wait(smem_addr(&acc_full[b]), (uint32_t)(done >> 1) & 1u, p.timeout_ns))
+        atomicOr(p.fault, (unsigned)kFaultDrainWait);
     }
-  } else {
-    // ------------------------------------------------ splitters / folders, then epilogue
+  } else if (warp < kFirstFoldWarp) {
+    // ------------------------------------------------ splitters
     const int st = threadIdx.x - 64;                 // 0..255
     const int q = warp & 3;                          // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;                // which 64 accumulator columns
+    const int half = (warp - 2) >> 2;                // which 16 k of A
+    for (int t = 0; t < nkt; ++t) {
+      const int r = t % kRawStages, s = t % kSplitStages;
+      bool w = warp_wait(smem_addr(&raw_full[r]), (uint32_t)(t / kRawStages) & 1u, p.timeout_ns);
+      if (w && t >= kSplitStages)
+        w = warp_wait(smem_addr(&split_empty[s]), (uint32_t)((t / kSplitStages) - 1) & 1u, p.timeout_ns);
+      if (!w) {
+        if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
+        break;
+      }
+      tmem_fence_after_sync();
+      // A: this thread takes row m = 32q + lane (its TMEM lane) and k = 16*half .. +15.
+      {
+        const uint8_t* ra = smem + (raw_a(r) - sbase);
+        const int m = 32 * q + lane;
+        float hi[16], lo[16];
+        if (!TA) {
+          // K-contiguous rows, 128-byte swizzle: chunk c of row m sits at c ^ (m & 7)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = 4 * half + j;
+            const float4 x = *reinterpret_cast<const float4*>(ra + m * 128 + ((c ^ (m & 7)) << 4));
+            float4 h, l;
+            split4(x, h, l);
+            hi[4 * j + 0] = h.x; hi[4 * j + 1] = h.y; hi[4 * j + 2] = h.z; hi[4 * j + 3] = h.w;
+            lo[4 * j + 0] = l.x; lo[4 * j + 1] = l.y; lo[4 * j + 2] = l.z; lo[4 * j + 3] = l.w;
+          }
+        } else {
+          // M-contiguous [32 k][128 m]: one float per k (a warp reads 32 adjacent m)
+          const float* fa = reinterpret_cast<const float*>(ra);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float x = fa[(16 * half + j) * BM + m];
+            hi[j] = tf32_round(x);
+            lo[j] = x - hi[j];
+          }
+        }
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kAColBase + (uint32_t)s * kACols + 16u * half;
+        tmem_st16(ta, hi);
+        tmem_st16(ta + 32u, lo);
+      }
+      // B -> K-major [128 n][32 k], 128-byte swizzle, the layout the descriptors describe.
+      {
+        uint8_t* bhi = smem + (split_tile(s, 0) - sbase);
+        uint8_t* blo = smem + (split_tile(s, 1) - sbase);
+        if (!TB) {
+          // raw [32 k][128 n]: transpose; thread st owns column n = st % 128, k chunks 4*(st/128) .. +3
+          const float* rb = reinterpret_cast<const float*>(smem + (raw_b(r) - sbase));
+          const int n = st & 127, kh = st >> 7;
+#pragma unroll
+          for (int kq = 0; kq < 4; ++kq) {
+            const int kc = 4 * kh + kq;
+            const float4 x = make_float4(rb[(4 * kc + 0) * BN + n], rb[(4 * kc + 1) * BN + n],
+                                         rb[(4 * kc + 2) * BN + n], rb[(4 * kc + 3) * BN + n]);
+            float4 hi, lo;
+            split4(x, hi, lo);
+            const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(kc ^ (n & 7)) << 4);
+            *reinterpret_cast<float4*>(bhi + off) = hi;
+            *reinterpret_cast<float4*>(blo + off) = lo;
+          }
+        } else {
+          // raw is already K-major and swizzled: split 16-byte chunks in place
+          const uint8_t* rb = smem + (raw_b(r) - sbase);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t off = (uint32_t)(st + kSplitters * j) * 16u;
+            float4 hi, lo;
+            split4(*reinterpret_cast<const float4*>(rb + off), hi, lo);
+            *reinterpret_cast<float4*>(bhi + off) = hi;
+            *reinterpret_cast<float4*>(blo + off) = lo;
+          }
+        }
+      }
+      tmem_wait_st();            // A parts have reached TMEM
+      fence_proxy_async_smem();  // B parts (generic-proxy writes) -> visible to the tensor core
+      tmem_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&split_full[s]));
+        mbar_arrive(smem_addr(&raw_empty[r]));
+      }
+    }
+  } else {
+    // ------------------------------------------------ folders, then epilogue
+    const int q = warp & 3;                          // TMEM lane quarter this warp may access
+    const int half = (warp - kFirstFoldWarp) >> 2;   // which 64 accumulator columns
     const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * half);
     float master[64];
 #pragma unroll
     for (int e = 0; e < 64; ++e) master[e] = 0.0f;
-
-    // fold accumulator of K tile u into master (round-to-nearest FP32 adds)
-    auto fold = [&](int u) -> bool {
+    bool ok = true;
+    for (int u = 0; u < nkt; ++u) {
       const int b = u & 1;
-      bool w = __all_sync(0xffffffffu, mbar_wait(smem_addr(&acc_full[b]), (uint32_t)(u >> 1) & 1u, p.timeout_ns));
-      if (!w) return false;
+      if (!warp_wait(smem_addr(&acc_full[b]), (uint32_t)(u >> 1) & 1u, p.timeout_ns)) {
+        ok = false;
+        if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
+        break;
+      }
       tmem_fence_after_sync();
       float v[4][16];
 #pragma unroll
@@ -239,90 +368,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c) {
         tmem_ld_ready(v[c]);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) master[16 * c + e] += v[c][e];
+        for (int e = 0; e < 16; ++e) master[16 * c + e] += v[c][e];  // round-to-nearest FP32 adds
       }
       tmem_fence_before_sync();
-      mbar_arrive(smem_addr(&acc_empty[b]));
-      return true;
-    };
-
-    bool ok = true;
-    for (int t = 0; t < nkt; ++t) {
-      const int r = t % kRawStages, s = t % kSplitStages;
-      bool w = mbar_wait(smem_addr(&raw_full[r]), (uint32_t)(t / kRawStages) & 1u, p.timeout_ns);
-      if (w && t >= kSplitStages)
-        w = mbar_wait(smem_addr(&split_empty[s]), (uint32_t)((t / kSplitStages) - 1) & 1u, p.timeout_ns);
-      ok = __all_sync(0xffffffffu, w);
-      if (!ok) {
-        if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
-        break;
-      }
-      // A: same swizzled K-major layout in and out -> elementwise on 16-byte chunks.
-      const uint8_t* ra = smem + (raw_a(r) - sbase);
-      uint8_t* ahi = smem + (split_tile(s, 0) - sbase);
-      uint8_t* alo = smem + (split_tile(s, 1) - sbase);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t off = (uint32_t)(st + kSplitters * j) * 16u;
-        float4 hi, lo;
-        split4(*reinterpret_cast<const float4*>(ra + off), hi, lo);
-        *reinterpret_cast<float4*>(ahi + off) = hi;
-        *reinterpret_cast<float4*>(alo + off) = lo;
-      }
-      // B: raw [32 k][128 n] -> K-major [128 n][32 k], 128-byte swizzle;
-      // thread st owns column n = st % 128 and k chunks 4*(st/128) .. +3.
-      const float* rb = reinterpret_cast<const float*>(smem + (raw_b(r) - sbase));
-      uint8_t* bhi = smem + (split_tile(s, 2) - sbase);
-      uint8_t* blo = smem + (split_tile(s, 3) - sbase);
-      const int n = st & 127, kh = st >> 7;
-#pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
-        const int kc = 4 * kh + kq;
-        const float4 x = make_float4(rb[(4 * kc + 0) * BN + n], rb[(4 * kc + 1) * BN + n],
-                                     rb[(4 * kc + 2) * BN + n], rb[(4 * kc + 3) * BN + n]);
-        float4 hi, lo;
-        split4(x, hi, lo);
-        const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(kc ^ (n & 7)) << 4);
-        *reinterpret_cast<float4*>(bhi + off) = hi;
-        *reinterpret_cast<float4*>(blo + off) = lo;
-      }
-      fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
-      mbar_arrive(smem_addr(&split_full[s]));
-      mbar_arrive(smem_addr(&raw_empty[r]));
-      if (t >= 1 && !fold(t - 1)) {
-        ok = false;
-        if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
-        break;
-      }
-    }
-    if (ok && nkt >= 1 && !fold(nkt - 1)) {
-      ok = false;
-      if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
     }
     if (ok) {
       // epilogue: this thread holds row 32q + lane, columns 64*half .. +63 of the tile
       const int row = m0 + 32 * q + lane;
       if (row < p.M) {
-        float* crow = p.C + (int64_t)row * p.ldc;
+        if (SPLIT) {
+          float* wrow = p.ws + ((int64_t)blockIdx.y * p.M + row) * p.ws_ld;
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
-          const int col = n0 + 64 * half + 4 * g;
-          const float* x = &master[4 * g];
-          if (p.c_vec && col + 3 < p.N) {
-            float4 o;
-            if (p.beta == 0.0f) {
-              o = make_float4(p.alpha * x[0], p.alpha * x[1], p.alpha * x[2], p.alpha * x[3]);
+          for (int g = 0; g < 16; ++g) {
+            const int col = n0 + 64 * half + 4 * g;
+            if (col < p.N)
+              *reinterpret_cast<float4*>(wrow + col) =
+                  make_float4(master[4 * g], master[4 * g + 1], master[4 * g + 2], master[4 * g + 3]);
+          }
+        } else {
+          float* crow = p.C + (int64_t)row * p.ldc;
+#pragma unroll
+          for (int g = 0; g < 16; ++g) {
+            const int col = n0 + 64 * half + 4 * g;
+            const float* x = &master[4 * g];
+            if (p.c_vec && col + 3 < p.N) {
+              float4 o;
+              if (p.beta == 0.0f) {
+                o = make_float4(p.alpha * x[0], p.alpha * x[1], p.alpha * x[2], p.alpha * x[3]);
+              } else {
+                const float4 old = *reinterpret_cast<const float4*>(crow + col);
+                o = make_float4(fmaf(p.alpha, x[0], p.beta * old.x), fmaf(p.alpha, x[1], p.beta * old.y),
+                                fmaf(p.alpha, x[2], p.beta * old.z), fmaf(p.alpha, x[3], p.beta * old.w));
+              }
+              *reinterpret_cast<float4*>(crow + col) = o;
             } else {
-              const float4 old = *reinterpret_cast<const float4*>(crow + col);
-              o = make_float4(fmaf(p.alpha, x[0], p.beta * old.x), fmaf(p.alpha, x[1], p.beta * old.y),
-                              fmaf(p.alpha, x[2], p.beta * old.z), fmaf(p.alpha, x[3], p.beta * old.w));
-            }
-            *reinterpret_cast<float4*>(crow + col) = o;
-          } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (col + e < p.N)
-                crow[col + e] = p.beta == 0.0f ? p.alpha * x[e] : fmaf(p.alpha, x[e], p.beta * crow[col + e]);
+              for (int e = 0; e < 4; ++e)
+                if (col + e < p.N)
+                  crow[col + e] = p.beta == 0.0f ? p.alpha * x[e] : fmaf(p.alpha, x[e], p.beta * crow[col + e]);
+            }
           }
         }
       }
@@ -337,15 +423,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace tc
 
-cudaError_t prepare_tf32x3() {
-  return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
+namespace {
+
+template <bool TA, bool TB>
+cudaError_t set_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<TA, TB, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<TA, TB, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              tc::kSmemBytes);
 }
 
-cudaError_t launch_tf32x3_nn(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
-                             cudaStream_t stream) {
-  tc::tf32x3_gemm_kernel<<<(unsigned)(p.tiles_m * p.tiles_n), tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB,
-                                                                                                       p);
+template <bool TA, bool TB>
+cudaError_t launch(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p, int split,
+                   cudaStream_t stream) {
+  const dim3 grid((unsigned)(p.tiles_m * p.tiles_n), (unsigned)split);
+  if (split > 1)
+    tc::tf32x3_gemm_kernel<TA, TB, true><<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB, p);
+  else
+    tc::tf32x3_gemm_kernel<TA, TB, false><<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB, p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t prepare_tf32x3() {
+  cudaError_t e = set_attrs<false, false>();
+  if (e == cudaSuccess) e = set_attrs<false, true>();
+  if (e == cudaSuccess) e = set_attrs<true, false>();
+  if (e == cudaSuccess) e = set_attrs<true, true>();
+  return e;
+}
+
+cudaError_t launch_tf32x3(bool transA, bool transB, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                          const GemmParams& p, int split, cudaStream_t stream) {
+  if (!transA && !transB) return launch<false, false>(mapA, mapB, p, split, stream);
+  if (!transA && transB) return launch<false, true>(mapA, mapB, p, split, stream);
+  if (transA && !transB) return launch<true, false>(mapA, mapB, p, split, stream);
+  return launch<true, true>(mapA, mapB, p, split, stream);
 }
 
 }  // namespace sgemm_impl

@@ -61,6 +61,7 @@ cudaError_t setup(int dev, NoallocDevice** out) {
     if (e == cudaSuccess) e = prepare_tma_op_nt();
     if (e == cudaSuccess) e = prepare_tma_op_tn();
     if (e == cudaSuccess) e = prepare_tma_op_tt();
+    if (e == cudaSuccess) e = prepare_tf32x3();
     d.err = e;
   });
   *out = &d;
@@ -154,7 +155,8 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
       e = tb ? encode_2d(B, K, N, ldb, bk, bn, true, &mapB) : encode_2d(B, N, K, ldb, bn, bk, false, &mapB);
     if (e != cudaSuccess) return SGEMM_ERR_CUDA;
     const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
-    if (!ta && !tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, cs);
+    if (plan.variant == SGEMM_VARIANT_TC_TF32X3) e = launch_tf32x3(ta, tb, mapA, mapB, p, split, cs);
+    else if (!ta && !tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, cs);
     else if (!ta && tb) e = launch_tma_op_nt(tile, mapA, mapB, p, split, cs);
     else if (ta && !tb) e = launch_tma_op_tn(tile, mapA, mapB, p, split, cs);
     else e = launch_tma_op_tt(tile, mapA, mapB, p, split, cs);

@@ -42,10 +42,10 @@ SGEMM_DECLARE_TMA_OP(nt)
 SGEMM_DECLARE_TMA_OP(tn)
 SGEMM_DECLARE_TMA_OP(tt)
 #undef SGEMM_DECLARE_TMA_OP
-// 3xTF32 tensor-core kernel (kernel_tf32x3.cu), op(A) = A, op(B) = B, 128x128x32 tiles.
+// 3xTF32 tensor-core kernel (kernel_tf32x3.cu), 128x128x32 tiles, any op, optional K split.
 cudaError_t prepare_tf32x3();
-cudaError_t launch_tf32x3_nn(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
-                             cudaStream_t stream);
+cudaError_t launch_tf32x3(bool transA, bool transB, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                          const GemmParams& p, int split, cudaStream_t stream);
 cudaError_t launch_generic_gemm(bool transA, bool transB, const GemmParams& p, int split,
                                 cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const GemmParams& p, int split, cudaStream_t stream);

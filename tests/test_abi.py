@@ -89,17 +89,17 @@ def test_planner_variants(lib):
     assert plan("N", "N", 0, 10, 10)["variant_name"] == "NONE"
     assert plan("N", "N", 10, 10, 0)["variant_name"] == "SCALE"
     big = plan("N", "N", 4096, 4096, 4096)
-    assert big["variant_name"] == "TMA_128x128" and big["split_k"] == 1 and big["kernel_launches"] == 1
-    assert big["grid_x"] == 32 * 32 and big["tile_k"] == 32 and big["threads"] == 256
+    assert big["variant_name"] == "TC_TF32X3" and big["split_k"] == 1 and big["kernel_launches"] == 1
+    assert big["grid_x"] == 32 * 32 and big["tile_k"] == 32 and big["threads"] == 608
     assert big["smem_bytes"] <= 227 * 1024
     # unaligned base or ld not a multiple of 4 -> the generic (edge) kernel
     assert plan("N", "N", 512, 512, 512, A=FAKE_ODD)["variant_name"] == "GENERIC"
     assert plan("N", "N", 512, 512, 513, lda=515)["variant_name"] == "GENERIC"
     assert plan("T", "T", 512, 512, 512, ldb=514)["variant_name"] == "GENERIC"
-    # ragged padded shapes of the transpose sweep keep the TMA path (ld % 4 == 0)
+    # ragged padded shapes of the transpose sweep keep the TMA-fed path (ld % 4 == 0)
     for ta, tb, lda, ldb in (("N", "N", 2060, 3008), ("N", "T", 2060, 2060), ("T", "N", 4104, 3008),
                              ("T", "T", 4104, 2060)):
-        assert plan(ta, tb, 4097, 3001, 2053, lda=lda, ldb=ldb)["variant_name"] == "TMA_128x128"
+        assert plan(ta, tb, 4097, 3001, 2053, lda=lda, ldb=ldb)["variant_name"] == "TC_TF32X3"
 
 
 def test_planner_split_k(lib):
@@ -107,9 +107,16 @@ def test_planner_split_k(lib):
     p = plan("N", "N", 1024, 1024, 1024)
     assert p["split_k"] == 2 and p["kernel_launches"] == 2 and p["grid_y"] == 2
     assert p["workspace_bytes"] == 2 * 1024 * 1024 * 4
-    # skinny FC shape: 64x256 tiles, 16 of them -> 9 slices
+    # skinny FC shape: 32 tiles of 128x128 -> 4 slices
     s = plan("N", "N", 64, 4096, 16384)
-    assert s["variant_name"] == "TMA_64x256" and s["grid_x"] == 16 and s["split_k"] == 9
+    assert s["variant_name"] == "TC_TF32X3" and s["grid_x"] == 32 and s["split_k"] == 4
+    # the FFMA kernel's short-M tiles when forced: 64x256 tiles, 16 of them -> 9 slices
+    try:
+        sg.sgemm_set_variant_override("TMA_64x256", 0)
+        f = plan("N", "N", 64, 4096, 16384)
+        assert f["variant_name"] == "TMA_64x256" and f["grid_x"] == 16 and f["split_k"] == 9
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
     # never more slices than K tiles, and every slice non-empty
     t = plan("N", "N", 8, 8, 64)
     assert t["split_k"] <= 2
@@ -130,7 +137,7 @@ def test_variant_override(lib):
             sg.sgemm_set_variant_override(99, 0)
     finally:
         sg.sgemm_set_variant_override("AUTO", 0)
-    assert plan("N", "N", 4096, 4096, 4096)["variant_name"] == "TMA_128x128"
+    assert plan("N", "N", 4096, 4096, 4096)["variant_name"] == "TC_TF32X3"
 
 
 def test_plan_rejects_huge_dimensions(lib):

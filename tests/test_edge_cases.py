@@ -165,21 +165,58 @@ def test_random_inputs_within_bound_all_ops():
         check_bound(got, ref, S, K, f"random {ta}{tb}")
 
 
-def test_deterministic_and_transpose_identity():
-    """Two runs are bit-identical, and sgemm('T','T', B, A) is exactly the transpose of sgemm('N','N', A, B)."""
+@pytest.mark.parametrize("variant", ["AUTO", "TMA_128x128"])
+def test_deterministic_and_transpose_identity(variant):
+    """Two runs are bit-identical; sgemm('T','T', B, A) is the transpose of sgemm('N','N', A, B).
+
+    The FP32 FFMA kernel sums the same products in the same order for both, so
+    the transpose is exact there; the 3xTF32 kernel adds its two cross terms in
+    the opposite order for the transposed problem, so there it must agree within
+    the per-element bound.
+    """
     torch = pytest.importorskip("torch")
     M, N, K = 1024, 768, 2048
-    A = to_dev(si.uniform_pm1(M, K, 11, 1))
-    B = to_dev(si.uniform_pm1(K, N, 11, 2))
+    a_np, b_np = si.uniform_pm1(M, K, 11, 1), si.uniform_pm1(K, N, 11, 2)
+    A, B = to_dev(a_np), to_dev(b_np)
     C1 = torch.empty(M, N, device="cuda")
     C2 = torch.empty(M, N, device="cuda")
     Ct = torch.empty(N, M, device="cuda")
-    sg.sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C1, N)
-    sg.sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C2, N)
-    sg.sgemm("T", "T", N, M, K, 1.0, B, N, A, K, 0.0, Ct, M)
+    sg.sgemm_set_variant_override(variant, 0)
+    try:
+        sg.sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C1, N)
+        sg.sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C2, N)
+        sg.sgemm("T", "T", N, M, K, 1.0, B, N, A, K, 0.0, Ct, M)
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
     assert sg.sgemm_sync_status() == 0
     assert torch.equal(C1, C2)
-    assert torch.equal(Ct.t(), C1)
+    if variant == "TMA_128x128":
+        assert torch.equal(Ct.t(), C1)
+    else:
+        S = (np.abs(a_np).astype(np.float64) @ np.abs(b_np).astype(np.float64))
+        err = np.abs(Ct.t().cpu().numpy().astype(np.float64) - C1.cpu().numpy().astype(np.float64))
+        assert np.all(err <= 2 * (K + 2) * 2.0 ** -24 * S)
+
+
+def test_nonfinite_inputs():
+    """NaN in A gives NaN in its row on every path; Inf gives +-Inf on the FFMA path and a
+    non-finite value (Inf or NaN) on the 3xTF32 path (documented in include/sgemm.h)."""
+    rng = np.random.default_rng(31)
+    M, N, K = 64, 96, 128
+    A = dyadic(rng, M, K) + 2.0  # positive entries
+    B = np.abs(dyadic(rng, K, N)) + 0.25
+    C = np.zeros((M, N), np.float32)
+    A[3, 5] = np.nan
+    A[7, 9] = np.inf
+    for variant in ("AUTO", "TMA_128x128", "GENERIC"):
+        got = gpu_sgemm("N", "N", M, N, K, 1.0, A.astype(np.float32), K, B, N, 0.0, C, N, variant=variant)
+        assert np.all(np.isnan(got[3])), variant
+        assert np.all(~np.isfinite(got[7])), variant
+        if variant != "AUTO":
+            assert np.all(np.isposinf(got[7])), variant
+        mask = np.ones(M, bool)
+        mask[[3, 7]] = False
+        assert np.all(np.isfinite(got[mask])), variant
 
 
 def test_non_default_stream_and_matmul_helper():

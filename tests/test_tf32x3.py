@@ -1,36 +1,55 @@
-"""GPU parity of the 3xTF32 tensor-core kernel (variant TC_TF32X3, op = NN).
+"""GPU parity of the 3xTF32 tensor-core kernel (variant TC_TF32X3), every operand layout.
 
 Dyadic inputs (multiples of 2^-6) split exactly (lo = 0) and all partial sums
 are exact, so those results must equal the oracle bit for bit: this checks
-the operand layouts, swizzles, descriptors and the epilogue.  Random inputs
-must meet the same per-element and Frobenius bounds as every other path.
+the operand layouts, swizzles, descriptors, the TMEM A operand, the K split
+and the epilogue.  Random inputs must meet the same per-element and
+Frobenius bounds as every other path.
 """
 import numpy as np
 import pytest
 
+import oracle
 import sgemm_inputs as si
-import sgemm_row_major_gb300 as sg
 from gpu_util import check_bound, check_exact, dyadic, gpu_sgemm, oracle_rows, sample_rows
 
 pytestmark = pytest.mark.gpu
 
 V = "TC_TF32X3"
+OPS = ["NN", "NT", "TN", "TT"]
 
 
+def _stored(rng, op, rows, cols):
+    r, c = si.stored_shape(op, rows, cols)
+    return dyadic(rng, r, c)
+
+
+@pytest.mark.parametrize("ops", OPS)
 @pytest.mark.parametrize("M,N,K", [(128, 128, 32), (1, 1, 1), (7, 5, 3), (129, 130, 70), (300, 260, 1000),
                                    (256, 384, 96), (1000, 1300, 700)])
-def test_dyadic_exact(M, N, K):
-    rng = np.random.default_rng(M * 7 + N)
-    A, B, C = dyadic(rng, M, K), dyadic(rng, K, N), dyadic(rng, M, N)
+def test_dyadic_exact(ops, M, N, K):
+    ta, tb = ops
+    rng = np.random.default_rng(M * 7 + N + K)
+    A, B, C = _stored(rng, ta, M, K), _stored(rng, tb, K, N), dyadic(rng, M, N)
     for alpha, beta in ((1.0, 0.0), (1.5, -0.5)):
-        got = gpu_sgemm("N", "N", M, N, K, alpha, A, K, B, N, beta, C, N, variant=V)
-        import oracle
-        ref = oracle.sgemm("N", "N", A, B, C, alpha, beta)
-        check_exact(got, ref, f"tf32x3 {M}x{N}x{K} a={alpha} b={beta}")
+        got = gpu_sgemm(ta, tb, M, N, K, alpha, A, A.shape[1], B, B.shape[1], beta, C, N, variant=V)
+        ref = oracle.sgemm(ta, tb, A, B, C, alpha, beta)
+        check_exact(got, ref, f"tf32x3 {ops} {M}x{N}x{K} a={alpha} b={beta}")
 
 
-@pytest.mark.parametrize("name", ["pr1_random", "pr1_int", "square1024", "square4096", "t2048_NN",
-                                  "ragged_NN", "fc_8192x4096x1024", "fc_16384x1024x4096"])
+@pytest.mark.parametrize("ops", OPS)
+@pytest.mark.parametrize("split", [2, 5, 31])
+def test_forced_split_k_exact(ops, split):
+    ta, tb = ops
+    rng = np.random.default_rng(split)
+    M, N, K = 150, 260, 1000
+    A, B, C = _stored(rng, ta, M, K), _stored(rng, tb, K, N), dyadic(rng, M, N)
+    got = gpu_sgemm(ta, tb, M, N, K, -2.0, A, A.shape[1], B, B.shape[1], 0.5, C, N, variant=V, split=split)
+    ref = oracle.sgemm(ta, tb, A, B, C, -2.0, 0.5)
+    check_exact(got, ref, f"tf32x3 split={split} {ops}")
+
+
+@pytest.mark.parametrize("name", [c.name for c in si.CASES])
 def test_config_parity(name):
     c = si.case(name)
     d = si.make_case(c)
