@@ -29,8 +29,8 @@
 // CTA (one 128x128 output tile or, with a K split, one K slice of it; 19 warps):
 //   warp 0     TMA producer: FP32 tiles of op(A) and op(B) (as stored) into a
 //              4-stage "raw" ring (32 KB per stage).
-//   warps 1,18 MMA issuers (one thread each; warp 1 takes even K tiles into
-//              accumulator 0, warp 18 odd K tiles into accumulator 1): per
+//   warps 1,18 MMA issuers (one thread each; warp 1 takes even K tiles,
+//              warp 18 odd ones; tile t goes to accumulator t % 3): per
 //              32-k tile, 4 k-steps x 3 tcgen05.mma (M=128, N=128, K=8);
 //              tcgen05.commit releases the split stage and hands the
 //              accumulator to the folders.  Issuing one tcgen05.mma takes a
@@ -47,8 +47,8 @@
 // completed phase once) and arrives on it, which keeps barrier traffic off
 // the shared-memory path.  Every wait is bounded (mbarrier phases).
 //
-// TMEM columns: [0,128) and [128,256) accumulators; [256 + 64 s, +32) A hi
-// and [288 + 64 s, +32) A lo of split stage s (s < 2).
+// TMEM columns: [128 b, +128) accumulator b (b < 3); [384 + 64 s, +32) A hi
+// and [416 + 64 s, +32) A lo of split stage s (s < 2).
 #include "device_utils.cuh"
 #include "sgemm_internal.h"
 
@@ -68,9 +68,10 @@ constexpr int kFirstFoldWarp = 2 + kSplitWarps;
 constexpr int kSecondMmaWarp = kFirstFoldWarp + kFoldWarps;  // warp 18
 constexpr int kThreads = 32 * (3 + kSplitWarps + kFoldWarps);
 constexpr uint32_t kAccCols = 128;                  // one 128 x 128 FP32 accumulator
+constexpr int kAccBufs = 3;                         // accumulators in flight (MMA ahead of the fold)
 constexpr uint32_t kACols = 64;                     // A hi (32 k) + A lo (32 k) of one split stage
-constexpr uint32_t kAColBase = 2 * kAccCols;
-constexpr uint32_t kTmemCols = 512;                 // 2 accumulators + 2 A stages (384 used)
+constexpr uint32_t kAColBase = kAccBufs * kAccCols;
+constexpr uint32_t kTmemCols = 512;                 // 3 accumulators + 2 A stages = 512
 
 // tcgen05 instruction descriptor, kind::tf32: FP32 accumulator, TF32 A and B,
 // both K-major, N = 128, M = 128.
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kRawStages], raw_empty[kRawStages];
   __shared__ __align__(8) uint64_t split_full[kSplitStages], split_empty[kSplitStages];
-  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
+  __shared__ __align__(8) uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   __shared__ uint32_t tmem_slot;
 
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&split_full[s]), kSplitWarps);
       mbar_init(smem_addr(&split_empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(smem_addr(&acc_full[b]), 1);
       mbar_init(smem_addr(&acc_empty[b]), kFoldWarps);
     }
@@ -225,14 +226,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicOr(p.fault, (unsigned)kFaultDrainWait);
     }
   } else if (warp == 1 || warp == kSecondMmaWarp) {
-    // ------------------------------------------------ MMA issuers (K tiles t with t & 1 == b)
+    // ------------------------------------------------ MMA issuers (K tiles t with t & 1 == issuer)
     if (lane == 0) {
-      const int b = warp == 1 ? 0 : 1;
+      const int issuer = warp == 1 ? 0 : 1;
       int done = -1;  // last K tile whose MMAs this thread issued
-      for (int t = b; t < nkt; t += 2) {
-        const int s = t % kSplitStages;
+      for (int t = issuer; t < nkt; t += 2) {
+        const int s = t % kSplitStages, b = t % kAccBufs;
         bool w = mbar_wait(smem_addr(&split_full[s]), (uint32_t)(t / kSplitStages) & 1u, p.timeout_ns);
-        if (w && t >= 2) w = mbar_wait(smem_addr(&acc_empty[b]), (uint32_t)((t >> 1) - 1) & 1u, p.timeout_ns);
+        if (w && t >= kAccBufs)
+          w = mbar_wait(smem_addr(&acc_empty[b]), (uint32_t)((t / kAccBufs) - 1) & 1u, p.timeout_ns);
         if (!w) {
           atomicOr(p.fault, (unsigned)kFaultFullWait);
           break;
@@ -254,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         done = t;
       }
       // leave only when none of this thread's MMAs is in flight
-      if (done >= 0 && !mbar_wait(smem_addr(&acc_full[b]), (uint32_t)(done >> 1) & 1u, p.timeout_ns))
+      if (done >= 0 &&
+          !mbar_wait(smem_addr(&acc_full[done % kAccBufs]), (uint32_t)(done / kAccBufs) & 1u, p.timeout_ns))
         atomicOr(p.fault, (unsigned)kFaultDrainWait);
     }
   } else if (warp < kFirstFoldWarp) {
@@ -353,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = 0; e < 64; ++e) master[e] = 0.0f;
     bool ok = true;
     for (int u = 0; u < nkt; ++u) {
-      const int b = u & 1;
-      if (!warp_wait(smem_addr(&acc_full[b]), (uint32_t)(u >> 1) & 1u, p.timeout_ns)) {
+      const int b = u % kAccBufs;
+      if (!warp_wait(smem_addr(&acc_full[b]), (uint32_t)(u / kAccBufs) & 1u, p.timeout_ns)) {
         ok = false;
         if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
         break;
