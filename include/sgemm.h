@@ -151,6 +151,24 @@ int sgemm_set_variant_override(int variant, int split_k);
 int sgemm_selftest_wait_timeout(unsigned timeout_us, struct CUstream_st *stream);
 
 /*
+ * sgemm_host -- the same operation with A, B and C in HOST memory (same
+ * layout rules and argument checks as sgemm(); page-locked memory gives full
+ * copy speed, pageable memory works but its copies are staged by the driver
+ * and device-to-host copies then block the calling thread).  B is copied to
+ * the device once; op(A) and C move in row blocks of C on two library-owned
+ * streams, so copies of one block overlap the GEMM of the other.  Device
+ * buffers come from a library-owned stream-ordered pool.  Asynchronous on
+ * `stream`: the work starts after what is already on `stream`, and `stream`
+ * waits for all of it; keep the host buffers alive and do not read C until
+ * `stream` has completed.  Calls are serialised per device.
+ */
+int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_t K,
+               float alpha, const float *A, int64_t lda,
+               const float *B, int64_t ldb,
+               float beta, float *C, int64_t ldc,
+               struct CUstream_st *stream);
+
+/*
  * sgemm_noalloc -- the same operation, arguments and results as sgemm(), for
  * callers that cannot allocate device memory during the call.  (The pages
  * have no counterpart; this is a library convenience.)

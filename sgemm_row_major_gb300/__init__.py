@@ -16,7 +16,7 @@ import os
 import threading
 
 __all__ = [
-    "SgemmError", "load", "library_path", "sgemm", "sgemm_noalloc", "sgemm_plan", "sgemm_status_string",
+    "SgemmError", "load", "library_path", "sgemm", "sgemm_host", "sgemm_noalloc", "sgemm_plan", "sgemm_status_string",
     "sgemm_last_cuda_error", "sgemm_sync_status", "sgemm_set_variant_override",
     "sgemm_selftest_wait_timeout", "matmul", "VARIANTS", "STATUS",
 ]
@@ -65,6 +65,8 @@ def load() -> ctypes.CDLL:
         i64, f32, vp, ch = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_char
         lib.sgemm.restype = ctypes.c_int
         lib.sgemm.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        lib.sgemm_host.restype = ctypes.c_int
+        lib.sgemm_host.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_noalloc.restype = ctypes.c_int
         lib.sgemm_noalloc.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_plan.restype = ctypes.c_int
@@ -124,6 +126,34 @@ def sgemm(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=N
                       _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), _stream(stream))
     if st != 0 and raise_on_error:
         raise SgemmError(st)
+    return st
+
+
+def _host_ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if getattr(x, "is_cuda", False):
+            raise TypeError("sgemm_host operands must be host memory")
+        return int(x.data_ptr())
+    if hasattr(x, "__array_interface__"):
+        return int(x.__array_interface__["data"][0])
+    raise TypeError(f"cannot pass {type(x).__name__} as a host pointer")
+
+
+def sgemm_host(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None, *,
+               raise_on_error: bool = True) -> int:
+    """sgemm() on HOST operands (numpy arrays, CPU tensors or addresses); C is written back to host memory.
+
+    Asynchronous on ``stream``: synchronise it before reading C.  Page-locked
+    host memory (e.g. ``torch.empty(..., pin_memory=True)``) gives full speed.
+    """
+    st = load().sgemm_host(_ch(transA), _ch(transB), int(M), int(N), int(K), float(alpha), _host_ptr(A),
+                           int(lda), _host_ptr(B), int(ldb), float(beta), _host_ptr(C), int(ldc), _stream(stream))
+    if st != 0 and raise_on_error:
+        raise SgemmError(st, "sgemm_host")
     return st
 
 
