@@ -16,10 +16,10 @@
 //
 // The tensor core's FP32 accumulation is not round-to-nearest: measured on
 // GB300, one accumulator over K = 4096 drifts to a relative Frobenius error of
-// ~3e-5, growing linearly with the number of accumulated MMAs.  So every 32-k
-// tile gets a fresh accumulator (12 MMAs), and the splitter warps fold it into
-// FP32 registers with round-to-nearest adds; the error then no longer grows
-// with K (~2e-7 relative).
+// ~3e-5, growing linearly with the number of accumulated MMAs (~2e-8 each).
+// So every chunk of kFoldTiles 32-k tiles gets a fresh accumulator, and the
+// folder warps add it into FP32 registers with round-to-nearest adds; the
+// error then no longer grows with K.
 //
 // Shared-memory bandwidth is the limit of this design (TMA writes, split
 // reads and writes and the tensor core's operand reads all use the same
@@ -69,6 +69,11 @@ constexpr int kSecondMmaWarp = kFirstFoldWarp + kFoldWarps;  // warp 18
 constexpr int kThreads = 32 * (3 + kSplitWarps + kFoldWarps);
 constexpr uint32_t kAccCols = 128;                  // one 128 x 128 FP32 accumulator
 constexpr int kAccBufs = 3;                         // accumulators in flight (MMA ahead of the fold)
+constexpr int kFoldTiles = 1;                       // 32-k tiles summed in one accumulator before a fold
+// Two issuers may alternate only single-tile chunks: an issuer that skipped a
+// phase of a stage barrier could not tell the phase it needs from the one
+// two ahead (mbarrier waits are by phase parity).
+constexpr int kIssuers = kFoldTiles == 1 ? 2 : 1;
 constexpr uint32_t kACols = 64;                     // A hi (32 k) + A lo (32 k) of one split stage
 constexpr uint32_t kAColBase = kAccBufs * kAccCols;
 constexpr uint32_t kTmemCols = 512;                 // 3 accumulators + 2 A stages = 512
@@ -226,35 +231,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicOr(p.fault, (unsigned)kFaultDrainWait);
     }
   } else if (warp == 1 || warp == kSecondMmaWarp) {
-    // ------------------------------------------------ MMA issuers (K tiles t with t & 1 == issuer)
-    if (lane == 0) {
-      const int issuer = warp == 1 ? 0 : 1;
-      int done = -1;  // last K tile whose MMAs this thread issued
-      for (int t = issuer; t < nkt; t += 2) {
-        const int s = t % kSplitStages, b = t % kAccBufs;
-        bool w = mbar_wait(smem_addr(&split_full[s]), (uint32_t)(t / kSplitStages) & 1u, p.timeout_ns);
-        if (w && t >= kAccBufs)
-          w = mbar_wait(smem_addr(&acc_empty[b]), (uint32_t)((t / kAccBufs) - 1) & 1u, p.timeout_ns);
-        if (!w) {
-          atomicOr(p.fault, (unsigned)kFaultFullWait);
+    // ------------------------------------------------ MMA issuers (fold chunks c with c % kIssuers == issuer)
+    const int issuer = warp == 1 ? 0 : 1;
+    if (lane == 0 && issuer < kIssuers) {
+      const int nchunks = (nkt + kFoldTiles - 1) / kFoldTiles;
+      int done = -1;  // last chunk whose MMAs this thread issued
+      bool ok = true;
+      for (int c = issuer; ok && c < nchunks; c += kIssuers) {
+        const int b = c % kAccBufs;
+        if (c >= kAccBufs &&
+            !mbar_wait(smem_addr(&acc_empty[b]), (uint32_t)((c / kAccBufs) - 1) & 1u, p.timeout_ns)) {
+          ok = false;
           break;
         }
-        tmem_fence_after_sync();
         const uint32_t acc = tmem + (uint32_t)b * kAccCols;
-        const uint32_t ahi = tmem + kAColBase + (uint32_t)s * kACols, alo = ahi + 32u;
-        const uint64_t bhi = kmajor_sw128_desc(split_tile(s, 0)), blo = kmajor_sw128_desc(split_tile(s, 1));
+        for (int t = c * kFoldTiles; t < min(nkt, (c + 1) * kFoldTiles); ++t) {
+          const int s = t % kSplitStages;
+          if (!mbar_wait(smem_addr(&split_full[s]), (uint32_t)(t / kSplitStages) & 1u, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tmem_fence_after_sync();
+          const uint32_t ahi = tmem + kAColBase + (uint32_t)s * kACols, alo = ahi + 32u;
+          const uint64_t bhi = kmajor_sw128_desc(split_tile(s, 0)), blo = kmajor_sw128_desc(split_tile(s, 1));
+          const bool first = t == c * kFoldTiles;
 #pragma unroll
-        for (int ks = 0; ks < BK / 8; ++ks) {
-          const uint64_t step = (uint64_t)(ks * 32) >> 4;  // 8 TF32 = 32 bytes along K
-          const uint32_t acol = (uint32_t)(8 * ks);        // 8 TF32 = 8 TMEM columns
-          mma_tf32_ts(acc, alo + acol, bhi + step, ks > 0 ? 1u : 0u);  // fresh accumulator per K tile
-          mma_tf32_ts(acc, ahi + acol, blo + step, 1u);
-          mma_tf32_ts(acc, ahi + acol, bhi + step, 1u);
+          for (int ks = 0; ks < BK / 8; ++ks) {
+            const uint64_t step = (uint64_t)(ks * 32) >> 4;  // 8 TF32 = 32 bytes along K
+            const uint32_t acol = (uint32_t)(8 * ks);        // 8 TF32 = 8 TMEM columns
+            mma_tf32_ts(acc, alo + acol, bhi + step, (first && ks == 0) ? 0u : 1u);  // fresh accumulator per chunk
+            mma_tf32_ts(acc, ahi + acol, blo + step, 1u);
+            mma_tf32_ts(acc, ahi + acol, bhi + step, 1u);
+          }
+          mma_commit(smem_addr(&split_empty[s]));  // split stage reusable once these MMAs have read it
         }
-        mma_commit(smem_addr(&split_empty[s]));  // split stage reusable once these MMAs have read it
-        mma_commit(smem_addr(&acc_full[b]));     // accumulator b holds K tile t
-        done = t;
+        mma_commit(smem_addr(&acc_full[b]));  // accumulator b holds chunk c
+        done = c;
       }
+      if (!ok) atomicOr(p.fault, (unsigned)kFaultFullWait);
       // leave only when none of this thread's MMAs is in flight
       if (done >= 0 &&
           !mbar_wait(smem_addr(&acc_full[done % kAccBufs]), (uint32_t)(done / kAccBufs) & 1u, p.timeout_ns))
@@ -355,7 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int e = 0; e < 64; ++e) master[e] = 0.0f;
     bool ok = true;
-    for (int u = 0; u < nkt; ++u) {
+    const int nchunks = (nkt + kFoldTiles - 1) / kFoldTiles;
+    for (int u = 0; u < nchunks; ++u) {
       const int b = u % kAccBufs;
       if (!warp_wait(smem_addr(&acc_full[b]), (uint32_t)(u / kAccBufs) & 1u, p.timeout_ns)) {
         ok = false;
