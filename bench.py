@@ -185,6 +185,22 @@ def cpu_baseline(case, d, seconds):
                       f"{flops / 1e9:.2f} GFLOP) in {t:.1f} s; TFLOPS = 2*rows*N*K/t"}
 
 
+def reduce_max_ms(ms: float, world: int, device=None) -> float:
+    """Slowest rank's time: the job is done when every replica is done."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> float:
+    """Whole-job rate: the work all replicas did over the slowest replica's time."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -339,14 +355,10 @@ def run_ours(args):
     if sg.sgemm_sync_status(sh) != 0:
         raise RuntimeError("libsgemm reported a kernel fault during the benchmark")
 
-    total_ms = g0.elapsed_time(g1)
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max_ms(g0.elapsed_time(g1), world, dev)
     flops_step = si.flops(M, N, K)
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(world, flops_step, args.steps, total_ms)
     kernel_ms = statistics.mean(step_ms)
     achieved = flops_step / (kernel_ms * 1e-3) / 1e12
 
@@ -367,12 +379,8 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * flops_step * args.e2e_steps / (e2e_ms * 1e-3) / 1e12 if args.e2e_steps > 0 else None
+    e2e_ms = reduce_max_ms(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_tflops(world, flops_step, args.e2e_steps, e2e_ms) if args.e2e_steps > 0 else None
     h2d = (hA.numel() + hB.numel() + (hC.numel() if case.beta != 0.0 else 0)) * 4
     d2h = hC.numel() * 4
 
