@@ -115,7 +115,6 @@ extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_
       e = cudaMemcpy2DAsync(dB, (size_t)ldb_d * 4, B, (size_t)ldb * 4, (size_t)b_cols * 4, (size_t)b_rows,
                             cudaMemcpyHostToDevice, d->s[0]);
     if (e == cudaSuccess) e = cudaEventRecord(d->ev_b, d->s[0]);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->s[1], d->ev_b, 0);
     if (e != cudaSuccess) fail(e);
   }
   for (int i = 0; i < 2 && status == SGEMM_OK; ++i) {
@@ -144,6 +143,11 @@ extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_
     if (reads_c) {
       e = cudaMemcpy2DAsync(dC[i], (size_t)ldc_d * 4, C + r0 * ldc, (size_t)ldc * 4, (size_t)N * 4, (size_t)rows,
                             cudaMemcpyHostToDevice, s);
+      if (e != cudaSuccess) { fail(e); break; }
+    }
+    // only the GEMM needs B; stream 1's first copies already ran beside B's
+    if (reads_ab && i == 1 && blk == 1) {
+      e = cudaStreamWaitEvent(s, d->ev_b, 0);
       if (e != cudaSuccess) { fail(e); break; }
     }
     st = sgemm(transA, transB, rows, N, K, alpha, dA[i], lda_d, dB, ldb_d, beta, dC[i], ldc_d,
