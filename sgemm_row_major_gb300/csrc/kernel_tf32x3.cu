@@ -134,7 +134,11 @@ __device__ __forceinline__ float tf32_round(float x) {
 
 __device__ __forceinline__ void split4(const float4 x, float4& hi, float4& lo) {
   hi = make_float4(tf32_round(x.x), tf32_round(x.y), tf32_round(x.z), tf32_round(x.w));
-  lo = make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
+  // lo = x - hi (exact), two at a time: fma(hi, -1, x) rounds an exact value
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+  const float2 l01 = __ffma2_rn(make_float2(hi.x, hi.y), m1, make_float2(x.x, x.y));
+  const float2 l23 = __ffma2_rn(make_float2(hi.z, hi.w), m1, make_float2(x.z, x.w));
+  lo = make_float4(l01.x, l01.y, l23.x, l23.y);
 }
 
 __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, int& tm, int& tn) {
@@ -365,9 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                          // TMEM lane quarter this warp may access
     const int half = (warp - kFirstFoldWarp) >> 2;   // which 64 accumulator columns
     const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * half);
-    float master[64];
+    float2 master2[32];  // columns 2e, 2e+1 of this thread's 64
 #pragma unroll
-    for (int e = 0; e < 64; ++e) master[e] = 0.0f;
+    for (int e = 0; e < 32; ++e) master2[e] = make_float2(0.0f, 0.0f);
     bool ok = true;
     const int nchunks = (nkt + kFoldTiles - 1) / kFoldTiles;
     for (int u = 0; u < nchunks; ++u) {
@@ -386,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c) {
         tmem_ld_ready(v[c]);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) master[16 * c + e] += v[c][e];  // round-to-nearest FP32 adds
+        for (int e = 0; e < 8; ++e)  // round-to-nearest FP32 adds, two per instruction
+          master2[8 * c + e] = __fadd2_rn(master2[8 * c + e], make_float2(v[c][2 * e], v[c][2 * e + 1]));
       }
       tmem_fence_before_sync();
       __syncwarp();
@@ -394,6 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       // epilogue: this thread holds row 32q + lane, columns 64*half .. +63 of the tile
+      float master[64];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        master[2 * e] = master2[e].x;
+        master[2 * e + 1] = master2[e].y;
+      }
       const int row = m0 + 32 * q + lane;
       if (row < p.M) {
         if (SPLIT) {
