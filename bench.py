@@ -52,7 +52,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default=si.HEADLINE, help="workload name from sgemm_inputs.CASES")
+    ap.add_argument("--config", default=si.HEADLINE,
+                    help="workload name from sgemm_inputs.CASES or sgemm_inputs.BATCHED_CASES")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -279,6 +280,60 @@ def cublas_context(case, sets, steps, stream):
         torch.backends.cuda.matmul.allow_tf32 = prev
 
 
+def timed_steps(step, args, stream, dev, local, barrier, world):
+    """Pre-warm, W warm-up steps, then exactly K timed steps between barriers.
+
+    Returns (per-step kernel ms from CUDA events on `stream`, the slowest
+    rank's total ms, the clock summary sampled during the timed region)."""
+    import torch
+    t_end = time.time() + args.prewarm_s
+    i = 0
+    while time.time() < t_end:
+        step(i)
+        i += 1
+        if i % 20 == 0:
+            torch.cuda.synchronize(dev)
+    for w in range(args.warmup):
+        step(w)
+    barrier()
+
+    sampler = ClockSampler(gpu_selector(local))
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    t0_wall = time.time()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        step(s)
+        ev[s][1].record(stream)
+    g1.record(stream)
+    barrier()
+    t1_wall = time.time()
+    time.sleep(0.1)
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = reduce_max_ms(g0.elapsed_time(g1), world, dev)
+    return step_ms, total_ms, sampler.summary(t0_wall, t1_wall)
+
+
+def tensor_roofline(achieved, peaks, traffic, kernel_ms):
+    """Roofline object of the 3xTF32 tensor-core kernel (see the module docstring of the kernel)."""
+    bf16 = peaks.get("bf16_tflops")
+    basis = "measured" if bf16 else "fallback"
+    bf16 = bf16 or 1900.0
+    tf32 = bf16 * NOMINAL_TF32_PF / NOMINAL_BF16_PF
+    return {"bound": "tensor", "achieved": achieved, "peak": tf32 / TF32_PRODUCTS, "unit": "TFLOP/s",
+            "frac": achieved / (tf32 / TF32_PRODUCTS), "traffic": traffic,
+            "peak_basis": f"{basis} bf16 burst {bf16:.0f} TFLOP/s x nominal tf32/bf16 "
+                          f"{NOMINAL_TF32_PF}/{NOMINAL_BF16_PF} = {tf32:.0f} TFLOP/s of tf32, / {TF32_PRODUCTS} "
+                          f"tensor products per SGEMM FMA (3xTF32 split); achieved counts 2MNK only",
+            "kernel": "tf32x3_gemm_kernel (tcgen05.mma kind::tf32, 3xTF32 split)", "kernel_ms": kernel_ms}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -322,41 +377,9 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    # pre-warm so clocks settle, then exactly W warm-up steps
-    t_end = time.time() + args.prewarm_s
-    i = 0
-    while time.time() < t_end:
-        step(i)
-        i += 1
-        if i % 20 == 0:
-            torch.cuda.synchronize(dev)
-    for w in range(args.warmup):
-        step(w)
-    barrier()
-
-    sampler = ClockSampler(gpu_selector(local))
-    sampler.start()
-    time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier()
-    t0_wall = time.time()
-    g0 = torch.cuda.Event(enable_timing=True)
-    g1 = torch.cuda.Event(enable_timing=True)
-    g0.record(stream)
-    for s in range(args.steps):
-        ev[s][0].record(stream)
-        step(s)
-        ev[s][1].record(stream)
-    g1.record(stream)
-    barrier()
-    t1_wall = time.time()
-    time.sleep(0.1)
-    sampler.stop()
+    step_ms, total_ms, clocks = timed_steps(step, args, stream, dev, local, barrier, world)
     if sg.sgemm_sync_status(sh) != 0:
         raise RuntimeError("libsgemm reported a kernel fault during the benchmark")
-
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = reduce_max_ms(g0.elapsed_time(g1), world, dev)
     flops_step = si.flops(M, N, K)
     value = job_tflops(world, flops_step, args.steps, total_ms)
     kernel_ms = statistics.mean(step_ms)
@@ -391,23 +414,13 @@ def run_ours(args):
 
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
-    clocks = sampler.summary(t0_wall, t1_wall)
     peaks = measured_peaks()
     max_mhz = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
     ffma_peak = sms * FMA_PER_SM_PER_CLK * 2 * max_mhz * 1e6 / 1e12
     variant = plan["variant_name"]
     if variant == "TC_TF32X3":
-        bf16 = peaks.get("bf16_tflops")
-        basis = "measured" if bf16 else "fallback"
-        bf16 = bf16 or 1900.0
-        tf32 = bf16 * NOMINAL_TF32_PF / NOMINAL_BF16_PF
-        roof = {"bound": "tensor", "achieved": achieved, "peak": tf32 / TF32_PRODUCTS, "unit": "TFLOP/s",
-                "frac": achieved / (tf32 / TF32_PRODUCTS),
-                "traffic": traffic_from_profile(variant, lib_build.tc_kernel_digest()),
-                "peak_basis": f"{basis} bf16 burst {bf16:.0f} TFLOP/s x nominal tf32/bf16 "
-                              f"{NOMINAL_TF32_PF}/{NOMINAL_BF16_PF} = {tf32:.0f} TFLOP/s of tf32, / {TF32_PRODUCTS} "
-                              f"tensor products per SGEMM FMA (3xTF32 split); achieved counts 2MNK only",
-                "kernel": "tf32x3_gemm_kernel (tcgen05.mma kind::tf32, 3xTF32 split)", "kernel_ms": kernel_ms}
+        roof = tensor_roofline(achieved, peaks, traffic_from_profile(variant, lib_build.tc_kernel_digest()),
+                               kernel_ms)
     else:
         roof = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
                 "frac": achieved / ffma_peak,
@@ -442,9 +455,182 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- strided batch workloads
+
+BATCHED_METRIC = "strided-batched SGEMM TFLOPS (2*batch*MNK/t) on 1 GB300"
+
+
+def batched_config_block(c, d, n_gpus):
+    return {"workload": f"sgemm_strided_batched_{c.transA}{c.transB}_{c.batch}x{c.M}x{c.N}x{c.K}",
+            "name": c.name, "batch": c.batch, "M": c.M, "N": c.N, "K": c.K, "ops": c.ops,
+            "alpha": c.alpha, "beta": c.beta, "inputs": c.dist, "shared": c.shared or "none",
+            "strides": {k: d["stride" + k] for k in "ABC"}, "layout": "row-major fp32, packed products",
+            "l2": "two input sets used in turn, each larger than the 129 MB L2; no flush kernel",
+            "parallelism": f"replicas x{n_gpus}"}
+
+
+def batched_oracle_run(c, d, products):
+    """Oracle strided batch over the first `products` products; returns seconds."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.sgemm_strided_batched(c.transA, c.transB, c.M, c.N, c.K, c.alpha, d["A"], d["lda"], d["strideA"],
+                                 d["B"], d["ldb"], d["strideB"], c.beta, d["C"], d["ldc"], d["strideC"], products)
+    return time.perf_counter() - t0
+
+
+def batched_oracle_sample(c, d, seconds):
+    """Number of whole products whose oracle run takes about `seconds`, and that run's time."""
+    t = max(batched_oracle_run(c, d, 1), 1e-4)
+    n = int(max(1, min(c.batch, round(seconds / t))))
+    return n, batched_oracle_run(c, d, n)
+
+
+def run_reference_batched(args, c):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    d = si.make_batched(c.batch, c.M, c.N, c.K, c.transA, c.transB, seed=c.seed, dist=c.dist, shared=c.shared,
+                        c_init="uniform" if c.beta != 0 else "zero")
+    per_step = max(0.5, min(5.0, 100.0 / max(1, args.steps + args.warmup)))
+    products, _ = batched_oracle_sample(c, d, per_step)
+    for _ in range(args.warmup):
+        batched_oracle_run(c, d, products)
+    total = sum(batched_oracle_run(c, d, products) for _ in range(args.steps))
+    value = products * si.flops(c.M, c.N, c.K) * args.steps / total / 1e12
+    sample = (f"each step: the first {products} of {c.batch} products ({c.M}x{c.N}x{c.K} each); "
+              f"TFLOPS = 2*products*M*N*K/t")
+    print(json.dumps({
+        "impl": "reference", "metric": BATCHED_METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate",
+        "data": "synthetic", "config": batched_config_block(c, d, args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours_batched(args, c):
+    """One step = one sgemm_strided_batched() call over the whole batch."""
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from sgemm_row_major_gb300 import build as lib_build
+    lib_build.build()
+    import sgemm_row_major_gb300 as sg
+
+    d = si.make_batched(c.batch, c.M, c.N, c.K, c.transA, c.transB, seed=c.seed, dist=c.dist, shared=c.shared,
+                        c_init="uniform" if c.beta != 0 else "zero")
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    if args.variant != "AUTO":
+        sg.sgemm_set_variant_override(args.variant, 0)
+    sets = [tuple(torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C")) for _ in range(2)]
+    torch.cuda.synchronize(dev)
+    strides = (d["strideA"], d["strideB"], d["strideC"])
+    plan = sg.sgemm_plan_strided_batched(c.transA, c.transB, c.M, c.N, c.K, c.alpha, sets[0][0], d["lda"],
+                                         sets[0][1], d["ldb"], c.beta, sets[0][2], d["ldc"], *strides, c.batch)
+
+    def step(i):
+        A, B, C = sets[i & 1]
+        sg.sgemm_strided_batched(c.transA, c.transB, c.M, c.N, c.K, c.alpha, A, d["lda"], B, d["ldb"], c.beta, C,
+                                 d["ldc"], *strides, c.batch, sh)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    step_ms, total_ms, clocks = timed_steps(step, args, stream, dev, local, barrier, world)
+    if sg.sgemm_sync_status(sh) != 0:
+        raise RuntimeError("libsgemm reported a kernel fault during the benchmark")
+    flops_step = c.batch * si.flops(c.M, c.N, c.K)
+    value = job_tflops(world, flops_step, args.steps, total_ms)
+    kernel_ms = statistics.mean(step_ms)
+    achieved = flops_step / (kernel_ms * 1e-3) / 1e12
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peaks = measured_peaks()
+    line = {
+        "metric": BATCHED_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {**batched_config_block(c, d, world), "prewarm_s": args.prewarm_s,
+                   "plan": {k: plan[k] for k in ("variant_name", "split_k", "grid_x", "grid_y")}},
+        "roofline": (tensor_roofline(achieved, peaks, None, kernel_ms) if plan["variant_name"] == "TC_TF32X3"
+                     else {"bound": "alu", "achieved": achieved, "peak": None, "unit": "TFLOP/s", "frac": None,
+                           "traffic": None, "kernel": plan["variant_name"], "kernel_ms": kernel_ms}),
+        "e2e": {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                "note": "no host-buffer batched entry point; the device-resident value is the measurement"},
+        "gpu_launches": plan["kernel_launches"] * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cublas_context:
+        prev = torch.backends.cuda.matmul.allow_tf32
+        torch.backends.cuda.matmul.allow_tf32 = False
+        try:
+            def view(flat, n, rows, cols, ld, stride):
+                return flat.as_strided((n, rows, cols), (stride, ld, 1))
+            outs = [torch.empty_like(s_[2]) for s_ in sets]
+
+            def one(i):
+                A, B, C = sets[i & 1]
+                ar, ac = si.stored_shape(c.transA, c.M, c.K)
+                br, bc = si.stored_shape(c.transB, c.K, c.N)
+                a = view(A, c.batch, ar, ac, d["lda"], d["strideA"])
+                b = view(B, c.batch, br, bc, d["ldb"], d["strideB"])
+                a = a.transpose(1, 2) if c.transA == "T" else a
+                b = b.transpose(1, 2) if c.transB == "T" else b
+                o = view(outs[i & 1], c.batch, c.M, c.N, d["ldc"], d["strideC"])
+                torch.baddbmm(view(C, c.batch, c.M, c.N, d["ldc"], d["strideC"]), a, b, beta=c.beta, alpha=c.alpha,
+                              out=o)
+            for i in range(5):
+                one(i)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = min(args.steps, 50)
+            e0.record(stream)
+            for i in range(n):
+                one(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            line["context_cublas_fp32"] = {
+                "value": flops_step / (e0.elapsed_time(e1) / n * 1e-3) / 1e12, "unit": UNIT,
+                "what": "cuBLAS FP32 strided batch via torch.baddbmm, allow_tf32=False; context only"}
+        finally:
+            torch.backends.cuda.matmul.allow_tf32 = prev
+    if not args.no_cpu_baseline:
+        import oracle
+        products, t = batched_oracle_sample(c, d, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": products * si.flops(c.M, c.N, c.K) / t / 1e12, "unit": UNIT,
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"the first {products} of {c.batch} products ({c.M}x{c.N}x{c.K}) in {t:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    batched = {c.name: c for c in si.BATCHED_CASES}
+    if args.config in batched:
+        c = batched[args.config]
+        if args.impl == "reference":
+            run_reference_batched(args, c)
+        else:
+            run_ours_batched(args, c)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -151,6 +151,48 @@ int sgemm_set_variant_override(int variant, int split_k);
 int sgemm_selftest_wait_timeout(unsigned timeout_us, struct CUstream_st *stream);
 
 /*
+ * sgemm_strided_batched -- batch_count independent products in one call
+ * (the FC-layer use of SGEMM: itan.pw "CUDA NVIDIA 4090 高性能計算", 概要,
+ * names fully connected and convolution layers as what SGEMM serves):
+ *
+ *     C_b = alpha * op(A_b) * op(B_b) + beta * C_b,   b = 0 .. batch_count-1,
+ *     A_b = A + b*strideA,  B_b = B + b*strideB,  C_b = C + b*strideC,
+ *
+ * strides in ELEMENTS, every product with the shapes, leading dimensions and
+ * layout rules of sgemm().  The first 13 arguments are sgemm()'s, so a
+ * negative status names the same argument; then 14 strideA, 15 strideB,
+ * 16 strideC, 17 batch_count, 18 stream.
+ *   - strideA or strideB may be 0 (one matrix shared by every product) or
+ *     smaller than a matrix (overlapping operands are only read).
+ *   - With batch_count > 1 the C matrices must not overlap:
+ *     strideC >= (M-1)*ldc + N, else -16.  Negative strides: -14/-15/-16.
+ *   - batch_count < 0: -17; batch_count == 0 (or M == 0 or N == 0): nothing
+ *     is done, SGEMM_OK.
+ *   - The arithmetic, special values and error behaviour of each product are
+ *     those of sgemm(); one call launches one GEMM kernel for all products
+ *     (plus the split-K reduction when the products are too few to fill the
+ *     GPU).  The fast paths need strides that are multiples of 4 floats (and
+ *     non-overlapping operands or a 0 stride); other strides take the
+ *     any-alignment kernel.
+ */
+int sgemm_strided_batched(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                          float alpha, const float *A, int64_t lda,
+                          const float *B, int64_t ldb,
+                          float beta, float *C, int64_t ldc,
+                          int64_t strideA, int64_t strideB, int64_t strideC,
+                          int64_t batch_count, struct CUstream_st *stream);
+
+/* What sgemm_strided_batched() would launch (grid_x counts the tiles of all
+ * products, workspace_bytes the partial sums of all products); argument
+ * checks as there, sm_count as in sgemm_plan(); plan == NULL gives -19. */
+int sgemm_plan_strided_batched(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                               float alpha, const float *A, int64_t lda,
+                               const float *B, int64_t ldb,
+                               float beta, const float *C, int64_t ldc,
+                               int64_t strideA, int64_t strideB, int64_t strideC,
+                               int64_t batch_count, int sm_count, sgemm_plan_t *plan);
+
+/*
  * sgemm_host -- the same operation with A, B and C in HOST memory (same
  * layout rules and argument checks as sgemm(); page-locked memory gives full
  * copy speed, pageable memory works but its copies are staged by the driver

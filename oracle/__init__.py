@@ -18,7 +18,9 @@ against an independent float64 einsum on tiny shapes, exact integer results on
 the pages' (j-i)%3 pattern against an int64 matmul, the K=1 correctly rounded
 product, alpha=0 -> beta*C, identity -> alpha*B + beta*C, (AB)^T = B^T A^T,
 op='T' on a transposed copy, exact power-of-two scaling of alpha, and the
-bound magnitude S against |A|@|B|.  tests/test_oracle_mutations.py plants
+bound magnitude S against |A|@|B|; the strided batch against a float64 einsum
+over stacked dyadic operands, with shared (stride 0) operands and NaN gaps
+between matrices.  tests/test_oracle_mutations.py plants
 mistakes in a copy of the C source and checks that a pin catches each one.
 """
 from __future__ import annotations
@@ -70,6 +72,14 @@ def load_library(path: str) -> ctypes.CDLL:
                   ctypes.c_void_p, ctypes.c_int64,
                   ctypes.c_float, ctypes.c_void_p, ctypes.c_int64,
                   ctypes.c_void_p, ctypes.c_int64]
+    g = lib.oracle_sgemm_strided_batched
+    g.restype = ctypes.c_int
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    g.argtypes = [ctypes.c_char, ctypes.c_char, i64, i64, i64,
+                  ctypes.c_float, vp, i64, i64,
+                  vp, i64, i64,
+                  ctypes.c_float, vp, i64, i64,
+                  i64, vp, i64, i64]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     return lib
@@ -111,6 +121,29 @@ def sgemm_raw(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, S=No
     return int(lib.oracle_sgemm(_c(transA), _c(transB), int(M), int(N), int(K),
                                 float(alpha), _ptr(A), int(lda), _ptr(B), int(ldb),
                                 float(beta), _ptr(C), int(ldc), _ptr(S), int(lds)))
+
+
+def sgemm_strided_batched(transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+                          strideC, batch, want_bound: bool = False, lib=None):
+    """Strided batch on flat float32 buffers: product b reads A[b*strideA:],
+    B[b*strideB:] and updates C[b*strideC:] (see oracle_sgemm_strided_batched).
+
+    Returns a new flat C buffer (the input C is not modified) and, with
+    ``want_bound``, S as a (batch, M, N) float64 array.
+    """
+    lib = lib or _library()
+    for name, arr in (("A", A), ("B", B), ("C", C)):
+        if arr is not None and (arr.dtype != np.float32 or arr.ndim != 1 or not arr.flags.c_contiguous):
+            raise OracleError(f"{name} must be a flat C-contiguous float32 array")
+    out = None if C is None else C.copy()
+    S = np.zeros((max(int(batch), 0), int(M), int(N)), dtype=np.float64) if want_bound else None
+    st = int(lib.oracle_sgemm_strided_batched(
+        _c(transA), _c(transB), int(M), int(N), int(K), float(alpha), _ptr(A), int(lda), int(strideA),
+        _ptr(B), int(ldb), int(strideB), float(beta), _ptr(out), int(ldc), int(strideC), int(batch),
+        _ptr(S), int(N), int(M) * int(N)))
+    if st != 0:
+        raise OracleError(f"oracle_sgemm_strided_batched returned {st}")
+    return (out, S) if want_bound else out
 
 
 def _c(t) -> bytes:

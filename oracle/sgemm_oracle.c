@@ -104,6 +104,33 @@ int oracle_sgemm(char transA, char transB, int64_t M, int64_t N, int64_t K,
     return 0;
 }
 
+/*
+ * Strided batch (the use of SGEMM for many fully connected layers at once,
+ * itan.pw page, 概要): product b = 0 .. batch-1 is the SGEMM above on the
+ * matrices that start at A + b*strideA, B + b*strideB and C + b*strideC
+ * (strides in elements; 0 shares one matrix).  S, when given, receives
+ * product b's magnitudes at S + b*strideS.  Products are computed one after
+ * another in ascending b.  Returns 0, -100 for a negative stride or batch, or
+ * the first product's own error status.
+ */
+int oracle_sgemm_strided_batched(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                                 float alpha, const float *A, int64_t lda, int64_t strideA,
+                                 const float *B, int64_t ldb, int64_t strideB,
+                                 float beta, float *C, int64_t ldc, int64_t strideC,
+                                 int64_t batch, double *S, int64_t lds, int64_t strideS)
+{
+    if (strideA < 0 || strideB < 0 || strideC < 0 || strideS < 0 || batch < 0) return -100;
+    for (int64_t b = 0; b < batch; ++b) {
+        const float *Ab = A ? A + b * strideA : A;
+        const float *Bb = B ? B + b * strideB : B;
+        float *Cb = C ? C + b * strideC : C;
+        double *Sb = S ? S + b * strideS : S;
+        const int st = oracle_sgemm(transA, transB, M, N, K, alpha, Ab, lda, Bb, ldb, beta, Cb, ldc, Sb, lds);
+        if (st != 0) return st;
+    }
+    return 0;
+}
+
 /* Number of OpenMP threads a parallel region of the oracle uses. */
 int oracle_num_threads(void)
 {

@@ -30,6 +30,7 @@ import numpy as np
 __all__ = [
     "uniform_pm1", "normal", "int_pattern", "stored_shape", "embed_padded",
     "Case", "CASES", "case", "make_case", "flops", "min_bytes", "HEADLINE",
+    "embed_batched", "make_batched", "BatchedCase", "BATCHED_CASES", "batched_case",
 ]
 
 
@@ -165,6 +166,109 @@ def make_case(c: Case, rows_a: int | None = None):
         out[name] = embed_padded(X, ld) if c.pad else X
         out["ld" + name.lower()] = ld
     return out
+
+
+def embed_batched(X: np.ndarray, ld: int, stride: int, fill: float = float("nan")) -> np.ndarray:
+    """Lay out a (batch, rows, cols) stack as a flat buffer: matrix b starts at
+    b*stride, rows ld apart; padding and gaps hold ``fill``.  stride 0 stores
+    the single matrix X[0] (one matrix shared by every product)."""
+    batch, rows, cols = X.shape
+    if ld < cols:
+        raise ValueError("ld < cols")
+    if stride == 0:
+        out = np.full(rows * ld, fill, dtype=np.float32)
+        out.reshape(rows, ld)[:, :cols] = X[0]
+        return out
+    if stride < rows * ld:
+        raise ValueError("stride smaller than one matrix")
+    out = np.full(max(batch - 1, 0) * stride + rows * ld, fill, dtype=np.float32)
+    for b in range(batch):
+        out[b * stride:b * stride + rows * ld].reshape(rows, ld)[:, :cols] = X[b]
+    return out
+
+
+def _round_up(x: int, a: int) -> int:
+    return (x + a - 1) // a * a
+
+
+def make_batched(batch: int, M: int, N: int, K: int, transA: str = "N", transB: str = "N", seed: int = 0,
+                 dist: str = "uniform", pad: int = 0, gap: int = 0, align: int = 4, shared: str = "",
+                 c_init: str = "uniform"):
+    """Operands of a strided batch of ``batch`` products, as flat float32 buffers.
+
+    Each stored matrix has ``pad`` extra floats per row; consecutive matrices
+    are ``rows*ld + gap`` floats apart, rounded up to a multiple of ``align``
+    (align=4 keeps every matrix 16-byte aligned).  ``shared`` may name "A"
+    and/or "B": that operand is one matrix with stride 0.  Padding and gaps
+    hold NaN, so a read of them poisons a result and a write to them shows.
+    Returns dict(A, B, C, lda, ldb, ldc, strideA, strideB, strideC, stacks)
+    where ``stacks`` holds the (batch, rows, cols) logical matrices.
+    """
+    a_shape = stored_shape(transA, M, K)
+    b_shape = stored_shape(transB, K, N)
+    nA = 1 if "A" in shared else batch
+    nB = 1 if "B" in shared else batch
+    if dist == "uniform":
+        A = uniform_pm1(nA * a_shape[0], a_shape[1], seed, 1)
+        B = uniform_pm1(nB * b_shape[0], b_shape[1], seed, 2)
+    elif dist == "fc":
+        A = normal(nA * a_shape[0], a_shape[1], seed, 1, 1.0)
+        B = normal(nB * b_shape[0], b_shape[1], seed, 2, 1.0 / math.sqrt(max(K, 1)))
+    else:
+        raise ValueError(dist)
+    A = A.reshape(nA, *a_shape)
+    B = B.reshape(nB, *b_shape)
+    if c_init == "uniform":
+        C = uniform_pm1(batch * M, N, seed, 3).reshape(batch, M, N)
+    else:
+        C = np.zeros((batch, M, N), dtype=np.float32)
+    out = {"stacks": {"A": A, "B": B, "C": C}}
+    for name, X, is_shared in (("A", A, "A" in shared), ("B", B, "B" in shared), ("C", C, False)):
+        rows, cols = X.shape[1:]
+        ld = cols + pad
+        stride = 0 if is_shared else _round_up(rows * ld + gap, align)
+        out[name] = embed_batched(X, ld, stride)
+        out["ld" + name.lower()] = ld
+        out["stride" + name] = stride
+    return out
+
+
+@dataclasses.dataclass(frozen=True)
+class BatchedCase:
+    """A strided batch of identical-shape products C_b = alpha op(A_b) op(B_b) + beta C_b."""
+    name: str
+    batch: int
+    M: int
+    N: int
+    K: int
+    transA: str = "N"
+    transB: str = "N"
+    alpha: float = 1.0
+    beta: float = 0.0
+    seed: int = 0
+    dist: str = "fc"
+    shared: str = ""
+
+    @property
+    def ops(self) -> str:
+        return self.transA + self.transB
+
+
+BATCHED_CASES: list[BatchedCase] = [
+    # many fully connected layers of one network size per call (itan.pw page, 概要)
+    BatchedCase("batched_fc_64x512x1024x1024", 64, 512, 1024, 1024, seed=21),
+    # one weight matrix shared by every product (stride 0 for B)
+    BatchedCase("batched_fc_shared_w_32x2048x1024x1024", 32, 2048, 1024, 1024, seed=22, shared="B"),
+    # many small products: the launch and tail overheads dominate
+    BatchedCase("batched_small_8192x64x64x64", 8192, 64, 64, 64, seed=23, dist="uniform"),
+]
+
+
+def batched_case(name: str) -> BatchedCase:
+    for c in BATCHED_CASES:
+        if c.name == name:
+            return c
+    raise KeyError(name)
 
 
 def flops(M: int, N: int, K: int) -> int:

@@ -16,7 +16,8 @@ import os
 import threading
 
 __all__ = [
-    "SgemmError", "load", "library_path", "sgemm", "sgemm_host", "sgemm_noalloc", "sgemm_plan", "sgemm_status_string",
+    "SgemmError", "load", "library_path", "sgemm", "sgemm_host", "sgemm_noalloc", "sgemm_plan",
+    "sgemm_strided_batched", "sgemm_plan_strided_batched", "sgemm_status_string",
     "sgemm_last_cuda_error", "sgemm_sync_status", "sgemm_set_variant_override",
     "sgemm_selftest_wait_timeout", "matmul", "VARIANTS", "STATUS",
 ]
@@ -72,6 +73,12 @@ def load() -> ctypes.CDLL:
         lib.sgemm_plan.restype = ctypes.c_int
         lib.sgemm_plan.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ctypes.c_int,
                                    ctypes.POINTER(PlanStruct)]
+        lib.sgemm_strided_batched.restype = ctypes.c_int
+        lib.sgemm_strided_batched.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                              i64, i64, i64, i64, vp]
+        lib.sgemm_plan_strided_batched.restype = ctypes.c_int
+        lib.sgemm_plan_strided_batched.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                                   i64, i64, i64, i64, ctypes.c_int, ctypes.POINTER(PlanStruct)]
         lib.sgemm_status_string.restype = ctypes.c_char_p
         lib.sgemm_status_string.argtypes = [ctypes.c_int]
         lib.sgemm_last_cuda_error.restype = ctypes.c_int
@@ -180,6 +187,32 @@ def sgemm_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, sm_
                            _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), int(sm_count), ctypes.byref(plan))
     if st != 0:
         raise SgemmError(st, "sgemm_plan")
+    out = {name: getattr(plan, name) for name, _ in PlanStruct._fields_}
+    out["variant_name"] = VARIANT_NAMES.get(out["variant"], str(out["variant"]))
+    return out
+
+
+def sgemm_strided_batched(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                          strideA, strideB, strideC, batch_count, stream=None, *, raise_on_error: bool = True) -> int:
+    """batch_count products C_b = alpha*op(A_b)*op(B_b) + beta*C_b with X_b = X + b*strideX (elements)."""
+    st = load().sgemm_strided_batched(_ch(transA), _ch(transB), int(M), int(N), int(K), float(alpha), _ptr(A),
+                                      int(lda), _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), int(strideA),
+                                      int(strideB), int(strideC), int(batch_count), _stream(stream))
+    if st != 0 and raise_on_error:
+        raise SgemmError(st, "sgemm_strided_batched")
+    return st
+
+
+def sgemm_plan_strided_batched(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                               strideA, strideB, strideC, batch_count, sm_count: int = 0) -> dict:
+    """The launch sgemm_strided_batched() would make.  Raises on invalid arguments."""
+    plan = PlanStruct()
+    st = load().sgemm_plan_strided_batched(_ch(transA), _ch(transB), int(M), int(N), int(K), float(alpha), _ptr(A),
+                                           int(lda), _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc),
+                                           int(strideA), int(strideB), int(strideC), int(batch_count),
+                                           int(sm_count), ctypes.byref(plan))
+    if st != 0:
+        raise SgemmError(st, "sgemm_plan_strided_batched")
     out = {name: getattr(plan, name) for name, _ in PlanStruct._fields_}
     out["variant_name"] = VARIANT_NAMES.get(out["variant"], str(out["variant"]))
     return out

@@ -35,11 +35,6 @@ struct DeviceState {
 };
 DeviceState g_devices[kMaxDevices];
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-std::once_flag g_encode_once;
-EncodeTiledFn g_encode = nullptr;
 
 int cuda_fail(cudaError_t e) {
   t_last_cuda_error = (int)e;
@@ -97,39 +92,6 @@ int device_state(int* device_out, DeviceState** st_out) {
   return SGEMM_OK;
 }
 
-int encode_fn(EncodeTiledFn* fn) {
-  static cudaError_t err = cudaSuccess;
-  std::call_once(g_encode_once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
-    if (err == cudaSuccess && q != cudaDriverEntryPointSuccess) err = cudaErrorNotSupported;
-    g_encode = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  if (err != cudaSuccess || !g_encode) return cuda_fail(err != cudaSuccess ? err : cudaErrorNotSupported);
-  *fn = g_encode;
-  return SGEMM_OK;
-}
-
-// 2-D float32 tensor map over a row-major matrix: `inner` contiguous elements
-// per row, `outer` rows, row stride `ld` elements; box {box_inner, box_outer}.
-int encode_2d(const float* base, int64_t inner, int64_t outer, int64_t ld, int box_inner, int box_outer,
-              bool swizzle128, CUtensorMap* map) {
-  EncodeTiledFn fn;
-  int st = encode_fn(&fn);
-  if (st != SGEMM_OK) return st;
-  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  const cuuint64_t strides[1] = {(cuuint64_t)ld * 4u};
-  const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
-  return SGEMM_OK;
-}
-
 struct Problem {
   int ta, tb;
   int64_t M, N, K;
@@ -138,6 +100,8 @@ struct Problem {
   const float* B;
   const float* C;
   int64_t lda, ldb, ldc;
+  int64_t stride_a = 0, stride_b = 0, stride_c = 0;  // strided batch (elements)
+  int64_t batch = 1;
 };
 
 int validate(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
@@ -160,6 +124,29 @@ int validate(char transA, char transB, int64_t M, int64_t N, int64_t K, float al
   return SGEMM_OK;
 }
 
+// Extra checks of a strided batch (argument indices of sgemm_strided_batched:
+// 14 strideA, 15 strideB, 16 strideC, 17 batch_count).  Strides may be 0
+// (one matrix shared by every product) or let A and B matrices overlap, but
+// the C matrices of different products must not overlap.
+int validate_batch(int64_t stride_a, int64_t stride_b, int64_t stride_c, int64_t batch, Problem* pr) {
+  if (stride_a < 0) return -14;
+  if (stride_b < 0) return -15;
+  if (stride_c < 0) return -16;
+  if (batch < 0) return -17;
+  if (batch > 1 && pr->M > 0 && pr->N > 0) {
+    const int64_t c_extent = (pr->M - 1) * pr->ldc + pr->N;  // elements one C matrix spans
+    if (stride_c < c_extent) return -16;
+    // every element offset of the last product must fit in int64
+    const int64_t lim = INT64_MAX / 2;
+    if (stride_a > lim / batch || stride_b > lim / batch || stride_c > lim / batch) return SGEMM_ERR_UNSUPPORTED;
+  }
+  pr->stride_a = stride_a;
+  pr->stride_b = stride_b;
+  pr->stride_c = stride_c;
+  pr->batch = batch;
+  return SGEMM_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -168,19 +155,26 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   *plan = sgemm_plan_t{};
   plan->split_k = 1;
-  if (pr.M == 0 || pr.N == 0) {
+  if (pr.M == 0 || pr.N == 0 || pr.batch == 0) {
     plan->variant = SGEMM_VARIANT_NONE;
     return SGEMM_OK;
   }
-  if (pr.M > INT_MAX || pr.N > INT_MAX || pr.K > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
+  if (pr.M > INT_MAX || pr.N > INT_MAX || pr.K > INT_MAX || pr.batch > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
   if (pr.K == 0 || pr.alpha == 0.0f) {
     plan->variant = SGEMM_VARIANT_SCALE;
     plan->kernel_launches = 1;
     plan->threads = 256;
     return SGEMM_OK;
   }
-  // TMA needs 16-byte aligned bases and row strides that are multiples of 16 bytes.
-  const bool tma_ok = aligned16(pr.A) && aligned16(pr.B) && pr.lda % 4 == 0 && pr.ldb % 4 == 0;
+  // TMA needs 16-byte aligned bases and row strides that are multiples of 16
+  // bytes; in a batch, every product's base too (a stride that is a multiple
+  // of 4 floats), and matrices that do not overlap (or one shared matrix).
+  const auto batch_ok = [&](int64_t stride, int64_t rows, int64_t ld) {
+    return pr.batch == 1 || stride == 0 || (stride % 4 == 0 && stride >= rows * ld);
+  };
+  const bool tma_ok = aligned16(pr.A) && aligned16(pr.B) && pr.lda % 4 == 0 && pr.ldb % 4 == 0 &&
+                      batch_ok(pr.stride_a, pr.ta ? pr.K : pr.M, pr.lda) &&
+                      batch_ok(pr.stride_b, pr.tb ? pr.N : pr.K, pr.ldb);
   // Default: the 3xTF32 tensor-core kernel whenever TMA can load the operands
   // (it beats the FP32 FFMA kernels on every measured shape); the generic
   // SIMT kernel otherwise.  The FFMA kernels stay selectable by override.
@@ -204,7 +198,8 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
     using T = tma::Tile<2, 4>;
     bm = T::BM; bn = T::BN; bk = tma::kBK; threads = tma::kThreads; stages = tma::kStages; smem = T::SMEM_BYTES;
   }
-  const int64_t tiles = ceil_div(pr.M, bm) * ceil_div(pr.N, bn);
+  // output tiles of all products (the grid's x extent)
+  const int64_t tiles = ceil_div(pr.M, bm) * ceil_div(pr.N, bn) * pr.batch;
   const int64_t kt = ceil_div(pr.K, bk);
   if (tiles > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
 
@@ -229,7 +224,7 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   plan->grid_x = tiles;
   plan->grid_y = split;
   plan->smem_bytes = smem;
-  plan->workspace_bytes = split > 1 ? split * pr.M * (ceil_div(pr.N, 4) * 4) * 4 : 0;
+  plan->workspace_bytes = split > 1 ? pr.batch * split * pr.M * (ceil_div(pr.N, 4) * 4) * 4 : 0;
   return SGEMM_OK;
 }
 
@@ -247,7 +242,11 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   p.lda = pr.lda;
   p.ldb = pr.ldb;
   p.ldc = pr.ldc;
-  p.c_vec = aligned16(C) && pr.ldc % 4 == 0;
+  p.c_vec = aligned16(C) && pr.ldc % 4 == 0 && (pr.batch == 1 || pr.stride_c % 4 == 0);
+  p.batch = (int)pr.batch;
+  p.stride_a = pr.stride_a;
+  p.stride_b = pr.stride_b;
+  p.stride_c = pr.stride_c;
   p.timeout_ns = wait_timeout_ns();
   p.fault = st.fault;
 
@@ -264,16 +263,10 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
 
   CUtensorMap mapA, mapB;
   if (plan.variant != SGEMM_VARIANT_GENERIC) {
-    const int bm = plan.tile_m, bn = plan.tile_n, bk = plan.tile_k;
-    // op(A): 'N' -> stored M x K, K contiguous (swizzled K-major tile);
-    //        'T' -> stored K x M, M contiguous.
-    int s = pr.ta ? encode_2d(pr.A, pr.M, pr.K, pr.lda, bm, bk, false, &mapA)
-                  : encode_2d(pr.A, pr.K, pr.M, pr.lda, bk, bm, true, &mapA);
-    if (s != SGEMM_OK) return s;
-    // op(B): 'N' -> stored K x N, N contiguous; 'T' -> stored N x K, K contiguous (swizzled).
-    s = pr.tb ? encode_2d(pr.B, pr.K, pr.N, pr.ldb, bk, bn, true, &mapB)
-              : encode_2d(pr.B, pr.N, pr.K, pr.ldb, bn, bk, false, &mapB);
-    if (s != SGEMM_OK) return s;
+    cudaError_t e = encode_operand_maps(pr.ta, pr.tb, pr.M, pr.N, pr.K, pr.A, pr.lda, pr.stride_a, pr.B, pr.ldb,
+                                        pr.stride_b, p.batch, plan.tile_m, plan.tile_n, plan.tile_k, &mapA, &mapB,
+                                        &p.za, &p.zb);
+    if (e != cudaSuccess) return cuda_fail(e);
   }
 
   void* ws = nullptr;
@@ -343,6 +336,46 @@ int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float 
   return make_plan(pr, sm_count, plan);
 }
 
+int sgemm_strided_batched(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                          int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+                          int64_t strideA, int64_t strideB, int64_t strideC, int64_t batch_count,
+                          struct CUstream_st* stream) {
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  s = validate_batch(strideA, strideB, strideC, batch_count, &pr);
+  if (s != SGEMM_OK) return s;
+  if (M == 0 || N == 0 || batch_count == 0) return SGEMM_OK;
+  int dev;
+  DeviceState* st;
+  s = device_state(&dev, &st);
+  if (s != SGEMM_OK) return s;
+  sgemm_plan_t plan;
+  s = make_plan(pr, st->sm_count, &plan);
+  if (s != SGEMM_OK) return s;
+  return launch_gemm(pr, plan, *st, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_plan_strided_batched(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
+                               const float* A, int64_t lda, const float* B, int64_t ldb, float beta, const float* C,
+                               int64_t ldc, int64_t strideA, int64_t strideB, int64_t strideC, int64_t batch_count,
+                               int sm_count, sgemm_plan_t* plan) {
+  if (!plan) return -19;
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  s = validate_batch(strideA, strideB, strideC, batch_count, &pr);
+  if (s != SGEMM_OK) return s;
+  if (sm_count <= 0) {
+    int dev;
+    DeviceState* st;
+    s = device_state(&dev, &st);
+    if (s != SGEMM_OK) return s;
+    sm_count = st->sm_count;
+  }
+  return make_plan(pr, sm_count, plan);
+}
+
 int sgemm_set_variant_override(int variant, int split_k) {
   if (variant != SGEMM_VARIANT_AUTO && variant != SGEMM_VARIANT_GENERIC && variant != SGEMM_VARIANT_TMA_128x128 &&
       variant != SGEMM_VARIANT_TMA_64x256 && variant != SGEMM_VARIANT_TC_TF32X3)
@@ -372,7 +405,11 @@ const char* sgemm_status_string(int status) {
     case -10: return "invalid argument 10 (ldb too small)";
     case -12: return "invalid argument 12 (C is NULL)";
     case -13: return "invalid argument 13 (ldc too small)";
-    case -15: return "invalid argument 15 (plan is NULL)";
+    case -14: return "invalid argument 14 (strideA < 0)";
+    case -15: return "invalid argument 15 (plan is NULL, or strideB < 0 in the batched calls)";
+    case -16: return "invalid argument 16 (strideC < 0, or C matrices of a batch overlap)";
+    case -17: return "invalid argument 17 (batch_count < 0)";
+    case -19: return "invalid argument 19 (plan is NULL)";
     default: return status < 0 ? "invalid argument" : "unknown status";
   }
 }

@@ -90,15 +90,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   return mbar_wait_slow(bar, parity, timeout_ns);
 }
 
-// 2-D TMA tile load into shared memory; completion is signalled on `bar` as
-// transaction bytes.  Coordinates are element indices {inner, outer}; the
-// tensor map zero-fills any part of the box outside the tensor.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t inner, int32_t outer) {
+// TMA tile load from a 3-D map {inner, outer, product} into shared memory;
+// completion is signalled on `bar` as transaction bytes.  Coordinates are
+// element indices; the tensor map zero-fills any part of the box outside the
+// tensor.  `inner` times 4 bytes must be a multiple of 16 (tile origins are).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t inner, int32_t outer, int32_t product) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(inner), "r"(outer)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(inner), "r"(outer), "r"(product)
       : "memory");
 }
 

@@ -18,23 +18,27 @@ __device__ __forceinline__ float epilogue(float alpha, float beta, float v, cons
 
 // Sums the split partial tiles in slice order 0, 1, ..., split-1 (a fixed
 // order, so the result does not depend on scheduling), then applies
-// C = alpha * sum + beta * C.  One thread per 4 consecutive columns.
+// C = alpha * sum + beta * C.  One thread per 4 consecutive columns of one
+// row of one product; the workspace is [product][slice][M][ws_ld].
 template <bool CVEC>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p, int split) {
   const int64_t groups = (p.N + 3) / 4;
-  const int64_t total = (int64_t)p.M * groups;
+  const int64_t per_product = (int64_t)p.M * groups;
+  const int64_t total = per_product * p.batch;
   const int64_t slice = (int64_t)p.M * p.ws_ld;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
        g += (int64_t)gridDim.x * blockDim.x) {
-    const int row = (int)(g / groups);
-    const int col = (int)(g % groups) * 4;
-    const float* w = p.ws + (int64_t)row * p.ws_ld + col;
+    const int64_t prod = g / per_product;
+    const int64_t r = g - prod * per_product;
+    const int row = (int)(r / groups);
+    const int col = (int)(r % groups) * 4;
+    const float* w = p.ws + prod * split * slice + (int64_t)row * p.ws_ld + col;
     float4 v = *reinterpret_cast<const float4*>(w);
     for (int z = 1; z < split; ++z) {
       const float4 u = *reinterpret_cast<const float4*>(w + z * slice);
       v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
     }
-    float* c = p.C + (int64_t)row * p.ldc + col;
+    float* c = p.C + prod * p.stride_c + (int64_t)row * p.ldc + col;
     if (CVEC && col + 3 < p.N) {
       float4 o;
       if (p.beta == 0.0f) {
@@ -54,12 +58,15 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p, 
   }
 }
 
-// C = beta * C; with beta == 0, C = 0 without reading C.
+// C = beta * C (every product); with beta == 0, C = 0 without reading C.
 __global__ void __launch_bounds__(256) scale_kernel(const GemmParams p) {
-  const int64_t total = (int64_t)p.M * p.N;
+  const int64_t per_product = (int64_t)p.M * p.N;
+  const int64_t total = per_product * p.batch;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
-    float* c = p.C + (e / p.N) * p.ldc + (e % p.N);
+    const int64_t prod = e / per_product;
+    const int64_t r = e - prod * per_product;
+    float* c = p.C + prod * p.stride_c + (r / p.N) * p.ldc + (r % p.N);
     *c = p.beta == 0.0f ? 0.0f : p.beta * *c;
   }
 }
@@ -87,7 +94,7 @@ unsigned grid_for(int64_t work, int per_block) {
 }  // namespace
 
 cudaError_t launch_splitk_reduce(const GemmParams& p, int split, cudaStream_t stream) {
-  const int64_t work = (int64_t)p.M * ((p.N + 3) / 4);
+  const int64_t work = (int64_t)p.batch * p.M * ((p.N + 3) / 4);
   if (p.c_vec)
     splitk_reduce_kernel<true><<<grid_for(work, 256), 256, 0, stream>>>(p, split);
   else
@@ -96,7 +103,7 @@ cudaError_t launch_splitk_reduce(const GemmParams& p, int split, cudaStream_t st
 }
 
 cudaError_t launch_scale(const GemmParams& p, cudaStream_t stream) {
-  scale_kernel<<<grid_for((int64_t)p.M * p.N, 256), 256, 0, stream>>>(p);
+  scale_kernel<<<grid_for((int64_t)p.batch * p.M * p.N, 256), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

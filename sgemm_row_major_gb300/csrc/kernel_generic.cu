@@ -29,7 +29,12 @@ __global__ void __launch_bounds__(GTHREADS) generic_gemm_kernel(const GemmParams
 
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
-  const int tm = blockIdx.x / p.tiles_n, tn = blockIdx.x % p.tiles_n;
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int prod = (int)(blockIdx.x / (unsigned)tiles);  // product of a strided batch
+  const int tile = (int)(blockIdx.x - (unsigned)(prod * tiles));
+  const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
+  const float* __restrict__ Ab = p.A + (int64_t)prod * p.stride_a;
+  const float* __restrict__ Bb = p.B + (int64_t)prod * p.stride_b;
   const int m0 = tm * GBM, n0 = tn * GBN;
   const int kt_total = (p.K + GBK - 1) / GBK;
   const int kt0 = blockIdx.y * p.k_tiles_per_split;
@@ -45,13 +50,13 @@ __global__ void __launch_bounds__(GTHREADS) generic_gemm_kernel(const GemmParams
       else     { mm = tid & 63; kk = (tid >> 6) + 4 * r; }    // consecutive threads walk m
       const int gm = m0 + mm, gk = k0 + kk;
       ra[r] = (gm < p.M && gk < p.K)
-                  ? (TA ? p.A[(int64_t)gk * p.lda + gm] : p.A[(int64_t)gm * p.lda + gk]) : 0.0f;
+                  ? (TA ? Ab[(int64_t)gk * p.lda + gm] : Ab[(int64_t)gm * p.lda + gk]) : 0.0f;
       int nn;
       if (!TB) { nn = tid & 63; kk = (tid >> 6) + 4 * r; }
       else     { kk = tid & 15; nn = (tid >> 4) + 16 * r; }
       const int gn = n0 + nn, gk2 = k0 + kk;
       rb[r] = (gn < p.N && gk2 < p.K)
-                  ? (TB ? p.B[(int64_t)gn * p.ldb + gk2] : p.B[(int64_t)gk2 * p.ldb + gn]) : 0.0f;
+                  ? (TB ? Bb[(int64_t)gn * p.ldb + gk2] : Bb[(int64_t)gk2 * p.ldb + gn]) : 0.0f;
     }
   };
   auto store = [&](int buf) {
@@ -113,9 +118,9 @@ __global__ void __launch_bounds__(GTHREADS) generic_gemm_kernel(const GemmParams
       if (col >= p.N) continue;
       const float v = mst[i][j] + acc[i][j];
       if (SPLIT) {
-        p.ws[((int64_t)blockIdx.y * p.M + row) * p.ws_ld + col] = v;
+        p.ws[(((int64_t)prod * gridDim.y + blockIdx.y) * p.M + row) * p.ws_ld + col] = v;
       } else {
-        float* c = p.C + (int64_t)row * p.ldc + col;
+        float* c = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
         *c = epilogue(p.alpha, p.beta, v, c);
       }
     }
@@ -124,7 +129,7 @@ __global__ void __launch_bounds__(GTHREADS) generic_gemm_kernel(const GemmParams
 
 template <bool TA, bool TB>
 cudaError_t launch_one(const GemmParams& p, int split, cudaStream_t stream) {
-  dim3 grid((unsigned)(p.tiles_m * p.tiles_n), (unsigned)split);
+  dim3 grid((unsigned)((int64_t)p.batch * p.tiles_m * p.tiles_n), (unsigned)split);
   if (split > 1)
     generic_gemm_kernel<TA, TB, true><<<grid, GTHREADS, 0, stream>>>(p);
   else

@@ -156,6 +156,7 @@ __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, i
 //   op(A) 'N': [128 rows of M][32 k], K contiguous, 128-byte swizzle;  'T': [32 k][128 m], M contiguous.
 //   op(B) 'N': [32 k][128 n], N contiguous;  'T': [128 n][32 k], K contiguous, 128-byte swizzle.
 // SPLIT: write the raw sums of this CTA's K slice (blockIdx.y) to the workspace instead of C.
+// blockIdx.x = product * tiles + output tile (a strided batch of products).
 template <bool TA, bool TB, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
@@ -179,9 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int prod = (int)(blockIdx.x / (unsigned)tiles);  // product of a strided batch
   int tm, tn;
-  tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
+  tile_coords((int)(blockIdx.x - (unsigned)(prod * tiles)), p.tiles_m, p.tiles_n, tm, tn);
   const int m0 = tm * BM, n0 = tn * BN;
+  const int za = prod * p.za, zb = prod * p.zb;
   const int kt_total = (p.K + BK - 1) / BK;
   const int kt0 = blockIdx.y * p.k_tiles_per_split;
   const int nkt = min(kt_total, kt0 + p.k_tiles_per_split) - kt0;  // >= 1 by construction
@@ -223,10 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t fb = smem_addr(&raw_full[r]);
         mbar_arrive_expect_tx(fb, (uint32_t)kRawBytes);
         const int k0 = (kt0 + t) * BK;
-        if (!TA) tma_load_2d(raw_a(r), &mapA, fb, k0, m0);
-        else     tma_load_2d(raw_a(r), &mapA, fb, m0, k0);
-        if (!TB) tma_load_2d(raw_b(r), &mapB, fb, n0, k0);
-        else     tma_load_2d(raw_b(r), &mapB, fb, k0, n0);
+        if (!TA) tma_load_3d(raw_a(r), &mapA, fb, k0, m0, za);
+        else     tma_load_3d(raw_a(r), &mapA, fb, m0, k0, za);
+        if (!TB) tma_load_3d(raw_b(r), &mapB, fb, n0, k0, zb);
+        else     tma_load_3d(raw_b(r), &mapB, fb, k0, n0, zb);
         issued = t + 1;
       }
       // leave only when every copy into shared memory has landed
@@ -408,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = m0 + 32 * q + lane;
       if (row < p.M) {
         if (SPLIT) {
-          float* wrow = p.ws + ((int64_t)blockIdx.y * p.M + row) * p.ws_ld;
+          float* wrow = p.ws + (((int64_t)prod * gridDim.y + blockIdx.y) * p.M + row) * p.ws_ld;
 #pragma unroll
           for (int g = 0; g < 16; ++g) {
             const int col = n0 + 64 * half + 4 * g;
@@ -417,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   make_float4(master[4 * g], master[4 * g + 1], master[4 * g + 2], master[4 * g + 3]);
           }
         } else {
-          float* crow = p.C + (int64_t)row * p.ldc;
+          float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
 #pragma unroll
           for (int g = 0; g < 16; ++g) {
             const int col = n0 + 64 * half + 4 * g;
@@ -466,7 +470,7 @@ cudaError_t set_attrs() {
 template <bool TA, bool TB>
 cudaError_t launch(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p, int split,
                    cudaStream_t stream) {
-  const dim3 grid((unsigned)(p.tiles_m * p.tiles_n), (unsigned)split);
+  const dim3 grid((unsigned)((int64_t)p.batch * p.tiles_m * p.tiles_n), (unsigned)split);
   if (split > 1)
     tc::tf32x3_gemm_kernel<TA, TB, true><<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB, p);
   else

@@ -189,12 +189,13 @@ __device__ __forceinline__ void fold_into_tmem(uint32_t taddr, float2 (&acc)[8][
 }
 
 // C = alpha * v + beta * C for the thread's 8x8 block (v[8i + j] is row i,
-// column j of the block), or the raw sums into slice blockIdx.y of the
-// split-K workspace.  C is not read when beta == 0; 128-bit accesses where
-// the 4 columns are in range and C allows it.
+// column j of the block), or the raw sums into this CTA's slice of the
+// split-K workspace.  `cm` is this product's C, `wm_base` its workspace slice
+// (both row 0).  C is not read when beta == 0; 128-bit accesses where the 4
+// columns are in range and C allows it.
 template <int WM, int WN, bool TA, bool TB, bool SPLIT>
-__device__ __forceinline__ void epilogue(const GemmParams& p, int m0, int n0, int wm, int wn, int ty, int tx,
-                                         const float (&v)[64]) {
+__device__ __forceinline__ void epilogue(const GemmParams& p, float* cm, float* wm_base, int m0, int n0, int wm,
+                                         int wn, int ty, int tx, const float (&v)[64]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int row = m0 + row_of<TA>(i, wm, ty);
@@ -206,12 +207,12 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int m0, int n0, in
         const float* x = &v[8 * i + 4 * h];
         if (SPLIT) {
           if (col < p.N) {
-            float* w = p.ws + ((int64_t)blockIdx.y * p.M + row) * p.ws_ld + col;
+            float* w = wm_base + (int64_t)row * p.ws_ld + col;
             *reinterpret_cast<float4*>(w) = make_float4(x[0], x[1], x[2], x[3]);
           }
           continue;
         }
-        float* c = p.C + (int64_t)row * p.ldc + col;
+        float* c = cm + (int64_t)row * p.ldc + col;
         if (p.c_vec && col + 3 < p.N) {
           float4 o;
           if (p.beta == 0.0f) {
@@ -235,9 +236,9 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int m0, int n0, in
         if (col >= p.N) continue;
         const float x = v[8 * i + j];
         if (SPLIT) {
-          p.ws[((int64_t)blockIdx.y * p.M + row) * p.ws_ld + col] = x;
+          wm_base[(int64_t)row * p.ws_ld + col] = x;
         } else {
-          float* c = p.C + (int64_t)row * p.ldc + col;
+          float* c = cm + (int64_t)row * p.ldc + col;
           *c = p.beta == 0.0f ? p.alpha * x : fmaf(p.alpha, x, p.beta * *c);
         }
       }
@@ -263,10 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int prod = (int)(blockIdx.x / (unsigned)tiles);  // product of a strided batch
   int tm, tn;
-  tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
+  tile_coords((int)(blockIdx.x - (unsigned)(prod * tiles)), p.tiles_m, p.tiles_n, tm, tn);
   const int m0 = tm * T::BM;
   const int n0 = tn * T::BN;
+  const int za = prod * p.za, zb = prod * p.zb;
   const int kt_total = (p.K + kBK - 1) / kBK;
   const int kt0 = blockIdx.y * p.k_tiles_per_split;
   const int nkt = min(kt_total, kt0 + p.k_tiles_per_split) - kt0;  // >= 1 by construction
@@ -293,10 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_dst = a_dst + (uint32_t)T::A_BYTES;
     const int k0 = (kt0 + t) * kBK;
     mbar_arrive_expect_tx(fb, (uint32_t)T::STAGE_BYTES);
-    if (!TA) tma_load_2d(a_dst, &mapA, fb, k0, m0);
-    else     tma_load_2d(a_dst, &mapA, fb, m0, k0);
-    if (!TB) tma_load_2d(b_dst, &mapB, fb, n0, k0);
-    else     tma_load_2d(b_dst, &mapB, fb, k0, n0);
+    if (!TA) tma_load_3d(a_dst, &mapA, fb, k0, m0, za);
+    else     tma_load_3d(a_dst, &mapA, fb, m0, k0, za);
+    if (!TB) tma_load_3d(b_dst, &mapB, fb, n0, k0, zb);
+    else     tma_load_3d(b_dst, &mapB, fb, k0, n0, zb);
   };
   const bool producer = threadIdx.x == 0;
   int issued = 0;  // K tiles whose loads thread 0 has issued
@@ -406,7 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         fin[8 * i + 2 * q] += acc[i][q].x;
         fin[8 * i + 2 * q + 1] += acc[i][q].y;
       }
-    epilogue<WM, WN, TA, TB, SPLIT>(p, m0, n0, wm, wn, ty, tx, fin);
+    epilogue<WM, WN, TA, TB, SPLIT>(p, p.C + (int64_t)prod * p.stride_c,
+                                    p.ws + ((int64_t)prod * gridDim.y + blockIdx.y) * p.M * p.ws_ld, m0, n0, wm,
+                                    wn, ty, tx, fin);
   } else if (producer) {
     // A wait gave up.  Thread 0 must not leave while copies it issued into this
     // CTA's shared memory may still land: wait (bounded) for the last phase of
@@ -427,7 +433,7 @@ template <int WM, int WN, bool TA, bool TB>
 cudaError_t launch(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p, int split,
                    cudaStream_t stream) {
   using T = Tile<WM, WN>;
-  dim3 grid((unsigned)(p.tiles_m * p.tiles_n), (unsigned)split);
+  dim3 grid((unsigned)((int64_t)p.batch * p.tiles_m * p.tiles_n), (unsigned)split);
   if (split > 1)
     tma_gemm_kernel<WM, WN, TA, TB, true><<<grid, kThreads, T::SMEM_BYTES, stream>>>(mapA, mapB, p);
   else

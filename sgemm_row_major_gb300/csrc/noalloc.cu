@@ -45,10 +45,6 @@ struct NoallocDevice {
 };
 NoallocDevice g_nd[kMaxDevices];
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 // Per-device set-up, once, with the device current: SM count, fault word,
 // scratch address and kernel attributes.  No allocation happens here.
 cudaError_t setup(int dev, NoallocDevice** out) {
@@ -66,29 +62,6 @@ cudaError_t setup(int dev, NoallocDevice** out) {
   });
   *out = &d;
   return d.err;
-}
-
-cudaError_t encode_2d(const float* base, int64_t inner, int64_t outer, int64_t ld, int box_inner, int box_outer,
-                      bool swizzle128, CUtensorMap* map) {
-  static EncodeTiledFn fn = nullptr;
-  static cudaError_t fn_err = cudaSuccess;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    fn_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
-    if (fn_err == cudaSuccess && (q != cudaDriverEntryPointSuccess || !p)) fn_err = cudaErrorNotSupported;
-    fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  if (fn_err != cudaSuccess) return fn_err;
-  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  const cuuint64_t strides[1] = {(cuuint64_t)ld * 4u};
-  const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -149,10 +122,8 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
     e = launch_generic_gemm(ta, tb, p, split, cs);
   } else {
     CUtensorMap mapA, mapB;
-    const int bm = plan.tile_m, bn = plan.tile_n, bk = plan.tile_k;
-    e = ta ? encode_2d(A, M, K, lda, bm, bk, false, &mapA) : encode_2d(A, K, M, lda, bk, bm, true, &mapA);
-    if (e == cudaSuccess)
-      e = tb ? encode_2d(B, K, N, ldb, bk, bn, true, &mapB) : encode_2d(B, N, K, ldb, bn, bk, false, &mapB);
+    e = encode_operand_maps(ta, tb, M, N, K, A, lda, 0, B, ldb, 0, 1, plan.tile_m, plan.tile_n, plan.tile_k, &mapA,
+                            &mapB, &p.za, &p.zb);
     if (e != cudaSuccess) return SGEMM_ERR_CUDA;
     const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
     if (plan.variant == SGEMM_VARIANT_TC_TF32X3) e = launch_tf32x3(ta, tb, mapA, mapB, p, split, cs);

@@ -8,20 +8,38 @@
 namespace sgemm_impl {
 
 // Everything a GEMM kernel needs besides its tensor maps.
+//
+// A call computes `batch` independent products; product b reads
+// A + b*stride_a, B + b*stride_b and updates C + b*stride_c.  Grid: x =
+// batch * tiles_m * tiles_n (CTA x works on product x / tiles, output tile
+// x % tiles), y = K slices.
 struct GemmParams {
-  int M, N, K;
-  float alpha, beta;
-  const float* A;  // used by the generic kernel (the TMA kernel reads through tensor maps)
-  const float* B;
-  float* C;        // final output (split == 1) ...
-  float* ws;       // ... or the partial-sum workspace [split][M][ws_ld] (split > 1)
-  int64_t lda, ldb, ldc, ws_ld;
-  int k_tiles_per_split;  // K tiles (of the kernel's BK) per slice
-  int tiles_m, tiles_n;   // output tiles
-  int c_vec;              // 1: C is 16-byte aligned and ldc % 4 == 0
-  uint64_t timeout_ns;    // limit of every in-kernel wait
-  unsigned* fault;        // device fault word (bits of FaultBits), see fault_word()
+  int M = 0, N = 0, K = 0;
+  float alpha = 1.0f, beta = 0.0f;
+  const float* A = nullptr;  // used by the generic kernel (the TMA kernels read through tensor maps)
+  const float* B = nullptr;
+  float* C = nullptr;        // final output (split == 1) ...
+  float* ws = nullptr;       // ... or the partial-sum workspace [batch][split][M][ws_ld] (split > 1)
+  int64_t lda = 0, ldb = 0, ldc = 0, ws_ld = 0;
+  int64_t stride_a = 0, stride_b = 0, stride_c = 0;  // elements between consecutive products
+  int batch = 1;
+  int za = 0, zb = 0;            // TMA kernels: 1 = the map's third coordinate is the product index
+  int k_tiles_per_split = 0;     // K tiles (of the kernel's BK) per slice
+  int tiles_m = 0, tiles_n = 0;  // output tiles of one product
+  int c_vec = 0;                 // 1: C (every product) is 16-byte aligned and ldc % 4 == 0
+  uint64_t timeout_ns = 0;       // limit of every in-kernel wait
+  unsigned* fault = nullptr;     // device fault word (bits of FaultBits), see fault_word()
 };
+
+// Tensor maps of the operands of a TMA-fed kernel: 3-D {contiguous, rows,
+// product} float32 maps over the stored A and B, boxes of the kernel's tile
+// (A: bm x bk of op(A), B: bk x bn of op(B)), 128-byte swizzle where a box
+// row is 32 floats of K (K-major tiles), none otherwise.  A map whose stride
+// is 0 or whose call has one product gets a product extent of 1 and its z flag
+// (GemmParams::za / zb) is 0.  Returns the encode error.
+cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                                int64_t stride_a, const float* B, int64_t ldb, int64_t stride_b, int batch,
+                                int bm, int bn, int bk, CUtensorMap* mapA, CUtensorMap* mapB, int* za, int* zb);
 
 // Shapes of the TMA-fed SIMT kernel.
 enum class TmaTile { k128x128, k64x256 };

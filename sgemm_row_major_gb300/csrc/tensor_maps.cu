@@ -1,0 +1,75 @@
+// tensor_maps.cu -- TMA tensor maps of the GEMM operands (host code).
+//
+// Every TMA-fed kernel reads A and B through 3-D float32 maps {contiguous
+// elements of a stored row, stored rows, product index}.  A single product
+// (sgemm) is the case of a product extent of 1; a strided batch gives the
+// third dimension the batch count and the batch stride, so one map serves
+// every product of the call and a kernel only changes the third coordinate.
+#include <mutex>
+
+#include "sgemm_internal.h"
+
+namespace sgemm_impl {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t encode_fn(EncodeTiledFn* out) {
+  static EncodeTiledFn fn = nullptr;
+  static cudaError_t err = cudaSuccess;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && (q != cudaDriverEntryPointSuccess || !p)) err = cudaErrorNotSupported;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  *out = fn;
+  return err;
+}
+
+// Map over `products` row-major matrices of `outer` rows x `inner` contiguous
+// floats, row stride `ld`, product stride `stride` (elements); box
+// {box_inner, box_outer, 1}.
+cudaError_t encode_3d(const float* base, int64_t inner, int64_t outer, int64_t ld, int64_t products,
+                      int64_t stride, int box_inner, int box_outer, bool swizzle128, CUtensorMap* map) {
+  EncodeTiledFn fn = nullptr;
+  cudaError_t e = encode_fn(&fn);
+  if (e != cudaSuccess) return e;
+  if (products <= 1) {
+    products = 1;
+    stride = outer * ld;  // unused with one product, but must be a valid stride
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)products};
+  const cuuint64_t strides[2] = {(cuuint64_t)ld * 4u, (cuuint64_t)stride * 4u};
+  const cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1u};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                                int64_t stride_a, const float* B, int64_t ldb, int64_t stride_b, int batch,
+                                int bm, int bn, int bk, CUtensorMap* mapA, CUtensorMap* mapB, int* za, int* zb) {
+  const int64_t pa = (batch > 1 && stride_a != 0) ? batch : 1;
+  const int64_t pb = (batch > 1 && stride_b != 0) ? batch : 1;
+  *za = pa > 1 ? 1 : 0;
+  *zb = pb > 1 ? 1 : 0;
+  // op(A): 'N' -> stored M x K, K contiguous (swizzled K-major tile);
+  //        'T' -> stored K x M, M contiguous.
+  cudaError_t e = ta ? encode_3d(A, M, K, lda, pa, stride_a, bm, bk, false, mapA)
+                     : encode_3d(A, K, M, lda, pa, stride_a, bk, bm, true, mapA);
+  if (e != cudaSuccess) return e;
+  // op(B): 'N' -> stored K x N, N contiguous; 'T' -> stored N x K, K contiguous (swizzled).
+  return tb ? encode_3d(B, K, N, ldb, pb, stride_b, bk, bn, true, mapB)
+            : encode_3d(B, N, K, ldb, pb, stride_b, bn, bk, false, mapB);
+}
+
+}  // namespace sgemm_impl

@@ -280,9 +280,66 @@ def pin_conjugate_is_transpose(lib):
     assert np.array_equal(oracle.sgemm("n", "t", An, B, lib=lib), oracle.sgemm("N", "T", An, B, lib=lib))
 
 
+def _dyadic_stack(rng, n, rows, cols, bits=6):
+    scale = 2 ** bits
+    return (rng.integers(-scale, scale, size=(n, rows, cols)) / scale).astype(np.float32)
+
+
+def pin_batched_dyadic(lib):
+    """Strided batch: each product equals a float64 einsum over the stacked
+    dyadic operands (exact), for every op, with odd strides, NaN gaps between
+    matrices (never read, never written) and one shared operand (stride 0);
+    S of product b is that product's |alpha| |A_b|@|B_b| + |beta C_b|."""
+    rng = np.random.default_rng(18)
+    batch, M, N, K = 4, 5, 6, 7
+    alpha, beta = -1.5, 0.5
+    for (ta, tb), shared in itertools.product(OPS, ("", "A", "B")):
+        a_shape, b_shape = si.stored_shape(ta, M, K), si.stored_shape(tb, K, N)
+        A = _dyadic_stack(rng, 1 if shared == "A" else batch, *a_shape)
+        B = _dyadic_stack(rng, 1 if shared == "B" else batch, *b_shape)
+        C = _dyadic_stack(rng, batch, M, N)
+        lda, ldb, ldc = a_shape[1] + 1, b_shape[1] + 2, N + 3
+        sa = 0 if shared == "A" else a_shape[0] * lda + 5
+        sb = 0 if shared == "B" else b_shape[0] * ldb + 3
+        sc = M * ldc + 1
+        Af, Bf, Cf = si.embed_batched(A, lda, sa), si.embed_batched(B, ldb, sb), si.embed_batched(C, ldc, sc)
+        out, S = oracle.sgemm_strided_batched(ta, tb, M, N, K, alpha, Af, lda, sa, Bf, ldb, sb, beta, Cf, ldc, sc,
+                                              batch, want_bound=True, lib=lib)
+        opA = np.stack([_op(A[0 if shared == "A" else b], ta) for b in range(batch)]).astype(np.float64)
+        opB = np.stack([_op(B[0 if shared == "B" else b], tb) for b in range(batch)]).astype(np.float64)
+        ref = (alpha * np.einsum("bik,bkj->bij", opA, opB) + beta * C.astype(np.float64)).astype(np.float32)
+        want = si.embed_batched(ref, ldc, sc)
+        assert np.array_equal(out, want, equal_nan=True), (ta, tb, shared)
+        sref = abs(alpha) * np.einsum("bik,bkj->bij", np.abs(opA), np.abs(opB)) + abs(beta) * np.abs(C)
+        assert np.array_equal(S, sref), (ta, tb, shared)
+
+
+def pin_batched_edges(lib):
+    """batch_count 0 leaves C untouched; one product equals the plain SGEMM;
+    negative strides or counts are rejected."""
+    rng = np.random.default_rng(19)
+    A = _dyadic_stack(rng, 1, 4, 3)
+    B = _dyadic_stack(rng, 1, 3, 5)
+    C = _dyadic_stack(rng, 1, 4, 5)
+    Af, Bf, Cf = A.ravel(), B.ravel(), C.ravel()
+    out = oracle.sgemm_strided_batched("N", "N", 4, 5, 3, 1.0, Af, 3, 12, Bf, 5, 15, 2.0, Cf, 5, 20, 0, lib=lib)
+    assert np.array_equal(out, Cf)
+    one = oracle.sgemm_strided_batched("N", "N", 4, 5, 3, 1.0, Af, 3, 12, Bf, 5, 15, 2.0, Cf, 5, 20, 1, lib=lib)
+    ref = (A[0].astype(np.float64) @ B[0].astype(np.float64) + 2.0 * C[0]).astype(np.float32)
+    assert np.array_equal(one.reshape(4, 5), ref)
+    for bad in ((-1, 15, 20, 2), (12, -1, 20, 2), (12, 15, -1, 2), (12, 15, 20, -1)):
+        try:
+            oracle.sgemm_strided_batched("N", "N", 4, 5, 3, 1.0, Af, 3, bad[0], Bf, 5, bad[1], 2.0, Cf, 5, bad[2],
+                                         bad[3], lib=lib)
+        except oracle.OracleError:
+            continue
+        raise AssertionError(f"accepted {bad}")
+
+
 ALL_PINS = [
     pin_hand_2x2, pin_bruteforce_tiny, pin_integer_pattern, pin_integer_alpha_beta, pin_k1_exact,
     pin_alpha_zero, pin_k_zero, pin_beta_zero_nan_c, pin_identity, pin_transpose_identity,
     pin_transposed_copy, pin_alpha_pow2, pin_padding_not_read, pin_random_vs_float64_matmul,
-    pin_bound_magnitude, pin_argument_errors, pin_conjugate_is_transpose,
+    pin_bound_magnitude, pin_argument_errors, pin_conjugate_is_transpose, pin_batched_dyadic,
+    pin_batched_edges,
 ]

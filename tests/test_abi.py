@@ -144,3 +144,55 @@ def test_plan_rejects_huge_dimensions(lib):
     with pytest.raises(sg.SgemmError) as e:
         plan("N", "N", 1 << 31, 8, 8, lda=8, ldb=8)
     assert e.value.status == 4
+
+
+def bplan(ta, tb, M, N, K, batch, sA, sB, sC, lda=None, ldb=None, ldc=None, A=FAKE, B=FAKE, C=FAKE, sm=152,
+          alpha=1.0):
+    lda = lda or (M if ta == "T" else K)
+    ldb = ldb or (K if tb == "T" else N)
+    ldc = ldc or N
+    return sg.sgemm_plan_strided_batched(ta, tb, M, N, K, alpha, A, lda, B, ldb, 0.0, C, ldc, sA, sB, sC, batch, sm)
+
+
+def test_batched_planner(lib):
+    # 64 FC products of 512x1024x1024: 32 tiles each, one launch over all 2048 tiles, no split
+    p = bplan("N", "N", 512, 1024, 1024, 64, 512 * 1024, 1024 * 1024, 512 * 1024)
+    assert p["variant_name"] == "TC_TF32X3" and p["grid_x"] == 64 * 32 and p["split_k"] == 1
+    assert p["kernel_launches"] == 1 and p["workspace_bytes"] == 0
+    # shared weight (stride 0) keeps the tensor-core path
+    assert bplan("N", "N", 512, 1024, 1024, 8, 512 * 1024, 0, 512 * 1024)["variant_name"] == "TC_TF32X3"
+    # few tiles in all: split K over the whole batch, workspace for every product
+    s = bplan("N", "N", 64, 4096, 16384, 2, 64 * 16384, 0, 64 * 4096)
+    assert s["grid_x"] == 64 and s["split_k"] == 2 and s["workspace_bytes"] == 2 * 2 * 64 * 4096 * 4
+    # one product plans exactly like sgemm()
+    one = bplan("N", "N", 64, 4096, 16384, 1, 0, 0, 0)
+    single = plan("N", "N", 64, 4096, 16384)
+    assert one == single
+    # strides that break 16-byte alignment, or overlapping operands, take the any-alignment kernel
+    assert bplan("N", "N", 64, 64, 64, 4, 64 * 64 + 2, 64 * 64, 64 * 64)["variant_name"] == "GENERIC"
+    assert bplan("N", "N", 64, 64, 64, 4, 64 * 32, 64 * 64, 64 * 64)["variant_name"] == "GENERIC"
+    # empty batches and alpha == 0
+    assert bplan("N", "N", 64, 64, 64, 0, 0, 0, 0)["variant_name"] == "NONE"
+    assert bplan("N", "N", 64, 64, 64, 3, 0, 0, 64 * 64, alpha=0.0)["variant_name"] == "SCALE"
+
+
+def test_batched_argument_checks(lib):
+    def st(sA, sB, sC, batch, M=4, N=4, ldc=4):
+        return lib.sgemm_plan_strided_batched(b"N", b"N", M, N, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, ldc, sA, sB,
+                                              sC, batch, 152, ctypes.byref(sg.PlanStruct()))
+    assert st(16, 16, 16, 3) == 0
+    assert st(-1, 16, 16, 3) == -14
+    assert st(16, -1, 16, 3) == -15
+    assert st(16, 16, -1, 3) == -16
+    assert st(16, 16, 15, 3) == -16          # C matrices would overlap: (M-1)*ldc + N = 16
+    assert st(16, 16, 0, 1) == 0             # one product: strideC is never used
+    assert st(16, 16, 16, -1) == -17
+    assert lib.sgemm_plan_strided_batched(b"N", b"N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4, 16, 16, 16, 3,
+                                          152, None) == -19
+    # the sgemm() checks come first, with the same argument numbers
+    assert lib.sgemm_plan_strided_batched(b"N", b"N", 4, 4, 8, 1.0, FAKE, 7, FAKE, 4, 0.0, FAKE, 4, 16, 16, 16, 3,
+                                          152, ctypes.byref(sg.PlanStruct())) == -8
+    # and the entry point itself rejects before touching a device
+    assert lib.sgemm_strided_batched(b"N", b"N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4, 16, 16, 15, 3,
+                                     None) == -16
+    assert sg.sgemm_status_string(-17).startswith("invalid argument 17")

@@ -35,6 +35,11 @@ MUTATIONS = [
     ("ldc ignored", "C[i * ldc + j] = (float)r;", "C[i * N + j] = (float)r;"),
     ("column index modulo M", "const int64_t j = e % N;", "const int64_t j = e % (M > 0 ? M : 1);"),
     ("'C' not accepted as transpose", "t == 'C' || t == 'c'", "t == 'C' && t == 'c'"),
+    ("batch: last product dropped", "for (int64_t b = 0; b < batch; ++b)", "for (int64_t b = 0; b < batch - 1; ++b)"),
+    ("batch: A advanced by B's stride", "A ? A + b * strideA : A", "A ? A + b * strideB : A"),
+    ("batch: C taken as packed", "C ? C + b * strideC : C", "C ? C + b * M * ldc : C"),
+    ("batch: S not advanced", "S ? S + b * strideS : S", "S"),
+    ("batch: negative stride accepted", "strideA < 0 || strideB", "strideB"),
 ]
 
 _CHILD = r"""
