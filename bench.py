@@ -59,6 +59,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prewarm-s", type=float, default=0.5, help="untimed seconds of steps before the warm-up")
     ap.add_argument("--variant", default="AUTO", help="planner override (tests and experiments)")
+    ap.add_argument("--split", type=int, default=0,
+                    help="planner override of the K split (0 = planner's choice; with the tensor-core kernel, "
+                         "1 = one CTA per output tile, hardware-scheduled)")
     ap.add_argument("--no-cublas-context", action="store_true",
                     help="skip the cuBLAS FP32 context number (torch.matmul, TF32 off)")
     return ap.parse_args()
@@ -354,8 +357,8 @@ def run_ours(args):
     d = si.make_case(case)
     M, N, K = case.M, case.N, case.K
     stream = torch.cuda.current_stream(dev)
-    if args.variant != "AUTO":
-        sg.sgemm_set_variant_override(args.variant, 0)
+    if args.variant != "AUTO" or args.split:
+        sg.sgemm_set_variant_override(args.variant, args.split)
     sh = stream.cuda_stream
 
     # two device-resident input sets, used in turn
@@ -437,7 +440,7 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {**config_block(case, world), "prewarm_s": args.prewarm_s,
                    "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "tile_k", "stages",
-                                                 "split_k", "grid_x", "grid_y")}},
+                                                 "split_k", "grid_x", "grid_y", "dp_tiles", "sk_tiles")}},
         "pct_ffma_peak": 100.0 * achieved / ffma_peak,
         "ffma_peak": {"value": ffma_peak, "unit": "TFLOP/s",
                       "basis": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz"},
@@ -532,8 +535,8 @@ def run_ours_batched(args, c):
                         c_init="uniform" if c.beta != 0 else "zero")
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    if args.variant != "AUTO":
-        sg.sgemm_set_variant_override(args.variant, 0)
+    if args.variant != "AUTO" or args.split:
+        sg.sgemm_set_variant_override(args.variant, args.split)
     sets = [tuple(torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C")) for _ in range(2)]
     torch.cuda.synchronize(dev)
     strides = (d["strideA"], d["strideB"], d["strideC"])
@@ -567,7 +570,8 @@ def run_ours_batched(args, c):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {**batched_config_block(c, d, world), "prewarm_s": args.prewarm_s,
-                   "plan": {k: plan[k] for k in ("variant_name", "split_k", "grid_x", "grid_y")}},
+                   "plan": {k: plan[k] for k in ("variant_name", "split_k", "grid_x", "grid_y", "dp_tiles",
+                                                 "sk_tiles")}},
         "roofline": (tensor_roofline(achieved, peaks, None, kernel_ms) if plan["variant_name"] == "TC_TF32X3"
                      else {"bound": "alu", "achieved": achieved, "peak": None, "unit": "TFLOP/s", "frac": None,
                            "traffic": None, "kernel": plan["variant_name"], "kernel_ms": kernel_ms}),

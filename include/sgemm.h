@@ -115,8 +115,16 @@ typedef struct sgemm_plan_t {
     int split_k;             /* number of K slices (1 = no split) */
     int kernel_launches;     /* kernels one sgemm() call launches */
     int64_t grid_x, grid_y;  /* CTAs of the GEMM kernel: tiles x K slices */
-    int64_t workspace_bytes; /* split-K partial-sum bytes taken from the pool */
+    int64_t workspace_bytes; /* split-K / stream-K partial-sum bytes taken from the pool */
     int64_t smem_bytes;      /* dynamic shared memory per CTA */
+    /* Tensor-core kernel only (persistent CTAs, grid_x of them): the first
+     * dp_tiles output tiles are taken whole, round robin (CTA c: tiles c,
+     * c + grid_x, ...); the sk_iters K tiles of the last sk_tiles output tiles
+     * are then shared evenly by all CTAs (stream-K); split_k is the most CTAs
+     * that share one output tile. */
+    int64_t dp_tiles;
+    int64_t sk_tiles;
+    int64_t sk_iters;
 } sgemm_plan_t;
 
 /*
@@ -219,7 +227,9 @@ int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_t K,
  * that has already given nearly all device memory to its own allocator, or
  * latency-critical code that cannot absorb a pool growing mid-run, cannot
  * allow that.  sgemm_noalloc() calls no cudaMalloc, cudaFree or other
- * allocating routine: the partial sums go to a fixed scratch array of
+ * allocating routine: the partial sums (split-K slices, or the stream-K
+ * slots of the tensor-core kernel: 2 x 64 KiB per CTA, 19 MiB on 152 SMs)
+ * go to a fixed scratch array of
  * SGEMM_NOALLOC_SCRATCH_BYTES compiled into the library, one per device,
  * held by every GPU that loads the library until the process exits.
  *
@@ -232,7 +242,7 @@ int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_t K,
  * calls whose kernels can overlap on the GPU (e.g. on unordered streams) race
  * on it, so order them.  CUDA failures return SGEMM_ERR_CUDA.
  */
-#define SGEMM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20) /* 16 MiB per device */
+#define SGEMM_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB per device */
 
 int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int64_t K,
                   float alpha, const float *A, int64_t lda,

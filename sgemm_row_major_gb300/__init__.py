@@ -26,7 +26,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_lib", "libsgemm.so")
 
 STATUS = {"OK": 0, "ERR_CUDA": 1, "ERR_TIMEOUT": 2, "ERR_NOMEM": 3, "ERR_UNSUPPORTED": 4, "ERR_SCRATCH_LIMIT": 5}
-NOALLOC_SCRATCH_BYTES = 16 << 20  # SGEMM_NOALLOC_SCRATCH_BYTES in include/sgemm.h
+NOALLOC_SCRATCH_BYTES = 32 << 20  # SGEMM_NOALLOC_SCRATCH_BYTES in include/sgemm.h
 VARIANTS = {"AUTO": 0, "NONE": 1, "SCALE": 2, "GENERIC": 3, "TMA_128x128": 4, "TMA_64x256": 5, "TC_TF32X3": 6}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 
@@ -42,7 +42,8 @@ class PlanStruct(ctypes.Structure):
                 ("tile_k", ctypes.c_int), ("stages", ctypes.c_int), ("threads", ctypes.c_int),
                 ("split_k", ctypes.c_int), ("kernel_launches", ctypes.c_int),
                 ("grid_x", ctypes.c_int64), ("grid_y", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
+                ("dp_tiles", ctypes.c_int64), ("sk_tiles", ctypes.c_int64), ("sk_iters", ctypes.c_int64)]
 
 
 _lock = threading.Lock()

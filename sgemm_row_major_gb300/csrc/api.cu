@@ -151,6 +151,65 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Schedule of the persistent tensor-core kernel (see kernel_tf32x3.cu).
+// Stream-K pays for every output tile it splits (partial sums written and
+// read back by the fixup kernel), so it is used only when each CTA gets at
+// least kMinStreamKIters K tiles of it:
+//   tiles >= SMs: whole-tile rounds on one CTA per SM; when the last round is
+//     ragged, the last SMs + (tiles % SMs) tiles go to stream-K instead (each
+//     CTA's share is then 1-2 tiles), or stay whole if that share is short;
+//   tiles <  SMs: stream-K over all tiles on one CTA per SM, or, if that
+//     share is short, S = min(SMs / tiles, K tiles / 4) CTAs per tile;
+//   forced split S (override): S CTAs per tile.
+constexpr int64_t kMinStreamKIters = 32;
+
+int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
+  const int64_t sms = std::max(1, sm_count);
+  int64_t grid, dp_tiles, sk_tiles;
+  const int ov_split = g_override_split.load();
+  if (ov_split > 0) {
+    dp_tiles = 0;
+    sk_tiles = tiles;
+    grid = std::min<int64_t>({tiles * ov_split, tiles * kt, int64_t{1} << 20});
+  } else if (tiles >= sms) {
+    grid = sms;
+    sk_tiles = tiles % sms ? sms + tiles % sms : 0;
+    if (sk_tiles * kt / sms < kMinStreamKIters) sk_tiles = 0;
+    dp_tiles = tiles - sk_tiles;
+  } else {
+    dp_tiles = 0;
+    sk_tiles = tiles;
+    if (tiles * kt / sms >= kMinStreamKIters) {
+      grid = sms;
+    } else {
+      const int64_t split = std::max<int64_t>(1, std::min<int64_t>(sms / tiles, kt / 4));
+      grid = tiles * split;
+    }
+  }
+  const int64_t sk_iters = sk_tiles * kt;
+  // int64 headroom of the device's c * sk_iters and (i + 1) * grid products,
+  // and an int count of K tiles per CTA
+  if (sk_iters > (INT64_MAX / 4) / (grid + 1) || (dp_tiles / grid + 1) * kt + sk_iters / grid + 1 > INT_MAX)
+    return SGEMM_ERR_UNSUPPORTED;
+  // the most CTAs sharing one stream-K tile (owner(i) = ceil((i+1) G / I) - 1)
+  int64_t most = 1;
+  for (int64_t j = 0; j < sk_tiles; ++j) {
+    const int64_t i0 = j * kt, i1 = i0 + kt - 1;
+    const int64_t c0 = ((i0 + 1) * grid + sk_iters - 1) / sk_iters - 1;
+    const int64_t c1 = ((i1 + 1) * grid + sk_iters - 1) / sk_iters - 1;
+    most = std::max(most, c1 - c0 + 1);
+  }
+  plan->split_k = (int)std::min<int64_t>(most, INT_MAX);
+  plan->kernel_launches = most > 1 ? 2 : 1;
+  plan->grid_x = grid;
+  plan->grid_y = 1;
+  plan->workspace_bytes = most > 1 ? 2 * grid * (int64_t)(128 * 128 * 4) : 0;
+  plan->dp_tiles = dp_tiles;
+  plan->sk_tiles = sk_tiles;
+  plan->sk_iters = sk_iters;
+  return SGEMM_OK;
+}
+
 // The planner: a pure function of the problem, the SM count and the override.
 int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   *plan = sgemm_plan_t{};
@@ -203,6 +262,15 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   const int64_t kt = ceil_div(pr.K, bk);
   if (tiles > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
 
+  plan->variant = variant;
+  plan->tile_m = bm;
+  plan->tile_n = bn;
+  plan->tile_k = bk;
+  plan->stages = stages;
+  plan->threads = threads;
+  plan->smem_bytes = smem;
+  if (variant == SGEMM_VARIANT_TC_TF32X3) return plan_stream_k(tiles, kt, sm_count, plan);
+
   // Split K only when the output tiles cannot fill the SMs, keeping at least
   // 4 K tiles per slice.
   int64_t split = 1;
@@ -213,17 +281,10 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   const int64_t per = ceil_div(kt, split);
   split = ceil_div(kt, per);  // no empty slice
 
-  plan->variant = variant;
-  plan->tile_m = bm;
-  plan->tile_n = bn;
-  plan->tile_k = bk;
-  plan->stages = stages;
-  plan->threads = threads;
   plan->split_k = (int)split;
   plan->kernel_launches = split > 1 ? 2 : 1;
   plan->grid_x = tiles;
   plan->grid_y = split;
-  plan->smem_bytes = smem;
   plan->workspace_bytes = split > 1 ? pr.batch * split * pr.M * (ceil_div(pr.N, 4) * 4) * 4 : 0;
   return SGEMM_OK;
 }
@@ -260,6 +321,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   p.tiles_n = (int)ceil_div(pr.N, plan.tile_n);
   p.k_tiles_per_split = (int)ceil_div(ceil_div(pr.K, plan.tile_k), split);
   p.ws_ld = ceil_div(pr.N, 4) * 4;
+  set_schedule(plan, &p);
 
   CUtensorMap mapA, mapB;
   if (plan.variant != SGEMM_VARIANT_GENERIC) {
@@ -270,7 +332,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   }
 
   void* ws = nullptr;
-  if (split > 1) {
+  if (plan.workspace_bytes > 0) {
     cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)plan.workspace_bytes, st.pool, stream);
     if (e != cudaSuccess) {
       t_last_cuda_error = (int)e;
@@ -283,7 +345,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   if (plan.variant == SGEMM_VARIANT_GENERIC) {
     e = launch_generic_gemm(pr.ta, pr.tb, p, split, stream);
   } else if (plan.variant == SGEMM_VARIANT_TC_TF32X3) {
-    e = launch_tf32x3(pr.ta, pr.tb, mapA, mapB, p, split, stream);
+    e = launch_tf32x3(pr.ta, pr.tb, mapA, mapB, p, stream);
+    if (e == cudaSuccess && plan.kernel_launches > 1) e = launch_streamk_fixup(p, (int)plan.sk_tiles, stream);
   } else {
     const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
     if (!pr.ta && !pr.tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, stream);
@@ -291,7 +354,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
     else if (pr.ta && !pr.tb) e = launch_tma_op_tn(tile, mapA, mapB, p, split, stream);
     else e = launch_tma_op_tt(tile, mapA, mapB, p, split, stream);
   }
-  if (e == cudaSuccess && split > 1) e = launch_splitk_reduce(p, split, stream);
+  if (e == cudaSuccess && split > 1 && plan.variant != SGEMM_VARIANT_TC_TF32X3)
+    e = launch_splitk_reduce(p, split, stream);
   if (ws) {
     cudaError_t ef = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = ef;

@@ -26,7 +26,19 @@
 // shared-memory data path), so the A operand's hi/lo parts go to tensor
 // memory instead (tcgen05.mma reads A from TMEM, B from shared memory).
 //
-// CTA (one 128x128 output tile or, with a K split, one K slice of it; 19 warps):
+// Schedule (persistent CTAs, stream-K balancing without waits between CTAs):
+// the grid has G CTAs (at most one per SM when the work allows).  CTA c first
+// takes the whole 128x128 output tiles c, c+G, c+2G, ... below sk_tile0
+// (data-parallel rounds), then an even share [B(c), B(c+1)) of the K
+// iterations of the remaining tiles, B(c) = floor(c*I/G), I = (tiles -
+// sk_tile0) * (K tiles per output tile).  A CTA writes a tile it covers whole straight to C; a tile
+// whose K range is shared by several CTAs is written as partial sums to the
+// CTA's slots (2c: its first stream-K tile, 2c+1: its last), and
+// streamk_fixup_kernel, launched after it on the same stream, adds the slots
+// of each shared tile in CTA order and applies alpha/beta.  The output tiles
+// of all products of a strided batch form one sequence.
+//
+// CTA roles (19 warps):
 //   warp 0     TMA producer: FP32 tiles of op(A) and op(B) (as stored) into a
 //              4-stage "raw" ring (32 KB per stage).
 //   warps 1,18 MMA issuers (one thread each; warp 1 takes even K tiles,
@@ -74,6 +86,7 @@ constexpr int kFoldTiles = 1;                       // 32-k tiles summed in one 
 // phase of a stage barrier could not tell the phase it needs from the one
 // two ahead (mbarrier waits are by phase parity).
 constexpr int kIssuers = kFoldTiles == 1 ? 2 : 1;
+static_assert(kFoldTiles == 1, "the folders walk the CTA's segments one accumulator per K tile");
 constexpr uint32_t kACols = 64;                     // A hi (32 k) + A lo (32 k) of one split stage
 constexpr uint32_t kAColBase = kAccBufs * kAccCols;
 constexpr uint32_t kTmemCols = 512;                 // 3 accumulators + 2 A stages = 512
@@ -152,12 +165,77 @@ __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, i
   tn = local / rows;
 }
 
+// Product and origin of output tile `tile` (numbered over all products).
+__device__ __forceinline__ void tile_origin(const GemmParams& p, int tile, int& prod, int& m0, int& n0) {
+  const int tiles = p.tiles_m * p.tiles_n;
+  prod = tile / tiles;
+  int tm, tn;
+  tile_coords(tile - prod * tiles, p.tiles_m, p.tiles_n, tm, tn);
+  m0 = tm * BM;
+  n0 = tn * BN;
+}
+
+// First stream-K iteration of CTA c: floor(c * I / G).
+__device__ __forceinline__ int64_t sk_bound(const GemmParams& p, int c) {
+  return (int64_t)c * p.sk_iters / p.sk_grid;
+}
+
+// The CTA whose stream-K range holds iteration i: the largest c with B(c) <= i.
+__device__ __forceinline__ int sk_owner(const GemmParams& p, int64_t i) {
+  return (int)(((i + 1) * p.sk_grid + p.sk_iters - 1) / p.sk_iters - 1);
+}
+
+// Partial-sum slot of CTA c for stream-K tile j (relative to the first stream-K tile).
+__device__ __forceinline__ int sk_slot(const GemmParams& p, int c, int j, int kt) {
+  return (int)(sk_bound(p, c) / kt) == j ? 2 * c : 2 * c + 1;
+}
+
+// A CTA's work: `dp` whole tiles (c, c+G, ... below sk_tile0), then stream-K
+// iterations [b, e) covering relative stream-K tiles j0 .. j0 + nseg - dp - 1.
+struct CtaWork {
+  int dp, j0, nseg, units;
+  int64_t b, e;
+};
+
+__device__ __forceinline__ CtaWork cta_work(const GemmParams& p, int c, int kt) {
+  CtaWork w;
+  w.dp = c < p.sk_tile0 ? (p.sk_tile0 - c + p.sk_grid - 1) / p.sk_grid : 0;
+  w.b = p.sk_iters > 0 ? sk_bound(p, c) : 0;
+  w.e = p.sk_iters > 0 ? sk_bound(p, c + 1) : 0;
+  w.j0 = (int)(w.b / kt);
+  w.nseg = w.dp + (w.e > w.b ? (int)((w.e - 1) / kt) - w.j0 + 1 : 0);
+  w.units = w.dp * kt + (int)(w.e - w.b);
+  return w;
+}
+
+// Segment s of a CTA's work: K tiles [kb, ke) of output tile `tile`; slot -1
+// when the segment is the tile's whole K range (result goes to C).
+struct Segment {
+  int tile, kb, ke, slot;
+};
+
+__device__ __forceinline__ Segment cta_segment(const GemmParams& p, const CtaWork& w, int c, int s, int kt) {
+  Segment g;
+  if (s < w.dp) {
+    g.tile = s * p.sk_grid + c;
+    g.kb = 0;
+    g.ke = kt;
+    g.slot = -1;
+  } else {
+    const int j = w.j0 + (s - w.dp);
+    const int64_t t0 = (int64_t)j * kt;
+    g.tile = p.sk_tile0 + j;
+    g.kb = (int)(max(w.b, t0) - t0);
+    g.ke = (int)(min(w.e, t0 + kt) - t0);
+    g.slot = (g.kb == 0 && g.ke == kt) ? -1 : sk_slot(p, c, j, kt);
+  }
+  return g;
+}
+
 // Raw tile layouts (as the TMA engine copies them):
 //   op(A) 'N': [128 rows of M][32 k], K contiguous, 128-byte swizzle;  'T': [32 k][128 m], M contiguous.
 //   op(B) 'N': [32 k][128 n], N contiguous;  'T': [128 n][32 k], K contiguous, 128-byte swizzle.
-// SPLIT: write the raw sums of this CTA's K slice (blockIdx.y) to the workspace instead of C.
-// blockIdx.x = product * tiles + output tile (a strided batch of products).
-template <bool TA, bool TB, bool SPLIT>
+template <bool TA, bool TB>
 __global__ void __launch_bounds__(kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                        const GemmParams p) {
@@ -166,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t split_full[kSplitStages], split_empty[kSplitStages];
   __shared__ __align__(8) uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   __shared__ uint32_t tmem_slot;
+  __shared__ CtaWork work_s;  // this CTA's schedule, written once by thread 0 (kept out of registers)
 
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -180,17 +259,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int tiles = p.tiles_m * p.tiles_n;
-  const int prod = (int)(blockIdx.x / (unsigned)tiles);  // product of a strided batch
-  int tm, tn;
-  tile_coords((int)(blockIdx.x - (unsigned)(prod * tiles)), p.tiles_m, p.tiles_n, tm, tn);
-  const int m0 = tm * BM, n0 = tn * BN;
-  const int za = prod * p.za, zb = prod * p.zb;
+  const int cta = (int)blockIdx.x;
   const int kt_total = (p.K + BK - 1) / BK;
-  const int kt0 = blockIdx.y * p.k_tiles_per_split;
-  const int nkt = min(kt_total, kt0 + p.k_tiles_per_split) - kt0;  // >= 1 by construction
 
   if (threadIdx.x == 0) {
+    work_s = cta_work(p, cta, kt_total);
     for (int r = 0; r < kRawStages; ++r) {
       mbar_init(smem_addr(&raw_full[r]), 1);
       mbar_init(smem_addr(&raw_empty[r]), kSplitWarps);
@@ -210,28 +283,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tmem_fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  const int nkt = work_s.units;  // K tiles this CTA processes, over all its segments (>= 1)
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tensormap(&mapA);
       prefetch_tensormap(&mapB);
-      int issued = 0;
-      for (int t = 0; t < nkt; ++t) {
-        const int r = t % kRawStages;
-        if (t >= kRawStages &&
-            !mbar_wait(smem_addr(&raw_empty[r]), (uint32_t)((t / kRawStages) - 1) & 1u, p.timeout_ns)) {
-          atomicOr(p.fault, (unsigned)kFaultEmptyWait);
-          break;
+      int issued = 0;  // loads issued so far (= the next K tile's position in the ring sequence)
+      bool ok = true;
+      const CtaWork work = work_s;
+      for (int sgi = 0; ok && sgi < work.nseg; ++sgi) {
+        const Segment g = cta_segment(p, work, cta, sgi, kt_total);
+        int prod, m0, n0;
+        tile_origin(p, g.tile, prod, m0, n0);
+        const int za = prod * p.za, zb = prod * p.zb;
+        for (int kt = g.kb; kt < g.ke; ++kt) {
+          const int t = issued;
+          const int r = t % kRawStages;
+          if (t >= kRawStages &&
+              !mbar_wait(smem_addr(&raw_empty[r]), (uint32_t)((t / kRawStages) - 1) & 1u, p.timeout_ns)) {
+            atomicOr(p.fault, (unsigned)kFaultEmptyWait);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_addr(&raw_full[r]);
+          mbar_arrive_expect_tx(fb, (uint32_t)kRawBytes);
+          const int k0 = kt * BK;
+          if (!TA) tma_load_3d(raw_a(r), &mapA, fb, k0, m0, za);
+          else     tma_load_3d(raw_a(r), &mapA, fb, m0, k0, za);
+          if (!TB) tma_load_3d(raw_b(r), &mapB, fb, n0, k0, zb);
+          else     tma_load_3d(raw_b(r), &mapB, fb, k0, n0, zb);
+          issued = t + 1;
         }
-        const uint32_t fb = smem_addr(&raw_full[r]);
-        mbar_arrive_expect_tx(fb, (uint32_t)kRawBytes);
-        const int k0 = (kt0 + t) * BK;
-        if (!TA) tma_load_3d(raw_a(r), &mapA, fb, k0, m0, za);
-        else     tma_load_3d(raw_a(r), &mapA, fb, m0, k0, za);
-        if (!TB) tma_load_3d(raw_b(r), &mapB, fb, n0, k0, zb);
-        else     tma_load_3d(raw_b(r), &mapB, fb, k0, n0, zb);
-        issued = t + 1;
       }
       // leave only when every copy into shared memory has landed
       for (int t = issued > kRawStages ? issued - kRawStages : 0; t < issued; ++t)
@@ -377,55 +461,56 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int e = 0; e < 32; ++e) master2[e] = make_float2(0.0f, 0.0f);
     bool ok = true;
-    const int nchunks = (nkt + kFoldTiles - 1) / kFoldTiles;
-    for (int u = 0; u < nchunks; ++u) {
-      const int b = u % kAccBufs;
-      if (!warp_wait(smem_addr(&acc_full[b]), (uint32_t)(u / kAccBufs) & 1u, p.timeout_ns)) {
-        ok = false;
-        if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
-        break;
+    int u = 0;  // accumulator sequence number (one per K tile; kFoldTiles == 1)
+    for (int sgi = 0; ok && sgi < work_s.nseg; ++sgi) {
+      int len;  // K tiles of this segment (the segment itself is looked up again for its epilogue)
+      {
+        const Segment g = cta_segment(p, work_s, cta, sgi, kt_total);
+        len = g.ke - g.kb;
       }
-      tmem_fence_after_sync();
-      float v[4][16];
+      for (int i = 0; i < len; ++i, ++u) {
+        const int b = u % kAccBufs;
+        if (!warp_wait(smem_addr(&acc_full[b]), (uint32_t)(u / kAccBufs) & 1u, p.timeout_ns)) {
+          ok = false;
+          if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
+          break;
+        }
+        tmem_fence_after_sync();
+        float v[4][16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld16(tq + (uint32_t)b * kAccCols + 16u * c, v[c]);
-      tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) tmem_ld16(tq + (uint32_t)b * kAccCols + 16u * c, v[c]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld_ready(v[c]);
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld_ready(v[c]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)  // round-to-nearest FP32 adds, two per instruction
-          master2[8 * c + e] = __fadd2_rn(master2[8 * c + e], make_float2(v[c][2 * e], v[c][2 * e + 1]));
+          for (int e = 0; e < 8; ++e)  // round-to-nearest FP32 adds, two per instruction
+            master2[8 * c + e] = __fadd2_rn(master2[8 * c + e], make_float2(v[c][2 * e], v[c][2 * e + 1]));
+        }
+        tmem_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
       }
-      tmem_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
-    }
-    if (ok) {
-      // epilogue: this thread holds row 32q + lane, columns 64*half .. +63 of the tile
-      float master[64];
+      if (!ok) break;
+      // epilogue of this segment: this thread holds row 32q + lane, columns 64*half .. +63 of the tile
+      const Segment g = cta_segment(p, work_s, cta, sgi, kt_total);
+      if (g.slot >= 0) {
+        // partial sums of a shared stream-K tile -> this CTA's slot (whole 128 x 128, no bounds)
+        float* w = p.ws + (int64_t)g.slot * (BM * BN) + (32 * q + lane) * BN + 64 * half;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        master[2 * e] = master2[e].x;
-        master[2 * e + 1] = master2[e].y;
-      }
-      const int row = m0 + 32 * q + lane;
-      if (row < p.M) {
-        if (SPLIT) {
-          float* wrow = p.ws + (((int64_t)prod * gridDim.y + blockIdx.y) * p.M + row) * p.ws_ld;
-#pragma unroll
-          for (int g = 0; g < 16; ++g) {
-            const int col = n0 + 64 * half + 4 * g;
-            if (col < p.N)
-              *reinterpret_cast<float4*>(wrow + col) =
-                  make_float4(master[4 * g], master[4 * g + 1], master[4 * g + 2], master[4 * g + 3]);
-          }
-        } else {
+        for (int e = 0; e < 16; ++e)
+          *reinterpret_cast<float4*>(w + 4 * e) =
+              make_float4(master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y);
+      } else {
+        int prod, m0, n0;
+        tile_origin(p, g.tile, prod, m0, n0);
+        const int row = m0 + 32 * q + lane;
+        if (row < p.M) {
           float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
 #pragma unroll
-          for (int g = 0; g < 16; ++g) {
-            const int col = n0 + 64 * half + 4 * g;
-            const float* x = &master[4 * g];
+          for (int e = 0; e < 16; ++e) {
+            const int col = n0 + 64 * half + 4 * e;
+            const float x[4] = {master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y};
             if (p.c_vec && col + 3 < p.N) {
               float4 o;
               if (p.beta == 0.0f) {
@@ -438,13 +523,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<float4*>(crow + col) = o;
             } else {
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (col + e < p.N)
-                  crow[col + e] = p.beta == 0.0f ? p.alpha * x[e] : fmaf(p.alpha, x[e], p.beta * crow[col + e]);
+              for (int k = 0; k < 4; ++k)
+                if (col + k < p.N)
+                  crow[col + k] = p.beta == 0.0f ? p.alpha * x[k] : fmaf(p.alpha, x[k], p.beta * crow[col + k]);
             }
           }
         }
       }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) master2[e] = make_float2(0.0f, 0.0f);
     }
   }
 
@@ -454,27 +541,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// CTA (j, y) of the fixup grid: rows 8y .. 8y+7 of stream-K tile j, one float4
+// of 4 columns per thread.  If several CTAs shared tile j, C = alpha * (sum of
+// their slots, in CTA order) + beta * C over the in-range elements.  The
+// order is fixed, so the result does not depend on scheduling.
+constexpr int kFixupRowsPerCta = 8;
+template <bool CVEC>
+__global__ void __launch_bounds__(256) streamk_fixup_kernel(const GemmParams p) {
+  const int kt = (p.K + BK - 1) / BK;
+  const int j = (int)blockIdx.x;
+  const int64_t i0 = (int64_t)j * kt;
+  const int c0 = sk_owner(p, i0), c1 = sk_owner(p, i0 + kt - 1);
+  if (c0 == c1) return;  // one CTA covered the whole tile and wrote C itself
+  int prod, m0, n0;
+  tile_origin(p, p.sk_tile0 + j, prod, m0, n0);
+  const int r = (int)blockIdx.y * kFixupRowsPerCta + (int)(threadIdx.x >> 5);
+  const int cc = (int)(threadIdx.x & 31) * 4;
+  const int row = m0 + r, col = n0 + cc;
+  if (row >= p.M || col >= p.N) return;
+  const float* w = p.ws + r * BN + cc;
+  float4 v = *reinterpret_cast<const float4*>(w + (int64_t)sk_slot(p, c0, j, kt) * (BM * BN));
+#pragma unroll 4
+  for (int c = c0 + 1; c <= c1; ++c) {
+    const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)sk_slot(p, c, j, kt) * (BM * BN));
+    v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+  }
+  float* cp = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
+  if (CVEC && col + 3 < p.N) {
+    float4 o;
+    if (p.beta == 0.0f) {
+      o = make_float4(p.alpha * v.x, p.alpha * v.y, p.alpha * v.z, p.alpha * v.w);
+    } else {
+      const float4 old = *reinterpret_cast<const float4*>(cp);
+      o = make_float4(fmaf(p.alpha, v.x, p.beta * old.x), fmaf(p.alpha, v.y, p.beta * old.y),
+                      fmaf(p.alpha, v.z, p.beta * old.z), fmaf(p.alpha, v.w, p.beta * old.w));
+    }
+    *reinterpret_cast<float4*>(cp) = o;
+  } else {
+    const float x[4] = {v.x, v.y, v.z, v.w};
+    for (int k = 0; k < 4 && col + k < p.N; ++k)
+      cp[k] = p.beta == 0.0f ? p.alpha * x[k] : fmaf(p.alpha, x[k], p.beta * cp[k]);
+  }
+}
+
 }  // namespace tc
 
 namespace {
 
 template <bool TA, bool TB>
 cudaError_t set_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<TA, TB, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<TA, TB, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<TA, TB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               tc::kSmemBytes);
 }
 
 template <bool TA, bool TB>
-cudaError_t launch(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p, int split,
-                   cudaStream_t stream) {
-  const dim3 grid((unsigned)((int64_t)p.batch * p.tiles_m * p.tiles_n), (unsigned)split);
-  if (split > 1)
-    tc::tf32x3_gemm_kernel<TA, TB, true><<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB, p);
-  else
-    tc::tf32x3_gemm_kernel<TA, TB, false><<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB, p);
+cudaError_t launch(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p, cudaStream_t stream) {
+  tc::tf32x3_gemm_kernel<TA, TB><<<(unsigned)p.sk_grid, tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB, p);
   return cudaGetLastError();
 }
 
@@ -489,11 +611,20 @@ cudaError_t prepare_tf32x3() {
 }
 
 cudaError_t launch_tf32x3(bool transA, bool transB, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                          const GemmParams& p, int split, cudaStream_t stream) {
-  if (!transA && !transB) return launch<false, false>(mapA, mapB, p, split, stream);
-  if (!transA && transB) return launch<false, true>(mapA, mapB, p, split, stream);
-  if (transA && !transB) return launch<true, false>(mapA, mapB, p, split, stream);
-  return launch<true, true>(mapA, mapB, p, split, stream);
+                          const GemmParams& p, cudaStream_t stream) {
+  if (!transA && !transB) return launch<false, false>(mapA, mapB, p, stream);
+  if (!transA && transB) return launch<false, true>(mapA, mapB, p, stream);
+  if (transA && !transB) return launch<true, false>(mapA, mapB, p, stream);
+  return launch<true, true>(mapA, mapB, p, stream);
+}
+
+cudaError_t launch_streamk_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream) {
+  const dim3 grid((unsigned)sk_tiles, tc::BM / tc::kFixupRowsPerCta);
+  if (p.c_vec)
+    tc::streamk_fixup_kernel<true><<<grid, 256, 0, stream>>>(p);
+  else
+    tc::streamk_fixup_kernel<false><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace sgemm_impl

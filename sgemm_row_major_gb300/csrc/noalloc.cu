@@ -116,7 +116,8 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
   p.tiles_n = (int)ceil_div(N, plan.tile_n);
   p.k_tiles_per_split = (int)ceil_div(ceil_div(K, plan.tile_k), split);
   p.ws_ld = ceil_div(N, 4) * 4;
-  p.ws = split > 1 ? nd->scratch : nullptr;
+  p.ws = plan.workspace_bytes > 0 ? nd->scratch : nullptr;
+  set_schedule(plan, &p);
 
   if (plan.variant == SGEMM_VARIANT_GENERIC) {
     e = launch_generic_gemm(ta, tb, p, split, cs);
@@ -126,12 +127,14 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
                             &mapB, &p.za, &p.zb);
     if (e != cudaSuccess) return SGEMM_ERR_CUDA;
     const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
-    if (plan.variant == SGEMM_VARIANT_TC_TF32X3) e = launch_tf32x3(ta, tb, mapA, mapB, p, split, cs);
-    else if (!ta && !tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, cs);
+    if (plan.variant == SGEMM_VARIANT_TC_TF32X3) {
+      e = launch_tf32x3(ta, tb, mapA, mapB, p, cs);
+      if (e == cudaSuccess && plan.kernel_launches > 1) e = launch_streamk_fixup(p, (int)plan.sk_tiles, cs);
+    } else if (!ta && !tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, cs);
     else if (!ta && tb) e = launch_tma_op_nt(tile, mapA, mapB, p, split, cs);
     else if (ta && !tb) e = launch_tma_op_tn(tile, mapA, mapB, p, split, cs);
     else e = launch_tma_op_tt(tile, mapA, mapB, p, split, cs);
   }
-  if (e == cudaSuccess && split > 1) e = launch_splitk_reduce(p, split, cs);
+  if (e == cudaSuccess && split > 1 && plan.variant != SGEMM_VARIANT_TC_TF32X3) e = launch_splitk_reduce(p, split, cs);
   return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
 }

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "sgemm.h"
+
 namespace sgemm_impl {
 
 // Everything a GEMM kernel needs besides its tensor maps.
@@ -27,6 +29,12 @@ struct GemmParams {
   int k_tiles_per_split = 0;     // K tiles (of the kernel's BK) per slice
   int tiles_m = 0, tiles_n = 0;  // output tiles of one product
   int c_vec = 0;                 // 1: C (every product) is 16-byte aligned and ldc % 4 == 0
+  // Persistent schedule of the tensor-core kernel (kernel_tf32x3.cu): sk_grid
+  // CTAs; CTA c takes whole tiles c, c + sk_grid, ... below sk_tile0, then an
+  // even share of the sk_iters K tiles of output tiles sk_tile0 .. (all tiles
+  // - 1); partial tiles go to slots of BM*BN floats in ws (2 per CTA).
+  int sk_grid = 0, sk_tile0 = 0;
+  int64_t sk_iters = 0;
   uint64_t timeout_ns = 0;       // limit of every in-kernel wait
   unsigned* fault = nullptr;     // device fault word (bits of FaultBits), see fault_word()
 };
@@ -40,6 +48,14 @@ struct GemmParams {
 cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                                 int64_t stride_a, const float* B, int64_t ldb, int64_t stride_b, int batch,
                                 int bm, int bn, int bk, CUtensorMap* mapA, CUtensorMap* mapB, int* za, int* zb);
+
+// Copies the tensor-core kernel's schedule from a plan (no-op for other variants).
+inline void set_schedule(const sgemm_plan_t& plan, GemmParams* p) {
+  if (plan.variant != SGEMM_VARIANT_TC_TF32X3) return;
+  p->sk_grid = (int)plan.grid_x;
+  p->sk_iters = plan.sk_iters;
+  p->sk_tile0 = (int)plan.dp_tiles;
+}
 
 // Shapes of the TMA-fed SIMT kernel.
 enum class TmaTile { k128x128, k64x256 };
@@ -60,10 +76,13 @@ SGEMM_DECLARE_TMA_OP(nt)
 SGEMM_DECLARE_TMA_OP(tn)
 SGEMM_DECLARE_TMA_OP(tt)
 #undef SGEMM_DECLARE_TMA_OP
-// 3xTF32 tensor-core kernel (kernel_tf32x3.cu), 128x128x32 tiles, any op, optional K split.
+// 3xTF32 tensor-core kernel (kernel_tf32x3.cu), 128x128x32 tiles, any op,
+// persistent data-parallel + stream-K schedule (GemmParams::sk_*), then the
+// fixup kernel over the sk_tiles stream-K tiles when any of them is shared.
 cudaError_t prepare_tf32x3();
 cudaError_t launch_tf32x3(bool transA, bool transB, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                          const GemmParams& p, int split, cudaStream_t stream);
+                          const GemmParams& p, cudaStream_t stream);
+cudaError_t launch_streamk_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
 cudaError_t launch_generic_gemm(bool transA, bool transB, const GemmParams& p, int split,
                                 cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const GemmParams& p, int split, cudaStream_t stream);

@@ -89,8 +89,8 @@ def test_planner_variants(lib):
     assert plan("N", "N", 0, 10, 10)["variant_name"] == "NONE"
     assert plan("N", "N", 10, 10, 0)["variant_name"] == "SCALE"
     big = plan("N", "N", 4096, 4096, 4096)
-    assert big["variant_name"] == "TC_TF32X3" and big["split_k"] == 1 and big["kernel_launches"] == 1
-    assert big["grid_x"] == 32 * 32 and big["tile_k"] == 32 and big["threads"] == 608
+    assert big["variant_name"] == "TC_TF32X3" and big["grid_x"] == 152 and big["grid_y"] == 1
+    assert big["tile_m"] == big["tile_n"] == 128 and big["tile_k"] == 32 and big["threads"] == 608
     assert big["smem_bytes"] <= 227 * 1024
     # unaligned base or ld not a multiple of 4 -> the generic (edge) kernel
     assert plan("N", "N", 512, 512, 512, A=FAKE_ODD)["variant_name"] == "GENERIC"
@@ -103,25 +103,60 @@ def test_planner_variants(lib):
 
 
 def test_planner_split_k(lib):
-    # 1024^3: 64 tiles of 128x128 on 152 SMs -> split K in 2
-    p = plan("N", "N", 1024, 1024, 1024)
-    assert p["split_k"] == 2 and p["kernel_launches"] == 2 and p["grid_y"] == 2
-    assert p["workspace_bytes"] == 2 * 1024 * 1024 * 4
-    # skinny FC shape: 32 tiles of 128x128 -> 4 slices
-    s = plan("N", "N", 64, 4096, 16384)
-    assert s["variant_name"] == "TC_TF32X3" and s["grid_x"] == 32 and s["split_k"] == 4
-    # the FFMA kernel's short-M tiles when forced: 64x256 tiles, 16 of them -> 9 slices
+    # the FFMA kernels split K into grid.y slices when the tiles cannot fill the SMs:
+    # 1024^3 with 128x128 tiles -> 64 tiles, 2 slices
     try:
+        sg.sgemm_set_variant_override("TMA_128x128", 0)
+        p = plan("N", "N", 1024, 1024, 1024)
+        assert p["split_k"] == 2 and p["kernel_launches"] == 2 and p["grid_y"] == 2
+        assert p["workspace_bytes"] == 2 * 1024 * 1024 * 4
+        # short-M tiles: 64x256 tiles, 16 of them -> 9 slices
         sg.sgemm_set_variant_override("TMA_64x256", 0)
         f = plan("N", "N", 64, 4096, 16384)
         assert f["variant_name"] == "TMA_64x256" and f["grid_x"] == 16 and f["split_k"] == 9
+        # never more slices than K tiles, and every slice non-empty
+        sg.sgemm_set_variant_override("GENERIC", 0)
+        t = plan("N", "N", 8, 8, 64)
+        assert t["split_k"] <= 4
+        # more SMs never reduce the split
+        assert plan("N", "N", 256, 256, 8192, sm=304)["split_k"] >= plan("N", "N", 256, 256, 8192)["split_k"]
     finally:
         sg.sgemm_set_variant_override("AUTO", 0)
-    # never more slices than K tiles, and every slice non-empty
-    t = plan("N", "N", 8, 8, 64)
-    assert t["split_k"] <= 2
-    # more SMs never reduce the split
-    assert plan("N", "N", 256, 256, 8192, sm=304)["split_k"] >= plan("N", "N", 256, 256, 8192)["split_k"]
+
+
+def test_planner_stream_k(lib):
+    """The tensor-core kernel's persistent schedule: whole-tile rounds, then stream-K."""
+    # 4096^3: 1024 tiles on 152 SMs = 6.74 rounds -> 760 whole tiles, then 264 stream-K tiles
+    p = plan("N", "N", 4096, 4096, 4096)
+    assert (p["grid_x"], p["grid_y"], p["dp_tiles"], p["sk_tiles"]) == (152, 1, 760, 264)
+    assert p["sk_iters"] == 264 * 128 and p["kernel_launches"] == 2 and p["split_k"] == 2
+    assert p["workspace_bytes"] == 2 * 152 * 128 * 128 * 4
+    # a whole number of rounds: whole tiles only, one launch, no workspace
+    w = plan("N", "N", 128 * 19, 128 * 16, 512)
+    assert (w["dp_tiles"], w["sk_tiles"], w["kernel_launches"], w["workspace_bytes"]) == (304, 0, 1, 0)
+    # a ragged last round whose stream-K share would be short (K = 64): whole tiles, ragged rounds
+    r = plan("N", "N", 128 * 20, 128 * 16, 64)
+    assert (r["grid_x"], r["dp_tiles"], r["sk_tiles"], r["kernel_launches"]) == (152, 320, 0, 1)
+    # fewer tiles than SMs with long K: stream-K over all of them on every SM
+    s = plan("N", "N", 64, 4096, 16384)
+    assert (s["grid_x"], s["dp_tiles"], s["sk_tiles"], s["sk_iters"]) == (152, 0, 32, 32 * 512)
+    assert s["split_k"] > 1 and s["kernel_launches"] == 2
+    # fewer tiles than SMs with short K: S = min(SMs / tiles, K tiles / 4) CTAs per tile
+    assert plan("N", "N", 1024, 1024, 1024)["grid_x"] == 64 * 2
+    t = plan("N", "N", 300, 260, 700)
+    assert t["grid_x"] == 9 * 5 and t["sk_tiles"] == 9 and t["split_k"] >= 5
+    q = plan("N", "N", 1000, 1300, 700)      # 88 tiles, 22 K tiles: one CTA per tile
+    assert (q["grid_x"], q["split_k"], q["kernel_launches"], q["workspace_bytes"]) == (88, 1, 1, 0)
+    # one tile, one K tile: one CTA, no fixup
+    o = plan("N", "N", 128, 128, 32)
+    assert (o["grid_x"], o["kernel_launches"], o["workspace_bytes"]) == (1, 1, 0)
+    # a forced split: S CTAs per tile
+    try:
+        sg.sgemm_set_variant_override("AUTO", 5)
+        f = plan("N", "N", 150, 260, 1000)
+        assert f["grid_x"] == 6 * 5 and f["dp_tiles"] == 0 and f["split_k"] >= 5
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
 
 
 def test_variant_override(lib):
@@ -155,15 +190,16 @@ def bplan(ta, tb, M, N, K, batch, sA, sB, sC, lda=None, ldb=None, ldc=None, A=FA
 
 
 def test_batched_planner(lib):
-    # 64 FC products of 512x1024x1024: 32 tiles each, one launch over all 2048 tiles, no split
+    # 64 FC products of 512x1024x1024: 32 tiles each, one persistent launch over all 2048 tiles
     p = bplan("N", "N", 512, 1024, 1024, 64, 512 * 1024, 1024 * 1024, 512 * 1024)
-    assert p["variant_name"] == "TC_TF32X3" and p["grid_x"] == 64 * 32 and p["split_k"] == 1
-    assert p["kernel_launches"] == 1 and p["workspace_bytes"] == 0
+    assert p["variant_name"] == "TC_TF32X3" and p["grid_x"] == 152
+    assert p["dp_tiles"] + p["sk_tiles"] == 64 * 32 and p["sk_tiles"] == 152 + 64 * 32 % 152
     # shared weight (stride 0) keeps the tensor-core path
     assert bplan("N", "N", 512, 1024, 1024, 8, 512 * 1024, 0, 512 * 1024)["variant_name"] == "TC_TF32X3"
-    # few tiles in all: split K over the whole batch, workspace for every product
+    # few tiles in all: stream-K over the tiles of every product
     s = bplan("N", "N", 64, 4096, 16384, 2, 64 * 16384, 0, 64 * 4096)
-    assert s["grid_x"] == 64 and s["split_k"] == 2 and s["workspace_bytes"] == 2 * 2 * 64 * 4096 * 4
+    assert s["grid_x"] == 152 and s["sk_tiles"] == 64 and s["split_k"] > 1
+    assert s["workspace_bytes"] == 2 * 152 * 128 * 128 * 4
     # one product plans exactly like sgemm()
     one = bplan("N", "N", 64, 4096, 16384, 1, 0, 0, 0)
     single = plan("N", "N", 64, 4096, 16384)

@@ -3,7 +3,7 @@
 sgemm() keeps split-K partial sums in a memory pool that may grow during a
 call.  Callers whose own allocator already holds nearly all device memory,
 or that cannot afford a pool growing mid-run, use sgemm_noalloc() instead:
-it runs the same kernels with the partial sums in a fixed 16 MiB array built
+it runs the same kernels with the partial sums in a fixed 32 MiB array built
 into the library.  These tests call it through the C ABI (ctypes), on shapes
 whose plan splits K (so the array is really used), and check its output
 against sgemm() on the same inputs for two calls in a row: the second call
@@ -81,7 +81,7 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
     B = torch.ones(K, N, device="cuda")
     C = torch.full((M, N), 3.0, device="cuda")
     try:
-        sg.sgemm_set_variant_override("TMA_128x128", 8)      # 8 slices x 4 MiB > 16 MiB
+        sg.sgemm_set_variant_override("TMA_128x128", 9)      # 9 slices x 4 MiB > 32 MiB
         need = sg.sgemm_plan("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C, N)["workspace_bytes"]
         assert need > sg.NOALLOC_SCRATCH_BYTES
         st = _c_abi()(b"N", b"N", M, N, K, 1.0, A.data_ptr(), K, B.data_ptr(), N, 0.0, C.data_ptr(), N, None)
@@ -95,7 +95,7 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
 
 def test_noalloc_without_split_and_empty_problems():
     import torch
-    M, N, K = 1024, 2048, 256      # 128 output tiles and 8 K tiles: the plan does not split K
+    M, N, K = 2432, 1024, 256      # 152 output tiles (one per SM) and 8 K tiles: no K split
     A = torch.from_numpy(si.uniform_pm1(M, K, 77, 1)).cuda()
     B = torch.from_numpy(si.uniform_pm1(K, N, 77, 2)).cuda()
     assert sg.sgemm_plan("N", "N", M, N, K, 2.0, A, K, B, N, 0.0, A, N)["split_k"] == 1
