@@ -334,7 +334,9 @@ def tensor_roofline(achieved, peaks, traffic, kernel_ms):
             "peak_basis": f"{basis} bf16 burst {bf16:.0f} TFLOP/s x nominal tf32/bf16 "
                           f"{NOMINAL_TF32_PF}/{NOMINAL_BF16_PF} = {tf32:.0f} TFLOP/s of tf32, / {TF32_PRODUCTS} "
                           f"tensor products per SGEMM FMA (3xTF32 split); achieved counts 2MNK only",
-            "kernel": "tf32x3_gemm_kernel (tcgen05.mma kind::tf32, 3xTF32 split)", "kernel_ms": kernel_ms}
+            "kernel": "tf32x3_gemm_kernel (tcgen05.mma kind::tf32, 3xTF32 split)", "kernel_ms": kernel_ms,
+            "kernel_ms_covers": "one sgemm() call: the GEMM kernel and, when stream-K tiles are shared, "
+                                "the fixup kernel after it (about 2% of the step in the ncu launch list)"}
 
 
 def run_ours(args):

@@ -160,7 +160,8 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 //     CTA's share is then 1-2 tiles), or stay whole if that share is short;
 //   tiles <  SMs: stream-K over all tiles on one CTA per SM, or, if that
 //     share is short, S = min(SMs / tiles, K tiles / 4) CTAs per tile;
-//   forced split S (override): S CTAs per tile.
+//   forced split S (override): S CTAs per tile (S = 1: one CTA per tile,
+//     scheduled by the hardware).
 constexpr int64_t kMinStreamKIters = 32;
 
 int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {

@@ -1,13 +1,21 @@
 // host_pipeline.cu -- sgemm_host(): SGEMM on operands that live in host memory.
 //
-// B is copied to the device once; op(A) and C then move in row blocks of C
-// on two library-owned streams, so the host-to-device copies of block i and
-// the device-to-host copy of block i-1 overlap the GEMM of the other block.
-// Device copies get leading dimensions rounded up to 4 floats and 256-byte
-// aligned bases from the stream-ordered pool, so every block can take the
-// TMA-fed kernels whatever the host layout.  The whole sequence is ordered
-// after the work already on the caller's stream, and the caller's stream waits
-// for all of it, so the call is asynchronous exactly like sgemm().
+// Three library-owned streams per device:
+//   h2d   copies B once, then op(A) and C of each row block of C, in order;
+//   comp  runs the GEMM of each row block as soon as its inputs are in;
+//   d2h   copies each finished row block of C back to the host.
+// The host link is the slowest part (B alone is a quarter to a half of the
+// bytes that cross it), so copies are issued strictly in the order the GEMMs
+// need them: the first GEMM starts after B and the first block, and from
+// then on the GEMMs, the remaining host-to-device copies and the
+// device-to-host copies of finished blocks overlap.  Row blocks rotate
+// through kSets device buffer sets; a set is refilled only after its GEMM has
+// read it and its C has left.  Device copies get leading dimensions rounded
+// up to 4 floats and 256-byte aligned bases from the stream-ordered pool, so
+// every block can take the TMA-fed kernels whatever the host layout.  The
+// whole sequence is ordered after the work already on the caller's stream,
+// and the caller's stream waits for all of it, so the call is asynchronous
+// exactly like sgemm().
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
@@ -18,12 +26,14 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kSets = 3;  // device buffer sets for row blocks in flight
 
 struct HostPipeDevice {
   std::once_flag once;
   cudaError_t err = cudaSuccess;
-  cudaStream_t s[2] = {nullptr, nullptr};
-  cudaEvent_t ev_start = nullptr, ev_b = nullptr, ev_done[2] = {nullptr, nullptr};
+  cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_done = nullptr, ev_h2d_end = nullptr, ev_comp_end = nullptr;
+  cudaEvent_t ev_in[kSets] = {}, ev_gemm[kSets] = {}, ev_out[kSets] = {};
   cudaMemPool_t pool = nullptr;
   std::mutex mu;  // one enqueue sequence at a time per device (the events are shared)
 };
@@ -34,11 +44,17 @@ int64_t round4(int64_t x) { return (x + 3) / 4 * 4; }
 cudaError_t setup(int dev, HostPipeDevice** out) {
   HostPipeDevice& d = g_hp[dev];
   std::call_once(d.once, [&] {
-    cudaError_t e = cudaSuccess;
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&d.s[i], cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_start, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_b, cudaEventDisableTiming);
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&d.ev_done[i], cudaEventDisableTiming);
+    cudaError_t e = cudaStreamCreateWithFlags(&d.h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d.comp, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d.d2h, cudaStreamNonBlocking);
+    cudaEvent_t* evs[] = {&d.ev_start, &d.ev_done, &d.ev_h2d_end, &d.ev_comp_end};
+    for (cudaEvent_t* ev : evs)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    for (int i = 0; i < kSets && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&d.ev_in[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_gemm[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_out[i], cudaEventDisableTiming);
+    }
     if (e == cudaSuccess) {
       cudaMemPoolProps props = {};
       props.allocType = cudaMemAllocationTypePinned;
@@ -89,6 +105,7 @@ extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_
   const int64_t nblocks = std::max<int64_t>(1, std::min<int64_t>(8, M / 512));
   int64_t mb = ((M + nblocks - 1) / nblocks + 127) / 128 * 128;
   if (mb > M) mb = M;
+  const int nsets = (int)std::min<int64_t>(kSets, (M + mb - 1) / mb);
   // Device leading dimensions (multiples of 4 floats).
   const int64_t b_rows = tb ? N : K, b_cols = tb ? K : N;  // stored B
   const int64_t ldb_d = round4(std::max<int64_t>(b_cols, 1));
@@ -97,82 +114,91 @@ extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_
   const int64_t ldc_d = round4(N);
 
   float* dB = nullptr;
-  float* dA[2] = {nullptr, nullptr};
-  float* dC[2] = {nullptr, nullptr};
+  float* dA[kSets] = {};
+  float* dC[kSets] = {};
   int status = SGEMM_OK;
   auto fail = [&](cudaError_t err) {
     if (status == SGEMM_OK) status = status_of(err);
   };
 
   e = cudaEventRecord(d->ev_start, user);
-  for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(d->s[i], d->ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(d->h2d, d->ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(d->comp, d->ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(d->d2h, d->ev_start, 0);
   if (e != cudaSuccess) return SGEMM_ERR_CUDA;
 
-  // B once, on stream 0.
+  // Buffers (ordered on h2d; the other streams use them only after its events), then B.
   if (reads_ab) {
-    e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dB), (size_t)(b_rows * ldb_d * 4), d->pool, d->s[0]);
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dB), (size_t)(b_rows * ldb_d * 4), d->pool, d->h2d);
     if (e == cudaSuccess)
       e = cudaMemcpy2DAsync(dB, (size_t)ldb_d * 4, B, (size_t)ldb * 4, (size_t)b_cols * 4, (size_t)b_rows,
-                            cudaMemcpyHostToDevice, d->s[0]);
-    if (e == cudaSuccess) e = cudaEventRecord(d->ev_b, d->s[0]);
+                            cudaMemcpyHostToDevice, d->h2d);
     if (e != cudaSuccess) fail(e);
   }
-  for (int i = 0; i < 2 && status == SGEMM_OK; ++i) {
+  for (int i = 0; i < nsets && status == SGEMM_OK; ++i) {
     if (reads_ab) {
-      e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dA[i]), (size_t)(a_rows * lda_d * 4), d->pool, d->s[i]);
+      e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dA[i]), (size_t)(a_rows * lda_d * 4), d->pool, d->h2d);
       if (e != cudaSuccess) fail(e);
     }
-    e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dC[i]), (size_t)(mb * ldc_d * 4), d->pool, d->s[i]);
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dC[i]), (size_t)(mb * ldc_d * 4), d->pool, d->h2d);
     if (e != cudaSuccess) fail(e);
   }
 
   for (int64_t r0 = 0, blk = 0; r0 < M && status == SGEMM_OK; r0 += mb, ++blk) {
-    const int i = (int)(blk & 1);
-    cudaStream_t s = d->s[i];
+    const int i = (int)(blk % nsets);
     const int64_t rows = std::min<int64_t>(mb, M - r0);
+    // h2d: refill set i once its previous GEMM has read it and its C has left
+    if (blk >= nsets) {
+      e = cudaStreamWaitEvent(d->h2d, d->ev_gemm[i], 0);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(d->h2d, d->ev_out[i], 0);
+      if (e != cudaSuccess) { fail(e); break; }
+    }
     if (reads_ab) {
       // op(A) rows r0 .. r0+rows: stored rows for 'N', stored columns for 'T'
       if (!ta)
         e = cudaMemcpy2DAsync(dA[i], (size_t)lda_d * 4, A + r0 * lda, (size_t)lda * 4, (size_t)K * 4, (size_t)rows,
-                              cudaMemcpyHostToDevice, s);
+                              cudaMemcpyHostToDevice, d->h2d);
       else
         e = cudaMemcpy2DAsync(dA[i], (size_t)lda_d * 4, A + r0, (size_t)lda * 4, (size_t)rows * 4, (size_t)K,
-                              cudaMemcpyHostToDevice, s);
+                              cudaMemcpyHostToDevice, d->h2d);
       if (e != cudaSuccess) { fail(e); break; }
     }
     if (reads_c) {
       e = cudaMemcpy2DAsync(dC[i], (size_t)ldc_d * 4, C + r0 * ldc, (size_t)ldc * 4, (size_t)N * 4, (size_t)rows,
-                            cudaMemcpyHostToDevice, s);
+                            cudaMemcpyHostToDevice, d->h2d);
       if (e != cudaSuccess) { fail(e); break; }
     }
-    // only the GEMM needs B; stream 1's first copies already ran beside B's
-    if (reads_ab && i == 1 && blk == 1) {
-      e = cudaStreamWaitEvent(s, d->ev_b, 0);
-      if (e != cudaSuccess) { fail(e); break; }
-    }
+    e = cudaEventRecord(d->ev_in[i], d->h2d);
+    // comp: the block's GEMM (the GEMMs run one after another, each on the whole GPU)
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->comp, d->ev_in[i], 0);
+    if (e != cudaSuccess) { fail(e); break; }
     st = sgemm(transA, transB, rows, N, K, alpha, dA[i], lda_d, dB, ldb_d, beta, dC[i], ldc_d,
-               reinterpret_cast<struct CUstream_st*>(s));
+               reinterpret_cast<struct CUstream_st*>(d->comp));
     if (st != SGEMM_OK) { status = st; break; }
-    e = cudaMemcpy2DAsync(C + r0 * ldc, (size_t)ldc * 4, dC[i], (size_t)ldc_d * 4, (size_t)N * 4, (size_t)rows,
-                          cudaMemcpyDeviceToHost, s);
+    e = cudaEventRecord(d->ev_gemm[i], d->comp);
+    // d2h: the block's C back to the host
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->d2h, d->ev_gemm[i], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(C + r0 * ldc, (size_t)ldc * 4, dC[i], (size_t)ldc_d * 4, (size_t)N * 4, (size_t)rows,
+                            cudaMemcpyDeviceToHost, d->d2h);
+    if (e == cudaSuccess) e = cudaEventRecord(d->ev_out[i], d->d2h);
     if (e != cudaSuccess) { fail(e); break; }
   }
 
-  // Free in stream order and make the caller's stream wait for both streams.
-  for (int i = 0; i < 2; ++i) {
-    if (dA[i]) cudaFreeAsync(dA[i], d->s[i]);
-    if (dC[i]) cudaFreeAsync(dC[i], d->s[i]);
+  // Free in stream order once all three streams are done with the buffers,
+  // then make the caller's stream wait for all of it.
+  e = cudaEventRecord(d->ev_h2d_end, d->h2d);
+  if (e == cudaSuccess) e = cudaEventRecord(d->ev_comp_end, d->comp);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(d->d2h, d->ev_h2d_end, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(d->d2h, d->ev_comp_end, 0);
+  if (e != cudaSuccess) fail(e);
+  for (int i = 0; i < kSets; ++i) {
+    if (dA[i]) cudaFreeAsync(dA[i], d->d2h);
+    if (dC[i]) cudaFreeAsync(dC[i], d->d2h);
   }
-  if (dB) {
-    // stream 1 may still read B: free it after both streams are done
-    cudaEventRecord(d->ev_done[1], d->s[1]);
-    cudaStreamWaitEvent(d->s[0], d->ev_done[1], 0);
-    cudaFreeAsync(dB, d->s[0]);
-  }
-  for (int i = 0; i < 2; ++i) {
-    e = cudaEventRecord(d->ev_done[i], d->s[i]);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(user, d->ev_done[i], 0);
-    if (e != cudaSuccess) fail(e);
-  }
+  if (dB) cudaFreeAsync(dB, d->d2h);
+  e = cudaEventRecord(d->ev_done, d->d2h);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(user, d->ev_done, 0);
+  if (e != cudaSuccess) fail(e);
   return status;
 }
