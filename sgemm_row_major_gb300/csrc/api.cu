@@ -171,7 +171,7 @@ int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
   if (ov_split > 0) {
     dp_tiles = 0;
     sk_tiles = tiles;
-    grid = std::min<int64_t>({tiles * ov_split, tiles * kt, int64_t{1} << 20});
+    grid = std::min<int64_t>({tiles * std::min(ov_split, 128), tiles * kt, int64_t{1} << 20});
   } else if (tiles >= sms) {
     grid = sms;
     sk_tiles = tiles % sms ? sms + tiles % sms : 0;
@@ -180,10 +180,11 @@ int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
   } else {
     dp_tiles = 0;
     sk_tiles = tiles;
+    // (at most 254 CTAs per tile: the fixup kernel handles up to 256 sharers of a tile)
     if (tiles * kt / sms >= kMinStreamKIters) {
-      grid = sms;
+      grid = std::min<int64_t>(sms, tiles * 254);
     } else {
-      const int64_t split = std::max<int64_t>(1, std::min<int64_t>(sms / tiles, kt / 4));
+      const int64_t split = std::max<int64_t>(1, std::min<int64_t>({sms / tiles, kt / 4, 254}));
       grid = tiles * split;
     }
   }
@@ -200,7 +201,8 @@ int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
     const int64_t c1 = ((i1 + 1) * grid + sk_iters - 1) / sk_iters - 1;
     most = std::max(most, c1 - c0 + 1);
   }
-  plan->split_k = (int)std::min<int64_t>(most, INT_MAX);
+  if (most > 256) return SGEMM_ERR_UNSUPPORTED;  // the fixup kernel's limit (cannot happen: <= SMs/tiles + 2)
+  plan->split_k = (int)most;
   plan->kernel_launches = most > 1 ? 2 : 1;
   plan->grid_x = grid;
   plan->grid_y = 1;

@@ -74,6 +74,13 @@ constexpr int kRawBytes = 2 * kTileBytes;           // A + B as loaded
 constexpr int kSplitBytes = 2 * kTileBytes;         // B_hi, B_lo (A's parts live in TMEM)
 constexpr int kSmemBytes = kRawStages * kRawBytes + kSplitStages * kSplitBytes + 1024;
 constexpr int kSplitWarps = 8;                      // warps 2-9
+// The splitters work in two independent groups of 4 warps, one per 16-k half
+// of a K tile (warps 2-5: k 0-15, warps 6-9: k 16-31).  Each half of a split
+// stage has its own full/empty barriers, so the MMAs of a half start as soon
+// as that half is split, and a half is refilled as soon as its 6 MMAs have
+// read it.
+constexpr int kHalves = 2;
+constexpr int kHalfWarps = kSplitWarps / kHalves;
 constexpr int kSplitters = 32 * kSplitWarps;
 constexpr int kFoldWarps = 8;                       // warps 10-17
 constexpr int kFirstFoldWarp = 2 + kSplitWarps;
@@ -90,6 +97,8 @@ static_assert(kFoldTiles == 1, "the folders walk the CTA's segments one accumula
 constexpr uint32_t kACols = 64;                     // A hi (32 k) + A lo (32 k) of one split stage
 constexpr uint32_t kAColBase = kAccBufs * kAccCols;
 constexpr uint32_t kTmemCols = 512;                 // 3 accumulators + 2 A stages = 512
+static_assert(kAColBase + kSplitStages * kACols <= kTmemCols, "accumulators and A stages must fit in TMEM");
+static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA");
 
 // tcgen05 instruction descriptor, kind::tf32: FP32 accumulator, TF32 A and B,
 // both K-major, N = 128, M = 128.
@@ -241,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kRawStages], raw_empty[kRawStages];
-  __shared__ __align__(8) uint64_t split_full[kSplitStages], split_empty[kSplitStages];
+  __shared__ __align__(8) uint64_t split_full[kSplitStages][kHalves], split_empty[kSplitStages][kHalves];
   __shared__ __align__(8) uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   __shared__ uint32_t tmem_slot;
   __shared__ CtaWork work_s;  // this CTA's schedule, written once by thread 0 (kept out of registers)
@@ -269,8 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&raw_empty[r]), kSplitWarps);
     }
     for (int s = 0; s < kSplitStages; ++s) {
-      mbar_init(smem_addr(&split_full[s]), kSplitWarps);
-      mbar_init(smem_addr(&split_empty[s]), 1);
+      for (int h = 0; h < kHalves; ++h) {
+        mbar_init(smem_addr(&split_full[s][h]), kHalfWarps);
+        mbar_init(smem_addr(&split_empty[s][h]), 1);
+      }
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(smem_addr(&acc_full[b]), 1);
@@ -339,23 +350,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acc = tmem + (uint32_t)b * kAccCols;
         for (int t = c * kFoldTiles; t < min(nkt, (c + 1) * kFoldTiles); ++t) {
           const int s = t % kSplitStages;
-          if (!mbar_wait(smem_addr(&split_full[s]), (uint32_t)(t / kSplitStages) & 1u, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          tmem_fence_after_sync();
           const uint32_t ahi = tmem + kAColBase + (uint32_t)s * kACols, alo = ahi + 32u;
           const uint64_t bhi = kmajor_sw128_desc(split_tile(s, 0)), blo = kmajor_sw128_desc(split_tile(s, 1));
           const bool first = t == c * kFoldTiles;
 #pragma unroll
-          for (int ks = 0; ks < BK / 8; ++ks) {
-            const uint64_t step = (uint64_t)(ks * 32) >> 4;  // 8 TF32 = 32 bytes along K
-            const uint32_t acol = (uint32_t)(8 * ks);        // 8 TF32 = 8 TMEM columns
-            mma_tf32_ts(acc, alo + acol, bhi + step, (first && ks == 0) ? 0u : 1u);  // fresh accumulator per chunk
-            mma_tf32_ts(acc, ahi + acol, blo + step, 1u);
-            mma_tf32_ts(acc, ahi + acol, bhi + step, 1u);
+          for (int h = 0; h < kHalves; ++h) {
+            if (!mbar_wait(smem_addr(&split_full[s][h]), (uint32_t)(t / kSplitStages) & 1u, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tmem_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < BK / 8 / kHalves; ++kk) {
+              const int ks = h * (BK / 8 / kHalves) + kk;
+              const uint64_t step = (uint64_t)(ks * 32) >> 4;  // 8 TF32 = 32 bytes along K
+              const uint32_t acol = (uint32_t)(8 * ks);        // 8 TF32 = 8 TMEM columns
+              mma_tf32_ts(acc, alo + acol, bhi + step, (first && ks == 0) ? 0u : 1u);  // fresh accumulator per chunk
+              mma_tf32_ts(acc, ahi + acol, blo + step, 1u);
+              mma_tf32_ts(acc, ahi + acol, bhi + step, 1u);
+            }
+            mma_commit(smem_addr(&split_empty[s][h]));  // this half reusable once these MMAs have read it
           }
-          mma_commit(smem_addr(&split_empty[s]));  // split stage reusable once these MMAs have read it
+          if (!ok) break;
         }
         mma_commit(smem_addr(&acc_full[b]));  // accumulator b holds chunk c
         done = c;
@@ -375,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = t % kRawStages, s = t % kSplitStages;
       bool w = warp_wait(smem_addr(&raw_full[r]), (uint32_t)(t / kRawStages) & 1u, p.timeout_ns);
       if (w && t >= kSplitStages)
-        w = warp_wait(smem_addr(&split_empty[s]), (uint32_t)((t / kSplitStages) - 1) & 1u, p.timeout_ns);
+        w = warp_wait(smem_addr(&split_empty[s][half]), (uint32_t)((t / kSplitStages) - 1) & 1u, p.timeout_ns);
       if (!w) {
         if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
         break;
@@ -411,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(ta, hi);
         tmem_st16(ta + 32u, lo);
       }
-      // B -> K-major [128 n][32 k], 128-byte swizzle, the layout the descriptors describe.
+      // B -> K-major [128 n][32 k], 128-byte swizzle, the layout the descriptors describe;
+      // this group writes the 16 k of its half (st / 128 == half).
       {
         uint8_t* bhi = smem + (split_tile(s, 0) - sbase);
         uint8_t* blo = smem + (split_tile(s, 1) - sbase);
@@ -431,11 +448,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float4*>(blo + off) = lo;
           }
         } else {
-          // raw is already K-major and swizzled: split 16-byte chunks in place
+          // raw is already K-major and swizzled: split this half's 16-byte chunks in place
+          // (thread st: row n = st % 128, logical k chunks 4*(st/128) .. +3)
           const uint8_t* rb = smem + (raw_b(r) - sbase);
+          const int n = st & 127, kh = st >> 7;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t off = (uint32_t)(st + kSplitters * j) * 16u;
+          for (int kq = 0; kq < 4; ++kq) {
+            const int kc = 4 * kh + kq;
+            const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(kc ^ (n & 7)) << 4);
             float4 hi, lo;
             split4(*reinterpret_cast<const float4*>(rb + off), hi, lo);
             *reinterpret_cast<float4*>(bhi + off) = hi;
@@ -448,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_addr(&split_full[s]));
+        mbar_arrive(smem_addr(&split_full[s][half]));
         mbar_arrive(smem_addr(&raw_empty[r]));
       }
     }
@@ -546,13 +566,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 // their slots, in CTA order) + beta * C over the in-range elements.  The
 // order is fixed, so the result does not depend on scheduling.
 constexpr int kFixupRowsPerCta = 8;
+constexpr int kFixupThreads = 256;
+constexpr int kMaxSharers = 256;  // CTAs that may share one tile (the planner keeps to it)
 template <bool CVEC>
-__global__ void __launch_bounds__(256) streamk_fixup_kernel(const GemmParams p) {
+__global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(const GemmParams p) {
+  __shared__ int s_n;
+  __shared__ int s_slot[kMaxSharers];
   const int kt = (p.K + BK - 1) / BK;
   const int j = (int)blockIdx.x;
-  const int64_t i0 = (int64_t)j * kt;
-  const int c0 = sk_owner(p, i0), c1 = sk_owner(p, i0 + kt - 1);
-  if (c0 == c1) return;  // one CTA covered the whole tile and wrote C itself
+  // the tile's sharers and their slots, once per CTA (64-bit divisions stay off the threads' path)
+  if (threadIdx.x == 0) {
+    const int64_t i0 = (int64_t)j * kt;
+    const int c0 = sk_owner(p, i0), c1 = sk_owner(p, i0 + kt - 1);
+    s_n = min(c1 - c0 + 1, kMaxSharers);
+    s_slot[0] = c0;
+  }
+  __syncthreads();
+  const int n = s_n;
+  if (n == 1) return;  // one CTA covered the whole tile and wrote C itself
+  const int c0 = s_slot[0];
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kFixupThreads) s_slot[i] = sk_slot(p, c0 + i, j, kt);
+  __syncthreads();
   int prod, m0, n0;
   tile_origin(p, p.sk_tile0 + j, prod, m0, n0);
   const int r = (int)blockIdx.y * kFixupRowsPerCta + (int)(threadIdx.x >> 5);
@@ -560,10 +595,10 @@ __global__ void __launch_bounds__(256) streamk_fixup_kernel(const GemmParams p) 
   const int row = m0 + r, col = n0 + cc;
   if (row >= p.M || col >= p.N) return;
   const float* w = p.ws + r * BN + cc;
-  float4 v = *reinterpret_cast<const float4*>(w + (int64_t)sk_slot(p, c0, j, kt) * (BM * BN));
+  float4 v = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[0] * (BM * BN));
 #pragma unroll 4
-  for (int c = c0 + 1; c <= c1; ++c) {
-    const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)sk_slot(p, c, j, kt) * (BM * BN));
+  for (int i = 1; i < n; ++i) {
+    const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[i] * (BM * BN));
     v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
   }
   float* cp = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
@@ -621,9 +656,9 @@ cudaError_t launch_tf32x3(bool transA, bool transB, const CUtensorMap& mapA, con
 cudaError_t launch_streamk_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream) {
   const dim3 grid((unsigned)sk_tiles, tc::BM / tc::kFixupRowsPerCta);
   if (p.c_vec)
-    tc::streamk_fixup_kernel<true><<<grid, 256, 0, stream>>>(p);
+    tc::streamk_fixup_kernel<true><<<grid, tc::kFixupThreads, 0, stream>>>(p);
   else
-    tc::streamk_fixup_kernel<false><<<grid, 256, 0, stream>>>(p);
+    tc::streamk_fixup_kernel<false><<<grid, tc::kFixupThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
