@@ -270,6 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int cta = (int)blockIdx.x;
   const int kt_total = (p.K + BK - 1) / BK;
+  // the fixup kernel launched after this one (programmatic dependent launch) may be
+  // scheduled now; it waits for this grid to complete before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     work_s = cta_work(p, cta, kt_total);
@@ -572,6 +575,9 @@ template <bool CVEC>
 __global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(const GemmParams p) {
   __shared__ int s_n;
   __shared__ int s_slot[kMaxSharers];
+  // launched as a programmatic dependent of the GEMM kernel: wait for that grid to
+  // complete and its writes to be visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int kt = (p.K + BK - 1) / BK;
   const int j = (int)blockIdx.x;
   // the tile's sharers and their slots, once per CTA (64-bit divisions stay off the threads' path)
@@ -654,12 +660,18 @@ cudaError_t launch_tf32x3(bool transA, bool transB, const CUtensorMap& mapA, con
 }
 
 cudaError_t launch_streamk_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream) {
-  const dim3 grid((unsigned)sk_tiles, tc::BM / tc::kFixupRowsPerCta);
-  if (p.c_vec)
-    tc::streamk_fixup_kernel<true><<<grid, tc::kFixupThreads, 0, stream>>>(p);
-  else
-    tc::streamk_fixup_kernel<false><<<grid, tc::kFixupThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sk_tiles, tc::BM / tc::kFixupRowsPerCta);
+  cfg.blockDim = dim3(tc::kFixupThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the GEMM kernel ends
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return p.c_vec ? cudaLaunchKernelEx(&cfg, tc::streamk_fixup_kernel<true>, p)
+                 : cudaLaunchKernelEx(&cfg, tc::streamk_fixup_kernel<false>, p);
 }
 
 }  // namespace sgemm_impl
