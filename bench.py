@@ -179,14 +179,36 @@ def cpu_rows_for(case, d, seconds: float):
     return list(range(n))
 
 
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return os.uname().machine
+
+
 def cpu_baseline(case, d, seconds):
     import oracle
+    cores = oracle.num_threads()
     rows = cpu_rows_for(case, d, seconds)
     t = oracle_sample_run(case, d, rows)
     flops = si.flops(len(rows), case.N, case.K)
-    return {"value": flops / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{len(rows)} of {case.M} rows of C ({len(rows)}x{case.N}x{case.K}, "
-                      f"{flops / 1e9:.2f} GFLOP) in {t:.1f} s; TFLOPS = 2*rows*N*K/t"}
+    out = {"value": flops / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"{len(rows)} of {case.M} rows of C ({len(rows)}x{case.N}x{case.K}, "
+                     f"{flops / 1e9:.2f} GFLOP) in {t:.1f} s; TFLOPS = 2*rows*N*K/t",
+           "cpu": cpu_model()}
+    # the same oracle on one core, for a per-core figure
+    oracle.set_num_threads(1)
+    try:
+        rows1 = cpu_rows_for(case, d, min(3.0, seconds / 4))
+        t1 = oracle_sample_run(case, d, rows1)
+        out["per_core"] = {"value": si.flops(len(rows1), case.N, case.K) / t1 / 1e12, "unit": UNIT,
+                           "sample": f"{len(rows1)} rows in {t1:.2f} s on 1 thread"}
+    finally:
+        oracle.set_num_threads(cores)
+    return out
 
 
 def reduce_max_ms(ms: float, world: int, device=None) -> float:
@@ -241,7 +263,6 @@ def config_block(case, n_gpus):
     return {"workload": f"sgemm_{case.transA}{case.transB}_{case.M}x{case.N}x{case.K}",
             "name": case.name, "M": case.M, "N": case.N, "K": case.K, "ops": case.ops,
             "alpha": case.alpha, "beta": case.beta, "inputs": case.dist, "layout": "row-major fp32",
-            "l2": "two input sets used in turn, each larger than the 129 MB L2; no flush kernel",
             "parallelism": f"replicas x{n_gpus}"}
 
 
@@ -283,11 +304,30 @@ def cublas_context(case, sets, steps, stream):
         torch.backends.cuda.matmul.allow_tf32 = prev
 
 
-def timed_steps(step, args, stream, dev, local, barrier, world):
+L2_BYTES = 129 * 1000 * 1000  # GB300 L2
+
+
+def l2_flusher(dev, set_bytes):
+    """A step-separating L2 flush (a memset of 2x the L2 size) when one input set fits in L2, else None."""
+    import torch
+    if set_bytes >= L2_BYTES:
+        return None
+    buf = torch.empty(2 * L2_BYTES + (1 << 20), dtype=torch.uint8, device=dev)
+    state = {"v": 0}
+
+    def flush():
+        state["v"] = (state["v"] + 1) & 0xFF
+        buf.fill_(state["v"])
+    return flush
+
+
+def timed_steps(step, args, stream, dev, local, barrier, world, flush=None):
     """Pre-warm, W warm-up steps, then exactly K timed steps between barriers.
 
-    Returns (per-step kernel ms from CUDA events on `stream`, the slowest
-    rank's total ms, the clock summary sampled during the timed region)."""
+    With `flush`, L2 is flushed before every step (outside the step's events)
+    and the job time is the sum of the steps' event times.  Returns (per-step
+    ms from CUDA events on `stream`, the slowest rank's job ms, the clock
+    summary sampled during the timed region)."""
     import torch
     t_end = time.time() + args.prewarm_s
     i = 0
@@ -310,6 +350,8 @@ def timed_steps(step, args, stream, dev, local, barrier, world):
     g1 = torch.cuda.Event(enable_timing=True)
     g0.record(stream)
     for s in range(args.steps):
+        if flush:
+            flush()
         ev[s][0].record(stream)
         step(s)
         ev[s][1].record(stream)
@@ -319,8 +361,19 @@ def timed_steps(step, args, stream, dev, local, barrier, world):
     time.sleep(0.1)
     sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = reduce_max_ms(g0.elapsed_time(g1), world, dev)
+    job_ms = sum(step_ms) if flush else g0.elapsed_time(g1)
+    total_ms = reduce_max_ms(job_ms, world, dev)
     return step_ms, total_ms, sampler.summary(t0_wall, t1_wall)
+
+
+def step_stats(step_ms):
+    return {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)}
+
+
+def l2_note(flush):
+    return ("L2 flushed before every step (2x L2 memset outside the step's events); value from the "
+            "steps' event times" if flush else
+            "two input sets used in turn, each larger than the 129 MB L2; no flush")
 
 
 def tensor_roofline(achieved, peaks, traffic, kernel_ms):
@@ -382,7 +435,8 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    step_ms, total_ms, clocks = timed_steps(step, args, stream, dev, local, barrier, world)
+    flush = l2_flusher(dev, sum(x.numel() * 4 for x in sets[0]))
+    step_ms, total_ms, clocks = timed_steps(step, args, stream, dev, local, barrier, world, flush)
     if sg.sgemm_sync_status(sh) != 0:
         raise RuntimeError("libsgemm reported a kernel fault during the benchmark")
     flops_step = si.flops(M, N, K)
@@ -440,7 +494,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {**config_block(case, world), "prewarm_s": args.prewarm_s,
+        "step_ms": step_stats(step_ms),
+        "config": {**config_block(case, world), "l2": l2_note(flush), "prewarm_s": args.prewarm_s,
                    "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "tile_k", "stages",
                                                  "split_k", "grid_x", "grid_y", "dp_tiles", "sk_tiles")}},
         "pct_ffma_peak": 100.0 * achieved / ffma_peak,
@@ -470,7 +525,6 @@ def batched_config_block(c, d, n_gpus):
             "name": c.name, "batch": c.batch, "M": c.M, "N": c.N, "K": c.K, "ops": c.ops,
             "alpha": c.alpha, "beta": c.beta, "inputs": c.dist, "shared": c.shared or "none",
             "strides": {k: d["stride" + k] for k in "ABC"}, "layout": "row-major fp32, packed products",
-            "l2": "two input sets used in turn, each larger than the 129 MB L2; no flush kernel",
             "parallelism": f"replicas x{n_gpus}"}
 
 
@@ -555,7 +609,8 @@ def run_ours_batched(args, c):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    step_ms, total_ms, clocks = timed_steps(step, args, stream, dev, local, barrier, world)
+    flush = l2_flusher(dev, sum(x.numel() * 4 for x in sets[0]))
+    step_ms, total_ms, clocks = timed_steps(step, args, stream, dev, local, barrier, world, flush)
     if sg.sgemm_sync_status(sh) != 0:
         raise RuntimeError("libsgemm reported a kernel fault during the benchmark")
     flops_step = c.batch * si.flops(c.M, c.N, c.K)
@@ -571,7 +626,8 @@ def run_ours_batched(args, c):
         "metric": BATCHED_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {**batched_config_block(c, d, world), "prewarm_s": args.prewarm_s,
+        "step_ms": step_stats(step_ms),
+        "config": {**batched_config_block(c, d, world), "l2": l2_note(flush), "prewarm_s": args.prewarm_s,
                    "plan": {k: plan[k] for k in ("variant_name", "split_k", "grid_x", "grid_y", "dp_tiles",
                                                  "sk_tiles")}},
         "roofline": (tensor_roofline(achieved, peaks, None, kernel_ms) if plan["variant_name"] == "TC_TF32X3"

@@ -82,6 +82,8 @@ def load_library(path: str) -> ctypes.CDLL:
                   i64, vp, i64, i64]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
+    lib.oracle_set_num_threads.restype = None
+    lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
     return lib
 
 
@@ -91,6 +93,11 @@ def _library() -> ctypes.CDLL:
         if _lib is None:
             _lib = load_library(build())
         return _lib
+
+
+def set_num_threads(n: int) -> None:
+    """Threads later oracle calls use (the arithmetic of an element does not depend on it)."""
+    _library().oracle_set_num_threads(int(n))
 
 
 def num_threads() -> int:

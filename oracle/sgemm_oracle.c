@@ -131,6 +131,16 @@ int oracle_sgemm_strided_batched(char transA, char transB, int64_t M, int64_t N,
     return 0;
 }
 
+/* Sets the number of OpenMP threads later oracle calls use (n >= 1). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Number of OpenMP threads a parallel region of the oracle uses. */
 int oracle_num_threads(void)
 {
