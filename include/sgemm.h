@@ -37,7 +37,10 @@
  * results meet |C - C_exact| <= (K+2) 2^-24 (|alpha| sum|a b| + |beta c|) and
  * are deterministic, but are not the IEEE FP32 FMA sums of a SIMT loop, and
  * an Inf in A or B may give NaN where IEEE arithmetic gives Inf (a NaN input
- * gives NaN on every path).  The FP32 FFMA kernels (IEEE operations, exact Inf
+ * gives NaN on every path); so may a finite input within 2^-11 of FLT_MAX,
+ * whose TF32 part rounds up to Inf.  Scaling A and B by powers of two scales C
+ * exactly, as in FP32 arithmetic, down to products near the FP32 subnormal
+ * range.  The FP32 FFMA kernels (IEEE operations, exact Inf
  * handling) are selected with sgemm_set_variant_override(SGEMM_VARIANT_TMA_128x128
  * or SGEMM_VARIANT_TMA_64x256, 0); unaligned operands always use the FFMA path.
  *

@@ -66,3 +66,19 @@ def test_config_parity(name):
     else:
         worst, frob = check_bound(g, ref, S, c.K, name)
         print(f"{name}: worst err/bound {worst:.3g}, relative Frobenius {frob:.3g}")
+
+
+@pytest.mark.parametrize("variant", [V, "TMA_128x128"])
+@pytest.mark.parametrize("e", [-24, 24])
+def test_power_of_two_scaling_is_exact(variant, e):
+    """Scaling A and B by 2^e scales every split part, product and sum exactly, so C(2^e A, 2^e B)
+    equals 2^(2e) C(A, B) bit for bit (no flushed partial products, no overflow in the split)."""
+    rng = np.random.default_rng(50 + e)
+    M, N, K = 192, 320, 700
+    A = (2 * rng.random((M, K)) - 1).astype(np.float32)
+    B = (2 * rng.random((K, N)) - 1).astype(np.float32)
+    C = np.zeros((M, N), np.float32)
+    base = gpu_sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C, N, variant=variant)
+    s = np.float32(2.0 ** e)
+    scaled = gpu_sgemm("N", "N", M, N, K, 1.0, A * s, K, B * s, N, 0.0, C, N, variant=variant)
+    check_exact(scaled, base * np.float32(2.0 ** (2 * e)), f"{variant} scale 2^{e}")
