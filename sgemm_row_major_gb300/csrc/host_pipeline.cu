@@ -1,14 +1,17 @@
 // host_pipeline.cu -- sgemm_host(): SGEMM on operands that live in host memory.
 //
 // Three library-owned streams per device:
-//   h2d   copies B once, then op(A) and C of each row block of C, in order;
+//   h2d   copies op(A) and C of each row block of C, and B once, in order;
 //   comp  runs the GEMM of each row block as soon as its inputs are in;
 //   d2h   copies each finished row block of C back to the host.
 // The host link is the slowest part (B alone is a quarter to a half of the
 // bytes that cross it), so copies are issued strictly in the order the GEMMs
-// need them: the first GEMM starts after B and the first block, and from
-// then on the GEMMs, the remaining host-to-device copies and the
-// device-to-host copies of finished blocks overlap.  Row blocks rotate
+// need them: the first block's op(A) and C, then B in kBChunks K-chunks --
+// the GEMM of the first block (of the first kChunkedBlocks blocks) runs one
+// per chunk (beta on the first, 1 after), each as soon as its chunk of B is
+// in -- then the other blocks; from then on the GEMMs, the remaining
+// host-to-device copies and the device-to-host copies of finished blocks
+// overlap.  Row blocks rotate
 // through kSets device buffer sets; a set is refilled only after its GEMM has
 // read it and its C has left.  Device copies get leading dimensions rounded
 // up to 4 floats and 256-byte aligned bases from the stream-ordered pool, so
@@ -26,7 +29,10 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kSets = 3;  // device buffer sets for row blocks in flight
+constexpr int kSets = 3;     // device buffer sets for row blocks in flight
+constexpr int kBChunks = 4;        // K-chunks of B when K is large enough
+constexpr int kChunkedBlocks = 1;  // first row blocks whose GEMMs run chunk by chunk as B arrives
+                                   // (2 measured no faster: the later blocks' GEMMs then bound the call)
 
 struct HostPipeDevice {
   std::once_flag once;
@@ -34,6 +40,7 @@ struct HostPipeDevice {
   cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
   cudaEvent_t ev_start = nullptr, ev_done = nullptr, ev_h2d_end = nullptr, ev_comp_end = nullptr;
   cudaEvent_t ev_in[kSets] = {}, ev_gemm[kSets] = {}, ev_out[kSets] = {};
+  cudaEvent_t ev_b[kBChunks] = {};
   cudaMemPool_t pool = nullptr;
   std::mutex mu;  // one enqueue sequence at a time per device (the events are shared)
 };
@@ -50,6 +57,8 @@ cudaError_t setup(int dev, HostPipeDevice** out) {
     cudaEvent_t* evs[] = {&d.ev_start, &d.ev_done, &d.ev_h2d_end, &d.ev_comp_end};
     for (cudaEvent_t* ev : evs)
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    for (int i = 0; i < kBChunks && e == cudaSuccess; ++i)
+      e = cudaEventCreateWithFlags(&d.ev_b[i], cudaEventDisableTiming);
     for (int i = 0; i < kSets && e == cudaSuccess; ++i) {
       e = cudaEventCreateWithFlags(&d.ev_in[i], cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_gemm[i], cudaEventDisableTiming);
@@ -112,6 +121,9 @@ extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_
   const int64_t a_rows = ta ? K : mb, a_cols = ta ? mb : K;  // stored A block
   const int64_t lda_d = round4(std::max<int64_t>(a_cols, 1));
   const int64_t ldc_d = round4(N);
+  // K-chunks of B: multiples of 32 floats, so every chunk of A and B starts 128-byte aligned
+  const int nq = (reads_ab && K >= kBChunks * 256) ? kBChunks : 1;
+  const int64_t kc = ((K + nq - 1) / nq + 31) / 32 * 32;
 
   float* dB = nullptr;
   float* dA[kSets] = {};
@@ -127,14 +139,20 @@ extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_
   if (e == cudaSuccess) e = cudaStreamWaitEvent(d->d2h, d->ev_start, 0);
   if (e != cudaSuccess) return SGEMM_ERR_CUDA;
 
-  // Buffers (ordered on h2d; the other streams use them only after its events), then B.
+  // Buffers (ordered on h2d; the other streams use them only after its events).
   if (reads_ab) {
     e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dB), (size_t)(b_rows * ldb_d * 4), d->pool, d->h2d);
-    if (e == cudaSuccess)
-      e = cudaMemcpy2DAsync(dB, (size_t)ldb_d * 4, B, (size_t)ldb * 4, (size_t)b_cols * 4, (size_t)b_rows,
-                            cudaMemcpyHostToDevice, d->h2d);
     if (e != cudaSuccess) fail(e);
   }
+  // B's K-chunk q: stored rows q*kc.. for 'N', stored columns q*kc.. for 'T'
+  auto copy_b_chunk = [&](int q) {
+    const int64_t k0 = q * kc, kq = std::min<int64_t>(kc, K - k0);
+    if (!tb)
+      return cudaMemcpy2DAsync(dB + k0 * ldb_d, (size_t)ldb_d * 4, B + k0 * ldb, (size_t)ldb * 4, (size_t)N * 4,
+                               (size_t)kq, cudaMemcpyHostToDevice, d->h2d);
+    return cudaMemcpy2DAsync(dB + k0, (size_t)ldb_d * 4, B + k0, (size_t)ldb * 4, (size_t)kq * 4, (size_t)N,
+                             cudaMemcpyHostToDevice, d->h2d);
+  };
   for (int i = 0; i < nsets && status == SGEMM_OK; ++i) {
     if (reads_ab) {
       e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dA[i]), (size_t)(a_rows * lda_d * 4), d->pool, d->h2d);
@@ -144,44 +162,88 @@ extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_
     if (e != cudaSuccess) fail(e);
   }
 
-  for (int64_t r0 = 0, blk = 0; r0 < M && status == SGEMM_OK; r0 += mb, ++blk) {
+  const int64_t nblk = (M + mb - 1) / mb;
+  // the first blocks' GEMMs run chunk by chunk while B arrives
+  const int64_t nchunked = (reads_ab && nq > 1) ? std::min<int64_t>(kChunkedBlocks, nblk) : 0;
+
+  // h2d: op(A) rows of block blk (stored rows for 'N', stored columns for 'T') and its C, into set
+  // blk % nsets once that set's previous GEMM has read it and its C has left
+  auto copy_in = [&](int64_t blk) -> cudaError_t {
     const int i = (int)(blk % nsets);
-    const int64_t rows = std::min<int64_t>(mb, M - r0);
-    // h2d: refill set i once its previous GEMM has read it and its C has left
+    const int64_t r0 = blk * mb, rows = std::min<int64_t>(mb, M - r0);
+    cudaError_t err = cudaSuccess;
     if (blk >= nsets) {
-      e = cudaStreamWaitEvent(d->h2d, d->ev_gemm[i], 0);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(d->h2d, d->ev_out[i], 0);
-      if (e != cudaSuccess) { fail(e); break; }
+      err = cudaStreamWaitEvent(d->h2d, d->ev_gemm[i], 0);
+      if (err == cudaSuccess) err = cudaStreamWaitEvent(d->h2d, d->ev_out[i], 0);
     }
-    if (reads_ab) {
-      // op(A) rows r0 .. r0+rows: stored rows for 'N', stored columns for 'T'
-      if (!ta)
-        e = cudaMemcpy2DAsync(dA[i], (size_t)lda_d * 4, A + r0 * lda, (size_t)lda * 4, (size_t)K * 4, (size_t)rows,
+    if (err == cudaSuccess && reads_ab)
+      err = !ta ? cudaMemcpy2DAsync(dA[i], (size_t)lda_d * 4, A + r0 * lda, (size_t)lda * 4, (size_t)K * 4,
+                                    (size_t)rows, cudaMemcpyHostToDevice, d->h2d)
+                : cudaMemcpy2DAsync(dA[i], (size_t)lda_d * 4, A + r0, (size_t)lda * 4, (size_t)rows * 4, (size_t)K,
+                                    cudaMemcpyHostToDevice, d->h2d);
+    if (err == cudaSuccess && reads_c)
+      err = cudaMemcpy2DAsync(dC[i], (size_t)ldc_d * 4, C + r0 * ldc, (size_t)ldc * 4, (size_t)N * 4, (size_t)rows,
                               cudaMemcpyHostToDevice, d->h2d);
-      else
-        e = cudaMemcpy2DAsync(dA[i], (size_t)lda_d * 4, A + r0, (size_t)lda * 4, (size_t)rows * 4, (size_t)K,
-                              cudaMemcpyHostToDevice, d->h2d);
-      if (e != cudaSuccess) { fail(e); break; }
+    if (err == cudaSuccess) err = cudaEventRecord(d->ev_in[i], d->h2d);
+    return err;
+  };
+  // comp: the GEMM of block blk over K-chunk q (q < 0: all of K):
+  // C = alpha*op(A)[:, chunk]*op(B)[chunk, :] + (first chunk ? beta : 1)*C
+  auto gemm = [&](int64_t blk, int q) -> int {
+    const int i = (int)(blk % nsets);
+    const int64_t rows = std::min<int64_t>(mb, M - blk * mb);
+    const int64_t k0 = q < 0 ? 0 : q * kc, kq = q < 0 ? K : std::min<int64_t>(kc, K - k0);
+    const float* a_q = dA[i] ? (ta ? dA[i] + k0 * lda_d : dA[i] + k0) : nullptr;
+    const float* b_q = dB ? (tb ? dB + k0 : dB + k0 * ldb_d) : nullptr;
+    return sgemm(transA, transB, rows, N, kq, alpha, a_q, lda_d, b_q, ldb_d, q > 0 ? 1.0f : beta, dC[i], ldc_d,
+                 reinterpret_cast<struct CUstream_st*>(d->comp));
+  };
+  // comp -> d2h: block blk's C back to the host once its GEMM is done
+  auto copy_out = [&](int64_t blk) -> cudaError_t {
+    const int i = (int)(blk % nsets);
+    const int64_t r0 = blk * mb, rows = std::min<int64_t>(mb, M - r0);
+    cudaError_t err = cudaEventRecord(d->ev_gemm[i], d->comp);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(d->d2h, d->ev_gemm[i], 0);
+    if (err == cudaSuccess)
+      err = cudaMemcpy2DAsync(C + r0 * ldc, (size_t)ldc * 4, dC[i], (size_t)ldc_d * 4, (size_t)N * 4, (size_t)rows,
+                              cudaMemcpyDeviceToHost, d->d2h);
+    if (err == cudaSuccess) err = cudaEventRecord(d->ev_out[i], d->d2h);
+    return err;
+  };
+
+  if (status == SGEMM_OK && nchunked > 0) {
+    // h2d order: block 0, B chunk 0, the other chunked blocks, the rest of B
+    e = copy_in(0);
+    if (e == cudaSuccess) e = copy_b_chunk(0);
+    if (e == cudaSuccess) e = cudaEventRecord(d->ev_b[0], d->h2d);
+    for (int64_t blk = 1; blk < nchunked && e == cudaSuccess; ++blk) e = copy_in(blk);
+    for (int q = 1; q < nq && e == cudaSuccess; ++q) {
+      e = copy_b_chunk(q);
+      if (e == cudaSuccess) e = cudaEventRecord(d->ev_b[q], d->h2d);
     }
-    if (reads_c) {
-      e = cudaMemcpy2DAsync(dC[i], (size_t)ldc_d * 4, C + r0 * ldc, (size_t)ldc * 4, (size_t)N * 4, (size_t)rows,
-                            cudaMemcpyHostToDevice, d->h2d);
-      if (e != cudaSuccess) { fail(e); break; }
+    // comp: chunk q of every chunked block as soon as chunk q of B is in
+    for (int q = 0; q < nq && e == cudaSuccess && status == SGEMM_OK; ++q) {
+      e = cudaStreamWaitEvent(d->comp, d->ev_b[q], 0);
+      for (int64_t blk = 0; blk < nchunked && e == cudaSuccess; ++blk) {
+        if (q == 0) e = cudaStreamWaitEvent(d->comp, d->ev_in[blk % nsets], 0);
+        if (e != cudaSuccess) break;
+        st = gemm(blk, q);
+        if (st != SGEMM_OK) { status = st; break; }
+        if (q == nq - 1) e = copy_out(blk);
+      }
     }
-    e = cudaEventRecord(d->ev_in[i], d->h2d);
-    // comp: the block's GEMM (the GEMMs run one after another, each on the whole GPU)
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->comp, d->ev_in[i], 0);
+    if (e != cudaSuccess) fail(e);
+  } else if (status == SGEMM_OK && reads_ab) {
+    e = copy_b_chunk(0);  // nq == 1: all of B, before any block
+    if (e != cudaSuccess) fail(e);
+  }
+  for (int64_t blk = nchunked; blk < nblk && status == SGEMM_OK; ++blk) {
+    e = copy_in(blk);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->comp, d->ev_in[blk % nsets], 0);
     if (e != cudaSuccess) { fail(e); break; }
-    st = sgemm(transA, transB, rows, N, K, alpha, dA[i], lda_d, dB, ldb_d, beta, dC[i], ldc_d,
-               reinterpret_cast<struct CUstream_st*>(d->comp));
+    st = gemm(blk, -1);
     if (st != SGEMM_OK) { status = st; break; }
-    e = cudaEventRecord(d->ev_gemm[i], d->comp);
-    // d2h: the block's C back to the host
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->d2h, d->ev_gemm[i], 0);
-    if (e == cudaSuccess)
-      e = cudaMemcpy2DAsync(C + r0 * ldc, (size_t)ldc * 4, dC[i], (size_t)ldc_d * 4, (size_t)N * 4, (size_t)rows,
-                            cudaMemcpyDeviceToHost, d->d2h);
-    if (e == cudaSuccess) e = cudaEventRecord(d->ev_out[i], d->d2h);
+    e = copy_out(blk);
     if (e != cudaSuccess) { fail(e); break; }
   }
 
