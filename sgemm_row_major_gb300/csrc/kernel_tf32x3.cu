@@ -21,22 +21,24 @@
 // folder warps add it into FP32 registers with round-to-nearest adds; the
 // error then no longer grows with K.
 //
-// Shared-memory bandwidth is the limit of this design (TMA writes, split
-// reads and writes and the tensor core's operand reads all use the same
-// shared-memory data path), so the A operand's hi/lo parts go to tensor
-// memory instead (tcgen05.mma reads A from TMEM, B from shared memory).
+// TMA writes, split reads and writes and the tensor core's operand reads all
+// use the shared-memory data path, so to keep that traffic down the A
+// operand's hi/lo parts go to tensor memory (tcgen05.mma reads A from TMEM,
+// B from shared memory).  What bounds the kernel is the latency of the feed
+// chain (TMA, split, MMA issue, fold), not a bandwidth.
 //
 // Schedule (persistent CTAs, stream-K balancing without waits between CTAs):
 // the grid has G CTAs (at most one per SM when the work allows).  CTA c first
 // takes the whole 128x128 output tiles c, c+G, c+2G, ... below sk_tile0
 // (data-parallel rounds), then an even share [B(c), B(c+1)) of the K
 // iterations of the remaining tiles, B(c) = floor(c*I/G), I = (tiles -
-// sk_tile0) * (K tiles per output tile).  A CTA writes a tile it covers whole straight to C; a tile
-// whose K range is shared by several CTAs is written as partial sums to the
-// CTA's slots (2c: its first stream-K tile, 2c+1: its last), and
-// streamk_fixup_kernel, launched after it on the same stream, adds the slots
-// of each shared tile in CTA order and applies alpha/beta.  The output tiles
-// of all products of a strided batch form one sequence.
+// sk_tile0) * (K tiles per output tile).  A CTA writes a tile it covers
+// whole straight to C; a tile whose K range is shared by several CTAs is
+// written as partial sums to the CTA's slots (2c: its first stream-K tile,
+// 2c+1: its last), and streamk_fixup_kernel (launched after it on the same
+// stream as a programmatic dependent, so its launch overlaps this kernel)
+// adds the slots of each shared tile in CTA order and applies alpha/beta.
+// The output tiles of all products of a strided batch form one sequence.
 //
 // CTA roles (19 warps):
 //   warp 0     TMA producer: FP32 tiles of op(A) and op(B) (as stored) into a
@@ -51,7 +53,11 @@
 //   warps 2-9  splitters: raw stage t -> A hi/lo in TMEM (row m in lane m, k
 //              in columns) and B hi/lo tiles in the K-major, 128-byte swizzled
 //              shared-memory layout the tensor core reads (transposed on the
-//              way when B is N-contiguous in memory), 2 split stages.
+//              way when B is N-contiguous in memory), 2 split stages.  Warps
+//              2-5 split k 0-15 of every tile, warps 6-9 k 16-31; each half of
+//              a split stage has its own full/empty barriers, so the issuer
+//              starts a half's 6 MMAs as soon as it is split and releases it
+//              right after them.
 //   warps 10-17 folders: add accumulator t into FP32 registers (each thread:
 //              64 columns of one row) as soon as its MMAs complete, then the
 //              alpha/beta epilogue.
