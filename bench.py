@@ -571,6 +571,34 @@ def run_reference_batched(args, c):
     }), flush=True)
 
 
+def small_roofline(c, flops_step, kernel_ms, peaks, dev):
+    """Roofline of the small-product kernel: each operand is read once and C written once (read too
+    when beta != 0), so the launch is bound by HBM or by the FP32 FMA pipes, whichever takes longer."""
+    import torch
+    n_a = 1 if "A" in c.shared else c.batch
+    n_b = 1 if "B" in c.shared else c.batch
+    nbytes = 4 * (n_a * c.M * c.K + n_b * c.K * c.N + c.batch * c.M * c.N * (2 if c.beta != 0 else 1))
+    hbm = peaks.get("hbm_gbs")
+    hbm_basis = "measured" if hbm else "fallback"
+    hbm = hbm or 6800.0
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    max_mhz = peaks.get("sm_max_mhz") or 2070.0
+    ffma_peak = sms * FMA_PER_SM_PER_CLK * 2 * max_mhz * 1e6 / 1e12
+    t = kernel_ms * 1e-3
+    gbs, tflops = nbytes / t / 1e9, flops_step / t / 1e12
+    hbm_bound = nbytes / (hbm * 1e9) >= flops_step / (ffma_peak * 1e12)
+    out = {"kernel": "small_gemm_kernel (one CTA per product, SIMT FFMA2)", "kernel_ms": kernel_ms,
+           "traffic": None, "algorithmic_bytes": nbytes,
+           "alu": {"achieved": tflops, "peak": ffma_peak, "unit": "TFLOP/s", "frac": tflops / ffma_peak},
+           "hbm": {"achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "basis": hbm_basis}}
+    if hbm_bound:
+        out.update({"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm})
+    else:
+        out.update({"bound": "alu", "achieved": tflops, "peak": ffma_peak, "unit": "TFLOP/s",
+                    "frac": tflops / ffma_peak})
+    return out
+
+
 def run_ours_batched(args, c):
     """One step = one sgemm_strided_batched() call over the whole batch."""
     import torch
@@ -631,6 +659,7 @@ def run_ours_batched(args, c):
                    "plan": {k: plan[k] for k in ("variant_name", "split_k", "grid_x", "grid_y", "dp_tiles",
                                                  "sk_tiles")}},
         "roofline": (tensor_roofline(achieved, peaks, None, kernel_ms) if plan["variant_name"] == "TC_TF32X3"
+                     else small_roofline(c, flops_step, kernel_ms, peaks, dev) if plan["variant_name"] == "SMALL"
                      else {"bound": "alu", "achieved": achieved, "peak": None, "unit": "TFLOP/s", "frac": None,
                            "traffic": None, "kernel": plan["variant_name"], "kernel_ms": kernel_ms}),
         "e2e": {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,

@@ -83,7 +83,8 @@ enum sgemm_variant {
     SGEMM_VARIANT_GENERIC = 3,    /* any alignment: 64x64 tiles, predicated loads */
     SGEMM_VARIANT_TMA_128x128 = 4,/* TMA-fed SIMT FFMA, 128x128x32 tiles, 4-stage mbarrier ring */
     SGEMM_VARIANT_TMA_64x256 = 5, /* same kernel, 64x256 tiles for short M */
-    SGEMM_VARIANT_TC_TF32X3 = 6   /* tcgen05 tensor cores, 3xTF32 split, 128x128x32 tiles */
+    SGEMM_VARIANT_TC_TF32X3 = 6,  /* tcgen05 tensor cores, 3xTF32 split, 128x128x32 tiles */
+    SGEMM_VARIANT_SMALL = 7       /* M, N <= 64 in a large batch: one CTA per product, FP32 FFMA */
 };
 
 /*

@@ -27,7 +27,7 @@ _LIB_PATH = os.path.join(_PKG, "_lib", "libsgemm.so")
 
 STATUS = {"OK": 0, "ERR_CUDA": 1, "ERR_TIMEOUT": 2, "ERR_NOMEM": 3, "ERR_UNSUPPORTED": 4, "ERR_SCRATCH_LIMIT": 5}
 NOALLOC_SCRATCH_BYTES = 32 << 20  # SGEMM_NOALLOC_SCRATCH_BYTES in include/sgemm.h
-VARIANTS = {"AUTO": 0, "NONE": 1, "SCALE": 2, "GENERIC": 3, "TMA_128x128": 4, "TMA_64x256": 5, "TC_TF32X3": 6}
+VARIANTS = {"AUTO": 0, "NONE": 1, "SCALE": 2, "GENERIC": 3, "TMA_128x128": 4, "TMA_64x256": 5, "TC_TF32X3": 6, "SMALL": 7}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 
 
@@ -170,7 +170,7 @@ def sgemm_noalloc(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 
     """sgemm() for callers that cannot allocate device memory during the call.
 
     Same arguments and results as sgemm(); split-K partial sums go to a fixed
-    16 MiB array inside the library instead of a memory pool.  Problems that
+    32 MiB array inside the library instead of a memory pool.  Problems that
     need more scratch return ERR_SCRATCH_LIMIT.  All calls on a device share
     that array, so calls that can overlap on the GPU must be ordered.
     """

@@ -12,6 +12,7 @@
 #include <cstdlib>
 #include <mutex>
 
+#include "kernel_small.h"
 #include "kernel_tma.cuh"
 #include "sgemm.h"
 #include "sgemm_internal.h"
@@ -164,6 +165,12 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 //     scheduled by the hardware).
 constexpr int64_t kMinStreamKIters = 32;
 
+// Small-product kernel (kernel_small.cu): output extents it covers, and the
+// longest K the planner gives it by default (beyond, one CTA per SM cannot
+// hide its load latency and the tensor-core kernel is faster).
+constexpr int64_t kSmallMaxMN = 64;
+constexpr int64_t kSmallMaxK = 1024;
+
 int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
   const int64_t sms = std::max(1, sm_count);
   int64_t grid, dp_tiles, sk_tiles;
@@ -237,14 +244,36 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   const bool tma_ok = aligned16(pr.A) && aligned16(pr.B) && pr.lda % 4 == 0 && pr.ldb % 4 == 0 &&
                       batch_ok(pr.stride_a, pr.ta ? pr.K : pr.M, pr.lda) &&
                       batch_ok(pr.stride_b, pr.tb ? pr.N : pr.K, pr.ldb);
+  // The small-product kernel reads whole float4s along the contiguous axis
+  // of each operand, so that extent must be a multiple of 4 as well.
+  const bool small_ok = pr.M <= kSmallMaxMN && pr.N <= kSmallMaxMN && aligned16(pr.A) && aligned16(pr.B) &&
+                        pr.lda % 4 == 0 && pr.ldb % 4 == 0 &&
+                        (pr.batch == 1 || (pr.stride_a % 4 == 0 && pr.stride_b % 4 == 0)) &&
+                        (pr.ta ? pr.M : pr.K) % 4 == 0 && (pr.tb ? pr.K : pr.N) % 4 == 0;
   // Default: the 3xTF32 tensor-core kernel whenever TMA can load the operands
-  // (it beats the FP32 FFMA kernels on every measured shape); the generic
-  // SIMT kernel otherwise.  The FFMA kernels stay selectable by override.
+  // (it beats the FP32 FFMA kernels on every measured shape), except for a
+  // batch of small products large enough to give every SM its own, which the
+  // one-CTA-per-product kernel serves without the 128x128 tile's padding; the
+  // generic SIMT kernel otherwise.  The other kernels stay selectable by
+  // override.
   int variant = tma_ok ? SGEMM_VARIANT_TC_TF32X3 : SGEMM_VARIANT_GENERIC;
+  if (small_ok && pr.batch >= sm_count && pr.K <= kSmallMaxK) variant = SGEMM_VARIANT_SMALL;
   const int ov = g_override_variant.load();
   if (ov == SGEMM_VARIANT_GENERIC || ov == SGEMM_VARIANT_TMA_128x128 || ov == SGEMM_VARIANT_TMA_64x256 ||
       ov == SGEMM_VARIANT_TC_TF32X3)
     variant = (ov == SGEMM_VARIANT_GENERIC || tma_ok) ? ov : SGEMM_VARIANT_GENERIC;
+  if (ov == SGEMM_VARIANT_SMALL) variant = small_ok ? ov : SGEMM_VARIANT_GENERIC;
+  if (variant == SGEMM_VARIANT_SMALL) {
+    plan->variant = variant;
+    plan->tile_m = plan->tile_n = plan->tile_k = (int)kSmallMaxMN;
+    plan->stages = 1;
+    plan->threads = 128;
+    plan->smem_bytes = 2 * kSmallMaxMN * kSmallMaxMN * 4;
+    plan->kernel_launches = 1;
+    plan->grid_x = pr.batch;
+    plan->grid_y = 1;
+    return SGEMM_OK;
+  }
 
   int bm, bn, bk, threads, stages;
   int64_t smem = 0;
@@ -327,7 +356,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   set_schedule(plan, &p);
 
   CUtensorMap mapA, mapB;
-  if (plan.variant != SGEMM_VARIANT_GENERIC) {
+  if (plan.variant != SGEMM_VARIANT_GENERIC && plan.variant != SGEMM_VARIANT_SMALL) {
     cudaError_t e = encode_operand_maps(pr.ta, pr.tb, pr.M, pr.N, pr.K, pr.A, pr.lda, pr.stride_a, pr.B, pr.ldb,
                                         pr.stride_b, p.batch, plan.tile_m, plan.tile_n, plan.tile_k, &mapA, &mapB,
                                         &p.za, &p.zb);
@@ -347,6 +376,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   cudaError_t e;
   if (plan.variant == SGEMM_VARIANT_GENERIC) {
     e = launch_generic_gemm(pr.ta, pr.tb, p, split, stream);
+  } else if (plan.variant == SGEMM_VARIANT_SMALL) {
+    e = launch_small_gemm(pr.ta, pr.tb, p, stream);
   } else if (plan.variant == SGEMM_VARIANT_TC_TF32X3) {
     e = launch_tf32x3(pr.ta, pr.tb, mapA, mapB, p, stream);
     if (e == cudaSuccess && plan.kernel_launches > 1) e = launch_streamk_fixup(p, (int)plan.sk_tiles, stream);
@@ -445,7 +476,7 @@ int sgemm_plan_strided_batched(char transA, char transB, int64_t M, int64_t N, i
 
 int sgemm_set_variant_override(int variant, int split_k) {
   if (variant != SGEMM_VARIANT_AUTO && variant != SGEMM_VARIANT_GENERIC && variant != SGEMM_VARIANT_TMA_128x128 &&
-      variant != SGEMM_VARIANT_TMA_64x256 && variant != SGEMM_VARIANT_TC_TF32X3)
+      variant != SGEMM_VARIANT_TMA_64x256 && variant != SGEMM_VARIANT_TC_TF32X3 && variant != SGEMM_VARIANT_SMALL)
     return -1;
   g_override_variant.store(variant);
   g_override_split.store(split_k < 0 ? 0 : split_k);

@@ -24,6 +24,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "kernel_small.h"
 #include "kernel_tma.cuh"
 #include "sgemm.h"
 #include "sgemm_internal.h"
@@ -121,6 +122,8 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
 
   if (plan.variant == SGEMM_VARIANT_GENERIC) {
     e = launch_generic_gemm(ta, tb, p, split, cs);
+  } else if (plan.variant == SGEMM_VARIANT_SMALL) {
+    e = launch_small_gemm(ta, tb, p, cs);
   } else {
     CUtensorMap mapA, mapB;
     e = encode_operand_maps(ta, tb, M, N, K, A, lda, 0, B, ldb, 0, 1, plan.tile_m, plan.tile_n, plan.tile_k, &mapA,

@@ -212,6 +212,48 @@ def test_batched_planner(lib):
     assert bplan("N", "N", 64, 64, 64, 3, 0, 0, 64 * 64, alpha=0.0)["variant_name"] == "SCALE"
 
 
+def test_small_product_planner(lib):
+    # 8192 products of 64x64x64: one 128-thread CTA per product, no tensor maps, no workspace
+    p = bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64)
+    assert p["variant_name"] == "SMALL" and (p["grid_x"], p["grid_y"], p["threads"]) == (8192, 1, 128)
+    assert (p["kernel_launches"], p["split_k"], p["workspace_bytes"]) == (1, 1, 0)
+    assert p["smem_bytes"] == 2 * 64 * 64 * 4
+    # every op combination, ragged M and N below the tile, shared operands
+    for ta in "NT":
+        for tb in "NT":
+            M, N, K = 36, 20, 100
+            q = bplan(ta, tb, M, N, K, 152, M * K, K * N, M * N)
+            assert q["variant_name"] == "SMALL", (ta, tb)
+    assert bplan("N", "N", 64, 64, 64, 500, 64 * 64, 0, 64 * 64)["variant_name"] == "SMALL"
+    # too few products to fill the SMs, too long K, outputs above 64: the tensor-core kernel
+    assert bplan("N", "N", 64, 64, 64, 151, 64 * 64, 64 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
+    assert bplan("N", "N", 64, 64, 1028, 8192, 64 * 1028, 1028 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
+    assert bplan("N", "N", 65, 64, 64, 8192, 65 * 64, 64 * 64, 65 * 64)["variant_name"] == "TC_TF32X3"
+    assert bplan("N", "N", 64, 68, 64, 8192, 64 * 64, 64 * 68, 64 * 68)["variant_name"] == "TC_TF32X3"
+    # the float4 rules: the contiguous extent of each operand a multiple of 4
+    assert bplan("N", "N", 64, 64, 62, 8192, 64 * 64, 64 * 64, 64 * 64, lda=64)["variant_name"] != "SMALL"
+    assert bplan("N", "N", 64, 62, 64, 8192, 64 * 64, 64 * 64, 64 * 64, ldb=64)["variant_name"] != "SMALL"
+    assert bplan("T", "N", 62, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64, lda=64)["variant_name"] != "SMALL"
+    assert bplan("N", "T", 64, 64, 62, 8192, 64 * 64, 64 * 64, 64 * 64, lda=64, ldb=64)["variant_name"] != "SMALL"
+    assert bplan("T", "T", 64, 62, 64, 8192, 64 * 64, 64 * 64, 64 * 64, ldb=64)["variant_name"] == "SMALL"
+    # alignment: A or B base, leading dimensions, strides
+    assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64, A=FAKE_ODD)["variant_name"] == "GENERIC"
+    assert bplan("N", "N", 64, 64, 64, 8192, 64 * 66, 64 * 64, 64 * 64, lda=66)["variant_name"] == "GENERIC"
+    assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64 + 2, 64 * 64, 64 * 64)["variant_name"] == "GENERIC"
+    # C is written with scalar stores when it is not 16-byte aligned: no rule on C
+    assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64 + 1, C=FAKE_ODD)["variant_name"] == "SMALL"
+    # forced: SMALL where its rules hold (any batch), GENERIC where they do not; forced TC wins over the rule
+    try:
+        sg.sgemm_set_variant_override("SMALL", 0)
+        assert bplan("N", "N", 64, 64, 2048, 2, 64 * 2048, 2048 * 64, 64 * 64)["variant_name"] == "SMALL"
+        assert plan("N", "N", 64, 64, 64)["variant_name"] == "SMALL"
+        assert plan("N", "N", 65, 64, 64)["variant_name"] == "GENERIC"
+        sg.sgemm_set_variant_override("TC_TF32X3", 0)
+        assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
+
+
 def test_batched_argument_checks(lib):
     def st(sA, sB, sC, batch, M=4, N=4, ldc=4):
         return lib.sgemm_plan_strided_batched(b"N", b"N", M, N, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, ldc, sA, sB,
