@@ -74,6 +74,7 @@ int device_state(int* device_out, DeviceState** st_out) {
     if (err == cudaSuccess) err = prepare_tma_op_tn();
     if (err == cudaSuccess) err = prepare_tma_op_tt();
     if (err == cudaSuccess) err = prepare_tf32x3();
+    if (err == cudaSuccess) err = prepare_small_gemm();
     if (err == cudaSuccess) {
       cudaMemPoolProps props = {};
       props.allocType = cudaMemAllocationTypePinned;
@@ -170,6 +171,7 @@ constexpr int64_t kMinStreamKIters = 32;
 // hide its load latency and the tensor-core kernel is faster).
 constexpr int64_t kSmallMaxMN = 64;
 constexpr int64_t kSmallMaxK = 1024;
+constexpr int64_t kSmallCtasPerSm = 3;  // persistent grid: 3 x 64 KB of stages per SM
 
 int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
   const int64_t sms = std::max(1, sm_count);
@@ -246,10 +248,14 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
                       batch_ok(pr.stride_b, pr.tb ? pr.N : pr.K, pr.ldb);
   // The small-product kernel reads whole float4s along the contiguous axis
   // of each operand, so that extent must be a multiple of 4 as well.
+  // Its persistent grid deals products round-robin; a CTA's (product, K
+  // chunk) items are counted in an int.
+  const int64_t small_grid = std::min<int64_t>(pr.batch, kSmallCtasPerSm * std::max(1, sm_count));
   const bool small_ok = pr.M <= kSmallMaxMN && pr.N <= kSmallMaxMN && aligned16(pr.A) && aligned16(pr.B) &&
                         pr.lda % 4 == 0 && pr.ldb % 4 == 0 &&
                         (pr.batch == 1 || (pr.stride_a % 4 == 0 && pr.stride_b % 4 == 0)) &&
-                        (pr.ta ? pr.M : pr.K) % 4 == 0 && (pr.tb ? pr.K : pr.N) % 4 == 0;
+                        (pr.ta ? pr.M : pr.K) % 4 == 0 && (pr.tb ? pr.K : pr.N) % 4 == 0 &&
+                        ceil_div(pr.batch, small_grid) * ceil_div(pr.K, kSmallMaxMN) < INT_MAX;
   // Default: the 3xTF32 tensor-core kernel whenever TMA can load the operands
   // (it beats the FP32 FFMA kernels on every measured shape), except for a
   // batch of small products large enough to give every SM its own, which the
@@ -266,11 +272,11 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   if (variant == SGEMM_VARIANT_SMALL) {
     plan->variant = variant;
     plan->tile_m = plan->tile_n = plan->tile_k = (int)kSmallMaxMN;
-    plan->stages = 1;
+    plan->stages = 2;
     plan->threads = 128;
-    plan->smem_bytes = 2 * kSmallMaxMN * kSmallMaxMN * 4;
+    plan->smem_bytes = 2 * 2 * kSmallMaxMN * kSmallMaxMN * 4;
     plan->kernel_launches = 1;
-    plan->grid_x = pr.batch;
+    plan->grid_x = small_grid;
     plan->grid_y = 1;
     return SGEMM_OK;
   }
@@ -377,7 +383,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   if (plan.variant == SGEMM_VARIANT_GENERIC) {
     e = launch_generic_gemm(pr.ta, pr.tb, p, split, stream);
   } else if (plan.variant == SGEMM_VARIANT_SMALL) {
-    e = launch_small_gemm(pr.ta, pr.tb, p, stream);
+    e = launch_small_gemm(pr.ta, pr.tb, p, (int)plan.grid_x, stream);
   } else if (plan.variant == SGEMM_VARIANT_TC_TF32X3) {
     e = launch_tf32x3(pr.ta, pr.tb, mapA, mapB, p, stream);
     if (e == cudaSuccess && plan.kernel_launches > 1) e = launch_streamk_fixup(p, (int)plan.sk_tiles, stream);

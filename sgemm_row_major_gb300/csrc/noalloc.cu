@@ -59,6 +59,7 @@ cudaError_t setup(int dev, NoallocDevice** out) {
     if (e == cudaSuccess) e = prepare_tma_op_tn();
     if (e == cudaSuccess) e = prepare_tma_op_tt();
     if (e == cudaSuccess) e = prepare_tf32x3();
+    if (e == cudaSuccess) e = prepare_small_gemm();
     d.err = e;
   });
   *out = &d;
@@ -123,7 +124,7 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
   if (plan.variant == SGEMM_VARIANT_GENERIC) {
     e = launch_generic_gemm(ta, tb, p, split, cs);
   } else if (plan.variant == SGEMM_VARIANT_SMALL) {
-    e = launch_small_gemm(ta, tb, p, cs);
+    e = launch_small_gemm(ta, tb, p, (int)plan.grid_x, cs);
   } else {
     CUtensorMap mapA, mapB;
     e = encode_operand_maps(ta, tb, M, N, K, A, lda, 0, B, ldb, 0, 1, plan.tile_m, plan.tile_n, plan.tile_k, &mapA,

@@ -215,9 +215,12 @@ def test_batched_planner(lib):
 def test_small_product_planner(lib):
     # 8192 products of 64x64x64: one 128-thread CTA per product, no tensor maps, no workspace
     p = bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64)
-    assert p["variant_name"] == "SMALL" and (p["grid_x"], p["grid_y"], p["threads"]) == (8192, 1, 128)
+    assert p["variant_name"] == "SMALL" and (p["grid_x"], p["grid_y"], p["threads"]) == (3 * 152, 1, 128)
     assert (p["kernel_launches"], p["split_k"], p["workspace_bytes"]) == (1, 1, 0)
-    assert p["smem_bytes"] == 2 * 64 * 64 * 4
+    assert p["smem_bytes"] == 2 * 2 * 64 * 64 * 4 and p["stages"] == 2
+    # the persistent grid never exceeds the batch
+    assert bplan("N", "N", 64, 64, 64, 200, 64 * 64, 64 * 64, 64 * 64)["grid_x"] == 200
+    assert bplan("N", "N", 64, 64, 64, 200, 64 * 64, 64 * 64, 64 * 64, sm=1)["grid_x"] == 3
     # every op combination, ragged M and N below the tile, shared operands
     for ta in "NT":
         for tb in "NT":
@@ -248,6 +251,10 @@ def test_small_product_planner(lib):
         assert bplan("N", "N", 64, 64, 2048, 2, 64 * 2048, 2048 * 64, 64 * 64)["variant_name"] == "SMALL"
         assert plan("N", "N", 64, 64, 64)["variant_name"] == "SMALL"
         assert plan("N", "N", 65, 64, 64)["variant_name"] == "GENERIC"
+        # a CTA's (product, K chunk) items must fit an int: 2300 products x 2^24 chunks do not
+        huge_k = 64 << 24
+        assert bplan("N", "N", 64, 64, huge_k, 1 << 20, 0, 0, 64 * 64, lda=huge_k)["variant_name"] == "GENERIC"
+        assert bplan("N", "N", 64, 64, huge_k, 4, 0, 0, 64 * 64, lda=huge_k)["variant_name"] == "SMALL"
         sg.sgemm_set_variant_override("TC_TF32X3", 0)
         assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
     finally:

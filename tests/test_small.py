@@ -40,6 +40,19 @@ def test_small_parity(ops, shared):
 
 
 @pytest.mark.parametrize("ops", OPS)
+def test_small_persistent_rounds(ops):
+    """1111 products on the persistent grid (2-3 products per CTA, 4 K chunks each, the last ragged)."""
+    ta, tb = ops
+    batch, M, N, K = 1111, 52, 44, 200
+    d = si.make_batched(batch, M, N, K, ta, tb, seed=58, pad=4, gap=4, align=4)
+    p = plan_of(ta, tb, M, N, K, d, batch)
+    assert p["variant_name"] == "SMALL" and p["grid_x"] < batch
+    got = gpu_batched(ta, tb, M, N, K, 0.5, 1.5, d, batch)
+    ref, S = oracle_batched(ta, tb, M, N, K, 0.5, 1.5, d, batch)
+    check_batched(got, ref, S, d, batch, M, N, K, f"persistent {ops}")
+
+
+@pytest.mark.parametrize("ops", OPS)
 def test_small_dyadic_exact(ops):
     """Full 64x64 tiles at the longest default K (16 chunks): bit-exact on dyadic inputs."""
     ta, tb = ops
