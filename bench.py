@@ -40,7 +40,8 @@ METRIC = "SGEMM TFLOPS (2MNK/t) at 4096^3 NN on 1 GB300; % of FP32 FFMA peak"
 UNIT = "TFLOPS"
 FMA_PER_SM_PER_CLK = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
 PROFILES = {"TC_TF32X3": os.path.join(ROOT, "profiles", "tf32x3_gemm_square4096.md"),
-            "TMA_128x128": os.path.join(ROOT, "profiles", "tma_gemm_square4096.md")}
+            "TMA_128x128": os.path.join(ROOT, "profiles", "tma_gemm_square4096.md"),
+            "SMALL": os.path.join(ROOT, "profiles", "small_gemm_batched8192x64x64x64.md")}
 # dense tensor-core peaks (PFLOP/s, nominal) used to scale the measured bf16 peak to tf32
 NOMINAL_BF16_PF, NOMINAL_TF32_PF = 2.25, 1.1
 TF32_PRODUCTS = 3  # tensor-core products per useful FMA in the 3xTF32 split
@@ -571,7 +572,7 @@ def run_reference_batched(args, c):
     }), flush=True)
 
 
-def small_roofline(c, flops_step, kernel_ms, peaks, dev):
+def small_roofline(c, flops_step, kernel_ms, peaks, dev, traffic):
     """Roofline of the small-product kernel: each operand is read once and C written once (read too
     when beta != 0), so the launch is bound by HBM or by the FP32 FMA pipes, whichever takes longer."""
     import torch
@@ -587,8 +588,8 @@ def small_roofline(c, flops_step, kernel_ms, peaks, dev):
     t = kernel_ms * 1e-3
     gbs, tflops = nbytes / t / 1e9, flops_step / t / 1e12
     hbm_bound = nbytes / (hbm * 1e9) >= flops_step / (ffma_peak * 1e12)
-    out = {"kernel": "small_gemm_kernel (one CTA per product, SIMT FFMA2)", "kernel_ms": kernel_ms,
-           "traffic": None, "algorithmic_bytes": nbytes,
+    out = {"kernel": "small_gemm_kernel (persistent, a 64x64 tile per product, SIMT FFMA2)", "kernel_ms": kernel_ms,
+           "traffic": traffic, "algorithmic_bytes": nbytes,
            "alu": {"achieved": tflops, "peak": ffma_peak, "unit": "TFLOP/s", "frac": tflops / ffma_peak},
            "hbm": {"achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "basis": hbm_basis}}
     if hbm_bound:
@@ -659,7 +660,9 @@ def run_ours_batched(args, c):
                    "plan": {k: plan[k] for k in ("variant_name", "split_k", "grid_x", "grid_y", "dp_tiles",
                                                  "sk_tiles")}},
         "roofline": (tensor_roofline(achieved, peaks, None, kernel_ms) if plan["variant_name"] == "TC_TF32X3"
-                     else small_roofline(c, flops_step, kernel_ms, peaks, dev) if plan["variant_name"] == "SMALL"
+                     else small_roofline(c, flops_step, kernel_ms, peaks, dev,
+                                         traffic_from_profile("SMALL", lib_build.small_kernel_digest()))
+                     if plan["variant_name"] == "SMALL"
                      else {"bound": "alu", "achieved": achieved, "peak": None, "unit": "TFLOP/s", "frac": None,
                            "traffic": None, "kernel": plan["variant_name"], "kernel_ms": kernel_ms}),
         "e2e": {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,

@@ -61,6 +61,9 @@ TMA_KERNEL_FILES = ["kernel_tma.cuh", "device_utils.cuh", "sgemm_internal.h", "k
 TC_KERNEL_FILES = ["kernel_tf32x3.cu", "device_utils.cuh", "sgemm_internal.h"]
 
 
+SMALL_KERNEL_FILES = ["kernel_small.cu", "kernel_small.h", "sgemm_internal.h"]
+
+
 def tma_kernel_digest() -> str:
     """Hash of the sources of the TMA-fed FFMA kernel only (identifies the profiled kernel build)."""
     return _digest(TMA_KERNEL_FILES)
@@ -69,6 +72,11 @@ def tma_kernel_digest() -> str:
 def tc_kernel_digest() -> str:
     """Hash of the sources of the 3xTF32 tensor-core kernel only."""
     return _digest(TC_KERNEL_FILES)
+
+
+def small_kernel_digest() -> str:
+    """Hash of the sources of the small-product kernel only."""
+    return _digest(SMALL_KERNEL_FILES)
 
 
 def _digest(files) -> str:

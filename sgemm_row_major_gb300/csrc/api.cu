@@ -167,11 +167,15 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 constexpr int64_t kMinStreamKIters = 32;
 
 // Small-product kernel (kernel_small.cu): output extents it covers, and the
-// longest K the planner gives it by default (beyond, one CTA per SM cannot
-// hide its load latency and the tensor-core kernel is faster).
+// products the planner gives it by default: at least two per SM and K <= 128
+// (measured on GB300, 64x64 products: at K = 64 it runs 40.9 TFLOPS against
+// 24.8 for the tensor-core kernel, at K = 128 44.6 against 38.3; from K = 256
+// on, and for batches of one product per SM, the tensor-core kernel is faster).
 constexpr int64_t kSmallMaxMN = 64;
-constexpr int64_t kSmallMaxK = 1024;
-constexpr int64_t kSmallCtasPerSm = 3;  // persistent grid: 3 x 64 KB of stages per SM
+constexpr int64_t kSmallMaxK = 128;
+constexpr int64_t kSmallMinProductsPerSm = 2;
+constexpr int64_t kSmallKChunk = 32;
+constexpr int64_t kSmallCtasPerSm = 6;  // persistent grid: 6 x 32 KB of stages per SM
 
 int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
   const int64_t sms = std::max(1, sm_count);
@@ -255,15 +259,15 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
                         pr.lda % 4 == 0 && pr.ldb % 4 == 0 &&
                         (pr.batch == 1 || (pr.stride_a % 4 == 0 && pr.stride_b % 4 == 0)) &&
                         (pr.ta ? pr.M : pr.K) % 4 == 0 && (pr.tb ? pr.K : pr.N) % 4 == 0 &&
-                        ceil_div(pr.batch, small_grid) * ceil_div(pr.K, kSmallMaxMN) < INT_MAX;
+                        ceil_div(pr.batch, small_grid) * ceil_div(pr.K, kSmallKChunk) < INT_MAX;
   // Default: the 3xTF32 tensor-core kernel whenever TMA can load the operands
   // (it beats the FP32 FFMA kernels on every measured shape), except for a
-  // batch of small products large enough to give every SM its own, which the
-  // one-CTA-per-product kernel serves without the 128x128 tile's padding; the
-  // generic SIMT kernel otherwise.  The other kernels stay selectable by
+  // large batch of small products with short K, which the small-product
+  // kernel serves without the 128x128 tile's padding; the generic SIMT kernel
+  // otherwise.  The other kernels stay selectable by
   // override.
   int variant = tma_ok ? SGEMM_VARIANT_TC_TF32X3 : SGEMM_VARIANT_GENERIC;
-  if (small_ok && pr.batch >= sm_count && pr.K <= kSmallMaxK) variant = SGEMM_VARIANT_SMALL;
+  if (small_ok && pr.batch >= kSmallMinProductsPerSm * sm_count && pr.K <= kSmallMaxK) variant = SGEMM_VARIANT_SMALL;
   const int ov = g_override_variant.load();
   if (ov == SGEMM_VARIANT_GENERIC || ov == SGEMM_VARIANT_TMA_128x128 || ov == SGEMM_VARIANT_TMA_64x256 ||
       ov == SGEMM_VARIANT_TC_TF32X3)
@@ -271,10 +275,11 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   if (ov == SGEMM_VARIANT_SMALL) variant = small_ok ? ov : SGEMM_VARIANT_GENERIC;
   if (variant == SGEMM_VARIANT_SMALL) {
     plan->variant = variant;
-    plan->tile_m = plan->tile_n = plan->tile_k = (int)kSmallMaxMN;
+    plan->tile_m = plan->tile_n = (int)kSmallMaxMN;
+    plan->tile_k = (int)kSmallKChunk;
     plan->stages = 2;
-    plan->threads = 128;
-    plan->smem_bytes = 2 * 2 * kSmallMaxMN * kSmallMaxMN * 4;
+    plan->threads = 64;
+    plan->smem_bytes = 2 * 2 * kSmallMaxMN * kSmallKChunk * 4;
     plan->kernel_launches = 1;
     plan->grid_x = small_grid;
     plan->grid_y = 1;

@@ -1,27 +1,27 @@
 // kernel_small.cu -- many small products (M <= 64, N <= 64; a strided batch of
-// them): one CTA computes a product's whole output tile, then moves on to the
-// next product, whose copies are already in flight.
+// them): one CTA computes a product's whole 64x64 output tile, then moves on
+// to the next product, whose copies are already in flight.
 //
 // For such products the tensor-core kernel's 128x128 tile is three quarters
 // padding, and its pipeline (TMA ring, split, MMA issue, fold) is set up for
-// long K loops.  Here the work of a CTA is a list of (product, 64-k chunk)
-// items; each item's op(A) and op(B) chunks (16 KB each) are copied into one
-// of two shared-memory stages with 16-byte cp.async copies, as they are
-// stored in global memory (no transposition), and the next item's copies are
-// issued before the current item is computed.  128 threads each accumulate a
-// 4x8 block of the 64x64 tile with packed FP32 FMAs (fma.rn.f32x2, IEEE
-// round-to-nearest); a chunk's partial sums are added into a second set of
-// registers after every chunk, so no accumulator sums more than 64 products.
-// The grid is persistent (three CTAs per SM, products dealt round-robin), so
+// long K loops.  Here the work of a CTA is a list of (product, 32-k chunk)
+// items; each item's op(A) and op(B) chunks (8 KB each) are copied into one
+// of two shared-memory stages with 16-byte cp.async copies, in the operands'
+// stored orientation, and the next item's copies are issued before the
+// current item is computed.  Two warps share the tile, 32 rows each; a
+// thread accumulates an 8x8 block with packed FP32 FMAs (fma.rn.f32x2, IEEE
+// round-to-nearest, k ascending), so each 128-bit shared load feeds 16 FMAs.
+// The grid is persistent (six CTAs per SM, products dealt round-robin), so
 // HBM traffic and FMA work overlap within a CTA and across the CTAs of an SM.
 //
-// Shared layout of a stage: the A chunk, then the B chunk, each 64 rows of 64
-// floats (16 groups of 16 bytes).  A stored K-contiguous (op 'N') is kept as
-// [m][k] and B stored K-contiguous (op 'T') as [n][k]; in both, group g of row
-// r sits at g XOR ((r / 4) % 8), which puts the rows a warp reads together in
-// distinct bank groups.  A stored M-contiguous ('T') and B stored
-// N-contiguous ('N') are kept as [k][m] and [k][n], unswizzled: a warp reads
-// contiguous groups of one row.
+// Shared layout of a stage: the A chunk, then the B chunk.  An operand stored
+// K-contiguous (A 'N' as [m][k], B 'T' as [n][k]) is kept as 64 rows of 32
+// floats with 16-byte group g of row r at g XOR (r % 8); one stored
+// M/N-contiguous (A 'T' as [k][m], B 'N' as [k][n]) as 32 rows of 64 floats.
+// The thread-to-row and thread-to-column maps depend on the orientation so
+// that every shared load of a warp touches distinct banks (rows 4 apart for a
+// K-contiguous A, 4 adjacent rows otherwise; columns 8 apart for a
+// K-contiguous B, 4 adjacent columns otherwise).
 //
 // Requirements (checked by the planner): A, B 16-byte aligned, lda, ldb and
 // the batch strides multiples of 4 floats, and the extent copied along a row
@@ -34,13 +34,15 @@
 namespace sgemm_impl {
 namespace {
 
-constexpr int SM_T = 64;                              // output tile and K chunk
-constexpr int SM_THREADS = 128;                       // 16 x 8 threads, 4 rows x 8 columns each
-constexpr int SM_CHUNK_FLOATS = SM_T * SM_T;          // one operand chunk
+constexpr int SM_T = 64;                              // output tile
+constexpr int SM_KC = 32;                             // K chunk
+constexpr int SM_THREADS = 64;                        // 2 warps, 8x8 results per thread
+constexpr int SM_CTAS = 6;                            // CTAs per SM
+constexpr int SM_CHUNK_FLOATS = SM_T * SM_KC;         // one operand chunk (8 KB)
 constexpr int SM_STAGE_FLOATS = 2 * SM_CHUNK_FLOATS;  // A chunk + B chunk
 constexpr int SM_SMEM_BYTES = 2 * SM_STAGE_FLOATS * 4;
-static_assert(SM_SMEM_BYTES == 65536, "two 32 KB stages");
-static_assert(3 * (SM_SMEM_BYTES + 1024) <= 228 * 1024, "three CTAs per SM");
+static_assert(SM_SMEM_BYTES == 32768, "two 16 KB stages");
+static_assert(SM_CTAS * (SM_SMEM_BYTES + 1024) <= 228 * 1024, "six CTAs per SM");
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -55,52 +57,83 @@ __device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wai
 
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-// Copy one operand chunk, 64 rows of 16 groups: row r is matrix row r0 + r and
-// group g its columns c0 + 4g .. +3; rows >= rows_valid and columns >=
-// cols_valid (a multiple of 4) are zero.  `swizzle` places group g of row r at
-// g ^ ((r / 4) % 8).
-__device__ __forceinline__ void copy_chunk(float* dst, const float* base, int64_t ld, int r0, int rows_valid,
-                                           int c0, int cols_valid, bool swizzle, int tid) {
+// One operand chunk stored K-contiguous: 64 rows (matrix rows 0..63, valid
+// below `rows`) of 8 groups (columns k0 + 4g, valid below K), swizzled.
+__device__ __forceinline__ void copy_k_rows(float* dst, const float* base, int64_t ld, int rows, int k0, int K,
+                                            int tid) {
   const uint32_t d0 = smem_addr(dst);
 #pragma unroll
   for (int q = 0; q < SM_CHUNK_FLOATS / 4 / SM_THREADS; ++q) {
-    const int e = tid + SM_THREADS * q;  // 0 .. 1023
-    const int r = e >> 4, g = e & 15;
-    const int row = r0 + r, col = c0 + 4 * g;
-    const bool ok = row < rows_valid && col < cols_valid;
-    const float* src = ok ? base + (int64_t)row * ld + col : base;
-    const int gs = swizzle ? (g ^ ((r >> 2) & 7)) : g;
-    cp_async16(d0 + (uint32_t)((r * SM_T + 4 * gs) * 4), src, ok ? 16 : 0);
+    const int e = tid + SM_THREADS * q;  // 0 .. 511
+    const int r = e >> 3, g = e & 7;
+    const int col = k0 + 4 * g;
+    const bool ok = r < rows && col < K;
+    cp_async16(d0 + (uint32_t)((r * SM_KC + 4 * (g ^ (r & 7))) * 4), ok ? base + (int64_t)r * ld + col : base,
+               ok ? 16 : 0);
   }
 }
 
+// One operand chunk stored M/N-contiguous: 32 rows (matrix rows k0 .. k0+31,
+// valid below K) of 16 groups (columns 4g, valid below `cols`), unswizzled.
+__device__ __forceinline__ void copy_mn_rows(float* dst, const float* base, int64_t ld, int cols, int k0, int K,
+                                             int tid) {
+  const uint32_t d0 = smem_addr(dst);
+#pragma unroll
+  for (int q = 0; q < SM_CHUNK_FLOATS / 4 / SM_THREADS; ++q) {
+    const int e = tid + SM_THREADS * q;
+    const int r = e >> 4, g = e & 15;
+    const int row = k0 + r;
+    const bool ok = row < K && 4 * g < cols;
+    cp_async16(d0 + (uint32_t)((r * SM_T + 4 * g) * 4), ok ? base + (int64_t)row * ld + 4 * g : base, ok ? 16 : 0);
+  }
+}
+
+// Tile row of the thread's i-th accumulator row, tile column of its j-th column.
+template <bool TA>
+__device__ __forceinline__ int row_of(int i, int wm, int ty) {
+  return TA ? 32 * wm + 16 * (i >> 2) + 4 * ty + (i & 3) : 32 * wm + ty + 4 * i;
+}
+template <bool TB>
+__device__ __forceinline__ int col_of(int j, int tx) {
+  return TB ? tx + 8 * j : 32 * (j >> 2) + 4 * tx + (j & 3);
+}
+
 template <bool TA, bool TB>
-__global__ void __launch_bounds__(SM_THREADS, 3) small_gemm_kernel(const GemmParams p) {
+__global__ void __launch_bounds__(SM_THREADS, SM_CTAS) small_gemm_kernel(const GemmParams p) {
   extern __shared__ __align__(16) float smem[];
   const int tid = threadIdx.x;
-  const int ty = tid >> 3, tx = tid & 7;  // rows 4ty .. +3, columns 4tx .. +3 and 32 + 4tx .. +3
-  const int chunks = (p.K + SM_T - 1) / SM_T;
+  const int wm = tid >> 5, lane = tid & 31;
+  const int ty = lane >> 3, tx = lane & 7;
+  const int chunks = (p.K + SM_KC - 1) / SM_KC;
   // items of this CTA: products blockIdx.x, blockIdx.x + gridDim.x, ..., `chunks` K chunks each
   const int my_products = (p.batch - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   const int items = my_products * chunks;
 
   const auto issue = [&](int item) {
     const int64_t prod = (int64_t)blockIdx.x + (int64_t)(item / chunks) * gridDim.x;
-    const int k0 = (item % chunks) * SM_T;
+    const int k0 = (item % chunks) * SM_KC;
     float* st = smem + (item & 1) * SM_STAGE_FLOATS;
     const float* A = p.A + prod * p.stride_a;
     const float* B = p.B + prod * p.stride_b;
-    if (!TA) copy_chunk(st, A, p.lda, 0, p.M, k0, p.K, true, tid);   // [m][k]
-    else copy_chunk(st, A, p.lda, k0, p.K, 0, p.M, false, tid);      // [k][m]
-    if (!TB) copy_chunk(st + SM_CHUNK_FLOATS, B, p.ldb, k0, p.K, 0, p.N, false, tid);  // [k][n]
-    else copy_chunk(st + SM_CHUNK_FLOATS, B, p.ldb, 0, p.N, k0, p.K, true, tid);       // [n][k]
+    if (!TA) copy_k_rows(st, A, p.lda, p.M, k0, p.K, tid);
+    else copy_mn_rows(st, A, p.lda, p.M, k0, p.K, tid);
+    if (!TB) copy_mn_rows(st + SM_CHUNK_FLOATS, B, p.ldb, p.N, k0, p.K, tid);
+    else copy_k_rows(st + SM_CHUNK_FLOATS, B, p.ldb, p.N, k0, p.K, tid);
   };
 
-  float2 acc[4][4], mst[4][4];
+  // per-thread float offsets of the M/N-contiguous fragments (first column of 4) and of the
+  // K-contiguous B rows
+  int a_off[2], b_off[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int h = 0; h < 2; ++h) a_off[h] = row_of<TA>(4 * h, wm, ty);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = mst[i][j] = make_float2(0.0f, 0.0f);
+  for (int j = 0; j < 8; ++j) b_off[j] = TB ? col_of<TB>(j, tx) * SM_KC : col_of<TB>(j, tx);
+
+  float2 acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
   if (items > 0) issue(0);
   cp_async_commit();
@@ -114,90 +147,97 @@ __global__ void __launch_bounds__(SM_THREADS, 3) small_gemm_kernel(const GemmPar
     const float* As = smem + (it & 1) * SM_STAGE_FLOATS;
     const float* Bs = As + SM_CHUNK_FLOATS;
 #pragma unroll 2
-    for (int k4 = 0; k4 < SM_T / 4; ++k4) {
-      float a[4][4];  // a[i][kk] = op(A)[4ty + i][4k4 + kk]
-      float b[8][4];  // b[j][kk] = op(B)[4k4 + kk][column j of the thread]
+    for (int g = 0; g < SM_KC / 4; ++g) {
+      float a[4][8], b[4][8];  // a[kk][i] = op(A)(row i, 4g + kk), b[kk][j] = op(B)(4g + kk, column j)
       if (!TA) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 v = lds4(As + (4 * ty + i) * SM_T + 4 * (k4 ^ (ty & 7)));
-          a[i][0] = v.x; a[i][1] = v.y; a[i][2] = v.z; a[i][3] = v.w;
+        for (int i = 0; i < 8; ++i) {
+          const int r = row_of<TA>(i, wm, ty);
+          const float4 v = lds4(As + r * SM_KC + 4 * (g ^ (r & 7)));
+          a[0][i] = v.x; a[1][i] = v.y; a[2][i] = v.z; a[3][i] = v.w;
         }
       } else {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const float4 v = lds4(As + (4 * k4 + kk) * SM_T + 4 * ty);
-          a[0][kk] = v.x; a[1][kk] = v.y; a[2][kk] = v.z; a[3][kk] = v.w;
-        }
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float4 v = lds4(As + (4 * g + kk) * SM_T + a_off[h]);
+            a[kk][4 * h] = v.x; a[kk][4 * h + 1] = v.y; a[kk][4 * h + 2] = v.z; a[kk][4 * h + 3] = v.w;
+          }
       }
       if (!TB) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const float4 v0 = lds4(Bs + (4 * k4 + kk) * SM_T + 4 * tx);
-          const float4 v1 = lds4(Bs + (4 * k4 + kk) * SM_T + 32 + 4 * tx);
-          b[0][kk] = v0.x; b[1][kk] = v0.y; b[2][kk] = v0.z; b[3][kk] = v0.w;
-          b[4][kk] = v1.x; b[5][kk] = v1.y; b[6][kk] = v1.z; b[7][kk] = v1.w;
-        }
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float4 v = lds4(Bs + (4 * g + kk) * SM_T + b_off[4 * h]);
+            b[kk][4 * h] = v.x; b[kk][4 * h + 1] = v.y; b[kk][4 * h + 2] = v.z; b[kk][4 * h + 3] = v.w;
+          }
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int n = (j < 4 ? 0 : 28) + 4 * tx + j;  // 4tx + j, then 32 + 4tx + j - 4; (n / 4) % 8 == tx
-          const float4 v = lds4(Bs + n * SM_T + 4 * (k4 ^ tx));
-          b[j][0] = v.x; b[j][1] = v.y; b[j][2] = v.z; b[j][3] = v.w;
+          const float4 v = lds4(Bs + b_off[j] + 4 * (g ^ tx));  // row tx + 8j: (row % 8) == tx
+          b[0][j] = v.x; b[1][j] = v.y; b[2][j] = v.z; b[3][j] = v.w;
         }
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 ai = make_float2(a[i][kk], a[i][kk]);
+        for (int i = 0; i < 8; ++i) {
+          const float2 ai = make_float2(a[kk][i], a[kk][i]);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            acc[i][j] = __ffma2_rn(ai, make_float2(b[2 * j][kk], b[2 * j + 1][kk]), acc[i][j]);
+          for (int q = 0; q < 4; ++q)
+            acc[i][q] = __ffma2_rn(ai, make_float2(b[kk][2 * q], b[kk][2 * q + 1]), acc[i][q]);
         }
     }
-    // fold the chunk's partial sums (round-to-nearest adds)
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        mst[i][j] = __fadd2_rn(mst[i][j], acc[i][j]);
-        acc[i][j] = make_float2(0.0f, 0.0f);
-      }
 
     if ((it + 1) % chunks == 0) {
-      // ---- last chunk of the product: C = alpha * sum + beta * C (C not read when
-      // beta == 0); a warp stores 128 contiguous bytes of each of 4 rows per instruction
+      // ---- last chunk of the product: C = alpha * sum + beta * C (C not read when beta == 0)
       const int64_t prod = (int64_t)blockIdx.x + (int64_t)(it / chunks) * gridDim.x;
       float* Cp = p.C + prod * p.stride_c;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int row = 4 * ty + i;
+      for (int i = 0; i < 8; ++i) {
+        const int row = row_of<TA>(i, wm, ty);
         if (row < p.M) {
           float* crow = Cp + (int64_t)row * p.ldc;
+          const float v[8] = {acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y,
+                              acc[i][2].x, acc[i][2].y, acc[i][3].x, acc[i][3].y};
+          if (!TB) {
+            // columns 4tx .. +3 and 32 + 4tx .. +3: a warp stores 128 contiguous bytes per row
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int col = 32 * q + 4 * tx;
-            const float v[4] = {mst[i][2 * q].x, mst[i][2 * q].y, mst[i][2 * q + 1].x, mst[i][2 * q + 1].y};
-            if (p.c_vec && col + 3 < p.N) {
-              float4* cp = reinterpret_cast<float4*>(crow + col);
-              if (p.beta == 0.0f) {
-                *cp = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
+            for (int h = 0; h < 2; ++h) {
+              const int col = 32 * h + 4 * tx;
+              if (p.c_vec && col + 3 < p.N) {
+                float4* cp = reinterpret_cast<float4*>(crow + col);
+                if (p.beta == 0.0f) {
+                  *cp = make_float4(p.alpha * v[4 * h], p.alpha * v[4 * h + 1], p.alpha * v[4 * h + 2],
+                                    p.alpha * v[4 * h + 3]);
+                } else {
+                  const float4 c = *cp;
+                  *cp = make_float4(fmaf(p.alpha, v[4 * h], p.beta * c.x), fmaf(p.alpha, v[4 * h + 1], p.beta * c.y),
+                                    fmaf(p.alpha, v[4 * h + 2], p.beta * c.z),
+                                    fmaf(p.alpha, v[4 * h + 3], p.beta * c.w));
+                }
               } else {
-                const float4 c = *cp;
-                *cp = make_float4(fmaf(p.alpha, v[0], p.beta * c.x), fmaf(p.alpha, v[1], p.beta * c.y),
-                                  fmaf(p.alpha, v[2], p.beta * c.z), fmaf(p.alpha, v[3], p.beta * c.w));
-              }
-            } else {
 #pragma unroll
-              for (int h = 0; h < 4; ++h)
-                if (col + h < p.N)
-                  crow[col + h] = p.beta == 0.0f ? p.alpha * v[h] : fmaf(p.alpha, v[h], p.beta * crow[col + h]);
+                for (int e = 0; e < 4; ++e)
+                  if (col + e < p.N)
+                    crow[col + e] = p.beta == 0.0f ? p.alpha * v[4 * h + e]
+                                                   : fmaf(p.alpha, v[4 * h + e], p.beta * crow[col + e]);
+              }
+            }
+          } else {
+            // columns tx + 8j: a warp stores 32 contiguous bytes of 4 rows per instruction
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int col = tx + 8 * j;
+              if (col < p.N)
+                crow[col] = p.beta == 0.0f ? p.alpha * v[j] : fmaf(p.alpha, v[j], p.beta * crow[col]);
             }
           }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) mst[i][j] = make_float2(0.0f, 0.0f);
+        for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.0f, 0.0f);
       }
     }
     __syncthreads();  // every thread is done with this stage before it is refilled

@@ -7,14 +7,14 @@
 
 namespace sgemm_impl {
 
-// Persistent grid of `grid` CTAs (1 <= grid <= p.batch; three fit on an SM),
-// 128 threads each, products dealt round-robin; M <= 64 and N <= 64, any K.
+// Persistent grid of `grid` CTAs (1 <= grid <= p.batch; six fit on an SM),
+// 64 threads each, products dealt round-robin; M <= 64 and N <= 64, any K.
 // The planner guarantees the kernel's copy rules: A and B 16-byte aligned,
 // lda, ldb and the batch strides multiples of 4, and K (op 'N' of A, op 'T'
 // of B), M (op 'T' of A) and N (op 'N' of B) multiples of 4.
 cudaError_t launch_small_gemm(bool transA, bool transB, const GemmParams& p, int grid, cudaStream_t stream);
 
-// Raises the kernel's dynamic shared-memory limit (64 KB); once per device.
+// Sets the kernels' dynamic shared-memory size (32 KB); once per device.
 cudaError_t prepare_small_gemm();
 
 }  // namespace sgemm_impl

@@ -213,24 +213,26 @@ def test_batched_planner(lib):
 
 
 def test_small_product_planner(lib):
-    # 8192 products of 64x64x64: one 128-thread CTA per product, no tensor maps, no workspace
+    # 8192 products of 64x64x64: a persistent grid of 64-thread CTAs, six per SM, no workspace
     p = bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64)
-    assert p["variant_name"] == "SMALL" and (p["grid_x"], p["grid_y"], p["threads"]) == (3 * 152, 1, 128)
+    assert p["variant_name"] == "SMALL" and (p["grid_x"], p["grid_y"], p["threads"]) == (6 * 152, 1, 64)
     assert (p["kernel_launches"], p["split_k"], p["workspace_bytes"]) == (1, 1, 0)
-    assert p["smem_bytes"] == 2 * 2 * 64 * 64 * 4 and p["stages"] == 2
+    assert p["smem_bytes"] == 2 * 2 * 64 * 32 * 4 and p["stages"] == 2 and p["tile_k"] == 32
     # the persistent grid never exceeds the batch
-    assert bplan("N", "N", 64, 64, 64, 200, 64 * 64, 64 * 64, 64 * 64)["grid_x"] == 200
-    assert bplan("N", "N", 64, 64, 64, 200, 64 * 64, 64 * 64, 64 * 64, sm=1)["grid_x"] == 3
+    assert bplan("N", "N", 64, 64, 64, 200, 64 * 64, 64 * 64, 64 * 64, sm=100)["grid_x"] == 200
+    assert bplan("N", "N", 64, 64, 64, 200, 64 * 64, 64 * 64, 64 * 64, sm=1)["grid_x"] == 6
     # every op combination, ragged M and N below the tile, shared operands
     for ta in "NT":
         for tb in "NT":
             M, N, K = 36, 20, 100
-            q = bplan(ta, tb, M, N, K, 152, M * K, K * N, M * N)
+            q = bplan(ta, tb, M, N, K, 304, M * K, K * N, M * N)
             assert q["variant_name"] == "SMALL", (ta, tb)
     assert bplan("N", "N", 64, 64, 64, 500, 64 * 64, 0, 64 * 64)["variant_name"] == "SMALL"
-    # too few products to fill the SMs, too long K, outputs above 64: the tensor-core kernel
-    assert bplan("N", "N", 64, 64, 64, 151, 64 * 64, 64 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
-    assert bplan("N", "N", 64, 64, 1028, 8192, 64 * 1028, 1028 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
+    # fewer than two products per SM, K above 128, outputs above 64: the tensor-core kernel
+    assert bplan("N", "N", 64, 64, 64, 303, 64 * 64, 64 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
+    assert bplan("N", "N", 64, 64, 128, 304, 64 * 128, 128 * 64, 64 * 64)["variant_name"] == "SMALL"
+    assert bplan("N", "N", 64, 64, 132, 8192, 64 * 132, 132 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
+    assert bplan("N", "N", 64, 64, 64, 303, 64 * 64, 64 * 64, 64 * 64, sm=100)["variant_name"] == "SMALL"
     assert bplan("N", "N", 65, 64, 64, 8192, 65 * 64, 64 * 64, 65 * 64)["variant_name"] == "TC_TF32X3"
     assert bplan("N", "N", 64, 68, 64, 8192, 64 * 64, 64 * 68, 64 * 68)["variant_name"] == "TC_TF32X3"
     # the float4 rules: the contiguous extent of each operand a multiple of 4
@@ -251,8 +253,8 @@ def test_small_product_planner(lib):
         assert bplan("N", "N", 64, 64, 2048, 2, 64 * 2048, 2048 * 64, 64 * 64)["variant_name"] == "SMALL"
         assert plan("N", "N", 64, 64, 64)["variant_name"] == "SMALL"
         assert plan("N", "N", 65, 64, 64)["variant_name"] == "GENERIC"
-        # a CTA's (product, K chunk) items must fit an int: 2300 products x 2^24 chunks do not
-        huge_k = 64 << 24
+        # a CTA's (product, K chunk) items must fit an int: 1150 products x 2^25 chunks do not
+        huge_k = 32 << 25
         assert bplan("N", "N", 64, 64, huge_k, 1 << 20, 0, 0, 64 * 64, lda=huge_k)["variant_name"] == "GENERIC"
         assert bplan("N", "N", 64, 64, huge_k, 4, 0, 0, 64 * 64, lda=huge_k)["variant_name"] == "SMALL"
         sg.sgemm_set_variant_override("TC_TF32X3", 0)

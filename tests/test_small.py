@@ -29,9 +29,9 @@ def _dyadic_stack(d, rng, bits=6):
 @pytest.mark.parametrize("shared", ["", "A", "B"])
 @pytest.mark.parametrize("ops", OPS)
 def test_small_parity(ops, shared):
-    """160 ragged products of 36x20x196 (4 K chunks, the last one ragged), padded rows, gaps."""
+    """320 ragged products of 36x20x100 (4 K chunks, the last one ragged), padded rows, gaps."""
     ta, tb = ops
-    batch, M, N, K = 160, 36, 20, 196
+    batch, M, N, K = 320, 36, 20, 100
     d = si.make_batched(batch, M, N, K, ta, tb, seed=51, pad=4, gap=4, align=4, shared=shared)
     assert plan_of(ta, tb, M, N, K, d, batch)["variant_name"] == "SMALL"
     got = gpu_batched(ta, tb, M, N, K, 1.5, -0.5, d, batch)
@@ -41,9 +41,9 @@ def test_small_parity(ops, shared):
 
 @pytest.mark.parametrize("ops", OPS)
 def test_small_persistent_rounds(ops):
-    """1111 products on the persistent grid (2-3 products per CTA, 4 K chunks each, the last ragged)."""
+    """1111 products on the persistent grid (1-2 products per CTA, 4 K chunks each, the last ragged)."""
     ta, tb = ops
-    batch, M, N, K = 1111, 52, 44, 200
+    batch, M, N, K = 1111, 52, 44, 124
     d = si.make_batched(batch, M, N, K, ta, tb, seed=58, pad=4, gap=4, align=4)
     p = plan_of(ta, tb, M, N, K, d, batch)
     assert p["variant_name"] == "SMALL" and p["grid_x"] < batch
@@ -54,13 +54,12 @@ def test_small_persistent_rounds(ops):
 
 @pytest.mark.parametrize("ops", OPS)
 def test_small_dyadic_exact(ops):
-    """Full 64x64 tiles at the longest default K (16 chunks): bit-exact on dyadic inputs."""
+    """Full 64x64 tiles at K = 1024 (32 chunks, kernel forced): bit-exact on dyadic inputs."""
     ta, tb = ops
     batch, M, N, K = 152, 64, 64, 1024
     d = _dyadic_stack(si.make_batched(batch, M, N, K, ta, tb, seed=0, pad=0, gap=8, align=4),
                       np.random.default_rng(52))
-    assert plan_of(ta, tb, M, N, K, d, batch)["variant_name"] == "SMALL"
-    got = gpu_batched(ta, tb, M, N, K, 1.5, -0.5, d, batch)
+    got = gpu_batched(ta, tb, M, N, K, 1.5, -0.5, d, batch, variant="SMALL")
     ref, S = oracle_batched(ta, tb, M, N, K, 1.5, -0.5, d, batch)
     check_batched(got, ref, S, d, batch, M, N, K, f"dyadic {ops}", exact=True)
 
@@ -92,8 +91,9 @@ def test_small_edges_forced(M, N, K, ops):
 
 def test_small_beta_zero_does_not_read_c():
     """beta = 0: C may hold NaN on entry and the result is alpha op(A) op(B) all the same."""
-    batch, M, N, K = 152, 64, 48, 64
+    batch, M, N, K = 400, 64, 48, 64
     d = si.make_batched(batch, M, N, K, "N", "T", seed=54, pad=0, gap=0, align=4)
+    assert plan_of("N", "T", M, N, K, d, batch)["variant_name"] == "SMALL"
     d["C"] = np.full_like(d["C"], np.nan)
     got = gpu_batched("N", "T", M, N, K, 0.75, 0.0, d, batch)
     zero = dict(d, C=np.zeros_like(d["C"]))
@@ -106,7 +106,7 @@ def test_small_scalar_c_path_with_guard_bands(ops):
     """C 4 bytes past 16-byte alignment, ldc % 4 == 1, NaN around every product: scalar stores only."""
     torch = torch_cuda()
     ta, tb = ops
-    batch, M, N, K, ldc = 152, 40, 24, 72, 25
+    batch, M, N, K, ldc = 400, 40, 24, 72, 25
     d = si.make_batched(batch, M, N, K, ta, tb, seed=55, pad=4, gap=4, align=4)
     strideC = M * ldc + 3
     C = si.embed_batched(d["stacks"]["C"], ldc, strideC)
@@ -130,8 +130,9 @@ def test_small_scalar_c_path_with_guard_bands(ops):
 
 def test_small_non_finite_follow_ieee():
     """Inf and NaN inputs give the non-finite pattern of IEEE arithmetic (the FFMA path keeps Inf)."""
-    batch, M, N, K = 152, 16, 16, 128
+    batch, M, N, K = 320, 16, 16, 128
     d = si.make_batched(batch, M, N, K, "N", "N", seed=56, pad=0, gap=0, align=4)
+    assert plan_of("N", "N", M, N, K, d, batch)["variant_name"] == "SMALL"
     A, B = d["stacks"]["A"].copy(), d["stacks"]["B"].copy()
     A[0, 3, 70] = np.inf          # row 3 of product 0: +-Inf where B[70, n] != 0
     A[1, 5, 10] = np.nan          # row 5 of product 1: NaN
