@@ -175,7 +175,7 @@ constexpr int64_t kSmallMaxMN = 64;
 constexpr int64_t kSmallMaxK = 128;
 constexpr int64_t kSmallMinProductsPerSm = 2;
 constexpr int64_t kSmallKChunk = 32;
-constexpr int64_t kSmallCtasPerSm = 6;  // persistent grid: 6 x 32 KB of stages per SM
+constexpr int64_t kSmallCtasPerSm = 4;  // persistent grid: 4 x 32 KB of stages per SM
 
 int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
   const int64_t sms = std::max(1, sm_count);

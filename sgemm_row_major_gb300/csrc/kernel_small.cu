@@ -10,9 +10,11 @@
 // stored orientation, and the next item's copies are issued before the
 // current item is computed.  Two warps share the tile, 32 rows each; a
 // thread accumulates an 8x8 block with packed FP32 FMAs (fma.rn.f32x2, IEEE
-// round-to-nearest, k ascending), so each 128-bit shared load feeds 16 FMAs.
-// The grid is persistent (six CTAs per SM, products dealt round-robin), so
-// HBM traffic and FMA work overlap within a CTA and across the CTAs of an SM.
+// round-to-nearest, k ascending), so each 128-bit shared load feeds 16 FMAs,
+// and loads the fragments of the next group of 4 k while the current group's
+// FMAs issue.  The grid is persistent (four CTAs per SM, products dealt
+// round-robin), so HBM traffic and FMA work overlap within a CTA and across
+// the CTAs of an SM.
 //
 // Shared layout of a stage: the A chunk, then the B chunk.  An operand stored
 // K-contiguous (A 'N' as [m][k], B 'T' as [n][k]) is kept as 64 rows of 32
@@ -37,12 +39,12 @@ namespace {
 constexpr int SM_T = 64;                              // output tile
 constexpr int SM_KC = 32;                             // K chunk
 constexpr int SM_THREADS = 64;                        // 2 warps, 8x8 results per thread
-constexpr int SM_CTAS = 6;                            // CTAs per SM
+constexpr int SM_CTAS = 4;                            // CTAs per SM
 constexpr int SM_CHUNK_FLOATS = SM_T * SM_KC;         // one operand chunk (8 KB)
 constexpr int SM_STAGE_FLOATS = 2 * SM_CHUNK_FLOATS;  // A chunk + B chunk
 constexpr int SM_SMEM_BYTES = 2 * SM_STAGE_FLOATS * 4;
 static_assert(SM_SMEM_BYTES == 32768, "two 16 KB stages");
-static_assert(SM_CTAS * (SM_SMEM_BYTES + 1024) <= 228 * 1024, "six CTAs per SM");
+static_assert(SM_CTAS * (SM_SMEM_BYTES + 1024) <= 228 * 1024, "CTAs per SM");
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -98,6 +100,56 @@ __device__ __forceinline__ int col_of(int j, int tx) {
   return TB ? tx + 8 * j : 32 * (j >> 2) + 4 * tx + (j & 3);
 }
 
+// Fragments of group g (k 4g .. 4g+3 of the chunk) for the thread's 8 rows and 8 columns.
+template <bool TA, bool TB>
+__device__ __forceinline__ void load_group(const float* As, const float* Bs, int g, int wm, int ty, int tx,
+                                           const int (&a_off)[2], const int (&b_off)[8], float (&a)[4][8],
+                                           float (&b)[4][8]) {
+  if (!TA) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = row_of<TA>(i, wm, ty);
+      const float4 v = lds4(As + r * SM_KC + 4 * (g ^ (r & 7)));
+      a[0][i] = v.x; a[1][i] = v.y; a[2][i] = v.z; a[3][i] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float4 v = lds4(As + (4 * g + kk) * SM_T + a_off[h]);
+        a[kk][4 * h] = v.x; a[kk][4 * h + 1] = v.y; a[kk][4 * h + 2] = v.z; a[kk][4 * h + 3] = v.w;
+      }
+  }
+  if (!TB) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float4 v = lds4(Bs + (4 * g + kk) * SM_T + b_off[4 * h]);
+        b[kk][4 * h] = v.x; b[kk][4 * h + 1] = v.y; b[kk][4 * h + 2] = v.z; b[kk][4 * h + 3] = v.w;
+      }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 v = lds4(Bs + b_off[j] + 4 * (g ^ tx));  // row tx + 8j: (row % 8) == tx
+      b[0][j] = v.x; b[1][j] = v.y; b[2][j] = v.z; b[3][j] = v.w;
+    }
+  }
+}
+
+// 4 rank-1 updates of the thread's 8x8 block, k ascending.
+__device__ __forceinline__ void fma_group(const float (&a)[4][8], const float (&b)[4][8], float2 (&acc)[8][4]) {
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 ai = make_float2(a[kk][i], a[kk][i]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[i][q] = __ffma2_rn(ai, make_float2(b[kk][2 * q], b[kk][2 * q + 1]), acc[i][q]);
+    }
+}
+
 template <bool TA, bool TB>
 __global__ void __launch_bounds__(SM_THREADS, SM_CTAS) small_gemm_kernel(const GemmParams p) {
   extern __shared__ __align__(16) float smem[];
@@ -146,49 +198,13 @@ __global__ void __launch_bounds__(SM_THREADS, SM_CTAS) small_gemm_kernel(const G
     __syncthreads();      // ... and every thread's
     const float* As = smem + (it & 1) * SM_STAGE_FLOATS;
     const float* Bs = As + SM_CHUNK_FLOATS;
-#pragma unroll 2
+    // fragments of group g + 1 are loaded while group g's FMAs issue
+    float a[2][4][8], b[2][4][8];  // a[.][kk][i] = op(A)(row i, 4g + kk), b[.][kk][j] = op(B)(4g + kk, column j)
+    load_group<TA, TB>(As, Bs, 0, wm, ty, tx, a_off, b_off, a[0], b[0]);
+#pragma unroll
     for (int g = 0; g < SM_KC / 4; ++g) {
-      float a[4][8], b[4][8];  // a[kk][i] = op(A)(row i, 4g + kk), b[kk][j] = op(B)(4g + kk, column j)
-      if (!TA) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = row_of<TA>(i, wm, ty);
-          const float4 v = lds4(As + r * SM_KC + 4 * (g ^ (r & 7)));
-          a[0][i] = v.x; a[1][i] = v.y; a[2][i] = v.z; a[3][i] = v.w;
-        }
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float4 v = lds4(As + (4 * g + kk) * SM_T + a_off[h]);
-            a[kk][4 * h] = v.x; a[kk][4 * h + 1] = v.y; a[kk][4 * h + 2] = v.z; a[kk][4 * h + 3] = v.w;
-          }
-      }
-      if (!TB) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float4 v = lds4(Bs + (4 * g + kk) * SM_T + b_off[4 * h]);
-            b[kk][4 * h] = v.x; b[kk][4 * h + 1] = v.y; b[kk][4 * h + 2] = v.z; b[kk][4 * h + 3] = v.w;
-          }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 v = lds4(Bs + b_off[j] + 4 * (g ^ tx));  // row tx + 8j: (row % 8) == tx
-          b[0][j] = v.x; b[1][j] = v.y; b[2][j] = v.z; b[3][j] = v.w;
-        }
-      }
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float2 ai = make_float2(a[kk][i], a[kk][i]);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            acc[i][q] = __ffma2_rn(ai, make_float2(b[kk][2 * q], b[kk][2 * q + 1]), acc[i][q]);
-        }
+      if (g + 1 < SM_KC / 4) load_group<TA, TB>(As, Bs, g + 1, wm, ty, tx, a_off, b_off, a[(g + 1) & 1], b[(g + 1) & 1]);
+      fma_group(a[g & 1], b[g & 1], acc);
     }
 
     if ((it + 1) % chunks == 0) {

@@ -7,7 +7,7 @@
 
 namespace sgemm_impl {
 
-// Persistent grid of `grid` CTAs (1 <= grid <= p.batch; six fit on an SM),
+// Persistent grid of `grid` CTAs (1 <= grid <= p.batch; four fit on an SM),
 // 64 threads each, products dealt round-robin; M <= 64 and N <= 64, any K.
 // The planner guarantees the kernel's copy rules: A and B 16-byte aligned,
 // lda, ldb and the batch strides multiples of 4, and K (op 'N' of A, op 'T'
