@@ -39,9 +39,16 @@ import sgemm_inputs as si  # noqa: E402
 METRIC = "SGEMM TFLOPS (2MNK/t) at 4096^3 NN on 1 GB300; % of FP32 FFMA peak"
 UNIT = "TFLOPS"
 FMA_PER_SM_PER_CLK = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
-PROFILES = {"TC_TF32X3": os.path.join(ROOT, "profiles", "tf32x3_gemm_square4096.md"),
-            "TMA_128x128": os.path.join(ROOT, "profiles", "tma_gemm_square4096.md"),
-            "SMALL": os.path.join(ROOT, "profiles", "small_gemm_batched8192x64x64x64.md")}
+# committed ncu summaries by (kernel variant, workload): their per-launch DRAM traffic is reported
+# while the kernel's source digest still matches the one they were captured with
+PROFILES = {("TC_TF32X3", "square4096"): os.path.join(ROOT, "profiles", "tf32x3_gemm_square4096.md"),
+            ("TMA_128x128", "square4096"): os.path.join(ROOT, "profiles", "tma_gemm_square4096.md"),
+            ("SMALL", "batched_small_8192x64x64x64"):
+                os.path.join(ROOT, "profiles", "small_gemm_batched8192x64x64x64.md"),
+            ("TC_PAIRED", "batched_small_k1024_2048x64x64x1024"):
+                os.path.join(ROOT, "profiles", "tf32x3_paired_batched2048x64x64x1024.md"),
+            ("TC_PAIRED", "batched_small_8192x64x64x64"):
+                os.path.join(ROOT, "profiles", "tf32x3_paired_batched8192x64x64x64.md")}
 # dense tensor-core peaks (PFLOP/s, nominal) used to scale the measured bf16 peak to tf32
 NOMINAL_BF16_PF, NOMINAL_TF32_PF = 2.25, 1.1
 TF32_PRODUCTS = 3  # tensor-core products per useful FMA in the 3xTF32 split
@@ -139,10 +146,10 @@ def gpu_selector(device_index: int) -> str:
 
 # ---------------------------------------------------------------- helpers
 
-def traffic_from_profile(variant: str, digest: str):
+def traffic_from_profile(variant: str, workload: str, digest: str):
     """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, if it is current."""
     try:
-        text = open(PROFILES[variant]).read()
+        text = open(PROFILES[(variant, workload)]).read()
     except (OSError, KeyError):
         return None
     d = re.search(r"kernel_digest:\s*([0-9a-f]+)", text)
@@ -479,12 +486,13 @@ def run_ours(args):
     ffma_peak = sms * FMA_PER_SM_PER_CLK * 2 * max_mhz * 1e6 / 1e12
     variant = plan["variant_name"]
     if variant == "TC_TF32X3":
-        roof = tensor_roofline(achieved, peaks, traffic_from_profile(variant, lib_build.tc_kernel_digest()),
+        roof = tensor_roofline(achieved, peaks,
+                               traffic_from_profile(variant, case.name, lib_build.tc_kernel_digest()),
                                kernel_ms)
     else:
         roof = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
                 "frac": achieved / ffma_peak,
-                "traffic": traffic_from_profile(variant, lib_build.tma_kernel_digest()),
+                "traffic": traffic_from_profile(variant, case.name, lib_build.tma_kernel_digest()),
                 "peak_basis": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz max SM clock",
                 "kernel": "tma_gemm_kernel (SIMT FFMA2)" if variant.startswith("TMA") else variant,
                 "kernel_ms": kernel_ms}
@@ -572,13 +580,48 @@ def run_reference_batched(args, c):
     }), flush=True)
 
 
+def batched_bytes(c):
+    """Algorithmic bytes of one strided-batch call: each operand read once (a shared one once in all),
+    C written once, and read too when beta != 0."""
+    n_a = 1 if "A" in c.shared else c.batch
+    n_b = 1 if "B" in c.shared else c.batch
+    return 4 * (n_a * c.M * c.K + n_b * c.K * c.N + c.batch * c.M * c.N * (2 if c.beta != 0 else 1))
+
+
+def batched_roofline(c, plan, flops_step, achieved, kernel_ms, peaks, dev, lib_build):
+    """Roofline object of the kernel a strided batch ran on.  For the tensor-core kernel the bound is
+    whichever of the 3xTF32 tensor peak and HBM takes longer for the call's algorithmic work."""
+    variant = plan["variant_name"]
+    if variant in ("TC_TF32X3", "TC_PAIRED"):
+        traffic = traffic_from_profile(variant, c.name, lib_build.tc_kernel_digest())
+        roof = tensor_roofline(achieved, peaks, traffic, kernel_ms)
+        if variant == "TC_PAIRED":
+            pairs = (c.batch + 1) // 2
+            roof["kernel"] = "tf32x3_gemm_kernel, two products per 128x128 tile (block-diagonal)"
+            roof["useful_fraction_of_tensor_work"] = c.batch * c.M * c.N / (pairs * 128 * 128)
+        nbytes = batched_bytes(c)
+        hbm = peaks.get("hbm_gbs")
+        hbm_basis = "measured" if hbm else "fallback"
+        hbm = hbm or 6800.0
+        if nbytes / (hbm * 1e9) > flops_step / (roof["peak"] * 1e12):
+            gbs = nbytes / (kernel_ms * 1e-3) / 1e9
+            tensor = {k: roof[k] for k in ("achieved", "peak", "unit", "frac", "peak_basis")}
+            roof.update({"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "peak_basis": f"{hbm_basis} HBM copy bandwidth", "algorithmic_bytes": nbytes,
+                         "tensor": tensor})
+        return roof
+    if variant == "SMALL":
+        return small_roofline(c, flops_step, kernel_ms, peaks, dev,
+                              traffic_from_profile(variant, c.name, lib_build.small_kernel_digest()))
+    return {"bound": "alu", "achieved": achieved, "peak": None, "unit": "TFLOP/s", "frac": None,
+            "traffic": None, "kernel": variant, "kernel_ms": kernel_ms}
+
+
 def small_roofline(c, flops_step, kernel_ms, peaks, dev, traffic):
     """Roofline of the small-product kernel: each operand is read once and C written once (read too
     when beta != 0), so the launch is bound by HBM or by the FP32 FMA pipes, whichever takes longer."""
     import torch
-    n_a = 1 if "A" in c.shared else c.batch
-    n_b = 1 if "B" in c.shared else c.batch
-    nbytes = 4 * (n_a * c.M * c.K + n_b * c.K * c.N + c.batch * c.M * c.N * (2 if c.beta != 0 else 1))
+    nbytes = batched_bytes(c)
     hbm = peaks.get("hbm_gbs")
     hbm_basis = "measured" if hbm else "fallback"
     hbm = hbm or 6800.0
@@ -659,12 +702,7 @@ def run_ours_batched(args, c):
         "config": {**batched_config_block(c, d, world), "l2": l2_note(flush), "prewarm_s": args.prewarm_s,
                    "plan": {k: plan[k] for k in ("variant_name", "split_k", "grid_x", "grid_y", "dp_tiles",
                                                  "sk_tiles")}},
-        "roofline": (tensor_roofline(achieved, peaks, None, kernel_ms) if plan["variant_name"] == "TC_TF32X3"
-                     else small_roofline(c, flops_step, kernel_ms, peaks, dev,
-                                         traffic_from_profile("SMALL", lib_build.small_kernel_digest()))
-                     if plan["variant_name"] == "SMALL"
-                     else {"bound": "alu", "achieved": achieved, "peak": None, "unit": "TFLOP/s", "frac": None,
-                           "traffic": None, "kernel": plan["variant_name"], "kernel_ms": kernel_ms}),
+        "roofline": batched_roofline(c, plan, flops_step, achieved, kernel_ms, peaks, dev, lib_build),
         "e2e": {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
                 "note": "no host-buffer batched entry point; the device-resident value is the measurement"},
         "gpu_launches": plan["kernel_launches"] * args.steps,

@@ -261,6 +261,8 @@ BATCHED_CASES: list[BatchedCase] = [
     BatchedCase("batched_fc_shared_w_32x2048x1024x1024", 32, 2048, 1024, 1024, seed=22, shared="B"),
     # many small products: the launch and tail overheads dominate
     BatchedCase("batched_small_8192x64x64x64", 8192, 64, 64, 64, seed=23, dist="uniform"),
+    # small outputs, long K: two products to a tensor-core tile
+    BatchedCase("batched_small_k1024_2048x64x64x1024", 2048, 64, 64, 1024, seed=24, dist="uniform"),
 ]
 
 

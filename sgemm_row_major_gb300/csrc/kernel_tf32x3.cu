@@ -250,7 +250,16 @@ __device__ __forceinline__ Segment cta_segment(const GemmParams& p, const CtaWor
 // Raw tile layouts (as the TMA engine copies them):
 //   op(A) 'N': [128 rows of M][32 k], K contiguous, 128-byte swizzle;  'T': [32 k][128 m], M contiguous.
 //   op(B) 'N': [32 k][128 n], N contiguous;  'T': [128 n][32 k], K contiguous, 128-byte swizzle.
-template <bool TA, bool TB>
+//
+// PAIR: products with M <= 64 and N <= 64 go two to a tile, block-diagonally:
+// rows 0-63 and columns 0-63 hold product 2t, rows 64-127 and columns 64-127
+// product 2t+1 (tile t; a missing partner of an odd batch reads zeros), so the
+// accumulator's diagonal 64x64 blocks are the two products and half of the
+// tensor-core work is useful instead of a quarter.  Each operand tile is then
+// two 64-wide TMA boxes: K-contiguous ones stack into the same layout, while
+// an M/N-contiguous one becomes two [32 k][64] halves.  Only the folder warps
+// on the diagonal blocks fold and write C; there is no stream-K in this mode.
+template <bool TA, bool TB, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                        const GemmParams p) {
@@ -316,8 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int sgi = 0; ok && sgi < work.nseg; ++sgi) {
         const Segment g = cta_segment(p, work, cta, sgi, kt_total);
         int prod, m0, n0;
-        tile_origin(p, g.tile, prod, m0, n0);
+        if (PAIR) {
+          prod = 2 * g.tile;
+          m0 = n0 = 0;
+        } else {
+          tile_origin(p, g.tile, prod, m0, n0);
+        }
         const int za = prod * p.za, zb = prod * p.zb;
+        const int za1 = (prod + 1) * p.za, zb1 = (prod + 1) * p.zb;  // PAIR: the second product
         for (int kt = g.kb; kt < g.ke; ++kt) {
           const int t = issued;
           const int r = t % kRawStages;
@@ -330,10 +345,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = smem_addr(&raw_full[r]);
           mbar_arrive_expect_tx(fb, (uint32_t)kRawBytes);
           const int k0 = kt * BK;
-          if (!TA) tma_load_3d(raw_a(r), &mapA, fb, k0, m0, za);
-          else     tma_load_3d(raw_a(r), &mapA, fb, m0, k0, za);
-          if (!TB) tma_load_3d(raw_b(r), &mapB, fb, n0, k0, zb);
-          else     tma_load_3d(raw_b(r), &mapB, fb, k0, n0, zb);
+          if (PAIR) {
+            // two 64-wide boxes per operand (8 KB each), second product at +8 KB
+            if (!TA) { tma_load_3d(raw_a(r), &mapA, fb, k0, 0, za); tma_load_3d(raw_a(r) + 8192u, &mapA, fb, k0, 0, za1); }
+            else     { tma_load_3d(raw_a(r), &mapA, fb, 0, k0, za); tma_load_3d(raw_a(r) + 8192u, &mapA, fb, 0, k0, za1); }
+            if (!TB) { tma_load_3d(raw_b(r), &mapB, fb, 0, k0, zb); tma_load_3d(raw_b(r) + 8192u, &mapB, fb, 0, k0, zb1); }
+            else     { tma_load_3d(raw_b(r), &mapB, fb, k0, 0, zb); tma_load_3d(raw_b(r) + 8192u, &mapB, fb, k0, 0, zb1); }
+          } else {
+            if (!TA) tma_load_3d(raw_a(r), &mapA, fb, k0, m0, za);
+            else     tma_load_3d(raw_a(r), &mapA, fb, m0, k0, za);
+            if (!TB) tma_load_3d(raw_b(r), &mapB, fb, n0, k0, zb);
+            else     tma_load_3d(raw_b(r), &mapB, fb, k0, n0, zb);
+          }
           issued = t + 1;
         }
       }
@@ -423,11 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo[4 * j + 0] = l.x; lo[4 * j + 1] = l.y; lo[4 * j + 2] = l.z; lo[4 * j + 3] = l.w;
           }
         } else {
-          // M-contiguous [32 k][128 m]: one float per k (a warp reads 32 adjacent m)
-          const float* fa = reinterpret_cast<const float*>(ra);
+          // M-contiguous [32 k][128 m] (PAIR: two [32 k][64 m] halves): one float per k (a warp
+          // reads 32 adjacent m)
+          const float* fa = reinterpret_cast<const float*>(ra) + (PAIR ? (m >> 6) * (BK * 64) : 0);
+          const int mm = PAIR ? (m & 63) : m;
+          constexpr int lda_s = PAIR ? 64 : BM;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float x = fa[(16 * half + j) * BM + m];
+            const float x = fa[(16 * half + j) * lda_s + mm];
             hi[j] = tf32_round(x);
             lo[j] = x - hi[j];
           }
@@ -442,14 +468,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* bhi = smem + (split_tile(s, 0) - sbase);
         uint8_t* blo = smem + (split_tile(s, 1) - sbase);
         if (!TB) {
-          // raw [32 k][128 n]: transpose; thread st owns column n = st % 128, k chunks 4*(st/128) .. +3
-          const float* rb = reinterpret_cast<const float*>(smem + (raw_b(r) - sbase));
+          // raw [32 k][128 n] (PAIR: two [32 k][64 n] halves): transpose; thread st owns column
+          // n = st % 128, k chunks 4*(st/128) .. +3
           const int n = st & 127, kh = st >> 7;
+          const float* rb = reinterpret_cast<const float*>(smem + (raw_b(r) - sbase)) + (PAIR ? (n >> 6) * (BK * 64) : 0);
+          const int nn = PAIR ? (n & 63) : n;
+          constexpr int ldb_s = PAIR ? 64 : BN;
 #pragma unroll
           for (int kq = 0; kq < 4; ++kq) {
             const int kc = 4 * kh + kq;
-            const float4 x = make_float4(rb[(4 * kc + 0) * BN + n], rb[(4 * kc + 1) * BN + n],
-                                         rb[(4 * kc + 2) * BN + n], rb[(4 * kc + 3) * BN + n]);
+            const float4 x = make_float4(rb[(4 * kc + 0) * ldb_s + nn], rb[(4 * kc + 1) * ldb_s + nn],
+                                         rb[(4 * kc + 2) * ldb_s + nn], rb[(4 * kc + 3) * ldb_s + nn]);
             float4 hi, lo;
             split4(x, hi, lo);
             const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(kc ^ (n & 7)) << 4);
@@ -486,6 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                          // TMEM lane quarter this warp may access
     const int half = (warp - kFirstFoldWarp) >> 2;   // which 64 accumulator columns
     const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * half);
+    // PAIR: only the diagonal blocks are products; the other warps keep to the barrier protocol
+    const bool useful = !PAIR || (q >> 1) == half;
     float2 master2[32];  // columns 2e, 2e+1 of this thread's 64
 #pragma unroll
     for (int e = 0; e < 32; ++e) master2[e] = make_float2(0.0f, 0.0f);
@@ -504,19 +535,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
           break;
         }
-        tmem_fence_after_sync();
-        float v[4][16];
+        if (useful) {
+          tmem_fence_after_sync();
+          float v[4][16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld16(tq + (uint32_t)b * kAccCols + 16u * c, v[c]);
-        tmem_wait_ld();
+          for (int c = 0; c < 4; ++c) tmem_ld16(tq + (uint32_t)b * kAccCols + 16u * c, v[c]);
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld_ready(v[c]);
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld_ready(v[c]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)  // round-to-nearest FP32 adds, two per instruction
-            master2[8 * c + e] = __fadd2_rn(master2[8 * c + e], make_float2(v[c][2 * e], v[c][2 * e + 1]));
+            for (int e = 0; e < 8; ++e)  // round-to-nearest FP32 adds, two per instruction
+              master2[8 * c + e] = __fadd2_rn(master2[8 * c + e], make_float2(v[c][2 * e], v[c][2 * e + 1]));
+          }
+          tmem_fence_before_sync();
         }
-        tmem_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&acc_empty[b]));
       }
@@ -530,11 +563,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e)
           *reinterpret_cast<float4*>(w + 4 * e) =
               make_float4(master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y);
-      } else {
+      } else if (useful) {
         int prod, m0, n0;
-        tile_origin(p, g.tile, prod, m0, n0);
+        if (PAIR) {
+          prod = 2 * g.tile + half;  // rows and columns 64*half .. +63 of the tile
+          m0 = -64 * half;
+          n0 = -64 * half;
+        } else {
+          tile_origin(p, g.tile, prod, m0, n0);
+        }
         const int row = m0 + 32 * q + lane;
-        if (row < p.M) {
+        if (row < p.M && (!PAIR || prod < p.batch)) {
           float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -635,34 +674,45 @@ __global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(const Gemm
 
 namespace {
 
-template <bool TA, bool TB>
+template <bool TA, bool TB, bool PAIR>
 cudaError_t set_attrs() {
-  return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<TA, TB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<TA, TB, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               tc::kSmemBytes);
 }
 
-template <bool TA, bool TB>
+template <bool TA, bool TB, bool PAIR>
 cudaError_t launch(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p, cudaStream_t stream) {
-  tc::tf32x3_gemm_kernel<TA, TB><<<(unsigned)p.sk_grid, tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB, p);
+  tc::tf32x3_gemm_kernel<TA, TB, PAIR><<<(unsigned)p.sk_grid, tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB, p);
   return cudaGetLastError();
+}
+
+template <bool PAIR>
+cudaError_t launch_ops(bool transA, bool transB, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                       const GemmParams& p, cudaStream_t stream) {
+  if (!transA && !transB) return launch<false, false, PAIR>(mapA, mapB, p, stream);
+  if (!transA && transB) return launch<false, true, PAIR>(mapA, mapB, p, stream);
+  if (transA && !transB) return launch<true, false, PAIR>(mapA, mapB, p, stream);
+  return launch<true, true, PAIR>(mapA, mapB, p, stream);
 }
 
 }  // namespace
 
 cudaError_t prepare_tf32x3() {
-  cudaError_t e = set_attrs<false, false>();
-  if (e == cudaSuccess) e = set_attrs<false, true>();
-  if (e == cudaSuccess) e = set_attrs<true, false>();
-  if (e == cudaSuccess) e = set_attrs<true, true>();
+  cudaError_t e = set_attrs<false, false, false>();
+  if (e == cudaSuccess) e = set_attrs<false, true, false>();
+  if (e == cudaSuccess) e = set_attrs<true, false, false>();
+  if (e == cudaSuccess) e = set_attrs<true, true, false>();
+  if (e == cudaSuccess) e = set_attrs<false, false, true>();
+  if (e == cudaSuccess) e = set_attrs<false, true, true>();
+  if (e == cudaSuccess) e = set_attrs<true, false, true>();
+  if (e == cudaSuccess) e = set_attrs<true, true, true>();
   return e;
 }
 
-cudaError_t launch_tf32x3(bool transA, bool transB, const CUtensorMap& mapA, const CUtensorMap& mapB,
+cudaError_t launch_tf32x3(bool transA, bool transB, bool paired, const CUtensorMap& mapA, const CUtensorMap& mapB,
                           const GemmParams& p, cudaStream_t stream) {
-  if (!transA && !transB) return launch<false, false>(mapA, mapB, p, stream);
-  if (!transA && transB) return launch<false, true>(mapA, mapB, p, stream);
-  if (transA && !transB) return launch<true, false>(mapA, mapB, p, stream);
-  return launch<true, true>(mapA, mapB, p, stream);
+  return paired ? launch_ops<true>(transA, transB, mapA, mapB, p, stream)
+                : launch_ops<false>(transA, transB, mapA, mapB, p, stream);
 }
 
 cudaError_t launch_streamk_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream) {

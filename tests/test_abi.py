@@ -213,52 +213,76 @@ def test_batched_planner(lib):
 
 
 def test_small_product_planner(lib):
-    # 8192 products of 64x64x64: a persistent grid of 64-thread CTAs, four per SM, no workspace
-    p = bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64)
-    assert p["variant_name"] == "SMALL" and (p["grid_x"], p["grid_y"], p["threads"]) == (4 * 152, 1, 64)
-    assert (p["kernel_launches"], p["split_k"], p["workspace_bytes"]) == (1, 1, 0)
-    assert p["smem_bytes"] == 2 * 2 * 64 * 32 * 4 and p["stages"] == 2 and p["tile_k"] == 32
-    # the persistent grid never exceeds the batch
-    assert bplan("N", "N", 64, 64, 64, 200, 64 * 64, 64 * 64, 64 * 64, sm=100)["grid_x"] == 200
-    assert bplan("N", "N", 64, 64, 64, 200, 64 * 64, 64 * 64, 64 * 64, sm=1)["grid_x"] == 4
-    # every op combination, ragged M and N below the tile, shared operands
-    for ta in "NT":
-        for tb in "NT":
-            M, N, K = 36, 20, 100
-            q = bplan(ta, tb, M, N, K, 304, M * K, K * N, M * N)
-            assert q["variant_name"] == "SMALL", (ta, tb)
-    assert bplan("N", "N", 64, 64, 64, 500, 64 * 64, 0, 64 * 64)["variant_name"] == "SMALL"
-    # fewer than two products per SM, K above 128, outputs above 64: the tensor-core kernel
-    assert bplan("N", "N", 64, 64, 64, 303, 64 * 64, 64 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
-    assert bplan("N", "N", 64, 64, 128, 304, 64 * 128, 128 * 64, 64 * 64)["variant_name"] == "SMALL"
-    assert bplan("N", "N", 64, 64, 132, 8192, 64 * 132, 132 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
-    assert bplan("N", "N", 64, 64, 64, 303, 64 * 64, 64 * 64, 64 * 64, sm=100)["variant_name"] == "SMALL"
-    assert bplan("N", "N", 65, 64, 64, 8192, 65 * 64, 64 * 64, 65 * 64)["variant_name"] == "TC_TF32X3"
-    assert bplan("N", "N", 64, 68, 64, 8192, 64 * 64, 64 * 68, 64 * 68)["variant_name"] == "TC_TF32X3"
-    # the float4 rules: the contiguous extent of each operand a multiple of 4
-    assert bplan("N", "N", 64, 64, 62, 8192, 64 * 64, 64 * 64, 64 * 64, lda=64)["variant_name"] != "SMALL"
-    assert bplan("N", "N", 64, 62, 64, 8192, 64 * 64, 64 * 64, 64 * 64, ldb=64)["variant_name"] != "SMALL"
-    assert bplan("T", "N", 62, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64, lda=64)["variant_name"] != "SMALL"
-    assert bplan("N", "T", 64, 64, 62, 8192, 64 * 64, 64 * 64, 64 * 64, lda=64, ldb=64)["variant_name"] != "SMALL"
-    assert bplan("T", "T", 64, 62, 64, 8192, 64 * 64, 64 * 64, 64 * 64, ldb=64)["variant_name"] == "SMALL"
-    # alignment: A or B base, leading dimensions, strides
-    assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64, A=FAKE_ODD)["variant_name"] == "GENERIC"
-    assert bplan("N", "N", 64, 64, 64, 8192, 64 * 66, 64 * 64, 64 * 64, lda=66)["variant_name"] == "GENERIC"
-    assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64 + 2, 64 * 64, 64 * 64)["variant_name"] == "GENERIC"
-    # C is written with scalar stores when it is not 16-byte aligned: no rule on C
-    assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64 + 1, C=FAKE_ODD)["variant_name"] == "SMALL"
-    # forced: SMALL where its rules hold (any batch), GENERIC where they do not; forced TC wins over the rule
+    """The FP32 FFMA small-product kernel is chosen by override only (batches of small products go to
+    the tensor cores, two to a tile); its own rules decide where it applies."""
+    def small(*a, **k):
+        return bplan(*a, **k)["variant_name"] == "SMALL"
+    assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64)["variant_name"] == "TC_PAIRED"
     try:
         sg.sgemm_set_variant_override("SMALL", 0)
-        assert bplan("N", "N", 64, 64, 2048, 2, 64 * 2048, 2048 * 64, 64 * 64)["variant_name"] == "SMALL"
+        # 8192 products of 64x64x64: a persistent grid of 64-thread CTAs, four per SM, no workspace
+        p = bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64)
+        assert p["variant_name"] == "SMALL" and (p["grid_x"], p["grid_y"], p["threads"]) == (4 * 152, 1, 64)
+        assert (p["kernel_launches"], p["split_k"], p["workspace_bytes"]) == (1, 1, 0)
+        assert p["smem_bytes"] == 2 * 2 * 64 * 32 * 4 and p["stages"] == 2 and p["tile_k"] == 32
+        # the persistent grid never exceeds the batch
+        assert bplan("N", "N", 64, 64, 64, 200, 64 * 64, 64 * 64, 64 * 64)["grid_x"] == 200
+        assert bplan("N", "N", 64, 64, 64, 200, 64 * 64, 64 * 64, 64 * 64, sm=1)["grid_x"] == 4
+        # every op combination, ragged M and N below the tile, shared operands, any batch and K
+        for ta in "NT":
+            for tb in "NT":
+                assert small(ta, tb, 36, 20, 100, 304, 36 * 100, 100 * 20, 36 * 20), (ta, tb)
+        assert small("N", "N", 64, 64, 64, 500, 64 * 64, 0, 64 * 64)
+        assert small("N", "N", 64, 64, 2048, 2, 64 * 2048, 2048 * 64, 64 * 64)
         assert plan("N", "N", 64, 64, 64)["variant_name"] == "SMALL"
-        assert plan("N", "N", 65, 64, 64)["variant_name"] == "GENERIC"
-        # a CTA's (product, K chunk) items must fit an int: 1150 products x 2^25 chunks do not
+        # outputs above 64, the float4 rules (contiguous extent of each operand a multiple of 4),
+        # alignment of A, B, lda and strides: the any-alignment kernel
+        assert bplan("N", "N", 65, 64, 64, 8192, 65 * 64, 64 * 64, 65 * 64)["variant_name"] == "GENERIC"
+        assert not small("N", "N", 64, 64, 62, 8192, 64 * 64, 64 * 64, 64 * 64, lda=64)
+        assert not small("N", "N", 64, 62, 64, 8192, 64 * 64, 64 * 64, 64 * 64, ldb=64)
+        assert not small("T", "N", 62, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64, lda=64)
+        assert not small("N", "T", 64, 64, 62, 8192, 64 * 64, 64 * 64, 64 * 64, lda=64, ldb=64)
+        assert small("T", "T", 64, 62, 64, 8192, 64 * 64, 64 * 64, 64 * 64, ldb=64)
+        assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64, A=FAKE_ODD)["variant_name"] == "GENERIC"
+        assert bplan("N", "N", 64, 64, 64, 8192, 64 * 66, 64 * 64, 64 * 64, lda=66)["variant_name"] == "GENERIC"
+        assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64 + 2, 64 * 64, 64 * 64)["variant_name"] == "GENERIC"
+        # C is written with scalar stores when it is not 16-byte aligned: no rule on C
+        assert small("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64 + 1, C=FAKE_ODD)
+        # a CTA's (product, K chunk) items must fit an int: 2300 products x 2^25 chunks do not
         huge_k = 32 << 25
         assert bplan("N", "N", 64, 64, huge_k, 1 << 20, 0, 0, 64 * 64, lda=huge_k)["variant_name"] == "GENERIC"
-        assert bplan("N", "N", 64, 64, huge_k, 4, 0, 0, 64 * 64, lda=huge_k)["variant_name"] == "SMALL"
-        sg.sgemm_set_variant_override("TC_TF32X3", 0)
-        assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
+        assert small("N", "N", 64, 64, huge_k, 4, 0, 0, 64 * 64, lda=huge_k)
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
+
+
+def test_paired_planner(lib):
+    # 2048 products of 64x64x1024: 1024 block-diagonal pairs on one persistent CTA per SM, no stream-K
+    p = bplan("N", "N", 64, 64, 1024, 2048, 64 * 1024, 1024 * 64, 64 * 64)
+    assert p["variant_name"] == "TC_PAIRED" and (p["grid_x"], p["threads"]) == (152, 608)
+    assert (p["dp_tiles"], p["sk_tiles"], p["split_k"], p["kernel_launches"], p["workspace_bytes"]) == (1024, 0, 1, 1, 0)
+    assert (p["tile_m"], p["tile_n"], p["tile_k"]) == (64, 64, 32)
+    # every op combination, ragged M and N, odd batch, shared operands
+    for ta in "NT":
+        for tb in "NT":
+            assert bplan(ta, tb, 36, 20, 300, 305, 36 * 300, 300 * 20, 36 * 20)["variant_name"] == "TC_PAIRED"
+            assert bplan(ta, tb, 36, 20, 64, 305, 36 * 64, 64 * 20, 36 * 20)["variant_name"] == "TC_PAIRED"
+    assert bplan("N", "T", 64, 64, 512, 400, 0, 64 * 512, 64 * 64)["variant_name"] == "TC_PAIRED"
+    # fewer products than SMs, M or N above 64, TMA rules broken
+    assert bplan("N", "N", 64, 64, 1024, 152, 64 * 1024, 1024 * 64, 64 * 64)["variant_name"] == "TC_PAIRED"
+    assert bplan("N", "N", 64, 64, 1024, 151, 64 * 1024, 1024 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
+    assert bplan("N", "N", 65, 64, 1024, 2048, 65 * 1024, 1024 * 64, 65 * 64)["variant_name"] == "TC_TF32X3"
+    assert bplan("N", "N", 64, 65, 1024, 2048, 64 * 1024, 1024 * 68, 64 * 65, ldb=68)["variant_name"] == "TC_TF32X3"
+    assert bplan("N", "N", 64, 64, 1024, 2048, 64 * 1024 + 2, 1024 * 64, 64 * 64)["variant_name"] == "GENERIC"
+    # fewer SMs: fewer CTAs, the same pairs
+    q = bplan("N", "N", 64, 64, 1024, 2048, 64 * 1024, 1024 * 64, 64 * 64, sm=100)
+    assert (q["variant_name"], q["grid_x"], q["dp_tiles"]) == ("TC_PAIRED", 100, 1024)
+    try:
+        sg.sgemm_set_variant_override("TC_PAIRED", 0)
+        one = plan("N", "N", 64, 64, 64)
+        assert (one["variant_name"], one["grid_x"], one["dp_tiles"]) == ("TC_PAIRED", 1, 1)
+        assert bplan("N", "N", 64, 64, 64, 3, 64 * 64, 64 * 64, 64 * 64)["dp_tiles"] == 2
+        assert plan("N", "N", 65, 64, 64)["variant_name"] == "GENERIC"
     finally:
         sg.sgemm_set_variant_override("AUTO", 0)
 

@@ -73,9 +73,9 @@ def test_graph_replays_back_to_back_accumulate():
     check_exact(dC.cpu().numpy(), (5 * one.astype(np.float64)).astype(np.float32), "5 replays")
 
 
-@pytest.mark.parametrize("batch,M,N,K,expect", [(1024, 64, 64, 64, "SMALL"), (16, 256, 384, 512, "TC_TF32X3")])
+@pytest.mark.parametrize("batch,M,N,K,expect", [(1024, 64, 64, 64, "TC_PAIRED"), (16, 256, 384, 512, "TC_TF32X3")])
 def test_strided_batch_graph_replay(batch, M, N, K, expect):
-    """Strided batches on the small-product kernel and on the tensor-core kernel, captured and replayed."""
+    """Strided batches of small products (two to a tensor-core tile) and of large ones, captured and replayed."""
     torch = torch_cuda()
     d = si.make_batched(batch, M, N, K, "N", "T", seed=63, pad=0, gap=0, align=4)
     plan = sg.sgemm_plan_strided_batched("N", "T", M, N, K, 1.0, 1 << 20, d["lda"], 1 << 20, d["ldb"], 0.0,

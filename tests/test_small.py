@@ -1,5 +1,6 @@
-"""GPU parity of the small-product kernel (M, N <= 64 in a large strided batch:
-one CTA per product, FP32 FFMA) against the oracle, through the C ABI.
+"""GPU parity of the small-product kernel (M, N <= 64 in a strided batch: a
+persistent SIMT kernel with a 64x64 tile per product, IEEE FP32 FFMA; chosen
+by override) against the oracle, through the C ABI.
 
 Values meet the per-element bound (K+2) u S; small dyadic inputs, whose every
 partial sum is exact in float32, must match bit for bit.  Padding and gaps hold
@@ -15,6 +16,14 @@ from gpu_util import check_bound, check_exact, gpu_sgemm, to_dev, torch_cuda
 from test_batched import OPS, check_batched, gpu_batched, oracle_batched, plan_of, product_view
 
 pytestmark = pytest.mark.gpu
+
+
+def small_plan(ta, tb, M, N, K, d, batch):
+    sg.sgemm_set_variant_override("SMALL", 0)
+    try:
+        return plan_of(ta, tb, M, N, K, d, batch)["variant_name"]
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
 
 
 def _dyadic_stack(d, rng, bits=6):
@@ -33,8 +42,8 @@ def test_small_parity(ops, shared):
     ta, tb = ops
     batch, M, N, K = 320, 36, 20, 100
     d = si.make_batched(batch, M, N, K, ta, tb, seed=51, pad=4, gap=4, align=4, shared=shared)
-    assert plan_of(ta, tb, M, N, K, d, batch)["variant_name"] == "SMALL"
-    got = gpu_batched(ta, tb, M, N, K, 1.5, -0.5, d, batch)
+    assert small_plan(ta, tb, M, N, K, d, batch) == "SMALL"
+    got = gpu_batched(ta, tb, M, N, K, 1.5, -0.5, d, batch, variant="SMALL")
     ref, S = oracle_batched(ta, tb, M, N, K, 1.5, -0.5, d, batch)
     check_batched(got, ref, S, d, batch, M, N, K, f"small {ops} shared={shared!r}")
 
@@ -45,9 +54,13 @@ def test_small_persistent_rounds(ops):
     ta, tb = ops
     batch, M, N, K = 1111, 52, 44, 124
     d = si.make_batched(batch, M, N, K, ta, tb, seed=58, pad=4, gap=4, align=4)
-    p = plan_of(ta, tb, M, N, K, d, batch)
+    sg.sgemm_set_variant_override("SMALL", 0)
+    try:
+        p = plan_of(ta, tb, M, N, K, d, batch)
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
     assert p["variant_name"] == "SMALL" and p["grid_x"] < batch
-    got = gpu_batched(ta, tb, M, N, K, 0.5, 1.5, d, batch)
+    got = gpu_batched(ta, tb, M, N, K, 0.5, 1.5, d, batch, variant="SMALL")
     ref, S = oracle_batched(ta, tb, M, N, K, 0.5, 1.5, d, batch)
     check_batched(got, ref, S, d, batch, M, N, K, f"persistent {ops}")
 
@@ -73,17 +86,13 @@ EDGE = [(1, 4, 4), (4, 4, 4), (64, 64, 4), (64, 64, 64), (64, 64, 68), (4, 64, 1
 @pytest.mark.parametrize("M,N,K", EDGE, ids=[f"{m}x{n}x{k}" for m, n, k in EDGE])
 @pytest.mark.parametrize("ops", ["NN", "TT"])
 def test_small_edges_forced(M, N, K, ops):
-    """Edge shapes on a short batch, with the kernel forced (the default needs >= one product per SM)."""
+    """Edge shapes on a short batch."""
     ta, tb = ops
     if ta == "T" and M % 4:
         M = 4 * ((M + 3) // 4)
     batch = 3
     d = si.make_batched(batch, M, N, K, ta, tb, seed=53 + M + N + K, pad=4, gap=4, align=4)
-    sg.sgemm_set_variant_override("SMALL", 0)
-    try:
-        assert plan_of(ta, tb, M, N, K, d, batch)["variant_name"] == "SMALL"
-    finally:
-        sg.sgemm_set_variant_override("AUTO", 0)
+    assert small_plan(ta, tb, M, N, K, d, batch) == "SMALL"
     got = gpu_batched(ta, tb, M, N, K, -1.0, 2.0, d, batch, variant="SMALL")
     ref, S = oracle_batched(ta, tb, M, N, K, -1.0, 2.0, d, batch)
     check_batched(got, ref, S, d, batch, M, N, K, f"edge {ops} {M}x{N}x{K}")
@@ -93,9 +102,9 @@ def test_small_beta_zero_does_not_read_c():
     """beta = 0: C may hold NaN on entry and the result is alpha op(A) op(B) all the same."""
     batch, M, N, K = 400, 64, 48, 64
     d = si.make_batched(batch, M, N, K, "N", "T", seed=54, pad=0, gap=0, align=4)
-    assert plan_of("N", "T", M, N, K, d, batch)["variant_name"] == "SMALL"
+    assert small_plan("N", "T", M, N, K, d, batch) == "SMALL"
     d["C"] = np.full_like(d["C"], np.nan)
-    got = gpu_batched("N", "T", M, N, K, 0.75, 0.0, d, batch)
+    got = gpu_batched("N", "T", M, N, K, 0.75, 0.0, d, batch, variant="SMALL")
     zero = dict(d, C=np.zeros_like(d["C"]))
     ref, S = oracle_batched("N", "T", M, N, K, 0.75, 0.0, zero, batch)
     check_batched(got, ref, S, d, batch, M, N, K, "beta=0 over NaN C")
@@ -113,11 +122,15 @@ def test_small_scalar_c_path_with_guard_bands(ops):
     buf = np.concatenate([np.full(1, np.nan, np.float32), C, np.full(ldc, np.nan, np.float32)])
     dbuf = to_dev(buf)
     c_ptr = dbuf.data_ptr() + 4
-    plan = sg.sgemm_plan_strided_batched(ta, tb, M, N, K, 1.0, 1 << 20, d["lda"], 1 << 20, d["ldb"], 0.5, c_ptr,
-                                         ldc, d["strideA"], d["strideB"], strideC, batch)
-    assert plan["variant_name"] == "SMALL"
-    sg.sgemm_strided_batched(ta, tb, M, N, K, 1.0, to_dev(d["A"]), d["lda"], to_dev(d["B"]), d["ldb"], 0.5, c_ptr,
-                             ldc, d["strideA"], d["strideB"], strideC, batch)
+    sg.sgemm_set_variant_override("SMALL", 0)
+    try:
+        plan = sg.sgemm_plan_strided_batched(ta, tb, M, N, K, 1.0, 1 << 20, d["lda"], 1 << 20, d["ldb"], 0.5, c_ptr,
+                                             ldc, d["strideA"], d["strideB"], strideC, batch)
+        assert plan["variant_name"] == "SMALL"
+        sg.sgemm_strided_batched(ta, tb, M, N, K, 1.0, to_dev(d["A"]), d["lda"], to_dev(d["B"]), d["ldb"], 0.5,
+                                 c_ptr, ldc, d["strideA"], d["strideB"], strideC, batch)
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
     assert sg.sgemm_sync_status() == 0
     torch.cuda.synchronize()
     out = dbuf.cpu().numpy()
@@ -132,7 +145,7 @@ def test_small_non_finite_follow_ieee():
     """Inf and NaN inputs give the non-finite pattern of IEEE arithmetic (the FFMA path keeps Inf)."""
     batch, M, N, K = 320, 16, 16, 128
     d = si.make_batched(batch, M, N, K, "N", "N", seed=56, pad=0, gap=0, align=4)
-    assert plan_of("N", "N", M, N, K, d, batch)["variant_name"] == "SMALL"
+    assert small_plan("N", "N", M, N, K, d, batch) == "SMALL"
     A, B = d["stacks"]["A"].copy(), d["stacks"]["B"].copy()
     A[0, 3, 70] = np.inf          # row 3 of product 0: +-Inf where B[70, n] != 0
     A[1, 5, 10] = np.nan          # row 5 of product 1: NaN
@@ -143,7 +156,7 @@ def test_small_non_finite_follow_ieee():
     for name, X in (("A", A), ("B", B)):
         d["stacks"][name] = X
         d[name] = si.embed_batched(X, d["ld" + name.lower()], d["stride" + name])
-    got = gpu_batched("N", "N", M, N, K, 1.0, 0.0, d, batch)
+    got = gpu_batched("N", "N", M, N, K, 1.0, 0.0, d, batch, variant="SMALL")
     ref = oracle.sgemm_strided_batched("N", "N", M, N, K, 1.0, d["A"], d["lda"], d["strideA"], d["B"], d["ldb"],
                                        d["strideB"], 0.0, d["C"], d["ldc"], d["strideC"], batch)
     assert np.array_equal(np.isnan(got), np.isnan(ref))
@@ -157,8 +170,8 @@ def test_small_full_workload_every_product():
     c = si.batched_case("batched_small_8192x64x64x64")
     d = si.make_batched(c.batch, c.M, c.N, c.K, c.transA, c.transB, seed=c.seed, dist=c.dist, shared=c.shared,
                         c_init="uniform" if c.beta != 0 else "zero")
-    assert plan_of(c.transA, c.transB, c.M, c.N, c.K, d, c.batch)["variant_name"] == "SMALL"
-    got = gpu_batched(c.transA, c.transB, c.M, c.N, c.K, c.alpha, c.beta, d, c.batch)
+    assert small_plan(c.transA, c.transB, c.M, c.N, c.K, d, c.batch) == "SMALL"
+    got = gpu_batched(c.transA, c.transB, c.M, c.N, c.K, c.alpha, c.beta, d, c.batch, variant="SMALL")
     ref, S = oracle_batched(c.transA, c.transB, c.M, c.N, c.K, c.alpha, c.beta, d, c.batch)
     check_batched(got, ref, S, d, c.batch, c.M, c.N, c.K, c.name)
 
