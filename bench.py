@@ -45,9 +45,9 @@ PROFILES = {("TC_TF32X3", "square4096"): os.path.join(ROOT, "profiles", "tf32x3_
             ("TMA_128x128", "square4096"): os.path.join(ROOT, "profiles", "tma_gemm_square4096.md"),
             ("SMALL", "batched_small_8192x64x64x64"):
                 os.path.join(ROOT, "profiles", "small_gemm_batched8192x64x64x64.md"),
-            ("TC_PAIRED", "batched_small_k1024_2048x64x64x1024"):
+            ("TC_GROUPED", "batched_small_k1024_2048x64x64x1024"):
                 os.path.join(ROOT, "profiles", "tf32x3_paired_batched2048x64x64x1024.md"),
-            ("TC_PAIRED", "batched_small_8192x64x64x64"):
+            ("TC_GROUPED", "batched_small_8192x64x64x64"):
                 os.path.join(ROOT, "profiles", "tf32x3_paired_batched8192x64x64x64.md")}
 # dense tensor-core peaks (PFLOP/s, nominal) used to scale the measured bf16 peak to tf32
 NOMINAL_BF16_PF, NOMINAL_TF32_PF = 2.25, 1.1
@@ -592,13 +592,14 @@ def batched_roofline(c, plan, flops_step, achieved, kernel_ms, peaks, dev, lib_b
     """Roofline object of the kernel a strided batch ran on.  For the tensor-core kernel the bound is
     whichever of the 3xTF32 tensor peak and HBM takes longer for the call's algorithmic work."""
     variant = plan["variant_name"]
-    if variant in ("TC_TF32X3", "TC_PAIRED"):
+    if variant in ("TC_TF32X3", "TC_GROUPED"):
         traffic = traffic_from_profile(variant, c.name, lib_build.tc_kernel_digest())
         roof = tensor_roofline(achieved, peaks, traffic, kernel_ms)
-        if variant == "TC_PAIRED":
-            pairs = (c.batch + 1) // 2
-            roof["kernel"] = "tf32x3_gemm_kernel, two products per 128x128 tile (block-diagonal)"
-            roof["useful_fraction_of_tensor_work"] = c.batch * c.M * c.N / (pairs * 128 * 128)
+        if variant == "TC_GROUPED":
+            group = 128 // plan["tile_m"]
+            tiles = (c.batch + group - 1) // group
+            roof["kernel"] = f"tf32x3_gemm_kernel, {group} products per 128x128 tile (block-diagonal)"
+            roof["useful_fraction_of_tensor_work"] = c.batch * c.M * c.N / (tiles * 128 * 128)
         nbytes = batched_bytes(c)
         hbm = peaks.get("hbm_gbs")
         hbm_basis = "measured" if hbm else "fallback"
@@ -700,8 +701,8 @@ def run_ours_batched(args, c):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "step_ms": step_stats(step_ms),
         "config": {**batched_config_block(c, d, world), "l2": l2_note(flush), "prewarm_s": args.prewarm_s,
-                   "plan": {k: plan[k] for k in ("variant_name", "split_k", "grid_x", "grid_y", "dp_tiles",
-                                                 "sk_tiles")}},
+                   "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "split_k", "grid_x", "grid_y",
+                                                 "dp_tiles", "sk_tiles")}},
         "roofline": batched_roofline(c, plan, flops_step, achieved, kernel_ms, peaks, dev, lib_build),
         "e2e": {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
                 "note": "no host-buffer batched entry point; the device-resident value is the measurement"},

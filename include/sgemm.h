@@ -85,7 +85,8 @@ enum sgemm_variant {
     SGEMM_VARIANT_TMA_64x256 = 5, /* same kernel, 64x256 tiles for short M */
     SGEMM_VARIANT_TC_TF32X3 = 6,  /* tcgen05 tensor cores, 3xTF32 split, 128x128x32 tiles */
     SGEMM_VARIANT_SMALL = 7,      /* M, N <= 64 in a large batch: one CTA per product, FP32 FFMA */
-    SGEMM_VARIANT_TC_PAIRED = 8   /* M, N <= 64 in a batch: 3xTF32 tensor cores, two products per 128x128 tile */
+    SGEMM_VARIANT_TC_GROUPED = 8  /* M, N <= 64 in a batch: 3xTF32 tensor cores, 2 (M, N <= 32: 4) products
+                                     per 128x128 tile, block-diagonally; tile_m = tile_n = 128 / group */
 };
 
 /*

@@ -263,6 +263,8 @@ BATCHED_CASES: list[BatchedCase] = [
     BatchedCase("batched_small_8192x64x64x64", 8192, 64, 64, 64, seed=23, dist="uniform"),
     # small outputs, long K: two products to a tensor-core tile
     BatchedCase("batched_small_k1024_2048x64x64x1024", 2048, 64, 64, 1024, seed=24, dist="uniform"),
+    # tiny products: four to a tensor-core tile
+    BatchedCase("batched_tiny_16384x32x32x32", 16384, 32, 32, 32, seed=25, dist="uniform"),
 ]
 
 

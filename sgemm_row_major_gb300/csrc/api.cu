@@ -169,12 +169,13 @@ constexpr int64_t kMinStreamKIters = 32;
 // Small-product kernel (kernel_small.cu, FP32 FFMA, selected by override):
 // the output extents it covers.
 constexpr int64_t kSmallMaxMN = 64;
-// Block-diagonal pairs on the tensor cores: products with M, N <= 64, chosen
-// by default for a batch of at least one product per SM (measured on GB300,
-// TFLOPS, paired / one product per tile / small-product kernel: 8192 x 64^3
-// 51.0 / 24.8 / 40.9, 2048 x 64x64x1024 90.9 / 51.2 / 50.0; 76 pairs on 152
-// SMs, K = 1024: 41.1 / 40.6 / 22.1).
-constexpr int64_t kPairMaxMN = 64;
+// Block-diagonal groups on the tensor cores: products with M, N <= 64 two to a
+// tile, with M, N <= 32 four to a tile, chosen by default for a batch of at
+// least one product per SM (measured on GB300, TFLOPS, pairs / one product per
+// tile / small-product kernel: 8192 x 64^3 51.0 / 24.8 / 40.9, 2048 x
+// 64x64x1024 90.9 / 51.2 / 50.0; 76 pairs on 152 SMs, K = 1024: 41.1 / 40.6 /
+// 22.1).
+constexpr int64_t kGroupMaxMN = 64;
 constexpr int64_t kSmallKChunk = 32;
 constexpr int64_t kSmallCtasPerSm = 4;  // persistent grid: 4 x 32 KB of stages per SM
 
@@ -262,28 +263,29 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
                         (pr.ta ? pr.M : pr.K) % 4 == 0 && (pr.tb ? pr.K : pr.N) % 4 == 0 &&
                         ceil_div(pr.batch, small_grid) * ceil_div(pr.K, kSmallKChunk) < INT_MAX;
   // Default: the 3xTF32 tensor-core kernel whenever TMA can load the operands
-  // (it beats the FP32 FFMA kernels on every measured shape), two products to
-  // a tile (block-diagonal) for a batch of at least one product per SM with
-  // M, N <= 64; the generic SIMT kernel otherwise.  The FP32 FFMA kernels
+  // (it beats the FP32 FFMA kernels on every measured shape), several
+  // products to a tile (block-diagonal) for a batch of at least one product
+  // per SM with M, N <= 64; the generic SIMT kernel otherwise.  The FP32 FFMA kernels
   // (TMA-fed, small-product) stay selectable by override: IEEE FP32
   // operations, exact Inf handling.
-  const int64_t pairs = (pr.batch + 1) / 2;
-  const bool pair_ok = tma_ok && pr.M <= kPairMaxMN && pr.N <= kPairMaxMN;
+  const int64_t group = pr.M <= kGroupMaxMN / 2 && pr.N <= kGroupMaxMN / 2 ? 4 : 2;
+  const bool group_ok = tma_ok && pr.M <= kGroupMaxMN && pr.N <= kGroupMaxMN;
   int variant = tma_ok ? SGEMM_VARIANT_TC_TF32X3 : SGEMM_VARIANT_GENERIC;
-  if (pair_ok && pr.batch >= sm_count) variant = SGEMM_VARIANT_TC_PAIRED;
+  if (group_ok && pr.batch >= sm_count) variant = SGEMM_VARIANT_TC_GROUPED;
   const int ov = g_override_variant.load();
   if (ov == SGEMM_VARIANT_GENERIC || ov == SGEMM_VARIANT_TMA_128x128 || ov == SGEMM_VARIANT_TMA_64x256 ||
       ov == SGEMM_VARIANT_TC_TF32X3)
     variant = (ov == SGEMM_VARIANT_GENERIC || tma_ok) ? ov : SGEMM_VARIANT_GENERIC;
   if (ov == SGEMM_VARIANT_SMALL) variant = small_ok ? ov : SGEMM_VARIANT_GENERIC;
-  if (ov == SGEMM_VARIANT_TC_PAIRED) variant = pair_ok ? ov : SGEMM_VARIANT_GENERIC;
-  if (variant == SGEMM_VARIANT_TC_PAIRED) {
-    // whole tiles (a pair each) on one persistent CTA per SM, no stream-K
+  if (ov == SGEMM_VARIANT_TC_GROUPED) variant = group_ok ? ov : SGEMM_VARIANT_GENERIC;
+  if (variant == SGEMM_VARIANT_TC_GROUPED) {
+    // whole tiles (a group of products each) on one persistent CTA per SM, no stream-K
+    const int64_t tiles = ceil_div(pr.batch, group);
     const int64_t kt = ceil_div(pr.K, 32);
-    const int64_t grid = std::min<int64_t>(pairs, std::max(1, sm_count));
-    if ((pairs / grid + 1) * kt > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
+    const int64_t grid = std::min<int64_t>(tiles, std::max(1, sm_count));
+    if ((tiles / grid + 1) * kt > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
     plan->variant = variant;
-    plan->tile_m = plan->tile_n = (int)kPairMaxMN;
+    plan->tile_m = plan->tile_n = (int)(128 / group);
     plan->tile_k = 32;
     plan->stages = 4;
     plan->threads = 608;
@@ -291,7 +293,7 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
     plan->kernel_launches = 1;
     plan->grid_x = grid;
     plan->grid_y = 1;
-    plan->dp_tiles = pairs;
+    plan->dp_tiles = tiles;
     return SGEMM_OK;
   }
   if (variant == SGEMM_VARIANT_SMALL) {
@@ -410,8 +412,9 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
     e = launch_generic_gemm(pr.ta, pr.tb, p, split, stream);
   } else if (plan.variant == SGEMM_VARIANT_SMALL) {
     e = launch_small_gemm(pr.ta, pr.tb, p, (int)plan.grid_x, stream);
-  } else if (plan.variant == SGEMM_VARIANT_TC_TF32X3 || plan.variant == SGEMM_VARIANT_TC_PAIRED) {
-    e = launch_tf32x3(pr.ta, pr.tb, plan.variant == SGEMM_VARIANT_TC_PAIRED, mapA, mapB, p, stream);
+  } else if (plan.variant == SGEMM_VARIANT_TC_TF32X3 || plan.variant == SGEMM_VARIANT_TC_GROUPED) {
+    e = launch_tf32x3(pr.ta, pr.tb, plan.variant == SGEMM_VARIANT_TC_GROUPED ? 128 / plan.tile_m : 1, mapA, mapB,
+                      p, stream);
     if (e == cudaSuccess && plan.kernel_launches > 1) e = launch_streamk_fixup(p, (int)plan.sk_tiles, stream);
   } else {
     const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
@@ -421,7 +424,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
     else e = launch_tma_op_tt(tile, mapA, mapB, p, split, stream);
   }
   if (e == cudaSuccess && split > 1 && plan.variant != SGEMM_VARIANT_TC_TF32X3 &&
-      plan.variant != SGEMM_VARIANT_TC_PAIRED)
+      plan.variant != SGEMM_VARIANT_TC_GROUPED)
     e = launch_splitk_reduce(p, split, stream);
   if (ws) {
     cudaError_t ef = cudaFreeAsync(ws, stream);
@@ -510,7 +513,7 @@ int sgemm_plan_strided_batched(char transA, char transB, int64_t M, int64_t N, i
 int sgemm_set_variant_override(int variant, int split_k) {
   if (variant != SGEMM_VARIANT_AUTO && variant != SGEMM_VARIANT_GENERIC && variant != SGEMM_VARIANT_TMA_128x128 &&
       variant != SGEMM_VARIANT_TMA_64x256 && variant != SGEMM_VARIANT_TC_TF32X3 && variant != SGEMM_VARIANT_SMALL &&
-      variant != SGEMM_VARIANT_TC_PAIRED)
+      variant != SGEMM_VARIANT_TC_GROUPED)
     return -1;
   g_override_variant.store(variant);
   g_override_split.store(split_k < 0 ? 0 : split_k);

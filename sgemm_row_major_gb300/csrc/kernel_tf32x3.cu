@@ -251,15 +251,17 @@ __device__ __forceinline__ Segment cta_segment(const GemmParams& p, const CtaWor
 //   op(A) 'N': [128 rows of M][32 k], K contiguous, 128-byte swizzle;  'T': [32 k][128 m], M contiguous.
 //   op(B) 'N': [32 k][128 n], N contiguous;  'T': [128 n][32 k], K contiguous, 128-byte swizzle.
 //
-// PAIR: products with M <= 64 and N <= 64 go two to a tile, block-diagonally:
-// rows 0-63 and columns 0-63 hold product 2t, rows 64-127 and columns 64-127
-// product 2t+1 (tile t; a missing partner of an odd batch reads zeros), so the
-// accumulator's diagonal 64x64 blocks are the two products and half of the
-// tensor-core work is useful instead of a quarter.  Each operand tile is then
-// two 64-wide TMA boxes: K-contiguous ones stack into the same layout, while
-// an M/N-contiguous one becomes two [32 k][64] halves.  Only the folder warps
-// on the diagonal blocks fold and write C; there is no stream-K in this mode.
-template <bool TA, bool TB, bool PAIR>
+// G > 1 (block-diagonal groups): products with M, N <= 128/G go G to a tile:
+// rows and columns [g*128/G, (g+1)*128/G) of tile t hold product G*t + g (a
+// missing product at the end of the batch reads zeros), so the accumulator's
+// diagonal blocks are the G products and 1/G of the tensor-core work is
+// useful, instead of 1/G^2 with one product per tile (pairs of 64x64: a half
+// instead of a quarter; quads of 32x32: a quarter instead of a sixteenth).  Each operand tile is then G TMA boxes of 128/G rows or
+// columns: K-contiguous ones stack into the same layout, while an
+// M/N-contiguous one becomes G [32 k][128/G] blocks.  Only the folder warps
+// over a diagonal block fold and write C (a warp's 32 rows lie in one block);
+// there is no stream-K in this mode.
+template <bool TA, bool TB, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                        const GemmParams p) {
@@ -325,14 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int sgi = 0; ok && sgi < work.nseg; ++sgi) {
         const Segment g = cta_segment(p, work, cta, sgi, kt_total);
         int prod, m0, n0;
-        if (PAIR) {
-          prod = 2 * g.tile;
+        if (G > 1) {
+          prod = G * g.tile;
           m0 = n0 = 0;
         } else {
           tile_origin(p, g.tile, prod, m0, n0);
         }
         const int za = prod * p.za, zb = prod * p.zb;
-        const int za1 = (prod + 1) * p.za, zb1 = (prod + 1) * p.zb;  // PAIR: the second product
         for (int kt = g.kb; kt < g.ke; ++kt) {
           const int t = issued;
           const int r = t % kRawStages;
@@ -345,12 +346,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = smem_addr(&raw_full[r]);
           mbar_arrive_expect_tx(fb, (uint32_t)kRawBytes);
           const int k0 = kt * BK;
-          if (PAIR) {
-            // two 64-wide boxes per operand (8 KB each), second product at +8 KB
-            if (!TA) { tma_load_3d(raw_a(r), &mapA, fb, k0, 0, za); tma_load_3d(raw_a(r) + 8192u, &mapA, fb, k0, 0, za1); }
-            else     { tma_load_3d(raw_a(r), &mapA, fb, 0, k0, za); tma_load_3d(raw_a(r) + 8192u, &mapA, fb, 0, k0, za1); }
-            if (!TB) { tma_load_3d(raw_b(r), &mapB, fb, 0, k0, zb); tma_load_3d(raw_b(r) + 8192u, &mapB, fb, 0, k0, zb1); }
-            else     { tma_load_3d(raw_b(r), &mapB, fb, k0, 0, zb); tma_load_3d(raw_b(r) + 8192u, &mapB, fb, k0, 0, zb1); }
+          if (G > 1) {
+            // G boxes of 128/G rows or columns per operand (16 KB / G each), product G*t + i at i * 16 KB / G
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+              const uint32_t off = (uint32_t)(i * (kTileBytes / G));
+              const int zai = (prod + i) * p.za, zbi = (prod + i) * p.zb;
+              if (!TA) tma_load_3d(raw_a(r) + off, &mapA, fb, k0, 0, zai);
+              else     tma_load_3d(raw_a(r) + off, &mapA, fb, 0, k0, zai);
+              if (!TB) tma_load_3d(raw_b(r) + off, &mapB, fb, 0, k0, zbi);
+              else     tma_load_3d(raw_b(r) + off, &mapB, fb, k0, 0, zbi);
+            }
           } else {
             if (!TA) tma_load_3d(raw_a(r), &mapA, fb, k0, m0, za);
             else     tma_load_3d(raw_a(r), &mapA, fb, m0, k0, za);
@@ -446,11 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo[4 * j + 0] = l.x; lo[4 * j + 1] = l.y; lo[4 * j + 2] = l.z; lo[4 * j + 3] = l.w;
           }
         } else {
-          // M-contiguous [32 k][128 m] (PAIR: two [32 k][64 m] halves): one float per k (a warp
-          // reads 32 adjacent m)
-          const float* fa = reinterpret_cast<const float*>(ra) + (PAIR ? (m >> 6) * (BK * 64) : 0);
-          const int mm = PAIR ? (m & 63) : m;
-          constexpr int lda_s = PAIR ? 64 : BM;
+          // M-contiguous [32 k][128 m] (G > 1: G blocks [32 k][128/G m]): one float per k (a warp
+          // reads 32 adjacent m, all in one block)
+          constexpr int lda_s = BM / G;
+          const float* fa = reinterpret_cast<const float*>(ra) + (G > 1 ? (m / lda_s) * (BK * lda_s) : 0);
+          const int mm = G > 1 ? m % lda_s : m;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float x = fa[(16 * half + j) * lda_s + mm];
@@ -468,12 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* bhi = smem + (split_tile(s, 0) - sbase);
         uint8_t* blo = smem + (split_tile(s, 1) - sbase);
         if (!TB) {
-          // raw [32 k][128 n] (PAIR: two [32 k][64 n] halves): transpose; thread st owns column
+          // raw [32 k][128 n] (G > 1: G blocks [32 k][128/G n]): transpose; thread st owns column
           // n = st % 128, k chunks 4*(st/128) .. +3
+          constexpr int ldb_s = BN / G;
           const int n = st & 127, kh = st >> 7;
-          const float* rb = reinterpret_cast<const float*>(smem + (raw_b(r) - sbase)) + (PAIR ? (n >> 6) * (BK * 64) : 0);
-          const int nn = PAIR ? (n & 63) : n;
-          constexpr int ldb_s = PAIR ? 64 : BN;
+          const float* rb =
+              reinterpret_cast<const float*>(smem + (raw_b(r) - sbase)) + (G > 1 ? (n / ldb_s) * (BK * ldb_s) : 0);
+          const int nn = G > 1 ? n % ldb_s : n;
 #pragma unroll
           for (int kq = 0; kq < 4; ++kq) {
             const int kc = 4 * kh + kq;
@@ -514,12 +521,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ folders, then epilogue
     const int q = warp & 3;                          // TMEM lane quarter this warp may access
     const int half = (warp - kFirstFoldWarp) >> 2;   // which 64 accumulator columns
-    const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * half);
-    // PAIR: only the diagonal blocks are products; the other warps keep to the barrier protocol
-    const bool useful = !PAIR || (q >> 1) == half;
-    float2 master2[32];  // columns 2e, 2e+1 of this thread's 64
+    // G > 1: the diagonal block of this warp's rows, whether its columns lie in this warp's 64, and
+    // where; the other warps keep to the barrier protocol only
+    constexpr int kBlock = BM / G;
+    constexpr int kCols = kBlock < 64 ? kBlock : 64;  // accumulator columns a warp folds
+    const int blk = G > 1 ? (32 * q) / kBlock : 0;
+    const bool useful = G == 1 || (kBlock * blk) / 64 == half;
+    const int c_off = G > 1 ? kBlock * blk - 64 * half : 0;
+    const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * half + c_off);
+    float2 master2[kCols / 2];  // columns 2e, 2e+1 of the thread's kCols
 #pragma unroll
-    for (int e = 0; e < 32; ++e) master2[e] = make_float2(0.0f, 0.0f);
+    for (int e = 0; e < kCols / 2; ++e) master2[e] = make_float2(0.0f, 0.0f);
     bool ok = true;
     int u = 0;  // accumulator sequence number (one per K tile; kFoldTiles == 1)
     for (int sgi = 0; ok && sgi < work_s.nseg; ++sgi) {
@@ -537,12 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (useful) {
           tmem_fence_after_sync();
-          float v[4][16];
+          float v[kCols / 16][16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld16(tq + (uint32_t)b * kAccCols + 16u * c, v[c]);
+          for (int c = 0; c < kCols / 16; ++c) tmem_ld16(tq + (uint32_t)b * kAccCols + 16u * c, v[c]);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < kCols / 16; ++c) {
             tmem_ld_ready(v[c]);
 #pragma unroll
             for (int e = 0; e < 8; ++e)  // round-to-nearest FP32 adds, two per instruction
@@ -564,20 +576,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float4*>(w + 4 * e) =
               make_float4(master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y);
       } else if (useful) {
-        int prod, m0, n0;
-        if (PAIR) {
-          prod = 2 * g.tile + half;  // rows and columns 64*half .. +63 of the tile
-          m0 = -64 * half;
-          n0 = -64 * half;
+        int prod, m0, c0;  // product, origin row of the tile in it, first column of this thread's
+        if (G > 1) {
+          prod = G * g.tile + blk;  // rows and columns kBlock*blk .. +kBlock-1 of the tile
+          m0 = -kBlock * blk;
+          c0 = 0;
         } else {
+          int n0;
           tile_origin(p, g.tile, prod, m0, n0);
+          c0 = n0 + 64 * half;
         }
         const int row = m0 + 32 * q + lane;
-        if (row < p.M && (!PAIR || prod < p.batch)) {
+        if (row < p.M && (G == 1 || prod < p.batch)) {
           float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int col = n0 + 64 * half + 4 * e;
+          for (int e = 0; e < kCols / 4; ++e) {
+            const int col = c0 + 4 * e;
             const float x[4] = {master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y};
             if (p.c_vec && col + 3 < p.N) {
               float4 o;
@@ -599,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 #pragma unroll
-      for (int e = 0; e < 32; ++e) master2[e] = make_float2(0.0f, 0.0f);
+      for (int e = 0; e < kCols / 2; ++e) master2[e] = make_float2(0.0f, 0.0f);
     }
   }
 
@@ -674,45 +688,53 @@ __global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(const Gemm
 
 namespace {
 
-template <bool TA, bool TB, bool PAIR>
+template <bool TA, bool TB, int G>
 cudaError_t set_attrs() {
-  return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<TA, TB, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<TA, TB, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               tc::kSmemBytes);
 }
 
-template <bool TA, bool TB, bool PAIR>
+template <int G>
+cudaError_t set_attrs_ops() {
+  cudaError_t e = set_attrs<false, false, G>();
+  if (e == cudaSuccess) e = set_attrs<false, true, G>();
+  if (e == cudaSuccess) e = set_attrs<true, false, G>();
+  if (e == cudaSuccess) e = set_attrs<true, true, G>();
+  return e;
+}
+
+template <bool TA, bool TB, int G>
 cudaError_t launch(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p, cudaStream_t stream) {
-  tc::tf32x3_gemm_kernel<TA, TB, PAIR><<<(unsigned)p.sk_grid, tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB, p);
+  tc::tf32x3_gemm_kernel<TA, TB, G><<<(unsigned)p.sk_grid, tc::kThreads, tc::kSmemBytes, stream>>>(mapA, mapB, p);
   return cudaGetLastError();
 }
 
-template <bool PAIR>
+template <int G>
 cudaError_t launch_ops(bool transA, bool transB, const CUtensorMap& mapA, const CUtensorMap& mapB,
                        const GemmParams& p, cudaStream_t stream) {
-  if (!transA && !transB) return launch<false, false, PAIR>(mapA, mapB, p, stream);
-  if (!transA && transB) return launch<false, true, PAIR>(mapA, mapB, p, stream);
-  if (transA && !transB) return launch<true, false, PAIR>(mapA, mapB, p, stream);
-  return launch<true, true, PAIR>(mapA, mapB, p, stream);
+  if (!transA && !transB) return launch<false, false, G>(mapA, mapB, p, stream);
+  if (!transA && transB) return launch<false, true, G>(mapA, mapB, p, stream);
+  if (transA && !transB) return launch<true, false, G>(mapA, mapB, p, stream);
+  return launch<true, true, G>(mapA, mapB, p, stream);
 }
 
 }  // namespace
 
 cudaError_t prepare_tf32x3() {
-  cudaError_t e = set_attrs<false, false, false>();
-  if (e == cudaSuccess) e = set_attrs<false, true, false>();
-  if (e == cudaSuccess) e = set_attrs<true, false, false>();
-  if (e == cudaSuccess) e = set_attrs<true, true, false>();
-  if (e == cudaSuccess) e = set_attrs<false, false, true>();
-  if (e == cudaSuccess) e = set_attrs<false, true, true>();
-  if (e == cudaSuccess) e = set_attrs<true, false, true>();
-  if (e == cudaSuccess) e = set_attrs<true, true, true>();
+  cudaError_t e = set_attrs_ops<1>();
+  if (e == cudaSuccess) e = set_attrs_ops<2>();
+  if (e == cudaSuccess) e = set_attrs_ops<4>();
   return e;
 }
 
-cudaError_t launch_tf32x3(bool transA, bool transB, bool paired, const CUtensorMap& mapA, const CUtensorMap& mapB,
+cudaError_t launch_tf32x3(bool transA, bool transB, int group, const CUtensorMap& mapA, const CUtensorMap& mapB,
                           const GemmParams& p, cudaStream_t stream) {
-  return paired ? launch_ops<true>(transA, transB, mapA, mapB, p, stream)
-                : launch_ops<false>(transA, transB, mapA, mapB, p, stream);
+  switch (group) {
+    case 1: return launch_ops<1>(transA, transB, mapA, mapB, p, stream);
+    case 2: return launch_ops<2>(transA, transB, mapA, mapB, p, stream);
+    case 4: return launch_ops<4>(transA, transB, mapA, mapB, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_streamk_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream) {

@@ -131,8 +131,9 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
                             &mapB, &p.za, &p.zb);
     if (e != cudaSuccess) return SGEMM_ERR_CUDA;
     const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
-    if (plan.variant == SGEMM_VARIANT_TC_TF32X3 || plan.variant == SGEMM_VARIANT_TC_PAIRED) {
-      e = launch_tf32x3(ta, tb, plan.variant == SGEMM_VARIANT_TC_PAIRED, mapA, mapB, p, cs);
+    if (plan.variant == SGEMM_VARIANT_TC_TF32X3 || plan.variant == SGEMM_VARIANT_TC_GROUPED) {
+      e = launch_tf32x3(ta, tb, plan.variant == SGEMM_VARIANT_TC_GROUPED ? 128 / plan.tile_m : 1, mapA, mapB, p,
+                        cs);
       if (e == cudaSuccess && plan.kernel_launches > 1) e = launch_streamk_fixup(p, (int)plan.sk_tiles, cs);
     } else if (!ta && !tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, cs);
     else if (!ta && tb) e = launch_tma_op_nt(tile, mapA, mapB, p, split, cs);

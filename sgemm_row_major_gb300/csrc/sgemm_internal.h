@@ -51,7 +51,7 @@ cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t 
 
 // Copies the tensor-core kernel's schedule from a plan (no-op for other variants).
 inline void set_schedule(const sgemm_plan_t& plan, GemmParams* p) {
-  if (plan.variant != SGEMM_VARIANT_TC_TF32X3 && plan.variant != SGEMM_VARIANT_TC_PAIRED) return;
+  if (plan.variant != SGEMM_VARIANT_TC_TF32X3 && plan.variant != SGEMM_VARIANT_TC_GROUPED) return;
   p->sk_grid = (int)plan.grid_x;
   p->sk_iters = plan.sk_iters;
   p->sk_tile0 = (int)plan.dp_tiles;
@@ -79,10 +79,11 @@ SGEMM_DECLARE_TMA_OP(tt)
 // 3xTF32 tensor-core kernel (kernel_tf32x3.cu), 128x128x32 tiles, any op,
 // persistent data-parallel + stream-K schedule (GemmParams::sk_*), then the
 // fixup kernel over the sk_tiles stream-K tiles when any of them is shared.
-// `paired`: products with M, N <= 64 two to a tile (tile t = products 2t and
-// 2t+1; tensor maps with 64-wide boxes; whole tiles only, no stream-K).
+// `group` G > 1 (2 or 4): products with M, N <= 128/G, G to a tile
+// block-diagonally (tile t = products G*t .. G*t+G-1; tensor maps with boxes
+// 128/G wide; whole tiles only, no stream-K).
 cudaError_t prepare_tf32x3();
-cudaError_t launch_tf32x3(bool transA, bool transB, bool paired, const CUtensorMap& mapA, const CUtensorMap& mapB,
+cudaError_t launch_tf32x3(bool transA, bool transB, int group, const CUtensorMap& mapA, const CUtensorMap& mapB,
                           const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_streamk_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
 cudaError_t launch_generic_gemm(bool transA, bool transB, const GemmParams& p, int split,

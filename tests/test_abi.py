@@ -217,7 +217,7 @@ def test_small_product_planner(lib):
     the tensor cores, two to a tile); its own rules decide where it applies."""
     def small(*a, **k):
         return bplan(*a, **k)["variant_name"] == "SMALL"
-    assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64)["variant_name"] == "TC_PAIRED"
+    assert bplan("N", "N", 64, 64, 64, 8192, 64 * 64, 64 * 64, 64 * 64)["variant_name"] == "TC_GROUPED"
     try:
         sg.sgemm_set_variant_override("SMALL", 0)
         # 8192 products of 64x64x64: a persistent grid of 64-thread CTAs, four per SM, no workspace
@@ -256,31 +256,37 @@ def test_small_product_planner(lib):
         sg.sgemm_set_variant_override("AUTO", 0)
 
 
-def test_paired_planner(lib):
+def test_grouped_planner(lib):
     # 2048 products of 64x64x1024: 1024 block-diagonal pairs on one persistent CTA per SM, no stream-K
     p = bplan("N", "N", 64, 64, 1024, 2048, 64 * 1024, 1024 * 64, 64 * 64)
-    assert p["variant_name"] == "TC_PAIRED" and (p["grid_x"], p["threads"]) == (152, 608)
+    assert p["variant_name"] == "TC_GROUPED" and (p["grid_x"], p["threads"]) == (152, 608)
     assert (p["dp_tiles"], p["sk_tiles"], p["split_k"], p["kernel_launches"], p["workspace_bytes"]) == (1024, 0, 1, 1, 0)
     assert (p["tile_m"], p["tile_n"], p["tile_k"]) == (64, 64, 32)
     # every op combination, ragged M and N, odd batch, shared operands
     for ta in "NT":
         for tb in "NT":
-            assert bplan(ta, tb, 36, 20, 300, 305, 36 * 300, 300 * 20, 36 * 20)["variant_name"] == "TC_PAIRED"
-            assert bplan(ta, tb, 36, 20, 64, 305, 36 * 64, 64 * 20, 36 * 20)["variant_name"] == "TC_PAIRED"
-    assert bplan("N", "T", 64, 64, 512, 400, 0, 64 * 512, 64 * 64)["variant_name"] == "TC_PAIRED"
+            assert bplan(ta, tb, 36, 20, 300, 305, 36 * 300, 300 * 20, 36 * 20)["variant_name"] == "TC_GROUPED"
+            assert bplan(ta, tb, 36, 20, 64, 305, 36 * 64, 64 * 20, 36 * 20)["variant_name"] == "TC_GROUPED"
+    assert bplan("N", "T", 64, 64, 512, 400, 0, 64 * 512, 64 * 64)["variant_name"] == "TC_GROUPED"
     # fewer products than SMs, M or N above 64, TMA rules broken
-    assert bplan("N", "N", 64, 64, 1024, 152, 64 * 1024, 1024 * 64, 64 * 64)["variant_name"] == "TC_PAIRED"
+    assert bplan("N", "N", 64, 64, 1024, 152, 64 * 1024, 1024 * 64, 64 * 64)["variant_name"] == "TC_GROUPED"
     assert bplan("N", "N", 64, 64, 1024, 151, 64 * 1024, 1024 * 64, 64 * 64)["variant_name"] == "TC_TF32X3"
     assert bplan("N", "N", 65, 64, 1024, 2048, 65 * 1024, 1024 * 64, 65 * 64)["variant_name"] == "TC_TF32X3"
     assert bplan("N", "N", 64, 65, 1024, 2048, 64 * 1024, 1024 * 68, 64 * 65, ldb=68)["variant_name"] == "TC_TF32X3"
     assert bplan("N", "N", 64, 64, 1024, 2048, 64 * 1024 + 2, 1024 * 64, 64 * 64)["variant_name"] == "GENERIC"
+    # M, N <= 32: four products to a tile (32x32 blocks); an odd batch rounds the tiles up
+    quad = bplan("N", "N", 32, 32, 32, 8193, 32 * 32, 32 * 32, 32 * 32)
+    assert (quad["variant_name"], quad["tile_m"], quad["tile_n"], quad["dp_tiles"]) == ("TC_GROUPED", 32, 32, 2049)
+    assert bplan("T", "T", 20, 28, 64, 1000, 20 * 64, 64 * 28, 20 * 28)["tile_m"] == 32
+    assert bplan("N", "N", 33, 32, 32, 8192, 33 * 32, 32 * 32, 33 * 32)["tile_m"] == 64
+    assert bplan("N", "N", 32, 33, 32, 8192, 32 * 32, 32 * 36, 32 * 33, ldb=36)["tile_m"] == 64
     # fewer SMs: fewer CTAs, the same pairs
     q = bplan("N", "N", 64, 64, 1024, 2048, 64 * 1024, 1024 * 64, 64 * 64, sm=100)
-    assert (q["variant_name"], q["grid_x"], q["dp_tiles"]) == ("TC_PAIRED", 100, 1024)
+    assert (q["variant_name"], q["grid_x"], q["dp_tiles"]) == ("TC_GROUPED", 100, 1024)
     try:
-        sg.sgemm_set_variant_override("TC_PAIRED", 0)
+        sg.sgemm_set_variant_override("TC_GROUPED", 0)
         one = plan("N", "N", 64, 64, 64)
-        assert (one["variant_name"], one["grid_x"], one["dp_tiles"]) == ("TC_PAIRED", 1, 1)
+        assert (one["variant_name"], one["grid_x"], one["dp_tiles"]) == ("TC_GROUPED", 1, 1)
         assert bplan("N", "N", 64, 64, 64, 3, 64 * 64, 64 * 64, 64 * 64)["dp_tiles"] == 2
         assert plan("N", "N", 65, 64, 64)["variant_name"] == "GENERIC"
     finally:

@@ -73,7 +73,7 @@ def test_graph_replays_back_to_back_accumulate():
     check_exact(dC.cpu().numpy(), (5 * one.astype(np.float64)).astype(np.float32), "5 replays")
 
 
-@pytest.mark.parametrize("batch,M,N,K,expect", [(1024, 64, 64, 64, "TC_PAIRED"), (16, 256, 384, 512, "TC_TF32X3")])
+@pytest.mark.parametrize("batch,M,N,K,expect", [(1024, 64, 64, 64, "TC_GROUPED"), (16, 256, 384, 512, "TC_TF32X3")])
 def test_strided_batch_graph_replay(batch, M, N, K, expect):
     """Strided batches of small products (two to a tensor-core tile) and of large ones, captured and replayed."""
     torch = torch_cuda()
