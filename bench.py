@@ -46,9 +46,11 @@ PROFILES = {("TC_TF32X3", "square4096"): os.path.join(ROOT, "profiles", "tf32x3_
             ("SMALL", "batched_small_8192x64x64x64"):
                 os.path.join(ROOT, "profiles", "small_gemm_batched8192x64x64x64.md"),
             ("TC_GROUPED", "batched_small_k1024_2048x64x64x1024"):
-                os.path.join(ROOT, "profiles", "tf32x3_paired_batched2048x64x64x1024.md"),
+                os.path.join(ROOT, "profiles", "tf32x3_grouped_batched2048x64x64x1024.md"),
             ("TC_GROUPED", "batched_small_8192x64x64x64"):
-                os.path.join(ROOT, "profiles", "tf32x3_paired_batched8192x64x64x64.md")}
+                os.path.join(ROOT, "profiles", "tf32x3_grouped_batched8192x64x64x64.md"),
+            ("TC_GROUPED", "batched_tiny_16384x32x32x32"):
+                os.path.join(ROOT, "profiles", "tf32x3_grouped_batched16384x32x32x32.md")}
 # dense tensor-core peaks (PFLOP/s, nominal) used to scale the measured bf16 peak to tf32
 NOMINAL_BF16_PF, NOMINAL_TF32_PF = 2.25, 1.1
 TF32_PRODUCTS = 3  # tensor-core products per useful FMA in the 3xTF32 split
