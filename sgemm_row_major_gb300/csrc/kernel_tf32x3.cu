@@ -258,9 +258,10 @@ __device__ __forceinline__ Segment cta_segment(const GemmParams& p, const CtaWor
 // useful, instead of 1/G^2 with one product per tile (pairs of 64x64: a half
 // instead of a quarter; quads of 32x32: a quarter instead of a sixteenth).  Each operand tile is then G TMA boxes of 128/G rows or
 // columns: K-contiguous ones stack into the same layout, while an
-// M/N-contiguous one becomes G [32 k][128/G] blocks.  Only the folder warps
-// over a diagonal block fold and write C (a warp's 32 rows lie in one block);
-// there is no stream-K in this mode.
+// M/N-contiguous one becomes G [32 k][128/G] blocks.  Only the diagonal blocks
+// are folded and written to C: a folder warp's 32 rows lie in one block, and
+// the two folder warps of a lane quarter take half of its columns each.  There
+// is no stream-K in this mode.
 template <bool TA, bool TB, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
@@ -521,14 +522,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ folders, then epilogue
     const int q = warp & 3;                          // TMEM lane quarter this warp may access
     const int half = (warp - kFirstFoldWarp) >> 2;   // which 64 accumulator columns
-    // G > 1: the diagonal block of this warp's rows, whether its columns lie in this warp's 64, and
-    // where; the other warps keep to the barrier protocol only
+    // G > 1: only the diagonal block of this warp's 32 rows is a product; the two folder warps of
+    // this lane quarter split its columns (the warp whose 64 columns hold the block takes the
+    // first half, the other warp the second)
     constexpr int kBlock = BM / G;
-    constexpr int kCols = kBlock < 64 ? kBlock : 64;  // accumulator columns a warp folds
+    constexpr int kCols = G == 1 ? 64 : (kBlock < 64 ? kBlock : 64) / 2;  // accumulator columns a warp folds
     const int blk = G > 1 ? (32 * q) / kBlock : 0;
-    const bool useful = G == 1 || (kBlock * blk) / 64 == half;
-    const int c_off = G > 1 ? kBlock * blk - 64 * half : 0;
-    const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * half + c_off);
+    const int col0 = G > 1 ? kBlock * blk + ((kBlock * blk) / 64 == half ? 0 : kCols) : 64 * half;
+    const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col0;
     float2 master2[kCols / 2];  // columns 2e, 2e+1 of the thread's kCols
 #pragma unroll
     for (int e = 0; e < kCols / 2; ++e) master2[e] = make_float2(0.0f, 0.0f);
@@ -547,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
           break;
         }
-        if (useful) {
+        {
           tmem_fence_after_sync();
           float v[kCols / 16][16];
 #pragma unroll
@@ -575,12 +576,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e)
           *reinterpret_cast<float4*>(w + 4 * e) =
               make_float4(master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y);
-      } else if (useful) {
+      } else {
         int prod, m0, c0;  // product, origin row of the tile in it, first column of this thread's
         if (G > 1) {
           prod = G * g.tile + blk;  // rows and columns kBlock*blk .. +kBlock-1 of the tile
           m0 = -kBlock * blk;
-          c0 = 0;
+          c0 = col0 - kBlock * blk;
         } else {
           int n0;
           tile_origin(p, g.tile, prod, m0, n0);
