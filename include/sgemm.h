@@ -127,7 +127,11 @@ typedef struct sgemm_plan_t {
      * dp_tiles output tiles are taken whole, round robin (CTA c: tiles c,
      * c + grid_x, ...); the sk_iters K tiles of the last sk_tiles output tiles
      * are then shared evenly by all CTAs (stream-K); split_k is the most CTAs
-     * that share one output tile. */
+     * that share one output tile.  SGEMM_VARIANT_TC_GROUPED: every tile is
+     * whole and holds 128 / tile_m products (tile_m = tile_n = 64: two, 32:
+     * four), so dp_tiles = ceil(batch_count / (128 / tile_m)).  For
+     * SGEMM_VARIANT_SMALL grid_x is the persistent grid (products dealt round
+     * robin) and tile_k its K chunk. */
     int64_t dp_tiles;
     int64_t sk_tiles;
     int64_t sk_iters;
@@ -188,6 +192,9 @@ int sgemm_selftest_wait_timeout(unsigned timeout_us, struct CUstream_st *stream)
  *     GPU).  The fast paths need strides that are multiples of 4 floats (and
  *     non-overlapping operands or a 0 stride); other strides take the
  *     any-alignment kernel.
+ *   - Products with M, N <= 64 (a batch of at least one per SM) run two to a
+ *     tensor-core tile, M, N <= 32 four to a tile (SGEMM_VARIANT_TC_GROUPED):
+ *     same arithmetic and bounds as the tensor-core path of sgemm().
  */
 int sgemm_strided_batched(char transA, char transB, int64_t M, int64_t N, int64_t K,
                           float alpha, const float *A, int64_t lda,
