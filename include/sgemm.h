@@ -99,6 +99,36 @@ int sgemm(char transA, char transB, int64_t M, int64_t N, int64_t K,
           float beta, float *C, int64_t ldc,
           struct CUstream_st *stream);
 
+/*
+ * Caller-supplied workspace: the same operation as sgemm() with the partial
+ * sums of a split K (split-K slices, stream-K tiles shared by several CTAs)
+ * in memory the caller owns, so a call allocates nothing, has no size limit
+ * and captures into a CUDA graph as kernels only.
+ *
+ * sgemm_workspace_size() stores in *bytes the workspace sgemm_ex() needs for
+ * these arguments on the current device (0: none; equal to the
+ * workspace_bytes of sgemm_plan() with sm_count <= 0).  Arguments 1-13 are
+ * checked as in sgemm() (C is only inspected); -14: bytes is NULL.
+ *
+ * sgemm_ex(): arguments 1-13 and 16 (stream) as in sgemm(); `workspace` is a
+ * device pointer, 16-byte aligned, to at least that many bytes, which the
+ * call uses in stream order on `stream` (the caller must not touch it, nor
+ * share it with another call that may run at the same time, until the call's
+ * work on the stream is done).  -14: workspace NULL although needed, or not
+ * 16-byte aligned; -15: workspace_bytes smaller than needed.  Nothing is
+ * launched on an argument error.
+ */
+int sgemm_workspace_size(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                         float alpha, const float *A, int64_t lda,
+                         const float *B, int64_t ldb,
+                         float beta, const float *C, int64_t ldc, size_t *bytes);
+int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t K,
+             float alpha, const float *A, int64_t lda,
+             const float *B, int64_t ldb,
+             float beta, float *C, int64_t ldc,
+             void *workspace, size_t workspace_bytes,
+             struct CUstream_st *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *sgemm_status_string(int status);
 

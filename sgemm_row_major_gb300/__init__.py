@@ -16,7 +16,8 @@ import os
 import threading
 
 __all__ = [
-    "SgemmError", "load", "library_path", "sgemm", "sgemm_host", "sgemm_noalloc", "sgemm_plan",
+    "SgemmError", "load", "library_path", "sgemm", "sgemm_host", "sgemm_noalloc", "sgemm_ex",
+    "sgemm_workspace_size", "sgemm_plan",
     "sgemm_strided_batched", "sgemm_plan_strided_batched", "sgemm_status_string",
     "sgemm_last_cuda_error", "sgemm_sync_status", "sgemm_set_variant_override",
     "sgemm_selftest_wait_timeout", "matmul", "VARIANTS", "STATUS",
@@ -27,7 +28,8 @@ _LIB_PATH = os.path.join(_PKG, "_lib", "libsgemm.so")
 
 STATUS = {"OK": 0, "ERR_CUDA": 1, "ERR_TIMEOUT": 2, "ERR_NOMEM": 3, "ERR_UNSUPPORTED": 4, "ERR_SCRATCH_LIMIT": 5}
 NOALLOC_SCRATCH_BYTES = 32 << 20  # SGEMM_NOALLOC_SCRATCH_BYTES in include/sgemm.h
-VARIANTS = {"AUTO": 0, "NONE": 1, "SCALE": 2, "GENERIC": 3, "TMA_128x128": 4, "TMA_64x256": 5, "TC_TF32X3": 6, "SMALL": 7, "TC_GROUPED": 8}
+VARIANTS = {"AUTO": 0, "NONE": 1, "SCALE": 2, "GENERIC": 3, "TMA_128x128": 4, "TMA_64x256": 5, "TC_TF32X3": 6,
+            "SMALL": 7, "TC_GROUPED": 8}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 
 
@@ -71,6 +73,11 @@ def load() -> ctypes.CDLL:
         lib.sgemm_host.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_noalloc.restype = ctypes.c_int
         lib.sgemm_noalloc.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        lib.sgemm_ex.restype = ctypes.c_int
+        lib.sgemm_ex.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp, ctypes.c_size_t, vp]
+        lib.sgemm_workspace_size.restype = ctypes.c_int
+        lib.sgemm_workspace_size.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                             ctypes.POINTER(ctypes.c_size_t)]
         lib.sgemm_plan.restype = ctypes.c_int
         lib.sgemm_plan.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ctypes.c_int,
                                    ctypes.POINTER(PlanStruct)]
@@ -178,6 +185,28 @@ def sgemm_noalloc(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 
                               int(lda), _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), _stream(stream))
     if st != 0 and raise_on_error:
         raise SgemmError(st, "sgemm_noalloc")
+    return st
+
+
+def sgemm_workspace_size(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> int:
+    """Bytes of workspace sgemm_ex() needs for these arguments on the current device (0: none)."""
+    n = ctypes.c_size_t(0)
+    st = load().sgemm_workspace_size(_ch(transA), _ch(transB), int(M), int(N), int(K), float(alpha), _ptr(A),
+                                     int(lda), _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), ctypes.byref(n))
+    if st != 0:
+        raise SgemmError(st, "sgemm_workspace_size")
+    return int(n.value)
+
+
+def sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, workspace, workspace_bytes,
+             stream=None, *, raise_on_error: bool = True) -> int:
+    """sgemm() with the split-K partial sums in a caller-owned device workspace (16-byte aligned, at
+    least sgemm_workspace_size() bytes; None when that is 0): no allocation, no size limit."""
+    st = load().sgemm_ex(_ch(transA), _ch(transB), int(M), int(N), int(K), float(alpha), _ptr(A), int(lda),
+                         _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), _ptr(workspace), int(workspace_bytes),
+                         _stream(stream))
+    if st != 0 and raise_on_error:
+        raise SgemmError(st, "sgemm_ex")
     return st
 
 

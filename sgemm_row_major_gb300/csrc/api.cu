@@ -355,8 +355,10 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   return SGEMM_OK;
 }
 
+// ext_ws: the caller's workspace of at least plan.workspace_bytes (sgemm_ex), or nullptr to take
+// the partial sums from the device's stream-ordered pool.
 int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& st, float* C,
-                cudaStream_t stream) {
+                cudaStream_t stream, void* ext_ws = nullptr) {
   GemmParams p{};
   p.M = (int)pr.M;
   p.N = (int)pr.N;
@@ -398,7 +400,9 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   }
 
   void* ws = nullptr;
-  if (plan.workspace_bytes > 0) {
+  if (plan.workspace_bytes > 0 && ext_ws) {
+    p.ws = static_cast<float*>(ext_ws);
+  } else if (plan.workspace_bytes > 0) {
     cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)plan.workspace_bytes, st.pool, stream);
     if (e != cudaSuccess) {
       t_last_cuda_error = (int)e;
@@ -451,6 +455,48 @@ int sgemm(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha
   s = make_plan(pr, st->sm_count, &plan);
   if (s != SGEMM_OK) return s;
   return launch_gemm(pr, plan, *st, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_workspace_size(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                         int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
+                         size_t* bytes) {
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  if (!bytes) return -14;
+  *bytes = 0;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  int dev;
+  DeviceState* st;
+  s = device_state(&dev, &st);
+  if (s != SGEMM_OK) return s;
+  sgemm_plan_t plan;
+  s = make_plan(pr, st->sm_count, &plan);
+  if (s != SGEMM_OK) return s;
+  *bytes = (size_t)plan.workspace_bytes;
+  return SGEMM_OK;
+}
+
+int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+             const float* B, int64_t ldb, float beta, float* C, int64_t ldc, void* workspace, size_t workspace_bytes,
+             struct CUstream_st* stream) {
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  if (workspace && !aligned16(workspace)) return -14;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  int dev;
+  DeviceState* st;
+  s = device_state(&dev, &st);
+  if (s != SGEMM_OK) return s;
+  sgemm_plan_t plan;
+  s = make_plan(pr, st->sm_count, &plan);
+  if (s != SGEMM_OK) return s;
+  if (plan.workspace_bytes > 0) {
+    if (!workspace) return -14;
+    if ((uint64_t)workspace_bytes < (uint64_t)plan.workspace_bytes) return -15;
+  }
+  return launch_gemm(pr, plan, *st, C, reinterpret_cast<cudaStream_t>(stream), workspace);
 }
 
 int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
@@ -540,8 +586,12 @@ const char* sgemm_status_string(int status) {
     case -10: return "invalid argument 10 (ldb too small)";
     case -12: return "invalid argument 12 (C is NULL)";
     case -13: return "invalid argument 13 (ldc too small)";
-    case -14: return "invalid argument 14 (strideA < 0)";
-    case -15: return "invalid argument 15 (plan is NULL, or strideB < 0 in the batched calls)";
+    case -14:
+      return "invalid argument 14 (strideA < 0; sgemm_ex: workspace NULL although needed, or not 16-byte aligned; "
+             "sgemm_workspace_size: bytes is NULL)";
+    case -15:
+      return "invalid argument 15 (plan is NULL; strideB < 0 in the batched calls; sgemm_ex: workspace_bytes "
+             "smaller than sgemm_workspace_size())";
     case -16: return "invalid argument 16 (strideC < 0, or C matrices of a batch overlap)";
     case -17: return "invalid argument 17 (batch_count < 0)";
     case -19: return "invalid argument 19 (plan is NULL)";

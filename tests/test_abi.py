@@ -61,6 +61,23 @@ def test_invalid_arguments_rejected_without_launch(lib):
     for args, want in cases:
         assert sg.sgemm(*args, stream=0, raise_on_error=False) == want, (args, want)
         assert "invalid argument" in sg.sgemm_status_string(want)
+        # the caller-workspace entry points check arguments 1-13 the same way, before any device use
+        assert sg.sgemm_ex(*args, FAKE, 1 << 20, stream=0, raise_on_error=False) == want, (args, want)
+        assert lib.sgemm_workspace_size(*[a.encode() if isinstance(a, str) else a for a in args],
+                                        ctypes.byref(ctypes.c_size_t())) == want, (args, want)
+
+
+def test_workspace_entry_points_own_arguments(lib):
+    ok = ("N", "N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4)
+    raw = [a.encode() if isinstance(a, str) else a for a in ok]
+    assert lib.sgemm_workspace_size(*raw, None) == -14                      # bytes is NULL
+    assert sg.sgemm_ex(*ok, FAKE_ODD, 1 << 20, stream=0, raise_on_error=False) == -14  # workspace misaligned
+    for code in (-14, -15):
+        assert "sgemm_ex" in sg.sgemm_status_string(code)
+    # empty problems need no workspace and launch nothing
+    empty = ("N", "N", 0, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4)
+    assert sg.sgemm_ex(*empty, None, 0, stream=0) == 0
+    assert sg.sgemm_workspace_size(*empty) == 0
 
 
 def test_null_operands_allowed_when_not_read(lib):
