@@ -36,7 +36,10 @@ VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 class SgemmError(RuntimeError):
     def __init__(self, status: int, where: str = "sgemm"):
         self.status = status
-        super().__init__(f"{where} returned {status}: {sgemm_status_string(status)}")
+        # the failed CUDA call's cudaError_t (kept per host thread; raised on the caller's thread)
+        self.cuda_error = sgemm_last_cuda_error() if status == STATUS["ERR_CUDA"] else 0
+        detail = f" (cudaError_t {self.cuda_error})" if self.cuda_error else ""
+        super().__init__(f"{where} returned {status}: {sgemm_status_string(status)}{detail}")
 
 
 class PlanStruct(ctypes.Structure):

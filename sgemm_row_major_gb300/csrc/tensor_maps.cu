@@ -53,6 +53,20 @@ cudaError_t encode_3d(const float* base, int64_t inner, int64_t outer, int64_t l
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// cuTensorMapEncodeTiled fails with CUDA_ERROR_INVALID_CONTEXT on a thread
+// that has no current context: a host thread whose first CUDA call is into
+// this library has none yet (cudaGetDevice does not bind one).  cudaSetDevice
+// makes the device's primary context current; once per thread and device.
+cudaError_t bind_primary_context() {
+  thread_local int bound = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || bound == dev) return e;
+  e = cudaSetDevice(dev);
+  if (e == cudaSuccess) bound = dev;
+  return e;
+}
+
 }  // namespace
 
 cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
@@ -60,12 +74,14 @@ cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t 
                                 int bm, int bn, int bk, CUtensorMap* mapA, CUtensorMap* mapB, int* za, int* zb) {
   const int64_t pa = (batch > 1 && stride_a != 0) ? batch : 1;
   const int64_t pb = (batch > 1 && stride_b != 0) ? batch : 1;
+  cudaError_t e = bind_primary_context();
+  if (e != cudaSuccess) return e;
   *za = pa > 1 ? 1 : 0;
   *zb = pb > 1 ? 1 : 0;
   // op(A): 'N' -> stored M x K, K contiguous (swizzled K-major tile);
   //        'T' -> stored K x M, M contiguous.
-  cudaError_t e = ta ? encode_3d(A, M, K, lda, pa, stride_a, bm, bk, false, mapA)
-                     : encode_3d(A, K, M, lda, pa, stride_a, bk, bm, true, mapA);
+  e = ta ? encode_3d(A, M, K, lda, pa, stride_a, bm, bk, false, mapA)
+         : encode_3d(A, K, M, lda, pa, stride_a, bk, bm, true, mapA);
   if (e != cudaSuccess) return e;
   // op(B): 'N' -> stored K x N, N contiguous; 'T' -> stored N x K, K contiguous (swizzled).
   return tb ? encode_3d(B, K, N, ldb, pb, stride_b, bk, bn, true, mapB)
