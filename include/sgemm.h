@@ -85,8 +85,10 @@ enum sgemm_variant {
     SGEMM_VARIANT_TMA_64x256 = 5, /* same kernel, 64x256 tiles for short M */
     SGEMM_VARIANT_TC_TF32X3 = 6,  /* tcgen05 tensor cores, 3xTF32 split, 128x128x32 tiles */
     SGEMM_VARIANT_SMALL = 7,      /* M, N <= 64 in a large batch: one CTA per product, FP32 FFMA */
-    SGEMM_VARIANT_TC_GROUPED = 8  /* M, N <= 64 in a batch: 3xTF32 tensor cores, 2 (M, N <= 32: 4) products
+    SGEMM_VARIANT_TC_GROUPED = 8, /* M, N <= 64 in a batch: 3xTF32 tensor cores, 2 (M, N <= 32: 4) products
                                      per 128x128 tile, block-diagonally; tile_m = tile_n = 128 / group */
+    SGEMM_VARIANT_TC_PAIR = 9     /* 3xTF32 tensor cores on CTA pairs (clusters of 2 on one TPC): 256x128x32
+                                     tiles, each CTA 128 rows and half of the tile's B columns */
 };
 
 /*
@@ -157,7 +159,9 @@ typedef struct sgemm_plan_t {
      * dp_tiles output tiles are taken whole, round robin (CTA c: tiles c,
      * c + grid_x, ...); the sk_iters K tiles of the last sk_tiles output tiles
      * are then shared evenly by all CTAs (stream-K); split_k is the most CTAs
-     * that share one output tile.  SGEMM_VARIANT_TC_GROUPED: every tile is
+     * that share one output tile.  SGEMM_VARIANT_TC_PAIR: the same schedule
+     * over 256 x 128 tiles with clusters of two CTAs as the unit (grid_x / 2
+     * clusters; split_k counts clusters).  SGEMM_VARIANT_TC_GROUPED: every tile is
      * whole and holds 128 / tile_m products (tile_m = tile_n = 64: two, 32:
      * four), so dp_tiles = ceil(batch_count / (128 / tile_m)).  For
      * SGEMM_VARIANT_SMALL grid_x is the persistent grid (products dealt round

@@ -58,7 +58,10 @@ TMA_KERNEL_FILES = ["kernel_tma.cuh", "device_utils.cuh", "sgemm_internal.h", "k
                     "kernel_tma_nt.cu", "kernel_tma_tn.cu", "kernel_tma_tt.cu"]
 
 
-TC_KERNEL_FILES = ["kernel_tf32x3.cu", "device_utils.cuh", "sgemm_internal.h"]
+TC_KERNEL_FILES = ["kernel_tf32x3.cu", "kernel_tc_common.cuh", "device_utils.cuh", "sgemm_internal.h"]
+
+
+PAIR_KERNEL_FILES = ["kernel_tc_pair.cu", "kernel_tc_common.cuh", "device_utils.cuh", "sgemm_internal.h"]
 
 
 SMALL_KERNEL_FILES = ["kernel_small.cu", "kernel_small.h", "sgemm_internal.h"]
@@ -72,6 +75,11 @@ def tma_kernel_digest() -> str:
 def tc_kernel_digest() -> str:
     """Hash of the sources of the 3xTF32 tensor-core kernel only."""
     return _digest(TC_KERNEL_FILES)
+
+
+def pair_kernel_digest() -> str:
+    """Hash of the sources of the CTA-pair tensor-core kernel only."""
+    return _digest(PAIR_KERNEL_FILES)
 
 
 def small_kernel_digest() -> str:

@@ -31,6 +31,7 @@ struct DeviceState {
   std::once_flag once;
   cudaError_t init_error = cudaSuccess;
   int sm_count = 0;
+  int pair_clusters = 0;  // co-resident clusters of the CTA-pair kernel
   unsigned* fault = nullptr;
   cudaMemPool_t pool = nullptr;
 };
@@ -75,6 +76,8 @@ int device_state(int* device_out, DeviceState** st_out) {
     if (err == cudaSuccess) err = prepare_tma_op_tt();
     if (err == cudaSuccess) err = prepare_tf32x3();
     if (err == cudaSuccess) err = prepare_small_gemm();
+    if (err == cudaSuccess) err = prepare_tc_pair();
+    if (err == cudaSuccess) err = tc_pair_max_clusters(&st.pair_clusters);
     if (err == cudaSuccess) {
       cudaMemPoolProps props = {};
       props.allocType = cudaMemAllocationTypePinned;
@@ -228,8 +231,13 @@ int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
   return SGEMM_OK;
 }
 
-// The planner: a pure function of the problem, the SM count and the override.
-int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
+// Shared memory per CTA of the CTA-pair kernel (kernel_tc_pair.cu: 6 raw
+// stages of 24 KB, 2 split stages of 16 KB, alignment slack).
+constexpr int64_t kPairSmemBytes = 6 * 24576 + 2 * 16384 + 1024;
+
+// The planner: a pure function of the problem, the SM count, the number of
+// co-resident CTA-pair clusters (<= 0: sm_count / 2) and the override.
+int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clusters = 0) {
   *plan = sgemm_plan_t{};
   plan->split_k = 1;
   if (pr.M == 0 || pr.N == 0 || pr.batch == 0) {
@@ -278,6 +286,7 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
     variant = (ov == SGEMM_VARIANT_GENERIC || tma_ok) ? ov : SGEMM_VARIANT_GENERIC;
   if (ov == SGEMM_VARIANT_SMALL) variant = small_ok ? ov : SGEMM_VARIANT_GENERIC;
   if (ov == SGEMM_VARIANT_TC_GROUPED) variant = group_ok ? ov : SGEMM_VARIANT_GENERIC;
+  if (ov == SGEMM_VARIANT_TC_PAIR) variant = tma_ok ? ov : SGEMM_VARIANT_GENERIC;
   if (variant == SGEMM_VARIANT_TC_GROUPED) {
     // whole tiles (a group of products each) on one persistent CTA per SM, no stream-K
     const int64_t tiles = ceil_div(pr.batch, group);
@@ -316,6 +325,8 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
     bm = g.bm; bn = g.bn; bk = g.bk; threads = g.threads; stages = 2;
   } else if (variant == SGEMM_VARIANT_TC_TF32X3) {
     bm = 128; bn = 128; bk = 32; threads = 608; stages = 4; smem = 4 * 32768 + 2 * 32768 + 1024;
+  } else if (variant == SGEMM_VARIANT_TC_PAIR) {
+    bm = 256; bn = 128; bk = 32; threads = 608; stages = 6; smem = kPairSmemBytes;
   } else if (variant == SGEMM_VARIANT_TMA_128x128) {
     using T = tma::Tile<4, 2>;
     bm = T::BM; bn = T::BN; bk = tma::kBK; threads = tma::kThreads; stages = tma::kStages; smem = T::SMEM_BYTES;
@@ -336,6 +347,14 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
   plan->threads = threads;
   plan->smem_bytes = smem;
   if (variant == SGEMM_VARIANT_TC_TF32X3) return plan_stream_k(tiles, kt, sm_count, plan);
+  if (variant == SGEMM_VARIANT_TC_PAIR) {
+    // the stream-K schedule with clusters as the unit; 2 CTAs, 2 partial-sum slots each, per cluster
+    const int clusters = std::max(1, pair_clusters > 0 ? pair_clusters : sm_count / 2);
+    const int s = plan_stream_k(tiles, kt, clusters, plan);
+    plan->grid_x *= 2;
+    plan->workspace_bytes *= 2;
+    return s;
+  }
 
   // Split K only when the output tiles cannot fill the SMs, keeping at least
   // 4 K tiles per slice.
@@ -393,9 +412,11 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
 
   CUtensorMap mapA, mapB;
   if (plan.variant != SGEMM_VARIANT_GENERIC && plan.variant != SGEMM_VARIANT_SMALL) {
+    int box_m, box_n;
+    operand_boxes(plan, &box_m, &box_n);
     cudaError_t e = encode_operand_maps(pr.ta, pr.tb, pr.M, pr.N, pr.K, pr.A, pr.lda, pr.stride_a, pr.B, pr.ldb,
-                                        pr.stride_b, p.batch, plan.tile_m, plan.tile_n, plan.tile_k, &mapA, &mapB,
-                                        &p.za, &p.zb);
+                                        pr.stride_b, p.batch, box_m, box_n, plan.tile_k, &mapA, &mapB, &p.za,
+                                        &p.zb);
     if (e != cudaSuccess) return cuda_fail(e);
   }
 
@@ -420,6 +441,9 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
     e = launch_tf32x3(pr.ta, pr.tb, plan.variant == SGEMM_VARIANT_TC_GROUPED ? 128 / plan.tile_m : 1, mapA, mapB,
                       p, stream);
     if (e == cudaSuccess && plan.kernel_launches > 1) e = launch_streamk_fixup(p, (int)plan.sk_tiles, stream);
+  } else if (plan.variant == SGEMM_VARIANT_TC_PAIR) {
+    e = launch_tc_pair(pr.ta, pr.tb, mapA, mapB, p, stream);
+    if (e == cudaSuccess && plan.kernel_launches > 1) e = launch_pair_fixup(p, (int)plan.sk_tiles, stream);
   } else {
     const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
     if (!pr.ta && !pr.tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, stream);
@@ -428,7 +452,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
     else e = launch_tma_op_tt(tile, mapA, mapB, p, split, stream);
   }
   if (e == cudaSuccess && split > 1 && plan.variant != SGEMM_VARIANT_TC_TF32X3 &&
-      plan.variant != SGEMM_VARIANT_TC_GROUPED)
+      plan.variant != SGEMM_VARIANT_TC_GROUPED && plan.variant != SGEMM_VARIANT_TC_PAIR)
     e = launch_splitk_reduce(p, split, stream);
   if (ws) {
     cudaError_t ef = cudaFreeAsync(ws, stream);
@@ -452,7 +476,7 @@ int sgemm(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha
   s = device_state(&dev, &st);
   if (s != SGEMM_OK) return s;
   sgemm_plan_t plan;
-  s = make_plan(pr, st->sm_count, &plan);
+  s = make_plan(pr, st->sm_count, &plan, st->pair_clusters);
   if (s != SGEMM_OK) return s;
   return launch_gemm(pr, plan, *st, C, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -471,7 +495,7 @@ int sgemm_workspace_size(char transA, char transB, int64_t M, int64_t N, int64_t
   s = device_state(&dev, &st);
   if (s != SGEMM_OK) return s;
   sgemm_plan_t plan;
-  s = make_plan(pr, st->sm_count, &plan);
+  s = make_plan(pr, st->sm_count, &plan, st->pair_clusters);
   if (s != SGEMM_OK) return s;
   *bytes = (size_t)plan.workspace_bytes;
   return SGEMM_OK;
@@ -490,7 +514,7 @@ int sgemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t K, float al
   s = device_state(&dev, &st);
   if (s != SGEMM_OK) return s;
   sgemm_plan_t plan;
-  s = make_plan(pr, st->sm_count, &plan);
+  s = make_plan(pr, st->sm_count, &plan, st->pair_clusters);
   if (s != SGEMM_OK) return s;
   if (plan.workspace_bytes > 0) {
     if (!workspace) return -14;
@@ -506,14 +530,16 @@ int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float 
   Problem pr;
   int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
   if (s != SGEMM_OK) return s;
+  int pair_clusters = 0;
   if (sm_count <= 0) {
     int dev;
     DeviceState* st;
     s = device_state(&dev, &st);
     if (s != SGEMM_OK) return s;
     sm_count = st->sm_count;
+    pair_clusters = st->pair_clusters;
   }
-  return make_plan(pr, sm_count, plan);
+  return make_plan(pr, sm_count, plan, pair_clusters);
 }
 
 int sgemm_strided_batched(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
@@ -531,7 +557,7 @@ int sgemm_strided_batched(char transA, char transB, int64_t M, int64_t N, int64_
   s = device_state(&dev, &st);
   if (s != SGEMM_OK) return s;
   sgemm_plan_t plan;
-  s = make_plan(pr, st->sm_count, &plan);
+  s = make_plan(pr, st->sm_count, &plan, st->pair_clusters);
   if (s != SGEMM_OK) return s;
   return launch_gemm(pr, plan, *st, C, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -546,20 +572,22 @@ int sgemm_plan_strided_batched(char transA, char transB, int64_t M, int64_t N, i
   if (s != SGEMM_OK) return s;
   s = validate_batch(strideA, strideB, strideC, batch_count, &pr);
   if (s != SGEMM_OK) return s;
+  int pair_clusters = 0;
   if (sm_count <= 0) {
     int dev;
     DeviceState* st;
     s = device_state(&dev, &st);
     if (s != SGEMM_OK) return s;
     sm_count = st->sm_count;
+    pair_clusters = st->pair_clusters;
   }
-  return make_plan(pr, sm_count, plan);
+  return make_plan(pr, sm_count, plan, pair_clusters);
 }
 
 int sgemm_set_variant_override(int variant, int split_k) {
   if (variant != SGEMM_VARIANT_AUTO && variant != SGEMM_VARIANT_GENERIC && variant != SGEMM_VARIANT_TMA_128x128 &&
       variant != SGEMM_VARIANT_TMA_64x256 && variant != SGEMM_VARIANT_TC_TF32X3 && variant != SGEMM_VARIANT_SMALL &&
-      variant != SGEMM_VARIANT_TC_GROUPED)
+      variant != SGEMM_VARIANT_TC_GROUPED && variant != SGEMM_VARIANT_TC_PAIR)
     return -1;
   g_override_variant.store(variant);
   g_override_split.store(split_k < 0 ? 0 : split_k);

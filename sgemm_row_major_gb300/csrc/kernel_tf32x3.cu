@@ -67,8 +67,7 @@
 //
 // TMEM columns: [128 b, +128) accumulator b (b < 3); [384 + 64 s, +32) A hi
 // and [416 + 64 s, +32) A lo of split stage s (s < 2).
-#include "device_utils.cuh"
-#include "sgemm_internal.h"
+#include "kernel_tc_common.cuh"
 
 namespace sgemm_impl {
 namespace tc {
@@ -114,18 +113,6 @@ constexpr uint32_t kIdesc = (1u << 4)                 // D format: F32
                           | ((uint32_t)(BN >> 3) << 17)
                           | ((uint32_t)(BM >> 4) << 24);
 
-// Shared-memory matrix descriptor of a K-major tile with the 128-byte swizzle:
-// rows of 128 bytes (32 TF32 values of K), 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t smem_byte_addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((smem_byte_addr & 0x3FFFFu) >> 4);  // start address
-  d |= (uint64_t)(16u >> 4) << 16;                    // leading byte offset (unused: K fits one atom)
-  d |= (uint64_t)(1024u >> 4) << 32;                  // stride byte offset: next 8 rows
-  d |= (uint64_t)1 << 46;                             // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;                             // 128-byte swizzle
-  return d;
-}
-
 // D (TMEM) = or += A (TMEM, 128 lanes x 8 columns) * B (shared memory, descriptor)
 __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t accumulate) {
   asm volatile(
@@ -136,48 +123,10 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-// Warp-level bounded wait: lane 0 polls, then every lane confirms the phase
-// (an immediate success) so each thread has its own acquire.  Warp-uniform.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
-  const int lane = threadIdx.x & 31;
-  bool ok = true;
-  if (lane == 0) ok = mbar_wait(bar, parity, timeout_ns);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  if (ok) ok = mbar_wait(bar, parity, timeout_ns);
-  return __all_sync(0xffffffffu, ok);
-}
-
 // Arrives on `bar` once every tcgen05.mma this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
-}
-
-// x rounded to TF32 (10 explicit mantissa bits), to nearest with ties away
-// from zero: add half of the dropped range to the magnitude bits, then clear
-// them (a carry into the exponent is the correct rounding).
-__device__ __forceinline__ float tf32_round(float x) {
-  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
-}
-
-__device__ __forceinline__ void split4(const float4 x, float4& hi, float4& lo) {
-  hi = make_float4(tf32_round(x.x), tf32_round(x.y), tf32_round(x.z), tf32_round(x.w));
-  // lo = x - hi (exact), two at a time: fma(hi, -1, x) rounds an exact value
-  const float2 m1 = make_float2(-1.0f, -1.0f);
-  const float2 l01 = __ffma2_rn(make_float2(hi.x, hi.y), m1, make_float2(x.x, x.y));
-  const float2 l23 = __ffma2_rn(make_float2(hi.z, hi.w), m1, make_float2(x.z, x.w));
-  lo = make_float4(l01.x, l01.y, l23.x, l23.y);
-}
-
-__device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, int& tm, int& tn) {
-  constexpr int kGroupM = 8;
-  const int span = kGroupM * tiles_n;
-  const int group = bid / span;
-  const int first = group * kGroupM;
-  const int rows = min(tiles_m - first, kGroupM);
-  const int local = bid - group * span;
-  tm = first + local % rows;
-  tn = local / rows;
 }
 
 // Product and origin of output tile `tile` (numbered over all products).
@@ -188,63 +137,6 @@ __device__ __forceinline__ void tile_origin(const GemmParams& p, int tile, int& 
   tile_coords(tile - prod * tiles, p.tiles_m, p.tiles_n, tm, tn);
   m0 = tm * BM;
   n0 = tn * BN;
-}
-
-// First stream-K iteration of CTA c: floor(c * I / G).
-__device__ __forceinline__ int64_t sk_bound(const GemmParams& p, int c) {
-  return (int64_t)c * p.sk_iters / p.sk_grid;
-}
-
-// The CTA whose stream-K range holds iteration i: the largest c with B(c) <= i.
-__device__ __forceinline__ int sk_owner(const GemmParams& p, int64_t i) {
-  return (int)(((i + 1) * p.sk_grid + p.sk_iters - 1) / p.sk_iters - 1);
-}
-
-// Partial-sum slot of CTA c for stream-K tile j (relative to the first stream-K tile).
-__device__ __forceinline__ int sk_slot(const GemmParams& p, int c, int j, int kt) {
-  return (int)(sk_bound(p, c) / kt) == j ? 2 * c : 2 * c + 1;
-}
-
-// A CTA's work: `dp` whole tiles (c, c+G, ... below sk_tile0), then stream-K
-// iterations [b, e) covering relative stream-K tiles j0 .. j0 + nseg - dp - 1.
-struct CtaWork {
-  int dp, j0, nseg, units;
-  int64_t b, e;
-};
-
-__device__ __forceinline__ CtaWork cta_work(const GemmParams& p, int c, int kt) {
-  CtaWork w;
-  w.dp = c < p.sk_tile0 ? (p.sk_tile0 - c + p.sk_grid - 1) / p.sk_grid : 0;
-  w.b = p.sk_iters > 0 ? sk_bound(p, c) : 0;
-  w.e = p.sk_iters > 0 ? sk_bound(p, c + 1) : 0;
-  w.j0 = (int)(w.b / kt);
-  w.nseg = w.dp + (w.e > w.b ? (int)((w.e - 1) / kt) - w.j0 + 1 : 0);
-  w.units = w.dp * kt + (int)(w.e - w.b);
-  return w;
-}
-
-// Segment s of a CTA's work: K tiles [kb, ke) of output tile `tile`; slot -1
-// when the segment is the tile's whole K range (result goes to C).
-struct Segment {
-  int tile, kb, ke, slot;
-};
-
-__device__ __forceinline__ Segment cta_segment(const GemmParams& p, const CtaWork& w, int c, int s, int kt) {
-  Segment g;
-  if (s < w.dp) {
-    g.tile = s * p.sk_grid + c;
-    g.kb = 0;
-    g.ke = kt;
-    g.slot = -1;
-  } else {
-    const int j = w.j0 + (s - w.dp);
-    const int64_t t0 = (int64_t)j * kt;
-    g.tile = p.sk_tile0 + j;
-    g.kb = (int)(max(w.b, t0) - t0);
-    g.ke = (int)(min(w.e, t0 + kt) - t0);
-    g.slot = (g.kb == 0 && g.ke == kt) ? -1 : sk_slot(p, c, j, kt);
-  }
-  return g;
 }
 
 // Raw tile layouts (as the TMA engine copies them):

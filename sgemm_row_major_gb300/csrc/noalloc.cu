@@ -60,6 +60,7 @@ cudaError_t setup(int dev, NoallocDevice** out) {
     if (e == cudaSuccess) e = prepare_tma_op_tt();
     if (e == cudaSuccess) e = prepare_tf32x3();
     if (e == cudaSuccess) e = prepare_small_gemm();
+    if (e == cudaSuccess) e = prepare_tc_pair();
     d.err = e;
   });
   *out = &d;
@@ -127,19 +128,26 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
     e = launch_small_gemm(ta, tb, p, (int)plan.grid_x, cs);
   } else {
     CUtensorMap mapA, mapB;
-    e = encode_operand_maps(ta, tb, M, N, K, A, lda, 0, B, ldb, 0, 1, plan.tile_m, plan.tile_n, plan.tile_k, &mapA,
-                            &mapB, &p.za, &p.zb);
+    int box_m, box_n;
+    operand_boxes(plan, &box_m, &box_n);
+    e = encode_operand_maps(ta, tb, M, N, K, A, lda, 0, B, ldb, 0, 1, box_m, box_n, plan.tile_k, &mapA, &mapB, &p.za,
+                            &p.zb);
     if (e != cudaSuccess) return SGEMM_ERR_CUDA;
     const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
     if (plan.variant == SGEMM_VARIANT_TC_TF32X3 || plan.variant == SGEMM_VARIANT_TC_GROUPED) {
       e = launch_tf32x3(ta, tb, plan.variant == SGEMM_VARIANT_TC_GROUPED ? 128 / plan.tile_m : 1, mapA, mapB, p,
                         cs);
       if (e == cudaSuccess && plan.kernel_launches > 1) e = launch_streamk_fixup(p, (int)plan.sk_tiles, cs);
+    } else if (plan.variant == SGEMM_VARIANT_TC_PAIR) {
+      e = launch_tc_pair(ta, tb, mapA, mapB, p, cs);
+      if (e == cudaSuccess && plan.kernel_launches > 1) e = launch_pair_fixup(p, (int)plan.sk_tiles, cs);
     } else if (!ta && !tb) e = launch_tma_op_nn(tile, mapA, mapB, p, split, cs);
     else if (!ta && tb) e = launch_tma_op_nt(tile, mapA, mapB, p, split, cs);
     else if (ta && !tb) e = launch_tma_op_tn(tile, mapA, mapB, p, split, cs);
     else e = launch_tma_op_tt(tile, mapA, mapB, p, split, cs);
   }
-  if (e == cudaSuccess && split > 1 && plan.variant != SGEMM_VARIANT_TC_TF32X3) e = launch_splitk_reduce(p, split, cs);
+  if (e == cudaSuccess && split > 1 && plan.variant != SGEMM_VARIANT_TC_TF32X3 &&
+      plan.variant != SGEMM_VARIANT_TC_PAIR)
+    e = launch_splitk_reduce(p, split, cs);
   return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
 }

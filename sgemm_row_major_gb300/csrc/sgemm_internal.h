@@ -49,12 +49,24 @@ cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t 
                                 int64_t stride_a, const float* B, int64_t ldb, int64_t stride_b, int batch,
                                 int bm, int bn, int bk, CUtensorMap* mapA, CUtensorMap* mapB, int* za, int* zb);
 
-// Copies the tensor-core kernel's schedule from a plan (no-op for other variants).
+// Copies the tensor-core kernel's schedule from a plan (no-op for other
+// variants); the pair kernel's scheduling unit is the cluster of 2 CTAs.
 inline void set_schedule(const sgemm_plan_t& plan, GemmParams* p) {
-  if (plan.variant != SGEMM_VARIANT_TC_TF32X3 && plan.variant != SGEMM_VARIANT_TC_GROUPED) return;
-  p->sk_grid = (int)plan.grid_x;
+  if (plan.variant != SGEMM_VARIANT_TC_TF32X3 && plan.variant != SGEMM_VARIANT_TC_GROUPED &&
+      plan.variant != SGEMM_VARIANT_TC_PAIR)
+    return;
+  p->sk_grid = (int)(plan.variant == SGEMM_VARIANT_TC_PAIR ? plan.grid_x / 2 : plan.grid_x);
   p->sk_iters = plan.sk_iters;
   p->sk_tile0 = (int)plan.dp_tiles;
+}
+
+// TMA box extents one CTA of a plan loads per K tile: rows of op(A) and
+// columns of op(B) (a CTA of a pair covers half of the tile's rows and loads
+// half of its B columns).
+inline void operand_boxes(const sgemm_plan_t& plan, int* bm, int* bn) {
+  const bool pair = plan.variant == SGEMM_VARIANT_TC_PAIR;
+  *bm = pair ? plan.tile_m / 2 : plan.tile_m;
+  *bn = pair ? plan.tile_n / 2 : plan.tile_n;
 }
 
 // Shapes of the TMA-fed SIMT kernel.
@@ -86,6 +98,14 @@ cudaError_t prepare_tf32x3();
 cudaError_t launch_tf32x3(bool transA, bool transB, int group, const CUtensorMap& mapA, const CUtensorMap& mapB,
                           const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_streamk_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
+// 3xTF32 on CTA pairs (kernel_tc_pair.cu): 256x128x32 tiles, clusters of 2,
+// p.sk_grid clusters, the schedule of the one-CTA kernel over pair tiles;
+// then the fixup over the sk_tiles stream-K pair tiles when any is shared.
+cudaError_t prepare_tc_pair();
+cudaError_t tc_pair_max_clusters(int* clusters);  // co-resident clusters of the pair kernel on this device
+cudaError_t launch_tc_pair(bool transA, bool transB, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                           const GemmParams& p, cudaStream_t stream);
+cudaError_t launch_pair_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
 cudaError_t launch_generic_gemm(bool transA, bool transB, const GemmParams& p, int split,
                                 cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const GemmParams& p, int split, cudaStream_t stream);
