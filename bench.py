@@ -41,7 +41,8 @@ UNIT = "TFLOPS"
 FMA_PER_SM_PER_CLK = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
 # committed ncu summaries by (kernel variant, workload): their per-launch DRAM traffic is reported
 # while the kernel's source digest still matches the one they were captured with
-PROFILES = {("TC_TF32X3", "square4096"): os.path.join(ROOT, "profiles", "tf32x3_gemm_square4096.md"),
+PROFILES = {("TC_PAIR", "square4096"): os.path.join(ROOT, "profiles", "tc_pair_gemm_square4096.md"),
+            ("TC_TF32X3", "square4096"): os.path.join(ROOT, "profiles", "tf32x3_gemm_square4096.md"),
             ("TMA_128x128", "square4096"): os.path.join(ROOT, "profiles", "tma_gemm_square4096.md"),
             ("SMALL", "batched_small_8192x64x64x64"):
                 os.path.join(ROOT, "profiles", "small_gemm_batched8192x64x64x64.md"),
@@ -386,8 +387,19 @@ def l2_note(flush):
             "two input sets used in turn, each larger than the 129 MB L2; no flush")
 
 
-def tensor_roofline(achieved, peaks, traffic, kernel_ms):
-    """Roofline object of the 3xTF32 tensor-core kernel (see the module docstring of the kernel)."""
+def kernel_digest(lib_build, variant):
+    """Source digest of the kernel a variant runs (matches the digest in its committed profile)."""
+    if variant == "TC_PAIR":
+        return lib_build.pair_kernel_digest()
+    if variant in ("TC_TF32X3", "TC_GROUPED"):
+        return lib_build.tc_kernel_digest()
+    if variant == "SMALL":
+        return lib_build.small_kernel_digest()
+    return lib_build.tma_kernel_digest()
+
+
+def tensor_roofline(achieved, peaks, traffic, kernel_ms, variant="TC_TF32X3"):
+    """Roofline object of the 3xTF32 tensor-core kernels (see the module docstrings of the kernels)."""
     bf16 = peaks.get("bf16_tflops")
     basis = "measured" if bf16 else "fallback"
     bf16 = bf16 or 1900.0
@@ -397,7 +409,9 @@ def tensor_roofline(achieved, peaks, traffic, kernel_ms):
             "peak_basis": f"{basis} bf16 burst {bf16:.0f} TFLOP/s x nominal tf32/bf16 "
                           f"{NOMINAL_TF32_PF}/{NOMINAL_BF16_PF} = {tf32:.0f} TFLOP/s of tf32, / {TF32_PRODUCTS} "
                           f"tensor products per SGEMM FMA (3xTF32 split); achieved counts 2MNK only",
-            "kernel": "tf32x3_gemm_kernel (tcgen05.mma kind::tf32, 3xTF32 split)", "kernel_ms": kernel_ms,
+            "kernel": ("pair_gemm_kernel (tcgen05.mma cta_group::2 kind::tf32, 3xTF32 split, 256x128 tiles "
+                       "on CTA pairs)" if variant == "TC_PAIR" else
+                       "tf32x3_gemm_kernel (tcgen05.mma kind::tf32, 3xTF32 split)"), "kernel_ms": kernel_ms,
             "kernel_ms_covers": "one sgemm() call: the GEMM kernel and, when stream-K tiles are shared, "
                                 "the fixup kernel after it (about 2% of the step in the ncu launch list)"}
 
@@ -487,10 +501,10 @@ def run_ours(args):
     max_mhz = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
     ffma_peak = sms * FMA_PER_SM_PER_CLK * 2 * max_mhz * 1e6 / 1e12
     variant = plan["variant_name"]
-    if variant == "TC_TF32X3":
+    if variant in ("TC_TF32X3", "TC_PAIR"):
         roof = tensor_roofline(achieved, peaks,
-                               traffic_from_profile(variant, case.name, lib_build.tc_kernel_digest()),
-                               kernel_ms)
+                               traffic_from_profile(variant, case.name, kernel_digest(lib_build, variant)),
+                               kernel_ms, variant)
     else:
         roof = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
                 "frac": achieved / ffma_peak,
@@ -594,9 +608,9 @@ def batched_roofline(c, plan, flops_step, achieved, kernel_ms, peaks, dev, lib_b
     """Roofline object of the kernel a strided batch ran on.  For the tensor-core kernel the bound is
     whichever of the 3xTF32 tensor peak and HBM takes longer for the call's algorithmic work."""
     variant = plan["variant_name"]
-    if variant in ("TC_TF32X3", "TC_GROUPED"):
-        traffic = traffic_from_profile(variant, c.name, lib_build.tc_kernel_digest())
-        roof = tensor_roofline(achieved, peaks, traffic, kernel_ms)
+    if variant in ("TC_TF32X3", "TC_GROUPED", "TC_PAIR"):
+        traffic = traffic_from_profile(variant, c.name, kernel_digest(lib_build, variant))
+        roof = tensor_roofline(achieved, peaks, traffic, kernel_ms, variant)
         if variant == "TC_GROUPED":
             group = 128 // plan["tile_m"]
             tiles = (c.batch + group - 1) // group

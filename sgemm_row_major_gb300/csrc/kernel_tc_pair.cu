@@ -258,23 +258,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1 || warp == kSecondMmaWarp) {
     // ------------------------------------------------ MMA issuers (even CTA; tile t goes to issuer t % 2)
     const int issuer = warp == 1 ? 0 : 1;
-    if (rank == 0 && lane == 0) {
+    if (rank == 0 && lane == 0 && issuer < kIssuers) {
       int done = -1;
       bool ok = true;
       for (int t = issuer; ok && t < nkt; t += kIssuers) {
         const int b = t % kAccBufs;
-        if (t >= kAccBufs &&
-            !mbar_wait(smem_addr(&acc_empty[b]), (uint32_t)((t / kAccBufs) - 1) & 1u, p.timeout_ns)) {
-          ok = false;
-          break;
-        }
         const uint32_t acc = tmem + (uint32_t)b * kAccCols;
         const int s = t % kSplitStages;
         const uint32_t ahi = tmem + kAColBase + (uint32_t)s * kACols, alo = ahi + 32u;
         const uint64_t bhi = kmajor_sw128_desc(split_tile(s, 0)), blo = kmajor_sw128_desc(split_tile(s, 1));
+        // The accumulator is taken only once the tile's first operands are split: an accumulator
+        // held while its issuer waits for split data lengthens the loop MMA -> fold -> MMA that
+        // the three accumulators have to cover.
 #pragma unroll
         for (int h = 0; h < kHalves; ++h) {
           if (!mbar_wait(smem_addr(&split_full[s][h]), (uint32_t)(t / kSplitStages) & 1u, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          if (h == 0 && t >= kAccBufs &&
+              !mbar_wait(smem_addr(&acc_empty[b]), (uint32_t)((t / kAccBufs) - 1) & 1u, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -307,19 +310,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int t = 0;
     for (; t < nkt; ++t) {
       const int r = t % kRawStages, s = t % kSplitStages;
-      bool w = warp_wait(smem_addr(&raw_full[r]), (uint32_t)(t / kRawStages) & 1u, p.timeout_ns);
-      if (w && t >= kSplitStages)
-        w = warp_wait(smem_addr(&split_empty[s][half]), (uint32_t)((t / kSplitStages) - 1) & 1u, p.timeout_ns);
-      if (!w) {
+      if (!warp_wait(smem_addr(&raw_full[r]), (uint32_t)(t / kRawStages) & 1u, p.timeout_ns)) {
         if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
         break;
       }
-      tmem_fence_after_sync();
+      // Load and split into registers first; only the stores wait for the split stage, so the
+      // loads and the split arithmetic stay off the loop MMA completion -> split stage -> MMA.
       // A: this thread takes row m = 32q + lane (its TMEM lane) and k = 16*half .. +15.
+      float hi[16], lo[16];
       {
         const uint8_t* ra = smem + (raw_a(r) - sbase);
         const int m = 32 * q + lane;
-        float hi[16], lo[16];
         if (!TA) {
           // K-contiguous rows, 128-byte swizzle: chunk c of row m sits at c ^ (m & 7)
 #pragma unroll
@@ -341,42 +342,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             lo[j] = x - hi[j];
           }
         }
-        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kAColBase + (uint32_t)s * kACols + 16u * half;
-        tmem_st16(ta, hi);
-        tmem_st16(ta + 32u, lo);
       }
       // B -> K-major [64 n][32 k], 128-byte swizzle, the layout the descriptors describe; thread st
       // takes column n = st % 64 and the two 4-k chunks 4*half + 2*((st / 64) % 2) + {0, 1}.
+      const int n = st & 63, kp = (st >> 6) & 1;
+      float4 bh[2], bl[2];
+      if (!TB) {
+        // raw [32 k][64 n]: transpose on the way (a warp reads 32 adjacent n of one k)
+        const float* rb = reinterpret_cast<const float*>(smem + (raw_b(r) - sbase));
+#pragma unroll
+        for (int kq = 0; kq < 2; ++kq) {
+          const int kc = 4 * half + 2 * kp + kq;
+          const float4 x = make_float4(rb[(4 * kc + 0) * BNC + n], rb[(4 * kc + 1) * BNC + n],
+                                       rb[(4 * kc + 2) * BNC + n], rb[(4 * kc + 3) * BNC + n]);
+          split4(x, bh[kq], bl[kq]);
+        }
+      } else {
+        // raw is already K-major and swizzled: the chunks keep their place
+        const uint8_t* rb = smem + (raw_b(r) - sbase);
+#pragma unroll
+        for (int kq = 0; kq < 2; ++kq) {
+          const int kc = 4 * half + 2 * kp + kq;
+          const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(kc ^ (n & 7)) << 4);
+          split4(*reinterpret_cast<const float4*>(rb + off), bh[kq], bl[kq]);
+        }
+      }
+      if (t >= kSplitStages &&
+          !warp_wait(smem_addr(&split_empty[s][half]), (uint32_t)((t / kSplitStages) - 1) & 1u, p.timeout_ns)) {
+        if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
+        break;
+      }
+      tmem_fence_after_sync();
       {
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kAColBase + (uint32_t)s * kACols + 16u * half;
+        tmem_st16(ta, hi);
+        tmem_st16(ta + 32u, lo);
         uint8_t* bhi = smem + (split_tile(s, 0) - sbase);
         uint8_t* blo = smem + (split_tile(s, 1) - sbase);
-        const int n = st & 63, kp = (st >> 6) & 1;
-        if (!TB) {
-          // raw [32 k][64 n]: transpose on the way (a warp reads 32 adjacent n of one k)
-          const float* rb = reinterpret_cast<const float*>(smem + (raw_b(r) - sbase));
 #pragma unroll
-          for (int kq = 0; kq < 2; ++kq) {
-            const int kc = 4 * half + 2 * kp + kq;
-            const float4 x = make_float4(rb[(4 * kc + 0) * BNC + n], rb[(4 * kc + 1) * BNC + n],
-                                         rb[(4 * kc + 2) * BNC + n], rb[(4 * kc + 3) * BNC + n]);
-            float4 hi, lo;
-            split4(x, hi, lo);
-            const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(kc ^ (n & 7)) << 4);
-            *reinterpret_cast<float4*>(bhi + off) = hi;
-            *reinterpret_cast<float4*>(blo + off) = lo;
-          }
-        } else {
-          // raw is already K-major and swizzled: split the chunks in place
-          const uint8_t* rb = smem + (raw_b(r) - sbase);
-#pragma unroll
-          for (int kq = 0; kq < 2; ++kq) {
-            const int kc = 4 * half + 2 * kp + kq;
-            const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(kc ^ (n & 7)) << 4);
-            float4 hi, lo;
-            split4(*reinterpret_cast<const float4*>(rb + off), hi, lo);
-            *reinterpret_cast<float4*>(bhi + off) = hi;
-            *reinterpret_cast<float4*>(blo + off) = lo;
-          }
+        for (int kq = 0; kq < 2; ++kq) {
+          const int kc = 4 * half + 2 * kp + kq;
+          const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(kc ^ (n & 7)) << 4);
+          *reinterpret_cast<float4*>(bhi + off) = bh[kq];
+          *reinterpret_cast<float4*>(blo + off) = bl[kq];
         }
       }
       tmem_wait_st();            // A parts have reached TMEM
@@ -420,23 +428,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
           break;
         }
-        {
-          tmem_fence_after_sync();
-          float v[4][16];
+        tmem_fence_after_sync();
+        float v[4][16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld16(tq + (uint32_t)b * kAccCols + 16u * c, v[c]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld_ready(v[c]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)  // round-to-nearest FP32 adds, two per instruction
-              master2[8 * c + e] = __fadd2_rn(master2[8 * c + e], make_float2(v[c][2 * e], v[c][2 * e + 1]));
-          }
-          tmem_fence_before_sync();
-        }
+        for (int c = 0; c < 4; ++c) tmem_ld16(tq + (uint32_t)b * kAccCols + 16u * c, v[c]);
+        tmem_wait_ld();
+        // the accumulator is in registers: hand it back to the issuer before adding
+        tmem_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(smem_addr(&acc_empty[b]), 0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld_ready(v[c]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)  // round-to-nearest FP32 adds, two per instruction
+            master2[8 * c + e] = __fadd2_rn(master2[8 * c + e], make_float2(v[c][2 * e], v[c][2 * e + 1]));
+        }
       }
       if (!ok) break;
       // epilogue of this segment: this thread holds row 32q + lane of the CTA's 128 rows, columns

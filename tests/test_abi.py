@@ -106,9 +106,15 @@ def test_planner_variants(lib):
     assert plan("N", "N", 0, 10, 10)["variant_name"] == "NONE"
     assert plan("N", "N", 10, 10, 0)["variant_name"] == "SCALE"
     big = plan("N", "N", 4096, 4096, 4096)
-    assert big["variant_name"] == "TC_TF32X3" and big["grid_x"] == 152 and big["grid_y"] == 1
-    assert big["tile_m"] == big["tile_n"] == 128 and big["tile_k"] == 32 and big["threads"] == 608
+    assert big["variant_name"] == "TC_PAIR" and big["grid_x"] == 152 and big["grid_y"] == 1
+    assert (big["tile_m"], big["tile_n"], big["tile_k"], big["threads"]) == (256, 128, 32, 608)
     assert big["smem_bytes"] <= 227 * 1024
+    # fewer pair tiles than clusters (1024^3: 32 < 76), or M <= 128: one CTA per 128 x 128 tile
+    one = plan("N", "N", 1024, 1024, 1024)
+    assert one["variant_name"] == "TC_TF32X3" and one["tile_m"] == one["tile_n"] == 128
+    assert plan("N", "N", 128, 65536, 1024)["variant_name"] == "TC_TF32X3"
+    assert plan("N", "N", 129, 128 * 76, 64)["variant_name"] == "TC_PAIR"
+    assert plan("N", "N", 129, 128 * 75, 64)["variant_name"] == "TC_TF32X3"
     # unaligned base or ld not a multiple of 4 -> the generic (edge) kernel
     assert plan("N", "N", 512, 512, 512, A=FAKE_ODD)["variant_name"] == "GENERIC"
     assert plan("N", "N", 512, 512, 513, lda=515)["variant_name"] == "GENERIC"
@@ -116,7 +122,7 @@ def test_planner_variants(lib):
     # ragged padded shapes of the transpose sweep keep the TMA-fed path (ld % 4 == 0)
     for ta, tb, lda, ldb in (("N", "N", 2060, 3008), ("N", "T", 2060, 2060), ("T", "N", 4104, 3008),
                              ("T", "T", 4104, 2060)):
-        assert plan(ta, tb, 4097, 3001, 2053, lda=lda, ldb=ldb)["variant_name"] == "TC_TF32X3"
+        assert plan(ta, tb, 4097, 3001, 2053, lda=lda, ldb=ldb)["variant_name"] == "TC_PAIR"
 
 
 def test_planner_split_k(lib):
@@ -142,7 +148,15 @@ def test_planner_split_k(lib):
 
 
 def test_planner_stream_k(lib):
-    """The tensor-core kernel's persistent schedule: whole-tile rounds, then stream-K."""
+    """The one-CTA tensor-core kernel's persistent schedule: whole-tile rounds, then stream-K."""
+    sg.sgemm_set_variant_override("TC_TF32X3", 0)
+    try:
+        _one_cta_schedules()
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
+
+
+def _one_cta_schedules():
     # 4096^3: 1024 tiles on 152 SMs = 6.74 rounds -> 760 whole tiles, then 264 stream-K tiles
     p = plan("N", "N", 4096, 4096, 4096)
     assert (p["grid_x"], p["grid_y"], p["dp_tiles"], p["sk_tiles"]) == (152, 1, 760, 264)
@@ -169,7 +183,7 @@ def test_planner_stream_k(lib):
     assert (o["grid_x"], o["kernel_launches"], o["workspace_bytes"]) == (1, 1, 0)
     # a forced split: S CTAs per tile
     try:
-        sg.sgemm_set_variant_override("AUTO", 5)
+        sg.sgemm_set_variant_override("TC_TF32X3", 5)
         f = plan("N", "N", 150, 260, 1000)
         assert f["grid_x"] == 6 * 5 and f["dp_tiles"] == 0 and f["split_k"] >= 5
     finally:
@@ -189,7 +203,7 @@ def test_variant_override(lib):
             sg.sgemm_set_variant_override(99, 0)
     finally:
         sg.sgemm_set_variant_override("AUTO", 0)
-    assert plan("N", "N", 4096, 4096, 4096)["variant_name"] == "TC_TF32X3"
+    assert plan("N", "N", 4096, 4096, 4096)["variant_name"] == "TC_PAIR"
 
 
 def test_plan_rejects_huge_dimensions(lib):
@@ -207,12 +221,14 @@ def bplan(ta, tb, M, N, K, batch, sA, sB, sC, lda=None, ldb=None, ldc=None, A=FA
 
 
 def test_batched_planner(lib):
-    # 64 FC products of 512x1024x1024: 32 tiles each, one persistent launch over all 2048 tiles
+    # 64 FC products of 512x1024x1024: 16 pair tiles each, one persistent launch of 76 clusters over
+    # all 1024 pair tiles
     p = bplan("N", "N", 512, 1024, 1024, 64, 512 * 1024, 1024 * 1024, 512 * 1024)
-    assert p["variant_name"] == "TC_TF32X3" and p["grid_x"] == 152
-    assert p["dp_tiles"] + p["sk_tiles"] == 64 * 32 and p["sk_tiles"] == 152 + 64 * 32 % 152
+    assert p["variant_name"] == "TC_PAIR" and p["grid_x"] == 152
+    assert p["dp_tiles"] + p["sk_tiles"] == 64 * 16 and p["sk_tiles"] == 76 + 64 * 16 % 76
     # shared weight (stride 0) keeps the tensor-core path
-    assert bplan("N", "N", 512, 1024, 1024, 8, 512 * 1024, 0, 512 * 1024)["variant_name"] == "TC_TF32X3"
+    assert bplan("N", "N", 512, 1024, 1024, 8, 512 * 1024, 0, 512 * 1024)["variant_name"] == "TC_PAIR"
+    assert bplan("N", "N", 512, 1024, 1024, 4, 512 * 1024, 0, 512 * 1024)["variant_name"] == "TC_TF32X3"
     # few tiles in all: stream-K over the tiles of every product
     s = bplan("N", "N", 64, 4096, 16384, 2, 64 * 16384, 0, 64 * 4096)
     assert s["grid_x"] == 152 and s["sk_tiles"] == 64 and s["split_k"] > 1

@@ -22,7 +22,7 @@ def _ints(torch, shape, seed):
     return torch.randint(-2, 3, shape, generator=g, device="cuda", dtype=torch.int32).to(torch.float32)
 
 
-@pytest.mark.parametrize("variant", [None, "GENERIC", "TMA_128x128"])
+@pytest.mark.parametrize("variant", [None, "TC_TF32X3", "GENERIC", "TMA_128x128"])
 def test_c_larger_than_2g_elements(variant):
     torch = torch_cuda()
     M, N, K = 70000, 32772, 32
@@ -46,16 +46,23 @@ def test_c_larger_than_2g_elements(variant):
     del dC
 
 
-def test_strided_batch_offsets_beyond_2g():
+@pytest.mark.parametrize("variant,expect", [(None, "TC_PAIR"), ("TC_TF32X3", "TC_TF32X3")])
+def test_strided_batch_offsets_beyond_2g(variant, expect):
     torch = torch_cuda()
     batch, M, N, K = 3000, 1024, 1024, 32
     assert batch * M * N > TWO31
     dA = _ints(torch, (batch, M, K), 93)
     dB = _ints(torch, (K, N), 94)  # shared by every product (stride 0)
     dC = torch.empty((batch, M, N), dtype=torch.float32, device="cuda")
-    assert sg.sgemm_plan_strided_batched("N", "N", M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N, M * K, 0, M * N,
-                                         batch)["variant_name"] == "TC_TF32X3"
-    sg.sgemm_strided_batched("N", "N", M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N, M * K, 0, M * N, batch)
+    if variant:
+        sg.sgemm_set_variant_override(variant, 0)
+    try:
+        assert sg.sgemm_plan_strided_batched("N", "N", M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N, M * K, 0, M * N,
+                                             batch)["variant_name"] == expect
+        sg.sgemm_strided_batched("N", "N", M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N, M * K, 0, M * N, batch)
+    finally:
+        if variant:
+            sg.sgemm_set_variant_override("AUTO", 0)
     assert sg.sgemm_sync_status() == 0
     first = TWO31 // (M * N)  # the first product whose offset passes 2^31
     B = dB.cpu().numpy()

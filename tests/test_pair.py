@@ -68,6 +68,46 @@ def test_plan_shape():
     assert p["workspace_bytes"] == 2 * 152 * 128 * 128 * 4
 
 
+SCHEDULES = [
+    (256 * 19, 512, 64, 0, "whole rounds"),            # 76 pair tiles: 1 round on 76 clusters
+    (256 * 20, 512, 64, 0, "ragged rounds"),           # 80 tiles, short K: ragged whole rounds
+    (256 * 39, 512, 2048, 0, "rounds + stream-K"),     # 156 tiles: 1 round + 80 stream-K tiles
+    (256, 256, 1216 * 32, 0, "stream-K on every cluster"),  # 2 tiles, 1216 K tiles each
+    (300, 260, 700, 0, "split per tile"),              # 6 tiles, short K: 5 clusters per tile
+    (256, 128, 8192, 64, "forced 64 per tile"),        # one tile shared by 64 clusters
+    (4, 4, 32, 0, "one tile one K tile"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,split,what", SCHEDULES, ids=[s[4] for s in SCHEDULES])
+def test_schedule_branches_exact(M, N, K, split, what):
+    """Every branch of the persistent schedule with clusters as the unit, on small integers (exact)."""
+    sg.sgemm_set_variant_override(V, split)
+    try:
+        p = sg.sgemm_plan("N", "N", M, N, K, 1.0, 1 << 20, K, 1 << 20, N, 0.5, 1 << 20, N, 152)
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
+    assert p["variant_name"] == V
+    if what == "whole rounds":
+        assert (p["dp_tiles"], p["sk_tiles"], p["kernel_launches"]) == (76, 0, 1)
+    elif what == "ragged rounds":
+        assert (p["dp_tiles"], p["sk_tiles"], p["kernel_launches"]) == (80, 0, 1)
+    elif what == "rounds + stream-K":
+        assert (p["dp_tiles"], p["sk_tiles"], p["kernel_launches"]) == (76, 80, 2)
+    elif what == "stream-K on every cluster":
+        assert (p["grid_x"], p["dp_tiles"], p["sk_tiles"]) == (152, 0, 2) and p["split_k"] >= 38
+    elif what == "split per tile":
+        assert (p["grid_x"], p["sk_tiles"]) == (2 * 6 * 5, 6)
+    elif what == "forced 64 per tile":
+        assert p["grid_x"] == 128 and p["split_k"] == 64
+    else:
+        assert (p["grid_x"], p["kernel_launches"], p["workspace_bytes"]) == (2, 1, 0)
+    rng = np.random.default_rng(M + N + K)
+    A, B, C = (rng.integers(-2, 3, size=s).astype(np.float32) for s in ((M, K), (K, N), (M, N)))
+    got = gpu_sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.5, C, N, variant=V, split=split)
+    check_exact(got, oracle.sgemm("N", "N", A, B, C, 1.0, 0.5), what)
+
+
 @pytest.mark.parametrize("name", [c.name for c in si.CASES])
 def test_config_parity(name):
     c = si.case(name)

@@ -1,4 +1,4 @@
-"""GPU tests of the tensor-core kernel's persistent schedule (whole-tile rounds + stream-K).
+"""GPU tests of the one-CTA tensor-core kernel's persistent schedule (whole-tile rounds + stream-K).
 
 Every branch of the planner is run on small-integer inputs (-2..2): their
 3xTF32 split is exact and every partial sum is an integer below 2^24, so the
@@ -26,14 +26,15 @@ def _case(seed, M, N, K):
     return _ints(rng, M, K), _ints(rng, K, N), _ints(rng, M, N)
 
 
+V = "TC_TF32X3"  # the CTA-pair kernel's schedule is tested in test_pair.py
+
+
 def _plan(M, N, K, split=0):
-    if split:
-        sg.sgemm_set_variant_override("AUTO", split)
+    sg.sgemm_set_variant_override(V, split)
     try:
         return sg.sgemm_plan("N", "N", M, N, K, 1.0, 1 << 20, K, 1 << 20, N, 0.5, 1 << 20, N)
     finally:
-        if split:
-            sg.sgemm_set_variant_override("AUTO", 0)
+        sg.sgemm_set_variant_override("AUTO", 0)
 
 
 # (M, N, K, forced split, what the plan must look like)
@@ -67,7 +68,7 @@ def test_schedule_branches_exact(M, N, K, split, what):
     else:
         assert (p["grid_x"], p["kernel_launches"], p["workspace_bytes"]) == (1, 1, 0)
     A, B, C = _case(M + N + K, M, N, K)
-    got = gpu_sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.5, C, N, split=split)
+    got = gpu_sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.5, C, N, variant=V, split=split)
     ref = oracle.sgemm("N", "N", A, B, C, 1.0, 0.5)
     check_exact(got, ref, what)
 
@@ -110,6 +111,7 @@ def test_stream_k_is_deterministic():
     B = (2 * rng.random((K, N)) - 1).astype(np.float32)
     C = np.zeros((M, N), np.float32)
     assert _plan(M, N, K)["split_k"] > 1
-    one = gpu_sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C, N)
-    two = gpu_sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C, N)
-    assert np.array_equal(one, two)
+    for v in (V, "TC_PAIR"):
+        one = gpu_sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C, N, variant=v)
+        two = gpu_sgemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C, N, variant=v)
+        assert np.array_equal(one, two), v
