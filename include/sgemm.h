@@ -87,8 +87,11 @@ enum sgemm_variant {
     SGEMM_VARIANT_SMALL = 7,      /* M, N <= 64 in a large batch: one CTA per product, FP32 FFMA */
     SGEMM_VARIANT_TC_GROUPED = 8, /* M, N <= 64 in a batch: 3xTF32 tensor cores, 2 (M, N <= 32: 4) products
                                      per 128x128 tile, block-diagonally; tile_m = tile_n = 128 / group */
-    SGEMM_VARIANT_TC_PAIR = 9     /* 3xTF32 tensor cores on CTA pairs (clusters of 2 on one TPC): 256x128x32
+    SGEMM_VARIANT_TC_PAIR = 9,    /* 3xTF32 tensor cores on CTA pairs (clusters of 2 on one TPC): 256x128x32
                                      tiles, each CTA 128 rows and half of the tile's B columns */
+    SGEMM_VARIANT_TC_PRESPLIT = 10 /* 3xTF32 with A and B split once per call into TF32 hi / FP32 lo arrays
+                                      (in the workspace), then CTA pairs on 256x256x32 tiles reading both
+                                      parts from shared memory */
 };
 
 /*

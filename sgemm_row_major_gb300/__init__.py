@@ -29,7 +29,8 @@ _LIB_PATH = os.path.join(_PKG, "_lib", "libsgemm.so")
 STATUS = {"OK": 0, "ERR_CUDA": 1, "ERR_TIMEOUT": 2, "ERR_NOMEM": 3, "ERR_UNSUPPORTED": 4, "ERR_SCRATCH_LIMIT": 5}
 NOALLOC_SCRATCH_BYTES = 32 << 20  # SGEMM_NOALLOC_SCRATCH_BYTES in include/sgemm.h
 VARIANTS = {"AUTO": 0, "NONE": 1, "SCALE": 2, "GENERIC": 3, "TMA_128x128": 4, "TMA_64x256": 5, "TC_TF32X3": 6,
-            "SMALL": 7, "TC_GROUPED": 8, "TC_PAIR": 9}
+            "SMALL": 7, "TC_GROUPED": 8, "TC_PAIR": 9,
+            "TC_PRESPLIT": 10}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 
 

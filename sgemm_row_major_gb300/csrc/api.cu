@@ -77,6 +77,7 @@ int device_state(int* device_out, DeviceState** st_out) {
     if (err == cudaSuccess) err = prepare_tf32x3();
     if (err == cudaSuccess) err = prepare_small_gemm();
     if (err == cudaSuccess) err = prepare_tc_pair();
+    if (err == cudaSuccess) err = prepare_presplit();
     if (err == cudaSuccess) err = tc_pair_max_clusters(&st.pair_clusters);
     if (err == cudaSuccess) {
       cudaMemPoolProps props = {};
@@ -234,10 +235,15 @@ int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
 // Shared memory per CTA of the CTA-pair kernel (kernel_tc_pair.cu: 6 raw
 // stages of 24 KB, 2 split stages of 16 KB, alignment slack).
 constexpr int64_t kPairSmemBytes = 6 * 24576 + 2 * 16384 + 1024;
+// ... and of the split-operand kernel (kernel_presplit.cu: 3 stages of A hi/lo and B hi/lo, 64 KB each).
+constexpr int64_t kPresplitSmemBytes = 3 * 65536 + 1024;
 
 // The planner: a pure function of the problem, the SM count, the number of
 // co-resident CTA-pair clusters (<= 0: sm_count / 2) and the override.
-int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clusters = 0) {
+// allow_presplit = false (sgemm_noalloc: the split arrays need workspace)
+// plans TC_PRESPLIT as TC_PAIR.
+int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clusters = 0,
+              bool allow_presplit = true) {
   *plan = sgemm_plan_t{};
   plan->split_k = 1;
   if (pr.M == 0 || pr.N == 0 || pr.batch == 0) {
@@ -294,6 +300,10 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   if (ov == SGEMM_VARIANT_SMALL) variant = small_ok ? ov : SGEMM_VARIANT_GENERIC;
   if (ov == SGEMM_VARIANT_TC_GROUPED) variant = group_ok ? ov : SGEMM_VARIANT_GENERIC;
   if (ov == SGEMM_VARIANT_TC_PAIR) variant = tma_ok ? ov : SGEMM_VARIANT_GENERIC;
+  // (the split pass's transposing grid: K / 32 and the products in grid dimensions y and z)
+  const bool presplit_ok = tma_ok && allow_presplit && ceil_div(pr.K, 32) <= 65535 && pr.batch <= 65535;
+  if (ov == SGEMM_VARIANT_TC_PRESPLIT)
+    variant = presplit_ok ? ov : tma_ok ? SGEMM_VARIANT_TC_PAIR : SGEMM_VARIANT_GENERIC;
   if (variant == SGEMM_VARIANT_TC_GROUPED) {
     // whole tiles (a group of products each) on one persistent CTA per SM, no stream-K
     const int64_t tiles = ceil_div(pr.batch, group);
@@ -334,6 +344,8 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
     bm = 128; bn = 128; bk = 32; threads = 608; stages = 4; smem = 4 * 32768 + 2 * 32768 + 1024;
   } else if (variant == SGEMM_VARIANT_TC_PAIR) {
     bm = 256; bn = 128; bk = 32; threads = 608; stages = 6; smem = kPairSmemBytes;
+  } else if (variant == SGEMM_VARIANT_TC_PRESPLIT) {
+    bm = 256; bn = 256; bk = 32; threads = 320; stages = 3; smem = kPresplitSmemBytes;
   } else if (variant == SGEMM_VARIANT_TMA_128x128) {
     using T = tma::Tile<4, 2>;
     bm = T::BM; bn = T::BN; bk = tma::kBK; threads = tma::kThreads; stages = tma::kStages; smem = T::SMEM_BYTES;
@@ -361,6 +373,18 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
     plan->workspace_bytes *= 2;
     return s;
   }
+  if (variant == SGEMM_VARIANT_TC_PRESPLIT) {
+    // as TC_PAIR with 256 x 256 tiles (slots of 128 x 256 floats per CTA), plus the split arrays;
+    // launches: the split pass of A and of B, the GEMM, the fixup when a tile is shared
+    const int s = plan_stream_k(tiles, kt, (int)clusters, plan);
+    if (s != SGEMM_OK) return s;
+    plan->grid_x *= 2;
+    plan->workspace_bytes *= 4;
+    plan->workspace_bytes =
+        split_layout(pr.M, pr.N, pr.K, pr.batch, pr.stride_a, pr.stride_b, plan->workspace_bytes).total();
+    plan->kernel_launches += 2;
+    return SGEMM_OK;
+  }
 
   // Split K only when the output tiles cannot fill the SMs, keeping at least
   // 4 K tiles per slice.
@@ -378,6 +402,36 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   plan->grid_y = split;
   plan->workspace_bytes = split > 1 ? pr.batch * split * pr.M * (ceil_div(pr.N, 4) * 4) * 4 : 0;
   return SGEMM_OK;
+}
+
+// TC_PRESPLIT: the split pass of op(A) and op(B) into the workspace ([stream-K slots][A hi][A lo]
+// [B hi][B lo], 256-byte aligned parts), then the GEMM over maps of the split arrays and the fixup.
+cudaError_t launch_presplit(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& st, uint8_t* ws,
+                            GemmParams* p, cudaStream_t stream) {
+  const int64_t slot_bytes = plan.kernel_launches > 3 ? 2 * plan.grid_x * (int64_t)(128 * 256 * 4) : 0;
+  const SplitLayout l = split_layout(pr.M, pr.N, pr.K, pr.batch, pr.stride_a, pr.stride_b, slot_bytes);
+  const int64_t ldk = split_ldk(pr.K);
+  float* ahi = reinterpret_cast<float*>(ws + round256(l.slots));
+  float* alo = reinterpret_cast<float*>(ws + round256(l.slots) + round256(l.a_bytes));
+  float* bhi = reinterpret_cast<float*>(ws + round256(l.slots) + 2 * round256(l.a_bytes));
+  float* blo = reinterpret_cast<float*>(ws + round256(l.slots) + 2 * round256(l.a_bytes) + round256(l.b_bytes));
+  p->ws = slot_bytes > 0 ? reinterpret_cast<float*>(ws) : nullptr;
+  // op(A) rows run along K when A is 'N'; op(B) rows (columns of op(B)) when B is 'T'
+  cudaError_t e = launch_split_operand(pr.A, pr.lda, pr.stride_a, !pr.ta, (int)pr.M, (int)pr.K,
+                                       (int)l.a_products, ahi, alo, ldk, st.sm_count, stream);
+  if (e == cudaSuccess)
+    e = launch_split_operand(pr.B, pr.ldb, pr.stride_b, pr.tb, (int)pr.N, (int)pr.K, (int)l.b_products, bhi, blo,
+                             ldk, st.sm_count, stream);
+  CUtensorMap mah, mal, mbh, mbl;
+  if (e == cudaSuccess) e = encode_split_map(ahi, pr.K, pr.M, ldk, l.a_products, &mah);
+  if (e == cudaSuccess) e = encode_split_map(alo, pr.K, pr.M, ldk, l.a_products, &mal);
+  if (e == cudaSuccess) e = encode_split_map(bhi, pr.K, pr.N, ldk, l.b_products, &mbh);
+  if (e == cudaSuccess) e = encode_split_map(blo, pr.K, pr.N, ldk, l.b_products, &mbl);
+  p->za = l.a_products > 1 ? 1 : 0;
+  p->zb = l.b_products > 1 ? 1 : 0;
+  if (e == cudaSuccess) e = launch_presplit_gemm(mah, mal, mbh, mbl, *p, stream);
+  if (e == cudaSuccess && slot_bytes > 0) e = launch_presplit_fixup(*p, (int)plan.sk_tiles, stream);
+  return e;
 }
 
 // ext_ws: the caller's workspace of at least plan.workspace_bytes (sgemm_ex), or nullptr to take
@@ -417,7 +471,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   set_schedule(plan, &p);
 
   CUtensorMap mapA, mapB;
-  if (plan.variant != SGEMM_VARIANT_GENERIC && plan.variant != SGEMM_VARIANT_SMALL) {
+  if (plan.variant != SGEMM_VARIANT_GENERIC && plan.variant != SGEMM_VARIANT_SMALL &&
+      plan.variant != SGEMM_VARIANT_TC_PRESPLIT) {
     int box_m, box_n;
     operand_boxes(plan, &box_m, &box_n);
     cudaError_t e = encode_operand_maps(pr.ta, pr.tb, pr.M, pr.N, pr.K, pr.A, pr.lda, pr.stride_a, pr.B, pr.ldb,
@@ -439,7 +494,9 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   }
 
   cudaError_t e;
-  if (plan.variant == SGEMM_VARIANT_GENERIC) {
+  if (plan.variant == SGEMM_VARIANT_TC_PRESPLIT) {
+    e = launch_presplit(pr, plan, st, static_cast<uint8_t*>(ws ? ws : ext_ws), &p, stream);
+  } else if (plan.variant == SGEMM_VARIANT_GENERIC) {
     e = launch_generic_gemm(pr.ta, pr.tb, p, split, stream);
   } else if (plan.variant == SGEMM_VARIANT_SMALL) {
     e = launch_small_gemm(pr.ta, pr.tb, p, (int)plan.grid_x, stream);
@@ -458,7 +515,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
     else e = launch_tma_op_tt(tile, mapA, mapB, p, split, stream);
   }
   if (e == cudaSuccess && split > 1 && plan.variant != SGEMM_VARIANT_TC_TF32X3 &&
-      plan.variant != SGEMM_VARIANT_TC_GROUPED && plan.variant != SGEMM_VARIANT_TC_PAIR)
+      plan.variant != SGEMM_VARIANT_TC_GROUPED && plan.variant != SGEMM_VARIANT_TC_PAIR &&
+      plan.variant != SGEMM_VARIANT_TC_PRESPLIT)
     e = launch_splitk_reduce(p, split, stream);
   if (ws) {
     cudaError_t ef = cudaFreeAsync(ws, stream);
@@ -468,6 +526,15 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
 }
 
 }  // namespace
+
+int sgemm_impl::plan_without_split_arrays(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                              int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
+                              int sm_count, sgemm_plan_t* plan) {
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  return make_plan(pr, sm_count, plan, 0, false);
+}
 
 extern "C" {
 
@@ -593,7 +660,8 @@ int sgemm_plan_strided_batched(char transA, char transB, int64_t M, int64_t N, i
 int sgemm_set_variant_override(int variant, int split_k) {
   if (variant != SGEMM_VARIANT_AUTO && variant != SGEMM_VARIANT_GENERIC && variant != SGEMM_VARIANT_TMA_128x128 &&
       variant != SGEMM_VARIANT_TMA_64x256 && variant != SGEMM_VARIANT_TC_TF32X3 && variant != SGEMM_VARIANT_SMALL &&
-      variant != SGEMM_VARIANT_TC_GROUPED && variant != SGEMM_VARIANT_TC_PAIR)
+      variant != SGEMM_VARIANT_TC_GROUPED && variant != SGEMM_VARIANT_TC_PAIR &&
+      variant != SGEMM_VARIANT_TC_PRESPLIT)
     return -1;
   g_override_variant.store(variant);
   g_override_split.store(split_k < 0 ? 0 : split_k);

@@ -1,0 +1,563 @@
+// kernel_presplit.cu -- 3xTF32 SGEMM with the operands split once per call, for sm_103a.
+//
+// The tensor-core kernels in kernel_tf32x3.cu and kernel_tc_pair.cu split
+// every operand tile into its TF32 hi part and FP32 lo part inside the
+// GEMM, once per output tile that reads it: an A panel is split by every
+// tile of its row, a B panel by every tile of its column, and measured on
+// GB300 that splitting bounds those kernels (with the split work removed
+// the CTA-pair kernel ran 28% faster).  Here a split pass writes each
+// operand once as K-contiguous hi and lo arrays (the same rounding: hi = x
+// rounded to TF32 to nearest with ties away, lo = x - hi exactly), and the
+// GEMM loads hi and lo tiles with TMA and hands them to the tensor cores
+// straight from shared memory: no splitter warps, no split stages.
+//
+// GEMM: 256 x 256 x 32 tiles on the two CTAs of a cluster with
+// tcgen05.mma.cta_group::2.kind::tf32, M = 256, N = 256, K = 8, A and B
+// both from shared memory (each CTA holds 128 rows of A hi/lo and 128 of
+// the tile's 256 columns of B hi/lo).  Per SM and K step the tensor core
+// reads 4 KB of A and 4 KB of B (each CTA's B half is read once for both
+// SMs) in 128 cycles, and the TMA ring writes 64 KB per K tile: about 106 of
+// the shared-memory path's 128 bytes per cycle at the tensor core's rate.
+// Each CTA's TMEM holds two 128 x 256 FP32 accumulators (512 columns); a
+// fresh one per 32-k tile is folded into FP32 registers by 8 folder warps,
+// as in the other tensor-core kernels.  The persistent data-parallel +
+// stream-K schedule of kernel_tc_common.cuh runs with the cluster as the
+// unit; presplit_fixup_kernel adds the partial sums of shared tiles in
+// cluster order.
+//
+// The pages name tensor cores and TF32 as the missing piece of their SGEMM
+// (itan.pw "CUDA NVIDIA 4090 高性能計算", §4; youngju.dev "CUDA architecture
+// visualized", テンソルコア).
+//
+// CTA roles (10 warps): warp 0 TMA producer (each CTA loads its own halves);
+// warp 1 of the even CTA issues the pair's MMAs, warp 1 of the odd CTA
+// relays its stage completions to the even CTA; warps 2-9 folders (lane
+// quarter warp % 4, columns 128 * ((warp - 2) / 4) .. +127) and epilogue.
+#include <algorithm>
+
+#include "kernel_tc_common.cuh"
+
+namespace sgemm_impl {
+namespace tps {
+
+using namespace tc;
+
+// ------------------------------------------------------------------ split pass
+// Splits op(X) for `products` products into hi and lo, written as rows of K
+// contiguous floats (row stride ldk, product stride rows * ldk): element (r,
+// k) of product p is src[p * stride + r * ld + k] when the stored rows run
+// along K, src[p * stride + k * ld + r] otherwise (then the pass transposes
+// through shared memory, 32 x 32 tiles).
+constexpr int kSplitTile = 32;
+
+__device__ __forceinline__ void split_one(float x, float& hi, float& lo) {
+  hi = tf32_round(x);
+  lo = __fmaf_rn(hi, -1.0f, x);  // exact: x - hi
+}
+
+// Rows run along K: each thread takes 4 consecutive k (16-byte loads and stores;
+// src and dst rows are 16-byte aligned, K % 4 == 0 is not required: the tail is scalar).
+__global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict__ src, int64_t ld, int64_t stride,
+                                                         int rows, int K, int products, float* __restrict__ hi,
+                                                         float* __restrict__ lo, int64_t ldk) {
+  const int k4n = (K + 3) / 4;
+  const int64_t total = (int64_t)products * rows * k4n;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int k4 = (int)(i % k4n);
+    const int64_t pr = i / k4n;  // product * rows + row
+    const int64_t p = pr / rows, r = pr - p * rows;
+    const float* s = src + p * stride + r * ld + 4 * k4;
+    float* h = hi + pr * ldk + 4 * k4;
+    float* l = lo + pr * ldk + 4 * k4;
+    if (4 * k4 + 3 < K) {
+      const float4 x = *reinterpret_cast<const float4*>(s);
+      float4 xh, xl;
+      split4(x, xh, xl);
+      *reinterpret_cast<float4*>(h) = xh;
+      *reinterpret_cast<float4*>(l) = xl;
+    } else {
+      for (int j = 0; j < K - 4 * k4; ++j) split_one(s[j], h[j], l[j]);
+    }
+  }
+}
+
+// Stored rows run along the other axis: a 32 x 32 block per CTA (32 x 8 threads), read along
+// the stored rows, written along K.
+__global__ void __launch_bounds__(256) split_transpose_kernel(const float* __restrict__ src, int64_t ld,
+                                                              int64_t stride, int rows, int K,
+                                                              float* __restrict__ hi, float* __restrict__ lo,
+                                                              int64_t ldk) {
+  __shared__ float tile[kSplitTile][kSplitTile + 1];
+  const int p = (int)blockIdx.z;
+  const int r0 = (int)blockIdx.x * kSplitTile, k0 = (int)blockIdx.y * kSplitTile;
+  const float* s = src + (int64_t)p * stride;
+  // read: stored row k = k0 + ty + 8j, element r = r0 + tx
+  for (int j = 0; j < kSplitTile; j += 8) {
+    const int k = k0 + (int)threadIdx.y + j, r = r0 + (int)threadIdx.x;
+    tile[threadIdx.y + j][threadIdx.x] = (k < K && r < rows) ? s[(int64_t)k * ld + r] : 0.0f;
+  }
+  __syncthreads();
+  // write: row r = r0 + ty + 8j, k = k0 + tx
+  float* h = hi + (int64_t)p * rows * ldk;
+  float* l = lo + (int64_t)p * rows * ldk;
+  for (int j = 0; j < kSplitTile; j += 8) {
+    const int r = r0 + (int)threadIdx.y + j, k = k0 + (int)threadIdx.x;
+    if (r < rows && k < K) {
+      float xh, xl;
+      split_one(tile[threadIdx.x][threadIdx.y + j], xh, xl);
+      h[(int64_t)r * ldk + k] = xh;
+      l[(int64_t)r * ldk + k] = xl;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ GEMM
+constexpr int BM = 256;                   // rows of a pair tile
+constexpr int BMC = 128;                  // rows one CTA covers
+constexpr int BN = 256;                   // columns of a pair tile
+constexpr int BNC = 128;                  // columns of B one CTA loads
+constexpr int BK = 32;
+constexpr int kStages = 3;
+constexpr int kPartBytes = 128 * BK * 4;  // 16 KB: 128 rows (or columns) x 32 k, K-major, 128-byte swizzle
+constexpr int kStageBytes = 4 * kPartBytes;  // A hi, A lo, B hi, B lo
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+constexpr int kFoldWarps = 8;             // warps 2-9
+constexpr int kThreads = 32 * (2 + kFoldWarps);
+constexpr int kAccBufs = 2;
+constexpr uint32_t kAccCols = 256;        // one 128 x 256 FP32 accumulator per CTA
+constexpr uint32_t kTmemCols = 512;
+constexpr int kFoldCols = 128;            // accumulator columns a folder thread owns
+constexpr int kFoldChunk = 32;            // columns loaded per round trip (register budget)
+constexpr uint16_t kPairMask = 0x3;
+static_assert(kAccBufs * kAccCols <= kTmemCols, "accumulators must fit in TMEM");
+static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA");
+
+// tcgen05 instruction descriptor, kind::tf32: FP32 accumulator, TF32 A and B,
+// both K-major, N = 256, M = 256 (the pair).
+constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t c;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(c));
+  return c;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D (both CTAs' TMEM) = or += A (128 rows in each CTA's shared memory) * B (128 columns in each
+// CTA's shared memory); both operands K-major, described by the same descriptors in both CTAs.
+__device__ __forceinline__ void mma_pair_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          bar),
+      "h"(kPairMask)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\t"
+      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+      "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar),
+      "r"(rank)
+      : "memory");
+}
+
+// Product and origin of pair tile `tile`.
+__device__ __forceinline__ void pair_tile_origin(const GemmParams& p, int tile, int& prod, int& m0, int& n0) {
+  const int tiles = p.tiles_m * p.tiles_n;
+  prod = tile / tiles;
+  int tm, tn;
+  tile_coords(tile - prod * tiles, p.tiles_m, p.tiles_n, tm, tn);
+  m0 = tm * BM;
+  n0 = tn * BN;
+}
+
+// Tensor maps: the split operands as {K, rows, products} with boxes {32, 128, 1}, 128-byte
+// swizzle; za / zb in GemmParams say whether the third coordinate is the product index.
+template <bool CVEC>
+__device__ __forceinline__ void store_row(const GemmParams& p, float* crow, int c0, const float2 (&m)[kFoldCols / 2]) {
+#pragma unroll
+  for (int e = 0; e < kFoldCols / 4; ++e) {
+    const int col = c0 + 4 * e;
+    const float x[4] = {m[2 * e].x, m[2 * e].y, m[2 * e + 1].x, m[2 * e + 1].y};
+    if (CVEC && col + 3 < p.N) {
+      float4 o;
+      if (p.beta == 0.0f) {
+        o = make_float4(p.alpha * x[0], p.alpha * x[1], p.alpha * x[2], p.alpha * x[3]);
+      } else {
+        const float4 old = *reinterpret_cast<const float4*>(crow + col);
+        o = make_float4(fmaf(p.alpha, x[0], p.beta * old.x), fmaf(p.alpha, x[1], p.beta * old.y),
+                        fmaf(p.alpha, x[2], p.beta * old.z), fmaf(p.alpha, x[3], p.beta * old.w));
+      }
+      *reinterpret_cast<float4*>(crow + col) = o;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (col + k < p.N)
+          crow[col + k] = p.beta == 0.0f ? p.alpha * x[k] : fmaf(p.alpha, x[k], p.beta * crow[col + k]);
+    }
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    presplit_gemm_kernel(const __grid_constant__ CUtensorMap mapAh, const __grid_constant__ CUtensorMap mapAl,
+                         const __grid_constant__ CUtensorMap mapBh, const __grid_constant__ CUtensorMap mapBl,
+                         const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], peer_full[kStages];
+  __shared__ __align__(8) uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
+  __shared__ __align__(8) uint64_t fin;
+  __shared__ uint32_t tmem_slot;
+  __shared__ CtaWork work_s;
+
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;  // the same in both CTAs (same kernel)
+  const uint32_t sbase = raw_addr + pad;
+  // stage s: [A hi][A lo][B hi][B lo], 16 KB each, 1024-byte aligned
+  auto part = [&](int s, int which) { return sbase + (uint32_t)(s * kStageBytes + which * kPartBytes); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int cl = (int)cluster_id_x();
+  const int kt_total = (p.K + BK - 1) / BK;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (threadIdx.x == 0) {
+    work_s = cta_work(p, cl, kt_total);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&empty[s]), 1);
+      mbar_init(smem_addr(&peer_full[s]), 1);
+    }
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(smem_addr(&acc_full[b]), 1);
+      mbar_init(smem_addr(&acc_empty[b]), 2 * kFoldWarps);
+    }
+    mbar_init(smem_addr(&fin), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc_pair(smem_addr(&tmem_slot), kTmemCols);
+  tmem_fence_before_sync();
+  cluster_sync();  // both CTAs' barriers initialised and TMEM allocated before any cross-CTA traffic
+  tmem_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  const int nkt = work_s.units;  // K tiles of this cluster's work (the same in both CTAs)
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (each CTA: its rows of A, its columns of B)
+    if (lane == 0) {
+      prefetch_tensormap(&mapAh);
+      prefetch_tensormap(&mapAl);
+      prefetch_tensormap(&mapBh);
+      prefetch_tensormap(&mapBl);
+      int issued = 0;
+      bool ok = true;
+      const CtaWork work = work_s;
+      for (int sgi = 0; ok && sgi < work.nseg; ++sgi) {
+        const Segment g = cta_segment(p, work, cl, sgi, kt_total);
+        int prod, m0, n0;
+        pair_tile_origin(p, g.tile, prod, m0, n0);
+        m0 += BMC * (int)rank;
+        n0 += BNC * (int)rank;
+        const int za = prod * p.za, zb = prod * p.zb;
+        for (int kt = g.kb; kt < g.ke; ++kt) {
+          const int t = issued;
+          const int s = t % kStages;
+          if (t >= kStages &&
+              !mbar_wait(smem_addr(&empty[s]), (uint32_t)((t / kStages) - 1) & 1u, p.timeout_ns)) {
+            atomicOr(p.fault, (unsigned)kFaultEmptyWait);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_addr(&full[s]);
+          mbar_arrive_expect_tx(fb, (uint32_t)kStageBytes);
+          const int k0 = kt * BK;
+          tma_load_3d(part(s, 0), &mapAh, fb, k0, m0, za);
+          tma_load_3d(part(s, 1), &mapAl, fb, k0, m0, za);
+          tma_load_3d(part(s, 2), &mapBh, fb, k0, n0, zb);
+          tma_load_3d(part(s, 3), &mapBl, fb, k0, n0, zb);
+          issued = t + 1;
+        }
+      }
+      for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
+        if (!mbar_wait(smem_addr(&full[t % kStages]), (uint32_t)(t / kStages) & 1u, p.timeout_ns))
+          atomicOr(p.fault, (unsigned)kFaultDrainWait);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank != 0) {
+      // ---------------------------------------------- relay (odd CTA): stage landed here -> tell the issuer
+      bool ok = true;
+      int t = 0;
+      for (; ok && t < nkt; ++t) {
+        const int s = t % kStages;
+        ok = mbar_wait(smem_addr(&full[s]), (uint32_t)(t / kStages) & 1u, p.timeout_ns);
+        if (ok) mbar_arrive_remote(smem_addr(&peer_full[s]), 0);
+      }
+      // the issuer's last commits on the stages land in this CTA: wait for them
+      for (int u = nkt > kStages ? nkt - kStages : 0; ok && u < nkt; ++u)
+        ok = mbar_wait(smem_addr(&empty[u % kStages]), (uint32_t)(u / kStages) & 1u, p.timeout_ns);
+      if (!ok) atomicOr(p.fault, (unsigned)kFaultFullWait);
+    } else if (lane == 0) {
+      // ---------------------------------------------- MMA issuer (even CTA)
+      bool ok = true;
+      int done = -1;
+      for (int t = 0; ok && t < nkt; ++t) {
+        const int s = t % kStages, b = t % kAccBufs;
+        const uint32_t ph = (uint32_t)(t / kStages) & 1u;
+        if (!mbar_wait(smem_addr(&full[s]), ph, p.timeout_ns) ||
+            !mbar_wait(smem_addr(&peer_full[s]), ph, p.timeout_ns) ||
+            (t >= kAccBufs &&
+             !mbar_wait(smem_addr(&acc_empty[b]), (uint32_t)((t / kAccBufs) - 1) & 1u, p.timeout_ns))) {
+          ok = false;
+          break;
+        }
+        tmem_fence_after_sync();
+        const uint32_t acc = tmem + (uint32_t)b * kAccCols;
+        const uint64_t ahi = kmajor_sw128_desc(part(s, 0)), alo = kmajor_sw128_desc(part(s, 1));
+        const uint64_t bhi = kmajor_sw128_desc(part(s, 2)), blo = kmajor_sw128_desc(part(s, 3));
+#pragma unroll
+        for (int ks = 0; ks < BK / 8; ++ks) {
+          const uint64_t step = (uint64_t)(ks * 32) >> 4;  // 8 TF32 = 32 bytes along K
+          mma_pair_ss(acc, alo + step, bhi + step, ks == 0 ? 0u : 1u);  // fresh accumulator per K tile
+          mma_pair_ss(acc, ahi + step, blo + step, 1u);
+          mma_pair_ss(acc, ahi + step, bhi + step, 1u);
+        }
+        mma_commit_pair(smem_addr(&empty[s]));     // stage s reusable in both CTAs
+        mma_commit_pair(smem_addr(&acc_full[b]));  // accumulator b (both CTAs) holds K tile t
+        done = t;
+      }
+      if (!ok) atomicOr(p.fault, (unsigned)kFaultFullWait);
+      // leave only when every MMA has completed and its commits have landed here
+      for (int u = done + 1 > kStages ? done + 1 - kStages : 0; u <= done; ++u)
+        if (!mbar_wait(smem_addr(&empty[u % kStages]), (uint32_t)(u / kStages) & 1u, p.timeout_ns))
+          atomicOr(p.fault, (unsigned)kFaultDrainWait);
+      if (done >= 0 &&
+          !mbar_wait(smem_addr(&acc_full[done % kAccBufs]), (uint32_t)(done / kAccBufs) & 1u, p.timeout_ns))
+        atomicOr(p.fault, (unsigned)kFaultDrainWait);
+    }
+  } else {
+    // ------------------------------------------------ folders, then epilogue (both CTAs)
+    const int q = warp & 3;                     // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;           // which 128 accumulator columns
+    const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kFoldCols * half);
+    float2 master2[kFoldCols / 2];
+#pragma unroll
+    for (int e = 0; e < kFoldCols / 2; ++e) master2[e] = make_float2(0.0f, 0.0f);
+    bool ok = true;
+    int u = 0;
+    for (int sgi = 0; ok && sgi < work_s.nseg; ++sgi) {
+      int len;
+      {
+        const Segment g = cta_segment(p, work_s, cl, sgi, kt_total);
+        len = g.ke - g.kb;
+      }
+      for (int i = 0; i < len; ++i, ++u) {
+        const int b = u % kAccBufs;
+        if (!warp_wait(smem_addr(&acc_full[b]), (uint32_t)(u / kAccBufs) & 1u, p.timeout_ns)) {
+          ok = false;
+          if (lane == 0) atomicOr(p.fault, (unsigned)kFaultFullWait);
+          break;
+        }
+        tmem_fence_after_sync();
+#pragma unroll
+        for (int ch = 0; ch < kFoldCols / kFoldChunk; ++ch) {
+          float v[2][16];
+          tmem_ld16(tq + (uint32_t)b * kAccCols + (uint32_t)(kFoldChunk * ch), v[0]);
+          tmem_ld16(tq + (uint32_t)b * kAccCols + (uint32_t)(kFoldChunk * ch + 16), v[1]);
+          tmem_wait_ld();
+          if (ch == kFoldCols / kFoldChunk - 1) {
+            // the whole accumulator is in registers or folded: hand it back to the issuer
+            tmem_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(smem_addr(&acc_empty[b]), 0);
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            tmem_ld_ready(v[c]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {  // round-to-nearest FP32 adds, two per instruction
+              float2& m = master2[(kFoldChunk * ch + 16 * c) / 2 + e];
+              m = __fadd2_rn(m, make_float2(v[c][2 * e], v[c][2 * e + 1]));
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      // epilogue: this thread holds row 32q + lane of the CTA's 128 rows, columns 128*half .. +127
+      const Segment g = cta_segment(p, work_s, cl, sgi, kt_total);
+      if (g.slot >= 0) {
+        float* w = p.ws + (int64_t)(2 * g.slot + (int)rank) * (BMC * BN) + (32 * q + lane) * BN + kFoldCols * half;
+#pragma unroll
+        for (int e = 0; e < kFoldCols / 4; ++e)
+          *reinterpret_cast<float4*>(w + 4 * e) =
+              make_float4(master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y);
+      } else {
+        int prod, m0, n0;
+        pair_tile_origin(p, g.tile, prod, m0, n0);
+        const int row = m0 + BMC * (int)rank + 32 * q + lane;
+        if (row < p.M) {
+          float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
+          if (p.c_vec) store_row<true>(p, crow, n0 + kFoldCols * half, master2);
+          else         store_row<false>(p, crow, n0 + kFoldCols * half, master2);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < kFoldCols / 2; ++e) master2[e] = make_float2(0.0f, 0.0f);
+    }
+  }
+
+  tmem_fence_before_sync();
+  __syncthreads();
+  // Bounded handshake of the two CTAs: neither releases its TMEM or exits while the other may
+  // still arrive on its barriers or have MMAs read its shared memory and TMEM.
+  if (threadIdx.x == 0) {
+    mbar_arrive_remote(smem_addr(&fin), rank ^ 1u);
+    if (!mbar_wait(smem_addr(&fin), 0u, p.timeout_ns)) atomicOr(p.fault, (unsigned)kFaultDrainWait);
+  }
+  __syncthreads();
+  tmem_fence_after_sync();
+  if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
+}
+
+// CTA (x, y) of the fixup grid: x = 2 j + r covers rows 128 r .. 128 r + 127 of
+// stream-K pair tile j, rows 8y .. 8y+7 of those, two float4s of 4 columns
+// per thread (columns 4 * lane and 128 + 4 * lane).  If several clusters
+// shared tile j, C = alpha * (sum of their slots, in cluster order) + beta * C
+// over the in-range elements.
+constexpr int kFixupRowsPerCta = 8;
+constexpr int kFixupThreads = 256;
+constexpr int kMaxSharers = 256;
+template <bool CVEC>
+__global__ void __launch_bounds__(kFixupThreads) presplit_fixup_kernel(const GemmParams p) {
+  __shared__ int s_n;
+  __shared__ int s_slot[kMaxSharers];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int kt = (p.K + BK - 1) / BK;
+  const int j = (int)blockIdx.x >> 1, r = (int)blockIdx.x & 1;
+  if (threadIdx.x == 0) {
+    const int64_t i0 = (int64_t)j * kt;
+    const int c0 = sk_owner(p, i0), c1 = sk_owner(p, i0 + kt - 1);
+    s_n = min(c1 - c0 + 1, kMaxSharers);
+    s_slot[0] = c0;
+  }
+  __syncthreads();
+  const int n = s_n;
+  if (n == 1) return;  // one cluster covered the whole tile and wrote C itself
+  const int c0 = s_slot[0];
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kFixupThreads) s_slot[i] = 2 * sk_slot(p, c0 + i, j, kt) + r;
+  __syncthreads();
+  int prod, m0, n0;
+  pair_tile_origin(p, p.sk_tile0 + j, prod, m0, n0);
+  const int rr = (int)blockIdx.y * kFixupRowsPerCta + (int)(threadIdx.x >> 5);
+  const int row = m0 + BMC * r + rr;
+  if (row >= p.M) return;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int cc = 128 * h + (int)(threadIdx.x & 31) * 4;
+    const int col = n0 + cc;
+    if (col >= p.N) continue;
+    const float* w = p.ws + rr * BN + cc;
+    float4 v = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[0] * (BMC * BN));
+#pragma unroll 4
+    for (int i = 1; i < n; ++i) {
+      const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[i] * (BMC * BN));
+      v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+    }
+    float* cp = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
+    if (CVEC && col + 3 < p.N) {
+      float4 o;
+      if (p.beta == 0.0f) {
+        o = make_float4(p.alpha * v.x, p.alpha * v.y, p.alpha * v.z, p.alpha * v.w);
+      } else {
+        const float4 old = *reinterpret_cast<const float4*>(cp);
+        o = make_float4(fmaf(p.alpha, v.x, p.beta * old.x), fmaf(p.alpha, v.y, p.beta * old.y),
+                        fmaf(p.alpha, v.z, p.beta * old.z), fmaf(p.alpha, v.w, p.beta * old.w));
+      }
+      *reinterpret_cast<float4*>(cp) = o;
+    } else {
+      const float x[4] = {v.x, v.y, v.z, v.w};
+      for (int k = 0; k < 4 && col + k < p.N; ++k)
+        cp[k] = p.beta == 0.0f ? p.alpha * x[k] : fmaf(p.alpha, x[k], p.beta * cp[k]);
+    }
+  }
+}
+
+}  // namespace tps
+
+cudaError_t prepare_presplit() {
+  return cudaFuncSetAttribute(tps::presplit_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              tps::kSmemBytes);
+}
+
+cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, bool k_contig, int rows, int K,
+                                 int products, float* hi, float* lo, int64_t ldk, int sm_count,
+                                 cudaStream_t stream) {
+  if (rows <= 0 || K <= 0 || products <= 0) return cudaSuccess;
+  if (k_contig) {
+    const int64_t work = (int64_t)products * rows * ((K + 3) / 4);
+    const int64_t blocks = std::min<int64_t>((work + 255) / 256, (int64_t)sm_count * 8);
+    tps::split_rows_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, stream>>>(src, ld, stride, rows, K,
+                                                                                      products, hi, lo, ldk);
+  } else {
+    const dim3 grid((unsigned)((rows + tps::kSplitTile - 1) / tps::kSplitTile),
+                    (unsigned)((K + tps::kSplitTile - 1) / tps::kSplitTile), (unsigned)products);
+    tps::split_transpose_kernel<<<grid, dim3(tps::kSplitTile, 8), 0, stream>>>(src, ld, stride, rows, K, hi, lo,
+                                                                               ldk);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_presplit_gemm(const CUtensorMap& mapAh, const CUtensorMap& mapAl, const CUtensorMap& mapBh,
+                                 const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream) {
+  tps::presplit_gemm_kernel<<<2u * (unsigned)p.sk_grid, tps::kThreads, tps::kSmemBytes, stream>>>(mapAh, mapAl,
+                                                                                                   mapBh, mapBl, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2u * (unsigned)sk_tiles, tps::BMC / tps::kFixupRowsPerCta);
+  cfg.blockDim = dim3(tps::kFixupThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the GEMM kernel ends
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return p.c_vec ? cudaLaunchKernelEx(&cfg, tps::presplit_fixup_kernel<true>, p)
+                 : cudaLaunchKernelEx(&cfg, tps::presplit_fixup_kernel<false>, p);
+}
+
+}  // namespace sgemm_impl

@@ -87,7 +87,7 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
   if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
   NoallocDevice* nd = nullptr;
   if (setup(dev, &nd) != cudaSuccess) return SGEMM_ERR_CUDA;
-  st = sgemm_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nd->sm_count, &plan);
+  st = plan_without_split_arrays(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nd->sm_count, &plan);
   if (st != SGEMM_OK) return st;
   if ((uint64_t)plan.workspace_bytes > (uint64_t)SGEMM_NOALLOC_SCRATCH_BYTES) return SGEMM_ERR_SCRATCH_LIMIT;
 

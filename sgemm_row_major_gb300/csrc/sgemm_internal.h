@@ -53,11 +53,34 @@ cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t 
 // variants); the pair kernel's scheduling unit is the cluster of 2 CTAs.
 inline void set_schedule(const sgemm_plan_t& plan, GemmParams* p) {
   if (plan.variant != SGEMM_VARIANT_TC_TF32X3 && plan.variant != SGEMM_VARIANT_TC_GROUPED &&
-      plan.variant != SGEMM_VARIANT_TC_PAIR)
+      plan.variant != SGEMM_VARIANT_TC_PAIR && plan.variant != SGEMM_VARIANT_TC_PRESPLIT)
     return;
-  p->sk_grid = (int)(plan.variant == SGEMM_VARIANT_TC_PAIR ? plan.grid_x / 2 : plan.grid_x);
+  p->sk_grid = (int)(plan.variant == SGEMM_VARIANT_TC_PAIR || plan.variant == SGEMM_VARIANT_TC_PRESPLIT
+                         ? plan.grid_x / 2 : plan.grid_x);
   p->sk_iters = plan.sk_iters;
   p->sk_tile0 = (int)plan.dp_tiles;
+}
+
+// Split-operand arrays of the TC_PRESPLIT variant: op(A) and op(B) as rows of
+// K contiguous floats (row stride split_ldk(K)), hi and lo parts, one set per
+// product whose operand differs (a stride of 0 shares one).
+inline int64_t split_ldk(int64_t K) { return (K + 3) / 4 * 4; }
+inline int64_t round256(int64_t bytes) { return (bytes + 255) / 256 * 256; }
+struct SplitLayout {
+  int64_t slots = 0;             // stream-K partial-sum slots (bytes, first in the workspace)
+  int64_t a_products = 1, b_products = 1;
+  int64_t a_bytes = 0, b_bytes = 0;  // one part (hi or lo) of op(A) / op(B), all products
+  int64_t total() const { return round256(slots) + 2 * round256(a_bytes) + 2 * round256(b_bytes); }
+};
+inline SplitLayout split_layout(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t stride_a, int64_t stride_b,
+                                int64_t slot_bytes) {
+  SplitLayout l;
+  l.slots = slot_bytes;
+  l.a_products = (batch > 1 && stride_a != 0) ? batch : 1;
+  l.b_products = (batch > 1 && stride_b != 0) ? batch : 1;
+  l.a_bytes = l.a_products * M * split_ldk(K) * 4;
+  l.b_bytes = l.b_products * N * split_ldk(K) * 4;
+  return l;
 }
 
 // TMA box extents one CTA of a plan loads per K tile: rows of op(A) and
@@ -106,6 +129,24 @@ cudaError_t tc_pair_max_clusters(int* clusters);  // co-resident clusters of the
 cudaError_t launch_tc_pair(bool transA, bool transB, const CUtensorMap& mapA, const CUtensorMap& mapB,
                            const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_pair_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
+// 3xTF32 on split operands (kernel_presplit.cu): the split pass (per operand:
+// rows x K of op(X), from a stored layout whose rows run along K or not), then
+// the CTA-pair GEMM on 256x256x32 tiles with four maps over the split arrays,
+// then the fixup over the sk_tiles stream-K pair tiles when any is shared.
+cudaError_t prepare_presplit();
+cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, bool k_contig, int rows, int K,
+                                 int products, float* hi, float* lo, int64_t ldk, int sm_count, cudaStream_t stream);
+cudaError_t launch_presplit_gemm(const CUtensorMap& mapAh, const CUtensorMap& mapAl, const CUtensorMap& mapBh,
+                                 const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream);
+cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
+// sgemm_plan() for a caller that cannot provide the split arrays of TC_PRESPLIT
+// (sgemm_noalloc): that variant, forced by override, is planned as TC_PAIR.
+int plan_without_split_arrays(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                              int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
+                              int sm_count, sgemm_plan_t* plan);
+// Map over a split array: {K, rows, products} float32, row stride ldk, box {32, 128, 1}, 128-byte swizzle.
+cudaError_t encode_split_map(const float* base, int64_t K, int64_t rows, int64_t ldk, int64_t products,
+                             CUtensorMap* map);
 cudaError_t launch_generic_gemm(bool transA, bool transB, const GemmParams& p, int split,
                                 cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const GemmParams& p, int split, cudaStream_t stream);

@@ -69,6 +69,13 @@ cudaError_t bind_primary_context() {
 
 }  // namespace
 
+cudaError_t encode_split_map(const float* base, int64_t K, int64_t rows, int64_t ldk, int64_t products,
+                             CUtensorMap* map) {
+  cudaError_t e = bind_primary_context();
+  if (e != cudaSuccess) return e;
+  return encode_3d(base, K, rows, ldk, products, rows * ldk, 32, 128, true, map);
+}
+
 cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                                 int64_t stride_a, const float* B, int64_t ldb, int64_t stride_b, int batch,
                                 int bm, int bn, int bk, CUtensorMap* mapA, CUtensorMap* mapB, int* za, int* zb) {
