@@ -41,7 +41,8 @@ UNIT = "TFLOPS"
 FMA_PER_SM_PER_CLK = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
 # committed ncu summaries by (kernel variant, workload): their per-launch DRAM traffic is reported
 # while the kernel's source digest still matches the one they were captured with
-PROFILES = {("TC_PAIR", "square4096"): os.path.join(ROOT, "profiles", "tc_pair_gemm_square4096.md"),
+PROFILES = {("TC_PRESPLIT", "square4096"): os.path.join(ROOT, "profiles", "presplit_gemm_square4096.md"),
+            ("TC_PAIR", "square4096"): os.path.join(ROOT, "profiles", "tc_pair_gemm_square4096.md"),
             ("TC_TF32X3", "square4096"): os.path.join(ROOT, "profiles", "tf32x3_gemm_square4096.md"),
             ("TMA_128x128", "square4096"): os.path.join(ROOT, "profiles", "tma_gemm_square4096.md"),
             ("SMALL", "batched_small_8192x64x64x64"):
@@ -387,8 +388,19 @@ def l2_note(flush):
             "two input sets used in turn, each larger than the 129 MB L2; no flush")
 
 
+KERNEL_NAMES = {
+    "TC_TF32X3": "tf32x3_gemm_kernel (tcgen05.mma kind::tf32, 3xTF32 split)",
+    "TC_PAIR": "pair_gemm_kernel (tcgen05.mma cta_group::2 kind::tf32, 3xTF32 split, 256x128 tiles on CTA pairs)",
+    "TC_PRESPLIT": "presplit_gemm_kernel (tcgen05.mma cta_group::2 kind::tf32, both operands from shared memory, "
+                   "256x256 tiles on CTA pairs) after split_rows/split_transpose (A and B split once into TF32 hi "
+                   "and FP32 lo)",
+}
+
+
 def kernel_digest(lib_build, variant):
     """Source digest of the kernel a variant runs (matches the digest in its committed profile)."""
+    if variant == "TC_PRESPLIT":
+        return lib_build.presplit_kernel_digest()
     if variant == "TC_PAIR":
         return lib_build.pair_kernel_digest()
     if variant in ("TC_TF32X3", "TC_GROUPED"):
@@ -409,11 +421,11 @@ def tensor_roofline(achieved, peaks, traffic, kernel_ms, variant="TC_TF32X3"):
             "peak_basis": f"{basis} bf16 burst {bf16:.0f} TFLOP/s x nominal tf32/bf16 "
                           f"{NOMINAL_TF32_PF}/{NOMINAL_BF16_PF} = {tf32:.0f} TFLOP/s of tf32, / {TF32_PRODUCTS} "
                           f"tensor products per SGEMM FMA (3xTF32 split); achieved counts 2MNK only",
-            "kernel": ("pair_gemm_kernel (tcgen05.mma cta_group::2 kind::tf32, 3xTF32 split, 256x128 tiles "
-                       "on CTA pairs)" if variant == "TC_PAIR" else
-                       "tf32x3_gemm_kernel (tcgen05.mma kind::tf32, 3xTF32 split)"), "kernel_ms": kernel_ms,
-            "kernel_ms_covers": "one sgemm() call: the GEMM kernel and, when stream-K tiles are shared, "
-                                "the fixup kernel after it (about 2% of the step in the ncu launch list)"}
+            "kernel": KERNEL_NAMES.get(variant, KERNEL_NAMES["TC_TF32X3"]), "kernel_ms": kernel_ms,
+            "kernel_ms_covers": ("one sgemm() call: the split passes of A and B, the GEMM kernel and, when "
+                                 "stream-K tiles are shared, the fixup kernel" if variant == "TC_PRESPLIT" else
+                                 "one sgemm() call: the GEMM kernel and, when stream-K tiles are shared, "
+                                 "the fixup kernel after it (about 2% of the step in the ncu launch list)")}
 
 
 def run_ours(args):
@@ -501,7 +513,7 @@ def run_ours(args):
     max_mhz = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
     ffma_peak = sms * FMA_PER_SM_PER_CLK * 2 * max_mhz * 1e6 / 1e12
     variant = plan["variant_name"]
-    if variant in ("TC_TF32X3", "TC_PAIR"):
+    if variant in ("TC_TF32X3", "TC_PAIR", "TC_PRESPLIT"):
         roof = tensor_roofline(achieved, peaks,
                                traffic_from_profile(variant, case.name, kernel_digest(lib_build, variant)),
                                kernel_ms, variant)
@@ -608,7 +620,7 @@ def batched_roofline(c, plan, flops_step, achieved, kernel_ms, peaks, dev, lib_b
     """Roofline object of the kernel a strided batch ran on.  For the tensor-core kernel the bound is
     whichever of the 3xTF32 tensor peak and HBM takes longer for the call's algorithmic work."""
     variant = plan["variant_name"]
-    if variant in ("TC_TF32X3", "TC_GROUPED", "TC_PAIR"):
+    if variant in ("TC_TF32X3", "TC_GROUPED", "TC_PAIR", "TC_PRESPLIT"):
         traffic = traffic_from_profile(variant, c.name, kernel_digest(lib_build, variant))
         roof = tensor_roofline(achieved, peaks, traffic, kernel_ms, variant)
         if variant == "TC_GROUPED":

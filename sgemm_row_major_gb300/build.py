@@ -64,6 +64,9 @@ TC_KERNEL_FILES = ["kernel_tf32x3.cu", "kernel_tc_common.cuh", "device_utils.cuh
 PAIR_KERNEL_FILES = ["kernel_tc_pair.cu", "kernel_tc_common.cuh", "device_utils.cuh", "sgemm_internal.h"]
 
 
+PRESPLIT_KERNEL_FILES = ["kernel_presplit.cu", "kernel_tc_common.cuh", "device_utils.cuh", "sgemm_internal.h"]
+
+
 SMALL_KERNEL_FILES = ["kernel_small.cu", "kernel_small.h", "sgemm_internal.h"]
 
 
@@ -80,6 +83,11 @@ def tc_kernel_digest() -> str:
 def pair_kernel_digest() -> str:
     """Hash of the sources of the CTA-pair tensor-core kernel only."""
     return _digest(PAIR_KERNEL_FILES)
+
+
+def presplit_kernel_digest() -> str:
+    """Hash of the sources of the split-operand kernels (split pass, GEMM, fixup) only."""
+    return _digest(PRESPLIT_KERNEL_FILES)
 
 
 def small_kernel_digest() -> str:

@@ -161,9 +161,11 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Stream-K pays for every output tile it splits (partial sums written and
 // read back by the fixup kernel), so it is used only when each CTA gets at
 // least kMinStreamKIters K tiles of it:
-//   tiles >= SMs: whole-tile rounds on one CTA per SM; when the last round is
-//     ragged, the last SMs + (tiles % SMs) tiles go to stream-K instead (each
-//     CTA's share is then 1-2 tiles), or stay whole if that share is short;
+//   tiles >= SMs: whole-tile rounds on one CTA per SM; the (tiles % SMs)
+//     tiles of a ragged last round go to stream-K (measured at 4096^3: 266
+//     against 226 TFLOPS for the split-operand kernel, whose operands fit in L2
+//     only while the CTAs stay at the same K), or, when that share is short,
+//     the last SMs + (tiles % SMs) tiles, or they stay whole if that is short too;
 //   tiles <  SMs: stream-K over all tiles on one CTA per SM, or, if that
 //     share is short, S = min(SMs / tiles, K tiles / 4) CTAs per tile;
 //   forced split S (override): S CTAs per tile (S = 1: one CTA per tile,
@@ -192,9 +194,14 @@ int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
     sk_tiles = tiles;
     grid = std::min<int64_t>({tiles * std::min(ov_split, 128), tiles * kt, int64_t{1} << 20});
   } else if (tiles >= sms) {
+    // whole rounds, then the remainder's K iterations shared evenly (clusters or CTAs then work on
+    // the same K range at the same time in the whole rounds, which keeps the operands in L2); when
+    // that share is short, the last whole round goes to stream-K too
     grid = sms;
-    sk_tiles = tiles % sms ? sms + tiles % sms : 0;
-    if (sk_tiles * kt / sms < kMinStreamKIters) sk_tiles = 0;
+    const int64_t rem = tiles % sms;
+    sk_tiles = 0;
+    if (rem * kt / sms >= kMinStreamKIters) sk_tiles = rem;
+    else if (rem && (sms + rem) * kt / sms >= kMinStreamKIters) sk_tiles = sms + rem;
     dp_tiles = tiles - sk_tiles;
   } else {
     dp_tiles = 0;
@@ -237,6 +244,8 @@ int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
 constexpr int64_t kPairSmemBytes = 6 * 24576 + 2 * 16384 + 1024;
 // ... and of the split-operand kernel (kernel_presplit.cu: 3 stages of A hi/lo and B hi/lo, 64 KB each).
 constexpr int64_t kPresplitSmemBytes = 3 * 65536 + 1024;
+constexpr double kMinFlopPerSplitByte = 128.0;
+constexpr int64_t kMaxSplitBytes = int64_t{4} << 30;
 
 // The planner: a pure function of the problem, the SM count, the number of
 // co-resident CTA-pair clusters (<= 0: sm_count / 2) and the override.
@@ -290,8 +299,24 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   // 2048^3 .. 16384 x 1024 x 4096, slower on fewer tiles (1024^3: 70.5 against
   // 74.3 TFLOPS) and on M <= 128 (half of every pair tile idle).
   const int64_t clusters = std::max(1, pair_clusters > 0 ? pair_clusters : sm_count / 2);
+  // (the split pass's transposing grid: K / 32 and the products in grid dimensions y and z)
+  const bool presplit_ok = tma_ok && allow_presplit && ceil_div(pr.K, 32) <= 65535 && pr.batch <= 65535;
   if (tma_ok && pr.M > 128 && ceil_div(pr.M, 256) * ceil_div(pr.N, 128) * pr.batch >= clusters)
     variant = SGEMM_VARIANT_TC_PAIR;
+  // Operands split once per call (TC_PRESPLIT) when the GEMM reuses them enough to amortize the
+  // split pass (read once, hi and lo written: 12 bytes per element of op(A) and op(B)) and every
+  // cluster gets a whole 256 x 256 tile; measured on GB300 (TFLOPS, split pass included, against
+  // TC_PAIR): 4096^3 266.7 / 209.1, 8192x4096x1024 239.5 / 195.1, 16384x1024x4096 244.6 / 218.8,
+  // 4097x3001x2053 200.2 / 166.1, 32 x 2048x1024x1024 with a shared B 226.0 / 202.8; slower at
+  // 64 x 512x1024x1024 (60 FLOP per split byte: 142.4 / 195.1) and on fewer tiles than clusters
+  // (1024^3 49.7 / 71.7).  The split arrays are capped at kMaxSplitBytes of workspace.
+  if (presplit_ok && pr.M > 128 && ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.batch >= clusters) {
+    const SplitLayout sl = split_layout(pr.M, pr.N, pr.K, pr.batch, pr.stride_a, pr.stride_b, 0);
+    const double flops = 2.0 * (double)pr.M * (double)pr.N * (double)pr.K * (double)pr.batch;
+    if (flops >= kMinFlopPerSplitByte * 3.0 * (double)(sl.a_bytes + sl.b_bytes) &&
+        2 * (sl.a_bytes + sl.b_bytes) <= kMaxSplitBytes)
+      variant = SGEMM_VARIANT_TC_PRESPLIT;
+  }
   if (group_ok && pr.batch >= sm_count) variant = SGEMM_VARIANT_TC_GROUPED;
   const int ov = g_override_variant.load();
   if (ov == SGEMM_VARIANT_GENERIC || ov == SGEMM_VARIANT_TMA_128x128 || ov == SGEMM_VARIANT_TMA_64x256 ||
@@ -300,8 +325,6 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   if (ov == SGEMM_VARIANT_SMALL) variant = small_ok ? ov : SGEMM_VARIANT_GENERIC;
   if (ov == SGEMM_VARIANT_TC_GROUPED) variant = group_ok ? ov : SGEMM_VARIANT_GENERIC;
   if (ov == SGEMM_VARIANT_TC_PAIR) variant = tma_ok ? ov : SGEMM_VARIANT_GENERIC;
-  // (the split pass's transposing grid: K / 32 and the products in grid dimensions y and z)
-  const bool presplit_ok = tma_ok && allow_presplit && ceil_div(pr.K, 32) <= 65535 && pr.batch <= 65535;
   if (ov == SGEMM_VARIANT_TC_PRESPLIT)
     variant = presplit_ok ? ov : tma_ok ? SGEMM_VARIANT_TC_PAIR : SGEMM_VARIANT_GENERIC;
   if (variant == SGEMM_VARIANT_TC_GROUPED) {

@@ -106,9 +106,12 @@ def test_planner_variants(lib):
     assert plan("N", "N", 0, 10, 10)["variant_name"] == "NONE"
     assert plan("N", "N", 10, 10, 0)["variant_name"] == "SCALE"
     big = plan("N", "N", 4096, 4096, 4096)
-    assert big["variant_name"] == "TC_PAIR" and big["grid_x"] == 152 and big["grid_y"] == 1
-    assert (big["tile_m"], big["tile_n"], big["tile_k"], big["threads"]) == (256, 128, 32, 608)
+    assert big["variant_name"] == "TC_PRESPLIT" and big["grid_x"] == 152 and big["grid_y"] == 1
+    assert (big["tile_m"], big["tile_n"], big["tile_k"], big["threads"]) == (256, 256, 32, 320)
     assert big["smem_bytes"] <= 227 * 1024
+    # fewer 256 x 256 tiles than clusters (2048^3: 64 < 76): CTA pairs with 256 x 128 tiles
+    pair = plan("N", "N", 2048, 2048, 2048)
+    assert pair["variant_name"] == "TC_PAIR" and (pair["tile_m"], pair["tile_n"], pair["threads"]) == (256, 128, 608)
     # fewer pair tiles than clusters (1024^3: 32 < 76), or M <= 128: one CTA per 128 x 128 tile
     one = plan("N", "N", 1024, 1024, 1024)
     assert one["variant_name"] == "TC_TF32X3" and one["tile_m"] == one["tile_n"] == 128
@@ -122,7 +125,7 @@ def test_planner_variants(lib):
     # ragged padded shapes of the transpose sweep keep the TMA-fed path (ld % 4 == 0)
     for ta, tb, lda, ldb in (("N", "N", 2060, 3008), ("N", "T", 2060, 2060), ("T", "N", 4104, 3008),
                              ("T", "T", 4104, 2060)):
-        assert plan(ta, tb, 4097, 3001, 2053, lda=lda, ldb=ldb)["variant_name"] == "TC_PAIR"
+        assert plan(ta, tb, 4097, 3001, 2053, lda=lda, ldb=ldb)["variant_name"] == "TC_PRESPLIT"
 
 
 def test_planner_split_k(lib):
@@ -157,10 +160,14 @@ def test_planner_stream_k(lib):
 
 
 def _one_cta_schedules():
-    # 4096^3: 1024 tiles on 152 SMs = 6.74 rounds -> 760 whole tiles, then 264 stream-K tiles
+    # 4096^3: 1024 tiles on 152 SMs = 6.74 rounds -> 912 whole tiles, then the 112 tiles of the
+    # ragged last round by stream-K (94 K tiles per CTA: a tile shared by up to 3 CTAs)
     p = plan("N", "N", 4096, 4096, 4096)
-    assert (p["grid_x"], p["grid_y"], p["dp_tiles"], p["sk_tiles"]) == (152, 1, 760, 264)
-    assert p["sk_iters"] == 264 * 128 and p["kernel_launches"] == 2 and p["split_k"] == 2
+    assert (p["grid_x"], p["grid_y"], p["dp_tiles"], p["sk_tiles"]) == (152, 1, 912, 112)
+    assert p["sk_iters"] == 112 * 128 and p["kernel_launches"] == 2 and p["split_k"] == 3
+    # a remainder whose share would be short (153 tiles, 1 left over): the last round joins stream-K
+    e = plan("N", "N", 128 * 17, 128 * 9, 4096)
+    assert (e["dp_tiles"], e["sk_tiles"]) == (0, 153)
     assert p["workspace_bytes"] == 2 * 152 * 128 * 128 * 4
     # a whole number of rounds: whole tiles only, one launch, no workspace
     w = plan("N", "N", 128 * 19, 128 * 16, 512)
@@ -203,7 +210,26 @@ def test_variant_override(lib):
             sg.sgemm_set_variant_override(99, 0)
     finally:
         sg.sgemm_set_variant_override("AUTO", 0)
-    assert plan("N", "N", 4096, 4096, 4096)["variant_name"] == "TC_PAIR"
+    assert plan("N", "N", 4096, 4096, 4096)["variant_name"] == "TC_PRESPLIT"
+
+
+def test_split_operand_rule(lib):
+    """TC_PRESPLIT when the split pass is amortized (>= 128 FLOP per byte it moves) and every cluster
+    gets a 256 x 256 tile; CTA pairs otherwise."""
+    assert plan("N", "N", 8192, 4096, 1024)["variant_name"] == "TC_PRESPLIT"
+    assert plan("N", "N", 16384, 1024, 4096)["variant_name"] == "TC_PRESPLIT"
+    for ta, tb in (("N", "T"), ("T", "N"), ("T", "T")):
+        assert plan(ta, tb, 4096, 4096, 4096)["variant_name"] == "TC_PRESPLIT"
+    # 64 products of 512x1024x1024, each operand split for two or four tiles: 60 FLOP per split byte
+    assert bplan("N", "N", 512, 1024, 1024, 64, 512 * 1024, 1024 * 1024, 512 * 1024)["variant_name"] == "TC_PAIR"
+    # the same products sharing one B (split once): 176 FLOP per split byte
+    assert bplan("N", "N", 2048, 1024, 1024, 32, 2048 * 1024, 0, 2048 * 1024)["variant_name"] == "TC_PRESPLIT"
+    # split arrays above 4 GiB (A and B 2 GiB each): CTA pairs
+    assert plan("N", "N", 16384, 16384, 32768)["variant_name"] == "TC_PAIR"
+    # workspace: stream-K slots of 128 x 256 floats per CTA, then hi and lo of A and B
+    p = plan("N", "N", 8192, 4096, 1024)
+    slots = 2 * 152 * 128 * 256 * 4 if p["split_k"] > 1 else 0
+    assert p["workspace_bytes"] == slots + 2 * 8192 * 1024 * 4 + 2 * 4096 * 1024 * 4
 
 
 def test_plan_rejects_huge_dimensions(lib):

@@ -22,7 +22,7 @@ def _ints(torch, shape, seed):
     return torch.randint(-2, 3, shape, generator=g, device="cuda", dtype=torch.int32).to(torch.float32)
 
 
-@pytest.mark.parametrize("variant", [None, "TC_TF32X3", "GENERIC", "TMA_128x128"])
+@pytest.mark.parametrize("variant", [None, "TC_PAIR", "TC_TF32X3", "GENERIC", "TMA_128x128"])
 def test_c_larger_than_2g_elements(variant):
     torch = torch_cuda()
     M, N, K = 70000, 32772, 32
@@ -46,7 +46,7 @@ def test_c_larger_than_2g_elements(variant):
     del dC
 
 
-@pytest.mark.parametrize("variant,expect", [(None, "TC_PAIR"), ("TC_TF32X3", "TC_TF32X3")])
+@pytest.mark.parametrize("variant,expect", [(None, "TC_PRESPLIT"), ("TC_PAIR", "TC_PAIR"), ("TC_TF32X3", "TC_TF32X3")])
 def test_strided_batch_offsets_beyond_2g(variant, expect):
     torch = torch_cuda()
     batch, M, N, K = 3000, 1024, 1024, 32

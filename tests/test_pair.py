@@ -62,9 +62,9 @@ def test_plan_shape():
         p = sg.sgemm_plan("N", "N", 4096, 4096, 4096, 1.5, 1 << 20, 4096, 1 << 20, 4096, -0.5, 1 << 20, 4096, 152)
     finally:
         sg.sgemm_set_variant_override("AUTO", 0)
-    # 16 x 32 pair tiles on 76 clusters: 5 whole rounds (380 tiles), the last 132 tiles by stream-K
+    # 16 x 32 pair tiles on 76 clusters: 6 whole rounds (456 tiles), the last 56 tiles by stream-K
     assert (p["variant_name"], p["tile_m"], p["tile_n"], p["grid_x"]) == ("TC_PAIR", 256, 128, 152)
-    assert (p["dp_tiles"], p["sk_tiles"], p["sk_iters"]) == (380, 132, 132 * 128)
+    assert (p["dp_tiles"], p["sk_tiles"], p["sk_iters"]) == (456, 56, 56 * 128)
     assert p["workspace_bytes"] == 2 * 152 * 128 * 128 * 4
 
 
