@@ -131,7 +131,6 @@ constexpr uint32_t kAccCols = 256;        // one 128 x 256 FP32 accumulator per 
 constexpr uint32_t kTmemCols = 512;
 constexpr int kFoldCols = 128;            // accumulator columns a folder thread owns
 constexpr int kFoldChunk = 32;            // columns loaded per round trip (register budget; 64 measured slower)
-constexpr uint16_t kPairMask = 0x3;
 static_assert(kAccBufs * kAccCols <= kTmemCols, "accumulators must fit in TMEM");
 static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA");
 
@@ -139,32 +138,6 @@ static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA");
 // both K-major, N = 256, M = 256 (the pair).
 constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
                             ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_id_x() {
-  uint32_t c;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(c));
-  return c;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
 
 // D (both CTAs' TMEM) = or += A (128 rows in each CTA's shared memory) * B (128 columns in each
 // CTA's shared memory); both operands K-major, described by the same descriptors in both CTAs.
@@ -174,23 +147,6 @@ __device__ __forceinline__ void mma_pair_ss(uint32_t d_tmem, uint64_t adesc, uin
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          bar),
-      "h"(kPairMask)
-      : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
-  asm volatile(
-      "{\n\t.reg .b32 ra;\n\t"
-      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
-      "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar),
-      "r"(rank)
       : "memory");
 }
 
@@ -206,20 +162,9 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-
 // Product and origin of pair tile `tile`.
 __device__ __forceinline__ void pair_tile_origin(const GemmParams& p, int tile, int& prod, int& m0, int& n0) {
-  const int tiles = p.tiles_m * p.tiles_n;
-  prod = tile / tiles;
-  int tm, tn;
-  tile_coords(tile - prod * tiles, p.tiles_m, p.tiles_n, tm, tn);
-  m0 = tm * BM;
-  n0 = tn * BN;
+  tile_origin_of(p, tile, BM, BN, prod, m0, n0);
 }
 
 // Tensor maps: the split operands as {K, rows, products} with boxes {32, 128, 1}, 128-byte

@@ -1,8 +1,10 @@
 // kernel_tc_common.cuh -- device helpers shared by the tensor-core SGEMM
-// kernels (kernel_tf32x3.cu: one CTA per tile; kernel_tc_pair.cu: CTA pairs):
-// the 3xTF32 operand split, the shared-memory matrix descriptor of the
-// K-major tiles, warp-level bounded waits, the tile raster and the
-// persistent data-parallel + stream-K schedule.
+// kernels (kernel_tf32x3.cu: one CTA per tile; kernel_tc_pair.cu: CTA pairs;
+// kernel_presplit.cu: CTA pairs on split operands): the 3xTF32 operand split,
+// the shared-memory matrix descriptor of the K-major tiles, warp-level
+// bounded waits, the tile raster, the persistent data-parallel + stream-K
+// schedule, and the cluster, pair-TMEM and cross-CTA barrier operations of
+// the CTA-pair kernels.
 #pragma once
 
 #include "device_utils.cuh"
@@ -116,6 +118,76 @@ __device__ __forceinline__ Segment cta_segment(const GemmParams& p, const CtaWor
     g.slot = (g.kb == 0 && g.ke == kt) ? -1 : sk_slot(p, c, j, kt);
   }
   return g;
+}
+// ---- CTA pairs (clusters of two CTAs on one TPC, tcgen05 cta_group::2)
+
+constexpr uint16_t kPairMask = 0x3;  // both CTAs of the cluster
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t c;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(c));
+  return c;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Pair TMEM allocation: one warp of each CTA of the pair executes these.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Arrives on the barrier at offset `bar` in both CTAs once every tcgen05.mma
+// this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          bar),
+      "h"(kPairMask)
+      : "memory");
+}
+
+// The shared::cluster address of this CTA's shared-memory offset `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on the barrier at offset `bar` of CTA `rank` of this cluster.  The
+// default (release, CTA scope) semantics suffice and cost no fence wait: what
+// an arrival publishes is already ordered before it by the arriving warp --
+// tensor-memory stores and loads by tcgen05.wait + tcgen05.fence, shared-memory
+// operand writes by fence.proxy.async -- and the consumer is the tensor core,
+// ordered after the issuer's wait by tcgen05.fence::after_thread_sync.  A
+// cluster-scope release would also wait for the warp's outstanding global
+// stores (the previous tile's C) on every arrival.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(map_to_rank(bar, rank)) : "memory");
+}
+
+// Product and origin (first row, first column) of tile `tile` of bm x bn tiles.
+__device__ __forceinline__ void tile_origin_of(const GemmParams& p, int tile, int bm, int bn, int& prod, int& m0,
+                                               int& n0) {
+  const int tiles = p.tiles_m * p.tiles_n;
+  prod = tile / tiles;
+  int tm, tn;
+  tile_coords(tile - prod * tiles, p.tiles_m, p.tiles_n, tm, tn);
+  m0 = tm * bm;
+  n0 = tn * bn;
 }
 
 }  // namespace tc

@@ -69,7 +69,6 @@ constexpr int kIssuers = 2;
 constexpr uint32_t kACols = 64;
 constexpr uint32_t kAColBase = kAccBufs * kAccCols;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint16_t kPairMask = 0x3;                 // both CTAs of the cluster
 static_assert(kAColBase + kSplitStages * kACols <= kTmemCols, "accumulators and A stages must fit in TMEM");
 static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA");
 
@@ -80,33 +79,6 @@ constexpr uint32_t kIdesc = (1u << 4)                 // D format: F32
                           | (2u << 10)                // B format: TF32
                           | ((uint32_t)(BN >> 3) << 17)
                           | ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_id_x() {
-  uint32_t c;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(c));
-  return c;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Pair TMEM allocation: one warp of each CTA of the pair executes these.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
 
 // D (both CTAs' TMEM) = or += A (both CTAs' TMEM, 128 lanes x 8 columns each) * B (64 rows of
 // K-major shared memory in each CTA at the same address)
@@ -119,41 +91,9 @@ __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint32_t a_tmem, uint6
       : "memory");
 }
 
-// Arrives on the barrier at offset `bar` in both CTAs once every tcgen05.mma
-// this thread issued so far has completed.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          bar),
-      "h"(kPairMask)
-      : "memory");
-}
-
-// Arrive on the barrier at offset `bar` of CTA `rank` of this cluster.  The
-// default (release, CTA scope) semantics suffice and cost no fence wait: what
-// an arrival publishes is already ordered before it by the arriving warp --
-// tensor-memory stores and loads by tcgen05.wait + tcgen05.fence, shared-memory
-// operand writes by fence.proxy.async -- and the consumer is the tensor core,
-// ordered after the issuer's wait by tcgen05.fence::after_thread_sync.  A
-// cluster-scope release would also wait for the warp's outstanding global
-// stores (the previous tile's C) on every arrival.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
-  asm volatile(
-      "{\n\t.reg .b32 ra;\n\t"
-      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
-      "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar),
-      "r"(rank)
-      : "memory");
-}
-
 // Product and origin (first row, first column) of pair tile `tile`.
 __device__ __forceinline__ void pair_tile_origin(const GemmParams& p, int tile, int& prod, int& m0, int& n0) {
-  const int tiles = p.tiles_m * p.tiles_n;
-  prod = tile / tiles;
-  int tm, tn;
-  tile_coords(tile - prod * tiles, p.tiles_m, p.tiles_n, tm, tn);
-  m0 = tm * BM;
-  n0 = tn * BN;
+  tile_origin_of(p, tile, BM, BN, prod, m0, n0);
 }
 
 // Raw tile layouts (as the TMA engine copies them), per CTA:

@@ -94,7 +94,7 @@ def test_unaligned_operands_take_edge_path(ops):
     assert np.array_equal(got[:, N:], C[:, N:]), "columns past N were written"
 
 
-@pytest.mark.parametrize("variant", ["AUTO", "GENERIC"])
+@pytest.mark.parametrize("variant", ["AUTO", "GENERIC", "TC_TF32X3", "TC_PAIR", "TC_PRESPLIT"])
 def test_beta_zero_does_not_read_nan_c(variant):
     rng = np.random.default_rng(3)
     M, N, K = 300, 260, 200
@@ -130,7 +130,7 @@ def test_zero_m_or_n_is_noop():
     assert bool((dC == 7.0).all())
 
 
-@pytest.mark.parametrize("variant", ["AUTO", "GENERIC", "TMA_64x256"])
+@pytest.mark.parametrize("variant", ["AUTO", "GENERIC", "TMA_64x256", "TC_TF32X3", "TC_PAIR", "TC_PRESPLIT"])
 def test_guard_bands_around_c(variant):
     """C lives inside a NaN-filled buffer (rows above/below, columns past N): only C changes."""
     torch = pytest.importorskip("torch")
@@ -165,7 +165,7 @@ def test_random_inputs_within_bound_all_ops():
         check_bound(got, ref, S, K, f"random {ta}{tb}")
 
 
-@pytest.mark.parametrize("variant", ["AUTO", "TMA_128x128"])
+@pytest.mark.parametrize("variant", ["AUTO", "TMA_128x128", "TC_TF32X3", "TC_PAIR", "TC_PRESPLIT"])
 def test_deterministic_and_transpose_identity(variant):
     """Two runs are bit-identical; sgemm('T','T', B, A) is the transpose of sgemm('N','N', A, B).
 
@@ -208,11 +208,11 @@ def test_nonfinite_inputs():
     C = np.zeros((M, N), np.float32)
     A[3, 5] = np.nan
     A[7, 9] = np.inf
-    for variant in ("AUTO", "TMA_128x128", "GENERIC"):
+    for variant in ("AUTO", "TMA_128x128", "GENERIC", "TC_TF32X3", "TC_PAIR", "TC_PRESPLIT"):
         got = gpu_sgemm("N", "N", M, N, K, 1.0, A.astype(np.float32), K, B, N, 0.0, C, N, variant=variant)
         assert np.all(np.isnan(got[3])), variant
         assert np.all(~np.isfinite(got[7])), variant
-        if variant != "AUTO":
+        if variant in ("TMA_128x128", "GENERIC"):
             assert np.all(np.isposinf(got[7])), variant
         mask = np.ones(M, bool)
         mask[[3, 7]] = False

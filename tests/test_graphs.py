@@ -55,6 +55,33 @@ def test_single_product_graph_replay(entry):
         check_exact(dC.cpu().numpy(), oracle.sgemm("N", "N", A, B, C, 1.5, -0.5), f"{entry} replay {rep}")
 
 
+def test_split_operand_graph_replay():
+    """The split-operand path (split passes of A and B, GEMM, fixup, and its workspace from the
+    pool) captured once and replayed on new inputs."""
+    torch = torch_cuda()
+    M, N, K = 1280, 1536, 1024
+    sg.sgemm_set_variant_override("TC_PRESPLIT", 0)
+    try:
+        plan = sg.sgemm_plan("N", "T", M, N, K, 1.0, 1 << 20, K, 1 << 20, K, 0.5, 1 << 20, N)
+        assert plan["variant_name"] == "TC_PRESPLIT" and plan["kernel_launches"] >= 3
+        dA = torch.empty((M, K), dtype=torch.float32, device="cuda")
+        dB = torch.empty((N, K), dtype=torch.float32, device="cuda")
+        dC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+        g = _capture(torch, lambda: sg.sgemm("N", "T", M, N, K, 1.5, dA, K, dB, K, -0.5, dC, N))
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
+    rng = np.random.default_rng(64)
+    for rep in range(2):
+        A, B, C = _dyadic(rng, (M, K)), _dyadic(rng, (N, K)), _dyadic(rng, (M, N))
+        dA.copy_(torch.from_numpy(A))
+        dB.copy_(torch.from_numpy(B))
+        dC.copy_(torch.from_numpy(C))
+        g.replay()
+        torch.cuda.synchronize()
+        assert sg.sgemm_sync_status() == 0
+        check_exact(dC.cpu().numpy(), oracle.sgemm("N", "T", A, B, C, 1.5, -0.5), f"split-operand replay {rep}")
+
+
 def test_graph_replays_back_to_back_accumulate():
     """beta = 1: five replays without a sync between them add op(A) op(B) five times, in order."""
     torch = torch_cuda()
