@@ -20,8 +20,10 @@
  *
  * Ownership: A, B, C are caller-owned DEVICE pointers on the current CUDA
  * device; the library never frees or retains them.  The library owns only
- * internal state: a per-device stream-ordered memory pool for split-K
- * partial sums (allocated and freed in stream order on the caller's stream),
+ * internal state: a per-device stream-ordered memory pool for its workspace
+ * (split-K / stream-K partial sums and, for SGEMM_VARIANT_TC_PRESPLIT, the
+ * split copies of op(A) and op(B): 4 x 4 bytes per element of each, at most
+ * 4 GiB; allocated and freed in stream order on the caller's stream),
  * per-device kernel attributes, and a per-device fault word.
  *
  * Semantics of special values (BLAS conventions; the pages do not say):
@@ -69,7 +71,7 @@ enum sgemm_status {
     SGEMM_OK = 0,
     SGEMM_ERR_CUDA = 1,        /* a CUDA runtime call failed (see sgemm_last_cuda_error) */
     SGEMM_ERR_TIMEOUT = 2,     /* a bounded in-kernel wait gave up (reported by sgemm_sync_status) */
-    SGEMM_ERR_NOMEM = 3,       /* split-K workspace could not be allocated */
+    SGEMM_ERR_NOMEM = 3,       /* the call's workspace (partial sums, split operands) could not be allocated */
     SGEMM_ERR_UNSUPPORTED = 4, /* a dimension or leading dimension >= 2^31, or no usable device */
     SGEMM_ERR_SCRATCH_LIMIT = 5 /* sgemm_noalloc: the problem needs more scratch than its static array */
     /* negative values: -(index of the invalid argument), BLAS xerbla style */
@@ -105,10 +107,12 @@ int sgemm(char transA, char transB, int64_t M, int64_t N, int64_t K,
           struct CUstream_st *stream);
 
 /*
- * Caller-supplied workspace: the same operation as sgemm() with the partial
- * sums of a split K (split-K slices, stream-K tiles shared by several CTAs)
- * in memory the caller owns, so a call allocates nothing, has no size limit
- * and captures into a CUDA graph as kernels only.
+ * Caller-supplied workspace: the same operation as sgemm() with its workspace
+ * -- the partial sums of a split K (split-K slices, stream-K tiles shared by
+ * several CTAs) and, for SGEMM_VARIANT_TC_PRESPLIT, the TF32 hi / FP32 lo
+ * copies of op(A) and op(B) -- in memory the caller owns, so a call
+ * allocates nothing, has no size limit and captures into a CUDA graph as
+ * kernels only.
  *
  * sgemm_workspace_size() stores in *bytes the workspace sgemm_ex() needs for
  * these arguments on the current device (0: none; equal to the
@@ -156,7 +160,7 @@ typedef struct sgemm_plan_t {
     int split_k;             /* number of K slices (1 = no split) */
     int kernel_launches;     /* kernels one sgemm() call launches */
     int64_t grid_x, grid_y;  /* CTAs of the GEMM kernel: tiles x K slices */
-    int64_t workspace_bytes; /* split-K / stream-K partial-sum bytes taken from the pool */
+    int64_t workspace_bytes; /* split-K / stream-K partial sums (+ TC_PRESPLIT: split operands), from the pool */
     int64_t smem_bytes;      /* dynamic shared memory per CTA */
     /* Tensor-core kernel only (persistent CTAs, grid_x of them): the first
      * dp_tiles output tiles are taken whole, round robin (CTA c: tiles c,
@@ -164,7 +168,9 @@ typedef struct sgemm_plan_t {
      * are then shared evenly by all CTAs (stream-K); split_k is the most CTAs
      * that share one output tile.  SGEMM_VARIANT_TC_PAIR: the same schedule
      * over 256 x 128 tiles with clusters of two CTAs as the unit (grid_x / 2
-     * clusters; split_k counts clusters).  SGEMM_VARIANT_TC_GROUPED: every tile is
+     * clusters; split_k counts clusters); SGEMM_VARIANT_TC_PRESPLIT: likewise
+     * over 256 x 256 tiles, and kernel_launches counts the split passes of A
+     * and B.  SGEMM_VARIANT_TC_GROUPED: every tile is
      * whole and holds 128 / tile_m products (tile_m = tile_n = 64: two, 32:
      * four), so dp_tiles = ceil(batch_count / (128 / tile_m)).  For
      * SGEMM_VARIANT_SMALL grid_x is the persistent grid (products dealt round

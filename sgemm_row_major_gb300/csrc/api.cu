@@ -285,12 +285,13 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
                         (pr.batch == 1 || (pr.stride_a % 4 == 0 && pr.stride_b % 4 == 0)) &&
                         (pr.ta ? pr.M : pr.K) % 4 == 0 && (pr.tb ? pr.K : pr.N) % 4 == 0 &&
                         ceil_div(pr.batch, small_grid) * ceil_div(pr.K, kSmallKChunk) < INT_MAX;
-  // Default: the 3xTF32 tensor-core kernel whenever TMA can load the operands
-  // (it beats the FP32 FFMA kernels on every measured shape), several
-  // products to a tile (block-diagonal) for a batch of at least one product
-  // per SM with M, N <= 64; the generic SIMT kernel otherwise.  The FP32 FFMA kernels
-  // (TMA-fed, small-product) stay selectable by override: IEEE FP32
-  // operations, exact Inf handling.
+  // Default: a 3xTF32 tensor-core kernel whenever TMA can load the operands
+  // (they beat the FP32 FFMA kernels on every measured shape): the
+  // split-operand kernel, the CTA-pair kernel or one CTA per tile by the
+  // rules below, several products to a tile (block-diagonal) for a batch of
+  // at least one product per SM with M, N <= 64; the generic SIMT kernel
+  // otherwise.  The FP32 FFMA kernels (TMA-fed, small-product) stay
+  // selectable by override: IEEE FP32 operations, exact Inf handling.
   const int64_t group = pr.M <= kGroupMaxMN / 2 && pr.N <= kGroupMaxMN / 2 ? 4 : 2;
   const bool group_ok = tma_ok && pr.M <= kGroupMaxMN && pr.N <= kGroupMaxMN;
   int variant = tma_ok ? SGEMM_VARIANT_TC_TF32X3 : SGEMM_VARIANT_GENERIC;
@@ -696,7 +697,7 @@ const char* sgemm_status_string(int status) {
     case SGEMM_OK: return "SGEMM_OK";
     case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: a CUDA runtime call failed";
     case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a bounded in-kernel wait gave up";
-    case SGEMM_ERR_NOMEM: return "SGEMM_ERR_NOMEM: split-K workspace allocation failed";
+    case SGEMM_ERR_NOMEM: return "SGEMM_ERR_NOMEM: workspace allocation failed";
     case SGEMM_ERR_UNSUPPORTED: return "SGEMM_ERR_UNSUPPORTED: dimension too large or no usable device";
     case SGEMM_ERR_SCRATCH_LIMIT:
       return "SGEMM_ERR_SCRATCH_LIMIT: split-K partial sums exceed sgemm_noalloc's static scratch array";
