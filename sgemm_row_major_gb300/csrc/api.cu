@@ -305,13 +305,15 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   if (tma_ok && pr.M > 128 && ceil_div(pr.M, 256) * ceil_div(pr.N, 128) * pr.batch >= clusters)
     variant = SGEMM_VARIANT_TC_PAIR;
   // Operands split once per call (TC_PRESPLIT) when the GEMM reuses them enough to amortize the
-  // split pass (read once, hi and lo written: 12 bytes per element of op(A) and op(B)) and every
-  // cluster gets a whole 256 x 256 tile; measured on GB300 (TFLOPS, split pass included, against
-  // TC_PAIR): 4096^3 266.7 / 209.1, 8192x4096x1024 239.5 / 195.1, 16384x1024x4096 244.6 / 218.8,
-  // 4097x3001x2053 200.2 / 166.1, 32 x 2048x1024x1024 with a shared B 226.0 / 202.8; slower at
-  // 64 x 512x1024x1024 (60 FLOP per split byte: 142.4 / 195.1) and on fewer tiles than clusters
-  // (1024^3 49.7 / 71.7).  The split arrays are capped at kMaxSplitBytes of workspace.
-  if (presplit_ok && pr.M > 128 && ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.batch >= clusters) {
+  // split pass (read once, hi and lo written: 12 bytes per element of op(A) and op(B)) and there
+  // are at least 4/5 as many 256 x 256 tiles as clusters; measured on GB300 (TFLOPS, split pass
+  // included, against TC_PAIR): 4096^3 266.7 / 209.1, 8192x4096x1024 239.5 / 195.1,
+  // 16384x1024x4096 244.6 / 218.8, 4097x3001x2053 200.2 / 166.1, 32 x 2048x1024x1024 with a
+  // shared B 226.0 / 202.8, 64 tiles: 2048x2048x1024 166.7 / 139.1, 2048^3 163.8 / 159.5; slower
+  // at 64 x 512x1024x1024 (60 FLOP per split byte: 142.4 / 195.1) and on fewer tiles (48 tiles:
+  // 2048x1536x2048 154.8 / 160.5; 1024^3 49.7 / 71.7).  The split arrays are capped at
+  // kMaxSplitBytes of workspace.
+  if (presplit_ok && pr.M > 128 && 5 * ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.batch >= 4 * clusters) {
     const SplitLayout sl = split_layout(pr.M, pr.N, pr.K, pr.batch, pr.stride_a, pr.stride_b, 0);
     const double flops = 2.0 * (double)pr.M * (double)pr.N * (double)pr.K * (double)pr.batch;
     if (flops >= kMinFlopPerSplitByte * 3.0 * (double)(sl.a_bytes + sl.b_bytes) &&

@@ -109,9 +109,11 @@ def test_planner_variants(lib):
     assert big["variant_name"] == "TC_PRESPLIT" and big["grid_x"] == 152 and big["grid_y"] == 1
     assert (big["tile_m"], big["tile_n"], big["tile_k"], big["threads"]) == (256, 256, 32, 320)
     assert big["smem_bytes"] <= 227 * 1024
-    # fewer 256 x 256 tiles than clusters (2048^3: 64 < 76): CTA pairs with 256 x 128 tiles
-    pair = plan("N", "N", 2048, 2048, 2048)
+    # fewer than 4/5 as many 256 x 256 tiles as clusters (2048 x 1536: 48 < 60.8): CTA pairs with
+    # 256 x 128 tiles; 2048^3 (64 tiles) splits its operands
+    pair = plan("N", "N", 2048, 1536, 2048)
     assert pair["variant_name"] == "TC_PAIR" and (pair["tile_m"], pair["tile_n"], pair["threads"]) == (256, 128, 608)
+    assert plan("N", "N", 2048, 2048, 2048)["variant_name"] == "TC_PRESPLIT"
     # fewer pair tiles than clusters (1024^3: 32 < 76), or M <= 128: one CTA per 128 x 128 tile
     one = plan("N", "N", 1024, 1024, 1024)
     assert one["variant_name"] == "TC_TF32X3" and one["tile_m"] == one["tile_n"] == 128
@@ -253,7 +255,7 @@ def test_batched_planner(lib):
     assert p["variant_name"] == "TC_PAIR" and p["grid_x"] == 152
     assert p["dp_tiles"] + p["sk_tiles"] == 64 * 16 and p["sk_tiles"] == 76 + 64 * 16 % 76
     # shared weight (stride 0) keeps the tensor-core path
-    assert bplan("N", "N", 512, 1024, 1024, 8, 512 * 1024, 0, 512 * 1024)["variant_name"] == "TC_PAIR"
+    assert bplan("N", "N", 512, 1024, 1024, 8, 512 * 1024, 0, 512 * 1024)["variant_name"] == "TC_PRESPLIT"
     assert bplan("N", "N", 512, 1024, 1024, 4, 512 * 1024, 0, 512 * 1024)["variant_name"] == "TC_TF32X3"
     # few tiles in all: stream-K over the tiles of every product
     s = bplan("N", "N", 64, 4096, 16384, 2, 64 * 16384, 0, 64 * 4096)
