@@ -234,6 +234,32 @@ def test_split_operand_rule(lib):
     assert p["workspace_bytes"] == slots + 2 * 8192 * 1024 * 4 + 2 * 4096 * 1024 * 4
 
 
+def test_split_operand_workspace_layout(lib):
+    """Workspace of TC_PRESPLIT: stream-K slots (2 per CTA, 128 x 256 floats) when a tile is shared,
+    then hi and lo of op(A) and op(B) as rows of round4(K) floats, one copy per product whose operand
+    differs, each part rounded up to 256 bytes."""
+    def r256(x):
+        return (x + 255) // 256 * 256
+    sg.sgemm_set_variant_override("TC_PRESPLIT", 0)
+    try:
+        # K = 1001 -> rows of 1004 floats; 6 products sharing A (stride 0)
+        M, N, K, batch = 300, 520, 1001, 6
+        b = bplan("N", "N", M, N, K, batch, 0, 1004 * N, M * N, lda=1004, ldb=N)
+        assert b["variant_name"] == "TC_PRESPLIT"
+        slots = 2 * b["grid_x"] * 128 * 256 * 4 if b["kernel_launches"] == 4 else 0
+        a_part, b_part = r256(1 * M * 1004 * 4), r256(batch * N * 1004 * 4)
+        assert b["workspace_bytes"] == r256(slots) + 2 * a_part + 2 * b_part
+        # one tile, no sharing: no slots, three launches (two split passes and the GEMM)
+        one = plan("N", "N", 256, 256, 64)
+        assert (one["variant_name"], one["kernel_launches"]) == ("TC_PRESPLIT", 3)
+        assert one["workspace_bytes"] == 2 * r256(256 * 64 * 4) + 2 * r256(256 * 64 * 4)
+        # outside the split pass's grid limits (K / 32 > 65535, more than 65535 products): CTA pairs
+        assert plan("N", "N", 512, 512, 32 * 65536)["variant_name"] == "TC_PAIR"
+        assert bplan("N", "N", 256, 256, 32, 65536, 256 * 32, 32 * 256, 256 * 256)["variant_name"] == "TC_PAIR"
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
+
+
 def test_plan_rejects_huge_dimensions(lib):
     with pytest.raises(sg.SgemmError) as e:
         plan("N", "N", 1 << 31, 8, 8, lda=8, ldb=8)
