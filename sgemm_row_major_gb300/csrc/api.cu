@@ -247,44 +247,48 @@ constexpr int64_t kPresplitSmemBytes = 3 * 65536 + 1024;
 constexpr double kMinFlopPerSplitByte = 128.0;
 constexpr int64_t kMaxSplitBytes = int64_t{4} << 30;
 
-// The planner: a pure function of the problem, the SM count, the number of
-// co-resident CTA-pair clusters (<= 0: sm_count / 2) and the override.
-// allow_presplit = false (sgemm_noalloc: the split arrays need workspace)
-// plans TC_PRESPLIT as TC_PAIR.
-int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clusters = 0,
-              bool allow_presplit = true) {
-  *plan = sgemm_plan_t{};
-  plan->split_k = 1;
-  if (pr.M == 0 || pr.N == 0 || pr.batch == 0) {
-    plan->variant = SGEMM_VARIANT_NONE;
-    return SGEMM_OK;
-  }
-  if (pr.M > INT_MAX || pr.N > INT_MAX || pr.K > INT_MAX || pr.batch > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
-  if (pr.K == 0 || pr.alpha == 0.0f) {
-    plan->variant = SGEMM_VARIANT_SCALE;
-    plan->kernel_launches = 1;
-    plan->threads = 256;
-    return SGEMM_OK;
-  }
+// Which kernels can run a problem (alignment, extents, grid limits) and the
+// derived quantities the planner's rules use.
+struct Eligibility {
+  bool tma = false;       // TMA can load A and B (tensor-core kernels, TMA-fed FFMA kernels)
+  bool small = false;     // the small-product FP32 kernel can run it
+  bool group = false;     // block-diagonal groups on the tensor cores
+  bool presplit = false;  // the split-operand kernel (and its split pass) can run it
+  int64_t group_size = 2;   // products per tile in a group (4 when M, N <= 32)
+  int64_t small_grid = 0;   // persistent grid of the small-product kernel
+  int64_t clusters = 1;     // co-resident CTA-pair clusters
+};
+
+Eligibility eligibility(const Problem& pr, int sm_count, int pair_clusters, bool allow_presplit) {
+  Eligibility e;
   // TMA needs 16-byte aligned bases and row strides that are multiples of 16
   // bytes; in a batch, every product's base too (a stride that is a multiple
   // of 4 floats), and matrices that do not overlap (or one shared matrix).
   const auto batch_ok = [&](int64_t stride, int64_t rows, int64_t ld) {
     return pr.batch == 1 || stride == 0 || (stride % 4 == 0 && stride >= rows * ld);
   };
-  const bool tma_ok = aligned16(pr.A) && aligned16(pr.B) && pr.lda % 4 == 0 && pr.ldb % 4 == 0 &&
-                      batch_ok(pr.stride_a, pr.ta ? pr.K : pr.M, pr.lda) &&
-                      batch_ok(pr.stride_b, pr.tb ? pr.N : pr.K, pr.ldb);
+  e.tma = aligned16(pr.A) && aligned16(pr.B) && pr.lda % 4 == 0 && pr.ldb % 4 == 0 &&
+          batch_ok(pr.stride_a, pr.ta ? pr.K : pr.M, pr.lda) && batch_ok(pr.stride_b, pr.tb ? pr.N : pr.K, pr.ldb);
   // The small-product kernel reads whole float4s along the contiguous axis
   // of each operand, so that extent must be a multiple of 4 as well.
   // Its persistent grid deals products round-robin; a CTA's (product, K
   // chunk) items are counted in an int.
-  const int64_t small_grid = std::min<int64_t>(pr.batch, kSmallCtasPerSm * std::max(1, sm_count));
-  const bool small_ok = pr.M <= kSmallMaxMN && pr.N <= kSmallMaxMN && aligned16(pr.A) && aligned16(pr.B) &&
-                        pr.lda % 4 == 0 && pr.ldb % 4 == 0 &&
-                        (pr.batch == 1 || (pr.stride_a % 4 == 0 && pr.stride_b % 4 == 0)) &&
-                        (pr.ta ? pr.M : pr.K) % 4 == 0 && (pr.tb ? pr.K : pr.N) % 4 == 0 &&
-                        ceil_div(pr.batch, small_grid) * ceil_div(pr.K, kSmallKChunk) < INT_MAX;
+  e.small_grid = std::min<int64_t>(pr.batch, kSmallCtasPerSm * std::max(1, sm_count));
+  e.small = pr.M <= kSmallMaxMN && pr.N <= kSmallMaxMN && aligned16(pr.A) && aligned16(pr.B) &&
+            pr.lda % 4 == 0 && pr.ldb % 4 == 0 && (pr.batch == 1 || (pr.stride_a % 4 == 0 && pr.stride_b % 4 == 0)) &&
+            (pr.ta ? pr.M : pr.K) % 4 == 0 && (pr.tb ? pr.K : pr.N) % 4 == 0 &&
+            ceil_div(pr.batch, e.small_grid) * ceil_div(pr.K, kSmallKChunk) < INT_MAX;
+  e.group_size = pr.M <= kGroupMaxMN / 2 && pr.N <= kGroupMaxMN / 2 ? 4 : 2;
+  e.group = e.tma && pr.M <= kGroupMaxMN && pr.N <= kGroupMaxMN;
+  e.clusters = std::max(1, pair_clusters > 0 ? pair_clusters : sm_count / 2);
+  // (the split pass's transposing grid: K / 32 and the products in grid dimensions y and z)
+  e.presplit = e.tma && allow_presplit && ceil_div(pr.K, 32) <= 65535 && pr.batch <= 65535;
+  return e;
+}
+
+// The planner's default kernel, then the process-wide override (a forced
+// variant whose conditions the problem breaks falls back).
+int choose_variant(const Problem& pr, const Eligibility& e, int sm_count) {
   // Default: a 3xTF32 tensor-core kernel whenever TMA can load the operands
   // (they beat the FP32 FFMA kernels on every measured shape): the
   // split-operand kernel, the CTA-pair kernel or one CTA per tile by the
@@ -292,17 +296,12 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   // at least one product per SM with M, N <= 64; the generic SIMT kernel
   // otherwise.  The FP32 FFMA kernels (TMA-fed, small-product) stay
   // selectable by override: IEEE FP32 operations, exact Inf handling.
-  const int64_t group = pr.M <= kGroupMaxMN / 2 && pr.N <= kGroupMaxMN / 2 ? 4 : 2;
-  const bool group_ok = tma_ok && pr.M <= kGroupMaxMN && pr.N <= kGroupMaxMN;
-  int variant = tma_ok ? SGEMM_VARIANT_TC_TF32X3 : SGEMM_VARIANT_GENERIC;
+  int variant = e.tma ? SGEMM_VARIANT_TC_TF32X3 : SGEMM_VARIANT_GENERIC;
   // CTA pairs (256 x 128 tiles) when every cluster gets at least one whole
   // tile: measured on GB300 2-5% faster than one CTA per 128 x 128 tile on
   // 2048^3 .. 16384 x 1024 x 4096, slower on fewer tiles (1024^3: 70.5 against
   // 74.3 TFLOPS) and on M <= 128 (half of every pair tile idle).
-  const int64_t clusters = std::max(1, pair_clusters > 0 ? pair_clusters : sm_count / 2);
-  // (the split pass's transposing grid: K / 32 and the products in grid dimensions y and z)
-  const bool presplit_ok = tma_ok && allow_presplit && ceil_div(pr.K, 32) <= 65535 && pr.batch <= 65535;
-  if (tma_ok && pr.M > 128 && ceil_div(pr.M, 256) * ceil_div(pr.N, 128) * pr.batch >= clusters)
+  if (e.tma && pr.M > 128 && ceil_div(pr.M, 256) * ceil_div(pr.N, 128) * pr.batch >= e.clusters)
     variant = SGEMM_VARIANT_TC_PAIR;
   // Operands split once per call (TC_PRESPLIT) when the GEMM reuses them enough to amortize the
   // split pass (read once, hi and lo written: 12 bytes per element of op(A) and op(B)) and there
@@ -313,54 +312,65 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   // at 64 x 512x1024x1024 (60 FLOP per split byte: 142.4 / 195.1) and on fewer tiles (48 tiles:
   // 2048x1536x2048 154.8 / 160.5; 1024^3 49.7 / 71.7).  The split arrays are capped at
   // kMaxSplitBytes of workspace.
-  if (presplit_ok && pr.M > 128 && 5 * ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.batch >= 4 * clusters) {
+  if (e.presplit && pr.M > 128 && 5 * ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.batch >= 4 * e.clusters) {
     const SplitLayout sl = split_layout(pr.M, pr.N, pr.K, pr.batch, pr.stride_a, pr.stride_b, 0);
     const double flops = 2.0 * (double)pr.M * (double)pr.N * (double)pr.K * (double)pr.batch;
     if (flops >= kMinFlopPerSplitByte * 3.0 * (double)(sl.a_bytes + sl.b_bytes) &&
         2 * (sl.a_bytes + sl.b_bytes) <= kMaxSplitBytes)
       variant = SGEMM_VARIANT_TC_PRESPLIT;
   }
-  if (group_ok && pr.batch >= sm_count) variant = SGEMM_VARIANT_TC_GROUPED;
-  const int ov = g_override_variant.load();
-  if (ov == SGEMM_VARIANT_GENERIC || ov == SGEMM_VARIANT_TMA_128x128 || ov == SGEMM_VARIANT_TMA_64x256 ||
-      ov == SGEMM_VARIANT_TC_TF32X3)
-    variant = (ov == SGEMM_VARIANT_GENERIC || tma_ok) ? ov : SGEMM_VARIANT_GENERIC;
-  if (ov == SGEMM_VARIANT_SMALL) variant = small_ok ? ov : SGEMM_VARIANT_GENERIC;
-  if (ov == SGEMM_VARIANT_TC_GROUPED) variant = group_ok ? ov : SGEMM_VARIANT_GENERIC;
-  if (ov == SGEMM_VARIANT_TC_PAIR) variant = tma_ok ? ov : SGEMM_VARIANT_GENERIC;
-  if (ov == SGEMM_VARIANT_TC_PRESPLIT)
-    variant = presplit_ok ? ov : tma_ok ? SGEMM_VARIANT_TC_PAIR : SGEMM_VARIANT_GENERIC;
-  if (variant == SGEMM_VARIANT_TC_GROUPED) {
-    // whole tiles (a group of products each) on one persistent CTA per SM, no stream-K
-    const int64_t tiles = ceil_div(pr.batch, group);
-    const int64_t kt = ceil_div(pr.K, 32);
-    const int64_t grid = std::min<int64_t>(tiles, std::max(1, sm_count));
-    if ((tiles / grid + 1) * kt > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
-    plan->variant = variant;
-    plan->tile_m = plan->tile_n = (int)(128 / group);
-    plan->tile_k = 32;
-    plan->stages = 4;
-    plan->threads = 608;
-    plan->smem_bytes = 4 * 32768 + 2 * 32768 + 1024;
-    plan->kernel_launches = 1;
-    plan->grid_x = grid;
-    plan->grid_y = 1;
-    plan->dp_tiles = tiles;
-    return SGEMM_OK;
-  }
-  if (variant == SGEMM_VARIANT_SMALL) {
-    plan->variant = variant;
-    plan->tile_m = plan->tile_n = (int)kSmallMaxMN;
-    plan->tile_k = (int)kSmallKChunk;
-    plan->stages = 2;
-    plan->threads = 64;
-    plan->smem_bytes = 2 * 2 * kSmallMaxMN * kSmallKChunk * 4;
-    plan->kernel_launches = 1;
-    plan->grid_x = small_grid;
-    plan->grid_y = 1;
-    return SGEMM_OK;
-  }
+  if (e.group && pr.batch >= sm_count) variant = SGEMM_VARIANT_TC_GROUPED;
 
+  switch (g_override_variant.load()) {
+    case SGEMM_VARIANT_GENERIC: return SGEMM_VARIANT_GENERIC;
+    case SGEMM_VARIANT_TMA_128x128: return e.tma ? SGEMM_VARIANT_TMA_128x128 : SGEMM_VARIANT_GENERIC;
+    case SGEMM_VARIANT_TMA_64x256: return e.tma ? SGEMM_VARIANT_TMA_64x256 : SGEMM_VARIANT_GENERIC;
+    case SGEMM_VARIANT_TC_TF32X3: return e.tma ? SGEMM_VARIANT_TC_TF32X3 : SGEMM_VARIANT_GENERIC;
+    case SGEMM_VARIANT_SMALL: return e.small ? SGEMM_VARIANT_SMALL : SGEMM_VARIANT_GENERIC;
+    case SGEMM_VARIANT_TC_GROUPED: return e.group ? SGEMM_VARIANT_TC_GROUPED : SGEMM_VARIANT_GENERIC;
+    case SGEMM_VARIANT_TC_PAIR: return e.tma ? SGEMM_VARIANT_TC_PAIR : SGEMM_VARIANT_GENERIC;
+    case SGEMM_VARIANT_TC_PRESPLIT:
+      return e.presplit ? SGEMM_VARIANT_TC_PRESPLIT : e.tma ? SGEMM_VARIANT_TC_PAIR : SGEMM_VARIANT_GENERIC;
+    default: return variant;
+  }
+}
+
+// Block-diagonal groups: whole tiles (a group of products each) on one persistent CTA per SM,
+// no stream-K.
+int plan_grouped(const Problem& pr, const Eligibility& e, int sm_count, sgemm_plan_t* plan) {
+  const int64_t tiles = ceil_div(pr.batch, e.group_size);
+  const int64_t kt = ceil_div(pr.K, 32);
+  const int64_t grid = std::min<int64_t>(tiles, std::max(1, sm_count));
+  if ((tiles / grid + 1) * kt > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
+  plan->variant = SGEMM_VARIANT_TC_GROUPED;
+  plan->tile_m = plan->tile_n = (int)(128 / e.group_size);
+  plan->tile_k = 32;
+  plan->stages = 4;
+  plan->threads = 608;
+  plan->smem_bytes = 4 * 32768 + 2 * 32768 + 1024;
+  plan->kernel_launches = 1;
+  plan->grid_x = grid;
+  plan->grid_y = 1;
+  plan->dp_tiles = tiles;
+  return SGEMM_OK;
+}
+
+int plan_small(const Eligibility& e, sgemm_plan_t* plan) {
+  plan->variant = SGEMM_VARIANT_SMALL;
+  plan->tile_m = plan->tile_n = (int)kSmallMaxMN;
+  plan->tile_k = (int)kSmallKChunk;
+  plan->stages = 2;
+  plan->threads = 64;
+  plan->smem_bytes = 2 * 2 * kSmallMaxMN * kSmallKChunk * 4;
+  plan->kernel_launches = 1;
+  plan->grid_x = e.small_grid;
+  plan->grid_y = 1;
+  return SGEMM_OK;
+}
+
+// Kernels over output tiles: the tensor-core kernels' persistent schedule, or grid.y K slices
+// for the FFMA and generic kernels.
+int plan_tiled(const Problem& pr, const Eligibility& e, int variant, int sm_count, sgemm_plan_t* plan) {
   int bm, bn, bk, threads, stages;
   int64_t smem = 0;
   if (variant == SGEMM_VARIANT_GENERIC) {
@@ -394,7 +404,7 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   if (variant == SGEMM_VARIANT_TC_TF32X3) return plan_stream_k(tiles, kt, sm_count, plan);
   if (variant == SGEMM_VARIANT_TC_PAIR) {
     // the stream-K schedule with clusters as the unit; 2 CTAs, 2 partial-sum slots each, per cluster
-    const int s = plan_stream_k(tiles, kt, (int)clusters, plan);
+    const int s = plan_stream_k(tiles, kt, (int)e.clusters, plan);
     plan->grid_x *= 2;
     plan->workspace_bytes *= 2;
     return s;
@@ -402,7 +412,7 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   if (variant == SGEMM_VARIANT_TC_PRESPLIT) {
     // as TC_PAIR with 256 x 256 tiles (slots of 128 x 256 floats per CTA), plus the split arrays;
     // launches: the split pass of A and of B, the GEMM, the fixup when a tile is shared
-    const int s = plan_stream_k(tiles, kt, (int)clusters, plan);
+    const int s = plan_stream_k(tiles, kt, (int)e.clusters, plan);
     if (s != SGEMM_OK) return s;
     plan->grid_x *= 2;
     plan->workspace_bytes *= 4;
@@ -428,6 +438,32 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   plan->grid_y = split;
   plan->workspace_bytes = split > 1 ? pr.batch * split * pr.M * (ceil_div(pr.N, 4) * 4) * 4 : 0;
   return SGEMM_OK;
+}
+
+// The planner: a pure function of the problem, the SM count, the number of
+// co-resident CTA-pair clusters (<= 0: sm_count / 2) and the override.
+// allow_presplit = false (sgemm_noalloc: the split arrays need workspace)
+// plans TC_PRESPLIT as TC_PAIR.
+int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clusters = 0,
+              bool allow_presplit = true) {
+  *plan = sgemm_plan_t{};
+  plan->split_k = 1;
+  if (pr.M == 0 || pr.N == 0 || pr.batch == 0) {
+    plan->variant = SGEMM_VARIANT_NONE;
+    return SGEMM_OK;
+  }
+  if (pr.M > INT_MAX || pr.N > INT_MAX || pr.K > INT_MAX || pr.batch > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
+  if (pr.K == 0 || pr.alpha == 0.0f) {
+    plan->variant = SGEMM_VARIANT_SCALE;
+    plan->kernel_launches = 1;
+    plan->threads = 256;
+    return SGEMM_OK;
+  }
+  const Eligibility e = eligibility(pr, sm_count, pair_clusters, allow_presplit);
+  const int variant = choose_variant(pr, e, sm_count);
+  if (variant == SGEMM_VARIANT_TC_GROUPED) return plan_grouped(pr, e, sm_count, plan);
+  if (variant == SGEMM_VARIANT_SMALL) return plan_small(e, plan);
+  return plan_tiled(pr, e, variant, sm_count, plan);
 }
 
 // TC_PRESPLIT: the split pass of op(A) and op(B) into the workspace ([stream-K slots][A hi][A lo]
