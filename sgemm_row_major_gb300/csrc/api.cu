@@ -78,7 +78,11 @@ int device_state(int* device_out, DeviceState** st_out) {
     if (err == cudaSuccess) err = prepare_small_gemm();
     if (err == cudaSuccess) err = prepare_tc_pair();
     if (err == cudaSuccess) err = prepare_presplit();
-    if (err == cudaSuccess) err = tc_pair_max_clusters(&st.pair_clusters);
+    // co-resident CTA-pair clusters; if the occupancy query fails, the planner assumes SMs / 2
+    if (err == cudaSuccess && tc_pair_max_clusters(&st.pair_clusters) != cudaSuccess) {
+      st.pair_clusters = 0;
+      (void)cudaGetLastError();  // the failed query must not surface at a later launch check
+    }
     if (err == cudaSuccess) {
       cudaMemPoolProps props = {};
       props.allocType = cudaMemAllocationTypePinned;
