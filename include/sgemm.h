@@ -37,14 +37,19 @@
  * ldb % 4 == 0) runs on the tensor cores with each float split into two
  * TF32 parts (3 products per term, partial sums folded in FP32 every 32 k);
  * results meet |C - C_exact| <= (K+2) 2^-24 (|alpha| sum|a b| + |beta c|) and
- * are deterministic, but are not the IEEE FP32 FMA sums of a SIMT loop, and
- * an Inf in A or B may give NaN where IEEE arithmetic gives Inf (a NaN input
- * gives NaN on every path); so may a finite input within 2^-11 of FLT_MAX,
- * whose TF32 part rounds up to Inf.  Scaling A and B by powers of two scales C
- * exactly, as in FP32 arithmetic, down to products near the FP32 subnormal
- * range.  The FP32 FFMA kernels (IEEE operations, exact Inf
- * handling) are selected with sgemm_set_variant_override(SGEMM_VARIANT_TMA_128x128
- * or SGEMM_VARIANT_TMA_64x256, 0); unaligned operands always use the FFMA path.
+ * are deterministic, but are not the IEEE FP32 FMA sums of a SIMT loop.
+ * Inputs the split cannot carry -- +-Inf, and finite values of magnitude
+ * >= (2 - 2^-11) 2^127, whose TF32 part would round to Inf -- make the
+ * tensor-core sums they enter NaN; every NaN sum is computed again with FP32
+ * FMAs (k ascending), so the results are those of IEEE FP32 arithmetic:
+ * +-Inf where the definition gives +-Inf, NaN for Inf * 0, Inf - Inf and NaN
+ * inputs, and finite values within the bound above.  As in any FP32
+ * accumulation, products or partial sums beyond FLT_MAX overflow to +-Inf.
+ * Scaling A and B by powers of two scales C exactly, as in FP32 arithmetic,
+ * down to products near the FP32 subnormal range.  The FP32 FFMA kernels
+ * (IEEE operations throughout) are selected with
+ * sgemm_set_variant_override(SGEMM_VARIANT_TMA_128x128 or
+ * SGEMM_VARIANT_TMA_64x256, 0); unaligned operands always use the FFMA path.
  *
  * Errors: invalid arguments return -(argument index) (1 = transA ... 14 =
  * stream) before anything is launched, and C is untouched.  CUDA launch or

@@ -515,6 +515,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   p.C = C;
   p.lda = pr.lda;
   p.ldb = pr.ldb;
+  p.ta = pr.ta;
+  p.tb = pr.tb;
   p.ldc = pr.ldc;
   p.c_vec = aligned16(C) && pr.ldc % 4 == 0 && (pr.batch == 1 || pr.stride_c % 4 == 0);
   p.batch = (int)pr.batch;

@@ -391,6 +391,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         pair_tile_origin(p, g.tile, prod, m0, n0);
         const int row = m0 + BMC * (int)rank + 32 * q + lane;
         if (row < p.M) {
+          repair_nans(p, prod, row, n0 + kFoldCols * half, master2);
           float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
           if (p.c_vec) store_row<true>(p, crow, n0 + kFoldCols * half, master2);
           else         store_row<false>(p, crow, n0 + kFoldCols * half, master2);
@@ -459,6 +460,7 @@ __global__ void __launch_bounds__(kFixupThreads) presplit_fixup_kernel(const Gem
       const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[i] * (BMC * BN));
       v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
     }
+    repair_nans4(p, prod, row, col, v);
     float* cp = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
     if (CVEC && col + 3 < p.N) {
       float4 o;

@@ -52,6 +52,94 @@ __device__ __forceinline__ void split4(const float4 x, float4& hi, float4& lo) {
   lo = make_float4(l01.x, l01.y, l23.x, l23.y);
 }
 
+// ---- Results the split cannot carry
+//
+// The split fails for two kinds of input: a finite x at or above (2 - 2^-11) *
+// 2^127 in magnitude, whose hi part rounds to Inf (lo = x - hi is then -Inf),
+// and x = +-Inf (hi = Inf, lo = Inf - Inf = NaN).  Every tensor-core product
+// such an element takes part in is then Inf - Inf, Inf * 0 or NaN, so the
+// folded sum is NaN, although the definition C_ij = sum_k op(A)_ik op(B)_kj
+// (klklkl10086.github.io "Sgemm单精度矩阵乘法", 问题定义) gives a finite sum
+// for the first kind and +-Inf (or NaN) for the second.  Nothing else makes
+// the folded sum NaN except a NaN operand (or Inf - Inf between products),
+// where the definition gives NaN too.  So the epilogues test the folded sums
+// of a thread once per tile (a chain of packed adds and one compare) and
+// compute each NaN sum again with FP32 FMAs over op(A)'s row and op(B)'s
+// column, k ascending, 32-k partial sums added into a running sum as the
+// fold does: IEEE FP32 semantics for Inf and NaN, the per-element error of a
+// plain FP32 dot product for finite results.  The hot loop gains nothing;
+// calls whose results are mostly NaN or +-Inf run this slow path for them.
+
+// sum_k a[k * as] * b[k * bs] with FP32 FMAs in k order.  A NaN running sum
+// is final, so the loop stops at it.
+__device__ __forceinline__ float fp32_dot(const float* __restrict__ a, int64_t as, const float* __restrict__ b,
+                                          int64_t bs, int K) {
+  float sum = 0.0f;
+#pragma unroll 1
+  for (int k0 = 0; k0 < K; k0 += 32) {
+    const int k1 = min(K, k0 + 32);
+    float part = 0.0f;
+#pragma unroll 1
+    for (int k = k0; k < k1; ++k) part = __fmaf_rn(a[(int64_t)k * as], b[(int64_t)k * bs], part);
+    sum = __fadd_rn(sum, part);
+    if (sum != sum) break;
+  }
+  return sum;
+}
+
+// True when some value of m is NaN or +-Inf (or the packed sum of the values
+// overflows, which only sends the caller to its per-element NaN test).
+template <int N2>
+__device__ __forceinline__ bool any_nonfinite(const float2 (&m)[N2]) {
+  float2 s0 = m[0], s1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int e = 1; e < N2; ++e) {
+    if (e & 1) s1 = __fadd2_rn(s1, m[e]);
+    else       s0 = __fadd2_rn(s0, m[e]);
+  }
+  s0 = __fadd2_rn(s0, s1);
+  return !(fabsf(s0.x + s0.y) <= 3.402823466e38f);
+}
+
+// Replaces each NaN sum v[i] (row `row`, column col0 + i < N of product
+// `prod`, i < n) by the FP32 dot product of op(A)'s row and op(B)'s column.
+// v is a local array: only this cold path indexes it at run time.
+__device__ __forceinline__ void repair_row(const GemmParams& p, int prod, int row, int col0, float* v, int n) {
+  const float* a = p.A + (int64_t)prod * p.stride_a + (p.ta ? (int64_t)row : (int64_t)row * p.lda);
+  const float* b0 = p.B + (int64_t)prod * p.stride_b;
+  const int64_t as = p.ta ? p.lda : 1, bs = p.tb ? 1 : p.ldb;
+#pragma unroll 1
+  for (int i = 0; i < n; ++i) {
+    const int col = col0 + i;
+    if (v[i] != v[i] && col < p.N)
+      v[i] = fp32_dot(a, as, b0 + (p.tb ? (int64_t)col * p.ldb : (int64_t)col), bs, p.K);
+  }
+}
+
+// The check and repair of a folder thread's sums m (row `row`, columns col0 ..
+// col0 + 2 * N2 - 1 of product `prod`); the caller has checked the row.
+template <int N2>
+__device__ __forceinline__ void repair_nans(const GemmParams& p, int prod, int row, int col0, float2 (&m)[N2]) {
+  if (!any_nonfinite(m)) return;
+  float v[2 * N2];
+#pragma unroll
+  for (int e = 0; e < N2; ++e) {
+    v[2 * e] = m[e].x;
+    v[2 * e + 1] = m[e].y;
+  }
+  repair_row(p, prod, row, col0, v, 2 * N2);
+#pragma unroll
+  for (int e = 0; e < N2; ++e) m[e] = make_float2(v[2 * e], v[2 * e + 1]);
+}
+
+// The same for the four sums of a fixup thread (columns col .. col + 3).
+__device__ __forceinline__ void repair_nans4(const GemmParams& p, int prod, int row, int col, float4& s) {
+  if (fabsf(s.x + s.y + s.z + s.w) <= 3.402823466e38f) return;
+  float v[4] = {s.x, s.y, s.z, s.w};
+  repair_row(p, prod, row, col, v, 4);
+  s = make_float4(v[0], v[1], v[2], v[3]);
+}
+
 __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, int& tm, int& tn) {
   constexpr int kGroupM = 8;
   const int span = kGroupM * tiles_n;

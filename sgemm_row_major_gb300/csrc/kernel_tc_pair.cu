@@ -402,6 +402,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int row = m0 + BMC * (int)rank + 32 * q + lane;
         const int c0 = n0 + 64 * half;
         if (row < p.M) {
+          repair_nans(p, prod, row, c0, master2);
           float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -487,6 +488,7 @@ __global__ void __launch_bounds__(kFixupThreads) pair_fixup_kernel(const GemmPar
     const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[i] * (BMC * BN));
     v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
   }
+  repair_nans4(p, prod, row, col, v);
   float* cp = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
   if (CVEC && col + 3 < p.N) {
     float4 o;

@@ -481,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int row = m0 + 32 * q + lane;
         if (row < p.M && (G == 1 || prod < p.batch)) {
+          repair_nans(p, prod, row, c0, master2);
           float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
 #pragma unroll
           for (int e = 0; e < kCols / 4; ++e) {
@@ -559,6 +560,7 @@ __global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(const Gemm
     const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[i] * (BM * BN));
     v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
   }
+  repair_nans4(p, prod, row, col, v);
   float* cp = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
   if (CVEC && col + 3 < p.N) {
     float4 o;

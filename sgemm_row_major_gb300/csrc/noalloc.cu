@@ -105,6 +105,8 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
   p.C = C;
   p.lda = lda;
   p.ldb = ldb;
+  p.ta = ta ? 1 : 0;
+  p.tb = tb ? 1 : 0;
   p.ldc = ldc;
   p.c_vec = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0;
   p.timeout_ns = 2000ull * 1000000ull;

@@ -18,12 +18,13 @@ namespace sgemm_impl {
 struct GemmParams {
   int M = 0, N = 0, K = 0;
   float alpha = 1.0f, beta = 0.0f;
-  const float* A = nullptr;  // used by the generic kernel (the TMA kernels read through tensor maps)
+  const float* A = nullptr;  // the generic kernel's operands; the tensor-core kernels' NaN repair reads them
   const float* B = nullptr;
   float* C = nullptr;        // final output (split == 1) ...
   float* ws = nullptr;       // ... or the partial-sum workspace [batch][split][M][ws_ld] (split > 1)
   int64_t lda = 0, ldb = 0, ldc = 0, ws_ld = 0;
   int64_t stride_a = 0, stride_b = 0, stride_c = 0;  // elements between consecutive products
+  int ta = 0, tb = 0;            // 1: op(A) / op(B) is the transpose of the stored matrix
   int batch = 1;
   int za = 0, zb = 0;            // TMA kernels: 1 = the map's third coordinate is the product index
   int k_tiles_per_split = 0;     // K tiles (of the kernel's BK) per slice

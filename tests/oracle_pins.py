@@ -10,7 +10,9 @@ raises AssertionError when the oracle disagrees with:
     beta=0 with NaN in C, identity, (AB)^T = B^T A^T, op='T' of a transposed
     copy, exact power-of-two scaling of alpha, padding never read),
   * a float64 BLAS matmul at a medium size within the final rounding,
-  * the bound magnitude S = |alpha| |A|@|B| + |beta C|.
+  * the bound magnitude S = |alpha| |A|@|B| + |beta C|,
+  * exact rational arithmetic, correctly rounded once, on values at the top of
+    the float32 range, and the IEEE 754 rules for Inf and NaN operands.
 The same pins run against deliberately broken copies of the oracle in
 test_oracle_mutations.py, which shows that each plausible mistake fails one.
 """
@@ -18,6 +20,7 @@ from __future__ import annotations
 
 import itertools
 import os
+from fractions import Fraction
 
 import numpy as np
 
@@ -336,10 +339,73 @@ def pin_batched_edges(lib):
         raise AssertionError(f"accepted {bad}")
 
 
+def _round_f32(x: Fraction) -> np.float32:
+    """x rounded to the nearest float32 (ties to an even significand), from exact arithmetic."""
+    c = np.float32(float(x))
+    best = None
+    for y in (np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))):
+        if not np.isfinite(y):
+            continue
+        d = abs(Fraction(float(y)) - x)
+        key = (d, int(np.float32(y).view(np.uint32)) & 1)
+        if best is None or key < best[0]:
+            best = (key, y)
+    return np.float32(best[1])
+
+
+def pin_large_finite_exact(lib):
+    """Values near FLT_MAX (2^128 (1 - 2^-13), FLT_MAX) times small ones, with alpha and beta:
+    the oracle equals the exact rational result rounded to float32 once."""
+    rng = np.random.default_rng(17)
+    big = [np.float32((2 - 2.0 ** -12) * 2.0 ** 127), np.finfo(np.float32).max, np.float32(-(2 - 2.0 ** -11) * 2.0 ** 127)]
+    for trial in range(40):
+        M, N, K = (int(v) for v in rng.integers(1, 5, size=3))
+        a = (rng.integers(-64, 64, size=(M, K)) / 64.0).astype(np.float32)
+        b = (rng.integers(-64, 64, size=(K, N)) / 64.0 * 2.0 ** -30).astype(np.float32)
+        for _ in range(int(rng.integers(1, 3))):
+            a[rng.integers(M), rng.integers(K)] = big[rng.integers(len(big))]
+        c = (rng.integers(-64, 64, size=(M, N)) / 64.0).astype(np.float32)
+        alpha, beta = [(1.0, 0.0), (1.5, -0.5), (-0.75, 2.0)][trial % 3]
+        out = oracle.sgemm("N", "N", a, b, c, alpha, beta, lib=lib)
+        for i in range(M):
+            for j in range(N):
+                exact = Fraction(alpha) * sum(Fraction(float(a[i, k])) * Fraction(float(b[k, j])) for k in range(K))
+                if beta != 0.0:
+                    exact += Fraction(beta) * Fraction(float(c[i, j]))
+                assert out[i, j] == _round_f32(exact), (trial, i, j, out[i, j], float(exact))
+
+
+def pin_ieee_special_values(lib):
+    """IEEE 754: Inf * finite = +-Inf with the product's sign, Inf * 0 = NaN, Inf - Inf = NaN,
+    NaN propagates; beta * C with Inf in C gives Inf, beta = 0 leaves C unread."""
+    inf, nan = np.inf, np.nan
+    cases = [  # (a row, b column, expected a.b)
+        ([inf, 1.0], [2.0, 3.0], inf),
+        ([inf, 1.0], [-2.0, 3.0], -inf),
+        ([-inf, 1.0], [-0.5, 3.0], inf),
+        ([inf, 1.0], [0.0, 3.0], nan),
+        ([0.0, 1.0], [inf, 3.0], nan),
+        ([inf, -inf], [1.0, 1.0], nan),
+        ([inf, inf], [1.0, 2.0], inf),
+        ([nan, 1.0], [0.0, 3.0], nan),
+        ([1.0, 2.0], [3.0, -inf], -inf),
+        ([2.0 ** 100, 2.0 ** 100], [2.0 ** 27, 2.0 ** 27], inf),  # the float32 result overflows
+    ]
+    for arow, bcol, want in cases:
+        a = np.array([arow], np.float32)
+        b = np.array(bcol, np.float32).reshape(2, 1)
+        got = oracle.sgemm("N", "N", a, b, lib=lib)[0, 0]
+        assert (np.isnan(want) and np.isnan(got)) or got == want, (arow, bcol, got)
+    a = np.ones((1, 1), np.float32)
+    c = np.array([[inf]], np.float32)
+    assert oracle.sgemm("N", "N", a, a, c, 1.0, -0.5, lib=lib)[0, 0] == -inf
+    assert oracle.sgemm("N", "N", a, a, c, 1.0, 0.0, lib=lib)[0, 0] == 1.0
+
+
 ALL_PINS = [
     pin_hand_2x2, pin_bruteforce_tiny, pin_integer_pattern, pin_integer_alpha_beta, pin_k1_exact,
     pin_alpha_zero, pin_k_zero, pin_beta_zero_nan_c, pin_identity, pin_transpose_identity,
     pin_transposed_copy, pin_alpha_pow2, pin_padding_not_read, pin_random_vs_float64_matmul,
     pin_bound_magnitude, pin_argument_errors, pin_conjugate_is_transpose, pin_batched_dyadic,
-    pin_batched_edges,
+    pin_batched_edges, pin_large_finite_exact, pin_ieee_special_values,
 ]

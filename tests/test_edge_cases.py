@@ -198,27 +198,6 @@ def test_deterministic_and_transpose_identity(variant):
         assert np.all(err <= 2 * (K + 2) * 2.0 ** -24 * S)
 
 
-def test_nonfinite_inputs():
-    """NaN in A gives NaN in its row on every path; Inf gives +-Inf on the FFMA path and a
-    non-finite value (Inf or NaN) on the 3xTF32 path (documented in include/sgemm.h)."""
-    rng = np.random.default_rng(31)
-    M, N, K = 64, 96, 128
-    A = dyadic(rng, M, K) + 2.0  # positive entries
-    B = np.abs(dyadic(rng, K, N)) + 0.25
-    C = np.zeros((M, N), np.float32)
-    A[3, 5] = np.nan
-    A[7, 9] = np.inf
-    for variant in ("AUTO", "TMA_128x128", "GENERIC", "TC_TF32X3", "TC_PAIR", "TC_PRESPLIT"):
-        got = gpu_sgemm("N", "N", M, N, K, 1.0, A.astype(np.float32), K, B, N, 0.0, C, N, variant=variant)
-        assert np.all(np.isnan(got[3])), variant
-        assert np.all(~np.isfinite(got[7])), variant
-        if variant in ("TMA_128x128", "GENERIC"):
-            assert np.all(np.isposinf(got[7])), variant
-        mask = np.ones(M, bool)
-        mask[[3, 7]] = False
-        assert np.all(np.isfinite(got[mask])), variant
-
-
 def test_non_default_stream_and_matmul_helper():
     torch = pytest.importorskip("torch")
     rng = np.random.default_rng(7)
