@@ -10,3 +10,17 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libsgemm")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The per-configuration parity figures of the GPU parity tests (when any ran)."""
+    try:
+        from gpu_util import PARITY_RECORDS
+    except ImportError:
+        return
+    if not PARITY_RECORDS:
+        return
+    w = terminalreporter
+    w.write_line("parity vs oracle: config / kernel / rows checked / worst err/bound / rel. Frobenius")
+    for name, kernel, rows, worst, frob in PARITY_RECORDS:
+        w.write_line(f"  {name:22s} {kernel:12s} {str(rows):>4s} {worst:9.3g} {frob:9.3g}")

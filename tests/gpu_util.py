@@ -9,6 +9,14 @@ import sgemm_inputs as si
 U = 2.0 ** -24           # unit roundoff of float32
 FROB_LIMIT = 1e-6        # relative Frobenius error limit on random inputs
 
+# (config, kernel, rows checked, worst err/bound, relative Frobenius error) of the parity tests,
+# printed at the end of the run by conftest.py
+PARITY_RECORDS: list = []
+
+
+def record_parity(name, kernel, rows, worst, frob):
+    PARITY_RECORDS.append((name, kernel, rows, worst, frob))
+
 
 def torch_cuda():
     import torch
