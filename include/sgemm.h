@@ -24,7 +24,10 @@
  * (split-K / stream-K partial sums and, for SGEMM_VARIANT_TC_PRESPLIT, the
  * split copies of op(A) and op(B): 4 x 4 bytes per element of each, at most
  * 4 GiB; allocated and freed in stream order on the caller's stream),
- * per-device kernel attributes, and a per-device fault word.
+ * per-device kernel attributes, and a per-device fault word.  The pool keeps
+ * the memory a call frees for later calls (so steady-state calls allocate
+ * nothing): the largest workspace any call needed stays reserved for the
+ * library until the process exits or sgemm_release_workspace() returns it.
  *
  * Semantics of special values (BLAS conventions; the pages do not say):
  *   - M == 0 or N == 0: nothing is done, SGEMM_OK.
@@ -188,14 +191,38 @@ typedef struct sgemm_plan_t {
 /*
  * Fills *plan with the launch sgemm() would make for these arguments on a
  * device with `sm_count` SMs (sm_count <= 0: query the current device).
- * Pure host logic when sm_count > 0; validates arguments like sgemm().
- * Pointers are only inspected for alignment and NULL.
+ * Pure host logic when sm_count > 0 (the device is then assumed to co-schedule
+ * sm_count / 2 CTA-pair clusters, one per TPC); validates arguments like
+ * sgemm().  Pointers are only inspected for alignment and NULL.
  */
 int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
                float alpha, const float *A, int64_t lda,
                const float *B, int64_t ldb,
                float beta, const float *C, int64_t ldc,
                int sm_count, sgemm_plan_t *plan);
+
+/*
+ * The plan for a device described by its SM count (> 0, else -14) and the
+ * number of clusters of two CTAs of the CTA-pair kernels it can hold at once
+ * (>= 0, else -15; the device's own figure comes from an occupancy query,
+ * which gives less than sm_count / 2 under an SM limit such as MPS, and 0 when
+ * such a cluster cannot be scheduled at all: the CTA-pair and split-operand
+ * kernels are then never chosen, and a forced one falls back to one CTA per
+ * tile).  plan == NULL: -16.  Pure host logic.
+ */
+int sgemm_plan_for_device(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                          float alpha, const float *A, int64_t lda,
+                          const float *B, int64_t ldb,
+                          float beta, const float *C, int64_t ldc,
+                          int sm_count, int pair_clusters, sgemm_plan_t *plan);
+
+/*
+ * Returns to the driver the pooled workspace memory of the current device
+ * (sgemm(), sgemm_strided_batched() and sgemm_host() buffers) beyond
+ * keep_bytes.  Memory of calls still running is not released; call it when
+ * the streams that ran libsgemm work are idle.  SGEMM_ERR_CUDA on failure.
+ */
+int sgemm_release_workspace(size_t keep_bytes);
 
 /*
  * Process-wide override of the planner, for tests and benchmarks:
@@ -304,9 +331,14 @@ int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_t K,
  * with SGEMM_ERR_SCRATCH_LIMIT before anything is launched; C is untouched.
  * The first call on a device does a one-time set-up there (it looks up the
  * array's device address and sets kernel attributes); make that first call
- * before any stream capture.  All calls on a device share the one array:
+ * before any stream capture (a set-up that fails returns SGEMM_ERR_CUDA and
+ * is tried again by the next call).  The plan is sgemm()'s for the same
+ * device (the same co-resident cluster count), except for the substitution
+ * above.  All calls on a device share the one array:
  * calls whose kernels can overlap on the GPU (e.g. on unordered streams) race
- * on it, so order them.  CUDA failures return SGEMM_ERR_CUDA.
+ * on it, so order them.  CUDA failures return SGEMM_ERR_CUDA (the error code
+ * is kept for sgemm_last_cuda_error(), as for sgemm()); in-kernel waits
+ * use sgemm()'s limit (SGEMM_WAIT_TIMEOUT_MS).
  */
 #define SGEMM_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB per device */
 

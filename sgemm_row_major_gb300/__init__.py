@@ -85,6 +85,11 @@ def load() -> ctypes.CDLL:
         lib.sgemm_plan.restype = ctypes.c_int
         lib.sgemm_plan.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ctypes.c_int,
                                    ctypes.POINTER(PlanStruct)]
+        lib.sgemm_plan_for_device.restype = ctypes.c_int
+        lib.sgemm_plan_for_device.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                              ctypes.c_int, ctypes.c_int, ctypes.POINTER(PlanStruct)]
+        lib.sgemm_release_workspace.restype = ctypes.c_int
+        lib.sgemm_release_workspace.argtypes = [ctypes.c_size_t]
         lib.sgemm_strided_batched.restype = ctypes.c_int
         lib.sgemm_strided_batched.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
                                               i64, i64, i64, i64, vp]
@@ -224,6 +229,28 @@ def sgemm_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, sm_
     out = {name: getattr(plan, name) for name, _ in PlanStruct._fields_}
     out["variant_name"] = VARIANT_NAMES.get(out["variant"], str(out["variant"]))
     return out
+
+
+def sgemm_plan_for_device(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, sm_count: int,
+                          pair_clusters: int) -> dict:
+    """The launch sgemm() would make on a device of sm_count SMs holding pair_clusters CTA-pair
+    clusters at once (0: none).  Pure host logic.  Raises on invalid arguments."""
+    plan = PlanStruct()
+    st = load().sgemm_plan_for_device(_ch(transA), _ch(transB), int(M), int(N), int(K), float(alpha), _ptr(A),
+                                      int(lda), _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), int(sm_count),
+                                      int(pair_clusters), ctypes.byref(plan))
+    if st != 0:
+        raise SgemmError(st, "sgemm_plan_for_device")
+    out = {name: getattr(plan, name) for name, _ in PlanStruct._fields_}
+    out["variant_name"] = VARIANT_NAMES.get(out["variant"], str(out["variant"]))
+    return out
+
+
+def sgemm_release_workspace(keep_bytes: int = 0) -> None:
+    """Return pooled workspace memory of the current device beyond keep_bytes to the driver."""
+    st = load().sgemm_release_workspace(int(keep_bytes))
+    if st != 0:
+        raise SgemmError(st, "sgemm_release_workspace")
 
 
 def sgemm_strided_batched(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,

@@ -19,34 +19,11 @@
 
 using namespace sgemm_impl;
 
-namespace {
+namespace sgemm_impl {
 
-constexpr int kMaxDevices = 64;
-
-thread_local int t_last_cuda_error = 0;
-std::atomic<int> g_override_variant{SGEMM_VARIANT_AUTO};
-std::atomic<int> g_override_split{0};
-
-struct DeviceState {
-  std::once_flag once;
-  cudaError_t init_error = cudaSuccess;
-  int sm_count = 0;
-  int pair_clusters = 0;  // co-resident clusters of the CTA-pair kernel
-  unsigned* fault = nullptr;
-  cudaMemPool_t pool = nullptr;
-};
-DeviceState g_devices[kMaxDevices];
-
-
-int cuda_fail(cudaError_t e) {
-  t_last_cuda_error = (int)e;
+int record_cuda_failure(cudaError_t e) {
+  t_last_cuda_error_slot() = (int)e;
   return SGEMM_ERR_CUDA;
-}
-
-int op_code(char t) {
-  if (t == 'N' || t == 'n') return 0;
-  if (t == 'T' || t == 't' || t == 'C' || t == 'c') return 1;
-  return -1;
 }
 
 uint64_t wait_timeout_ns() {
@@ -59,44 +36,90 @@ uint64_t wait_timeout_ns() {
   return ns;
 }
 
-// One-time per-device state: SM count, fault word address, kernel attributes,
-// and the stream-ordered pool split-K partial sums come from.
+int& t_last_cuda_error_slot() {
+  thread_local int slot = 0;
+  return slot;
+}
+
+int pair_clusters_or_none() {
+  int n = 0;
+  if (tc_pair_max_clusters(&n) != cudaSuccess) {
+    (void)cudaGetLastError();  // the failed query must not surface at a later launch check
+    return 0;
+  }
+  return n > 0 ? n : 0;
+}
+
+}  // namespace sgemm_impl
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::atomic<int> g_override_variant{SGEMM_VARIANT_AUTO};
+std::atomic<int> g_override_split{0};
+
+struct DeviceState {
+  std::mutex init_mutex;
+  std::atomic<bool> ready{false};  // set once the set-up below has succeeded (a failed one is retried)
+  int sm_count = 0;
+  int pair_clusters = 0;  // co-resident clusters of the CTA-pair kernel; 0: pairs cannot run here
+  unsigned* fault = nullptr;
+  cudaMemPool_t pool = nullptr;
+};
+DeviceState g_devices[kMaxDevices];
+
+int cuda_fail(cudaError_t e) { return record_cuda_failure(e); }
+
+int op_code(char t) {
+  if (t == 'N' || t == 'n') return 0;
+  if (t == 'T' || t == 't' || t == 'C' || t == 'c') return 1;
+  return -1;
+}
+
+// Per-device state: SM count, fault word address, kernel attributes, the
+// co-resident CTA-pair clusters and the stream-ordered pool the workspace comes
+// from.  Set up by the first call on the device that succeeds in it; a failed
+// set-up (e.g. a first call made during a stream capture) is tried again by the
+// next call.
 int device_state(int* device_out, DeviceState** st_out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
   DeviceState& st = g_devices[dev];
-  std::call_once(st.once, [&] {
-    cudaError_t err = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (err == cudaSuccess) err = fault_word(&st.fault);
-    if (err == cudaSuccess) err = prepare_tma_op_nn();
-    if (err == cudaSuccess) err = prepare_tma_op_nt();
-    if (err == cudaSuccess) err = prepare_tma_op_tn();
-    if (err == cudaSuccess) err = prepare_tma_op_tt();
-    if (err == cudaSuccess) err = prepare_tf32x3();
-    if (err == cudaSuccess) err = prepare_small_gemm();
-    if (err == cudaSuccess) err = prepare_tc_pair();
-    if (err == cudaSuccess) err = prepare_presplit();
-    // co-resident CTA-pair clusters; if the occupancy query fails, the planner assumes SMs / 2
-    if (err == cudaSuccess && tc_pair_max_clusters(&st.pair_clusters) != cudaSuccess) {
-      st.pair_clusters = 0;
-      (void)cudaGetLastError();  // the failed query must not surface at a later launch check
-    }
-    if (err == cudaSuccess) {
-      cudaMemPoolProps props = {};
-      props.allocType = cudaMemAllocationTypePinned;
-      props.location.type = cudaMemLocationTypeDevice;
-      props.location.id = dev;
-      err = cudaMemPoolCreate(&st.pool, &props);
-      if (err == cudaSuccess) {
-        uint64_t keep = UINT64_MAX;  // keep freed workspace for the next call
-        err = cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  if (!st.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(st.init_mutex);
+    if (!st.ready.load(std::memory_order_relaxed)) {
+      cudaError_t err = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
+      if (err == cudaSuccess) err = fault_word(&st.fault);
+      if (err == cudaSuccess) err = prepare_tma_op_nn();
+      if (err == cudaSuccess) err = prepare_tma_op_nt();
+      if (err == cudaSuccess) err = prepare_tma_op_tn();
+      if (err == cudaSuccess) err = prepare_tma_op_tt();
+      if (err == cudaSuccess) err = prepare_tf32x3();
+      if (err == cudaSuccess) err = prepare_small_gemm();
+      if (err == cudaSuccess) err = prepare_tc_pair();
+      if (err == cudaSuccess) err = prepare_presplit();
+      if (err == cudaSuccess) st.pair_clusters = pair_clusters_or_none();
+      if (err == cudaSuccess && !st.pool) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        err = cudaMemPoolCreate(&pool, &props);
+        if (err == cudaSuccess) {
+          uint64_t keep = UINT64_MAX;  // keep freed workspace for the next call (sgemm_release_workspace trims)
+          err = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+          if (err == cudaSuccess) st.pool = pool;
+          else (void)cudaMemPoolDestroy(pool);
+        }
       }
+      if (err != cudaSuccess) return cuda_fail(err);
+      st.ready.store(true, std::memory_order_release);
     }
-    st.init_error = err;
-  });
-  if (st.init_error != cudaSuccess) return cuda_fail(st.init_error);
+  }
   *device_out = dev;
   *st_out = &st;
   return SGEMM_OK;
@@ -258,6 +281,7 @@ struct Eligibility {
   bool small = false;     // the small-product FP32 kernel can run it
   bool group = false;     // block-diagonal groups on the tensor cores
   bool presplit = false;  // the split-operand kernel (and its split pass) can run it
+  bool pair = true;       // CTA pairs can be co-scheduled (the CTA-pair and split-operand kernels)
   int64_t group_size = 2;   // products per tile in a group (4 when M, N <= 32)
   int64_t small_grid = 0;   // persistent grid of the small-product kernel
   int64_t clusters = 1;     // co-resident CTA-pair clusters
@@ -284,9 +308,12 @@ Eligibility eligibility(const Problem& pr, int sm_count, int pair_clusters, bool
             ceil_div(pr.batch, e.small_grid) * ceil_div(pr.K, kSmallKChunk) < INT_MAX;
   e.group_size = pr.M <= kGroupMaxMN / 2 && pr.N <= kGroupMaxMN / 2 ? 4 : 2;
   e.group = e.tma && pr.M <= kGroupMaxMN && pr.N <= kGroupMaxMN;
+  // pair_clusters: > 0 the device's co-resident CTA-pair clusters, 0 none (the CTA-pair kernels
+  // cannot run), < 0 not known (a device of sm_count SMs: SMs / 2, one cluster per TPC)
+  e.pair = pair_clusters != 0;
   e.clusters = std::max(1, pair_clusters > 0 ? pair_clusters : sm_count / 2);
   // (the split pass's transposing grid: K / 32 and the products in grid dimensions y and z)
-  e.presplit = e.tma && allow_presplit && ceil_div(pr.K, 32) <= 65535 && pr.batch <= 65535;
+  e.presplit = e.tma && e.pair && allow_presplit && ceil_div(pr.K, 32) <= 65535 && pr.batch <= 65535;
   return e;
 }
 
@@ -305,7 +332,7 @@ int choose_variant(const Problem& pr, const Eligibility& e, int sm_count) {
   // tile: measured on GB300 2-5% faster than one CTA per 128 x 128 tile on
   // 2048^3 .. 16384 x 1024 x 4096, slower on fewer tiles (1024^3: 70.5 against
   // 74.3 TFLOPS) and on M <= 128 (half of every pair tile idle).
-  if (e.tma && pr.M > 128 && ceil_div(pr.M, 256) * ceil_div(pr.N, 128) * pr.batch >= e.clusters)
+  if (e.tma && e.pair && pr.M > 128 && ceil_div(pr.M, 256) * ceil_div(pr.N, 128) * pr.batch >= e.clusters)
     variant = SGEMM_VARIANT_TC_PAIR;
   // Operands split once per call (TC_PRESPLIT) when the GEMM reuses them enough to amortize the
   // split pass (read once, hi and lo written: 12 bytes per element of op(A) and op(B)) and there
@@ -332,9 +359,13 @@ int choose_variant(const Problem& pr, const Eligibility& e, int sm_count) {
     case SGEMM_VARIANT_TC_TF32X3: return e.tma ? SGEMM_VARIANT_TC_TF32X3 : SGEMM_VARIANT_GENERIC;
     case SGEMM_VARIANT_SMALL: return e.small ? SGEMM_VARIANT_SMALL : SGEMM_VARIANT_GENERIC;
     case SGEMM_VARIANT_TC_GROUPED: return e.group ? SGEMM_VARIANT_TC_GROUPED : SGEMM_VARIANT_GENERIC;
-    case SGEMM_VARIANT_TC_PAIR: return e.tma ? SGEMM_VARIANT_TC_PAIR : SGEMM_VARIANT_GENERIC;
+    case SGEMM_VARIANT_TC_PAIR:
+      return !e.tma ? SGEMM_VARIANT_GENERIC : e.pair ? SGEMM_VARIANT_TC_PAIR : SGEMM_VARIANT_TC_TF32X3;
     case SGEMM_VARIANT_TC_PRESPLIT:
-      return e.presplit ? SGEMM_VARIANT_TC_PRESPLIT : e.tma ? SGEMM_VARIANT_TC_PAIR : SGEMM_VARIANT_GENERIC;
+      return e.presplit ? SGEMM_VARIANT_TC_PRESPLIT
+             : !e.tma   ? SGEMM_VARIANT_GENERIC
+             : e.pair   ? SGEMM_VARIANT_TC_PAIR
+                        : SGEMM_VARIANT_TC_TF32X3;
     default: return variant;
   }
 }
@@ -445,11 +476,10 @@ int plan_tiled(const Problem& pr, const Eligibility& e, int variant, int sm_coun
 }
 
 // The planner: a pure function of the problem, the SM count, the number of
-// co-resident CTA-pair clusters (<= 0: sm_count / 2) and the override.
-// allow_presplit = false (sgemm_noalloc: the split arrays need workspace)
-// plans TC_PRESPLIT as TC_PAIR.
-int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clusters = 0,
-              bool allow_presplit = true) {
+// co-resident CTA-pair clusters (< 0: not known, sm_count / 2; 0: none, no
+// CTA-pair kernel) and the override.  allow_presplit = false (sgemm_noalloc:
+// the split arrays need workspace) plans TC_PRESPLIT as TC_PAIR.
+int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clusters, bool allow_presplit = true) {
   *plan = sgemm_plan_t{};
   plan->split_k = 1;
   if (pr.M == 0 || pr.N == 0 || pr.batch == 0) {
@@ -555,7 +585,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   } else if (plan.workspace_bytes > 0) {
     cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)plan.workspace_bytes, st.pool, stream);
     if (e != cudaSuccess) {
-      t_last_cuda_error = (int)e;
+      record_cuda_failure(e);
       return e == cudaErrorMemoryAllocation ? SGEMM_ERR_NOMEM : SGEMM_ERR_CUDA;
     }
     p.ws = static_cast<float*>(ws);
@@ -597,11 +627,11 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
 
 int sgemm_impl::plan_without_split_arrays(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                               int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
-                              int sm_count, sgemm_plan_t* plan) {
+                              int sm_count, int pair_clusters, sgemm_plan_t* plan) {
   Problem pr;
   int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
   if (s != SGEMM_OK) return s;
-  return make_plan(pr, sm_count, plan, 0, false);
+  return make_plan(pr, sm_count, plan, pair_clusters, false);
 }
 
 extern "C" {
@@ -671,7 +701,7 @@ int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float 
   Problem pr;
   int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
   if (s != SGEMM_OK) return s;
-  int pair_clusters = 0;
+  int pair_clusters = -1;
   if (sm_count <= 0) {
     int dev;
     DeviceState* st;
@@ -681,6 +711,28 @@ int sgemm_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float 
     pair_clusters = st->pair_clusters;
   }
   return make_plan(pr, sm_count, plan, pair_clusters);
+}
+
+int sgemm_plan_for_device(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                          int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
+                          int sm_count, int pair_clusters, sgemm_plan_t* plan) {
+  if (!plan) return -16;
+  if (sm_count <= 0) return -14;
+  if (pair_clusters < 0) return -15;
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  return make_plan(pr, sm_count, plan, pair_clusters);
+}
+
+int sgemm_release_workspace(size_t keep_bytes) {
+  int dev;
+  DeviceState* st;
+  int s = device_state(&dev, &st);
+  if (s != SGEMM_OK) return s;
+  cudaError_t e = cudaMemPoolTrimTo(st->pool, keep_bytes);
+  if (e == cudaSuccess) e = trim_host_pool(dev, keep_bytes);
+  return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
 }
 
 int sgemm_strided_batched(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
@@ -713,7 +765,7 @@ int sgemm_plan_strided_batched(char transA, char transB, int64_t M, int64_t N, i
   if (s != SGEMM_OK) return s;
   s = validate_batch(strideA, strideB, strideC, batch_count, &pr);
   if (s != SGEMM_OK) return s;
-  int pair_clusters = 0;
+  int pair_clusters = -1;
   if (sm_count <= 0) {
     int dev;
     DeviceState* st;
@@ -758,18 +810,20 @@ const char* sgemm_status_string(int status) {
     case -13: return "invalid argument 13 (ldc too small)";
     case -14:
       return "invalid argument 14 (strideA < 0; sgemm_ex: workspace NULL although needed, or not 16-byte aligned; "
-             "sgemm_workspace_size: bytes is NULL)";
+             "sgemm_workspace_size: bytes is NULL; sgemm_plan_for_device: sm_count <= 0)";
     case -15:
       return "invalid argument 15 (plan is NULL; strideB < 0 in the batched calls; sgemm_ex: workspace_bytes "
-             "smaller than sgemm_workspace_size())";
-    case -16: return "invalid argument 16 (strideC < 0, or C matrices of a batch overlap)";
+             "smaller than sgemm_workspace_size(); sgemm_plan_for_device: pair_clusters < 0)";
+    case -16:
+      return "invalid argument 16 (strideC < 0, or C matrices of a batch overlap; sgemm_plan_for_device: plan is "
+             "NULL)";
     case -17: return "invalid argument 17 (batch_count < 0)";
     case -19: return "invalid argument 19 (plan is NULL)";
     default: return status < 0 ? "invalid argument" : "unknown status";
   }
 }
 
-int sgemm_last_cuda_error(void) { return t_last_cuda_error; }
+int sgemm_last_cuda_error(void) { return t_last_cuda_error_slot(); }
 
 int sgemm_sync_status(struct CUstream_st* stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

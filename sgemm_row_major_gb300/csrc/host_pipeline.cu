@@ -21,10 +21,14 @@
 // exactly like sgemm().
 #include <algorithm>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "sgemm.h"
 #include "sgemm_internal.h"
+
+using sgemm_impl::record_cuda_failure;
 
 namespace {
 
@@ -35,8 +39,8 @@ constexpr int kChunkedBlocks = 1;  // first row blocks whose GEMMs run chunk by 
                                    // (2 measured no faster: the later blocks' GEMMs then bound the call)
 
 struct HostPipeDevice {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
+  std::mutex init_mutex;
+  std::atomic<bool> ready{false};  // set once the set-up has succeeded (a failed one is retried)
   cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
   cudaEvent_t ev_start = nullptr, ev_done = nullptr, ev_h2d_end = nullptr, ev_comp_end = nullptr;
   cudaEvent_t ev_in[kSets] = {}, ev_gemm[kSets] = {}, ev_out[kSets] = {};
@@ -48,45 +52,59 @@ HostPipeDevice g_hp[kMaxDevices];
 
 int64_t round4(int64_t x) { return (x + 3) / 4 * 4; }
 
+// Streams, events and the buffer pool of a device, made by the first call
+// there that succeeds; what a failed attempt made is kept and the rest is
+// made by the next call.
 cudaError_t setup(int dev, HostPipeDevice** out) {
   HostPipeDevice& d = g_hp[dev];
-  std::call_once(d.once, [&] {
-    cudaError_t e = cudaStreamCreateWithFlags(&d.h2d, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d.comp, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d.d2h, cudaStreamNonBlocking);
-    cudaEvent_t* evs[] = {&d.ev_start, &d.ev_done, &d.ev_h2d_end, &d.ev_comp_end};
-    for (cudaEvent_t* ev : evs)
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
-    for (int i = 0; i < kBChunks && e == cudaSuccess; ++i)
-      e = cudaEventCreateWithFlags(&d.ev_b[i], cudaEventDisableTiming);
-    for (int i = 0; i < kSets && e == cudaSuccess; ++i) {
-      e = cudaEventCreateWithFlags(&d.ev_in[i], cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_gemm[i], cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_out[i], cudaEventDisableTiming);
-    }
-    if (e == cudaSuccess) {
-      cudaMemPoolProps props = {};
-      props.allocType = cudaMemAllocationTypePinned;
-      props.location.type = cudaMemLocationTypeDevice;
-      props.location.id = dev;
-      e = cudaMemPoolCreate(&d.pool, &props);
-      if (e == cudaSuccess) {
-        uint64_t keep = UINT64_MAX;
-        e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-      }
-    }
-    d.err = e;
-  });
   *out = &d;
-  return d.err;
+  if (d.ready.load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(d.init_mutex);
+  if (d.ready.load(std::memory_order_relaxed)) return cudaSuccess;
+  cudaError_t e = cudaSuccess;
+  for (cudaStream_t* s : {&d.h2d, &d.comp, &d.d2h})
+    if (e == cudaSuccess && !*s) e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
+  std::vector<cudaEvent_t*> evs = {&d.ev_start, &d.ev_done, &d.ev_h2d_end, &d.ev_comp_end};
+  for (int i = 0; i < kBChunks; ++i) evs.push_back(&d.ev_b[i]);
+  for (int i = 0; i < kSets; ++i) {
+    evs.push_back(&d.ev_in[i]);
+    evs.push_back(&d.ev_gemm[i]);
+    evs.push_back(&d.ev_out[i]);
+  }
+  for (cudaEvent_t* ev : evs)
+    if (e == cudaSuccess && !*ev) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  if (e == cudaSuccess && !d.pool) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    e = cudaMemPoolCreate(&pool, &props);
+    if (e == cudaSuccess) {
+      uint64_t keep = UINT64_MAX;  // keep freed buffers for the next call (sgemm_release_workspace trims)
+      e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      if (e == cudaSuccess) d.pool = pool;
+      else (void)cudaMemPoolDestroy(pool);
+    }
+  }
+  if (e == cudaSuccess) d.ready.store(true, std::memory_order_release);
+  return e;
 }
 
 int status_of(cudaError_t e) {
   if (e == cudaSuccess) return SGEMM_OK;
+  record_cuda_failure(e);
   return e == cudaErrorMemoryAllocation ? SGEMM_ERR_NOMEM : SGEMM_ERR_CUDA;
 }
 
 }  // namespace
+
+cudaError_t sgemm_impl::trim_host_pool(int dev, size_t keep_bytes) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaSuccess;
+  HostPipeDevice& d = g_hp[dev];
+  std::lock_guard<std::mutex> lock(d.mu);
+  return d.pool ? cudaMemPoolTrimTo(d.pool, keep_bytes) : cudaSuccess;
+}
 
 extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
                           const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C,
@@ -103,10 +121,11 @@ extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return SGEMM_ERR_CUDA;
+  if (e != cudaSuccess) return record_cuda_failure(e);
   if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
   HostPipeDevice* d = nullptr;
-  if (setup(dev, &d) != cudaSuccess) return SGEMM_ERR_CUDA;
+  e = setup(dev, &d);
+  if (e != cudaSuccess) return record_cuda_failure(e);
   std::lock_guard<std::mutex> lock(d->mu);
   cudaStream_t user = reinterpret_cast<cudaStream_t>(stream);
 
@@ -137,7 +156,7 @@ extern "C" int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_
   if (e == cudaSuccess) e = cudaStreamWaitEvent(d->h2d, d->ev_start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(d->comp, d->ev_start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(d->d2h, d->ev_start, 0);
-  if (e != cudaSuccess) return SGEMM_ERR_CUDA;
+  if (e != cudaSuccess) return record_cuda_failure(e);
 
   // Buffers (ordered on h2d; the other streams use them only after its events).
   if (reads_ab) {

@@ -15,11 +15,14 @@
 // as a device address (on the host it names a stand-in object), so the
 // device address is looked up with cudaGetSymbolAddress once per device, with
 // that device current, on the first sgemm_noalloc() call there; that first
-// call should therefore come before any stream capture.  Nothing in the array
+// call should therefore come before any stream capture (a set-up that fails,
+// for instance inside a capture, returns SGEMM_ERR_CUDA and is tried again
+// by the next call).  Nothing in the array
 // needs to start at zero: the GEMM kernel writes every partial sum the
 // reduction reads in the same call.  All calls on a device share the array,
 // so two calls whose kernels overlap on the GPU (different streams, no
 // ordering between them) race on it.
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <mutex>
@@ -38,33 +41,38 @@ static __device__ __align__(256) float g_noalloc_scratch[SGEMM_NOALLOC_SCRATCH_B
 constexpr int kMaxDevices = 64;
 
 struct NoallocDevice {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
+  std::mutex init_mutex;
+  std::atomic<bool> ready{false};  // set once the set-up has succeeded (a failed one is retried)
   int sm_count = 0;
+  int pair_clusters = 0;     // co-resident CTA-pair clusters (0: the CTA-pair kernel cannot run here)
   unsigned* fault = nullptr;
   float* scratch = nullptr;  // device address of g_noalloc_scratch on this device
 };
 NoallocDevice g_nd[kMaxDevices];
 
-// Per-device set-up, once, with the device current: SM count, fault word,
-// scratch address and kernel attributes.  No allocation happens here.
+// Per-device set-up with the device current: SM count, co-resident CTA-pair
+// clusters (the same query sgemm() plans with), fault word, scratch address
+// and kernel attributes.  No allocation happens here.  Done by the first call
+// on the device that succeeds in it; a failed set-up is tried again next call.
 cudaError_t setup(int dev, NoallocDevice** out) {
   NoallocDevice& d = g_nd[dev];
-  std::call_once(d.once, [&] {
-    cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = fault_word(&d.fault);
-    if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.scratch), g_noalloc_scratch);
-    if (e == cudaSuccess) e = prepare_tma_op_nn();
-    if (e == cudaSuccess) e = prepare_tma_op_nt();
-    if (e == cudaSuccess) e = prepare_tma_op_tn();
-    if (e == cudaSuccess) e = prepare_tma_op_tt();
-    if (e == cudaSuccess) e = prepare_tf32x3();
-    if (e == cudaSuccess) e = prepare_small_gemm();
-    if (e == cudaSuccess) e = prepare_tc_pair();
-    d.err = e;
-  });
   *out = &d;
-  return d.err;
+  if (d.ready.load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(d.init_mutex);
+  if (d.ready.load(std::memory_order_relaxed)) return cudaSuccess;
+  cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = fault_word(&d.fault);
+  if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.scratch), g_noalloc_scratch);
+  if (e == cudaSuccess) e = prepare_tma_op_nn();
+  if (e == cudaSuccess) e = prepare_tma_op_nt();
+  if (e == cudaSuccess) e = prepare_tma_op_tn();
+  if (e == cudaSuccess) e = prepare_tma_op_tt();
+  if (e == cudaSuccess) e = prepare_tf32x3();
+  if (e == cudaSuccess) e = prepare_small_gemm();
+  if (e == cudaSuccess) e = prepare_tc_pair();
+  if (e == cudaSuccess) d.pair_clusters = pair_clusters_or_none();
+  if (e == cudaSuccess) d.ready.store(true, std::memory_order_release);
+  return e;
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -83,11 +91,13 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
   if (plan.variant == SGEMM_VARIANT_NONE) return SGEMM_OK;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return SGEMM_ERR_CUDA;
+  if (e != cudaSuccess) return record_cuda_failure(e);
   if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
   NoallocDevice* nd = nullptr;
-  if (setup(dev, &nd) != cudaSuccess) return SGEMM_ERR_CUDA;
-  st = plan_without_split_arrays(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nd->sm_count, &plan);
+  e = setup(dev, &nd);
+  if (e != cudaSuccess) return record_cuda_failure(e);
+  st = plan_without_split_arrays(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nd->sm_count,
+                                 nd->pair_clusters, &plan);
   if (st != SGEMM_OK) return st;
   if ((uint64_t)plan.workspace_bytes > (uint64_t)SGEMM_NOALLOC_SCRATCH_BYTES) return SGEMM_ERR_SCRATCH_LIMIT;
 
@@ -109,12 +119,12 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
   p.tb = tb ? 1 : 0;
   p.ldc = ldc;
   p.c_vec = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0;
-  p.timeout_ns = 2000ull * 1000000ull;
+  p.timeout_ns = wait_timeout_ns();
   p.fault = nd->fault;
 
   if (plan.variant == SGEMM_VARIANT_SCALE) {
     e = launch_scale(p, cs);
-    return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+    return e == cudaSuccess ? SGEMM_OK : record_cuda_failure(e);
   }
   const int split = plan.split_k;
   p.tiles_m = (int)ceil_div(M, plan.tile_m);
@@ -134,7 +144,7 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
     operand_boxes(plan, &box_m, &box_n);
     e = encode_operand_maps(ta, tb, M, N, K, A, lda, 0, B, ldb, 0, 1, box_m, box_n, plan.tile_k, &mapA, &mapB, &p.za,
                             &p.zb);
-    if (e != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (e != cudaSuccess) return record_cuda_failure(e);
     const TmaTile tile = plan.variant == SGEMM_VARIANT_TMA_128x128 ? TmaTile::k128x128 : TmaTile::k64x256;
     if (plan.variant == SGEMM_VARIANT_TC_TF32X3 || plan.variant == SGEMM_VARIANT_TC_GROUPED) {
       e = launch_tf32x3(ta, tb, plan.variant == SGEMM_VARIANT_TC_GROUPED ? 128 / plan.tile_m : 1, mapA, mapB, p,
@@ -151,5 +161,5 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
   if (e == cudaSuccess && split > 1 && plan.variant != SGEMM_VARIANT_TC_TF32X3 &&
       plan.variant != SGEMM_VARIANT_TC_PAIR)
     e = launch_splitk_reduce(p, split, cs);
-  return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+  return e == cudaSuccess ? SGEMM_OK : record_cuda_failure(e);
 }

@@ -141,10 +141,11 @@ cudaError_t launch_presplit_gemm(const CUtensorMap& mapAh, const CUtensorMap& ma
                                  const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
 // sgemm_plan() for a caller that cannot provide the split arrays of TC_PRESPLIT
-// (sgemm_noalloc): that variant, forced by override, is planned as TC_PAIR.
+// (sgemm_noalloc): that variant, chosen or forced by override, is planned as TC_PAIR.
+// pair_clusters as in sgemm_plan_for_device().
 int plan_without_split_arrays(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                               int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
-                              int sm_count, sgemm_plan_t* plan);
+                              int sm_count, int pair_clusters, sgemm_plan_t* plan);
 // Map over a split array: {K, rows, products} float32, row stride ldk, box {32, 128, 1}, 128-byte swizzle.
 cudaError_t encode_split_map(const float* base, int64_t K, int64_t rows, int64_t ldk, int64_t products,
                              CUtensorMap* map);
@@ -153,6 +154,17 @@ cudaError_t launch_generic_gemm(bool transA, bool transB, const GemmParams& p, i
 cudaError_t launch_splitk_reduce(const GemmParams& p, int split, cudaStream_t stream);
 cudaError_t launch_scale(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, unsigned* fault, cudaStream_t stream);
+
+// Keeps e as this thread's last CUDA error (sgemm_last_cuda_error) and returns SGEMM_ERR_CUDA.
+int record_cuda_failure(cudaError_t e);
+int& t_last_cuda_error_slot();
+// The limit of every in-kernel wait: SGEMM_WAIT_TIMEOUT_MS (default 2000 ms), read once.
+uint64_t wait_timeout_ns();
+// Co-resident CTA-pair clusters on the current device, or 0 when the pair kernel cannot be
+// co-scheduled there (or the query fails): the planner then leaves out the CTA-pair kernels.
+int pair_clusters_or_none();
+// Returns the memory pool of sgemm_host() on device `dev` to the driver down to keep_bytes.
+cudaError_t trim_host_pool(int dev, size_t keep_bytes);
 
 // Device address of the current device's fault word (looked up once per device).
 cudaError_t fault_word(unsigned** ptr);

@@ -400,3 +400,36 @@ def test_batched_argument_checks(lib):
     assert lib.sgemm_strided_batched(b"N", b"N", 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4, 16, 16, 15, 3,
                                      None) == -16
     assert sg.sgemm_status_string(-17).startswith("invalid argument 17")
+
+
+def dplan(ta, tb, M, N, K, sm_count, pair_clusters, A=FAKE, B=FAKE):
+    lda = M if ta == "T" else K
+    ldb = K if tb == "T" else N
+    return sg.sgemm_plan_for_device(ta, tb, M, N, K, 1.0, A, lda, B, ldb, 0.0, FAKE, N, sm_count, pair_clusters)
+
+
+def test_planner_for_device_pair_clusters(lib):
+    """The co-resident CTA-pair cluster count steers the planner: SMs / 2 gives sgemm_plan()'s plan;
+    fewer clusters (an SM limit) size the pair grid; none leaves the CTA-pair kernels out, and a
+    forced one falls back to one CTA per tile."""
+    for shape in ((4096, 4096, 4096), (2048, 2048, 2048), (1000, 1300, 700), (8192, 4096, 1024)):
+        assert dplan("N", "N", *shape, 152, 76) == plan("N", "N", *shape)
+    p = dplan("N", "N", 4096, 4096, 4096, 152, 60)
+    assert p["variant_name"] == "TC_PRESPLIT" and p["grid_x"] == 120
+    for shape in ((4096, 4096, 4096), (2048, 2048, 2048), (8192, 4096, 1024)):
+        p = dplan("N", "N", *shape, 152, 0)
+        assert p["variant_name"] == "TC_TF32X3" and p["grid_x"] <= 152, shape
+    try:
+        for v in ("TC_PAIR", "TC_PRESPLIT"):
+            sg.sgemm_set_variant_override(v, 0)
+            assert dplan("N", "N", 4096, 4096, 4096, 152, 0)["variant_name"] == "TC_TF32X3"
+            assert dplan("N", "N", 4096, 4096, 4096, 152, 0, A=FAKE_ODD)["variant_name"] == "GENERIC"
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
+    # argument checks of the device description
+    for bad_sm, bad_pc, code in ((0, 76, -14), (152, -1, -15)):
+        with pytest.raises(sg.SgemmError) as ei:
+            dplan("N", "N", 64, 64, 64, bad_sm, bad_pc)
+        assert ei.value.status == code
+    st = lib.sgemm_plan_for_device(b"N", b"N", 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, 0.0, FAKE, 64, 152, 76, None)
+    assert st == -16

@@ -130,3 +130,27 @@ def test_ex_graph_capture_replay():
         torch.cuda.synchronize()
         assert sg.sgemm_sync_status() == 0
         check_exact(dC.cpu().numpy(), oracle.sgemm("N", "N", A, B, C, 1.5, -0.5), f"replay {rep}")
+
+
+def test_release_workspace_returns_pool_memory():
+    """The pool keeps a large call's split arrays until sgemm_release_workspace() returns them;
+    later calls allocate again and give the same bits."""
+    torch = torch_cuda()
+    M = N = K = 2048
+    rng = np.random.default_rng(41)
+    A, B = _dyadic(rng, (M, K)), _dyadic(rng, (K, N))
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    assert sg.sgemm_plan("N", "N", M, N, K, 1.0, dA, K, dB, N, 0.0, dA, N)["workspace_bytes"] >= 64 << 20
+    C1 = torch.empty(M, N, device="cuda")
+    C2 = torch.empty(M, N, device="cuda")
+    sg.sgemm("N", "N", M, N, K, 1.0, dA, K, dB, N, 0.0, C1, N)
+    assert sg.sgemm_sync_status() == 0
+    free_kept, _ = torch.cuda.mem_get_info()
+    sg.sgemm_release_workspace(0)
+    free_released, _ = torch.cuda.mem_get_info()
+    assert free_released - free_kept >= 60 << 20, (free_kept, free_released)
+    sg.sgemm("N", "N", M, N, K, 1.0, dA, K, dB, N, 0.0, C2, N)
+    assert sg.sgemm_sync_status() == 0
+    assert torch.equal(C1, C2)
+    ref = oracle.sgemm("N", "N", A, B)
+    check_exact(C2.cpu().numpy(), ref, "after release")
