@@ -39,20 +39,10 @@ import sgemm_inputs as si  # noqa: E402
 METRIC = "SGEMM TFLOPS (2MNK/t) at 4096^3 NN on 1 GB300; % of FP32 FFMA peak"
 UNIT = "TFLOPS"
 FMA_PER_SM_PER_CLK = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
-# committed ncu summaries by (kernel variant, workload): their per-launch DRAM traffic is reported
-# while the kernel's source digest still matches the one they were captured with
-PROFILES = {("TC_PRESPLIT", "square4096"): os.path.join(ROOT, "profiles", "presplit_gemm_square4096.md"),
-            ("TC_PAIR", "square4096"): os.path.join(ROOT, "profiles", "tc_pair_gemm_square4096.md"),
-            ("TC_TF32X3", "square4096"): os.path.join(ROOT, "profiles", "tf32x3_gemm_square4096.md"),
-            ("TMA_128x128", "square4096"): os.path.join(ROOT, "profiles", "tma_gemm_square4096.md"),
-            ("SMALL", "batched_small_8192x64x64x64"):
-                os.path.join(ROOT, "profiles", "small_gemm_batched8192x64x64x64.md"),
-            ("TC_GROUPED", "batched_small_k1024_2048x64x64x1024"):
-                os.path.join(ROOT, "profiles", "tf32x3_grouped_batched2048x64x64x1024.md"),
-            ("TC_GROUPED", "batched_small_8192x64x64x64"):
-                os.path.join(ROOT, "profiles", "tf32x3_grouped_batched8192x64x64x64.md"),
-            ("TC_GROUPED", "batched_tiny_16384x32x32x32"):
-                os.path.join(ROOT, "profiles", "tf32x3_grouped_batched16384x32x32x32.md")}
+# per-launch DRAM traffic of the dominant kernel by (variant, workload), from ncu captures
+# (profiles/traffic.json, written with the summaries in profiles/); reported while the kernel's
+# source digest still matches the one the capture was taken with
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 # dense tensor-core peaks (PFLOP/s, nominal) used to scale the measured bf16 peak to tf32
 NOMINAL_BF16_PF, NOMINAL_TF32_PF = 2.25, 1.1
 TF32_PRODUCTS = 3  # tensor-core products per useful FMA in the 3xTF32 split
@@ -123,7 +113,8 @@ class ClockSampler:
         rows = [l.split(", ") for (t, l) in self.lines if t0 <= t <= t1]
         rows = [r for r in rows if len(r) == len(self.FIELDS)]
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in timed region"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the loaded window"],
+                    "samples": 0}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -151,16 +142,16 @@ def gpu_selector(device_index: int) -> str:
 # ---------------------------------------------------------------- helpers
 
 def traffic_from_profile(variant: str, workload: str, digest: str):
-    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, if it is current."""
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu capture record, if it is
+    current (same kernel source digest)."""
     try:
-        text = open(PROFILES[(variant, workload)]).read()
-    except (OSError, KeyError):
+        entries = json.load(open(TRAFFIC_FILE))["entries"]
+    except (OSError, ValueError, KeyError):
         return None
-    d = re.search(r"kernel_digest:\s*([0-9a-f]+)", text)
-    t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    if not d or not t or d.group(1) != digest:
-        return None
-    return int(t.group(1))
+    for e in entries:
+        if e.get("variant") == variant and e.get("workload") == workload and e.get("kernel_digest") == digest:
+            return int(e["traffic_bytes_per_launch"])
+    return None
 
 
 def measured_peaks():
@@ -333,14 +324,35 @@ def l2_flusher(dev, set_bytes):
     return flush
 
 
+def snapshot_mhz(before, after):
+    """Median over SMs of (cycle counter delta) / (global timer delta) between two per-SM clock
+    snapshots (sgemm_clock_snapshot), in MHz, and the number of SMs it covers."""
+    b = before.view(-1, 2).cpu().numpy().astype(np.int64)
+    a = after.view(-1, 2).cpu().numpy().astype(np.int64)
+    ok = (b[:, 1] > 0) & (a[:, 1] > b[:, 1]) & (a[:, 0] > b[:, 0])
+    if not ok.any():
+        return None, 0
+    mhz = (a[ok, 0] - b[ok, 0]) / (a[ok, 1] - b[ok, 1]) * 1e3
+    return float(np.median(mhz)), int(ok.sum())
+
+
 def timed_steps(step, args, stream, dev, local, barrier, world, flush=None):
     """Pre-warm, W warm-up steps, then exactly K timed steps between barriers.
 
     With `flush`, L2 is flushed before every step (outside the step's events)
-    and the job time is the sum of the steps' event times.  Returns (per-step
-    ms from CUDA events on `stream`, the slowest rank's job ms, the clock
-    summary sampled during the timed region)."""
+    and the job time is the sum of the steps' event times.  Clocks: nvidia-smi
+    samples every 50 ms from the start of the pre-warm to the end of the timed
+    steps (the loaded window: a timed region of a few ms holds no sample of its
+    own), and a per-SM clock snapshot just before the first and just after the
+    last timed step gives the SMs' average clock over exactly the timed steps.
+    Returns (per-step ms from CUDA events on `stream`, the slowest rank's job
+    ms, the clock record)."""
     import torch
+    import sgemm_row_major_gb300 as sg
+    sampler = ClockSampler(gpu_selector(local))
+    sampler.start()
+    time.sleep(0.2)
+    t_load = time.time()
     t_end = time.time() + args.prewarm_s
     i = 0
     while time.time() < t_end:
@@ -352,14 +364,13 @@ def timed_steps(step, args, stream, dev, local, barrier, world, flush=None):
         step(w)
     barrier()
 
-    sampler = ClockSampler(gpu_selector(local))
-    sampler.start()
-    time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    snaps = [torch.zeros(2 * 1024, dtype=torch.int64, device=dev) for _ in range(2)]
     barrier()
     t0_wall = time.time()
     g0 = torch.cuda.Event(enable_timing=True)
     g1 = torch.cuda.Event(enable_timing=True)
+    sg.sgemm_clock_snapshot(snaps[0], stream)
     g0.record(stream)
     for s in range(args.steps):
         if flush:
@@ -368,6 +379,7 @@ def timed_steps(step, args, stream, dev, local, barrier, world, flush=None):
         step(s)
         ev[s][1].record(stream)
     g1.record(stream)
+    sg.sgemm_clock_snapshot(snaps[1], stream)
     barrier()
     t1_wall = time.time()
     time.sleep(0.1)
@@ -375,7 +387,15 @@ def timed_steps(step, args, stream, dev, local, barrier, world, flush=None):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     job_ms = sum(step_ms) if flush else g0.elapsed_time(g1)
     total_ms = reduce_max_ms(job_ms, world, dev)
-    return step_ms, total_ms, sampler.summary(t0_wall, t1_wall)
+    clocks = sampler.summary(t_load, t1_wall)
+    clocks["window"] = (f"nvidia-smi every 50 ms over the loaded window: pre-warm {args.prewarm_s:.1f} s, "
+                        f"{args.warmup} warm-up and {args.steps} timed steps ({1e3 * (t1_wall - t_load):.0f} ms)")
+    clocks["timed_samples"] = len([1 for (t, _) in sampler.lines if t0_wall <= t <= t1_wall])
+    mhz, n_sms = snapshot_mhz(*snaps)
+    clocks["sm_mhz_timed_steps"] = mhz
+    clocks["sm_mhz_timed_steps_basis"] = (f"median over {n_sms} SMs of SM cycle-counter / global-timer deltas "
+                                          f"between snapshots just before and just after the timed steps")
+    return step_ms, total_ms, clocks
 
 
 def step_stats(step_ms):
@@ -426,6 +446,22 @@ def tensor_roofline(achieved, peaks, traffic, kernel_ms, variant="TC_TF32X3"):
                                  "stream-K tiles are shared, the fixup kernel" if variant == "TC_PRESPLIT" else
                                  "one sgemm() call: the GEMM kernel and, when stream-K tiles are shared, "
                                  "the fixup kernel after it (about 2% of the step in the ncu launch list)")}
+
+
+def hbm_bound_roofline(roof, nbytes, flops_step, kernel_ms, peaks):
+    """Switches a tensor-core roofline to the HBM roof when the call's algorithmic bytes take longer
+    at the measured HBM bandwidth than its FLOPs at the tensor peak (the tensor figures stay
+    beside it)."""
+    hbm = peaks.get("hbm_gbs")
+    hbm_basis = "measured" if hbm else "fallback"
+    hbm = hbm or 6800.0
+    roof["algorithmic_bytes"] = nbytes
+    if nbytes / (hbm * 1e9) > flops_step / (roof["peak"] * 1e12):
+        gbs = nbytes / (kernel_ms * 1e-3) / 1e9
+        tensor = {k: roof[k] for k in ("achieved", "peak", "unit", "frac", "peak_basis")}
+        roof.update({"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "peak_basis": f"{hbm_basis} HBM copy bandwidth", "tensor": tensor})
+    return roof
 
 
 def run_ours(args):
@@ -517,6 +553,7 @@ def run_ours(args):
         roof = tensor_roofline(achieved, peaks,
                                traffic_from_profile(variant, case.name, kernel_digest(lib_build, variant)),
                                kernel_ms, variant)
+        hbm_bound_roofline(roof, si.min_bytes(M, N, K, case.beta), flops_step, kernel_ms, peaks)
     else:
         roof = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
                 "frac": achieved / ffma_peak,
@@ -532,9 +569,10 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "step_ms": step_stats(step_ms),
-        "config": {**config_block(case, world), "l2": l2_note(flush), "prewarm_s": args.prewarm_s,
-                   "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "tile_k", "stages",
-                                                 "split_k", "grid_x", "grid_y", "dp_tiles", "sk_tiles")}},
+        "config": config_block(case, world),
+        "run": {"l2": l2_note(flush), "prewarm_s": args.prewarm_s,
+                "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "tile_k", "stages",
+                                              "split_k", "grid_x", "grid_y", "dp_tiles", "sk_tiles")}},
         "pct_ffma_peak": 100.0 * achieved / ffma_peak,
         "ffma_peak": {"value": ffma_peak, "unit": "TFLOP/s",
                       "basis": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz"},
@@ -628,17 +666,7 @@ def batched_roofline(c, plan, flops_step, achieved, kernel_ms, peaks, dev, lib_b
             tiles = (c.batch + group - 1) // group
             roof["kernel"] = f"tf32x3_gemm_kernel, {group} products per 128x128 tile (block-diagonal)"
             roof["useful_fraction_of_tensor_work"] = c.batch * c.M * c.N / (tiles * 128 * 128)
-        nbytes = batched_bytes(c)
-        hbm = peaks.get("hbm_gbs")
-        hbm_basis = "measured" if hbm else "fallback"
-        hbm = hbm or 6800.0
-        if nbytes / (hbm * 1e9) > flops_step / (roof["peak"] * 1e12):
-            gbs = nbytes / (kernel_ms * 1e-3) / 1e9
-            tensor = {k: roof[k] for k in ("achieved", "peak", "unit", "frac", "peak_basis")}
-            roof.update({"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                         "peak_basis": f"{hbm_basis} HBM copy bandwidth", "algorithmic_bytes": nbytes,
-                         "tensor": tensor})
-        return roof
+        return hbm_bound_roofline(roof, batched_bytes(c), flops_step, kernel_ms, peaks)
     if variant == "SMALL":
         return small_roofline(c, flops_step, kernel_ms, peaks, dev,
                               traffic_from_profile(variant, c.name, lib_build.small_kernel_digest()))
@@ -728,9 +756,10 @@ def run_ours_batched(args, c):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "step_ms": step_stats(step_ms),
-        "config": {**batched_config_block(c, d, world), "l2": l2_note(flush), "prewarm_s": args.prewarm_s,
-                   "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "split_k", "grid_x", "grid_y",
-                                                 "dp_tiles", "sk_tiles")}},
+        "config": batched_config_block(c, d, world),
+        "run": {"l2": l2_note(flush), "prewarm_s": args.prewarm_s,
+                "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "split_k", "grid_x", "grid_y",
+                                              "dp_tiles", "sk_tiles")}},
         "roofline": batched_roofline(c, plan, flops_step, achieved, kernel_ms, peaks, dev, lib_build),
         "e2e": {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
                 "note": "no host-buffer batched entry point; the device-resident value is the measurement"},

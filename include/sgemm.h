@@ -289,6 +289,18 @@ int sgemm_plan_strided_batched(char transA, char transB, int64_t M, int64_t N, i
                                int64_t batch_count, int sm_count, sgemm_plan_t *plan);
 
 /*
+ * Measurement aid: enqueues on `stream` a tiny kernel whose CTAs (four per
+ * SM) write, for the SM each runs on, the SM's cycle counter and the global
+ * nanosecond timer to out[2 * smid] and out[2 * smid + 1].  `out` is a device
+ * buffer of 2 * slots unsigned 64-bit words (slots >= the SM count covers
+ * every SM; SMs with smid >= slots are skipped, entries of SMs no CTA ran on
+ * are left as they were).  Two snapshots around a stretch of work give each
+ * SM's average clock over it (cycles / ns); nothing is changed on the GPU.
+ * -1: out is NULL; -2: slots < 1.
+ */
+int sgemm_clock_snapshot(unsigned long long *out, int slots, struct CUstream_st *stream);
+
+/*
  * sgemm_host -- the same operation with A, B and C in HOST memory (same
  * layout rules and argument checks as sgemm(); page-locked memory gives full
  * copy speed, pageable memory works but its copies are staged by the driver

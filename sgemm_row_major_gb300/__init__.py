@@ -90,6 +90,8 @@ def load() -> ctypes.CDLL:
                                               ctypes.c_int, ctypes.c_int, ctypes.POINTER(PlanStruct)]
         lib.sgemm_release_workspace.restype = ctypes.c_int
         lib.sgemm_release_workspace.argtypes = [ctypes.c_size_t]
+        lib.sgemm_clock_snapshot.restype = ctypes.c_int
+        lib.sgemm_clock_snapshot.argtypes = [vp, ctypes.c_int, vp]
         lib.sgemm_strided_batched.restype = ctypes.c_int
         lib.sgemm_strided_batched.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
                                               i64, i64, i64, i64, vp]
@@ -251,6 +253,14 @@ def sgemm_release_workspace(keep_bytes: int = 0) -> None:
     st = load().sgemm_release_workspace(int(keep_bytes))
     if st != 0:
         raise SgemmError(st, "sgemm_release_workspace")
+
+
+def sgemm_clock_snapshot(out, stream=None) -> None:
+    """Per-SM (cycle counter, global ns timer) pairs into `out`, a CUDA int64 tensor of 2 * slots
+    elements (slot = SM id), enqueued on `stream`."""
+    st = load().sgemm_clock_snapshot(_ptr(out), int(out.numel()) // 2, _stream(stream))
+    if st != 0:
+        raise SgemmError(st, "sgemm_clock_snapshot")
 
 
 def sgemm_strided_batched(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,

@@ -834,6 +834,17 @@ int sgemm_sync_status(struct CUstream_st* stream) {
   return bits ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
 }
 
+int sgemm_clock_snapshot(unsigned long long* out, int slots, struct CUstream_st* stream) {
+  if (!out) return -1;
+  if (slots < 1) return -2;
+  int dev;
+  DeviceState* st;
+  int s = device_state(&dev, &st);
+  if (s != SGEMM_OK) return s;
+  cudaError_t e = launch_clock_snapshot(out, slots, st->sm_count, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
+}
+
 int sgemm_selftest_wait_timeout(unsigned timeout_us, struct CUstream_st* stream) {
   if (timeout_us < 1 || timeout_us > 10000000u) return -1;
   int dev;

@@ -1,6 +1,7 @@
 // kernel_aux.cu -- the small kernels around the GEMM kernels: the split-K
 // reduction with the fused alpha/beta epilogue, C = beta*C for alpha == 0 or
-// K == 0, the bounded-wait self-test, and the device fault word.
+// K == 0, the bounded-wait self-test, the per-SM clock snapshot, and the
+// device fault word.
 #include "device_utils.cuh"
 #include "sgemm_internal.h"
 
@@ -84,6 +85,20 @@ __global__ void wait_selftest_kernel(uint64_t timeout_ns, unsigned* fault) {
   if (threadIdx.x == 0 && !mbar_wait(b, 0, timeout_ns)) atomicOr(fault, (unsigned)kFaultSelftest);
 }
 
+// Thread 0 of every CTA writes its SM's cycle counter and the global nanosecond
+// timer to out[2 * smid], out[2 * smid + 1] (a later CTA on the same SM
+// overwrites an earlier one).  Two snapshots around a stretch of work give each
+// SM's average clock over it: cycles / nanoseconds.
+__global__ void clock_snapshot_kernel(unsigned long long* out, int slots) {
+  if (threadIdx.x != 0) return;
+  unsigned smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  if ((int)smid >= slots) return;
+  const unsigned long long t = global_timer_ns();
+  out[2 * smid] = (unsigned long long)clock64();
+  out[2 * smid + 1] = t;
+}
+
 unsigned grid_for(int64_t work, int per_block) {
   int64_t blocks = (work + per_block - 1) / per_block;
   if (blocks < 1) blocks = 1;
@@ -109,6 +124,11 @@ cudaError_t launch_scale(const GemmParams& p, cudaStream_t stream) {
 
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, unsigned* fault, cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns, fault);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_clock_snapshot(unsigned long long* out, int slots, int sm_count, cudaStream_t stream) {
+  clock_snapshot_kernel<<<(unsigned)(4 * sm_count), 32, 0, stream>>>(out, slots);
   return cudaGetLastError();
 }
 

@@ -154,6 +154,7 @@ cudaError_t launch_generic_gemm(bool transA, bool transB, const GemmParams& p, i
 cudaError_t launch_splitk_reduce(const GemmParams& p, int split, cudaStream_t stream);
 cudaError_t launch_scale(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, unsigned* fault, cudaStream_t stream);
+cudaError_t launch_clock_snapshot(unsigned long long* out, int slots, int sm_count, cudaStream_t stream);
 
 // Keeps e as this thread's last CUDA error (sgemm_last_cuda_error) and returns SGEMM_ERR_CUDA.
 int record_cuda_failure(cudaError_t e);

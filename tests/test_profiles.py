@@ -1,28 +1,60 @@
-"""The committed ncu summaries that bench.py reads DRAM traffic from: each
-exists, names the kernel digest and per-launch traffic it was captured with,
-and gives the commands that made it (never a capture that locks clocks)."""
+"""The committed ncu capture record bench.py reads DRAM traffic from
+(profiles/traffic.json): every entry names its kernel variant, workload,
+kernel digest and per-launch traffic, and points at an existing summary that
+gives the commands that made it (never a capture that locks clocks)."""
+import json
 import os
-import re
 
 import bench
 
 
-def test_every_profile_entry_parses():
-    assert bench.PROFILES
-    for (variant, workload), path in bench.PROFILES.items():
+def entries():
+    return json.load(open(bench.TRAFFIC_FILE))["entries"]
+
+
+def test_every_traffic_entry_is_complete():
+    es = entries()
+    assert es
+    seen = set()
+    for e in es:
+        key = (e["variant"], e["workload"])
+        assert key not in seen, key
+        seen.add(key)
+        assert len(e["kernel_digest"]) == 16 and int(e["kernel_digest"], 16) >= 0
+        assert int(e["traffic_bytes_per_launch"]) > 0
+        path = os.path.join(bench.ROOT, e["summary"])
         assert os.path.exists(path), path
         text = open(path).read()
-        assert re.search(r"^kernel_digest: [0-9a-f]{16}$", text, re.M), path
-        t = re.search(r"^traffic_bytes_per_launch: ([0-9]+)$", text, re.M)
-        assert t and int(t.group(1)) > 0, path
         cmds = [line for line in text.splitlines() if line.strip().startswith("ncu ")]
         assert cmds and all("--clock-control none" in c for c in cmds), path
-        assert workload in text or workload == "square4096", (path, workload)
 
 
 def test_traffic_only_for_the_matching_digest():
-    (variant, workload), path = next(iter(bench.PROFILES.items()))
-    digest = re.search(r"^kernel_digest: ([0-9a-f]+)$", open(path).read(), re.M).group(1)
-    assert bench.traffic_from_profile(variant, workload, digest) > 0
-    assert bench.traffic_from_profile(variant, workload, "0" * 16) is None
-    assert bench.traffic_from_profile(variant, "no_such_workload", digest) is None
+    e = entries()[0]
+    assert bench.traffic_from_profile(e["variant"], e["workload"], e["kernel_digest"]) == e["traffic_bytes_per_launch"]
+    assert bench.traffic_from_profile(e["variant"], e["workload"], "0" * 16) is None
+    assert bench.traffic_from_profile(e["variant"], "no_such_workload", e["kernel_digest"]) is None
+
+
+def test_snapshot_clock_from_counter_deltas():
+    import torch
+    b = torch.zeros(8, dtype=torch.int64)
+    a = torch.zeros(8, dtype=torch.int64)
+    # SM 0: 2.0e6 cycles in 1.0e6 ns (2000 MHz); SM 1: 1.9e6 in 1.0e6 (1900 MHz); SMs 2, 3 never ran
+    b[0], b[1], a[0], a[1] = 100, 5_000_000, 2_000_100, 6_000_000
+    b[2], b[3], a[2], a[3] = 7, 5_000_000, 1_900_007, 6_000_000
+    mhz, n = bench.snapshot_mhz(b, a)
+    assert n == 2 and abs(mhz - 1950.0) < 1e-6
+
+
+def test_hbm_roof_chosen_when_bytes_bind():
+    peaks = {"hbm_gbs": 6781.4, "bf16_tflops": 1910.0}
+    # skinny 64 x 4096 x 16384: 273.7 MB at HBM (40 us) outlast 8.6 GFLOP at the 3xTF32 peak (28 us)
+    roof = bench.tensor_roofline(100.0, peaks, None, 0.08)
+    bench.hbm_bound_roofline(roof, 273.7e6, 8.59e9, 0.08, peaks)
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s" and roof["tensor"]["unit"] == "TFLOP/s"
+    assert abs(roof["achieved"] - 273.7e6 / 0.08e-3 / 1e9) < 1e-6
+    # 4096^3: tensor-bound
+    roof = bench.tensor_roofline(270.0, peaks, None, 0.5)
+    bench.hbm_bound_roofline(roof, 268.4e6, 137.4e9, 0.5, peaks)
+    assert roof["bound"] == "tensor"
