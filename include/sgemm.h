@@ -99,9 +99,12 @@ enum sgemm_variant {
                                      per 128x128 tile, block-diagonally; tile_m = tile_n = 128 / group */
     SGEMM_VARIANT_TC_PAIR = 9,    /* 3xTF32 tensor cores on CTA pairs (clusters of 2 on one TPC): 256x128x32
                                      tiles, each CTA 128 rows and half of the tile's B columns */
-    SGEMM_VARIANT_TC_PRESPLIT = 10 /* 3xTF32 with A and B split once per call into TF32 hi / FP32 lo arrays
+    SGEMM_VARIANT_TC_PRESPLIT = 10,/* 3xTF32 with A and B split once per call into TF32 hi / FP32 lo arrays
                                       (in the workspace), then CTA pairs on 256x256x32 tiles reading both
                                       parts from shared memory */
+    SGEMM_VARIANT_TC_TF32 = 11    /* sgemm_tf32() only: A and B rounded to TF32 once per call (in the
+                                      workspace), one tensor-core product per k on CTA pairs, 256x256x32
+                                      tiles */
 };
 
 /*
@@ -299,6 +302,39 @@ int sgemm_plan_strided_batched(char transA, char transB, int64_t M, int64_t N, i
  * -1: out is NULL; -2: slots < 1.
  */
 int sgemm_clock_snapshot(unsigned long long *out, int slots, struct CUstream_st *stream);
+
+/*
+ * sgemm_tf32 -- reduced-precision inputs, FP32 accumulation: the tensor-core
+ * format for FP32 data that youngju.dev "CUDA architecture visualized"
+ * (テンソルコア) names.  Computes
+ *     C = alpha * op(tf32(A)) * op(tf32(B)) + beta * C
+ * where tf32(x) rounds x to 10 explicit significand bits, to nearest with
+ * ties away from zero (a finite x whose rounding carries past FLT_MAX gives
+ * +-Inf; +-Inf and NaN stay), and the products (exact in FP32) are summed in
+ * FP32.  Contract: |C - C_t| <= (K+2) 2^-24 (|alpha| sum|a_t b_t| + |beta c|)
+ * per element against that expression evaluated exactly on the rounded inputs
+ * (C_t), so the result differs from sgemm()'s by up to about 2^-11 relative
+ * per product -- this entry point trades FP32 accuracy for speed; sgemm()'s
+ * contract is unchanged.  Arguments, conventions, ownership, errors and
+ * asynchrony as sgemm(); any alignment.  Each operand is rounded once per
+ * call into a pooled workspace (4 bytes per element of op(A) and op(B), rows
+ * padded to a multiple of 4 floats), then CTA pairs compute 256x256 tiles with
+ * one tensor-core product per k (SGEMM_VARIANT_TC_TF32).  Needs a device
+ * where clusters of two CTAs can be co-scheduled, and K <= 2097120:
+ * SGEMM_ERR_UNSUPPORTED otherwise.
+ */
+int sgemm_tf32(char transA, char transB, int64_t M, int64_t N, int64_t K,
+               float alpha, const float *A, int64_t lda,
+               const float *B, int64_t ldb,
+               float beta, float *C, int64_t ldc,
+               struct CUstream_st *stream);
+
+/* What sgemm_tf32() would launch (sm_count as in sgemm_plan(); plan == NULL: -15). */
+int sgemm_tf32_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                    float alpha, const float *A, int64_t lda,
+                    const float *B, int64_t ldb,
+                    float beta, const float *C, int64_t ldc,
+                    int sm_count, sgemm_plan_t *plan);
 
 /*
  * sgemm_host -- the same operation with A, B and C in HOST memory (same

@@ -131,6 +131,35 @@ int oracle_sgemm_strided_batched(char transA, char transB, int64_t M, int64_t N,
     return 0;
 }
 
+/*
+ * TF32 rounding (the tensor-core format for FP32 data, youngju.dev "CUDA
+ * architecture visualized", テンソルコア): 1 sign bit, the 8 exponent bits of
+ * float32 and 10 fraction bits.  Its values are the floats whose 13 lowest
+ * fraction bits are zero, so the spacing (quantum) of values near |x| is
+ * 2^(floor(log2|x|) - 10) for normal x and 2^-136 below 2^-126.  y = x
+ * rounded to the nearest such value, ties away from zero; a rounding that
+ * carries past FLT_MAX gives +-Inf; +-0, +-Inf and NaN are kept.  Computed in
+ * double, where every step is exact.
+ */
+static float oracle_tf32(float x)
+{
+    if (x != x || isinf(x) || x == 0.0f) return x;
+    const double a = fabs((double)x);
+    int e;
+    frexp(a, &e);                       /* a = m * 2^e, 0.5 <= m < 1: floor(log2 a) = e - 1 */
+    int qexp = (e - 1) - 10;
+    if (qexp < -136) qexp = -136;       /* subnormal range: fixed quantum */
+    const double q = ldexp(1.0, qexp);
+    const double r = floor(a / q + 0.5) * q;   /* nearest multiple, ties away from zero */
+    const double y = x < 0.0f ? -r : r;
+    return (float)y;                    /* exact, or +-Inf past FLT_MAX */
+}
+
+void oracle_round_tf32(const float *x, float *y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_tf32(x[i]);
+}
+
 /* Sets the number of OpenMP threads later oracle calls use (n >= 1). */
 void oracle_set_num_threads(int n)
 {

@@ -500,6 +500,65 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   return plan_tiled(pr, e, variant, sm_count, plan);
 }
 
+// The TF32-input GEMM (sgemm_tf32): op(A) and op(B) rounded to TF32 once into the workspace
+// ([stream-K slots][A][B], 256-byte aligned parts, rows of round4(K) floats), then the CTA-pair
+// kernel with one tensor-core product per k over 256 x 256 tiles (the split-operand kernel's
+// schedule), then the fixup when a tile is shared.  Any alignment: the rounding pass reads the
+// operands as stored.  Needs CTA pairs (pair_clusters != 0).
+int make_tf32_plan(const Problem& pr, int sm_count, int pair_clusters, sgemm_plan_t* plan) {
+  *plan = sgemm_plan_t{};
+  plan->split_k = 1;
+  if (pr.M == 0 || pr.N == 0) {
+    plan->variant = SGEMM_VARIANT_NONE;
+    return SGEMM_OK;
+  }
+  if (pr.M > INT_MAX || pr.N > INT_MAX || pr.K > INT_MAX) return SGEMM_ERR_UNSUPPORTED;
+  if (pr.K == 0 || pr.alpha == 0.0f) {
+    plan->variant = SGEMM_VARIANT_SCALE;
+    plan->kernel_launches = 1;
+    plan->threads = 256;
+    return SGEMM_OK;
+  }
+  // the rounding pass's transposing grid holds K / 32 in dimension y
+  if (pair_clusters == 0 || ceil_div(pr.K, 32) > 65535) return SGEMM_ERR_UNSUPPORTED;
+  const int64_t clusters = std::max(1, pair_clusters > 0 ? pair_clusters : sm_count / 2);
+  const int64_t tiles = ceil_div(pr.M, 256) * ceil_div(pr.N, 256);
+  const int s = plan_stream_k(tiles, ceil_div(pr.K, 32), (int)clusters, plan);
+  if (s != SGEMM_OK) return s;
+  plan->variant = SGEMM_VARIANT_TC_TF32;
+  plan->tile_m = plan->tile_n = 256;
+  plan->tile_k = 32;
+  plan->stages = 6;
+  plan->threads = 320;
+  plan->smem_bytes = 6 * 32768 + 1024;
+  plan->grid_x *= 2;
+  plan->workspace_bytes = split_layout(pr.M, pr.N, pr.K, 1, 0, 0, plan->workspace_bytes * 4, 1).total();
+  plan->kernel_launches += 2;  // the rounding passes of A and B
+  return SGEMM_OK;
+}
+
+cudaError_t launch_tf32(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& st, uint8_t* ws,
+                        GemmParams* p, cudaStream_t stream) {
+  const int64_t slot_bytes = plan.split_k > 1 ? 2 * plan.grid_x * (int64_t)(128 * 256 * 4) : 0;
+  const SplitLayout l = split_layout(pr.M, pr.N, pr.K, 1, 0, 0, slot_bytes, 1);
+  const int64_t ldk = split_ldk(pr.K);
+  float* ar = reinterpret_cast<float*>(ws + round256(l.slots));
+  float* br = reinterpret_cast<float*>(ws + round256(l.slots) + round256(l.a_bytes));
+  p->ws = slot_bytes > 0 ? reinterpret_cast<float*>(ws) : nullptr;
+  p->za = p->zb = 0;
+  p->repair = 0;
+  cudaError_t e = launch_split_operand(pr.A, pr.lda, 0, !pr.ta, (int)pr.M, (int)pr.K, 1, ar, nullptr, ldk,
+                                       st.sm_count, stream);
+  if (e == cudaSuccess)
+    e = launch_split_operand(pr.B, pr.ldb, 0, pr.tb, (int)pr.N, (int)pr.K, 1, br, nullptr, ldk, st.sm_count, stream);
+  CUtensorMap ma, mb;
+  if (e == cudaSuccess) e = encode_split_map(ar, pr.K, pr.M, ldk, 1, &ma);
+  if (e == cudaSuccess) e = encode_split_map(br, pr.K, pr.N, ldk, 1, &mb);
+  if (e == cudaSuccess) e = launch_tf32_gemm(ma, mb, *p, stream);
+  if (e == cudaSuccess && slot_bytes > 0) e = launch_presplit_fixup(*p, (int)plan.sk_tiles, stream);
+  return e;
+}
+
 // TC_PRESPLIT: the split pass of op(A) and op(B) into the workspace ([stream-K slots][A hi][A lo]
 // [B hi][B lo], 256-byte aligned parts), then the GEMM over maps of the split arrays and the fixup.
 cudaError_t launch_presplit(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& st, uint8_t* ws,
@@ -570,7 +629,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
 
   CUtensorMap mapA, mapB;
   if (plan.variant != SGEMM_VARIANT_GENERIC && plan.variant != SGEMM_VARIANT_SMALL &&
-      plan.variant != SGEMM_VARIANT_TC_PRESPLIT) {
+      plan.variant != SGEMM_VARIANT_TC_PRESPLIT && plan.variant != SGEMM_VARIANT_TC_TF32) {
     int box_m, box_n;
     operand_boxes(plan, &box_m, &box_n);
     cudaError_t e = encode_operand_maps(pr.ta, pr.tb, pr.M, pr.N, pr.K, pr.A, pr.lda, pr.stride_a, pr.B, pr.ldb,
@@ -594,6 +653,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   cudaError_t e;
   if (plan.variant == SGEMM_VARIANT_TC_PRESPLIT) {
     e = launch_presplit(pr, plan, st, static_cast<uint8_t*>(ws ? ws : ext_ws), &p, stream);
+  } else if (plan.variant == SGEMM_VARIANT_TC_TF32) {
+    e = launch_tf32(pr, plan, st, static_cast<uint8_t*>(ws ? ws : ext_ws), &p, stream);
   } else if (plan.variant == SGEMM_VARIANT_GENERIC) {
     e = launch_generic_gemm(pr.ta, pr.tb, p, split, stream);
   } else if (plan.variant == SGEMM_VARIANT_SMALL) {
@@ -614,7 +675,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   }
   if (e == cudaSuccess && split > 1 && plan.variant != SGEMM_VARIANT_TC_TF32X3 &&
       plan.variant != SGEMM_VARIANT_TC_GROUPED && plan.variant != SGEMM_VARIANT_TC_PAIR &&
-      plan.variant != SGEMM_VARIANT_TC_PRESPLIT)
+      plan.variant != SGEMM_VARIANT_TC_PRESPLIT && plan.variant != SGEMM_VARIANT_TC_TF32)
     e = launch_splitk_reduce(p, split, stream);
   if (ws) {
     cudaError_t ef = cudaFreeAsync(ws, stream);
@@ -733,6 +794,41 @@ int sgemm_release_workspace(size_t keep_bytes) {
   cudaError_t e = cudaMemPoolTrimTo(st->pool, keep_bytes);
   if (e == cudaSuccess) e = trim_host_pool(dev, keep_bytes);
   return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
+}
+
+int sgemm_tf32(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+               const float* B, int64_t ldb, float beta, float* C, int64_t ldc, struct CUstream_st* stream) {
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  int dev;
+  DeviceState* st;
+  s = device_state(&dev, &st);
+  if (s != SGEMM_OK) return s;
+  sgemm_plan_t plan;
+  s = make_tf32_plan(pr, st->sm_count, st->pair_clusters, &plan);
+  if (s != SGEMM_OK) return s;
+  return launch_gemm(pr, plan, *st, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_tf32_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                    int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc, int sm_count,
+                    sgemm_plan_t* plan) {
+  if (!plan) return -15;
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  int pair_clusters = -1;
+  if (sm_count <= 0) {
+    int dev;
+    DeviceState* st;
+    s = device_state(&dev, &st);
+    if (s != SGEMM_OK) return s;
+    sm_count = st->sm_count;
+    pair_clusters = st->pair_clusters;
+  }
+  return make_tf32_plan(pr, sm_count, pair_clusters, plan);
 }
 
 int sgemm_strided_batched(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,

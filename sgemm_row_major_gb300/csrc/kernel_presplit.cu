@@ -56,8 +56,17 @@ __device__ __forceinline__ void split_one(float x, float& hi, float& lo) {
   lo = __fmaf_rn(hi, -1.0f, x);  // exact: x - hi
 }
 
-// Rows run along K: each thread takes 4 consecutive k (16-byte loads and stores;
-// src and dst rows are 16-byte aligned, K % 4 == 0 is not required: the tail is scalar).
+// The hi part alone is the TF32 rounding of x, except for a NaN: the tensor core reads only the
+// top 19 bits of a value, so a NaN whose payload lies in the 13 dropped fraction bits would reach
+// it as +-Inf (with the add-and-mask, or as stored).  Every NaN becomes a quiet NaN with all
+// payload bits set.  (With the lo part as well, lo = NaN carries it.)
+__device__ __forceinline__ float keep_nan(float x, float hi) { return x != x ? __uint_as_float(0x7FFFFFFFu) : hi; }
+
+// Rows run along K: each thread takes 4 consecutive k (16-byte stores; 16-byte loads when
+// VEC -- every source row 16-byte aligned -- else four 4-byte loads; K % 4 == 0 is not
+// required: the tail is scalar).  lo == nullptr: only hi is written (the rounding pass of the
+// TF32-input GEMM).
+template <bool VEC>
 __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict__ src, int64_t ld, int64_t stride,
                                                          int rows, int K, int products, float* __restrict__ hi,
                                                          float* __restrict__ lo, int64_t ldk) {
@@ -69,21 +78,29 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict
     const int64_t p = pr / rows, r = pr - p * rows;
     const float* s = src + p * stride + r * ld + 4 * k4;
     float* h = hi + pr * ldk + 4 * k4;
-    float* l = lo + pr * ldk + 4 * k4;
     if (4 * k4 + 3 < K) {
-      const float4 x = *reinterpret_cast<const float4*>(s);
+      const float4 x = VEC ? *reinterpret_cast<const float4*>(s) : make_float4(s[0], s[1], s[2], s[3]);
       float4 xh, xl;
       split4(x, xh, xl);
+      if (lo) {
+        *reinterpret_cast<float4*>(lo + pr * ldk + 4 * k4) = xl;
+      } else {
+        xh = make_float4(keep_nan(x.x, xh.x), keep_nan(x.y, xh.y), keep_nan(x.z, xh.z), keep_nan(x.w, xh.w));
+      }
       *reinterpret_cast<float4*>(h) = xh;
-      *reinterpret_cast<float4*>(l) = xl;
     } else {
-      for (int j = 0; j < K - 4 * k4; ++j) split_one(s[j], h[j], l[j]);
+      for (int j = 0; j < K - 4 * k4; ++j) {
+        float xh, xl;
+        split_one(s[j], xh, xl);
+        h[j] = lo ? xh : keep_nan(s[j], xh);
+        if (lo) lo[pr * ldk + 4 * k4 + j] = xl;
+      }
     }
   }
 }
 
 // Stored rows run along the other axis: a 32 x 32 block per CTA (32 x 8 threads), read along
-// the stored rows, written along K.
+// the stored rows (any alignment), written along K; lo == nullptr: hi only.
 __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __restrict__ src, int64_t ld,
                                                               int64_t stride, int rows, int K,
                                                               float* __restrict__ hi, float* __restrict__ lo,
@@ -100,14 +117,15 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __res
   __syncthreads();
   // write: row r = r0 + ty + 8j, k = k0 + tx
   float* h = hi + (int64_t)p * rows * ldk;
-  float* l = lo + (int64_t)p * rows * ldk;
+  float* l = lo ? lo + (int64_t)p * rows * ldk : nullptr;
   for (int j = 0; j < kSplitTile; j += 8) {
     const int r = r0 + (int)threadIdx.y + j, k = k0 + (int)threadIdx.x;
     if (r < rows && k < K) {
+      const float x = tile[threadIdx.x][threadIdx.y + j];
       float xh, xl;
-      split_one(tile[threadIdx.x][threadIdx.y + j], xh, xl);
-      h[(int64_t)r * ldk + k] = xh;
-      l[(int64_t)r * ldk + k] = xl;
+      split_one(x, xh, xl);
+      h[(int64_t)r * ldk + k] = lo ? xh : keep_nan(x, xh);
+      if (lo) l[(int64_t)r * ldk + k] = xl;
     }
   }
 }
@@ -118,12 +136,21 @@ constexpr int BMC = 128;                  // rows one CTA covers
 constexpr int BN = 256;                   // columns of a pair tile
 constexpr int BNC = 128;                  // columns of B one CTA loads
 constexpr int BK = 32;
-// Three stages fill shared memory (measured at 4096^3: 267 TFLOPS; two stages 212; six 16-k
-// stages with a 64-byte swizzle 247, their barrier, commit and relay traffic doubled).
-constexpr int kStages = 3;
 constexpr int kPartBytes = 128 * BK * 4;  // 16 KB: 128 rows (or columns) x 32 k, K-major, 128-byte swizzle
-constexpr int kStageBytes = 4 * kPartBytes;  // A hi, A lo, B hi, B lo
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+// PARTS = 2: 3xTF32 (a stage holds A hi, A lo, B hi, B lo); PARTS = 1: TF32 inputs (A hi, B hi:
+// one tensor-core product per k).  The stages fill shared memory (3xTF32 at 4096^3: three
+// stages 267 TFLOPS; two stages 212; six 16-k stages with a 64-byte swizzle 247, their barrier,
+// commit and relay traffic doubled).
+template <int PARTS>
+struct Cfg {
+  static constexpr int kStages = PARTS == 2 ? 3 : 6;
+  static constexpr int kStageBytes = 2 * PARTS * kPartBytes;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+  static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA");
+};
+constexpr int kStages = Cfg<2>::kStages;
+constexpr int kStageBytes = Cfg<2>::kStageBytes;
+constexpr int kSmemBytes = Cfg<2>::kSmemBytes;
 constexpr int kFoldWarps = 8;             // warps 2-9
 constexpr int kThreads = 32 * (2 + kFoldWarps);
 constexpr int kAccBufs = 2;
@@ -132,7 +159,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kFoldCols = 128;            // accumulator columns a folder thread owns
 constexpr int kFoldChunk = 32;            // columns loaded per round trip (register budget; 64 measured slower)
 static_assert(kAccBufs * kAccCols <= kTmemCols, "accumulators must fit in TMEM");
-static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA");
 
 // tcgen05 instruction descriptor, kind::tf32: FP32 accumulator, TF32 A and B,
 // both K-major, N = 256, M = 256 (the pair).
@@ -194,10 +220,13 @@ __device__ __forceinline__ void store_row(const GemmParams& p, float* crow, int 
   }
 }
 
+template <int PARTS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     presplit_gemm_kernel(const __grid_constant__ CUtensorMap mapAh, const __grid_constant__ CUtensorMap mapAl,
                          const __grid_constant__ CUtensorMap mapBh, const __grid_constant__ CUtensorMap mapBl,
                          const GemmParams p) {
+  constexpr int kStages = Cfg<PARTS>::kStages;
+  constexpr int kStageBytes = Cfg<PARTS>::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
   __shared__ __align__(8) uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
@@ -208,8 +237,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;  // the same in both CTAs (same kernel)
   const uint32_t sbase = raw_addr + pad;
-  // stage s: [A hi][A lo][B hi][B lo], 16 KB each, 1024-byte aligned
+  // stage s: [A hi][A lo][B hi][B lo] (PARTS = 1: [A hi][B hi]), 16 KB each, 1024-byte aligned
   auto part = [&](int s, int which) { return sbase + (uint32_t)(s * kStageBytes + which * kPartBytes); };
+  constexpr int kAhi = 0, kAlo = 1, kBhi = PARTS, kBlo = PARTS + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -270,10 +300,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // thread's remote arrive)
           const uint32_t fb = map_to_rank(smem_addr(&full[s]), 0);
           if (rank == 0) mbar_arrive_expect_tx(smem_addr(&full[s]), 2u * (uint32_t)kStageBytes);
-          tma_load_3d_pair(part(s, 0), &mapAh, fb, k0, m0, za);
-          tma_load_3d_pair(part(s, 1), &mapAl, fb, k0, m0, za);
-          tma_load_3d_pair(part(s, 2), &mapBh, fb, k0, n0, zb);
-          tma_load_3d_pair(part(s, 3), &mapBl, fb, k0, n0, zb);
+          tma_load_3d_pair(part(s, kAhi), &mapAh, fb, k0, m0, za);
+          if (PARTS == 2) tma_load_3d_pair(part(s, kAlo), &mapAl, fb, k0, m0, za);
+          tma_load_3d_pair(part(s, kBhi), &mapBh, fb, k0, n0, zb);
+          if (PARTS == 2) tma_load_3d_pair(part(s, kBlo), &mapBl, fb, k0, n0, zb);
           issued = t + 1;
         }
       }
@@ -307,14 +337,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tmem_fence_after_sync();
         const uint32_t acc = tmem + (uint32_t)b * kAccCols;
-        const uint64_t ahi = kmajor_sw128_desc(part(s, 0)), alo = kmajor_sw128_desc(part(s, 1));
-        const uint64_t bhi = kmajor_sw128_desc(part(s, 2)), blo = kmajor_sw128_desc(part(s, 3));
+        const uint64_t ahi = kmajor_sw128_desc(part(s, kAhi)), bhi = kmajor_sw128_desc(part(s, kBhi));
 #pragma unroll
         for (int ks = 0; ks < BK / 8; ++ks) {
           const uint64_t step = (uint64_t)(ks * 32) >> 4;  // 8 TF32 = 32 bytes along K
-          mma_pair_ss(acc, alo + step, bhi + step, ks == 0 ? 0u : 1u);  // fresh accumulator per K tile
-          mma_pair_ss(acc, ahi + step, blo + step, 1u);
-          mma_pair_ss(acc, ahi + step, bhi + step, 1u);
+          if (PARTS == 2) {
+            const uint64_t alo = kmajor_sw128_desc(part(s, kAlo)), blo = kmajor_sw128_desc(part(s, kBlo));
+            mma_pair_ss(acc, alo + step, bhi + step, ks == 0 ? 0u : 1u);  // fresh accumulator per K tile
+            mma_pair_ss(acc, ahi + step, blo + step, 1u);
+            mma_pair_ss(acc, ahi + step, bhi + step, 1u);
+          } else {
+            mma_pair_ss(acc, ahi + step, bhi + step, ks == 0 ? 0u : 1u);
+          }
         }
         mma_commit_pair(smem_addr(&empty[s]));     // stage s reusable in both CTAs
         mma_commit_pair(smem_addr(&acc_full[b]));  // accumulator b (both CTAs) holds K tile t
@@ -391,7 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         pair_tile_origin(p, g.tile, prod, m0, n0);
         const int row = m0 + BMC * (int)rank + 32 * q + lane;
         if (row < p.M) {
-          repair_nans(p, prod, row, n0 + kFoldCols * half, master2);
+          if (PARTS == 2) repair_nans(p, prod, row, n0 + kFoldCols * half, master2);
           float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
           if (p.c_vec) store_row<true>(p, crow, n0 + kFoldCols * half, master2);
           else         store_row<false>(p, crow, n0 + kFoldCols * half, master2);
@@ -460,7 +494,7 @@ __global__ void __launch_bounds__(kFixupThreads) presplit_fixup_kernel(const Gem
       const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[i] * (BMC * BN));
       v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
     }
-    repair_nans4(p, prod, row, col, v);
+    if (p.repair) repair_nans4(p, prod, row, col, v);
     float* cp = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
     if (CVEC && col + 3 < p.N) {
       float4 o;
@@ -483,8 +517,12 @@ __global__ void __launch_bounds__(kFixupThreads) presplit_fixup_kernel(const Gem
 }  // namespace tps
 
 cudaError_t prepare_presplit() {
-  return cudaFuncSetAttribute(tps::presplit_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              tps::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(tps::presplit_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       tps::Cfg<2>::kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tps::presplit_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tps::Cfg<1>::kSmemBytes);
+  return e;
 }
 
 cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, bool k_contig, int rows, int K,
@@ -493,9 +531,12 @@ cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, b
   if (rows <= 0 || K <= 0 || products <= 0) return cudaSuccess;
   if (k_contig) {
     const int64_t work = (int64_t)products * rows * ((K + 3) / 4);
-    const int64_t blocks = std::min<int64_t>((work + 255) / 256, (int64_t)sm_count * 8);
-    tps::split_rows_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, stream>>>(src, ld, stride, rows, K,
-                                                                                      products, hi, lo, ldk);
+    const unsigned blocks = (unsigned)std::max<int64_t>(std::min<int64_t>((work + 255) / 256, (int64_t)sm_count * 8), 1);
+    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && ld % 4 == 0 && (products == 1 || stride % 4 == 0);
+    if (vec)
+      tps::split_rows_kernel<true><<<blocks, 256, 0, stream>>>(src, ld, stride, rows, K, products, hi, lo, ldk);
+    else
+      tps::split_rows_kernel<false><<<blocks, 256, 0, stream>>>(src, ld, stride, rows, K, products, hi, lo, ldk);
   } else {
     const dim3 grid((unsigned)((rows + tps::kSplitTile - 1) / tps::kSplitTile),
                     (unsigned)((K + tps::kSplitTile - 1) / tps::kSplitTile), (unsigned)products);
@@ -507,8 +548,16 @@ cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, b
 
 cudaError_t launch_presplit_gemm(const CUtensorMap& mapAh, const CUtensorMap& mapAl, const CUtensorMap& mapBh,
                                  const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream) {
-  tps::presplit_gemm_kernel<<<2u * (unsigned)p.sk_grid, tps::kThreads, tps::kSmemBytes, stream>>>(mapAh, mapAl,
-                                                                                                   mapBh, mapBl, p);
+  tps::presplit_gemm_kernel<2><<<2u * (unsigned)p.sk_grid, tps::kThreads, tps::Cfg<2>::kSmemBytes, stream>>>(
+      mapAh, mapAl, mapBh, mapBl, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tf32_gemm(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
+                             cudaStream_t stream) {
+  // (the lo maps are not read with one part)
+  tps::presplit_gemm_kernel<1><<<2u * (unsigned)p.sk_grid, tps::kThreads, tps::Cfg<1>::kSmemBytes, stream>>>(
+      mapA, mapA, mapB, mapB, p);
   return cudaGetLastError();
 }
 

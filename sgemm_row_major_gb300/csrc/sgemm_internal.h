@@ -36,6 +36,7 @@ struct GemmParams {
   // - 1); partial tiles go to slots of BM*BN floats in ws (2 per CTA).
   int sk_grid = 0, sk_tile0 = 0;
   int64_t sk_iters = 0;
+  int repair = 1;                // tensor-core kernels: compute NaN sums again in FP32 (0: the TF32-input GEMM)
   uint64_t timeout_ns = 0;       // limit of every in-kernel wait
   unsigned* fault = nullptr;     // device fault word (bits of FaultBits), see fault_word()
 };
@@ -53,11 +54,10 @@ cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t 
 // Copies the tensor-core kernel's schedule from a plan (no-op for other
 // variants); the pair kernel's scheduling unit is the cluster of 2 CTAs.
 inline void set_schedule(const sgemm_plan_t& plan, GemmParams* p) {
-  if (plan.variant != SGEMM_VARIANT_TC_TF32X3 && plan.variant != SGEMM_VARIANT_TC_GROUPED &&
-      plan.variant != SGEMM_VARIANT_TC_PAIR && plan.variant != SGEMM_VARIANT_TC_PRESPLIT)
-    return;
-  p->sk_grid = (int)(plan.variant == SGEMM_VARIANT_TC_PAIR || plan.variant == SGEMM_VARIANT_TC_PRESPLIT
-                         ? plan.grid_x / 2 : plan.grid_x);
+  const bool pairs = plan.variant == SGEMM_VARIANT_TC_PAIR || plan.variant == SGEMM_VARIANT_TC_PRESPLIT ||
+                     plan.variant == SGEMM_VARIANT_TC_TF32;
+  if (plan.variant != SGEMM_VARIANT_TC_TF32X3 && plan.variant != SGEMM_VARIANT_TC_GROUPED && !pairs) return;
+  p->sk_grid = (int)(pairs ? plan.grid_x / 2 : plan.grid_x);
   p->sk_iters = plan.sk_iters;
   p->sk_tile0 = (int)plan.dp_tiles;
 }
@@ -71,12 +71,14 @@ struct SplitLayout {
   int64_t slots = 0;             // stream-K partial-sum slots (bytes, first in the workspace)
   int64_t a_products = 1, b_products = 1;
   int64_t a_bytes = 0, b_bytes = 0;  // one part (hi or lo) of op(A) / op(B), all products
-  int64_t total() const { return round256(slots) + 2 * round256(a_bytes) + 2 * round256(b_bytes); }
+  int parts = 2;                 // hi and lo (3xTF32), or hi only (the TF32-input GEMM)
+  int64_t total() const { return round256(slots) + parts * (round256(a_bytes) + round256(b_bytes)); }
 };
 inline SplitLayout split_layout(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t stride_a, int64_t stride_b,
-                                int64_t slot_bytes) {
+                                int64_t slot_bytes, int parts = 2) {
   SplitLayout l;
   l.slots = slot_bytes;
+  l.parts = parts;
   l.a_products = (batch > 1 && stride_a != 0) ? batch : 1;
   l.b_products = (batch > 1 && stride_b != 0) ? batch : 1;
   l.a_bytes = l.a_products * M * split_ldk(K) * 4;
@@ -131,7 +133,8 @@ cudaError_t launch_tc_pair(bool transA, bool transB, const CUtensorMap& mapA, co
                            const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_pair_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
 // 3xTF32 on split operands (kernel_presplit.cu): the split pass (per operand:
-// rows x K of op(X), from a stored layout whose rows run along K or not), then
+// rows x K of op(X), from a stored layout whose rows run along K or not, any
+// alignment; lo == nullptr writes hi only), then
 // the CTA-pair GEMM on 256x256x32 tiles with four maps over the split arrays,
 // then the fixup over the sk_tiles stream-K pair tiles when any is shared.
 cudaError_t prepare_presplit();
@@ -140,6 +143,11 @@ cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, b
 cudaError_t launch_presplit_gemm(const CUtensorMap& mapAh, const CUtensorMap& mapAl, const CUtensorMap& mapBh,
                                  const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
+// The TF32-input GEMM: the same CTA-pair kernel with one part per operand (maps over the rounded
+// copies, written by launch_split_operand with lo == nullptr) and one tensor-core product per k;
+// its stream-K tiles go through launch_presplit_fixup (p.repair = 0).
+cudaError_t launch_tf32_gemm(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
+                             cudaStream_t stream);
 // sgemm_plan() for a caller that cannot provide the split arrays of TC_PRESPLIT
 // (sgemm_noalloc): that variant, chosen or forced by override, is planned as TC_PAIR.
 // pair_clusters as in sgemm_plan_for_device().

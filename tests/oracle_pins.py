@@ -12,7 +12,10 @@ raises AssertionError when the oracle disagrees with:
   * a float64 BLAS matmul at a medium size within the final rounding,
   * the bound magnitude S = |alpha| |A|@|B| + |beta C|,
   * exact rational arithmetic, correctly rounded once, on values at the top of
-    the float32 range, and the IEEE 754 rules for Inf and NaN operands.
+    the float32 range, and the IEEE 754 rules for Inf and NaN operands,
+  * for the TF32-input GEMM: hand-worked roundings (tests/golden/tf32_round.txt),
+    a bit-level characterization of the rounding over all exponents, and a
+    float64 einsum of independently rounded tiny inputs.
 The same pins run against deliberately broken copies of the oracle in
 test_oracle_mutations.py, which shows that each plausible mistake fails one.
 """
@@ -402,10 +405,79 @@ def pin_ieee_special_values(lib):
     assert oracle.sgemm("N", "N", a, a, c, 1.0, 0.0, lib=lib)[0, 0] == 1.0
 
 
+def _tf32_by_bits(x: np.ndarray) -> np.ndarray:
+    """TF32 rounding characterized on the bits, independently of the oracle's arithmetic: the
+    candidates are x with its 13 low fraction bits cleared (t, toward zero) and the next TF32
+    value above it in magnitude (t + 2^13 ulps); the result is the nearer one, the larger
+    magnitude on a tie (ties away from zero).  Finite x only."""
+    x = np.asarray(x, np.float32)
+    b = x.view(np.uint32)
+    t = (b & np.uint32(0xFFFFE000)).view(np.float32)
+    u = ((b & np.uint32(0xFFFFE000)) + np.uint32(0x2000)).view(np.float32)  # may be +-Inf at the top
+    with np.errstate(over="ignore", invalid="ignore"):
+        dt = np.abs(x.astype(np.float64) - t.astype(np.float64))
+        du = np.abs(u.astype(np.float64) - x.astype(np.float64))
+    return np.where(dt < du, t, u).astype(np.float32)
+
+
+def pin_tf32_round_golden(lib):
+    """The hand-worked TF32 roundings of tests/golden/tf32_round.txt, and NaN stays NaN."""
+    rows = []
+    with open(os.path.join(GOLDEN, "tf32_round.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                x, y = line.split()[:2]
+                rows.append((int(x, 16), int(y, 16)))
+    x = np.array([r[0] for r in rows], np.uint32).view(np.float32)
+    want = np.array([r[1] for r in rows], np.uint32)
+    got = oracle.round_tf32(x, lib).view(np.uint32)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(hex(rows[i][0]), hex(int(got[i])), hex(rows[i][1])) for i in bad]
+    assert np.isnan(oracle.round_tf32(np.array([np.nan, -np.nan], np.float32), lib)).all()
+
+
+def pin_tf32_round_properties(lib):
+    """Finite floats over the whole exponent range (normal and subnormal, both signs): the result
+    is a TF32 value (13 low fraction bits zero, or +-Inf past the top) and equals the bit-level
+    characterization above."""
+    rng = np.random.default_rng(18)
+    bits = rng.integers(0, 1 << 32, size=200000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    got = oracle.round_tf32(x, lib)
+    fin = np.isfinite(got)
+    assert np.all((got[fin].view(np.uint32) & np.uint32(0x1FFF)) == 0)
+    assert np.array_equal(got.view(np.uint32), _tf32_by_bits(x).view(np.uint32))
+
+
+def pin_tf32_gemm(lib):
+    """The TF32-input GEMM: inputs that are already TF32 values give the FP32 oracle's result;
+    on tiny shapes with 12-bit dyadic inputs (which the rounding changes) it equals a float64
+    einsum of the bit-level-rounded inputs, rounded once (every product and sum exact)."""
+    rng = np.random.default_rng(19)
+    for (ta, tb), M, N, K in itertools.product(OPS, (1, 3, 7), (2, 5), (1, 4, 9)):
+        A = _stored(rng, ta, M, K, dyadic_bits=6)
+        B = _stored(rng, tb, K, N, dyadic_bits=6)
+        C = _stored(rng, "N", M, N, dyadic_bits=6)
+        assert np.array_equal(oracle.sgemm_tf32(ta, tb, A, B, C, 1.5, -0.5, lib=lib),
+                              oracle.sgemm(ta, tb, A, B, C, 1.5, -0.5, lib=lib)), (ta, tb, M, N, K)
+        A = _stored(rng, ta, M, K, dyadic_bits=12)
+        B = _stored(rng, tb, K, N, dyadic_bits=12)
+        ref = (1.5 * np.einsum("ik,kj->ij", _op(_tf32_by_bits(A), ta).astype(np.float64),
+                               _op(_tf32_by_bits(B), tb).astype(np.float64))
+               - 0.5 * C.astype(np.float64)).astype(np.float32)
+        got = oracle.sgemm_tf32(ta, tb, A, B, C, 1.5, -0.5, lib=lib)
+        assert np.array_equal(got, ref), (ta, tb, M, N, K)
+    # the rounding really happens: 1 + 2^-11 (a tie) times 1 gives 1 + 2^-10
+    a = np.array([[1 + 2.0 ** -11]], np.float32)
+    assert oracle.sgemm_tf32("N", "N", a, np.ones((1, 1), np.float32), lib=lib)[0, 0] == np.float32(1 + 2.0 ** -10)
+
+
 ALL_PINS = [
     pin_hand_2x2, pin_bruteforce_tiny, pin_integer_pattern, pin_integer_alpha_beta, pin_k1_exact,
     pin_alpha_zero, pin_k_zero, pin_beta_zero_nan_c, pin_identity, pin_transpose_identity,
     pin_transposed_copy, pin_alpha_pow2, pin_padding_not_read, pin_random_vs_float64_matmul,
     pin_bound_magnitude, pin_argument_errors, pin_conjugate_is_transpose, pin_batched_dyadic,
-    pin_batched_edges, pin_large_finite_exact, pin_ieee_special_values,
+    pin_batched_edges, pin_large_finite_exact, pin_ieee_special_values, pin_tf32_round_golden,
+    pin_tf32_round_properties, pin_tf32_gemm,
 ]

@@ -433,3 +433,23 @@ def test_planner_for_device_pair_clusters(lib):
         assert ei.value.status == code
     st = lib.sgemm_plan_for_device(b"N", b"N", 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, 0.0, FAKE, 64, 152, 76, None)
     assert st == -16
+
+
+def test_tf32_planner(lib):
+    """sgemm_tf32: rounded copies of op(A) and op(B) (one part each, rows of round4(K) floats)
+    after the stream-K slots, two rounding passes, the CTA-pair GEMM, the fixup when tiles are
+    shared; any alignment; no CTA-pair device: unsupported."""
+    def r256(x):
+        return (x + 255) // 256 * 256
+    p = sg.sgemm_tf32_plan("N", "N", 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, 0.0, FAKE, 4096, 152)
+    assert (p["variant_name"], p["tile_m"], p["tile_n"], p["grid_x"], p["stages"]) == ("TC_TF32", 256, 256, 152, 6)
+    slots = 2 * 152 * 128 * 256 * 4 if p["split_k"] > 1 else 0
+    assert p["workspace_bytes"] == r256(slots) + 2 * 4096 * 4096 * 4
+    assert p["kernel_launches"] == (4 if p["split_k"] > 1 else 3)
+    q = sg.sgemm_tf32_plan("T", "N", 333, 277, 501, 1.0, FAKE_ODD, 335, FAKE_ODD, 279, 0.0, FAKE, 277, 152)
+    assert q["variant_name"] == "TC_TF32"
+    assert q["workspace_bytes"] % 256 == 0 and q["workspace_bytes"] >= r256(333 * 504 * 4) + r256(277 * 504 * 4)
+    assert sg.sgemm_tf32_plan("N", "N", 64, 64, 0, 1.0, FAKE, 1, FAKE, 64, 0.0, FAKE, 64, 152)["variant_name"] == "SCALE"
+    with pytest.raises(sg.SgemmError) as ei:
+        sg.sgemm_tf32_plan("N", "N", 64, 64, 32 * 65536, 1.0, FAKE, 32 * 65536, FAKE, 64, 0.0, FAKE, 64, 152)
+    assert ei.value.status == sg.STATUS["ERR_UNSUPPORTED"]

@@ -40,6 +40,11 @@ MUTATIONS = [
     ("batch: C taken as packed", "C ? C + b * strideC : C", "C ? C + b * M * ldc : C"),
     ("batch: S not advanced", "S ? S + b * strideS : S", "S"),
     ("batch: negative stride accepted", "strideA < 0 || strideB", "strideB"),
+    ("tf32: truncation instead of rounding", "floor(a / q + 0.5) * q", "floor(a / q) * q"),
+    ("tf32: ties to even magnitude down", "floor(a / q + 0.5) * q", "ceil(a / q - 0.5) * q"),
+    ("tf32: 11 fraction bits", "int qexp = (e - 1) - 10;", "int qexp = (e - 1) - 11;"),
+    ("tf32: no subnormal quantum", "if (qexp < -136) qexp = -136;", "if (qexp < -149) qexp = -149;"),
+    ("tf32: sign dropped", "const double y = x < 0.0f ? -r : r;", "const double y = r;"),
 ]
 
 _CHILD = r"""
