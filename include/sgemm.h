@@ -52,7 +52,10 @@
  * down to products near the FP32 subnormal range.  The FP32 FFMA kernels
  * (IEEE operations throughout) are selected with
  * sgemm_set_variant_override(SGEMM_VARIANT_TMA_128x128 or
- * SGEMM_VARIANT_TMA_64x256, 0); unaligned operands always use the FFMA path.
+ * SGEMM_VARIANT_TMA_64x256, 0).  Operands TMA cannot load (a base not 16-byte
+ * aligned, lda or ldb not a multiple of 4) take the split-operand tensor-core
+ * kernel from 2 * 640^3 FLOP on (its split pass rewrites them aligned), the
+ * FP32 FFMA generic kernel below that.
  *
  * Errors: invalid arguments return -(argument index) (1 = transA ... 14 =
  * stream) before anything is launched, and C is untouched.  CUDA launch or

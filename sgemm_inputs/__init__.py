@@ -122,6 +122,10 @@ CASES: list[Case] = [
     Case("fc_8192x4096x1024", 8192, 4096, 1024, seed=6, dist="fc", group="fc"),
     Case("fc_16384x1024x4096", 16384, 1024, 4096, seed=7, dist="fc", group="fc"),
     Case("skinny_64x4096x16384", 64, 4096, 16384, seed=8, dist="fc", group="fc"),
+    # beyond the five configurations: the ragged shape with every stored row padded by one float,
+    # so no leading dimension is a multiple of 4 (operands TMA cannot load directly)
+    Case("unaligned_4097x3001x2053", 4097, 3001, 2053, "N", "N", 1.0, 1.0, 9, "uniform", 1, "uniform",
+         "unaligned"),
 ]
 
 HEADLINE = "square4096"

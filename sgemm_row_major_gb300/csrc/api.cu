@@ -272,6 +272,11 @@ constexpr int64_t kPairSmemBytes = 6 * 24576 + 2 * 16384 + 1024;
 // ... and of the split-operand kernel (kernel_presplit.cu: 3 stages of A hi/lo and B hi/lo, 64 KB each).
 constexpr int64_t kPresplitSmemBytes = 3 * 65536 + 1024;
 constexpr double kMinFlopPerSplitByte = 128.0;
+// Calls with operands TMA cannot load go to the split-operand kernel from this size on (measured
+// on GB300 with bases one float off alignment and ld % 4 != 0, split-operand / generic kernel:
+// 512^3 33.4 / 27.3 us, 1000x1300x700 44.2 / 107.2 us, 2048^3 102 / 638 us, 4097x3001x2053
+// 270 / 1862 us; below the crossover the split passes' latency dominates).
+constexpr double kMinUnalignedSplitFlop = 2.0 * 640 * 640 * 640;
 constexpr int64_t kMaxSplitBytes = int64_t{4} << 30;
 
 // Which kernels can run a problem (alignment, extents, grid limits) and the
@@ -312,8 +317,10 @@ Eligibility eligibility(const Problem& pr, int sm_count, int pair_clusters, bool
   // cannot run), < 0 not known (a device of sm_count SMs: SMs / 2, one cluster per TPC)
   e.pair = pair_clusters != 0;
   e.clusters = std::max(1, pair_clusters > 0 ? pair_clusters : sm_count / 2);
-  // (the split pass's transposing grid: K / 32 and the products in grid dimensions y and z)
-  e.presplit = e.tma && e.pair && allow_presplit && ceil_div(pr.K, 32) <= 65535 && pr.batch <= 65535;
+  // The split pass reads the operands as stored, whatever their alignment, and writes aligned
+  // K-contiguous arrays for the GEMM's TMA loads, so operands TMA cannot load qualify too (the
+  // transposing pass's grid holds K / 32 and the products in dimensions y and z).
+  e.presplit = e.pair && allow_presplit && ceil_div(pr.K, 32) <= 65535 && pr.batch <= 65535;
   return e;
 }
 
@@ -326,7 +333,7 @@ int choose_variant(const Problem& pr, const Eligibility& e, int sm_count) {
   // rules below, several products to a tile (block-diagonal) for a batch of
   // at least one product per SM with M, N <= 64; the generic SIMT kernel
   // otherwise.  The FP32 FFMA kernels (TMA-fed, small-product) stay
-  // selectable by override: IEEE FP32 operations, exact Inf handling.
+  // selectable by override: IEEE FP32 operations throughout.
   int variant = e.tma ? SGEMM_VARIANT_TC_TF32X3 : SGEMM_VARIANT_GENERIC;
   // CTA pairs (256 x 128 tiles) when every cluster gets at least one whole
   // tile: measured on GB300 2-5% faster than one CTA per 128 x 128 tile on
@@ -343,13 +350,21 @@ int choose_variant(const Problem& pr, const Eligibility& e, int sm_count) {
   // at 64 x 512x1024x1024 (60 FLOP per split byte: 142.4 / 195.1) and on fewer tiles (48 tiles:
   // 2048x1536x2048 154.8 / 160.5; 1024^3 49.7 / 71.7).  The split arrays are capped at
   // kMaxSplitBytes of workspace.
-  if (e.presplit && pr.M > 128 && 5 * ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.batch >= 4 * e.clusters) {
-    const SplitLayout sl = split_layout(pr.M, pr.N, pr.K, pr.batch, pr.stride_a, pr.stride_b, 0);
-    const double flops = 2.0 * (double)pr.M * (double)pr.N * (double)pr.K * (double)pr.batch;
-    if (flops >= kMinFlopPerSplitByte * 3.0 * (double)(sl.a_bytes + sl.b_bytes) &&
-        2 * (sl.a_bytes + sl.b_bytes) <= kMaxSplitBytes)
-      variant = SGEMM_VARIANT_TC_PRESPLIT;
-  }
+  const SplitLayout sl = split_layout(pr.M, pr.N, pr.K, pr.batch, pr.stride_a, pr.stride_b, 0);
+  const bool split_fits = 2 * (sl.a_bytes + sl.b_bytes) <= kMaxSplitBytes;
+  const double flops = 2.0 * (double)pr.M * (double)pr.N * (double)pr.K * (double)pr.batch;
+  if (e.tma && e.presplit && split_fits && pr.M > 128 &&
+      5 * ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.batch >= 4 * e.clusters &&
+      flops >= kMinFlopPerSplitByte * 3.0 * (double)(sl.a_bytes + sl.b_bytes))
+    variant = SGEMM_VARIANT_TC_PRESPLIT;
+  // Operands TMA cannot load (a base not 16-byte aligned, lda or ldb not a multiple of 4, a batch
+  // stride not a multiple of 4): the split pass rewrites them aligned, so the split-operand kernel
+  // runs them on the tensor cores whenever the call is large enough to amortize the pass and its
+  // 256 x 256 tiles are at least a quarter full; the generic FP32 kernel takes the rest (batches
+  // of small products among them).
+  if (!e.tma && e.presplit && split_fits && flops >= kMinUnalignedSplitFlop &&
+      4.0 * (double)pr.M * (double)pr.N >= (double)(ceil_div(pr.M, 256) * 256) * (double)(ceil_div(pr.N, 256) * 256))
+    variant = SGEMM_VARIANT_TC_PRESPLIT;
   if (e.group && pr.batch >= sm_count) variant = SGEMM_VARIANT_TC_GROUPED;
 
   switch (g_override_variant.load()) {

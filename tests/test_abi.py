@@ -120,10 +120,17 @@ def test_planner_variants(lib):
     assert plan("N", "N", 128, 65536, 1024)["variant_name"] == "TC_TF32X3"
     assert plan("N", "N", 129, 128 * 76, 64)["variant_name"] == "TC_PAIR"
     assert plan("N", "N", 129, 128 * 75, 64)["variant_name"] == "TC_TF32X3"
-    # unaligned base or ld not a multiple of 4 -> the generic (edge) kernel
+    # unaligned base or ld not a multiple of 4: the generic (edge) kernel up to 2 * 640^3 FLOP, the
+    # split-operand kernel (whose split pass rewrites the operands aligned) from there on
     assert plan("N", "N", 512, 512, 512, A=FAKE_ODD)["variant_name"] == "GENERIC"
     assert plan("N", "N", 512, 512, 513, lda=515)["variant_name"] == "GENERIC"
     assert plan("T", "T", 512, 512, 512, ldb=514)["variant_name"] == "GENERIC"
+    assert plan("N", "N", 640, 640, 639, A=FAKE_ODD)["variant_name"] == "GENERIC"
+    assert plan("N", "N", 640, 640, 640, A=FAKE_ODD)["variant_name"] == "TC_PRESPLIT"
+    assert plan("N", "N", 1000, 1300, 700, lda=701)["variant_name"] == "TC_PRESPLIT"
+    assert plan("T", "T", 4096, 4096, 4096, ldb=4097)["variant_name"] == "TC_PRESPLIT"
+    # ... unless CTA pairs cannot run (the split-operand kernel is a CTA-pair kernel)
+    assert dplan("N", "N", 2048, 2048, 2048, 152, 0, A=FAKE_ODD)["variant_name"] == "GENERIC"
     # ragged padded shapes of the transpose sweep keep the TMA-fed path (ld % 4 == 0)
     for ta, tb, lda, ldb in (("N", "N", 2060, 3008), ("N", "T", 2060, 2060), ("T", "N", 4104, 3008),
                              ("T", "T", 4104, 2060)):

@@ -105,6 +105,19 @@ def test_batched_dyadic_exact(ops, shared):
 
 
 @pytest.mark.parametrize("ops", ["NN", "TT"])
+def test_batched_odd_strides_on_tensor_cores(ops):
+    """Strides and leading dimensions that are not multiples of 4 floats on a batch large enough for
+    the split-operand kernel (its split pass reads any layout), a shared B among them."""
+    ta, tb = ops
+    batch, M, N, K = 6, 300, 270, 601
+    d = si.make_batched(batch, M, N, K, ta, tb, seed=33, pad=1, gap=3, align=1, shared="B")
+    assert plan_of(ta, tb, M, N, K, d, batch)["variant_name"] == "TC_PRESPLIT"
+    got = gpu_batched(ta, tb, M, N, K, 1.5, -0.5, d, batch)
+    ref, S = oracle_batched(ta, tb, M, N, K, 1.5, -0.5, d, batch)
+    check_batched(got, ref, S, d, batch, M, N, K, f"odd strides tensor cores {ops}")
+
+
+@pytest.mark.parametrize("ops", ["NN", "TT"])
 def test_batched_odd_strides_take_generic(ops):
     """Strides that are not multiples of 4 floats: the any-alignment kernel, same bounds."""
     ta, tb = ops

@@ -198,6 +198,36 @@ def test_deterministic_and_transpose_identity(variant):
         assert np.all(err <= 2 * (K + 2) * 2.0 ** -24 * S)
 
 
+@pytest.mark.parametrize("ops", OPS)
+def test_unaligned_operands_on_tensor_cores(ops):
+    """Operands TMA cannot load, large enough for the split-operand kernel: its split pass reads
+    them as stored (bases off alignment, ld % 4 != 0) and writes aligned arrays; dyadic inputs
+    give the oracle's result bit for bit, random ones meet the bounds."""
+    ta, tb = ops
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(22)
+    M, N, K = 700, 650, 1203
+    for fill in ("dyadic", "uniform"):
+        A = stored(rng, ta, M, K, pad=3, fill=fill)
+        B = stored(rng, tb, K, N, pad=1, fill=fill)
+        C = dyadic(rng, M, N + 5)
+        plan = sg.sgemm_plan(ta, tb, M, N, K, 1.0, 4, ld_of(A), 4, ld_of(B), 1.0, 4, N + 5, sm_count=152)
+        assert plan["variant_name"] == "TC_PRESPLIT"
+        dA = torch.zeros(A.size + 1, device="cuda"); dA[1:] = to_dev(A.reshape(-1))
+        dB = torch.zeros(B.size + 3, device="cuda"); dB[3:] = to_dev(B.reshape(-1))
+        dC = torch.zeros(C.size + 2, device="cuda"); dC[2:] = to_dev(C.reshape(-1))
+        sg.sgemm(ta, tb, M, N, K, 1.0, dA.data_ptr() + 4, ld_of(A), dB.data_ptr() + 12, ld_of(B), 1.0,
+                 dC.data_ptr() + 8, N + 5)
+        assert sg.sgemm_sync_status() == 0
+        got = dC[2:].cpu().numpy().reshape(M, N + 5)
+        ref, S = oracle_ref(ta, tb, A, B, C, 1.0, 1.0, M, N, K)
+        if fill == "dyadic":
+            check_exact(got[:, :N], ref, f"unaligned tensor-core {ops}")
+        else:
+            check_bound(got[:, :N], ref, S, K, f"unaligned tensor-core {ops}")
+        assert np.array_equal(got[:, N:], C[:, N:]), "columns past N were written"
+
+
 def test_non_default_stream_and_matmul_helper():
     torch = pytest.importorskip("torch")
     rng = np.random.default_rng(7)

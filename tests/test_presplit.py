@@ -91,13 +91,21 @@ def test_config_parity(name):
 
 @pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (777, 1000, 2053)])
 def test_same_sums_as_other_tensor_core_kernels(M, N, K):
-    """One cluster (or CTA) per tile, no stream-K: every element is summed in the same order."""
+    """One cluster (or CTA) per tile, no stream-K: every element is summed in the same order.
+    (A's rows are padded to a multiple of 4 floats, so TMA can load it for the one-CTA kernel.)"""
     rng = np.random.default_rng(K)
-    A = (2 * rng.random((M, K)) - 1).astype(np.float32)
+    lda = (K + 3) // 4 * 4
+    A = si.embed_padded((2 * rng.random((M, K)) - 1).astype(np.float32), lda)
     B = (2 * rng.random((K, N)) - 1).astype(np.float32)
     C = (2 * rng.random((M, N)) - 1).astype(np.float32)
-    one = gpu_sgemm("N", "N", M, N, K, 1.5, A, K, B, N, -0.5, C, N, variant="TC_TF32X3", split=1)
-    pre = gpu_sgemm("N", "N", M, N, K, 1.5, A, K, B, N, -0.5, C, N, variant=V, split=1)
+    for v in ("TC_TF32X3", V):
+        sg.sgemm_set_variant_override(v, 1)
+        try:
+            assert sg.sgemm_plan("N", "N", M, N, K, 1.5, 1 << 20, lda, 1 << 20, N, -0.5, 1 << 20, N)["variant_name"] == v
+        finally:
+            sg.sgemm_set_variant_override("AUTO", 0)
+    one = gpu_sgemm("N", "N", M, N, K, 1.5, A, lda, B, N, -0.5, C, N, variant="TC_TF32X3", split=1)
+    pre = gpu_sgemm("N", "N", M, N, K, 1.5, A, lda, B, N, -0.5, C, N, variant=V, split=1)
     check_exact(pre, one, f"presplit vs one-CTA {M}x{N}x{K}")
 
 
