@@ -84,7 +84,9 @@ enum sgemm_status {
     SGEMM_ERR_TIMEOUT = 2,     /* a bounded in-kernel wait gave up (reported by sgemm_sync_status) */
     SGEMM_ERR_NOMEM = 3,       /* the call's workspace (partial sums, split operands) could not be allocated */
     SGEMM_ERR_UNSUPPORTED = 4, /* a dimension or leading dimension >= 2^31, or no usable device */
-    SGEMM_ERR_SCRATCH_LIMIT = 5 /* sgemm_noalloc: the problem needs more scratch than its static array */
+    SGEMM_ERR_SCRATCH_LIMIT = 5,/* sgemm_noalloc: the problem needs more scratch than its static array */
+    SGEMM_ERR_BOUNDS = 6       /* debug build: a kernel index fell outside its buffer (reported by
+                                  sgemm_sync_status; the access was skipped) */
     /* negative values: -(index of the invalid argument), BLAS xerbla style */
 };
 
@@ -293,6 +295,28 @@ int sgemm_plan_strided_batched(char transA, char transB, int64_t M, int64_t N, i
                                float beta, const float *C, int64_t ldc,
                                int64_t strideA, int64_t strideB, int64_t strideC,
                                int64_t batch_count, int sm_count, sgemm_plan_t *plan);
+
+/*
+ * Debug build (libsgemm_debug.so, the same sources compiled with
+ * -DSGEMM_DEBUG_BOUNDS; the pages suggest checking every access, youngju.dev
+ * "CUDA architecture visualized", よくある落とし穴): every global-memory index
+ * of the kernels, and the shared- and tensor-memory offsets of the splitters,
+ * is checked against its buffer's extent before the access.  A violation skips
+ * the access (nothing traps, nothing is touched out of bounds), sets a bit that
+ * sgemm_sync_status() reports as SGEMM_ERR_BOUNDS, and keeps the first
+ * violation for sgemm_bounds_report(): *site (1 C, 2 workspace, 3 A or a split
+ * source, 4 B, 5 split arrays, 6 shared memory, 7 tensor memory, 8 self-test)
+ * and *offset (elements, bytes or columns from the buffer's start); both 0
+ * when there was none; reading clears it (-1 / -2: site / offset NULL).
+ * sgemm_debug_bounds_enabled() is 1 in the debug library, 0 in libsgemm.so.
+ * sgemm_selftest_bounds() runs one check of an index one past its limit (never
+ * dereferenced): in the debug library the next sgemm_sync_status() returns
+ * SGEMM_ERR_BOUNDS and the report gives site 8, offset 64; in libsgemm.so
+ * nothing is recorded.
+ */
+int sgemm_bounds_report(unsigned *site, long long *offset);
+int sgemm_debug_bounds_enabled(void);
+int sgemm_selftest_bounds(struct CUstream_st *stream);
 
 /*
  * Measurement aid: enqueues on `stream` a tiny kernel whose CTAs (four per

@@ -26,7 +26,8 @@ __all__ = [
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_lib", "libsgemm.so")
 
-STATUS = {"OK": 0, "ERR_CUDA": 1, "ERR_TIMEOUT": 2, "ERR_NOMEM": 3, "ERR_UNSUPPORTED": 4, "ERR_SCRATCH_LIMIT": 5}
+STATUS = {"OK": 0, "ERR_CUDA": 1, "ERR_TIMEOUT": 2, "ERR_NOMEM": 3, "ERR_UNSUPPORTED": 4, "ERR_SCRATCH_LIMIT": 5,
+          "ERR_BOUNDS": 6}
 NOALLOC_SCRATCH_BYTES = 32 << 20  # SGEMM_NOALLOC_SCRATCH_BYTES in include/sgemm.h
 VARIANTS = {"AUTO": 0, "NONE": 1, "SCALE": 2, "GENERIC": 3, "TMA_128x128": 4, "TMA_64x256": 5, "TC_TF32X3": 6,
             "SMALL": 7, "TC_GROUPED": 8, "TC_PAIR": 9,
@@ -60,6 +61,60 @@ def library_path() -> str:
     return _LIB_PATH
 
 
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """C signatures of the exported entry points."""
+    i64, f32, vp, ch = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_char
+    lib.sgemm.restype = ctypes.c_int
+    lib.sgemm.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+    lib.sgemm_host.restype = ctypes.c_int
+    lib.sgemm_host.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+    lib.sgemm_noalloc.restype = ctypes.c_int
+    lib.sgemm_noalloc.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+    lib.sgemm_ex.restype = ctypes.c_int
+    lib.sgemm_ex.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp, ctypes.c_size_t, vp]
+    lib.sgemm_workspace_size.restype = ctypes.c_int
+    lib.sgemm_workspace_size.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    lib.sgemm_plan.restype = ctypes.c_int
+    lib.sgemm_plan.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ctypes.c_int,
+                               ctypes.POINTER(PlanStruct)]
+    lib.sgemm_plan_for_device.restype = ctypes.c_int
+    lib.sgemm_plan_for_device.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                          ctypes.c_int, ctypes.c_int, ctypes.POINTER(PlanStruct)]
+    lib.sgemm_release_workspace.restype = ctypes.c_int
+    lib.sgemm_release_workspace.argtypes = [ctypes.c_size_t]
+    lib.sgemm_clock_snapshot.restype = ctypes.c_int
+    lib.sgemm_clock_snapshot.argtypes = [vp, ctypes.c_int, vp]
+    lib.sgemm_tf32.restype = ctypes.c_int
+    lib.sgemm_tf32.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+    lib.sgemm_tf32_plan.restype = ctypes.c_int
+    lib.sgemm_tf32_plan.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ctypes.c_int,
+                                    ctypes.POINTER(PlanStruct)]
+    lib.sgemm_strided_batched.restype = ctypes.c_int
+    lib.sgemm_strided_batched.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                          i64, i64, i64, i64, vp]
+    lib.sgemm_plan_strided_batched.restype = ctypes.c_int
+    lib.sgemm_plan_strided_batched.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                               i64, i64, i64, i64, ctypes.c_int, ctypes.POINTER(PlanStruct)]
+    lib.sgemm_status_string.restype = ctypes.c_char_p
+    lib.sgemm_status_string.argtypes = [ctypes.c_int]
+    lib.sgemm_last_cuda_error.restype = ctypes.c_int
+    lib.sgemm_last_cuda_error.argtypes = []
+    lib.sgemm_sync_status.restype = ctypes.c_int
+    lib.sgemm_sync_status.argtypes = [vp]
+    lib.sgemm_set_variant_override.restype = ctypes.c_int
+    lib.sgemm_set_variant_override.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.sgemm_selftest_wait_timeout.restype = ctypes.c_int
+    lib.sgemm_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+    lib.sgemm_bounds_report.restype = ctypes.c_int
+    lib.sgemm_bounds_report.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.POINTER(ctypes.c_longlong)]
+    lib.sgemm_debug_bounds_enabled.restype = ctypes.c_int
+    lib.sgemm_debug_bounds_enabled.argtypes = []
+    lib.sgemm_selftest_bounds.restype = ctypes.c_int
+    lib.sgemm_selftest_bounds.argtypes = [vp]
+    return lib
+
+
 def load() -> ctypes.CDLL:
     """Load the compiled libsgemm.so (build it with ``python -m sgemm_row_major_gb300.build``)."""
     global _lib
@@ -69,52 +124,18 @@ def load() -> ctypes.CDLL:
         if not os.path.exists(_LIB_PATH):
             raise ImportError(f"libsgemm.so not built: {_LIB_PATH} is missing "
                               "(run `python -m sgemm_row_major_gb300.build`)")
-        lib = ctypes.CDLL(_LIB_PATH)
-        i64, f32, vp, ch = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_char
-        lib.sgemm.restype = ctypes.c_int
-        lib.sgemm.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
-        lib.sgemm_host.restype = ctypes.c_int
-        lib.sgemm_host.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
-        lib.sgemm_noalloc.restype = ctypes.c_int
-        lib.sgemm_noalloc.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
-        lib.sgemm_ex.restype = ctypes.c_int
-        lib.sgemm_ex.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp, ctypes.c_size_t, vp]
-        lib.sgemm_workspace_size.restype = ctypes.c_int
-        lib.sgemm_workspace_size.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
-                                             ctypes.POINTER(ctypes.c_size_t)]
-        lib.sgemm_plan.restype = ctypes.c_int
-        lib.sgemm_plan.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ctypes.c_int,
-                                   ctypes.POINTER(PlanStruct)]
-        lib.sgemm_plan_for_device.restype = ctypes.c_int
-        lib.sgemm_plan_for_device.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
-                                              ctypes.c_int, ctypes.c_int, ctypes.POINTER(PlanStruct)]
-        lib.sgemm_release_workspace.restype = ctypes.c_int
-        lib.sgemm_release_workspace.argtypes = [ctypes.c_size_t]
-        lib.sgemm_clock_snapshot.restype = ctypes.c_int
-        lib.sgemm_clock_snapshot.argtypes = [vp, ctypes.c_int, vp]
-        lib.sgemm_tf32.restype = ctypes.c_int
-        lib.sgemm_tf32.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
-        lib.sgemm_tf32_plan.restype = ctypes.c_int
-        lib.sgemm_tf32_plan.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ctypes.c_int,
-                                        ctypes.POINTER(PlanStruct)]
-        lib.sgemm_strided_batched.restype = ctypes.c_int
-        lib.sgemm_strided_batched.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
-                                              i64, i64, i64, i64, vp]
-        lib.sgemm_plan_strided_batched.restype = ctypes.c_int
-        lib.sgemm_plan_strided_batched.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
-                                                   i64, i64, i64, i64, ctypes.c_int, ctypes.POINTER(PlanStruct)]
-        lib.sgemm_status_string.restype = ctypes.c_char_p
-        lib.sgemm_status_string.argtypes = [ctypes.c_int]
-        lib.sgemm_last_cuda_error.restype = ctypes.c_int
-        lib.sgemm_last_cuda_error.argtypes = []
-        lib.sgemm_sync_status.restype = ctypes.c_int
-        lib.sgemm_sync_status.argtypes = [vp]
-        lib.sgemm_set_variant_override.restype = ctypes.c_int
-        lib.sgemm_set_variant_override.argtypes = [ctypes.c_int, ctypes.c_int]
-        lib.sgemm_selftest_wait_timeout.restype = ctypes.c_int
-        lib.sgemm_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
-        _lib = lib
-        return lib
+        _lib = _declare(ctypes.CDLL(_LIB_PATH))
+        return _lib
+
+
+def load_debug() -> ctypes.CDLL:
+    """The bounds-checking build libsgemm_debug.so (``python -m sgemm_row_major_gb300.build --debug``),
+    loaded beside libsgemm.so with the same entry points; its kernels check every index."""
+    path = os.path.join(os.path.dirname(_LIB_PATH), "libsgemm_debug.so")
+    if not os.path.exists(path):
+        raise ImportError(f"libsgemm_debug.so not built: {path} is missing "
+                          "(run `python -m sgemm_row_major_gb300.build --debug`)")
+    return _declare(ctypes.CDLL(path))
 
 
 def _ptr(x) -> int | None:

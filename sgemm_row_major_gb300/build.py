@@ -22,6 +22,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIBRARY = os.path.join(LIB_DIR, "libsgemm.so")
+# the same sources with the kernels' bounds checks compiled in (-DSGEMM_DEBUG_BOUNDS)
+DEBUG_LIBRARY = os.path.join(LIB_DIR, "libsgemm_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
@@ -104,9 +106,9 @@ def _digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, verbose: bool, debug: bool = False) -> str:
+    obj = os.path.join(BUILD_DIR, ("debug_" if debug else "") + os.path.basename(src) + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *(["-DSGEMM_DEBUG_BOUNDS"] if debug else []), "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -117,27 +119,29 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libsgemm.so if any source changed; returns its path."""
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile and link libsgemm.so (debug=True: libsgemm_debug.so, the bounds-checking build) if
+    any source changed; returns its path."""
     os.makedirs(BUILD_DIR, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
-    stamp = os.path.join(BUILD_DIR, "digest.txt")
+    library = DEBUG_LIBRARY if debug else LIBRARY
+    stamp = os.path.join(BUILD_DIR, "digest_debug.txt" if debug else "digest.txt")
     digest = source_digest()
-    if not force and os.path.exists(LIBRARY) and os.path.exists(stamp) and open(stamp).read() == digest:
-        return LIBRARY
+    if not force and os.path.exists(library) and os.path.exists(stamp) and open(stamp).read() == digest:
+        return library
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    tmp = LIBRARY + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose, debug), srcs))
+    tmp = library + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stderr}")
-    os.replace(tmp, LIBRARY)
+    os.replace(tmp, library)
     with open(stamp, "w") as f:
         f.write(digest)
-    return LIBRARY
+    return library
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -65,6 +65,7 @@ struct DeviceState {
   int sm_count = 0;
   int pair_clusters = 0;  // co-resident clusters of the CTA-pair kernel; 0: pairs cannot run here
   unsigned* fault = nullptr;
+  unsigned long long* bounds = nullptr;  // debug build: first bounds violation
   cudaMemPool_t pool = nullptr;
 };
 DeviceState g_devices[kMaxDevices];
@@ -93,6 +94,7 @@ int device_state(int* device_out, DeviceState** st_out) {
     if (!st.ready.load(std::memory_order_relaxed)) {
       cudaError_t err = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
       if (err == cudaSuccess) err = fault_word(&st.fault);
+      if (err == cudaSuccess) err = bounds_word(&st.bounds);
       if (err == cudaSuccess) err = prepare_tma_op_nn();
       if (err == cudaSuccess) err = prepare_tma_op_nt();
       if (err == cudaSuccess) err = prepare_tma_op_tn();
@@ -563,9 +565,10 @@ cudaError_t launch_tf32(const Problem& pr, const sgemm_plan_t& plan, const Devic
   p->za = p->zb = 0;
   p->repair = 0;
   cudaError_t e = launch_split_operand(pr.A, pr.lda, 0, !pr.ta, (int)pr.M, (int)pr.K, 1, ar, nullptr, ldk,
-                                       st.sm_count, stream);
+                                       st.sm_count, stream, p->fault, p->bounds, p->a_elems);
   if (e == cudaSuccess)
-    e = launch_split_operand(pr.B, pr.ldb, 0, pr.tb, (int)pr.N, (int)pr.K, 1, br, nullptr, ldk, st.sm_count, stream);
+    e = launch_split_operand(pr.B, pr.ldb, 0, pr.tb, (int)pr.N, (int)pr.K, 1, br, nullptr, ldk, st.sm_count, stream,
+                             p->fault, p->bounds, p->b_elems);
   CUtensorMap ma, mb;
   if (e == cudaSuccess) e = encode_split_map(ar, pr.K, pr.M, ldk, 1, &ma);
   if (e == cudaSuccess) e = encode_split_map(br, pr.K, pr.N, ldk, 1, &mb);
@@ -588,10 +591,11 @@ cudaError_t launch_presplit(const Problem& pr, const sgemm_plan_t& plan, const D
   p->ws = slot_bytes > 0 ? reinterpret_cast<float*>(ws) : nullptr;
   // op(A) rows run along K when A is 'N'; op(B) rows (columns of op(B)) when B is 'T'
   cudaError_t e = launch_split_operand(pr.A, pr.lda, pr.stride_a, !pr.ta, (int)pr.M, (int)pr.K,
-                                       (int)l.a_products, ahi, alo, ldk, st.sm_count, stream);
+                                       (int)l.a_products, ahi, alo, ldk, st.sm_count, stream, p->fault, p->bounds,
+                                       p->a_elems);
   if (e == cudaSuccess)
     e = launch_split_operand(pr.B, pr.ldb, pr.stride_b, pr.tb, (int)pr.N, (int)pr.K, (int)l.b_products, bhi, blo,
-                             ldk, st.sm_count, stream);
+                             ldk, st.sm_count, stream, p->fault, p->bounds, p->b_elems);
   CUtensorMap mah, mal, mbh, mbl;
   if (e == cudaSuccess) e = encode_split_map(ahi, pr.K, pr.M, ldk, l.a_products, &mah);
   if (e == cudaSuccess) e = encode_split_map(alo, pr.K, pr.M, ldk, l.a_products, &mal);
@@ -629,6 +633,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   p.stride_c = pr.stride_c;
   p.timeout_ns = wait_timeout_ns();
   p.fault = st.fault;
+  set_extents(&p, plan.workspace_bytes, st.bounds);
 
   if (plan.variant == SGEMM_VARIANT_SCALE) {
     cudaError_t e = launch_scale(p, stream);
@@ -908,6 +913,8 @@ const char* sgemm_status_string(int status) {
     case SGEMM_ERR_UNSUPPORTED: return "SGEMM_ERR_UNSUPPORTED: dimension too large or no usable device";
     case SGEMM_ERR_SCRATCH_LIMIT:
       return "SGEMM_ERR_SCRATCH_LIMIT: split-K partial sums exceed sgemm_noalloc's static scratch array";
+    case SGEMM_ERR_BOUNDS:
+      return "SGEMM_ERR_BOUNDS: (debug build) a kernel index fell outside its buffer; the access was skipped";
     case -1: return "invalid argument 1 (transA)";
     case -2: return "invalid argument 2 (transB)";
     case -3: return "invalid argument 3 (M < 0)";
@@ -942,7 +949,44 @@ int sgemm_sync_status(struct CUstream_st* stream) {
   unsigned bits = 0;
   e = take_faults(&bits);
   if (e != cudaSuccess) return cuda_fail(e);
+  if (bits & kFaultBounds) return SGEMM_ERR_BOUNDS;
   return bits ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
+}
+
+int sgemm_bounds_report(unsigned* site, long long* offset) {
+  if (!site) return -1;
+  if (!offset) return -2;
+  unsigned long long w = 0;
+  cudaError_t e = take_bounds(&w);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *site = (unsigned)(w >> 48);
+  *offset = (long long)(w & ((1ull << 48) - 1));
+  return SGEMM_OK;
+}
+
+int sgemm_debug_bounds_enabled(void) {
+#ifdef SGEMM_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int sgemm_selftest_bounds(struct CUstream_st* stream) {
+  int dev;
+  DeviceState* st;
+  int s = device_state(&dev, &st);
+  if (s != SGEMM_OK) return s;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  unsigned bits = 0;
+  unsigned long long w = 0;
+  cudaError_t e = cudaStreamSynchronize(cs);
+  if (e == cudaSuccess) e = take_faults(&bits);
+  if (e == cudaSuccess) e = take_bounds(&w);
+  if (e == cudaSuccess) e = launch_bounds_selftest(st->fault, st->bounds, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return SGEMM_OK;
 }
 
 int sgemm_clock_snapshot(unsigned long long* out, int slots, struct CUstream_st* stream) {

@@ -14,7 +14,48 @@ enum FaultBits : unsigned {
   kFaultEmptyWait = 2u,    // producer gave up waiting for a free stage
   kFaultDrainWait = 4u,    // producer gave up waiting for its copies to land
   kFaultSelftest = 8u,     // the self-test wait gave up (expected)
+  kFaultBounds = 16u,      // debug build: an index fell outside its buffer (the access was skipped)
 };
+
+// ---- Bounds checks of the debug build (compiled with -DSGEMM_DEBUG_BOUNDS)
+//
+// The kernels pass every global-memory access (and the computed shared- and
+// tensor-memory offsets of the SIMT splitters) through in_range(): elements
+// [first, first + count) must lie in [0, limit) of their buffer.  In a debug
+// build a violation sets kFaultBounds in the fault word, keeps the first
+// violation's site and offset in the bounds word (site << 48 | offset), and the
+// caller skips the access -- nothing traps, nothing is read or written out of
+// bounds.  In the normal build in_range() is the constant true.
+enum BoundsSite : unsigned {
+  kSiteC = 1,        // C (epilogues, fixups, split-K reduction, scaling)
+  kSiteWs = 2,       // partial-sum workspace (stream-K slots, split-K slices)
+  kSiteA = 3,        // A (generic and small-product kernels, split pass, NaN repair)
+  kSiteB = 4,        // B
+  kSiteSplit = 5,    // split arrays written by the split pass
+  kSiteSmem = 6,     // shared-memory offsets of the splitters
+  kSiteTmem = 7,     // tensor-memory columns of the splitters
+  kSiteSelftest = 8  // the self-test's deliberate out-of-range index (never dereferenced)
+};
+
+#ifdef SGEMM_DEBUG_BOUNDS
+static __device__ __noinline__ bool bounds_violation(unsigned* fault, unsigned long long* word, unsigned site,
+                                              int64_t first) {
+  if (fault) atomicOr(fault, (unsigned)kFaultBounds);
+  if (word) {
+    const unsigned long long off = (unsigned long long)first & ((1ull << 48) - 1);
+    atomicCAS(word, 0ull, ((unsigned long long)site << 48) | off);
+  }
+  return false;
+}
+__device__ __forceinline__ bool in_range(unsigned* fault, unsigned long long* word, unsigned site, int64_t first,
+                                         int64_t count, int64_t limit) {
+  return (first >= 0 && count >= 0 && first <= limit - count) ? true : bounds_violation(fault, word, site, first);
+}
+#else
+__device__ __forceinline__ bool in_range(unsigned*, unsigned long long*, unsigned, int64_t, int64_t, int64_t) {
+  return true;
+}
+#endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -2,6 +2,7 @@
 // reduction with the fused alpha/beta epilogue, C = beta*C for alpha == 0 or
 // K == 0, the bounded-wait self-test, the per-SM clock snapshot, and the
 // device fault word.
+#include "bounds.cuh"
 #include "device_utils.cuh"
 #include "sgemm_internal.h"
 
@@ -10,6 +11,8 @@ namespace sgemm_impl {
 // One fault word per device (each device that loads the library has its own
 // copy of a __device__ variable).  Kernels receive its address in GemmParams.
 __device__ unsigned g_fault_word;
+// Debug build: the first bounds violation of the device (site << 48 | offset), 0 when none.
+__device__ unsigned long long g_bounds_word;
 
 namespace {
 
@@ -33,13 +36,18 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p, 
     const int64_t r = g - prod * per_product;
     const int row = (int)(r / groups);
     const int col = (int)(r % groups) * 4;
-    const float* w = p.ws + prod * split * slice + (int64_t)row * p.ws_ld + col;
-    float4 v = *reinterpret_cast<const float4*>(w);
-    for (int z = 1; z < split; ++z) {
+    const int64_t wi = prod * split * slice + (int64_t)row * p.ws_ld + col;
+    const float* w = p.ws + wi;
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int z = 0; z < split; ++z) {
+      if (!ws_ok(p, wi + z * slice, 4)) continue;
       const float4 u = *reinterpret_cast<const float4*>(w + z * slice);
-      v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+      if (z == 0) v = u;
+      else { v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w; }
     }
-    float* c = p.C + prod * p.stride_c + (int64_t)row * p.ldc + col;
+    const int64_t ci = prod * p.stride_c + (int64_t)row * p.ldc + col;
+    if (!c_ok(p, ci, min(4, p.N - col))) continue;
+    float* c = p.C + ci;
     if (CVEC && col + 3 < p.N) {
       float4 o;
       if (p.beta == 0.0f) {
@@ -67,7 +75,9 @@ __global__ void __launch_bounds__(256) scale_kernel(const GemmParams p) {
        e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t prod = e / per_product;
     const int64_t r = e - prod * per_product;
-    float* c = p.C + prod * p.stride_c + (r / p.N) * p.ldc + (r % p.N);
+    const int64_t ci = prod * p.stride_c + (r / p.N) * p.ldc + (r % p.N);
+    if (!c_ok(p, ci, 1)) continue;
+    float* c = p.C + ci;
     *c = p.beta == 0.0f ? 0.0f : p.beta * *c;
   }
 }
@@ -97,6 +107,12 @@ __global__ void clock_snapshot_kernel(unsigned long long* out, int slots) {
   const unsigned long long t = global_timer_ns();
   out[2 * smid] = (unsigned long long)clock64();
   out[2 * smid + 1] = t;
+}
+
+// Checks an index one past its limit: in the debug build the check records it and declines the
+// access (nothing is dereferenced); in the normal build there is no check and nothing happens.
+__global__ void bounds_selftest_kernel(unsigned* fault, unsigned long long* word) {
+  (void)in_range(fault, word, kSiteSelftest, 64, 1, 64);
 }
 
 unsigned grid_for(int64_t work, int per_block) {
@@ -132,8 +148,24 @@ cudaError_t launch_clock_snapshot(unsigned long long* out, int slots, int sm_cou
   return cudaGetLastError();
 }
 
+cudaError_t launch_bounds_selftest(unsigned* fault, unsigned long long* word, cudaStream_t stream) {
+  bounds_selftest_kernel<<<1, 1, 0, stream>>>(fault, word);
+  return cudaGetLastError();
+}
+
 cudaError_t fault_word(unsigned** ptr) {
   return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_fault_word);
+}
+
+cudaError_t bounds_word(unsigned long long** ptr) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_bounds_word);
+}
+
+cudaError_t take_bounds(unsigned long long* word) {
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_bounds_word, sizeof(unsigned long long));
+  if (e != cudaSuccess) return e;
+  const unsigned long long zero = 0;
+  return cudaMemcpyToSymbol(g_bounds_word, &zero, sizeof(unsigned long long));
 }
 
 cudaError_t take_faults(unsigned* bits) {

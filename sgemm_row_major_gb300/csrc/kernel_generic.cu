@@ -7,6 +7,7 @@
 // klklkl10086.github.io "Sgemm单精度矩阵乘法" (更优雅的实现): elements outside
 // op(A) or op(B) load as 0, so ragged M, N and K need no special case in the
 // inner loop, and only in-range elements of C are written.
+#include "bounds.cuh"
 #include "device_utils.cuh"
 #include "sgemm_internal.h"
 
@@ -49,14 +50,14 @@ __global__ void __launch_bounds__(GTHREADS) generic_gemm_kernel(const GemmParams
       if (!TA) { kk = tid & 15; mm = (tid >> 4) + 16 * r; }   // consecutive threads walk k
       else     { mm = tid & 63; kk = (tid >> 6) + 4 * r; }    // consecutive threads walk m
       const int gm = m0 + mm, gk = k0 + kk;
-      ra[r] = (gm < p.M && gk < p.K)
-                  ? (TA ? Ab[(int64_t)gk * p.lda + gm] : Ab[(int64_t)gm * p.lda + gk]) : 0.0f;
+      const int64_t ai = TA ? (int64_t)gk * p.lda + gm : (int64_t)gm * p.lda + gk;
+      ra[r] = (gm < p.M && gk < p.K && a_ok(p, (int64_t)prod * p.stride_a + ai, 1)) ? Ab[ai] : 0.0f;
       int nn;
       if (!TB) { nn = tid & 63; kk = (tid >> 6) + 4 * r; }
       else     { kk = tid & 15; nn = (tid >> 4) + 16 * r; }
       const int gn = n0 + nn, gk2 = k0 + kk;
-      rb[r] = (gn < p.N && gk2 < p.K)
-                  ? (TB ? Bb[(int64_t)gn * p.ldb + gk2] : Bb[(int64_t)gk2 * p.ldb + gn]) : 0.0f;
+      const int64_t bi = TB ? (int64_t)gn * p.ldb + gk2 : (int64_t)gk2 * p.ldb + gn;
+      rb[r] = (gn < p.N && gk2 < p.K && b_ok(p, (int64_t)prod * p.stride_b + bi, 1)) ? Bb[bi] : 0.0f;
     }
   };
   auto store = [&](int buf) {
@@ -118,10 +119,11 @@ __global__ void __launch_bounds__(GTHREADS) generic_gemm_kernel(const GemmParams
       if (col >= p.N) continue;
       const float v = mst[i][j] + acc[i][j];
       if (SPLIT) {
-        p.ws[(((int64_t)prod * gridDim.y + blockIdx.y) * p.M + row) * p.ws_ld + col] = v;
+        const int64_t wi = (((int64_t)prod * gridDim.y + blockIdx.y) * p.M + row) * p.ws_ld + col;
+        if (ws_ok(p, wi, 1)) p.ws[wi] = v;
       } else {
-        float* c = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
-        *c = epilogue(p.alpha, p.beta, v, c);
+        const int64_t ci = (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
+        if (c_ok(p, ci, 1)) p.C[ci] = epilogue(p.alpha, p.beta, v, p.C + ci);
       }
     }
   }

@@ -66,17 +66,33 @@ __device__ __forceinline__ float keep_nan(float x, float hi) { return x != x ? _
 // VEC -- every source row 16-byte aligned -- else four 4-byte loads; K % 4 == 0 is not
 // required: the tail is scalar).  lo == nullptr: only hi is written (the rounding pass of the
 // TF32-input GEMM).
+// (Chk: the bounds checks of the debug build on the source (extent src_elems) and on the split
+// arrays (products * rows * ldk elements each).)
+struct SplitChk {
+  unsigned* fault;
+  unsigned long long* word;
+  int64_t src_elems, dst_elems;
+  __device__ __forceinline__ bool src(int64_t off, int64_t n) const {
+    return in_range(fault, word, kSiteA, off, n, src_elems);
+  }
+  __device__ __forceinline__ bool dst(int64_t off, int64_t n) const {
+    return in_range(fault, word, kSiteSplit, off, n, dst_elems);
+  }
+};
+
 template <bool VEC>
 __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict__ src, int64_t ld, int64_t stride,
                                                          int rows, int K, int products, float* __restrict__ hi,
-                                                         float* __restrict__ lo, int64_t ldk) {
+                                                         float* __restrict__ lo, int64_t ldk, const SplitChk chk) {
   const int k4n = (K + 3) / 4;
   const int64_t total = (int64_t)products * rows * k4n;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int k4 = (int)(i % k4n);
     const int64_t pr = i / k4n;  // product * rows + row
     const int64_t p = pr / rows, r = pr - p * rows;
-    const float* s = src + p * stride + r * ld + 4 * k4;
+    const int64_t so = p * stride + r * ld + 4 * k4;
+    if (!chk.src(so, min(4, K - 4 * k4)) || !chk.dst(pr * ldk + 4 * k4, 4)) continue;
+    const float* s = src + so;
     float* h = hi + pr * ldk + 4 * k4;
     if (4 * k4 + 3 < K) {
       const float4 x = VEC ? *reinterpret_cast<const float4*>(s) : make_float4(s[0], s[1], s[2], s[3]);
@@ -104,7 +120,7 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict
 __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __restrict__ src, int64_t ld,
                                                               int64_t stride, int rows, int K,
                                                               float* __restrict__ hi, float* __restrict__ lo,
-                                                              int64_t ldk) {
+                                                              int64_t ldk, const SplitChk chk) {
   __shared__ float tile[kSplitTile][kSplitTile + 1];
   const int p = (int)blockIdx.z;
   const int r0 = (int)blockIdx.x * kSplitTile, k0 = (int)blockIdx.y * kSplitTile;
@@ -112,7 +128,9 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __res
   // read: stored row k = k0 + ty + 8j, element r = r0 + tx
   for (int j = 0; j < kSplitTile; j += 8) {
     const int k = k0 + (int)threadIdx.y + j, r = r0 + (int)threadIdx.x;
-    tile[threadIdx.y + j][threadIdx.x] = (k < K && r < rows) ? s[(int64_t)k * ld + r] : 0.0f;
+    const int64_t so = (int64_t)k * ld + r;
+    tile[threadIdx.y + j][threadIdx.x] =
+        (k < K && r < rows && chk.src((int64_t)p * stride + so, 1)) ? s[so] : 0.0f;
   }
   __syncthreads();
   // write: row r = r0 + ty + 8j, k = k0 + tx
@@ -120,7 +138,7 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __res
   float* l = lo ? lo + (int64_t)p * rows * ldk : nullptr;
   for (int j = 0; j < kSplitTile; j += 8) {
     const int r = r0 + (int)threadIdx.y + j, k = k0 + (int)threadIdx.x;
-    if (r < rows && k < K) {
+    if (r < rows && k < K && chk.dst(((int64_t)p * rows + r) * ldk + k, 1)) {
       const float x = tile[threadIdx.x][threadIdx.y + j];
       float xh, xl;
       split_one(x, xh, xl);
@@ -196,11 +214,13 @@ __device__ __forceinline__ void pair_tile_origin(const GemmParams& p, int tile, 
 // Tensor maps: the split operands as {K, rows, products} with boxes {32, 128, 1}, 128-byte
 // swizzle; za / zb in GemmParams say whether the third coordinate is the product index.
 template <bool CVEC>
-__device__ __forceinline__ void store_row(const GemmParams& p, float* crow, int c0, const float2 (&m)[kFoldCols / 2]) {
+__device__ __forceinline__ void store_row(const GemmParams& p, int64_t roff, int c0, const float2 (&m)[kFoldCols / 2]) {
+  float* crow = p.C + roff;
 #pragma unroll
   for (int e = 0; e < kFoldCols / 4; ++e) {
     const int col = c0 + 4 * e;
     const float x[4] = {m[2 * e].x, m[2 * e].y, m[2 * e + 1].x, m[2 * e + 1].y};
+    if (col >= p.N || !c_ok(p, roff + col, min(4, p.N - col))) continue;
     if (CVEC && col + 3 < p.N) {
       float4 o;
       if (p.beta == 0.0f) {
@@ -415,20 +435,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // epilogue: this thread holds row 32q + lane of the CTA's 128 rows, columns 128*half .. +127
       const Segment g = cta_segment(p, work_s, cl, sgi, kt_total);
       if (g.slot >= 0) {
-        float* w = p.ws + (int64_t)(2 * g.slot + (int)rank) * (BMC * BN) + (32 * q + lane) * BN + kFoldCols * half;
+        const int64_t woff =
+            (int64_t)(2 * g.slot + (int)rank) * (BMC * BN) + (32 * q + lane) * BN + kFoldCols * half;
+        float* w = p.ws + woff;
 #pragma unroll
         for (int e = 0; e < kFoldCols / 4; ++e)
-          *reinterpret_cast<float4*>(w + 4 * e) =
-              make_float4(master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y);
+          if (ws_ok(p, woff + 4 * e, 4))
+            *reinterpret_cast<float4*>(w + 4 * e) =
+                make_float4(master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y);
       } else {
         int prod, m0, n0;
         pair_tile_origin(p, g.tile, prod, m0, n0);
         const int row = m0 + BMC * (int)rank + 32 * q + lane;
         if (row < p.M) {
           if (PARTS == 2) repair_nans(p, prod, row, n0 + kFoldCols * half, master2);
-          float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
-          if (p.c_vec) store_row<true>(p, crow, n0 + kFoldCols * half, master2);
-          else         store_row<false>(p, crow, n0 + kFoldCols * half, master2);
+          const int64_t roff = (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
+          if (p.c_vec) store_row<true>(p, roff, n0 + kFoldCols * half, master2);
+          else         store_row<false>(p, roff, n0 + kFoldCols * half, master2);
         }
       }
 #pragma unroll
@@ -488,14 +511,18 @@ __global__ void __launch_bounds__(kFixupThreads) presplit_fixup_kernel(const Gem
     const int col = n0 + cc;
     if (col >= p.N) continue;
     const float* w = p.ws + rr * BN + cc;
-    float4 v = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[0] * (BMC * BN));
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 4
-    for (int i = 1; i < n; ++i) {
+    for (int i = 0; i < n; ++i) {
+      if (!ws_ok(p, rr * BN + cc + (int64_t)s_slot[i] * (BMC * BN), 4)) continue;
       const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[i] * (BMC * BN));
-      v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+      if (i == 0) v = u;
+      else { v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w; }
     }
     if (p.repair) repair_nans4(p, prod, row, col, v);
-    float* cp = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
+    const int64_t coff = (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
+    if (!c_ok(p, coff, min(4, p.N - col))) continue;
+    float* cp = p.C + coff;
     if (CVEC && col + 3 < p.N) {
       float4 o;
       if (p.beta == 0.0f) {
@@ -526,22 +553,23 @@ cudaError_t prepare_presplit() {
 }
 
 cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, bool k_contig, int rows, int K,
-                                 int products, float* hi, float* lo, int64_t ldk, int sm_count,
-                                 cudaStream_t stream) {
+                                 int products, float* hi, float* lo, int64_t ldk, int sm_count, cudaStream_t stream,
+                                 unsigned* fault, unsigned long long* bounds, int64_t src_elems) {
   if (rows <= 0 || K <= 0 || products <= 0) return cudaSuccess;
+  const tps::SplitChk chk{fault, bounds, src_elems, (int64_t)products * rows * ldk};
   if (k_contig) {
     const int64_t work = (int64_t)products * rows * ((K + 3) / 4);
     const unsigned blocks = (unsigned)std::max<int64_t>(std::min<int64_t>((work + 255) / 256, (int64_t)sm_count * 8), 1);
     const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && ld % 4 == 0 && (products == 1 || stride % 4 == 0);
     if (vec)
-      tps::split_rows_kernel<true><<<blocks, 256, 0, stream>>>(src, ld, stride, rows, K, products, hi, lo, ldk);
+      tps::split_rows_kernel<true><<<blocks, 256, 0, stream>>>(src, ld, stride, rows, K, products, hi, lo, ldk, chk);
     else
-      tps::split_rows_kernel<false><<<blocks, 256, 0, stream>>>(src, ld, stride, rows, K, products, hi, lo, ldk);
+      tps::split_rows_kernel<false><<<blocks, 256, 0, stream>>>(src, ld, stride, rows, K, products, hi, lo, ldk, chk);
   } else {
     const dim3 grid((unsigned)((rows + tps::kSplitTile - 1) / tps::kSplitTile),
                     (unsigned)((K + tps::kSplitTile - 1) / tps::kSplitTile), (unsigned)products);
     tps::split_transpose_kernel<<<grid, dim3(tps::kSplitTile, 8), 0, stream>>>(src, ld, stride, rows, K, hi, lo,
-                                                                               ldk);
+                                                                               ldk, chk);
   }
   return cudaGetLastError();
 }

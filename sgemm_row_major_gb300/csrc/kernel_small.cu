@@ -31,6 +31,7 @@
 // op(B) 'N'.  Groups outside the matrix are zero-filled, never read.
 #include <cstdint>
 
+#include "bounds.cuh"
 #include "kernel_small.h"
 
 namespace sgemm_impl {
@@ -61,15 +62,17 @@ __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cas
 
 // One operand chunk stored K-contiguous: 64 rows (matrix rows 0..63, valid
 // below `rows`) of 8 groups (columns k0 + 4g, valid below K), swizzled.
+// (chk: the bounds check of the debug build on the operand, `off` the chunk base's element offset)
+template <class Chk>
 __device__ __forceinline__ void copy_k_rows(float* dst, const float* base, int64_t ld, int rows, int k0, int K,
-                                            int tid) {
+                                            int tid, const Chk& chk, int64_t off) {
   const uint32_t d0 = smem_addr(dst);
 #pragma unroll
   for (int q = 0; q < SM_CHUNK_FLOATS / 4 / SM_THREADS; ++q) {
     const int e = tid + SM_THREADS * q;  // 0 .. 511
     const int r = e >> 3, g = e & 7;
     const int col = k0 + 4 * g;
-    const bool ok = r < rows && col < K;
+    const bool ok = r < rows && col < K && chk(off + (int64_t)r * ld + col, 4);
     cp_async16(d0 + (uint32_t)((r * SM_KC + 4 * (g ^ (r & 7))) * 4), ok ? base + (int64_t)r * ld + col : base,
                ok ? 16 : 0);
   }
@@ -77,15 +80,16 @@ __device__ __forceinline__ void copy_k_rows(float* dst, const float* base, int64
 
 // One operand chunk stored M/N-contiguous: 32 rows (matrix rows k0 .. k0+31,
 // valid below K) of 16 groups (columns 4g, valid below `cols`), unswizzled.
+template <class Chk>
 __device__ __forceinline__ void copy_mn_rows(float* dst, const float* base, int64_t ld, int cols, int k0, int K,
-                                             int tid) {
+                                             int tid, const Chk& chk, int64_t off) {
   const uint32_t d0 = smem_addr(dst);
 #pragma unroll
   for (int q = 0; q < SM_CHUNK_FLOATS / 4 / SM_THREADS; ++q) {
     const int e = tid + SM_THREADS * q;
     const int r = e >> 4, g = e & 15;
     const int row = k0 + r;
-    const bool ok = row < K && 4 * g < cols;
+    const bool ok = row < K && 4 * g < cols && chk(off + (int64_t)row * ld + 4 * g, 4);
     cp_async16(d0 + (uint32_t)((r * SM_T + 4 * g) * 4), ok ? base + (int64_t)row * ld + 4 * g : base, ok ? 16 : 0);
   }
 }
@@ -167,10 +171,12 @@ __global__ void __launch_bounds__(SM_THREADS, SM_CTAS) small_gemm_kernel(const G
     float* st = smem + (item & 1) * SM_STAGE_FLOATS;
     const float* A = p.A + prod * p.stride_a;
     const float* B = p.B + prod * p.stride_b;
-    if (!TA) copy_k_rows(st, A, p.lda, p.M, k0, p.K, tid);
-    else copy_mn_rows(st, A, p.lda, p.M, k0, p.K, tid);
-    if (!TB) copy_mn_rows(st + SM_CHUNK_FLOATS, B, p.ldb, p.N, k0, p.K, tid);
-    else copy_k_rows(st + SM_CHUNK_FLOATS, B, p.ldb, p.N, k0, p.K, tid);
+    const auto achk = [&](int64_t o, int64_t n) { return a_ok(p, o, n); };
+    const auto bchk = [&](int64_t o, int64_t n) { return b_ok(p, o, n); };
+    if (!TA) copy_k_rows(st, A, p.lda, p.M, k0, p.K, tid, achk, prod * p.stride_a);
+    else copy_mn_rows(st, A, p.lda, p.M, k0, p.K, tid, achk, prod * p.stride_a);
+    if (!TB) copy_mn_rows(st + SM_CHUNK_FLOATS, B, p.ldb, p.N, k0, p.K, tid, bchk, prod * p.stride_b);
+    else copy_k_rows(st + SM_CHUNK_FLOATS, B, p.ldb, p.N, k0, p.K, tid, bchk, prod * p.stride_b);
   };
 
   // per-thread float offsets of the M/N-contiguous fragments (first column of 4) and of the
@@ -215,6 +221,7 @@ __global__ void __launch_bounds__(SM_THREADS, SM_CTAS) small_gemm_kernel(const G
       for (int i = 0; i < 8; ++i) {
         const int row = row_of<TA>(i, wm, ty);
         if (row < p.M) {
+          const int64_t roff = prod * p.stride_c + (int64_t)row * p.ldc;
           float* crow = Cp + (int64_t)row * p.ldc;
           const float v[8] = {acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y,
                               acc[i][2].x, acc[i][2].y, acc[i][3].x, acc[i][3].y};
@@ -223,6 +230,7 @@ __global__ void __launch_bounds__(SM_THREADS, SM_CTAS) small_gemm_kernel(const G
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int col = 32 * h + 4 * tx;
+              if (col >= p.N || !c_ok(p, roff + col, min(4, p.N - col))) continue;
               if (p.c_vec && col + 3 < p.N) {
                 float4* cp = reinterpret_cast<float4*>(crow + col);
                 if (p.beta == 0.0f) {
@@ -247,7 +255,7 @@ __global__ void __launch_bounds__(SM_THREADS, SM_CTAS) small_gemm_kernel(const G
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int col = tx + 8 * j;
-              if (col < p.N)
+              if (col < p.N && c_ok(p, roff + col, 1))
                 crow[col] = p.beta == 0.0f ? p.alpha * v[j] : fmaf(p.alpha, v[j], p.beta * crow[col]);
             }
           }

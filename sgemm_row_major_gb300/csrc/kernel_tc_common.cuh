@@ -7,6 +7,7 @@
 // the CTA-pair kernels.
 #pragma once
 
+#include "bounds.cuh"
 #include "device_utils.cuh"
 #include "sgemm_internal.h"
 
@@ -105,14 +106,17 @@ __device__ __forceinline__ bool any_nonfinite(const float2 (&m)[N2]) {
 // `prod`, i < n) by the FP32 dot product of op(A)'s row and op(B)'s column.
 // v is a local array: only this cold path indexes it at run time.
 __device__ __forceinline__ void repair_row(const GemmParams& p, int prod, int row, int col0, float* v, int n) {
-  const float* a = p.A + (int64_t)prod * p.stride_a + (p.ta ? (int64_t)row : (int64_t)row * p.lda);
-  const float* b0 = p.B + (int64_t)prod * p.stride_b;
+  const int64_t aoff = (int64_t)prod * p.stride_a + (p.ta ? (int64_t)row : (int64_t)row * p.lda);
   const int64_t as = p.ta ? p.lda : 1, bs = p.tb ? 1 : p.ldb;
+  if (!a_ok(p, aoff, 1) || !a_ok(p, aoff + (int64_t)(p.K - 1) * as, 1)) return;
+  const float* a = p.A + aoff;
 #pragma unroll 1
   for (int i = 0; i < n; ++i) {
     const int col = col0 + i;
-    if (v[i] != v[i] && col < p.N)
-      v[i] = fp32_dot(a, as, b0 + (p.tb ? (int64_t)col * p.ldb : (int64_t)col), bs, p.K);
+    if (v[i] != v[i] && col < p.N) {
+      const int64_t boff = (int64_t)prod * p.stride_b + (p.tb ? (int64_t)col * p.ldb : (int64_t)col);
+      if (b_ok(p, boff, 1) && b_ok(p, boff + (int64_t)(p.K - 1) * bs, 1)) v[i] = fp32_dot(a, as, p.B + boff, bs, p.K);
+    }
   }
 }
 

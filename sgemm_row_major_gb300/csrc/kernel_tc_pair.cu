@@ -247,6 +247,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int st = threadIdx.x - 64;                 // 0..255
     const int q = warp & 3;                          // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;                // which 16 k of the tile (st >> 7)
+    // Debug build: the largest shared- and tensor-memory offsets this thread uses lie inside
+    // their tiles; otherwise its loads and stores are skipped.
+    const bool lay_ok = [&] {
+      const int m = 32 * q + lane, n = st & 63;
+      const int a_max = TA ? (16 * half + 15) * BMC + m : (m * 128 + 128) / 4 - 1;
+      const int b_max = !TB ? 31 * BNC + n : (n * 128 + 128) / 4 - 1;
+      return local_ok(p, kSiteSmem, a_max, 1, kATileBytes / 4) && local_ok(p, kSiteSmem, b_max, 1, kBTileBytes / 4) &&
+             local_ok(p, kSiteSmem, n * 128, 128, kBTileBytes) &&
+             local_ok(p, kSiteTmem, kAColBase + (kSplitStages - 1) * kACols + 16 * half + 32, 16, kTmemCols);
+    }();
     int t = 0;
     for (; t < nkt; ++t) {
       const int r = t % kRawStages, s = t % kSplitStages;
@@ -258,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // loads and the split arithmetic stay off the loop MMA completion -> split stage -> MMA.
       // A: this thread takes row m = 32q + lane (its TMEM lane) and k = 16*half .. +15.
       float hi[16], lo[16];
-      {
+      if (lay_ok) {
         const uint8_t* ra = smem + (raw_a(r) - sbase);
         const int m = 32 * q + lane;
         if (!TA) {
@@ -287,7 +297,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // takes column n = st % 64 and the two 4-k chunks 4*half + 2*((st / 64) % 2) + {0, 1}.
       const int n = st & 63, kp = (st >> 6) & 1;
       float4 bh[2], bl[2];
-      if (!TB) {
+      if (!lay_ok) {
+      } else if (!TB) {
         // raw [32 k][64 n]: transpose on the way (a warp reads 32 adjacent n of one k)
         const float* rb = reinterpret_cast<const float*>(smem + (raw_b(r) - sbase));
 #pragma unroll
@@ -313,7 +324,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       tmem_fence_after_sync();
-      {
+      if (lay_ok) {
         const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kAColBase + (uint32_t)s * kACols + 16u * half;
         tmem_st16(ta, hi);
         tmem_st16(ta + 32u, lo);
@@ -391,11 +402,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const Segment g = cta_segment(p, work_s, cl, sgi, kt_total);
       if (g.slot >= 0) {
         // partial sums of a shared stream-K tile -> this CTA's slot (whole 128 x 128, no bounds)
-        float* w = p.ws + (int64_t)(2 * g.slot + (int)rank) * (BMC * BN) + (32 * q + lane) * BN + 64 * half;
+        const int64_t woff = (int64_t)(2 * g.slot + (int)rank) * (BMC * BN) + (32 * q + lane) * BN + 64 * half;
+        float* w = p.ws + woff;
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          *reinterpret_cast<float4*>(w + 4 * e) =
-              make_float4(master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y);
+          if (ws_ok(p, woff + 4 * e, 4))
+            *reinterpret_cast<float4*>(w + 4 * e) =
+                make_float4(master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y);
       } else {
         int prod, m0, n0;
         pair_tile_origin(p, g.tile, prod, m0, n0);
@@ -403,11 +416,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int c0 = n0 + 64 * half;
         if (row < p.M) {
           repair_nans(p, prod, row, c0, master2);
-          float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
+          const int64_t roff = (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
+          float* crow = p.C + roff;
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int col = c0 + 4 * e;
             const float x[4] = {master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y};
+            if (col >= p.N || !c_ok(p, roff + col, min(4, p.N - col))) continue;
             if (p.c_vec && col + 3 < p.N) {
               float4 o;
               if (p.beta == 0.0f) {
@@ -482,14 +497,18 @@ __global__ void __launch_bounds__(kFixupThreads) pair_fixup_kernel(const GemmPar
   const int row = m0 + BMC * r + rr, col = n0 + cc;
   if (row >= p.M || col >= p.N) return;
   const float* w = p.ws + rr * BN + cc;
-  float4 v = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[0] * (BMC * BN));
+  float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 4
-  for (int i = 1; i < n; ++i) {
+  for (int i = 0; i < n; ++i) {
+    if (!ws_ok(p, rr * BN + cc + (int64_t)s_slot[i] * (BMC * BN), 4)) continue;
     const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[i] * (BMC * BN));
-    v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+    if (i == 0) v = u;
+    else { v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w; }
   }
   repair_nans4(p, prod, row, col, v);
-  float* cp = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
+  const int64_t coff = (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
+  if (!c_ok(p, coff, min(4, p.N - col))) return;
+  float* cp = p.C + coff;
   if (CVEC && col + 3 < p.N) {
     float4 o;
     if (p.beta == 0.0f) {

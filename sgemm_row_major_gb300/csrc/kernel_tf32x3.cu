@@ -318,6 +318,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int st = threadIdx.x - 64;                 // 0..255
     const int q = warp & 3;                          // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;                // which 16 k of A
+    // Debug build: the largest shared- and tensor-memory offsets this thread uses (they do not
+    // depend on the K tile) lie inside their tiles; otherwise its loads and stores are skipped.
+    const bool lay_ok = [&] {
+      const int m = 32 * q + lane, n = st & 127;
+      constexpr int lda_s = BM / G, ldb_s = BN / G;
+      const int a_max = TA ? (G > 1 ? (m / lda_s) * (BK * lda_s) : 0) + (16 * half + 15) * lda_s + (G > 1 ? m % lda_s : m)
+                           : (m * 128 + 128) / 4 - 1;
+      const int b_max = !TB ? (G > 1 ? (n / ldb_s) * (BK * ldb_s) : 0) + 31 * ldb_s + (G > 1 ? n % ldb_s : n)
+                            : (n * 128 + 128) / 4 - 1;
+      return local_ok(p, kSiteSmem, a_max, 1, kTileBytes / 4) && local_ok(p, kSiteSmem, b_max, 1, kTileBytes / 4) &&
+             local_ok(p, kSiteSmem, n * 128, 128, kTileBytes) &&
+             local_ok(p, kSiteTmem, kAColBase + (kSplitStages - 1) * kACols + 16 * half + 32, 16, kTmemCols);
+    }();
     for (int t = 0; t < nkt; ++t) {
       const int r = t % kRawStages, s = t % kSplitStages;
       bool w = warp_wait(smem_addr(&raw_full[r]), (uint32_t)(t / kRawStages) & 1u, p.timeout_ns);
@@ -329,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_fence_after_sync();
       // A: this thread takes row m = 32q + lane (its TMEM lane) and k = 16*half .. +15.
-      {
+      if (lay_ok) {
         const uint8_t* ra = smem + (raw_a(r) - sbase);
         const int m = 32 * q + lane;
         float hi[16], lo[16];
@@ -363,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // B -> K-major [128 n][32 k], 128-byte swizzle, the layout the descriptors describe;
       // this group writes the 16 k of its half (st / 128 == half).
-      {
+      if (lay_ok) {
         uint8_t* bhi = smem + (split_tile(s, 0) - sbase);
         uint8_t* blo = smem + (split_tile(s, 1) - sbase);
         if (!TB) {
@@ -463,11 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Segment g = cta_segment(p, work_s, cta, sgi, kt_total);
       if (g.slot >= 0) {
         // partial sums of a shared stream-K tile -> this CTA's slot (whole 128 x 128, no bounds)
-        float* w = p.ws + (int64_t)g.slot * (BM * BN) + (32 * q + lane) * BN + 64 * half;
+        const int64_t woff = (int64_t)g.slot * (BM * BN) + (32 * q + lane) * BN + 64 * half;
+        float* w = p.ws + woff;
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          *reinterpret_cast<float4*>(w + 4 * e) =
-              make_float4(master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y);
+          if (ws_ok(p, woff + 4 * e, 4))
+            *reinterpret_cast<float4*>(w + 4 * e) =
+                make_float4(master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y);
       } else {
         int prod, m0, c0;  // product, origin row of the tile in it, first column of this thread's
         if (G > 1) {
@@ -482,11 +497,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = m0 + 32 * q + lane;
         if (row < p.M && (G == 1 || prod < p.batch)) {
           repair_nans(p, prod, row, c0, master2);
-          float* crow = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
+          const int64_t roff = (int64_t)prod * p.stride_c + (int64_t)row * p.ldc;
+          float* crow = p.C + roff;
 #pragma unroll
           for (int e = 0; e < kCols / 4; ++e) {
             const int col = c0 + 4 * e;
             const float x[4] = {master2[2 * e].x, master2[2 * e].y, master2[2 * e + 1].x, master2[2 * e + 1].y};
+            if (col >= p.N || !c_ok(p, roff + col, min(4, p.N - col))) continue;
             if (p.c_vec && col + 3 < p.N) {
               float4 o;
               if (p.beta == 0.0f) {
@@ -554,14 +571,18 @@ __global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(const Gemm
   const int row = m0 + r, col = n0 + cc;
   if (row >= p.M || col >= p.N) return;
   const float* w = p.ws + r * BN + cc;
-  float4 v = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[0] * (BM * BN));
+  float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 4
-  for (int i = 1; i < n; ++i) {
+  for (int i = 0; i < n; ++i) {
+    if (!ws_ok(p, r * BN + cc + (int64_t)s_slot[i] * (BM * BN), 4)) continue;
     const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[i] * (BM * BN));
-    v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+    if (i == 0) v = u;
+    else { v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w; }
   }
   repair_nans4(p, prod, row, col, v);
-  float* cp = p.C + (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
+  const int64_t coff = (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
+  if (!c_ok(p, coff, min(4, p.N - col))) return;
+  float* cp = p.C + coff;
   if (CVEC && col + 3 < p.N) {
     float4 o;
     if (p.beta == 0.0f) {

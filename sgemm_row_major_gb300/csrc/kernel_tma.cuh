@@ -43,6 +43,7 @@
 // along its contiguous axis instead.
 #pragma once
 
+#include "bounds.cuh"
 #include "device_utils.cuh"
 #include "sgemm_internal.h"
 
@@ -208,11 +209,12 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, float* cm, float* 
         if (SPLIT) {
           if (col < p.N) {
             float* w = wm_base + (int64_t)row * p.ws_ld + col;
-            *reinterpret_cast<float4*>(w) = make_float4(x[0], x[1], x[2], x[3]);
+            if (ws_ok(p, w - p.ws, 4)) *reinterpret_cast<float4*>(w) = make_float4(x[0], x[1], x[2], x[3]);
           }
           continue;
         }
         float* c = cm + (int64_t)row * p.ldc + col;
+        if (col >= p.N || !c_ok(p, c - p.C, min(4, p.N - col))) continue;
         if (p.c_vec && col + 3 < p.N) {
           float4 o;
           if (p.beta == 0.0f) {
@@ -236,10 +238,11 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, float* cm, float* 
         if (col >= p.N) continue;
         const float x = v[8 * i + j];
         if (SPLIT) {
-          wm_base[(int64_t)row * p.ws_ld + col] = x;
+          float* w = wm_base + (int64_t)row * p.ws_ld + col;
+          if (ws_ok(p, w - p.ws, 1)) *w = x;
         } else {
           float* c = cm + (int64_t)row * p.ldc + col;
-          *c = p.beta == 0.0f ? p.alpha * x : fmaf(p.alpha, x, p.beta * *c);
+          if (c_ok(p, c - p.C, 1)) *c = p.beta == 0.0f ? p.alpha * x : fmaf(p.alpha, x, p.beta * *c);
         }
       }
     }

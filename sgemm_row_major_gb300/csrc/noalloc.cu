@@ -46,6 +46,7 @@ struct NoallocDevice {
   int sm_count = 0;
   int pair_clusters = 0;     // co-resident CTA-pair clusters (0: the CTA-pair kernel cannot run here)
   unsigned* fault = nullptr;
+  unsigned long long* bounds = nullptr;  // debug build: first bounds violation
   float* scratch = nullptr;  // device address of g_noalloc_scratch on this device
 };
 NoallocDevice g_nd[kMaxDevices];
@@ -62,6 +63,7 @@ cudaError_t setup(int dev, NoallocDevice** out) {
   if (d.ready.load(std::memory_order_relaxed)) return cudaSuccess;
   cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = fault_word(&d.fault);
+  if (e == cudaSuccess) e = bounds_word(&d.bounds);
   if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.scratch), g_noalloc_scratch);
   if (e == cudaSuccess) e = prepare_tma_op_nn();
   if (e == cudaSuccess) e = prepare_tma_op_nt();
@@ -121,6 +123,7 @@ extern "C" int sgemm_noalloc(char transA, char transB, int64_t M, int64_t N, int
   p.c_vec = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0;
   p.timeout_ns = wait_timeout_ns();
   p.fault = nd->fault;
+  set_extents(&p, plan.workspace_bytes, nd->bounds);
 
   if (plan.variant == SGEMM_VARIANT_SCALE) {
     e = launch_scale(p, cs);

@@ -39,7 +39,30 @@ struct GemmParams {
   int repair = 1;                // tensor-core kernels: compute NaN sums again in FP32 (0: the TF32-input GEMM)
   uint64_t timeout_ns = 0;       // limit of every in-kernel wait
   unsigned* fault = nullptr;     // device fault word (bits of FaultBits), see fault_word()
+  // Extents (elements from the base pointer) of the buffers, for the bounds checks of the debug
+  // build (device_utils.cuh, in_range); the normal build does not read them.
+  int64_t a_elems = 0, b_elems = 0, c_elems = 0, ws_elems = 0;
+  unsigned long long* bounds = nullptr;  // debug build: first bounds violation (site << 48 | offset)
 };
+
+// Elements a row-major matrix of `rows` x `cols` (row stride ld) spans from its first element,
+// over `batch` matrices `stride` elements apart (0 when empty).
+inline int64_t matrix_extent(int64_t rows, int64_t cols, int64_t ld, int64_t batch, int64_t stride) {
+  if (rows <= 0 || cols <= 0 || batch <= 0) return 0;
+  return (batch - 1) * stride + (rows - 1) * ld + cols;
+}
+
+// Fills the extents of GemmParams from its own shape, op flags, leading dimensions, strides and
+// batch, and the workspace size; `bounds` is the device's bounds word (bounds_word()).
+inline void set_extents(GemmParams* p, int64_t ws_bytes, unsigned long long* bounds) {
+  p->a_elems = p->ta ? matrix_extent(p->K, p->M, p->lda, p->batch, p->stride_a)
+                     : matrix_extent(p->M, p->K, p->lda, p->batch, p->stride_a);
+  p->b_elems = p->tb ? matrix_extent(p->N, p->K, p->ldb, p->batch, p->stride_b)
+                     : matrix_extent(p->K, p->N, p->ldb, p->batch, p->stride_b);
+  p->c_elems = matrix_extent(p->M, p->N, p->ldc, p->batch, p->stride_c);
+  p->ws_elems = ws_bytes / 4;
+  p->bounds = bounds;
+}
 
 // Tensor maps of the operands of a TMA-fed kernel: 3-D {contiguous, rows,
 // product} float32 maps over the stored A and B, boxes of the kernel's tile
@@ -139,7 +162,9 @@ cudaError_t launch_pair_fixup(const GemmParams& p, int sk_tiles, cudaStream_t st
 // then the fixup over the sk_tiles stream-K pair tiles when any is shared.
 cudaError_t prepare_presplit();
 cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, bool k_contig, int rows, int K,
-                                 int products, float* hi, float* lo, int64_t ldk, int sm_count, cudaStream_t stream);
+                                 int products, float* hi, float* lo, int64_t ldk, int sm_count, cudaStream_t stream,
+                                 unsigned* fault = nullptr, unsigned long long* bounds = nullptr,
+                                 int64_t src_elems = 0);
 cudaError_t launch_presplit_gemm(const CUtensorMap& mapAh, const CUtensorMap& mapAl, const CUtensorMap& mapBh,
                                  const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
@@ -177,6 +202,12 @@ cudaError_t trim_host_pool(int dev, size_t keep_bytes);
 
 // Device address of the current device's fault word (looked up once per device).
 cudaError_t fault_word(unsigned** ptr);
+// Device address of the current device's bounds word (debug build: first bounds violation).
+cudaError_t bounds_word(unsigned long long** ptr);
+// Reads and clears the bounds word (synchronous).
+cudaError_t take_bounds(unsigned long long* word);
+// Launches the bounds self-test: one check of an index past its limit (never dereferenced).
+cudaError_t launch_bounds_selftest(unsigned* fault, unsigned long long* word, cudaStream_t stream);
 // Reads and clears the current device's fault word (synchronous).
 cudaError_t take_faults(unsigned* bits);
 

@@ -460,3 +460,16 @@ def test_tf32_planner(lib):
     with pytest.raises(sg.SgemmError) as ei:
         sg.sgemm_tf32_plan("N", "N", 64, 64, 32 * 65536, 1.0, FAKE, 32 * 65536, FAKE, 64, 0.0, FAKE, 64, 152)
     assert ei.value.status == sg.STATUS["ERR_UNSUPPORTED"]
+
+
+def test_debug_library_exports_every_declared_symbol():
+    """libsgemm_debug.so (the bounds-checking build) exports the same entry points and reports
+    itself; libsgemm.so has the checks compiled out."""
+    from sgemm_row_major_gb300 import build
+    build.build(debug=True)
+    dbg = sg.load_debug()
+    for name in declared_functions():
+        assert hasattr(dbg, name), f"libsgemm_debug.so does not export {name}"
+    assert dbg.sgemm_debug_bounds_enabled() == 1
+    assert sg.load().sgemm_debug_bounds_enabled() == 0
+    assert "SGEMM_ERR_BOUNDS" in sg.sgemm_status_string(sg.STATUS["ERR_BOUNDS"])
