@@ -194,6 +194,11 @@ def _one_cta_schedules():
     assert t["grid_x"] == 9 * 5 and t["sk_tiles"] == 9 and t["split_k"] >= 5
     q = plan("N", "N", 1000, 1300, 700)      # 88 tiles, 22 K tiles: one CTA per tile
     assert (q["grid_x"], q["split_k"], q["kernel_launches"], q["workspace_bytes"]) == (88, 1, 1, 0)
+    # at least 3/4 as many tiles as SMs: whole tiles, one CTA each, no stream-K (144 of 152)
+    h = plan("N", "N", 128 * 12, 128 * 12, 4096)
+    assert (h["grid_x"], h["dp_tiles"], h["sk_tiles"], h["kernel_launches"]) == (144, 144, 0, 1)
+    g = plan("N", "N", 128 * 12, 128 * 9, 4096)  # 108 tiles: below 3/4, stream-K
+    assert (g["dp_tiles"], g["sk_tiles"], g["kernel_launches"]) == (0, 108, 2)
     # one tile, one K tile: one CTA, no fixup
     o = plan("N", "N", 128, 128, 32)
     assert (o["grid_x"], o["kernel_launches"], o["workspace_bytes"]) == (1, 1, 0)
@@ -235,6 +240,10 @@ def test_split_operand_rule(lib):
     assert bplan("N", "N", 2048, 1024, 1024, 32, 2048 * 1024, 0, 2048 * 1024)["variant_name"] == "TC_PRESPLIT"
     # split arrays above 4 GiB (A and B 2 GiB each): CTA pairs
     assert plan("N", "N", 16384, 16384, 32768)["variant_name"] == "TC_PAIR"
+    # 2048^3: 64 tiles of 256 x 256 for 76 clusters, whole tiles (no stream-K slots)
+    w = plan("N", "N", 2048, 2048, 2048)
+    assert (w["variant_name"], w["grid_x"], w["dp_tiles"], w["sk_tiles"]) == ("TC_PRESPLIT", 128, 64, 0)
+    assert w["workspace_bytes"] == 4 * 2048 * 2048 * 4
     # workspace: stream-K slots of 128 x 256 floats per CTA, then hi and lo of A and B
     p = plan("N", "N", 8192, 4096, 1024)
     slots = 2 * 152 * 128 * 256 * 4 if p["split_k"] > 1 else 0
