@@ -414,6 +414,8 @@ KERNEL_NAMES = {
     "TC_PRESPLIT": "presplit_gemm_kernel (tcgen05.mma cta_group::2 kind::tf32, both operands from shared memory, "
                    "256x256 tiles on CTA pairs) after split_rows/split_transpose (A and B split once into TF32 hi "
                    "and FP32 lo)",
+    "TC_SKINNY": "skinny_gemm_kernel (tcgen05.mma kind::tf32 N=64, 3xTF32 split, 128 x 64 tiles along the long x "
+                 "short side) after split_rows/split_transpose of the short operand",
 }
 
 
@@ -427,6 +429,8 @@ def kernel_digest(lib_build, variant):
         return lib_build.tc_kernel_digest()
     if variant == "SMALL":
         return lib_build.small_kernel_digest()
+    if variant == "TC_SKINNY":
+        return lib_build.skinny_kernel_digest()
     return lib_build.tma_kernel_digest()
 
 
@@ -444,8 +448,10 @@ def tensor_roofline(achieved, peaks, traffic, kernel_ms, variant="TC_TF32X3"):
             "kernel": KERNEL_NAMES.get(variant, KERNEL_NAMES["TC_TF32X3"]), "kernel_ms": kernel_ms,
             "kernel_ms_covers": ("one sgemm() call: the split passes of A and B, the GEMM kernel and, when "
                                  "stream-K tiles are shared, the fixup kernel" if variant == "TC_PRESPLIT" else
+                                 "one sgemm() call: the split pass of the short operand, the GEMM kernel and, "
+                                 "when stream-K tiles are shared, the fixup kernel" if variant == "TC_SKINNY" else
                                  "one sgemm() call: the GEMM kernel and, when stream-K tiles are shared, "
-                                 "the fixup kernel after it (about 2% of the step in the ncu launch list)")}
+                                 "the fixup kernel after it")}
 
 
 def hbm_bound_roofline(roof, nbytes, flops_step, kernel_ms, peaks):
@@ -549,7 +555,7 @@ def run_ours(args):
     max_mhz = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
     ffma_peak = sms * FMA_PER_SM_PER_CLK * 2 * max_mhz * 1e6 / 1e12
     variant = plan["variant_name"]
-    if variant in ("TC_TF32X3", "TC_PAIR", "TC_PRESPLIT"):
+    if variant in ("TC_TF32X3", "TC_PAIR", "TC_PRESPLIT", "TC_SKINNY"):
         roof = tensor_roofline(achieved, peaks,
                                traffic_from_profile(variant, case.name, kernel_digest(lib_build, variant)),
                                kernel_ms, variant)
@@ -572,7 +578,8 @@ def run_ours(args):
         "config": config_block(case, world),
         "run": {"l2": l2_note(flush), "prewarm_s": args.prewarm_s,
                 "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "tile_k", "stages",
-                                              "split_k", "grid_x", "grid_y", "dp_tiles", "sk_tiles")}},
+                                              "split_k", "grid_x", "grid_y", "dp_tiles", "sk_tiles",
+                                              "kernel_launches")}},
         "pct_ffma_peak": 100.0 * achieved / ffma_peak,
         "ffma_peak": {"value": ffma_peak, "unit": "TFLOP/s",
                       "basis": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz"},
@@ -759,7 +766,7 @@ def run_ours_batched(args, c):
         "config": batched_config_block(c, d, world),
         "run": {"l2": l2_note(flush), "prewarm_s": args.prewarm_s,
                 "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "split_k", "grid_x", "grid_y",
-                                              "dp_tiles", "sk_tiles")}},
+                                              "dp_tiles", "sk_tiles", "kernel_launches")}},
         "roofline": batched_roofline(c, plan, flops_step, achieved, kernel_ms, peaks, dev, lib_build),
         "e2e": {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
                 "note": "no host-buffer batched entry point; the device-resident value is the measurement"},

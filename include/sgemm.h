@@ -107,9 +107,14 @@ enum sgemm_variant {
     SGEMM_VARIANT_TC_PRESPLIT = 10,/* 3xTF32 with A and B split once per call into TF32 hi / FP32 lo arrays
                                       (in the workspace), then CTA pairs on 256x256x32 tiles reading both
                                       parts from shared memory */
-    SGEMM_VARIANT_TC_TF32 = 11    /* sgemm_tf32() only: A and B rounded to TF32 once per call (in the
+    SGEMM_VARIANT_TC_TF32 = 11,   /* sgemm_tf32() only: A and B rounded to TF32 once per call (in the
                                       workspace), one tensor-core product per k on CTA pairs, 256x256x32
                                       tiles */
+    SGEMM_VARIANT_TC_SKINNY = 12  /* one short side (M <= 64 or N <= 64), one product: the short operand
+                                     split once per call into hi / lo arrays (in the workspace), the long
+                                     one split in the kernel; 3xTF32 on tiles of 128 along the long side x
+                                     64 along the short one (tile_m = 128 and tile_n = 64 name those
+                                     sides, whichever of M and N is short) */
 };
 
 /*

@@ -31,7 +31,7 @@ STATUS = {"OK": 0, "ERR_CUDA": 1, "ERR_TIMEOUT": 2, "ERR_NOMEM": 3, "ERR_UNSUPPO
 NOALLOC_SCRATCH_BYTES = 32 << 20  # SGEMM_NOALLOC_SCRATCH_BYTES in include/sgemm.h
 VARIANTS = {"AUTO": 0, "NONE": 1, "SCALE": 2, "GENERIC": 3, "TMA_128x128": 4, "TMA_64x256": 5, "TC_TF32X3": 6,
             "SMALL": 7, "TC_GROUPED": 8, "TC_PAIR": 9,
-            "TC_PRESPLIT": 10, "TC_TF32": 11}
+            "TC_PRESPLIT": 10, "TC_TF32": 11, "TC_SKINNY": 12}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 
 

@@ -72,6 +72,10 @@ PRESPLIT_KERNEL_FILES = ["kernel_presplit.cu", "kernel_tc_common.cuh", "device_u
 SMALL_KERNEL_FILES = ["kernel_small.cu", "kernel_small.h", "sgemm_internal.h"]
 
 
+SKINNY_KERNEL_FILES = ["kernel_skinny.cu", "kernel_presplit.cu", "kernel_tc_common.cuh", "device_utils.cuh",
+                       "sgemm_internal.h"]
+
+
 def tma_kernel_digest() -> str:
     """Hash of the sources of the TMA-fed FFMA kernel only (identifies the profiled kernel build)."""
     return _digest(TMA_KERNEL_FILES)
@@ -95,6 +99,11 @@ def presplit_kernel_digest() -> str:
 def small_kernel_digest() -> str:
     """Hash of the sources of the small-product kernel only."""
     return _digest(SMALL_KERNEL_FILES)
+
+
+def skinny_kernel_digest() -> str:
+    """Hash of the sources of the short-side kernel and the split pass it runs first."""
+    return _digest(SKINNY_KERNEL_FILES)
 
 
 def _digest(files) -> str:

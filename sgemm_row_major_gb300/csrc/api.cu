@@ -103,6 +103,7 @@ int device_state(int* device_out, DeviceState** st_out) {
       if (err == cudaSuccess) err = prepare_small_gemm();
       if (err == cudaSuccess) err = prepare_tc_pair();
       if (err == cudaSuccess) err = prepare_presplit();
+      if (err == cudaSuccess) err = prepare_skinny();
       if (err == cudaSuccess) st.pair_clusters = pair_clusters_or_none();
       if (err == cudaSuccess && !st.pool) {
         cudaMemPoolProps props = {};
@@ -289,6 +290,12 @@ constexpr double kMinFlopPerSplitByte = 128.0;
 // 270 / 1862 us; below the crossover the split passes' latency dominates).
 constexpr double kMinUnalignedSplitFlop = 2.0 * 640 * 640 * 640;
 constexpr int64_t kMaxSplitBytes = int64_t{4} << 30;
+// The short-side kernel (kernel_skinny.cu): the short side fits one 64-column accumulator.
+constexpr int64_t kSkinnyMaxShort = 64;
+
+// Whether the short-side kernel takes M as the short side (it then computes C^T = op(B)^T op(A)^T
+// and writes C transposed); N otherwise.  The shorter of the two when both are short.
+bool skinny_m_short(const Problem& pr) { return pr.M <= kSkinnyMaxShort && pr.M <= pr.N; }
 
 // Which kernels can run a problem (alignment, extents, grid limits) and the
 // derived quantities the planner's rules use.
@@ -298,6 +305,7 @@ struct Eligibility {
   bool group = false;     // block-diagonal groups on the tensor cores
   bool presplit = false;  // the split-operand kernel (and its split pass) can run it
   bool pair = true;       // CTA pairs can be co-scheduled (the CTA-pair and split-operand kernels)
+  bool skinny = false;    // the short-side kernel (and its split pass of the short operand) can run it
   int64_t group_size = 2;   // products per tile in a group (4 when M, N <= 32)
   int64_t small_grid = 0;   // persistent grid of the small-product kernel
   int64_t clusters = 1;     // co-resident CTA-pair clusters
@@ -332,6 +340,16 @@ Eligibility eligibility(const Problem& pr, int sm_count, int pair_clusters, bool
   // K-contiguous arrays for the GEMM's TMA loads, so operands TMA cannot load qualify too (the
   // transposing pass's grid holds K / 32 and the products in dimensions y and z).
   e.presplit = e.pair && allow_presplit && ceil_div(pr.K, 32) <= 65535 && pr.batch <= 65535;
+  // The short-side kernel: one product, a side of at most 64, TMA loads of the long operand as
+  // stored (the short one goes through the split pass, any alignment), split arrays in the
+  // workspace within kMaxSplitBytes.
+  if (pr.batch == 1 && std::min(pr.M, pr.N) <= kSkinnyMaxShort && allow_presplit && ceil_div(pr.K, 32) <= 65535) {
+    const bool m_short = skinny_m_short(pr);
+    const float* lp = m_short ? pr.B : pr.A;
+    const int64_t lld = m_short ? pr.ldb : pr.lda;
+    e.skinny = aligned16(lp) && lld % 4 == 0 &&
+               2 * std::min(pr.M, pr.N) * split_ldk(pr.K) * 4 <= kMaxSplitBytes;
+  }
   return e;
 }
 
@@ -377,6 +395,16 @@ int choose_variant(const Problem& pr, const Eligibility& e, int sm_count) {
       4.0 * (double)pr.M * (double)pr.N >= (double)(ceil_div(pr.M, 256) * 256) * (double)(ceil_div(pr.N, 256) * 256))
     variant = SGEMM_VARIANT_TC_PRESPLIT;
   if (e.group && pr.batch >= sm_count) variant = SGEMM_VARIANT_TC_GROUPED;
+  // One short side (<= 64): the short-side kernel once the long side and K are large enough to
+  // amortize its split pass; measured on GB300 (us, short-side / one-CTA kernel): 64x4096x16384
+  // 81.0 / 98.6, 16384x64x16384 282 / 384, 8x16384x4096 91 / 111, 4096x64x4096 47.9 / 48.5;
+  // slower with a long side of 1024 (1024x64x4096 38.8 / 33.0, 1024x64x16384 51.0 / 47.7) and
+  // equal below L * K = 2^24 (64x4096x1024 31.4 / 31.1).
+  // (Only the long operand must be TMA-aligned: the split pass reads the short one as stored.)
+  if (e.skinny) {
+    const int64_t L = std::max(pr.M, pr.N);
+    if (L >= 2048 && (double)L * (double)pr.K >= 16777216.0) variant = SGEMM_VARIANT_TC_SKINNY;
+  }
 
   switch (g_override_variant.load()) {
     case SGEMM_VARIANT_GENERIC: return SGEMM_VARIANT_GENERIC;
@@ -392,6 +420,8 @@ int choose_variant(const Problem& pr, const Eligibility& e, int sm_count) {
              : !e.tma   ? SGEMM_VARIANT_GENERIC
              : e.pair   ? SGEMM_VARIANT_TC_PAIR
                         : SGEMM_VARIANT_TC_TF32X3;
+    case SGEMM_VARIANT_TC_SKINNY:
+      return e.skinny ? SGEMM_VARIANT_TC_SKINNY : e.tma ? SGEMM_VARIANT_TC_TF32X3 : SGEMM_VARIANT_GENERIC;
     default: return variant;
   }
 }
@@ -413,6 +443,27 @@ int plan_grouped(const Problem& pr, const Eligibility& e, int sm_count, sgemm_pl
   plan->grid_x = grid;
   plan->grid_y = 1;
   plan->dp_tiles = tiles;
+  return SGEMM_OK;
+}
+
+// The short-side kernel: tiles of 128 along the long side, the persistent stream-K schedule of the
+// one-CTA kernel (slots of 128 x 64 floats), the split arrays of the short operand; launches: its
+// split pass, the GEMM, the fixup when a tile is shared.
+int plan_skinny(const Problem& pr, int sm_count, sgemm_plan_t* plan) {
+  const bool m_short = skinny_m_short(pr);
+  const int64_t L = m_short ? pr.N : pr.M, S = m_short ? pr.M : pr.N;
+  const int s = plan_stream_k(ceil_div(L, 128), ceil_div(pr.K, 32), sm_count, plan);
+  if (s != SGEMM_OK) return s;
+  plan->variant = SGEMM_VARIANT_TC_SKINNY;
+  plan->tile_m = 128;
+  plan->tile_n = 64;
+  plan->tile_k = 32;
+  plan->stages = 8;                             // long-operand ring (the short one has 4 stages)
+  plan->threads = 640;
+  plan->smem_bytes = 8 * 16384 + 4 * 16384 + 1024;
+  const int64_t slots = plan->split_k > 1 ? 2 * plan->grid_x * (int64_t)(128 * 64 * 4) : 0;
+  plan->workspace_bytes = round256(slots) + 2 * round256(S * split_ldk(pr.K) * 4);
+  plan->kernel_launches += 1;
   return SGEMM_OK;
 }
 
@@ -523,6 +574,7 @@ int make_plan(const Problem& pr, int sm_count, sgemm_plan_t* plan, int pair_clus
   const int variant = choose_variant(pr, e, sm_count);
   if (variant == SGEMM_VARIANT_TC_GROUPED) return plan_grouped(pr, e, sm_count, plan);
   if (variant == SGEMM_VARIANT_SMALL) return plan_small(e, plan);
+  if (variant == SGEMM_VARIANT_TC_SKINNY) return plan_skinny(pr, sm_count, plan);
   return plan_tiled(pr, e, variant, sm_count, plan);
 }
 
@@ -617,6 +669,50 @@ cudaError_t launch_presplit(const Problem& pr, const sgemm_plan_t& plan, const D
   return e;
 }
 
+// TC_SKINNY: the short operand split into the workspace ([stream-K slots][short hi][short lo],
+// 256-byte aligned parts, rows of round4(K) floats), then the short-side GEMM on the product seen
+// as (long side) x (short side) -- its op(A) the long operand, its op(B) the short one (the NaN
+// repair reads both as stored), C written transposed when M is the short side -- then the fixup
+// when a tile is shared.
+cudaError_t launch_skinny(const Problem& pr, const sgemm_plan_t& plan, uint8_t* ws, const GemmParams& p,
+                          int sm_count, cudaStream_t stream) {
+  const bool m_short = skinny_m_short(pr);
+  const int64_t L = m_short ? pr.N : pr.M, S = m_short ? pr.M : pr.N;
+  const bool long_contig = m_short ? !pr.tb : pr.ta;    // long operand stored [K][L]
+  const bool short_kcontig = m_short ? !pr.ta : pr.tb;  // short operand stored [S][K]
+  const int64_t slot_bytes = plan.split_k > 1 ? 2 * plan.grid_x * (int64_t)(128 * 64 * 4) : 0;
+  const int64_t ldk = split_ldk(pr.K);
+  const int64_t part = round256(S * ldk * 4);
+  float* shi = reinterpret_cast<float*>(ws + round256(slot_bytes));
+  float* slo = reinterpret_cast<float*>(ws + round256(slot_bytes) + part);
+  GemmParams q = p;
+  q.M = (int)L;
+  q.N = (int)S;
+  q.A = m_short ? pr.B : pr.A;
+  q.lda = m_short ? pr.ldb : pr.lda;
+  q.ta = long_contig ? 1 : 0;
+  q.B = m_short ? pr.A : pr.B;
+  q.ldb = m_short ? pr.lda : pr.ldb;
+  q.tb = short_kcontig ? 1 : 0;
+  q.stride_a = q.stride_b = q.stride_c = 0;
+  q.tiles_m = (int)ceil_div(L, 128);
+  q.tiles_n = 1;
+  q.ws = slot_bytes > 0 ? reinterpret_cast<float*>(ws) : nullptr;
+  set_extents(&q, plan.workspace_bytes, p.bounds);
+  if (m_short) q.c_elems = matrix_extent(S, L, pr.ldc, 1, 0);  // C is S x L
+  cudaError_t e = launch_split_operand(q.B, q.ldb, 0, short_kcontig, (int)S, (int)pr.K, 1, shi, slo, ldk, sm_count,
+                                       stream, p.fault, p.bounds, q.b_elems);
+  CUtensorMap ml, msh, msl;
+  if (e == cudaSuccess)
+    e = long_contig ? encode_matrix_map(q.A, L, pr.K, q.lda, 128, 32, &ml)
+                    : encode_matrix_map(q.A, pr.K, L, q.lda, 32, 128, &ml);
+  if (e == cudaSuccess) e = encode_split_map(shi, pr.K, S, ldk, 1, &msh, 64);
+  if (e == cudaSuccess) e = encode_split_map(slo, pr.K, S, ldk, 1, &msl, 64);
+  if (e == cudaSuccess) e = launch_skinny_gemm(long_contig, m_short, ml, msh, msl, q, stream);
+  if (e == cudaSuccess && slot_bytes > 0) e = launch_skinny_fixup(m_short, q, (int)plan.sk_tiles, stream);
+  return e;
+}
+
 // ext_ws: the caller's workspace of at least plan.workspace_bytes (sgemm_ex), or nullptr to take
 // the partial sums from the device's stream-ordered pool.
 int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& st, float* C,
@@ -658,7 +754,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
 
   CUtensorMap mapA, mapB;
   if (plan.variant != SGEMM_VARIANT_GENERIC && plan.variant != SGEMM_VARIANT_SMALL &&
-      plan.variant != SGEMM_VARIANT_TC_PRESPLIT && plan.variant != SGEMM_VARIANT_TC_TF32) {
+      plan.variant != SGEMM_VARIANT_TC_PRESPLIT && plan.variant != SGEMM_VARIANT_TC_TF32 &&
+      plan.variant != SGEMM_VARIANT_TC_SKINNY) {
     int box_m, box_n;
     operand_boxes(plan, &box_m, &box_n);
     cudaError_t e = encode_operand_maps(pr.ta, pr.tb, pr.M, pr.N, pr.K, pr.A, pr.lda, pr.stride_a, pr.B, pr.ldb,
@@ -684,6 +781,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
     e = launch_presplit(pr, plan, st, static_cast<uint8_t*>(ws ? ws : ext_ws), &p, stream);
   } else if (plan.variant == SGEMM_VARIANT_TC_TF32) {
     e = launch_tf32(pr, plan, st, static_cast<uint8_t*>(ws ? ws : ext_ws), &p, stream);
+  } else if (plan.variant == SGEMM_VARIANT_TC_SKINNY) {
+    e = launch_skinny(pr, plan, static_cast<uint8_t*>(ws ? ws : ext_ws), p, st.sm_count, stream);
   } else if (plan.variant == SGEMM_VARIANT_GENERIC) {
     e = launch_generic_gemm(pr.ta, pr.tb, p, split, stream);
   } else if (plan.variant == SGEMM_VARIANT_SMALL) {
@@ -704,7 +803,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   }
   if (e == cudaSuccess && split > 1 && plan.variant != SGEMM_VARIANT_TC_TF32X3 &&
       plan.variant != SGEMM_VARIANT_TC_GROUPED && plan.variant != SGEMM_VARIANT_TC_PAIR &&
-      plan.variant != SGEMM_VARIANT_TC_PRESPLIT && plan.variant != SGEMM_VARIANT_TC_TF32)
+      plan.variant != SGEMM_VARIANT_TC_PRESPLIT && plan.variant != SGEMM_VARIANT_TC_TF32 &&
+      plan.variant != SGEMM_VARIANT_TC_SKINNY)
     e = launch_splitk_reduce(p, split, stream);
   if (ws) {
     cudaError_t ef = cudaFreeAsync(ws, stream);
@@ -906,7 +1006,7 @@ int sgemm_set_variant_override(int variant, int split_k) {
   if (variant != SGEMM_VARIANT_AUTO && variant != SGEMM_VARIANT_GENERIC && variant != SGEMM_VARIANT_TMA_128x128 &&
       variant != SGEMM_VARIANT_TMA_64x256 && variant != SGEMM_VARIANT_TC_TF32X3 && variant != SGEMM_VARIANT_SMALL &&
       variant != SGEMM_VARIANT_TC_GROUPED && variant != SGEMM_VARIANT_TC_PAIR &&
-      variant != SGEMM_VARIANT_TC_PRESPLIT)
+      variant != SGEMM_VARIANT_TC_PRESPLIT && variant != SGEMM_VARIANT_TC_SKINNY)
     return -1;
   g_override_variant.store(variant);
   g_override_split.store(split_k < 0 ? 0 : split_k);

@@ -79,7 +79,9 @@ cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t 
 inline void set_schedule(const sgemm_plan_t& plan, GemmParams* p) {
   const bool pairs = plan.variant == SGEMM_VARIANT_TC_PAIR || plan.variant == SGEMM_VARIANT_TC_PRESPLIT ||
                      plan.variant == SGEMM_VARIANT_TC_TF32;
-  if (plan.variant != SGEMM_VARIANT_TC_TF32X3 && plan.variant != SGEMM_VARIANT_TC_GROUPED && !pairs) return;
+  if (plan.variant != SGEMM_VARIANT_TC_TF32X3 && plan.variant != SGEMM_VARIANT_TC_GROUPED &&
+      plan.variant != SGEMM_VARIANT_TC_SKINNY && !pairs)
+    return;
   p->sk_grid = (int)(pairs ? plan.grid_x / 2 : plan.grid_x);
   p->sk_iters = plan.sk_iters;
   p->sk_tile0 = (int)plan.dp_tiles;
@@ -179,9 +181,23 @@ cudaError_t launch_tf32_gemm(const CUtensorMap& mapA, const CUtensorMap& mapB, c
 int plan_without_split_arrays(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                               int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc,
                               int sm_count, int pair_clusters, sgemm_plan_t* plan);
-// Map over a split array: {K, rows, products} float32, row stride ldk, box {32, 128, 1}, 128-byte swizzle.
+// Map over a split array: {K, rows, products} float32, row stride ldk, box {32, box_rows, 1}, 128-byte
+// swizzle.
 cudaError_t encode_split_map(const float* base, int64_t K, int64_t rows, int64_t ldk, int64_t products,
-                             CUtensorMap* map);
+                             CUtensorMap* map, int box_rows = 128);
+// Map over one row-major matrix of `outer` rows x `inner` contiguous floats (row stride ld), box
+// {box_inner, box_outer, 1}; 128-byte swizzle when box rows are 32 floats.
+cudaError_t encode_matrix_map(const float* base, int64_t inner, int64_t outer, int64_t ld, int box_inner,
+                              int box_outer, CUtensorMap* map);
+
+// The short-side kernel (kernel_skinny.cu).  long_contig: the long operand is stored long side
+// contiguous; trans_c: C is the transpose of the kernel's (long x short) result.  mapL: the long
+// operand as stored (box 128 x 32 floats); mapSh / mapSl: the short operand's hi / lo split arrays
+// (box 32 x 64, swizzled).
+cudaError_t prepare_skinny();
+cudaError_t launch_skinny_gemm(bool long_contig, bool trans_c, const CUtensorMap& mapL, const CUtensorMap& mapSh,
+                               const CUtensorMap& mapSl, const GemmParams& p, cudaStream_t stream);
+cudaError_t launch_skinny_fixup(bool trans_c, const GemmParams& p, int sk_tiles, cudaStream_t stream);
 cudaError_t launch_generic_gemm(bool transA, bool transB, const GemmParams& p, int split,
                                 cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const GemmParams& p, int split, cudaStream_t stream);

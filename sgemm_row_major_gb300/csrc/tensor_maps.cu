@@ -70,10 +70,17 @@ cudaError_t bind_primary_context() {
 }  // namespace
 
 cudaError_t encode_split_map(const float* base, int64_t K, int64_t rows, int64_t ldk, int64_t products,
-                             CUtensorMap* map) {
+                             CUtensorMap* map, int box_rows) {
   cudaError_t e = bind_primary_context();
   if (e != cudaSuccess) return e;
-  return encode_3d(base, K, rows, ldk, products, rows * ldk, 32, 128, true, map);
+  return encode_3d(base, K, rows, ldk, products, rows * ldk, 32, box_rows, true, map);
+}
+
+cudaError_t encode_matrix_map(const float* base, int64_t inner, int64_t outer, int64_t ld, int box_inner,
+                              int box_outer, CUtensorMap* map) {
+  cudaError_t e = bind_primary_context();
+  if (e != cudaSuccess) return e;
+  return encode_3d(base, inner, outer, ld, 1, 0, box_inner, box_outer, box_inner == 32, map);
 }
 
 cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,

@@ -250,6 +250,40 @@ def test_split_operand_rule(lib):
     assert p["workspace_bytes"] == slots + 2 * 8192 * 1024 * 4 + 2 * 4096 * 1024 * 4
 
 
+def test_short_side_planner(lib):
+    """TC_SKINNY for one short side (<= 64) once the long side is >= 2048 and L * K >= 2^24: tiles of
+    128 along the long side, the one-CTA stream-K schedule, slots of 128 x 64 floats, the short
+    operand's hi and lo arrays, and a launch for its split pass."""
+    p = plan("N", "N", 64, 4096, 16384)
+    assert (p["variant_name"], p["tile_m"], p["tile_n"], p["threads"]) == ("TC_SKINNY", 128, 64, 640)
+    assert (p["grid_x"], p["dp_tiles"], p["sk_tiles"], p["kernel_launches"]) == (152, 0, 32, 3)
+    slots = 2 * 152 * 128 * 64 * 4
+    assert p["workspace_bytes"] == slots + 2 * 64 * 16384 * 4
+    for ta, tb in (("N", "T"), ("T", "N"), ("T", "T")):
+        assert plan(ta, tb, 64, 4096, 16384)["variant_name"] == "TC_SKINNY"
+        assert plan(ta, tb, 4096, 33, 4096)["variant_name"] == "TC_SKINNY"
+    assert plan("N", "N", 4096, 64, 4096)["variant_name"] == "TC_SKINNY"
+    # whole tiles when they fill the SMs: 16384 x 64, K = 1024 -> 128 tiles of 128 on 152 SMs
+    w = plan("N", "N", 16384, 64, 1024)
+    assert (w["variant_name"], w["dp_tiles"], w["sk_tiles"], w["kernel_launches"]) == ("TC_SKINNY", 128, 0, 2)
+    assert w["workspace_bytes"] == 2 * 64 * 1024 * 4
+    # below the rule: a long side of 1024, a short side of 65, L * K < 2^24, a batch
+    assert plan("N", "N", 1024, 64, 16384)["variant_name"] == "TC_TF32X3"
+    assert plan("N", "N", 65, 4096, 16384)["variant_name"] != "TC_SKINNY"
+    assert plan("N", "N", 64, 4096, 2048)["variant_name"] == "TC_TF32X3"
+    assert bplan("N", "N", 64, 4096, 16384, 2, 64 * 16384, 16384 * 4096, 64 * 4096)["variant_name"] != "TC_SKINNY"
+    # the long operand not TMA-aligned: not this kernel (the short one may be anything)
+    assert plan("N", "N", 64, 4096, 16384, ldb=4097)["variant_name"] != "TC_SKINNY"
+    assert plan("N", "N", 64, 4096, 16384, lda=16385)["variant_name"] == "TC_SKINNY"
+    # no split arrays (sgemm_noalloc's planner): the one-CTA kernel
+    sg.sgemm_set_variant_override("TC_SKINNY", 0)
+    try:
+        assert plan("N", "N", 64, 4096, 16384)["variant_name"] == "TC_SKINNY"
+        assert plan("N", "N", 100, 4096, 16384)["variant_name"] == "TC_TF32X3"
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
+
+
 def test_split_operand_workspace_layout(lib):
     """Workspace of TC_PRESPLIT: stream-K slots (2 per CTA, 128 x 256 floats) when a tile is shared,
     then hi and lo of op(A) and op(B) as rows of round4(K) floats, one copy per product whose operand
