@@ -401,10 +401,11 @@ int sgemm_host(char transA, char transB, int64_t M, int64_t N, int64_t K,
  * SGEMM_NOALLOC_SCRATCH_BYTES compiled into the library, one per device,
  * held by every GPU that loads the library until the process exits.
  *
- * Where sgemm() would split A and B into workspace arrays
- * (SGEMM_VARIANT_TC_PRESPLIT), sgemm_noalloc() runs the CTA-pair kernel
- * (SGEMM_VARIANT_TC_PAIR) instead: the same error bounds, possibly different
- * rounding.
+ * Where sgemm() would split operands into workspace arrays, sgemm_noalloc()
+ * runs the kernel the planner takes without them: the CTA-pair kernel
+ * (SGEMM_VARIANT_TC_PAIR) for SGEMM_VARIANT_TC_PRESPLIT, the one-CTA kernel's
+ * rules (SGEMM_VARIANT_TC_TF32X3 or TC_PAIR) for SGEMM_VARIANT_TC_SKINNY:
+ * the same error bounds, possibly different rounding.
  *
  * Limit: a problem whose split-K partial sums need more than
  * SGEMM_NOALLOC_SCRATCH_BYTES (see sgemm_plan_t.workspace_bytes) is rejected
