@@ -626,10 +626,10 @@ cudaError_t launch_tf32(const Problem& pr, const sgemm_plan_t& plan, const Devic
   p->za = p->zb = 0;
   p->repair = 0;
   cudaError_t e = launch_split_operand(pr.A, pr.lda, 0, !pr.ta, (int)pr.M, (int)pr.K, 1, ar, nullptr, ldk,
-                                       st.sm_count, stream, p->fault, p->bounds, p->a_elems);
+                                       st.sm_count, stream, p->fault, p->bounds, p->a_elems, SplitOrder::kFirst);
   if (e == cudaSuccess)
     e = launch_split_operand(pr.B, pr.ldb, 0, pr.tb, (int)pr.N, (int)pr.K, 1, br, nullptr, ldk, st.sm_count, stream,
-                             p->fault, p->bounds, p->b_elems);
+                             p->fault, p->bounds, p->b_elems, SplitOrder::kDependent);
   CUtensorMap ma, mb;
   if (e == cudaSuccess) e = encode_split_map(ar, pr.K, pr.M, ldk, 1, &ma);
   if (e == cudaSuccess) e = encode_split_map(br, pr.K, pr.N, ldk, 1, &mb);
@@ -653,10 +653,10 @@ cudaError_t launch_presplit(const Problem& pr, const sgemm_plan_t& plan, const D
   // op(A) rows run along K when A is 'N'; op(B) rows (columns of op(B)) when B is 'T'
   cudaError_t e = launch_split_operand(pr.A, pr.lda, pr.stride_a, !pr.ta, (int)pr.M, (int)pr.K,
                                        (int)l.a_products, ahi, alo, ldk, st.sm_count, stream, p->fault, p->bounds,
-                                       p->a_elems);
+                                       p->a_elems, SplitOrder::kFirst);
   if (e == cudaSuccess)
     e = launch_split_operand(pr.B, pr.ldb, pr.stride_b, pr.tb, (int)pr.N, (int)pr.K, (int)l.b_products, bhi, blo,
-                             ldk, st.sm_count, stream, p->fault, p->bounds, p->b_elems);
+                             ldk, st.sm_count, stream, p->fault, p->bounds, p->b_elems, SplitOrder::kDependent);
   CUtensorMap mah, mal, mbh, mbl;
   if (e == cudaSuccess) e = encode_split_map(ahi, pr.K, pr.M, ldk, l.a_products, &mah);
   if (e == cudaSuccess) e = encode_split_map(alo, pr.K, pr.M, ldk, l.a_products, &mal);

@@ -25,6 +25,15 @@
 // unit; presplit_fixup_kernel adds the partial sums of shared tiles in
 // cluster order.
 //
+// Launch chain of a call: split pass of A, split pass of B, GEMM, fixup.
+// Each launch after the first is a programmatic dependent of the one before:
+// the B pass starts once every block of the A pass has started and waits for
+// that pass at its end; the GEMM's prologue (barriers, TMEM, tensor maps)
+// runs while the B pass finishes and its producer waits for that pass before
+// the first load; the fixup waits for the GEMM.  (A dependent grid starts
+// only when every block of the grid before it has started or finished, so
+// the early blocks cannot hold the SMs that later blocks of that grid need.)
+//
 // The pages name tensor cores and TF32 as the missing piece of their SGEMM
 // (itan.pw "CUDA NVIDIA 4090 高性能計算", §4; youngju.dev "CUDA architecture
 // visualized", テンソルコア).
@@ -80,10 +89,21 @@ struct SplitChk {
   }
 };
 
+// Launch order of a call's split passes and GEMM (programmatic dependent launches): the first
+// split pass lets the next one start at once (`trigger`); a split pass launched as a dependent
+// waits at its end for the pass before it, so its grid completes after that one; the GEMM,
+// launched as a dependent of the last pass, waits for it before its first load of split data.
+__device__ __forceinline__ void split_pass_begin(bool trigger) {
+  if (trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void split_pass_end() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <bool VEC>
 __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict__ src, int64_t ld, int64_t stride,
                                                          int rows, int K, int products, float* __restrict__ hi,
-                                                         float* __restrict__ lo, int64_t ldk, const SplitChk chk) {
+                                                         float* __restrict__ lo, int64_t ldk, const SplitChk chk,
+                                                         bool trigger) {
+  split_pass_begin(trigger);
   const int k4n = (K + 3) / 4;
   const int64_t total = (int64_t)products * rows * k4n;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -113,6 +133,7 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict
       }
     }
   }
+  split_pass_end();
 }
 
 // Stored rows run along the other axis: a 32 x 32 block per CTA (32 x 8 threads), read along
@@ -120,7 +141,8 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict
 __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __restrict__ src, int64_t ld,
                                                               int64_t stride, int rows, int K,
                                                               float* __restrict__ hi, float* __restrict__ lo,
-                                                              int64_t ldk, const SplitChk chk) {
+                                                              int64_t ldk, const SplitChk chk, bool trigger) {
+  split_pass_begin(trigger);
   __shared__ float tile[kSplitTile][kSplitTile + 1];
   const int p = (int)blockIdx.z;
   const int r0 = (int)blockIdx.x * kSplitTile, k0 = (int)blockIdx.y * kSplitTile;
@@ -146,6 +168,7 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __res
       if (lo) l[(int64_t)r * ldk + k] = xl;
     }
   }
+  split_pass_end();
 }
 
 // ------------------------------------------------------------------ GEMM
@@ -295,6 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&mapAl);
       prefetch_tensormap(&mapBh);
       prefetch_tensormap(&mapBl);
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the split passes' arrays are complete
       int issued = 0;
       bool ok = true;
       const CtaWork work = work_s;
@@ -554,39 +578,62 @@ cudaError_t prepare_presplit() {
 
 cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, bool k_contig, int rows, int K,
                                  int products, float* hi, float* lo, int64_t ldk, int sm_count, cudaStream_t stream,
-                                 unsigned* fault, unsigned long long* bounds, int64_t src_elems) {
+                                 unsigned* fault, unsigned long long* bounds, int64_t src_elems, SplitOrder order) {
   if (rows <= 0 || K <= 0 || products <= 0) return cudaSuccess;
   const tps::SplitChk chk{fault, bounds, src_elems, (int64_t)products * rows * ldk};
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = order == SplitOrder::kDependent ? 1 : 0;
+  const bool trigger = order == SplitOrder::kFirst;
   if (k_contig) {
     const int64_t work = (int64_t)products * rows * ((K + 3) / 4);
-    const unsigned blocks = (unsigned)std::max<int64_t>(std::min<int64_t>((work + 255) / 256, (int64_t)sm_count * 8), 1);
+    cfg.gridDim = dim3((unsigned)std::max<int64_t>(std::min<int64_t>((work + 255) / 256, (int64_t)sm_count * 8), 1));
+    cfg.blockDim = dim3(256);
     const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && ld % 4 == 0 && (products == 1 || stride % 4 == 0);
-    if (vec)
-      tps::split_rows_kernel<true><<<blocks, 256, 0, stream>>>(src, ld, stride, rows, K, products, hi, lo, ldk, chk);
-    else
-      tps::split_rows_kernel<false><<<blocks, 256, 0, stream>>>(src, ld, stride, rows, K, products, hi, lo, ldk, chk);
-  } else {
-    const dim3 grid((unsigned)((rows + tps::kSplitTile - 1) / tps::kSplitTile),
-                    (unsigned)((K + tps::kSplitTile - 1) / tps::kSplitTile), (unsigned)products);
-    tps::split_transpose_kernel<<<grid, dim3(tps::kSplitTile, 8), 0, stream>>>(src, ld, stride, rows, K, hi, lo,
-                                                                               ldk, chk);
+    return vec ? cudaLaunchKernelEx(&cfg, tps::split_rows_kernel<true>, src, ld, stride, rows, K, products, hi, lo, ldk,
+                                    chk, trigger)
+               : cudaLaunchKernelEx(&cfg, tps::split_rows_kernel<false>, src, ld, stride, rows, K, products, hi, lo,
+                                    ldk, chk, trigger);
   }
-  return cudaGetLastError();
+  cfg.gridDim = dim3((unsigned)((rows + tps::kSplitTile - 1) / tps::kSplitTile),
+                     (unsigned)((K + tps::kSplitTile - 1) / tps::kSplitTile), (unsigned)products);
+  cfg.blockDim = dim3(tps::kSplitTile, 8);
+  return cudaLaunchKernelEx(&cfg, tps::split_transpose_kernel, src, ld, stride, rows, K, hi, lo, ldk, chk, trigger);
 }
+
+namespace {
+// The GEMM after the split passes: a programmatic dependent launch (its prologue overlaps the
+// last pass; its producer waits for that pass before the first load).
+template <int PARTS>
+cudaError_t launch_gemm_after_split(const CUtensorMap& mapAh, const CUtensorMap& mapAl, const CUtensorMap& mapBh,
+                                    const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2u * (unsigned)p.sk_grid);
+  cfg.blockDim = dim3(tps::kThreads);
+  cfg.dynamicSmemBytes = tps::Cfg<PARTS>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tps::presplit_gemm_kernel<PARTS>, mapAh, mapAl, mapBh, mapBl, p);
+}
+}  // namespace
 
 cudaError_t launch_presplit_gemm(const CUtensorMap& mapAh, const CUtensorMap& mapAl, const CUtensorMap& mapBh,
                                  const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream) {
-  tps::presplit_gemm_kernel<2><<<2u * (unsigned)p.sk_grid, tps::kThreads, tps::Cfg<2>::kSmemBytes, stream>>>(
-      mapAh, mapAl, mapBh, mapBl, p);
-  return cudaGetLastError();
+  return launch_gemm_after_split<2>(mapAh, mapAl, mapBh, mapBl, p, stream);
 }
 
 cudaError_t launch_tf32_gemm(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
                              cudaStream_t stream) {
   // (the lo maps are not read with one part)
-  tps::presplit_gemm_kernel<1><<<2u * (unsigned)p.sk_grid, tps::kThreads, tps::Cfg<1>::kSmemBytes, stream>>>(
-      mapA, mapA, mapB, mapB, p);
-  return cudaGetLastError();
+  return launch_gemm_after_split<1>(mapA, mapA, mapB, mapB, p, stream);
 }
 
 cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream) {

@@ -17,7 +17,8 @@
 // The short operand is split once per call (split_rows_kernel /
 // split_transpose_kernel of kernel_presplit.cu) into K-contiguous hi and lo
 // arrays in the workspace, which TMA copies into shared memory already in the
-// layout the tensor core reads; only the long operand is split in the
+// layout the tensor core reads (the GEMM is a programmatic dependent launch of
+// that pass: only the short operand's producer waits for it); only the long operand is split in the
 // kernel, into tensor memory (A from TMEM, B from shared memory, as in the
 // one-CTA kernel).  Per 32-k tile a CTA moves 16 KB of the long operand
 // (read once from HBM for the whole call) and 16 KB of short hi/lo (L2).
@@ -202,6 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         prefetch_tensormap(&mapSh);
         prefetch_tensormap(&mapSl);
+        // launched as a programmatic dependent of the short operand's split pass: its arrays are
+        // complete once that grid is (the long operand is read as stored, without waiting)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
       }
       int issued = 0;
       bool ok = true;
@@ -505,12 +509,20 @@ cudaError_t prepare_skinny() {
 cudaError_t launch_skinny_gemm(bool long_contig, bool trans_c, const CUtensorMap& mapL, const CUtensorMap& mapSh,
                                const CUtensorMap& mapSl, const GemmParams& p, cudaStream_t stream) {
   using namespace skinny;
-  const dim3 grid((unsigned)p.sk_grid), block(kThreads);
-  if (long_contig && trans_c) skinny_gemm_kernel<true, true><<<grid, block, kSmemBytes, stream>>>(mapL, mapSh, mapSl, p);
-  else if (long_contig) skinny_gemm_kernel<true, false><<<grid, block, kSmemBytes, stream>>>(mapL, mapSh, mapSl, p);
-  else if (trans_c) skinny_gemm_kernel<false, true><<<grid, block, kSmemBytes, stream>>>(mapL, mapSh, mapSl, p);
-  else skinny_gemm_kernel<false, false><<<grid, block, kSmemBytes, stream>>>(mapL, mapSh, mapSl, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.sk_grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // after the split pass (see the producer)
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (long_contig && trans_c) return cudaLaunchKernelEx(&cfg, skinny_gemm_kernel<true, true>, mapL, mapSh, mapSl, p);
+  if (long_contig) return cudaLaunchKernelEx(&cfg, skinny_gemm_kernel<true, false>, mapL, mapSh, mapSl, p);
+  if (trans_c) return cudaLaunchKernelEx(&cfg, skinny_gemm_kernel<false, true>, mapL, mapSh, mapSl, p);
+  return cudaLaunchKernelEx(&cfg, skinny_gemm_kernel<false, false>, mapL, mapSh, mapSl, p);
 }
 
 cudaError_t launch_skinny_fixup(bool trans_c, const GemmParams& p, int sk_tiles, cudaStream_t stream) {

@@ -163,10 +163,14 @@ cudaError_t launch_pair_fixup(const GemmParams& p, int sk_tiles, cudaStream_t st
 // the CTA-pair GEMM on 256x256x32 tiles with four maps over the split arrays,
 // then the fixup over the sk_tiles stream-K pair tiles when any is shared.
 cudaError_t prepare_presplit();
+// Where a split pass stands in its call's launch chain: the first of the call (lets the next
+// launch start early), a dependent of the pass before it (a programmatic dependent launch that
+// completes only after that pass), or alone.
+enum class SplitOrder { kAlone, kFirst, kDependent };
 cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, bool k_contig, int rows, int K,
                                  int products, float* hi, float* lo, int64_t ldk, int sm_count, cudaStream_t stream,
                                  unsigned* fault = nullptr, unsigned long long* bounds = nullptr,
-                                 int64_t src_elems = 0);
+                                 int64_t src_elems = 0, SplitOrder order = SplitOrder::kAlone);
 cudaError_t launch_presplit_gemm(const CUtensorMap& mapAh, const CUtensorMap& mapAl, const CUtensorMap& mapBh,
                                  const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
