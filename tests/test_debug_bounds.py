@@ -77,7 +77,7 @@ def run(lib, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, variant="AUTO
 SHAPES = [(1, 1, 1), (7, 5, 3), (33, 65, 16), (129, 130, 70), (300, 260, 1000), (513, 257, 95), (64, 700, 2049)]
 VARIANTS = [("AUTO", 0), ("GENERIC", 0), ("GENERIC", 3), ("TMA_128x128", 0), ("TMA_128x128", 4), ("TMA_64x256", 0),
             ("TC_TF32X3", 0), ("TC_TF32X3", 3), ("TC_PAIR", 0), ("TC_PAIR", 3), ("TC_PRESPLIT", 0),
-            ("TC_PRESPLIT", 3)]
+            ("TC_PRESPLIT", 3), ("TC_SKINNY", 0), ("TC_SKINNY", 3)]
 
 
 @pytest.mark.parametrize("variant,split", VARIANTS, ids=[f"{v}-{s}" for v, s in VARIANTS])

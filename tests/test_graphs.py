@@ -82,6 +82,34 @@ def test_split_operand_graph_replay():
         check_exact(dC.cpu().numpy(), oracle.sgemm("N", "T", A, B, C, 1.5, -0.5), f"split-operand replay {rep}")
 
 
+@pytest.mark.parametrize("M,N", [(64, 2048), (2048, 33)])
+def test_short_side_graph_replay(M, N):
+    """The short-side path (split pass of the short operand, the GEMM as its programmatic
+    dependent, the fixup, workspace from the pool) captured once and replayed on new inputs."""
+    torch = torch_cuda()
+    K = 3000
+    sg.sgemm_set_variant_override("TC_SKINNY", 0)
+    try:
+        plan = sg.sgemm_plan("N", "N", M, N, K, 1.0, 1 << 20, K, 1 << 20, N, 0.5, 1 << 20, N)
+        assert plan["variant_name"] == "TC_SKINNY" and plan["kernel_launches"] == 3
+        dA = torch.empty((M, K), dtype=torch.float32, device="cuda")
+        dB = torch.empty((K, N), dtype=torch.float32, device="cuda")
+        dC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+        g = _capture(torch, lambda: sg.sgemm("N", "N", M, N, K, 1.5, dA, K, dB, N, -0.5, dC, N))
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
+    rng = np.random.default_rng(M + N)
+    for rep in range(2):
+        A, B, C = _dyadic(rng, (M, K)), _dyadic(rng, (K, N)), _dyadic(rng, (M, N))
+        dA.copy_(torch.from_numpy(A))
+        dB.copy_(torch.from_numpy(B))
+        dC.copy_(torch.from_numpy(C))
+        g.replay()
+        torch.cuda.synchronize()
+        assert sg.sgemm_sync_status() == 0
+        check_exact(dC.cpu().numpy(), oracle.sgemm("N", "N", A, B, C, 1.5, -0.5), f"short-side replay {rep}")
+
+
 def test_graph_replays_back_to_back_accumulate():
     """beta = 1: five replays without a sync between them add op(A) op(B) five times, in order."""
     torch = torch_cuda()
