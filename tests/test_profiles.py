@@ -58,3 +58,11 @@ def test_hbm_roof_chosen_when_bytes_bind():
     roof = bench.tensor_roofline(270.0, peaks, None, 0.5)
     bench.hbm_bound_roofline(roof, 268.4e6, 137.4e9, 0.5, peaks)
     assert roof["bound"] == "tensor"
+
+
+def test_l2_hot_block():
+    """Configs whose input set fits in L2 carry an L2-hot figure beside the flushed one; larger
+    ones say why they have none."""
+    assert bench.l2_hot_block(None, None, 1e9)["value"] is None
+    hot = bench.l2_hot_block(lambda: None, 0.01, 2.147e9)  # 10 us per 1024^3 step
+    assert abs(hot["value"] - 214.7) < 1e-9 and hot["unit"] == "TFLOPS" and hot["ms_per_step"] == 0.01
