@@ -185,6 +185,11 @@ constexpr int kPartBytes = 128 * BK * 4;  // 16 KB: 128 rows (or columns) x 32 k
 template <int PARTS>
 struct Cfg {
   static constexpr int kStages = PARTS == 2 ? 3 : 6;
+  // K tiles summed in one TMEM accumulator before the folders add it into FP32 registers: 12
+  // tensor-core products either way (3xTF32: 4 k-steps x 3 products; TF32 inputs: 3 K tiles x 4
+  // k-steps x 1), the count the fold was sized for (the tensor core's FP32 accumulation drifts
+  // with the number of products it adds; kernel_tf32x3.cu)
+  static constexpr int kFoldTiles = PARTS == 2 ? 1 : 3;
   static constexpr int kStageBytes = 2 * PARTS * kPartBytes;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
   static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA");
@@ -368,43 +373,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) atomicOr(p.fault, (unsigned)kFaultFullWait);
     } else if (lane == 0) {
       // ---------------------------------------------- MMA issuer (even CTA)
+      // K tile t of the CTA's sequence uses stage t % kStages; chunk c (up to kFoldTiles K tiles of
+      // one segment) accumulates in accumulator c % kAccBufs
+      constexpr int kFold = Cfg<PARTS>::kFoldTiles;
       bool ok = true;
-      int done = -1;
-      for (int t = 0; ok && t < nkt; ++t) {
-        const int s = t % kStages, b = t % kAccBufs;
-        const uint32_t ph = (uint32_t)(t / kStages) & 1u;
-        if (!mbar_wait(smem_addr(&full[s]), ph, p.timeout_ns) ||
-            (t >= kAccBufs &&
-             !mbar_wait(smem_addr(&acc_empty[b]), (uint32_t)((t / kAccBufs) - 1) & 1u, p.timeout_ns))) {
-          ok = false;
-          break;
-        }
-        tmem_fence_after_sync();
-        const uint32_t acc = tmem + (uint32_t)b * kAccCols;
-        const uint64_t ahi = kmajor_sw128_desc(part(s, kAhi)), bhi = kmajor_sw128_desc(part(s, kBhi));
-#pragma unroll
-        for (int ks = 0; ks < BK / 8; ++ks) {
-          const uint64_t step = (uint64_t)(ks * 32) >> 4;  // 8 TF32 = 32 bytes along K
-          if (PARTS == 2) {
-            const uint64_t alo = kmajor_sw128_desc(part(s, kAlo)), blo = kmajor_sw128_desc(part(s, kBlo));
-            mma_pair_ss(acc, alo + step, bhi + step, ks == 0 ? 0u : 1u);  // fresh accumulator per K tile
-            mma_pair_ss(acc, ahi + step, blo + step, 1u);
-            mma_pair_ss(acc, ahi + step, bhi + step, 1u);
-          } else {
-            mma_pair_ss(acc, ahi + step, bhi + step, ks == 0 ? 0u : 1u);
+      int t = 0, c = 0, t_done = -1, c_done = -1;
+      const CtaWork work = work_s;
+      for (int sgi = 0; ok && sgi < work.nseg; ++sgi) {
+        const Segment g = cta_segment(p, work, cl, sgi, kt_total);
+        for (int i0 = g.kb; ok && i0 < g.ke; i0 += kFold, ++c) {
+          const int n = min(kFold, g.ke - i0);
+          const int b = c % kAccBufs;
+          if (c >= kAccBufs &&
+              !mbar_wait(smem_addr(&acc_empty[b]), (uint32_t)((c / kAccBufs) - 1) & 1u, p.timeout_ns)) {
+            ok = false;
+            break;
           }
+          const uint32_t acc = tmem + (uint32_t)b * kAccCols;
+          for (int j = 0; j < n; ++j, ++t) {
+            const int s = t % kStages;
+            if (!mbar_wait(smem_addr(&full[s]), (uint32_t)(t / kStages) & 1u, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tmem_fence_after_sync();
+            const uint64_t ahi = kmajor_sw128_desc(part(s, kAhi)), bhi = kmajor_sw128_desc(part(s, kBhi));
+#pragma unroll
+            for (int ks = 0; ks < BK / 8; ++ks) {
+              const uint64_t step = (uint64_t)(ks * 32) >> 4;  // 8 TF32 = 32 bytes along K
+              const uint32_t fresh = (j == 0 && ks == 0) ? 0u : 1u;  // a fresh accumulator per chunk
+              if (PARTS == 2) {
+                const uint64_t alo = kmajor_sw128_desc(part(s, kAlo)), blo = kmajor_sw128_desc(part(s, kBlo));
+                mma_pair_ss(acc, alo + step, bhi + step, fresh);
+                mma_pair_ss(acc, ahi + step, blo + step, 1u);
+                mma_pair_ss(acc, ahi + step, bhi + step, 1u);
+              } else {
+                mma_pair_ss(acc, ahi + step, bhi + step, fresh);
+              }
+            }
+            mma_commit_pair(smem_addr(&empty[s]));  // stage s reusable in both CTAs
+            t_done = t;
+          }
+          if (!ok) break;
+          mma_commit_pair(smem_addr(&acc_full[b]));  // accumulator b (both CTAs) holds chunk c
+          c_done = c;
         }
-        mma_commit_pair(smem_addr(&empty[s]));     // stage s reusable in both CTAs
-        mma_commit_pair(smem_addr(&acc_full[b]));  // accumulator b (both CTAs) holds K tile t
-        done = t;
       }
       if (!ok) atomicOr(p.fault, (unsigned)kFaultFullWait);
       // leave only when every MMA has completed and its commits have landed here
-      for (int u = done + 1 > kStages ? done + 1 - kStages : 0; u <= done; ++u)
+      for (int u = t_done + 1 > kStages ? t_done + 1 - kStages : 0; u <= t_done; ++u)
         if (!mbar_wait(smem_addr(&empty[u % kStages]), (uint32_t)(u / kStages) & 1u, p.timeout_ns))
           atomicOr(p.fault, (unsigned)kFaultDrainWait);
-      if (done >= 0 &&
-          !mbar_wait(smem_addr(&acc_full[done % kAccBufs]), (uint32_t)(done / kAccBufs) & 1u, p.timeout_ns))
+      if (c_done >= 0 &&
+          !mbar_wait(smem_addr(&acc_full[c_done % kAccBufs]), (uint32_t)(c_done / kAccBufs) & 1u, p.timeout_ns))
         atomicOr(p.fault, (unsigned)kFaultDrainWait);
     }
   } else {
@@ -423,7 +444,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const Segment g = cta_segment(p, work_s, cl, sgi, kt_total);
         len = g.ke - g.kb;
       }
-      for (int i = 0; i < len; ++i, ++u) {
+      for (int i = 0; i < len; i += Cfg<PARTS>::kFoldTiles, ++u) {  // chunk u: as the issuer's chunks
         const int b = u % kAccBufs;
         if (!warp_wait(smem_addr(&acc_full[b]), (uint32_t)(u / kAccBufs) & 1u, p.timeout_ns)) {
           ok = false;

@@ -91,3 +91,36 @@ def test_grouped_batch_offsets_beyond_2g():
                            1.0, 0.0)
         check_exact(dC[b].cpu().numpy(), ref, f"product {b}")
     del dA, dB, dC
+
+
+@pytest.mark.parametrize("M,N", [(64, 40_000_000), (50_000_000, 48)])
+def test_short_side_offsets_beyond_2g(M, N):
+    """The short-side kernel with C past 2^31 elements: M short (C written transposed, a column of
+    the kernel's tile spans 64 rows of C 40 M floats apart) and N short (rows of 48)."""
+    torch = torch_cuda()
+    K = 32
+    assert M * N > TWO31
+    dA, dB = _ints(torch, (M, K), 97), _ints(torch, (K, N), 98)
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    sg.sgemm_set_variant_override("TC_SKINNY", 0)
+    try:
+        assert sg.sgemm_plan("N", "N", M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N)["variant_name"] == "TC_SKINNY"
+        sg.sgemm("N", "N", M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N)
+    finally:
+        sg.sgemm_set_variant_override("AUTO", 0)
+    assert sg.sgemm_sync_status() == 0
+    if M == 64:
+        # every row of columns around the one where row r = 2^31 // N passes 2^31 (offset r * N + c)
+        c_b = TWO31 - (TWO31 // N) * N
+        cols = sorted({0, 1, N - 2, N - 1, c_b - 1, c_b, c_b + 1, 12_345_678})
+        got = dC[:, cols].cpu().numpy()
+        ref = oracle.sgemm("N", "N", dA.cpu().numpy(), np.ascontiguousarray(dB[:, cols].cpu().numpy()),
+                           np.zeros((M, len(cols)), np.float32), 1.0, 0.0)
+    else:
+        boundary = TWO31 // N
+        rows = sorted({0, boundary - 1, boundary, boundary + 1, M - 2, M - 1, 12345})
+        got = dC[rows].cpu().numpy()
+        ref = oracle.sgemm("N", "N", dA[rows].cpu().numpy(), dB.cpu().numpy(), np.zeros((len(rows), N), np.float32),
+                           1.0, 0.0)
+    check_exact(got, ref, f"short side {M}x{N} beyond 2^31")
+    del dC
