@@ -48,12 +48,13 @@
 //              warp 18 odd ones): 4 k-steps x 3 tcgen05.mma (M=128, N=64,
 //              K=8) per K tile.  Every ring has an even number of slots, so
 //              each slot of each ring belongs to one issuer and its barrier
-//              phases are consecutive for it.  Measured on GB300 (clock64
-//              traces of one CTA at 64 x 4096 x 16384): a K tile every ~1190
-//              cycles, the time one thread takes to issue its 12 MMAs; a
-//              third and fourth issuer did not shorten it (the SM takes
-//              about one tcgen05.mma per 100 cycles whichever thread issues
-//              it), and the tensor pipe is ~33% busy.
+//              phases are consecutive for it.  Measured on GB300 at 64 x 4096
+//              x 16384 (clock64 traces of one CTA; µs per call): a K tile
+//              every ~1190 cycles, about the time one thread takes to issue
+//              its 12 MMAs; one issuer 121 µs, two 80, three 85, four 82;
+//              the tensor pipe is ~33% busy.  Ring sizes measured no faster:
+//              6 + 6 long/short stages, 2 split stages with 6 accumulators,
+//              6 split stages with 2 accumulators (one issuer), 10 long stages.
 //   warps 2-9  splitters: the long tile -> hi/lo in TMEM (row in lane, k in
 //              columns), 4 TMEM stages; warps 2-5 split k 0-15, warps 6-9
 //              k 16-31, each half with its own full/empty barriers.
@@ -91,7 +92,7 @@ constexpr int kFirstFoldWarp = 2 + kSplitWarps;
 constexpr int kSecondMmaWarp = kFirstFoldWarp + kFoldWarps;
 constexpr int kShortProducerWarp = kSecondMmaWarp + 1;
 constexpr int kThreads = 32 * (4 + kSplitWarps + kFoldWarps);
-constexpr int kIssuers = 2;
+constexpr int kIssuers = 2;  // 1 or 2 (warps 1 and 18)
 constexpr int kAccBufs = 4;
 constexpr uint32_t kAccCols = BN;
 constexpr uint32_t kACols = 64;  // long hi (32 k) + long lo (32 k) of one split stage
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 || warp == kSecondMmaWarp) {
     // ------------------------------------------------ MMA issuers (K tiles t with t % kIssuers == issuer)
     const int issuer = warp == 1 ? 0 : 1;
-    if (lane == 0) {
+    if (lane == 0 && issuer < kIssuers) {
       int done = -1;
       bool ok = true;
       for (int t = issuer; ok && t < nkt; t += kIssuers) {
