@@ -286,8 +286,8 @@ constexpr int64_t kPresplitSmemBytes = 3 * 65536 + 1024;
 constexpr double kMinFlopPerSplitByte = 128.0;
 // Calls with operands TMA cannot load go to the split-operand kernel from this size on (measured
 // on GB300 with bases one float off alignment and ld % 4 != 0, split-operand / generic kernel:
-// 512^3 33.4 / 27.3 us, 1000x1300x700 44.2 / 107.2 us, 2048^3 102 / 638 us, 4097x3001x2053
-// 270 / 1862 us; below the crossover the split passes' latency dominates).
+// 512^3 27.3 / 22.7 us, 1000x1300x700 38.5 / 82.6 us, 2048^3 85.2 / 439 us, 4097x3001x2053
+// 263 / 1311 us; below the crossover the split passes' latency dominates).
 constexpr double kMinUnalignedSplitFlop = 2.0 * 640 * 640 * 640;
 constexpr int64_t kMaxSplitBytes = int64_t{4} << 30;
 // The short-side kernel (kernel_skinny.cu): the short side fits one 64-column accumulator.
