@@ -14,7 +14,8 @@ klklkl10086.github.io "Sgemm单精度矩阵乘法", 问题定义)::
     Cref_ij = fl32(alpha * sum_k op(A)_ik op(B)_kj + beta * C_ij)   (in double)
 
 Also the TF32-input GEMM: A and B rounded to TF32 (round_tf32, ties away
-from zero), then the same SGEMM.
+from zero), then the same SGEMM; and the BF16-input GEMM: A and B rounded to
+BF16 (round_bf16, ties to even), then the same SGEMM.
 
 Pins (tests/test_oracle.py): the 2MNK FLOP count the pages print, brute force
 against an independent float64 einsum on tiny shapes, exact integer results on
@@ -85,6 +86,8 @@ def load_library(path: str) -> ctypes.CDLL:
                   i64, vp, i64, i64]
     lib.oracle_round_tf32.restype = None
     lib.oracle_round_tf32.argtypes = [vp, vp, i64]
+    lib.oracle_round_bf16.restype = None
+    lib.oracle_round_bf16.argtypes = [vp, vp, i64]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_set_num_threads.restype = None
@@ -225,6 +228,27 @@ def round_tf32(x: np.ndarray, lib=None) -> np.ndarray:
     if src.size:
         lib.oracle_round_tf32(src.ctypes.data, out.ctypes.data, src.size)
     return out
+
+
+def round_bf16(x: np.ndarray, lib=None) -> np.ndarray:
+    """x (float32) rounded to BF16 -- 7 fraction bits, to nearest with ties to even; past the
+    largest BF16 value to +-Inf; +-0, +-Inf, NaN kept -- by the C oracle's rounding, returned as
+    float32 (a new array)."""
+    lib = lib or _library()
+    src = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(src)
+    if src.size:
+        lib.oracle_round_bf16(src.ctypes.data, out.ctypes.data, src.size)
+    return out
+
+
+def sgemm_bf16(transA: str, transB: str, A: np.ndarray, B: np.ndarray, C: np.ndarray | None = None,
+               alpha: float = 1.0, beta: float = 0.0, M: int | None = None, N: int | None = None,
+               K: int | None = None, want_bound: bool = False, lib=None):
+    """The BF16-input GEMM: oracle SGEMM (sgemm above) on the stored A and B rounded to BF16
+    (round_bf16); C, alpha, beta as they are.  S, when wanted, is that of the rounded inputs."""
+    return sgemm(transA, transB, round_bf16(A, lib), round_bf16(B, lib), C, alpha, beta, M=M, N=N, K=K,
+                 want_bound=want_bound, lib=lib)
 
 
 def sgemm_tf32(transA: str, transB: str, A: np.ndarray, B: np.ndarray, C: np.ndarray | None = None,

@@ -160,6 +160,39 @@ void oracle_round_tf32(const float *x, float *y, int64_t n)
     for (int64_t i = 0; i < n; ++i) y[i] = oracle_tf32(x[i]);
 }
 
+/*
+ * BF16 rounding (the other tensor-core input format for FP32-range data the
+ * page names, youngju.dev "CUDA architecture visualized", テンソルコア): 1 sign
+ * bit, float32's 8 exponent bits and 7 fraction bits, so the quantum near |x|
+ * is 2^(floor(log2|x|) - 7) for normal x and 2^-133 below 2^-126.  y = x
+ * rounded to the nearest such value, ties to the one whose last kept bit is
+ * 0 (IEEE round to nearest even; the pages give no rule, so the IEEE default);
+ * past the largest BF16 value (2 - 2^-7) 2^127 to +-Inf; +-0, +-Inf and NaN
+ * kept.  Computed in double, where every step is exact.
+ */
+static float oracle_bf16(float x)
+{
+    if (x != x || isinf(x) || x == 0.0f) return x;
+    const double a = fabs((double)x);
+    int e;
+    frexp(a, &e);                       /* floor(log2 a) = e - 1 */
+    int qexp = (e - 1) - 7;
+    if (qexp < -133) qexp = -133;       /* subnormal range: fixed quantum */
+    const double q = ldexp(1.0, qexp);
+    const double n = a / q;             /* exact: a has at most 24 significant bits */
+    double m = floor(n);
+    const double frac = n - m;
+    if (frac > 0.5 || (frac == 0.5 && fmod(m, 2.0) != 0.0)) m += 1.0;   /* nearest, ties to even */
+    const double r = m * q;
+    const double y = (x < 0.0f) ? -r : r;
+    return (float)y;                    /* exact, or +-Inf past the largest BF16 value */
+}
+
+void oracle_round_bf16(const float *x, float *y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_bf16(x[i]);
+}
+
 /* Sets the number of OpenMP threads later oracle calls use (n >= 1). */
 void oracle_set_num_threads(int n)
 {

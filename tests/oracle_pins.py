@@ -15,7 +15,8 @@ raises AssertionError when the oracle disagrees with:
     the float32 range, and the IEEE 754 rules for Inf and NaN operands,
   * for the TF32-input GEMM: hand-worked roundings (tests/golden/tf32_round.txt),
     a bit-level characterization of the rounding over all exponents, and a
-    float64 einsum of independently rounded tiny inputs.
+    float64 einsum of independently rounded tiny inputs; the same three for the
+    BF16-input GEMM (tests/golden/bf16_round.txt, ties to even).
 The same pins run against deliberately broken copies of the oracle in
 test_oracle_mutations.py, which shows that each plausible mistake fails one.
 """
@@ -405,6 +406,16 @@ def pin_ieee_special_values(lib):
     assert oracle.sgemm("N", "N", a, a, c, 1.0, 0.0, lib=lib)[0, 0] == 1.0
 
 
+def _nearer(x, t, u, tie_to_t):
+    """Of the candidates t (toward zero) and u (away from zero) around finite x, the nearer one;
+    a tie goes to u unless tie_to_t.  A u of +-Inf stands for the value 2^128 just past the top of
+    the format (rounding there overflows to +-Inf), so distances use that value."""
+    x64, t64 = x.astype(np.float64), t.astype(np.float64)
+    u64 = np.where(np.isinf(u), np.copysign(2.0 ** 128, x64), u.astype(np.float64))
+    dt, du = np.abs(x64 - t64), np.abs(u64 - x64)
+    return np.where((dt < du) | ((dt == du) & tie_to_t), t, u).astype(np.float32)
+
+
 def _tf32_by_bits(x: np.ndarray) -> np.ndarray:
     """TF32 rounding characterized on the bits, independently of the oracle's arithmetic: the
     candidates are x with its 13 low fraction bits cleared (t, toward zero) and the next TF32
@@ -413,11 +424,8 @@ def _tf32_by_bits(x: np.ndarray) -> np.ndarray:
     x = np.asarray(x, np.float32)
     b = x.view(np.uint32)
     t = (b & np.uint32(0xFFFFE000)).view(np.float32)
-    u = ((b & np.uint32(0xFFFFE000)) + np.uint32(0x2000)).view(np.float32)  # may be +-Inf at the top
-    with np.errstate(over="ignore", invalid="ignore"):
-        dt = np.abs(x.astype(np.float64) - t.astype(np.float64))
-        du = np.abs(u.astype(np.float64) - x.astype(np.float64))
-    return np.where(dt < du, t, u).astype(np.float32)
+    u = ((b & np.uint32(0xFFFFE000)) + np.uint32(0x2000)).view(np.float32)  # +-Inf at the top
+    return _nearer(x, t, u, np.zeros(x.shape, bool))
 
 
 def pin_tf32_round_golden(lib):
@@ -473,11 +481,78 @@ def pin_tf32_gemm(lib):
     assert oracle.sgemm_tf32("N", "N", a, np.ones((1, 1), np.float32), lib=lib)[0, 0] == np.float32(1 + 2.0 ** -10)
 
 
+def _bf16_by_bits(x: np.ndarray) -> np.ndarray:
+    """BF16 rounding characterized on the bits, independently of the oracle's arithmetic: the
+    candidates are x with its 16 low bits cleared (t, toward zero) and the next BF16 value above
+    it in magnitude (t + 2^16 ulps); the result is the nearer one, on a tie the one whose lowest
+    kept bit (bit 16) is 0.  Finite x only."""
+    x = np.asarray(x, np.float32)
+    b = x.view(np.uint32)
+    tb = b & np.uint32(0xFFFF0000)
+    ub = tb + np.uint32(0x10000)  # +-Inf at the top
+    return _nearer(x, tb.view(np.float32), ub.view(np.float32), (tb & np.uint32(0x10000)) == 0)
+
+
+def pin_bf16_round_golden(lib):
+    """The hand-worked BF16 roundings of tests/golden/bf16_round.txt, and NaN stays NaN."""
+    rows = []
+    with open(os.path.join(GOLDEN, "bf16_round.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                x, y = line.split()[:2]
+                rows.append((int(x, 16), int(y, 16)))
+    x = np.array([r[0] for r in rows], np.uint32).view(np.float32)
+    want = np.array([r[1] for r in rows], np.uint32)
+    got = oracle.round_bf16(x, lib).view(np.uint32)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(hex(rows[i][0]), hex(int(got[i])), hex(rows[i][1])) for i in bad]
+    assert np.isnan(oracle.round_bf16(np.array([np.nan, -np.nan], np.float32), lib)).all()
+
+
+def pin_bf16_round_properties(lib):
+    """Finite floats over the whole exponent range (normal and subnormal, both signs): the result
+    is a BF16 value (16 low bits zero, or +-Inf past the top) and equals the bit-level
+    characterization above."""
+    rng = np.random.default_rng(20)
+    bits = rng.integers(0, 1 << 32, size=200000, dtype=np.uint64).astype(np.uint32)
+    # and exact ties: a kept pattern followed by exactly half a quantum
+    ties = (rng.integers(0, 1 << 16, size=20000, dtype=np.uint64).astype(np.uint32) << np.uint32(16)) | np.uint32(0x8000)
+    x = np.concatenate([bits, ties]).view(np.float32)
+    x = x[np.isfinite(x)]
+    got = oracle.round_bf16(x, lib)
+    fin = np.isfinite(got)
+    assert np.all((got[fin].view(np.uint32) & np.uint32(0xFFFF)) == 0)
+    assert np.array_equal(got.view(np.uint32), _bf16_by_bits(x).view(np.uint32))
+
+
+def pin_bf16_gemm(lib):
+    """The BF16-input GEMM: inputs that are already BF16 values give the FP32 oracle's result; on
+    tiny shapes with 12-bit dyadic inputs (which the rounding changes) it equals a float64 einsum
+    of the bit-level-rounded inputs, rounded once (every product and sum exact)."""
+    rng = np.random.default_rng(21)
+    for (ta, tb), M, N, K in itertools.product(OPS, (1, 3, 7), (2, 5), (1, 4, 9)):
+        A = _stored(rng, ta, M, K, dyadic_bits=6)
+        B = _stored(rng, tb, K, N, dyadic_bits=6)
+        C = _stored(rng, "N", M, N, dyadic_bits=6)
+        assert np.array_equal(oracle.sgemm_bf16(ta, tb, A, B, C, 1.5, -0.5, lib=lib),
+                              oracle.sgemm(ta, tb, A, B, C, 1.5, -0.5, lib=lib)), (ta, tb, M, N, K)
+        A = _stored(rng, ta, M, K, dyadic_bits=12)
+        B = _stored(rng, tb, K, N, dyadic_bits=12)
+        ref = (1.5 * np.einsum("ik,kj->ij", _op(_bf16_by_bits(A), ta).astype(np.float64),
+                               _op(_bf16_by_bits(B), tb).astype(np.float64))
+               - 0.5 * C.astype(np.float64)).astype(np.float32)
+        got = oracle.sgemm_bf16(ta, tb, A, B, C, 1.5, -0.5, lib=lib)
+        assert np.array_equal(got, ref), (ta, tb, M, N, K)
+    # the rounding really happens: 1 + 3 * 2^-8 (a tie, to even) times 1 gives 1 + 2^-6
+    a = np.array([[1 + 3 * 2.0 ** -8]], np.float32)
+    assert oracle.sgemm_bf16("N", "N", a, np.ones((1, 1), np.float32), lib=lib)[0, 0] == np.float32(1 + 2.0 ** -6)
+
+
 ALL_PINS = [
     pin_hand_2x2, pin_bruteforce_tiny, pin_integer_pattern, pin_integer_alpha_beta, pin_k1_exact,
     pin_alpha_zero, pin_k_zero, pin_beta_zero_nan_c, pin_identity, pin_transpose_identity,
     pin_transposed_copy, pin_alpha_pow2, pin_padding_not_read, pin_random_vs_float64_matmul,
     pin_bound_magnitude, pin_argument_errors, pin_conjugate_is_transpose, pin_batched_dyadic,
     pin_batched_edges, pin_large_finite_exact, pin_ieee_special_values, pin_tf32_round_golden,
-    pin_tf32_round_properties, pin_tf32_gemm,
+    pin_tf32_round_properties, pin_tf32_gemm, pin_bf16_round_golden, pin_bf16_round_properties, pin_bf16_gemm,
 ]

@@ -45,6 +45,12 @@ MUTATIONS = [
     ("tf32: 11 fraction bits", "int qexp = (e - 1) - 10;", "int qexp = (e - 1) - 11;"),
     ("tf32: no subnormal quantum", "if (qexp < -136) qexp = -136;", "if (qexp < -149) qexp = -149;"),
     ("tf32: sign dropped", "const double y = x < 0.0f ? -r : r;", "const double y = r;"),
+    ("bf16: ties away from zero", "(frac > 0.5 || (frac == 0.5 && fmod(m, 2.0) != 0.0))", "(frac >= 0.5)"),
+    ("bf16: truncation", "if (frac > 0.5 || (frac == 0.5 && fmod(m, 2.0) != 0.0)) m += 1.0;", ""),
+    ("bf16: 8 fraction bits", "int qexp = (e - 1) - 7;", "int qexp = (e - 1) - 8;"),
+    ("bf16: no subnormal quantum", "if (qexp < -133) qexp = -133;", "if (qexp < -149) qexp = -149;"),
+    ("bf16: ties to odd", "fmod(m, 2.0) != 0.0", "fmod(m, 2.0) == 0.0"),
+    ("bf16: sign dropped", "const double y = (x < 0.0f) ? -r : r;", "const double y = r;"),
 ]
 
 _CHILD = r"""
