@@ -110,11 +110,14 @@ enum sgemm_variant {
     SGEMM_VARIANT_TC_TF32 = 11,   /* sgemm_tf32() only: A and B rounded to TF32 once per call (in the
                                       workspace), one tensor-core product per k on CTA pairs, 256x256x32
                                       tiles */
-    SGEMM_VARIANT_TC_SKINNY = 12  /* one short side (M <= 64 or N <= 64), one product: the short operand
+    SGEMM_VARIANT_TC_SKINNY = 12, /* one short side (M <= 64 or N <= 64), one product: the short operand
                                      split once per call into hi / lo arrays (in the workspace), the long
                                      one split in the kernel; 3xTF32 on tiles of 128 along the long side x
                                      64 along the short one (tile_m = 128 and tile_n = 64 name those
                                      sides, whichever of M and N is short) */
+    SGEMM_VARIANT_TC_BF16 = 13    /* sgemm_bf16() only: A and B rounded to BF16 once per call (in the
+                                     workspace), one kind::f16 tensor-core product per 16 k on CTA pairs,
+                                     256x256x64 tiles */
 };
 
 /*
@@ -363,6 +366,38 @@ int sgemm_tf32(char transA, char transB, int64_t M, int64_t N, int64_t K,
 
 /* What sgemm_tf32() would launch (sm_count as in sgemm_plan(); plan == NULL: -15). */
 int sgemm_tf32_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                    float alpha, const float *A, int64_t lda,
+                    const float *B, int64_t ldb,
+                    float beta, const float *C, int64_t ldc,
+                    int sm_count, sgemm_plan_t *plan);
+
+/*
+ * sgemm_bf16 -- as sgemm_tf32, with BF16 inputs: the other tensor-core input
+ * format youngju.dev "CUDA architecture visualized" (テンソルコア) names for
+ * FP32-range data.  Computes
+ *     C = alpha * op(bf16(A)) * op(bf16(B)) + beta * C
+ * where bf16(x) rounds x to 7 explicit significand bits, to nearest with ties
+ * to even (a finite x whose rounding carries past (2 - 2^-7) 2^127 gives
+ * +-Inf; +-Inf and NaN stay), and the products (exact in FP32) are summed in
+ * FP32.  Contract: |C - C_b| <= (K+2) 2^-24 (|alpha| sum|a_b b_b| + |beta c|)
+ * per element against that expression evaluated exactly on the rounded inputs
+ * (C_b): the result differs from sgemm()'s by up to about 2^-8 relative per
+ * product.  Arguments, conventions, ownership, errors and asynchrony as
+ * sgemm(); any alignment.  Each operand is rounded once per call into a
+ * pooled workspace (2 bytes per element of op(A) and op(B), rows padded to a
+ * multiple of 8 values), then CTA pairs compute 256x256 tiles, 64 k per
+ * tile, with tcgen05.mma kind::f16 (SGEMM_VARIANT_TC_BF16).  Needs a device
+ * where clusters of two CTAs can be co-scheduled, and K <= 2097120:
+ * SGEMM_ERR_UNSUPPORTED otherwise.
+ */
+int sgemm_bf16(char transA, char transB, int64_t M, int64_t N, int64_t K,
+               float alpha, const float *A, int64_t lda,
+               const float *B, int64_t ldb,
+               float beta, float *C, int64_t ldc,
+               struct CUstream_st *stream);
+
+/* What sgemm_bf16() would launch (sm_count as in sgemm_plan(); plan == NULL: -15). */
+int sgemm_bf16_plan(char transA, char transB, int64_t M, int64_t N, int64_t K,
                     float alpha, const float *A, int64_t lda,
                     const float *B, int64_t ldb,
                     float beta, const float *C, int64_t ldc,

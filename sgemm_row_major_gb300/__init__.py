@@ -31,7 +31,8 @@ STATUS = {"OK": 0, "ERR_CUDA": 1, "ERR_TIMEOUT": 2, "ERR_NOMEM": 3, "ERR_UNSUPPO
 NOALLOC_SCRATCH_BYTES = 32 << 20  # SGEMM_NOALLOC_SCRATCH_BYTES in include/sgemm.h
 VARIANTS = {"AUTO": 0, "NONE": 1, "SCALE": 2, "GENERIC": 3, "TMA_128x128": 4, "TMA_64x256": 5, "TC_TF32X3": 6,
             "SMALL": 7, "TC_GROUPED": 8, "TC_PAIR": 9,
-            "TC_PRESPLIT": 10, "TC_TF32": 11, "TC_SKINNY": 12}
+            "TC_PRESPLIT": 10, "TC_TF32": 11, "TC_SKINNY": 12,
+            "TC_BF16": 13}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 
 
@@ -85,6 +86,11 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.sgemm_release_workspace.argtypes = [ctypes.c_size_t]
     lib.sgemm_clock_snapshot.restype = ctypes.c_int
     lib.sgemm_clock_snapshot.argtypes = [vp, ctypes.c_int, vp]
+    lib.sgemm_bf16.restype = ctypes.c_int
+    lib.sgemm_bf16.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+    lib.sgemm_bf16_plan.restype = ctypes.c_int
+    lib.sgemm_bf16_plan.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ctypes.c_int,
+                                    ctypes.POINTER(PlanStruct)]
     lib.sgemm_tf32.restype = ctypes.c_int
     lib.sgemm_tf32.argtypes = [ch, ch, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
     lib.sgemm_tf32_plan.restype = ctypes.c_int
@@ -299,6 +305,29 @@ def sgemm_tf32_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc
                                 _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), int(sm_count), ctypes.byref(plan))
     if st != 0:
         raise SgemmError(st, "sgemm_tf32_plan")
+    out = {name: getattr(plan, name) for name, _ in PlanStruct._fields_}
+    out["variant_name"] = VARIANT_NAMES.get(out["variant"], str(out["variant"]))
+    return out
+
+
+def sgemm_bf16(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None, *,
+               raise_on_error: bool = True) -> int:
+    """C = alpha*op(bf16(A))*op(bf16(B)) + beta*C: inputs rounded to BF16 (nearest, ties to even),
+    FP32 accumulation on the tensor cores."""
+    st = load().sgemm_bf16(_ch(transA), _ch(transB), int(M), int(N), int(K), float(alpha), _ptr(A), int(lda),
+                           _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), _stream(stream))
+    if st != 0 and raise_on_error:
+        raise SgemmError(st, "sgemm_bf16")
+    return st
+
+
+def sgemm_bf16_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, sm_count: int = 0) -> dict:
+    """The launch sgemm_bf16() would make.  Raises on invalid arguments."""
+    plan = PlanStruct()
+    st = load().sgemm_bf16_plan(_ch(transA), _ch(transB), int(M), int(N), int(K), float(alpha), _ptr(A), int(lda),
+                                _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), int(sm_count), ctypes.byref(plan))
+    if st != 0:
+        raise SgemmError(st, "sgemm_bf16_plan")
     out = {name: getattr(plan, name) for name, _ in PlanStruct._fields_}
     out["variant_name"] = VARIANT_NAMES.get(out["variant"], str(out["variant"]))
     return out

@@ -615,6 +615,53 @@ int make_tf32_plan(const Problem& pr, int sm_count, int pair_clusters, sgemm_pla
   return SGEMM_OK;
 }
 
+// The BF16-input GEMM (sgemm_bf16): as the TF32-input GEMM, with op(A) and op(B) rounded to BF16
+// (rows of round8(K) two-byte values) and K tiles of 64.
+int64_t bf16_ldk(int64_t K) { return (K + 7) / 8 * 8; }
+
+int make_bf16_plan(const Problem& pr, int sm_count, int pair_clusters, sgemm_plan_t* plan) {
+  const int s = make_tf32_plan(pr, sm_count, pair_clusters, plan);  // shape checks, NONE / SCALE
+  if (s != SGEMM_OK || plan->variant != SGEMM_VARIANT_TC_TF32) return s;
+  const int64_t clusters = std::max(1, pair_clusters > 0 ? pair_clusters : sm_count / 2);
+  const int64_t tiles = ceil_div(pr.M, 256) * ceil_div(pr.N, 256);
+  *plan = sgemm_plan_t{};
+  const int t = plan_stream_k(tiles, ceil_div(pr.K, 64), (int)clusters, plan);
+  if (t != SGEMM_OK) return t;
+  plan->variant = SGEMM_VARIANT_TC_BF16;
+  plan->tile_m = plan->tile_n = 256;
+  plan->tile_k = 64;
+  plan->stages = 6;
+  plan->threads = 320;
+  plan->smem_bytes = 6 * 32768 + 1024;
+  plan->grid_x *= 2;
+  const int64_t ldk = bf16_ldk(pr.K);
+  plan->workspace_bytes = round256(plan->workspace_bytes * 4) + round256(pr.M * ldk * 2) + round256(pr.N * ldk * 2);
+  plan->kernel_launches += 2;  // the rounding passes of A and B
+  return SGEMM_OK;
+}
+
+cudaError_t launch_bf16(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& st, uint8_t* ws,
+                        GemmParams* p, cudaStream_t stream) {
+  const int64_t slot_bytes = plan.split_k > 1 ? 2 * plan.grid_x * (int64_t)(128 * 256 * 4) : 0;
+  const int64_t ldk = bf16_ldk(pr.K);
+  uint8_t* ar = ws + round256(slot_bytes);
+  uint8_t* br = ar + round256(pr.M * ldk * 2);
+  p->ws = slot_bytes > 0 ? reinterpret_cast<float*>(ws) : nullptr;
+  p->za = p->zb = 0;
+  p->repair = 0;
+  cudaError_t e = launch_round_bf16(pr.A, pr.lda, !pr.ta, (int)pr.M, (int)pr.K, ar, ldk, st.sm_count, stream,
+                                    p->fault, p->bounds, p->a_elems, SplitOrder::kFirst);
+  if (e == cudaSuccess)
+    e = launch_round_bf16(pr.B, pr.ldb, pr.tb, (int)pr.N, (int)pr.K, br, ldk, st.sm_count, stream, p->fault,
+                          p->bounds, p->b_elems, SplitOrder::kDependent);
+  CUtensorMap ma, mb;
+  if (e == cudaSuccess) e = encode_bf16_map(ar, pr.K, pr.M, ldk, &ma);
+  if (e == cudaSuccess) e = encode_bf16_map(br, pr.K, pr.N, ldk, &mb);
+  if (e == cudaSuccess) e = launch_bf16_gemm(ma, mb, *p, stream);
+  if (e == cudaSuccess && slot_bytes > 0) e = launch_presplit_fixup(*p, (int)plan.sk_tiles, stream, 64);
+  return e;
+}
+
 cudaError_t launch_tf32(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& st, uint8_t* ws,
                         GemmParams* p, cudaStream_t stream) {
   const int64_t slot_bytes = plan.split_k > 1 ? 2 * plan.grid_x * (int64_t)(128 * 256 * 4) : 0;
@@ -755,7 +802,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   CUtensorMap mapA, mapB;
   if (plan.variant != SGEMM_VARIANT_GENERIC && plan.variant != SGEMM_VARIANT_SMALL &&
       plan.variant != SGEMM_VARIANT_TC_PRESPLIT && plan.variant != SGEMM_VARIANT_TC_TF32 &&
-      plan.variant != SGEMM_VARIANT_TC_SKINNY) {
+      plan.variant != SGEMM_VARIANT_TC_SKINNY && plan.variant != SGEMM_VARIANT_TC_BF16) {
     int box_m, box_n;
     operand_boxes(plan, &box_m, &box_n);
     cudaError_t e = encode_operand_maps(pr.ta, pr.tb, pr.M, pr.N, pr.K, pr.A, pr.lda, pr.stride_a, pr.B, pr.ldb,
@@ -781,6 +828,8 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
     e = launch_presplit(pr, plan, st, static_cast<uint8_t*>(ws ? ws : ext_ws), &p, stream);
   } else if (plan.variant == SGEMM_VARIANT_TC_TF32) {
     e = launch_tf32(pr, plan, st, static_cast<uint8_t*>(ws ? ws : ext_ws), &p, stream);
+  } else if (plan.variant == SGEMM_VARIANT_TC_BF16) {
+    e = launch_bf16(pr, plan, st, static_cast<uint8_t*>(ws ? ws : ext_ws), &p, stream);
   } else if (plan.variant == SGEMM_VARIANT_TC_SKINNY) {
     e = launch_skinny(pr, plan, static_cast<uint8_t*>(ws ? ws : ext_ws), p, st.sm_count, stream);
   } else if (plan.variant == SGEMM_VARIANT_GENERIC) {
@@ -804,7 +853,7 @@ int launch_gemm(const Problem& pr, const sgemm_plan_t& plan, const DeviceState& 
   if (e == cudaSuccess && split > 1 && plan.variant != SGEMM_VARIANT_TC_TF32X3 &&
       plan.variant != SGEMM_VARIANT_TC_GROUPED && plan.variant != SGEMM_VARIANT_TC_PAIR &&
       plan.variant != SGEMM_VARIANT_TC_PRESPLIT && plan.variant != SGEMM_VARIANT_TC_TF32 &&
-      plan.variant != SGEMM_VARIANT_TC_SKINNY)
+      plan.variant != SGEMM_VARIANT_TC_SKINNY && plan.variant != SGEMM_VARIANT_TC_BF16)
     e = launch_splitk_reduce(p, split, stream);
   if (ws) {
     cudaError_t ef = cudaFreeAsync(ws, stream);
@@ -958,6 +1007,41 @@ int sgemm_tf32_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, f
     pair_clusters = st->pair_clusters;
   }
   return make_tf32_plan(pr, sm_count, pair_clusters, plan);
+}
+
+int sgemm_bf16(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+               const float* B, int64_t ldb, float beta, float* C, int64_t ldc, struct CUstream_st* stream) {
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  int dev;
+  DeviceState* st;
+  s = device_state(&dev, &st);
+  if (s != SGEMM_OK) return s;
+  sgemm_plan_t plan;
+  s = make_bf16_plan(pr, st->sm_count, st->pair_clusters, &plan);
+  if (s != SGEMM_OK) return s;
+  return launch_gemm(pr, plan, *st, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_bf16_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                    int64_t lda, const float* B, int64_t ldb, float beta, const float* C, int64_t ldc, int sm_count,
+                    sgemm_plan_t* plan) {
+  if (!plan) return -15;
+  Problem pr;
+  int s = validate(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &pr);
+  if (s != SGEMM_OK) return s;
+  int pair_clusters = -1;
+  if (sm_count <= 0) {
+    int dev;
+    DeviceState* st;
+    s = device_state(&dev, &st);
+    if (s != SGEMM_OK) return s;
+    sm_count = st->sm_count;
+    pair_clusters = st->pair_clusters;
+  }
+  return make_bf16_plan(pr, sm_count, pair_clusters, plan);
 }
 
 int sgemm_strided_batched(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,

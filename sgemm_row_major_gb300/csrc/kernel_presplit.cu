@@ -45,6 +45,8 @@
 // quarter warp % 4, columns 128 * ((warp - 2) / 4) .. +127) and epilogue.
 #include <algorithm>
 
+#include <cuda_bf16.h>
+
 #include "kernel_tc_common.cuh"
 
 namespace sgemm_impl {
@@ -70,6 +72,23 @@ __device__ __forceinline__ void split_one(float x, float& hi, float& lo) {
 // it as +-Inf (with the add-and-mask, or as stored).  Every NaN becomes a quiet NaN with all
 // payload bits set.  (With the lo part as well, lo = NaN carries it.)
 __device__ __forceinline__ float keep_nan(float x, float hi) { return x != x ? __uint_as_float(0x7FFFFFFFu) : hi; }
+
+// Stores of the hi part.  float: the TF32 hi of x (3xTF32, with lo) or its NaN-keeping form (hi
+// only); __nv_bfloat16 (the BF16-input GEMM, hi only, lo == nullptr): x rounded to BF16, to
+// nearest even (cvt.rn.bf16.f32: NaN stays NaN, a rounding past the largest BF16 value gives Inf).
+__device__ __forceinline__ void store_hi(float* h, float x, float xh, bool with_lo) { *h = with_lo ? xh : keep_nan(x, xh); }
+__device__ __forceinline__ void store_hi(__nv_bfloat16* h, float x, float, bool) { *h = __float2bfloat16_rn(x); }
+__device__ __forceinline__ void store_hi4(float* h, float4 x, float4 xh, bool with_lo) {
+  if (!with_lo) xh = make_float4(keep_nan(x.x, xh.x), keep_nan(x.y, xh.y), keep_nan(x.z, xh.z), keep_nan(x.w, xh.w));
+  *reinterpret_cast<float4*>(h) = xh;
+}
+__device__ __forceinline__ void store_hi4(__nv_bfloat16* h, float4 x, float4, bool) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y), b = __floats2bfloat162_rn(x.z, x.w);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&a);
+  u.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(h) = u;  // 8-byte aligned: row strides are multiples of 8 elements
+}
 
 // Rows run along K: each thread takes 4 consecutive k (16-byte stores; 16-byte loads when
 // VEC -- every source row 16-byte aligned -- else four 4-byte loads; K % 4 == 0 is not
@@ -98,9 +117,9 @@ __device__ __forceinline__ void split_pass_begin(bool trigger) {
 }
 __device__ __forceinline__ void split_pass_end() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-template <bool VEC>
+template <bool VEC, typename OutT>
 __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict__ src, int64_t ld, int64_t stride,
-                                                         int rows, int K, int products, float* __restrict__ hi,
+                                                         int rows, int K, int products, OutT* __restrict__ hi,
                                                          float* __restrict__ lo, int64_t ldk, const SplitChk chk,
                                                          bool trigger) {
   split_pass_begin(trigger);
@@ -113,22 +132,18 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict
     const int64_t so = p * stride + r * ld + 4 * k4;
     if (!chk.src(so, min(4, K - 4 * k4)) || !chk.dst(pr * ldk + 4 * k4, 4)) continue;
     const float* s = src + so;
-    float* h = hi + pr * ldk + 4 * k4;
+    OutT* h = hi + pr * ldk + 4 * k4;
     if (4 * k4 + 3 < K) {
       const float4 x = VEC ? *reinterpret_cast<const float4*>(s) : make_float4(s[0], s[1], s[2], s[3]);
       float4 xh, xl;
       split4(x, xh, xl);
-      if (lo) {
-        *reinterpret_cast<float4*>(lo + pr * ldk + 4 * k4) = xl;
-      } else {
-        xh = make_float4(keep_nan(x.x, xh.x), keep_nan(x.y, xh.y), keep_nan(x.z, xh.z), keep_nan(x.w, xh.w));
-      }
-      *reinterpret_cast<float4*>(h) = xh;
+      if (lo) *reinterpret_cast<float4*>(lo + pr * ldk + 4 * k4) = xl;
+      store_hi4(h, x, xh, lo != nullptr);
     } else {
       for (int j = 0; j < K - 4 * k4; ++j) {
         float xh, xl;
         split_one(s[j], xh, xl);
-        h[j] = lo ? xh : keep_nan(s[j], xh);
+        store_hi(h + j, s[j], xh, lo != nullptr);
         if (lo) lo[pr * ldk + 4 * k4 + j] = xl;
       }
     }
@@ -138,9 +153,10 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict
 
 // Stored rows run along the other axis: a 32 x 32 block per CTA (32 x 8 threads), read along
 // the stored rows (any alignment), written along K; lo == nullptr: hi only.
+template <typename OutT>
 __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __restrict__ src, int64_t ld,
                                                               int64_t stride, int rows, int K,
-                                                              float* __restrict__ hi, float* __restrict__ lo,
+                                                              OutT* __restrict__ hi, float* __restrict__ lo,
                                                               int64_t ldk, const SplitChk chk, bool trigger) {
   split_pass_begin(trigger);
   __shared__ float tile[kSplitTile][kSplitTile + 1];
@@ -156,7 +172,7 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __res
   }
   __syncthreads();
   // write: row r = r0 + ty + 8j, k = k0 + tx
-  float* h = hi + (int64_t)p * rows * ldk;
+  OutT* h = hi + (int64_t)p * rows * ldk;
   float* l = lo ? lo + (int64_t)p * rows * ldk : nullptr;
   for (int j = 0; j < kSplitTile; j += 8) {
     const int r = r0 + (int)threadIdx.y + j, k = k0 + (int)threadIdx.x;
@@ -164,7 +180,7 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __res
       const float x = tile[threadIdx.x][threadIdx.y + j];
       float xh, xl;
       split_one(x, xh, xl);
-      h[(int64_t)r * ldk + k] = lo ? xh : keep_nan(x, xh);
+      store_hi(h + (int64_t)r * ldk + k, x, xh, lo != nullptr);
       if (lo) l[(int64_t)r * ldk + k] = xl;
     }
   }
@@ -211,6 +227,11 @@ static_assert(kAccBufs * kAccCols <= kTmemCols, "accumulators must fit in TMEM")
 constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
                             ((uint32_t)(BM >> 4) << 24);
 
+// ... and kind::f16 with BF16 A and B (the BF16-input GEMM): FP32 accumulator, both K-major,
+// N = 256, M = 256; K = 16 per MMA, the same 32 bytes of a K-major row as 8 TF32 values.
+constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                ((uint32_t)(BM >> 4) << 24);
+
 // D (both CTAs' TMEM) = or += A (128 rows in each CTA's shared memory) * B (128 columns in each
 // CTA's shared memory); both operands K-major, described by the same descriptors in both CTAs.
 __device__ __forceinline__ void mma_pair_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
@@ -219,6 +240,16 @@ __device__ __forceinline__ void mma_pair_ss(uint32_t d_tmem, uint64_t adesc, uin
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_pair_ss_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdescBf16), "r"(accumulate)
       : "memory");
 }
 
@@ -268,7 +299,9 @@ __device__ __forceinline__ void store_row(const GemmParams& p, int64_t roff, int
   }
 }
 
-template <int PARTS>
+// BF16 (with PARTS == 1): the split arrays hold BF16 values, 64 per 128-byte row of a tile, so a
+// K tile is 64 deep and its 4 k-steps are kind::f16 MMAs of K = 16.
+template <int PARTS, bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     presplit_gemm_kernel(const __grid_constant__ CUtensorMap mapAh, const __grid_constant__ CUtensorMap mapAl,
                          const __grid_constant__ CUtensorMap mapBh, const __grid_constant__ CUtensorMap mapBl,
@@ -293,7 +326,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const int cl = (int)cluster_id_x();
-  const int kt_total = (p.K + BK - 1) / BK;
+  constexpr int kKTile = BF16 ? 2 * BK : BK;  // K elements per K tile (one 128-byte row of a tile)
+  static_assert(!BF16 || PARTS == 1, "the BF16-input GEMM has one part per operand");
+  const int kt_total = (p.K + kKTile - 1) / kKTile;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
@@ -343,7 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const int k0 = kt * BK;
+          const int k0 = kt * kKTile;
           // both CTAs' loads complete on the even CTA's barrier, which expects all their bytes
           // (measured: 270.1 TFLOPS at 4096^3, 268.3 with the odd CTA's completions relayed by a
           // thread's remote arrive)
@@ -407,6 +442,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mma_pair_ss(acc, alo + step, bhi + step, fresh);
                 mma_pair_ss(acc, ahi + step, blo + step, 1u);
                 mma_pair_ss(acc, ahi + step, bhi + step, 1u);
+              } else if (BF16) {
+                mma_pair_ss_bf16(acc, ahi + step, bhi + step, fresh);
               } else {
                 mma_pair_ss(acc, ahi + step, bhi + step, fresh);
               }
@@ -526,11 +563,11 @@ constexpr int kFixupRowsPerCta = 8;
 constexpr int kFixupThreads = 256;
 constexpr int kMaxSharers = 256;
 template <bool CVEC>
-__global__ void __launch_bounds__(kFixupThreads) presplit_fixup_kernel(const GemmParams p) {
+__global__ void __launch_bounds__(kFixupThreads) presplit_fixup_kernel(const GemmParams p, int k_tile) {
   __shared__ int s_n;
   __shared__ int s_slot[kMaxSharers];
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int kt = (p.K + BK - 1) / BK;
+  const int kt = (p.K + k_tile - 1) / k_tile;  // the GEMM's K tiles (32, or 64 for BF16 inputs)
   const int j = (int)blockIdx.x >> 1, r = (int)blockIdx.x & 1;
   if (threadIdx.x == 0) {
     const int64_t i0 = (int64_t)j * kt;
@@ -589,17 +626,22 @@ __global__ void __launch_bounds__(kFixupThreads) presplit_fixup_kernel(const Gem
 }  // namespace tps
 
 cudaError_t prepare_presplit() {
-  cudaError_t e = cudaFuncSetAttribute(tps::presplit_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(tps::presplit_gemm_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        tps::Cfg<2>::kSmemBytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tps::presplit_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tps::presplit_gemm_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tps::Cfg<1>::kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tps::presplit_gemm_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              tps::Cfg<1>::kSmemBytes);
   return e;
 }
 
-cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, bool k_contig, int rows, int K,
-                                 int products, float* hi, float* lo, int64_t ldk, int sm_count, cudaStream_t stream,
-                                 unsigned* fault, unsigned long long* bounds, int64_t src_elems, SplitOrder order) {
+namespace {
+template <typename OutT>
+cudaError_t launch_split_pass(const float* src, int64_t ld, int64_t stride, bool k_contig, int rows, int K,
+                              int products, OutT* hi, float* lo, int64_t ldk, int sm_count, cudaStream_t stream,
+                              unsigned* fault, unsigned long long* bounds, int64_t src_elems, SplitOrder order) {
   if (rows <= 0 || K <= 0 || products <= 0) return cudaSuccess;
   const tps::SplitChk chk{fault, bounds, src_elems, (int64_t)products * rows * ldk};
   cudaLaunchConfig_t cfg = {};
@@ -615,21 +657,37 @@ cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, b
     cfg.gridDim = dim3((unsigned)std::max<int64_t>(std::min<int64_t>((work + 255) / 256, (int64_t)sm_count * 8), 1));
     cfg.blockDim = dim3(256);
     const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && ld % 4 == 0 && (products == 1 || stride % 4 == 0);
-    return vec ? cudaLaunchKernelEx(&cfg, tps::split_rows_kernel<true>, src, ld, stride, rows, K, products, hi, lo, ldk,
-                                    chk, trigger)
-               : cudaLaunchKernelEx(&cfg, tps::split_rows_kernel<false>, src, ld, stride, rows, K, products, hi, lo,
-                                    ldk, chk, trigger);
+    return vec ? cudaLaunchKernelEx(&cfg, tps::split_rows_kernel<true, OutT>, src, ld, stride, rows, K, products, hi,
+                                    lo, ldk, chk, trigger)
+               : cudaLaunchKernelEx(&cfg, tps::split_rows_kernel<false, OutT>, src, ld, stride, rows, K, products, hi,
+                                    lo, ldk, chk, trigger);
   }
   cfg.gridDim = dim3((unsigned)((rows + tps::kSplitTile - 1) / tps::kSplitTile),
                      (unsigned)((K + tps::kSplitTile - 1) / tps::kSplitTile), (unsigned)products);
   cfg.blockDim = dim3(tps::kSplitTile, 8);
-  return cudaLaunchKernelEx(&cfg, tps::split_transpose_kernel, src, ld, stride, rows, K, hi, lo, ldk, chk, trigger);
+  return cudaLaunchKernelEx(&cfg, tps::split_transpose_kernel<OutT>, src, ld, stride, rows, K, hi, lo, ldk, chk,
+                            trigger);
+}
+}  // namespace
+
+cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, bool k_contig, int rows, int K,
+                                 int products, float* hi, float* lo, int64_t ldk, int sm_count, cudaStream_t stream,
+                                 unsigned* fault, unsigned long long* bounds, int64_t src_elems, SplitOrder order) {
+  return launch_split_pass<float>(src, ld, stride, k_contig, rows, K, products, hi, lo, ldk, sm_count, stream, fault,
+                                  bounds, src_elems, order);
+}
+
+cudaError_t launch_round_bf16(const float* src, int64_t ld, bool k_contig, int rows, int K, void* out, int64_t ldk,
+                              int sm_count, cudaStream_t stream, unsigned* fault, unsigned long long* bounds,
+                              int64_t src_elems, SplitOrder order) {
+  return launch_split_pass<__nv_bfloat16>(src, ld, 0, k_contig, rows, K, 1, static_cast<__nv_bfloat16*>(out),
+                                          nullptr, ldk, sm_count, stream, fault, bounds, src_elems, order);
 }
 
 namespace {
 // The GEMM after the split passes: a programmatic dependent launch (its prologue overlaps the
 // last pass; its producer waits for that pass before the first load).
-template <int PARTS>
+template <int PARTS, bool BF16>
 cudaError_t launch_gemm_after_split(const CUtensorMap& mapAh, const CUtensorMap& mapAl, const CUtensorMap& mapBh,
                                     const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -642,22 +700,27 @@ cudaError_t launch_gemm_after_split(const CUtensorMap& mapAh, const CUtensorMap&
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tps::presplit_gemm_kernel<PARTS>, mapAh, mapAl, mapBh, mapBl, p);
+  return cudaLaunchKernelEx(&cfg, tps::presplit_gemm_kernel<PARTS, BF16>, mapAh, mapAl, mapBh, mapBl, p);
 }
 }  // namespace
 
 cudaError_t launch_presplit_gemm(const CUtensorMap& mapAh, const CUtensorMap& mapAl, const CUtensorMap& mapBh,
                                  const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream) {
-  return launch_gemm_after_split<2>(mapAh, mapAl, mapBh, mapBl, p, stream);
+  return launch_gemm_after_split<2, false>(mapAh, mapAl, mapBh, mapBl, p, stream);
 }
 
 cudaError_t launch_tf32_gemm(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
                              cudaStream_t stream) {
   // (the lo maps are not read with one part)
-  return launch_gemm_after_split<1>(mapA, mapA, mapB, mapB, p, stream);
+  return launch_gemm_after_split<1, false>(mapA, mapA, mapB, mapB, p, stream);
 }
 
-cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream) {
+cudaError_t launch_bf16_gemm(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
+                             cudaStream_t stream) {
+  return launch_gemm_after_split<1, true>(mapA, mapA, mapB, mapB, p, stream);
+}
+
+cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream, int k_tile) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2u * (unsigned)sk_tiles, tps::BMC / tps::kFixupRowsPerCta);
   cfg.blockDim = dim3(tps::kFixupThreads);
@@ -668,8 +731,8 @@ cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return p.c_vec ? cudaLaunchKernelEx(&cfg, tps::presplit_fixup_kernel<true>, p)
-                 : cudaLaunchKernelEx(&cfg, tps::presplit_fixup_kernel<false>, p);
+  return p.c_vec ? cudaLaunchKernelEx(&cfg, tps::presplit_fixup_kernel<true>, p, k_tile)
+                 : cudaLaunchKernelEx(&cfg, tps::presplit_fixup_kernel<false>, p, k_tile);
 }
 
 }  // namespace sgemm_impl

@@ -78,7 +78,7 @@ cudaError_t encode_operand_maps(bool ta, bool tb, int64_t M, int64_t N, int64_t 
 // variants); the pair kernel's scheduling unit is the cluster of 2 CTAs.
 inline void set_schedule(const sgemm_plan_t& plan, GemmParams* p) {
   const bool pairs = plan.variant == SGEMM_VARIANT_TC_PAIR || plan.variant == SGEMM_VARIANT_TC_PRESPLIT ||
-                     plan.variant == SGEMM_VARIANT_TC_TF32;
+                     plan.variant == SGEMM_VARIANT_TC_TF32 || plan.variant == SGEMM_VARIANT_TC_BF16;
   if (plan.variant != SGEMM_VARIANT_TC_TF32X3 && plan.variant != SGEMM_VARIANT_TC_GROUPED &&
       plan.variant != SGEMM_VARIANT_TC_SKINNY && !pairs)
     return;
@@ -173,12 +173,22 @@ cudaError_t launch_split_operand(const float* src, int64_t ld, int64_t stride, b
                                  int64_t src_elems = 0, SplitOrder order = SplitOrder::kAlone);
 cudaError_t launch_presplit_gemm(const CUtensorMap& mapAh, const CUtensorMap& mapAl, const CUtensorMap& mapBh,
                                  const CUtensorMap& mapBl, const GemmParams& p, cudaStream_t stream);
-cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream);
+cudaError_t launch_presplit_fixup(const GemmParams& p, int sk_tiles, cudaStream_t stream, int k_tile = 32);
 // The TF32-input GEMM: the same CTA-pair kernel with one part per operand (maps over the rounded
 // copies, written by launch_split_operand with lo == nullptr) and one tensor-core product per k;
 // its stream-K tiles go through launch_presplit_fixup (p.repair = 0).
 cudaError_t launch_tf32_gemm(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
                              cudaStream_t stream);
+// The BF16-input GEMM: the same CTA-pair kernel over maps of BF16 arrays (64 K per tile, kind::f16
+// MMAs), written by launch_round_bf16 (out: rows of ldk BF16 values, ldk a multiple of 8); its
+// stream-K tiles go through launch_presplit_fixup with k_tile = 64.
+cudaError_t launch_bf16_gemm(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
+                             cudaStream_t stream);
+cudaError_t launch_round_bf16(const float* src, int64_t ld, bool k_contig, int rows, int K, void* out, int64_t ldk,
+                              int sm_count, cudaStream_t stream, unsigned* fault, unsigned long long* bounds,
+                              int64_t src_elems, SplitOrder order);
+// Map over a BF16 array of `rows` rows of K values (row stride ldk elements): box {64, 128, 1}, 128-byte swizzle.
+cudaError_t encode_bf16_map(const void* base, int64_t K, int64_t rows, int64_t ldk, CUtensorMap* map);
 // sgemm_plan() for a caller that cannot provide the split arrays of TC_PRESPLIT
 // (sgemm_noalloc): that variant, chosen or forced by override, is planned as TC_PAIR.
 // pair_clusters as in sgemm_plan_for_device().

@@ -76,6 +76,22 @@ cudaError_t encode_split_map(const float* base, int64_t K, int64_t rows, int64_t
   return encode_3d(base, K, rows, ldk, products, rows * ldk, 32, box_rows, true, map);
 }
 
+cudaError_t encode_bf16_map(const void* base, int64_t K, int64_t rows, int64_t ldk, CUtensorMap* map) {
+  cudaError_t e = bind_primary_context();
+  if (e != cudaSuccess) return e;
+  EncodeTiledFn fn = nullptr;
+  e = encode_fn(&fn);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, 1};
+  const cuuint64_t strides[2] = {(cuuint64_t)ldk * 2u, (cuuint64_t)(rows * ldk) * 2u};
+  const cuuint32_t box[3] = {64u, 128u, 1u};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t encode_matrix_map(const float* base, int64_t inner, int64_t outer, int64_t ld, int box_inner,
                               int box_outer, CUtensorMap* map) {
   cudaError_t e = bind_primary_context();

@@ -505,6 +505,28 @@ def test_tf32_planner(lib):
     assert ei.value.status == sg.STATUS["ERR_UNSUPPORTED"]
 
 
+def test_bf16_planner(lib):
+    """sgemm_bf16: BF16 copies of op(A) and op(B) (rows of round8(K) two-byte values) after the
+    stream-K slots, two rounding passes, the CTA-pair GEMM on 64-deep K tiles, the fixup when tiles
+    are shared; any alignment; the same shape limits as sgemm_tf32."""
+    def r256(x):
+        return (x + 255) // 256 * 256
+    p = sg.sgemm_bf16_plan("N", "N", 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, 0.0, FAKE, 4096, 152)
+    assert (p["variant_name"], p["tile_m"], p["tile_n"], p["tile_k"], p["grid_x"], p["stages"]) == \
+        ("TC_BF16", 256, 256, 64, 152, 6)
+    slots = 2 * 152 * 128 * 256 * 4 if p["split_k"] > 1 else 0
+    assert p["workspace_bytes"] == r256(slots) + 2 * 4096 * 4096 * 2
+    assert p["kernel_launches"] == (4 if p["split_k"] > 1 else 3)
+    q = sg.sgemm_bf16_plan("T", "N", 333, 277, 501, 1.0, FAKE_ODD, 335, FAKE_ODD, 279, 0.0, FAKE, 277, 152)
+    assert q["variant_name"] == "TC_BF16"
+    assert q["workspace_bytes"] % 256 == 0 and q["workspace_bytes"] >= r256(333 * 504 * 2) + r256(277 * 504 * 2)
+    assert sg.sgemm_bf16_plan("N", "N", 64, 64, 0, 1.0, FAKE, 1, FAKE, 64, 0.0, FAKE, 64, 152)["variant_name"] == "SCALE"
+    assert sg.sgemm_bf16_plan("N", "N", 0, 64, 64, 1.0, FAKE, 64, FAKE, 64, 0.0, FAKE, 64, 152)["variant_name"] == "NONE"
+    with pytest.raises(sg.SgemmError) as ei:
+        sg.sgemm_bf16_plan("N", "N", 64, 64, 32 * 65536, 1.0, FAKE, 32 * 65536, FAKE, 64, 0.0, FAKE, 64, 152)
+    assert ei.value.status == sg.STATUS["ERR_UNSUPPORTED"]
+
+
 def test_debug_library_exports_every_declared_symbol():
     """libsgemm_debug.so (the bounds-checking build) exports the same entry points and reports
     itself; libsgemm.so has the checks compiled out."""

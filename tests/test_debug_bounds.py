@@ -101,7 +101,7 @@ def test_variants_clean_and_exact(dbg, variant, split, ops):
 @pytest.mark.parametrize("ops", ["NN", "TT"])
 def test_unaligned_and_tf32_clean(dbg, ops):
     """Operands one float off alignment with odd leading dimensions (generic kernel and the
-    split-operand kernel's any-alignment split pass), and the TF32-input entry point."""
+    split-operand kernel's any-alignment split pass), and the TF32- and BF16-input entry points."""
     ta, tb = ops
     rng = np.random.default_rng(5)
     for M, N, K in [(203, 157, 301), (700, 650, 1203)]:
@@ -114,6 +114,8 @@ def test_unaligned_and_tf32_clean(dbg, ops):
         assert np.array_equal(got, oracle.sgemm(ta, tb, A[:, :ac], B[:, :bc], C, 1.0, 1.0, M=M, N=N, K=K))
         got = run(dbg, ta, tb, M, N, K, 1.0, A, ac + 3, B, bc + 1, 1.0, C, N, offset=1, entry="sgemm_tf32")
         assert np.array_equal(got, oracle.sgemm_tf32(ta, tb, A[:, :ac], B[:, :bc], C, 1.0, 1.0, M=M, N=N, K=K))
+        got = run(dbg, ta, tb, M, N, K, 1.0, A, ac + 3, B, bc + 1, 1.0, C, N, offset=1, entry="sgemm_bf16")
+        assert np.array_equal(got, oracle.sgemm_bf16(ta, tb, A[:, :ac], B[:, :bc], C, 1.0, 1.0, M=M, N=N, K=K))
 
 
 def test_noalloc_and_scale_clean(dbg):
