@@ -46,6 +46,10 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 # dense tensor-core peaks (PFLOP/s, nominal) used to scale the measured bf16 peak to tf32
 NOMINAL_BF16_PF, NOMINAL_TF32_PF = 2.25, 1.1
 TF32_PRODUCTS = 3  # tensor-core products per useful FMA in the 3xTF32 split
+# entry points bench.py can time: (library function, plan function, oracle function, dtype)
+ENTRIES = {"sgemm": ("sgemm", "sgemm_plan", "sgemm", "f32"),
+           "tf32": ("sgemm_tf32", "sgemm_tf32_plan", "sgemm_tf32", "tf32 inputs, f32 accumulation"),
+           "bf16": ("sgemm_bf16", "sgemm_bf16_plan", "sgemm_bf16", "bf16 inputs, f32 accumulation")}
 
 
 def parse_args():
@@ -64,6 +68,9 @@ def parse_args():
     ap.add_argument("--split", type=int, default=0,
                     help="planner override of the K split (0 = planner's choice; with the tensor-core kernel, "
                          "1 = one CTA per output tile, hardware-scheduled)")
+    ap.add_argument("--entry", choices=list(ENTRIES), default="sgemm",
+                    help="entry point timed: sgemm (the FP32 contract) or the reduced-precision-input GEMMs "
+                         "sgemm_tf32 / sgemm_bf16 (inputs rounded to TF32 / BF16, FP32 accumulation)")
     ap.add_argument("--no-cublas-context", action="store_true",
                     help="skip the cuBLAS FP32 context number (torch.matmul, TF32 off)")
     return ap.parse_args()
@@ -161,23 +168,24 @@ def measured_peaks():
         return {}
 
 
-def oracle_sample_run(case, d, rows):
-    """Oracle on `rows` of C; returns seconds."""
+def oracle_sample_run(case, d, rows, entry="sgemm"):
+    """Oracle (the entry point's oracle function) on `rows` of C; returns seconds."""
     import oracle
+    fn = getattr(oracle, ENTRIES[entry][2])
     from_rows = np.asarray(rows, dtype=np.int64)
     A = d["A"][:, :(case.M if case.transA == "T" else case.K)]
     A = np.ascontiguousarray(A[:, from_rows] if case.transA == "T" else A[from_rows, :])
     B = d["B"][:, :(case.K if case.transB == "T" else case.N)]
     C = np.ascontiguousarray(d["C"][from_rows, :case.N])
     t0 = time.perf_counter()
-    oracle.sgemm(case.transA, case.transB, A, B, C, case.alpha, case.beta, M=len(from_rows), N=case.N, K=case.K)
+    fn(case.transA, case.transB, A, B, C, case.alpha, case.beta, M=len(from_rows), N=case.N, K=case.K)
     return time.perf_counter() - t0
 
 
-def cpu_rows_for(case, d, seconds: float):
+def cpu_rows_for(case, d, seconds: float, entry="sgemm"):
     """Rows of C whose oracle run takes about `seconds` (calibrated on a few rows)."""
     probe = list(range(min(4, case.M)))
-    t = max(oracle_sample_run(case, d, probe), 1e-4)
+    t = max(oracle_sample_run(case, d, probe, entry), 1e-4)
     n = int(max(1, min(case.M, round(len(probe) * seconds / t))))
     return list(range(n))
 
@@ -192,11 +200,11 @@ def cpu_model():
     return os.uname().machine
 
 
-def cpu_baseline(case, d, seconds):
+def cpu_baseline(case, d, seconds, entry="sgemm"):
     import oracle
     cores = oracle.num_threads()
-    rows = cpu_rows_for(case, d, seconds)
-    t = oracle_sample_run(case, d, rows)
+    rows = cpu_rows_for(case, d, seconds, entry)
+    t = oracle_sample_run(case, d, rows, entry)
     flops = si.flops(len(rows), case.N, case.K)
     out = {"value": flops / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
            "sample": f"{len(rows)} of {case.M} rows of C ({len(rows)}x{case.N}x{case.K}, "
@@ -205,8 +213,8 @@ def cpu_baseline(case, d, seconds):
     # the same oracle on one core, for a per-core figure
     oracle.set_num_threads(1)
     try:
-        rows1 = cpu_rows_for(case, d, min(3.0, seconds / 4))
-        t1 = oracle_sample_run(case, d, rows1)
+        rows1 = cpu_rows_for(case, d, min(3.0, seconds / 4), entry)
+        t1 = oracle_sample_run(case, d, rows1, entry)
         out["per_core"] = {"value": si.flops(len(rows1), case.N, case.K) / t1 / 1e12, "unit": UNIT,
                            "sample": f"{len(rows1)} rows in {t1:.2f} s on 1 thread"}
     finally:
@@ -262,26 +270,31 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def config_block(case, n_gpus):
-    return {"workload": f"sgemm_{case.transA}{case.transB}_{case.M}x{case.N}x{case.K}",
-            "name": case.name, "M": case.M, "N": case.N, "K": case.K, "ops": case.ops,
-            "alpha": case.alpha, "beta": case.beta, "inputs": case.dist, "layout": "row-major fp32",
-            "parallelism": f"replicas x{n_gpus}"}
+def config_block(case, n_gpus, entry=None):
+    """The workload; `entry` names a reduced-precision-input entry point when that is what runs."""
+    out = {"workload": f"sgemm_{case.transA}{case.transB}_{case.M}x{case.N}x{case.K}",
+           "name": case.name, "M": case.M, "N": case.N, "K": case.K, "ops": case.ops,
+           "alpha": case.alpha, "beta": case.beta, "inputs": case.dist, "layout": "row-major fp32",
+           "parallelism": f"replicas x{n_gpus}"}
+    if entry:
+        out["entry"] = entry
+    return out
 
 
 # ---------------------------------------------------------------- our arm
 
-def cublas_context(case, sets, steps, stream):
-    """cuBLAS FP32 SGEMM through torch.matmul with TF32 disabled, same shapes, as a context number.
-
-    Computes alpha*op(A)@op(B) + beta*C with torch.addmm into a preallocated
-    output; not part of the measured path.
+def cublas_context(case, sets, steps, stream, entry="sgemm"):
+    """cuBLAS through torch.addmm on the same shapes and input sets, as a context number: FP32
+    SGEMM with TF32 disabled (entry "sgemm"); with TF32 enabled (entry "tf32"); or on inputs cast
+    to BF16 inside the timed region, BF16 output (entry "bf16").  Computes
+    alpha*op(A)@op(B) + beta*C into a preallocated output; not part of the measured path.
     """
     import torch
     prev = torch.backends.cuda.matmul.allow_tf32
-    torch.backends.cuda.matmul.allow_tf32 = False
+    torch.backends.cuda.matmul.allow_tf32 = entry == "tf32"
     try:
-        outs = [torch.empty_like(s[2][:, :case.N]) for s in sets]
+        dt = torch.bfloat16 if entry == "bf16" else torch.float32
+        outs = [torch.empty(case.M, case.N, dtype=dt, device=s[2].device) for s in sets]
 
         def one(i):
             A, B, C = sets[i & 1]
@@ -289,7 +302,10 @@ def cublas_context(case, sets, steps, stream):
             b = B[:, :(case.K if case.transB == "T" else case.N)]
             a = a.t() if case.transA == "T" else a
             b = b.t() if case.transB == "T" else b
-            torch.addmm(C[:, :case.N], a, b, beta=case.beta, alpha=case.alpha, out=outs[i & 1])
+            c = C[:, :case.N]
+            if entry == "bf16":
+                a, b, c = a.to(dt), b.to(dt), c.to(dt)
+            torch.addmm(c, a, b, beta=case.beta, alpha=case.alpha, out=outs[i & 1])
 
         for i in range(5):
             one(i)
@@ -301,8 +317,11 @@ def cublas_context(case, sets, steps, stream):
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
+        what = {"sgemm": "cuBLAS FP32 via torch.addmm, allow_tf32=False",
+                "tf32": "cuBLAS TF32 via torch.addmm, allow_tf32=True",
+                "bf16": "cuBLAS BF16 via torch.addmm on A, B, C cast to BF16 in the timed region, BF16 output"}[entry]
         return {"value": si.flops(case.M, case.N, case.K) / (ms * 1e-3) / 1e12, "unit": UNIT,
-                "what": "cuBLAS FP32 via torch.addmm, allow_tf32=False, same shapes and input sets; context only"}
+                "what": what + ", same shapes and input sets; context only"}
     finally:
         torch.backends.cuda.matmul.allow_tf32 = prev
 
@@ -478,6 +497,27 @@ def tensor_roofline(achieved, peaks, traffic, kernel_ms, variant="TC_TF32X3"):
                                  "the fixup kernel after it")}
 
 
+def reduced_roofline(achieved, peaks, variant, kernel_ms, traffic):
+    """Roofline object of the reduced-precision-input GEMMs (one tensor-core product per term):
+    the measured bf16 peak for BF16 inputs, that peak x the nominal tf32/bf16 ratio for TF32."""
+    bf16 = peaks.get("bf16_tflops")
+    basis = "measured" if bf16 else "fallback"
+    bf16 = bf16 or 1900.0
+    bf = variant == "TC_BF16"
+    peak = bf16 if bf else bf16 * NOMINAL_TF32_PF / NOMINAL_BF16_PF
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": traffic,
+            "peak_basis": f"{basis} bf16 burst {bf16:.0f} TFLOP/s" +
+                          ("" if bf else f" x nominal tf32/bf16 {NOMINAL_TF32_PF}/{NOMINAL_BF16_PF}") +
+                          "; one tensor-core product per term; achieved counts 2MNK only",
+            "kernel": ("presplit_gemm_kernel<1, BF16> (tcgen05.mma cta_group::2 kind::f16, 256x256 tiles, 64-deep K "
+                       "tiles)" if bf else "presplit_gemm_kernel<1> (tcgen05.mma cta_group::2 kind::tf32, 256x256 "
+                       "tiles)") + " after the rounding passes of A and B",
+            "kernel_ms": kernel_ms,
+            "kernel_ms_covers": "one call: the rounding passes of A and B, the GEMM kernel and, when stream-K "
+                                "tiles are shared, the fixup kernel"}
+
+
 def hbm_bound_roofline(roof, nbytes, flops_step, kernel_ms, peaks):
     """Switches a tensor-core roofline to the HBM roof when the call's algorithmic bytes take longer
     at the measured HBM bandwidth than its FLOPs at the tensor peak (the tensor figures stay
@@ -524,13 +564,14 @@ def run_ours(args):
         sets.append(tuple(torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C")))
     torch.cuda.synchronize(dev)
 
-    plan = sg.sgemm_plan(case.transA, case.transB, M, N, K, case.alpha, sets[0][0], d["lda"], sets[0][1],
-                         d["ldb"], case.beta, sets[0][2], d["ldc"])
+    lib_fn, plan_fn, _, dtype = ENTRIES[args.entry]
+    call = getattr(sg, lib_fn)
+    plan = getattr(sg, plan_fn)(case.transA, case.transB, M, N, K, case.alpha, sets[0][0], d["lda"], sets[0][1],
+                                d["ldb"], case.beta, sets[0][2], d["ldc"])
 
     def step(i):
         A, B, C = sets[i & 1]
-        sg.sgemm(case.transA, case.transB, M, N, K, case.alpha, A, d["lda"], B, d["ldb"], case.beta, C,
-                 d["ldc"], sh)
+        call(case.transA, case.transB, M, N, K, case.alpha, A, d["lda"], B, d["ldb"], case.beta, C, d["ldc"], sh)
 
     def barrier():
         if world > 1:
@@ -550,9 +591,22 @@ def run_ours(args):
     # ---- e2e: host buffers through the C ABI (sgemm_host), copies inside the timed region
     hA, hB, hC = (torch.from_numpy(d[k]).pin_memory() for k in ("A", "B", "C"))
 
-    def e2e_step():
-        sg.sgemm_host(case.transA, case.transB, M, N, K, case.alpha, hA, d["lda"], hB, d["ldb"], case.beta, hC,
-                      d["ldc"], sh)
+    if args.entry != "sgemm":
+        # no host-buffer form of the reduced-precision entry points: the same copies, made here
+        dA, dB, dC = (torch.empty_like(x) for x in sets[0])
+
+        def e2e_step():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            if case.beta != 0.0:
+                dC.copy_(hC, non_blocking=True)
+            call(case.transA, case.transB, M, N, K, case.alpha, dA, d["lda"], dB, d["ldb"], case.beta, dC,
+                 d["ldc"], sh)
+            hC.copy_(dC, non_blocking=True)
+    else:
+        def e2e_step():
+            sg.sgemm_host(case.transA, case.transB, M, N, K, case.alpha, hA, d["lda"], hB, d["ldb"], case.beta,
+                          hC, d["ldc"], sh)
 
     for _ in range(2 if args.e2e_steps > 0 else 0):
         e2e_step()
@@ -580,7 +634,11 @@ def run_ours(args):
     max_mhz = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
     ffma_peak = sms * FMA_PER_SM_PER_CLK * 2 * max_mhz * 1e6 / 1e12
     variant = plan["variant_name"]
-    if variant in ("TC_TF32X3", "TC_PAIR", "TC_PRESPLIT", "TC_SKINNY"):
+    if variant in ("TC_TF32", "TC_BF16"):
+        roof = reduced_roofline(achieved, peaks, variant, kernel_ms,
+                                traffic_from_profile(variant, case.name, lib_build.presplit_kernel_digest()))
+        hbm_bound_roofline(roof, si.min_bytes(M, N, K, case.beta), flops_step, kernel_ms, peaks)
+    elif variant in ("TC_TF32X3", "TC_PAIR", "TC_PRESPLIT", "TC_SKINNY"):
         roof = tensor_roofline(achieved, peaks,
                                traffic_from_profile(variant, case.name, kernel_digest(lib_build, variant)),
                                kernel_ms, variant)
@@ -598,9 +656,9 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
         "step_ms": step_stats(step_ms),
-        "config": config_block(case, world),
+        "config": config_block(case, world, None if args.entry == "sgemm" else lib_fn),
         "l2_hot": l2_hot_block(flush, hot_ms, flops_step),
         "run": {"l2": l2_note(flush), "prewarm_s": args.prewarm_s,
                 "plan": {k: plan[k] for k in ("variant_name", "tile_m", "tile_n", "tile_k", "stages",
@@ -616,8 +674,11 @@ def run_ours(args):
     }
     if not args.no_cublas_context:
         line["context_cublas_fp32"] = cublas_context(case, sets, min(args.steps, 50), stream)
+        if args.entry != "sgemm":
+            line["context_cublas_" + args.entry] = cublas_context(case, sets, min(args.steps, 50), stream,
+                                                                  args.entry)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(case, d, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(case, d, args.cpu_seconds, args.entry)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

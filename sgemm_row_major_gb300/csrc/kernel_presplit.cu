@@ -59,8 +59,13 @@ using namespace tc;
 // contiguous floats (row stride ldk, product stride rows * ldk): element (r,
 // k) of product p is src[p * stride + r * ld + k] when the stored rows run
 // along K, src[p * stride + k * ld + r] otherwise (then the pass transposes
-// through shared memory, 32 x 32 tiles).
-constexpr int kSplitTile = 32;
+// through shared memory, 64 x 64 tiles).  Both forms are HBM streams; each
+// thread loads 16 (transposing) or kSplitUnroll x 4 (rows) elements before it
+// splits and stores any, so an SM keeps about 128 KB of loads in flight (with
+// one load per thread, 32 KB, the passes ran at 3.0-4.6 TB/s).
+constexpr int kSplitTile = 64;
+constexpr int kSplitUnroll = 4;
+constexpr int kSplitSegChunks = 32 * kSplitUnroll;  // 4-float chunks one warp takes per row segment
 
 __device__ __forceinline__ void split_one(float x, float& hi, float& lo) {
   hi = tf32_round(x);
@@ -117,42 +122,62 @@ __device__ __forceinline__ void split_pass_begin(bool trigger) {
 }
 __device__ __forceinline__ void split_pass_end() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Rows run along K.  Work unit: a segment of kSplitSegChunks 4-float chunks of one row, taken by
+// one warp, lane l the chunks l, l + 32, l + 64, l + 96 of it (each load instruction of the warp
+// reads 512 contiguous bytes); the last segment of a row also takes its tail of K % 4 elements.
+// VEC: every source row 16-byte aligned (16-byte loads), else four 4-byte loads per chunk.
 template <bool VEC, typename OutT>
 __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict__ src, int64_t ld, int64_t stride,
                                                          int rows, int K, int products, OutT* __restrict__ hi,
                                                          float* __restrict__ lo, int64_t ldk, const SplitChk chk,
                                                          bool trigger) {
   split_pass_begin(trigger);
-  const int k4n = (K + 3) / 4;
-  const int64_t total = (int64_t)products * rows * k4n;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int k4 = (int)(i % k4n);
-    const int64_t pr = i / k4n;  // product * rows + row
+  const int lane = (int)threadIdx.x & 31;
+  const int kfull = K / 4;  // chunks of 4 whole k
+  const int nseg = max(1, (kfull + kSplitSegChunks - 1) / kSplitSegChunks);
+  const int64_t units = (int64_t)products * rows * nseg;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); u < units; u += warps) {
+    const int64_t pr = u / nseg;  // product * rows + row
+    const int sg = (int)(u - pr * nseg);
     const int64_t p = pr / rows, r = pr - p * rows;
-    const int64_t so = p * stride + r * ld + 4 * k4;
-    if (!chk.src(so, min(4, K - 4 * k4)) || !chk.dst(pr * ldk + 4 * k4, 4)) continue;
+    const int64_t so = p * stride + r * ld;
     const float* s = src + so;
-    OutT* h = hi + pr * ldk + 4 * k4;
-    if (4 * k4 + 3 < K) {
-      const float4 x = VEC ? *reinterpret_cast<const float4*>(s) : make_float4(s[0], s[1], s[2], s[3]);
+    OutT* h = hi + pr * ldk;
+    float* l = lo ? lo + pr * ldk : nullptr;
+    float4 x[kSplitUnroll];
+    bool ok[kSplitUnroll];
+#pragma unroll
+    for (int j = 0; j < kSplitUnroll; ++j) {
+      const int c = sg * kSplitSegChunks + 32 * j + lane;
+      ok[j] = c < kfull && chk.src(so + 4 * c, 4) && chk.dst(pr * ldk + 4 * c, 4);
+      x[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (ok[j])
+        x[j] = VEC ? *reinterpret_cast<const float4*>(s + 4 * c) : make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2],
+                                                                              s[4 * c + 3]);
+    }
+#pragma unroll
+    for (int j = 0; j < kSplitUnroll; ++j) {
+      if (!ok[j]) continue;
+      const int c = sg * kSplitSegChunks + 32 * j + lane;
       float4 xh, xl;
-      split4(x, xh, xl);
-      if (lo) *reinterpret_cast<float4*>(lo + pr * ldk + 4 * k4) = xl;
-      store_hi4(h, x, xh, lo != nullptr);
-    } else {
-      for (int j = 0; j < K - 4 * k4; ++j) {
-        float xh, xl;
-        split_one(s[j], xh, xl);
-        store_hi(h + j, s[j], xh, lo != nullptr);
-        if (lo) lo[pr * ldk + 4 * k4 + j] = xl;
-      }
+      split4(x[j], xh, xl);
+      if (l) *reinterpret_cast<float4*>(l + 4 * c) = xl;
+      store_hi4(h + 4 * c, x[j], xh, l != nullptr);
+    }
+    const int kt = 4 * kfull + lane;  // the tail: fewer than 4 elements
+    if (sg == nseg - 1 && kt < K && chk.src(so + kt, 1) && chk.dst(pr * ldk + kt, 1)) {
+      float xh, xl;
+      split_one(s[kt], xh, xl);
+      store_hi(h + kt, s[kt], xh, l != nullptr);
+      if (l) l[kt] = xl;
     }
   }
   split_pass_end();
 }
 
-// Stored rows run along the other axis: a 32 x 32 block per CTA (32 x 8 threads), read along
-// the stored rows (any alignment), written along K; lo == nullptr: hi only.
+// Stored rows run along the other axis: a 64 x 64 block per CTA (32 x 8 threads, 16 elements
+// each), read along the stored rows (any alignment), written along K; lo == nullptr: hi only.
 template <typename OutT>
 __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __restrict__ src, int64_t ld,
                                                               int64_t stride, int rows, int K,
@@ -162,28 +187,38 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __res
   __shared__ float tile[kSplitTile][kSplitTile + 1];
   const int p = (int)blockIdx.z;
   const int r0 = (int)blockIdx.x * kSplitTile, k0 = (int)blockIdx.y * kSplitTile;
+  const int tx = (int)threadIdx.x, ty = (int)threadIdx.y;
   const float* s = src + (int64_t)p * stride;
-  // read: stored row k = k0 + ty + 8j, element r = r0 + tx
-  for (int j = 0; j < kSplitTile; j += 8) {
-    const int k = k0 + (int)threadIdx.y + j, r = r0 + (int)threadIdx.x;
+  // read: stored row k = k0 + ty + j, element r = r0 + tx + c; all 16 loads before any store
+  constexpr int kReads = (kSplitTile / 8) * (kSplitTile / 32);
+  float v[kReads];
+#pragma unroll
+  for (int i = 0; i < kReads; ++i) {
+    const int j = 8 * (i >> 1), c = 32 * (i & 1);
+    const int k = k0 + ty + j, r = r0 + tx + c;
     const int64_t so = (int64_t)k * ld + r;
-    tile[threadIdx.y + j][threadIdx.x] =
-        (k < K && r < rows && chk.src((int64_t)p * stride + so, 1)) ? s[so] : 0.0f;
+    v[i] = 0.0f;
+    if (k < K && r < rows && chk.src((int64_t)p * stride + so, 1)) v[i] = s[so];
   }
+#pragma unroll
+  for (int i = 0; i < kReads; ++i) tile[ty + 8 * (i >> 1)][tx + 32 * (i & 1)] = v[i];
   __syncthreads();
-  // write: row r = r0 + ty + 8j, k = k0 + tx
+  // write: row r = r0 + ty + j, k = k0 + tx + c
   OutT* h = hi + (int64_t)p * rows * ldk;
   float* l = lo ? lo + (int64_t)p * rows * ldk : nullptr;
-  for (int j = 0; j < kSplitTile; j += 8) {
-    const int r = r0 + (int)threadIdx.y + j, k = k0 + (int)threadIdx.x;
-    if (r < rows && k < K && chk.dst(((int64_t)p * rows + r) * ldk + k, 1)) {
-      const float x = tile[threadIdx.x][threadIdx.y + j];
-      float xh, xl;
-      split_one(x, xh, xl);
-      store_hi(h + (int64_t)r * ldk + k, x, xh, lo != nullptr);
-      if (lo) l[(int64_t)r * ldk + k] = xl;
+#pragma unroll
+  for (int j = 0; j < kSplitTile; j += 8)
+#pragma unroll
+    for (int c = 0; c < kSplitTile; c += 32) {
+      const int r = r0 + ty + j, k = k0 + tx + c;
+      if (r < rows && k < K && chk.dst(((int64_t)p * rows + r) * ldk + k, 1)) {
+        const float x = tile[tx + c][ty + j];
+        float xh, xl;
+        split_one(x, xh, xl);
+        store_hi(h + (int64_t)r * ldk + k, x, xh, lo != nullptr);
+        if (lo) l[(int64_t)r * ldk + k] = xl;
+      }
     }
-  }
   split_pass_end();
 }
 
@@ -653,8 +688,10 @@ cudaError_t launch_split_pass(const float* src, int64_t ld, int64_t stride, bool
   cfg.numAttrs = order == SplitOrder::kDependent ? 1 : 0;
   const bool trigger = order == SplitOrder::kFirst;
   if (k_contig) {
-    const int64_t work = (int64_t)products * rows * ((K + 3) / 4);
-    cfg.gridDim = dim3((unsigned)std::max<int64_t>(std::min<int64_t>((work + 255) / 256, (int64_t)sm_count * 8), 1));
+    // one warp per row segment, at most 64 warps per SM (8 CTAs of 256 threads), row-segment loop
+    const int64_t nseg = std::max<int64_t>(1, ((K / 4) + tps::kSplitSegChunks - 1) / tps::kSplitSegChunks);
+    const int64_t warps = std::min<int64_t>((int64_t)products * rows * nseg, (int64_t)sm_count * 64);
+    cfg.gridDim = dim3((unsigned)std::max<int64_t>((warps + 7) / 8, 1));
     cfg.blockDim = dim3(256);
     const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && ld % 4 == 0 && (products == 1 || stride % 4 == 0);
     return vec ? cudaLaunchKernelEx(&cfg, tps::split_rows_kernel<true, OutT>, src, ld, stride, rows, K, products, hi,
@@ -664,7 +701,7 @@ cudaError_t launch_split_pass(const float* src, int64_t ld, int64_t stride, bool
   }
   cfg.gridDim = dim3((unsigned)((rows + tps::kSplitTile - 1) / tps::kSplitTile),
                      (unsigned)((K + tps::kSplitTile - 1) / tps::kSplitTile), (unsigned)products);
-  cfg.blockDim = dim3(tps::kSplitTile, 8);
+  cfg.blockDim = dim3(32, 8);  // 32 x 8 threads, 16 elements each
   return cudaLaunchKernelEx(&cfg, tps::split_transpose_kernel<OutT>, src, ld, stride, rows, K, hi, lo, ldk, chk,
                             trigger);
 }
