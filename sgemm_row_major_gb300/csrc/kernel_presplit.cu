@@ -601,7 +601,8 @@ template <bool CVEC>
 __global__ void __launch_bounds__(kFixupThreads) presplit_fixup_kernel(const GemmParams p, int k_tile) {
   __shared__ int s_n;
   __shared__ int s_slot[kMaxSharers];
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The schedule and C's old values come first (fixup_prefetch_c); the grid is a programmatic
+  // dependent of the GEMM kernel and waits for it only before reading the partial sums.
   const int kt = (p.K + k_tile - 1) / k_tile;  // the GEMM's K tiles (32, or 64 for BF16 inputs)
   const int j = (int)blockIdx.x >> 1, r = (int)blockIdx.x & 1;
   if (threadIdx.x == 0) {
@@ -622,39 +623,22 @@ __global__ void __launch_bounds__(kFixupThreads) presplit_fixup_kernel(const Gem
   const int rr = (int)blockIdx.y * kFixupRowsPerCta + (int)(threadIdx.x >> 5);
   const int row = m0 + BMC * r + rr;
   if (row >= p.M) return;
+  FixupOut f[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int col = n0 + 128 * h + (int)(threadIdx.x & 31) * 4;
+    f[h].cp = nullptr;
+    if (col < p.N) f[h] = fixup_prefetch_c<CVEC>(p, prod, row, col);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int cc = 128 * h + (int)(threadIdx.x & 31) * 4;
     const int col = n0 + cc;
     if (col >= p.N) continue;
-    const float* w = p.ws + rr * BN + cc;
-    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 4
-    for (int i = 0; i < n; ++i) {
-      if (!ws_ok(p, rr * BN + cc + (int64_t)s_slot[i] * (BMC * BN), 4)) continue;
-      const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[i] * (BMC * BN));
-      if (i == 0) v = u;
-      else { v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w; }
-    }
+    float4 v = fixup_sum(p, s_slot, n, BMC * BN, (int64_t)rr * BN + cc);
     if (p.repair) repair_nans4(p, prod, row, col, v);
-    const int64_t coff = (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
-    if (!c_ok(p, coff, min(4, p.N - col))) continue;
-    float* cp = p.C + coff;
-    if (CVEC && col + 3 < p.N) {
-      float4 o;
-      if (p.beta == 0.0f) {
-        o = make_float4(p.alpha * v.x, p.alpha * v.y, p.alpha * v.z, p.alpha * v.w);
-      } else {
-        const float4 old = *reinterpret_cast<const float4*>(cp);
-        o = make_float4(fmaf(p.alpha, v.x, p.beta * old.x), fmaf(p.alpha, v.y, p.beta * old.y),
-                        fmaf(p.alpha, v.z, p.beta * old.z), fmaf(p.alpha, v.w, p.beta * old.w));
-      }
-      *reinterpret_cast<float4*>(cp) = o;
-    } else {
-      const float x[4] = {v.x, v.y, v.z, v.w};
-      for (int k = 0; k < 4 && col + k < p.N; ++k)
-        cp[k] = p.beta == 0.0f ? p.alpha * x[k] : fmaf(p.alpha, x[k], p.beta * cp[k]);
-    }
+    fixup_store<CVEC>(p, f[h], v);
   }
 }
 

@@ -452,7 +452,9 @@ template <bool TRANSC>
 __global__ void __launch_bounds__(kFixupThreads) skinny_fixup_kernel(const GemmParams p) {
   __shared__ int s_n;
   __shared__ int s_slot[kMaxSharers];
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The schedule and C's old values come first (as tc::fixup_prefetch_c: the GEMM never writes C
+  // of a shared tile); the grid is a programmatic dependent of the GEMM kernel and waits for it
+  // only before reading the partial sums.
   const int kt = (p.K + BK - 1) / BK;
   const int j = (int)blockIdx.x;
   if (threadIdx.x == 0) {
@@ -472,23 +474,24 @@ __global__ void __launch_bounds__(kFixupThreads) skinny_fixup_kernel(const GemmP
   const int c = e / BM, r = e % BM;                                     // short index, first long index
   const int m0 = (p.sk_tile0 + j) * BM;
   if (c >= p.N || m0 + r >= p.M) return;
-  float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 4
-  for (int i = 0; i < n; ++i) {
-    const int64_t o = (int64_t)s_slot[i] * (BM * BN) + e;
-    if (!ws_ok(p, o, 4)) continue;
-    const float4 u = *reinterpret_cast<const float4*>(p.ws + o);
-    if (i == 0) v = u;
-    else { v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w; }
-  }
-  float x[4] = {v.x, v.y, v.z, v.w};
+  bool ok[4];
+  float old[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int i = m0 + r + k;
-    if (i >= p.M) break;
+    ok[k] = i < p.M && c_ok(p, c_index<TRANSC>(p, i, c), 1);
+    old[k] = 0.0f;
+    if (ok[k] && p.beta != 0.0f) old[k] = p.C[c_index<TRANSC>(p, i, c)];
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const float4 v = tc::fixup_sum(p, s_slot, n, BM * BN, e);
+  float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (!ok[k]) continue;
+    const int i = m0 + r + k;
     if (!(fabsf(x[k]) <= 3.402823466e38f)) tc::repair_row(p, 0, i, c, &x[k], 1);
-    const int64_t ci = c_index<TRANSC>(p, i, c);
-    if (c_ok(p, ci, 1)) p.C[ci] = epi(p, x[k], p.C + ci);
+    p.C[c_index<TRANSC>(p, i, c)] = p.beta == 0.0f ? p.alpha * x[k] : fmaf(p.alpha, x[k], p.beta * old[k]);
   }
 }
 

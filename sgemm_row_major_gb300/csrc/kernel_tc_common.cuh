@@ -144,6 +144,93 @@ __device__ __forceinline__ void repair_nans4(const GemmParams& p, int prod, int 
   s = make_float4(v[0], v[1], v[2], v[3]);
 }
 
+// ---- fixup of tiles that several CTAs (or clusters) shared under stream-K
+// A fixup thread owns 4 consecutive columns of one row of C.  It reads C's old values before it
+// waits for its GEMM grid (it is launched as that grid's programmatic dependent): the GEMM never
+// writes C of a shared tile, and every kernel of the stream before that GEMM has completed once
+// this grid runs, so the read is off the path that starts when the GEMM ends.
+struct FixupOut {
+  float* cp;     // C element of the first column (nullptr: nothing to write)
+  int cnt;       // columns in range, 1..4
+  float old[4];  // C's old values (read when beta != 0)
+};
+
+template <bool CVEC>
+__device__ __forceinline__ FixupOut fixup_prefetch_c(const GemmParams& p, int prod, int row, int col) {
+  FixupOut f;
+  f.cp = nullptr;
+  f.cnt = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) f.old[k] = 0.0f;
+  const int64_t coff = (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
+  const int cnt = min(4, p.N - col);
+  if (!c_ok(p, coff, cnt)) return f;
+  f.cp = p.C + coff;
+  f.cnt = cnt;
+  if (p.beta != 0.0f) {
+    if (CVEC && cnt == 4) {
+      const float4 o = *reinterpret_cast<const float4*>(f.cp);
+      f.old[0] = o.x;
+      f.old[1] = o.y;
+      f.old[2] = o.z;
+      f.old[3] = o.w;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (k < cnt) f.old[k] = f.cp[k];
+    }
+  }
+  return f;
+}
+
+// Sum of one float4 of n slots in sharer order (slot[i] * slot_elems + off in the workspace); the
+// loads of four slots are issued before their adds.
+__device__ __forceinline__ float4 fixup_sum(const GemmParams& p, const int* slot, int n, int64_t slot_elems,
+                                            int64_t off) {
+  float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int i0 = 0; i0 < n; i0 += 4) {
+    float4 u[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      u[t] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (i0 + t < n) {
+        const int64_t o = (int64_t)slot[i0 + t] * slot_elems + off;
+        if (ws_ok(p, o, 4)) u[t] = *reinterpret_cast<const float4*>(p.ws + o);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (i0 + t >= n) break;
+      if (i0 + t == 0) {
+        v = u[t];
+      } else {
+        v.x += u[t].x;
+        v.y += u[t].y;
+        v.z += u[t].z;
+        v.w += u[t].w;
+      }
+    }
+  }
+  return v;
+}
+
+// C = alpha * v + beta * old over the thread's in-range columns.
+template <bool CVEC>
+__device__ __forceinline__ void fixup_store(const GemmParams& p, const FixupOut& f, float4 v) {
+  if (f.cp == nullptr) return;
+  const float x[4] = {v.x, v.y, v.z, v.w};
+  float o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) o[k] = p.beta == 0.0f ? p.alpha * x[k] : fmaf(p.alpha, x[k], p.beta * f.old[k]);
+  if (CVEC && f.cnt == 4) {
+    *reinterpret_cast<float4*>(f.cp) = make_float4(o[0], o[1], o[2], o[3]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (k < f.cnt) f.cp[k] = o[k];
+  }
+}
+
 __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, int& tm, int& tn) {
   constexpr int kGroupM = 8;
   const int span = kGroupM * tiles_n;

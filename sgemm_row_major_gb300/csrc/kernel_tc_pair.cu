@@ -472,9 +472,8 @@ template <bool CVEC>
 __global__ void __launch_bounds__(kFixupThreads) pair_fixup_kernel(const GemmParams p) {
   __shared__ int s_n;
   __shared__ int s_slot[kMaxSharers];
-  // launched as a programmatic dependent of the GEMM kernel: wait for that grid to
-  // complete and its writes to be visible
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The schedule and C's old values come first (fixup_prefetch_c); the grid is a programmatic
+  // dependent of the GEMM kernel and waits for it only before reading the partial sums.
   const int kt = (p.K + BK - 1) / BK;
   const int j = (int)blockIdx.x >> 1, r = (int)blockIdx.x & 1;
   if (threadIdx.x == 0) {
@@ -496,34 +495,11 @@ __global__ void __launch_bounds__(kFixupThreads) pair_fixup_kernel(const GemmPar
   const int cc = (int)(threadIdx.x & 31) * 4;
   const int row = m0 + BMC * r + rr, col = n0 + cc;
   if (row >= p.M || col >= p.N) return;
-  const float* w = p.ws + rr * BN + cc;
-  float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 4
-  for (int i = 0; i < n; ++i) {
-    if (!ws_ok(p, rr * BN + cc + (int64_t)s_slot[i] * (BMC * BN), 4)) continue;
-    const float4 u = *reinterpret_cast<const float4*>(w + (int64_t)s_slot[i] * (BMC * BN));
-    if (i == 0) v = u;
-    else { v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w; }
-  }
+  const FixupOut f = fixup_prefetch_c<CVEC>(p, prod, row, col);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  float4 v = fixup_sum(p, s_slot, n, BMC * BN, (int64_t)rr * BN + cc);
   repair_nans4(p, prod, row, col, v);
-  const int64_t coff = (int64_t)prod * p.stride_c + (int64_t)row * p.ldc + col;
-  if (!c_ok(p, coff, min(4, p.N - col))) return;
-  float* cp = p.C + coff;
-  if (CVEC && col + 3 < p.N) {
-    float4 o;
-    if (p.beta == 0.0f) {
-      o = make_float4(p.alpha * v.x, p.alpha * v.y, p.alpha * v.z, p.alpha * v.w);
-    } else {
-      const float4 old = *reinterpret_cast<const float4*>(cp);
-      o = make_float4(fmaf(p.alpha, v.x, p.beta * old.x), fmaf(p.alpha, v.y, p.beta * old.y),
-                      fmaf(p.alpha, v.z, p.beta * old.z), fmaf(p.alpha, v.w, p.beta * old.w));
-    }
-    *reinterpret_cast<float4*>(cp) = o;
-  } else {
-    const float x[4] = {v.x, v.y, v.z, v.w};
-    for (int k = 0; k < 4 && col + k < p.N; ++k)
-      cp[k] = p.beta == 0.0f ? p.alpha * x[k] : fmaf(p.alpha, x[k], p.beta * cp[k]);
-  }
+  fixup_store<CVEC>(p, f, v);
 }
 
 }  // namespace tcp
