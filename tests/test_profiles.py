@@ -66,3 +66,23 @@ def test_l2_hot_block():
     assert bench.l2_hot_block(None, None, 1e9)["value"] is None
     hot = bench.l2_hot_block(lambda: None, 0.01, 2.147e9)  # 10 us per 1024^3 step
     assert abs(hot["value"] - 214.7) < 1e-9 and hot["unit"] == "TFLOPS" and hot["ms_per_step"] == 0.01
+
+
+def test_reduced_precision_entries():
+    """bench.py --entry tf32 / bf16: the library, plan and oracle functions it names exist, the
+    roofline takes the measured bf16 peak (BF16 inputs) or that peak x 1.1/2.25 (TF32 inputs),
+    and the config names the entry point only when it is not sgemm()."""
+    import oracle
+    import sgemm_row_major_gb300 as sg
+    for e, (lib_fn, plan_fn, oracle_fn, dtype) in bench.ENTRIES.items():
+        assert callable(getattr(sg, lib_fn)) and callable(getattr(sg, plan_fn)) and callable(getattr(oracle, oracle_fn))
+        assert dtype
+    peaks = {"bf16_tflops": 1910.0}
+    bf = bench.reduced_roofline(955.0, peaks, "TC_BF16", 0.144, None)
+    assert bf["bound"] == "tensor" and bf["peak"] == 1910.0 and abs(bf["frac"] - 0.5) < 1e-12
+    tf = bench.reduced_roofline(467.0, peaks, "TC_TF32", 0.294, None)
+    assert abs(tf["peak"] - 1910.0 * 1.1 / 2.25) < 1e-9 and abs(tf["frac"] - 467.0 / tf["peak"]) < 1e-12
+    import sgemm_inputs as si
+    c = si.case("square4096")
+    assert "entry" not in bench.config_block(c, 1)
+    assert bench.config_block(c, 1, "sgemm_bf16")["entry"] == "sgemm_bf16"
