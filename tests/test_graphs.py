@@ -82,6 +82,31 @@ def test_split_operand_graph_replay():
         check_exact(dC.cpu().numpy(), oracle.sgemm("N", "T", A, B, C, 1.5, -0.5), f"split-operand replay {rep}")
 
 
+@pytest.mark.parametrize("entry", ["sgemm_tf32", "sgemm_bf16"])
+def test_reduced_precision_graph_replay(entry):
+    """The TF32- and BF16-input GEMMs (two rounding passes, the GEMM, the fixup, the workspace
+    from the pool) captured once and replayed on new inputs; dyadic values are exact in both
+    formats, so the replays equal the oracle bit for bit."""
+    torch = torch_cuda()
+    M, N, K = 1100, 900, 1500
+    dA = torch.empty((K, M), dtype=torch.float32, device="cuda")   # op(A) = A^T
+    dB = torch.empty((K, N), dtype=torch.float32, device="cuda")
+    dC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    call = getattr(sg, entry)
+    g = _capture(torch, lambda: call("T", "N", M, N, K, 1.5, dA, M, dB, N, -0.5, dC, N))
+    rng = np.random.default_rng(65)
+    ref_fn = getattr(oracle, entry)
+    for rep in range(2):
+        A, B, C = _dyadic(rng, (K, M)), _dyadic(rng, (K, N)), _dyadic(rng, (M, N))
+        dA.copy_(torch.from_numpy(A))
+        dB.copy_(torch.from_numpy(B))
+        dC.copy_(torch.from_numpy(C))
+        g.replay()
+        torch.cuda.synchronize()
+        assert sg.sgemm_sync_status() == 0
+        check_exact(dC.cpu().numpy(), ref_fn("T", "N", A, B, C, 1.5, -0.5), f"{entry} replay {rep}")
+
+
 @pytest.mark.parametrize("M,N", [(64, 2048), (2048, 33)])
 def test_short_side_graph_replay(M, N):
     """The short-side path (split pass of the short operand, the GEMM as its programmatic

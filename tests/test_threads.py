@@ -89,7 +89,8 @@ def test_concurrent_calls_from_threads():
     assert not errors, errors
 
 
-@pytest.mark.parametrize("entry", ["sgemm", "sgemm_noalloc", "sgemm_ex", "strided_batched"])
+@pytest.mark.parametrize("entry", ["sgemm", "sgemm_noalloc", "sgemm_ex", "strided_batched", "sgemm_tf32",
+                                   "sgemm_bf16"])
 def test_first_cuda_call_of_a_thread(entry):
     """A fresh host thread whose first CUDA call is the library's (stream handle made elsewhere)."""
     torch = torch_cuda()
@@ -130,5 +131,6 @@ def test_first_cuda_call_of_a_thread(entry):
     assert out == [0], out
     stream.synchronize()
     got = dC.cpu().numpy()
+    ref_fn = getattr(oracle, entry) if entry in ("sgemm_tf32", "sgemm_bf16") else oracle.sgemm
     for b in range(P):
-        np.testing.assert_array_equal(got[b], oracle.sgemm("N", "N", A[b], B[b], C[b], 1.5, -0.5))
+        np.testing.assert_array_equal(got[b], ref_fn("N", "N", A[b], B[b], C[b], 1.5, -0.5))
