@@ -218,7 +218,13 @@ constexpr int64_t kGroupMaxMN = 64;
 constexpr int64_t kSmallKChunk = 32;
 constexpr int64_t kSmallCtasPerSm = 4;  // persistent grid: 4 x 32 KB of stages per SM
 
-int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
+// min_iters: the stream-K share's minimum in K tiles; last_round: whether a short remainder may
+// take the last whole round into stream-K with it.  The BF16-input GEMM (64-deep K tiles, a third
+// of a 3xTF32 tile's tensor time) uses 16 and no last round: measured at 4096^3 694.6 against
+// 670.2 TFLOPS (28 stream-K tiles instead of 104), 16384x1024x4096 678.4 / 656.6, 4097x3001x2053
+// 432.3 / 409.5; with the last round, 8192x4096x1024 fell from 571.0 to 500.1 (132 tiles).
+int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan,
+                  int64_t min_iters = kMinStreamKIters, bool last_round = true) {
   const int64_t sms = std::max(1, sm_count);
   int64_t grid, dp_tiles, sk_tiles;
   const int ov_split = g_override_split.load();
@@ -233,8 +239,8 @@ int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
     grid = sms;
     const int64_t rem = tiles % sms;
     sk_tiles = 0;
-    if (rem * kt / sms >= kMinStreamKIters) sk_tiles = rem;
-    else if (rem && (sms + rem) * kt / sms >= kMinStreamKIters) sk_tiles = sms + rem;
+    if (rem * kt / sms >= min_iters) sk_tiles = rem;
+    else if (last_round && rem && (sms + rem) * kt / sms >= min_iters) sk_tiles = sms + rem;
     dp_tiles = tiles - sk_tiles;
   } else if (4 * tiles >= 3 * sms) {
     // at least 3/4 as many tiles as units: whole tiles, one per unit, the rest idle (at 2048^3 the
@@ -246,7 +252,7 @@ int plan_stream_k(int64_t tiles, int64_t kt, int sm_count, sgemm_plan_t* plan) {
     dp_tiles = 0;
     sk_tiles = tiles;
     // (at most 254 CTAs per tile: the fixup kernel handles up to 256 sharers of a tile)
-    if (tiles * kt / sms >= kMinStreamKIters) {
+    if (tiles * kt / sms >= min_iters) {
       grid = std::min<int64_t>(sms, tiles * 254);
     } else {
       const int64_t split = std::max<int64_t>(1, std::min<int64_t>({sms / tiles, kt / 4, 254}));
@@ -625,7 +631,7 @@ int make_bf16_plan(const Problem& pr, int sm_count, int pair_clusters, sgemm_pla
   const int64_t clusters = std::max(1, pair_clusters > 0 ? pair_clusters : sm_count / 2);
   const int64_t tiles = ceil_div(pr.M, 256) * ceil_div(pr.N, 256);
   *plan = sgemm_plan_t{};
-  const int t = plan_stream_k(tiles, ceil_div(pr.K, 64), (int)clusters, plan);
+  const int t = plan_stream_k(tiles, ceil_div(pr.K, 64), (int)clusters, plan, kMinStreamKIters / 2, false);
   if (t != SGEMM_OK) return t;
   plan->variant = SGEMM_VARIANT_TC_BF16;
   plan->tile_m = plan->tile_n = 256;

@@ -517,6 +517,11 @@ def test_bf16_planner(lib):
     slots = 2 * 152 * 128 * 256 * 4 if p["split_k"] > 1 else 0
     assert p["workspace_bytes"] == r256(slots) + 2 * 4096 * 4096 * 2
     assert p["kernel_launches"] == (4 if p["split_k"] > 1 else 3)
+    # stream-K for the ragged last round only (28 of 256 tiles: 16 of the 64-deep K tiles per
+    # cluster is enough), never the last whole round with it (K = 1024: whole tiles)
+    assert (p["dp_tiles"], p["sk_tiles"]) == (228, 28) and p["split_k"] > 1
+    fc = sg.sgemm_bf16_plan("N", "N", 8192, 4096, 1024, 1.0, FAKE, 1024, FAKE, 4096, 0.0, FAKE, 4096, 152)
+    assert (fc["dp_tiles"], fc["sk_tiles"], fc["split_k"]) == (512, 0, 1)
     q = sg.sgemm_bf16_plan("T", "N", 333, 277, 501, 1.0, FAKE_ODD, 335, FAKE_ODD, 279, 0.0, FAKE, 277, 152)
     assert q["variant_name"] == "TC_BF16"
     assert q["workspace_bytes"] % 256 == 0 and q["workspace_bytes"] >= r256(333 * 504 * 2) + r256(277 * 504 * 2)
