@@ -236,11 +236,14 @@ constexpr int kPartBytes = 128 * BK * 4;  // 16 KB: 128 rows (or columns) x 32 k
 template <int PARTS>
 struct Cfg {
   static constexpr int kStages = PARTS == 2 ? 3 : 6;
-  // K tiles summed in one TMEM accumulator before the folders add it into FP32 registers: 12
-  // tensor-core products either way (3xTF32: 4 k-steps x 3 products; TF32 inputs: 3 K tiles x 4
-  // k-steps x 1), the count the fold was sized for (the tensor core's FP32 accumulation drifts
-  // with the number of products it adds; kernel_tf32x3.cu)
-  static constexpr int kFoldTiles = PARTS == 2 ? 1 : 3;
+  // K tiles summed in one TMEM accumulator before the folders add it into FP32 registers (the
+  // tensor core's FP32 accumulation drifts with the number of products it adds; kernel_tf32x3.cu):
+  // 3xTF32 12 products (4 k-steps x 3), the count the fold was sized for; one product per term
+  // (TF32 or BF16 inputs) 24 (6 K tiles x 4 k-steps).  Measured at 4096^3 against the
+  // rounded-input oracle, relative Frobenius error and TFLOPS for TF32 / BF16 inputs: 12 products
+  // 2.8e-7, 479 / 1.7e-7, 708; 24 products 4.9e-7, 522 / 2.9e-7, 763; 48 products 9.2e-7, 555 /
+  // 6.0e-7, 819 (too close to the 1e-6 gate for TF32).
+  static constexpr int kFoldTiles = PARTS == 2 ? 1 : 6;
   static constexpr int kStageBytes = 2 * PARTS * kPartBytes;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
   static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA");
