@@ -49,7 +49,14 @@
  * inputs, and finite values within the bound above.  As in any FP32
  * accumulation, products or partial sums beyond FLT_MAX overflow to +-Inf.
  * Scaling A and B by powers of two scales C exactly, as in FP32 arithmetic,
- * down to products near the FP32 subnormal range.  The FP32 FFMA kernels
+ * down to products near the FP32 subnormal range (products and sums in that
+ * range are kept; measured exact).  Tiny INPUTS are the exception: TF32's
+ * smallest step is 2^-136, so an input of magnitude below 2^-115 reaches the
+ * tensor cores only to within 2^-137 (its remainder below TF32's range is
+ * dropped), which adds up to 2^-137 * sum_k(|b_k| over the k whose a_k is
+ * that small, and |a_k| over the k whose b_k is) to an element's error; that
+ * exceeds the bound above only when the whole dot product is of that order.
+ * The FP32 FFMA kernels
  * (IEEE operations throughout) are selected with
  * sgemm_set_variant_override(SGEMM_VARIANT_TMA_128x128 or
  * SGEMM_VARIANT_TMA_64x256, 0).  Operands TMA cannot load (a base not 16-byte
